@@ -1,0 +1,463 @@
+"""Plain CPU oracle of QEvict's recoverable three-tier KV cache on the decode path.
+
+TEST INFRASTRUCTURE. Only the test-suite, the smoke check and the benchmark's
+CPU-baseline leg import this module. The library (C-ABI + CUDA kernels) never
+calls it, and this module imports nothing from the library.
+
+What it follows, cited by page title and section:
+
+* "Technische Samenvatting: QEvict" (gist.science/nl/paper/2608.05326) and its
+  Chinese twin (gist.science/zh/paper/2608.05326), sections "Methodologie:
+  QEvict" (three tiers: full precision, recoverable INT2, evicted; a fixed
+  byte budget) and "Kernmechanismen" (window-level routing, cumulative
+  scoring, demotion, promotion, the write-once quantisation ledger, GQA).
+* "Technische Samenvatting: LogQuant" (gist.science/nl/paper/2503.19950),
+  Methodologie 3 (evicting a token removes it from the softmax normalisation)
+  and 4 (the order of cache entries does not change A.V).
+* "Technische Samenvatting: RDKV" (gist.science/nl/paper/2605.08317), 2.1
+  (the importance of a token is the attention mass it receives, summed over
+  queries).
+
+The pages give no formulas for QEvict's quantiser or router. Where they are
+silent this module takes the plainest reading (one tier per window shared by
+all KV heads, asymmetric min/max INT2 over groups of 32 channels with fp16
+scale and minimum, window score = mean over query heads of the window's
+softmax mass, budget counts only attention-visible bytes, the last window is
+always full precision, FP share of the budget rho). Each reading is named
+where it is used.
+
+Floating point: attention, masses and scores in float64. The quantiser and the
+promotion dequantiser are integer-producing / rounding steps whose results must
+match bit for bit, so they are written in the exact float32 / float16
+operations they are defined by (numpy float32 arithmetic and float32 ->
+float16 casts are IEEE round-to-nearest-even).
+
+Parity status: attention/masses/scores pinned by the dense-softmax special
+case, mass sums, closed forms and brute force; quantiser pinned by exact-grid
+groups, nearest-level optimality and the error bound; router pinned by brute
+force over all tier assignments on small inputs. Nothing here is "parity
+unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+TIER_FP, TIER_Q, TIER_E = 0, 1, 2
+GROUP = 32          # channels per INT2 quantisation group
+LEVELS = 3          # 2-bit codes 0..3 -> (max - min) / 3 per step
+
+
+class OracleError(Exception):
+    """Base of the oracle's error conditions (mirrors the library's status codes)."""
+
+
+class BudgetError(OracleError):
+    pass
+
+
+class StateError(OracleError):
+    pass
+
+
+class QuantError(OracleError):
+    pass
+
+
+# --------------------------------------------------------------------------
+# Exact rounding helpers
+# --------------------------------------------------------------------------
+
+def bf16_round(x) -> np.ndarray:
+    """Round float32 values to the nearest bfloat16 (ties to even); returns float32.
+
+    bfloat16 keeps the top 16 bits of a float32. Adding 0x7FFF plus the lowest
+    kept bit to the 32-bit pattern and truncating rounds the dropped 16 bits to
+    nearest, ties to the even kept value; an overflow out of the largest finite
+    value carries into the exponent and yields infinity, as IEEE rounding does.
+    NaN stays NaN.
+    """
+    x = np.asarray(x, dtype=np.float32)
+    b = x.view(np.uint32).astype(np.uint64)
+    lsb = (b >> np.uint64(16)) & np.uint64(1)
+    r = ((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
+    out = r.astype(np.uint32).view(np.float32)
+    return np.where(np.isnan(x), x, out).astype(np.float32)
+
+
+def half_round(x) -> np.ndarray:
+    """Round float32 values to float16 (IEEE round-to-nearest-even, with subnormals)."""
+    with np.errstate(over="ignore"):
+        return np.asarray(x, dtype=np.float32).astype(np.float16)
+
+
+# --------------------------------------------------------------------------
+# INT2 quantiser (demotion) and dequantisers
+# --------------------------------------------------------------------------
+
+def quantize_groups(x):
+    """Asymmetric 2-bit quantisation of groups of 32 bf16 values.
+
+    Reading of QEvict "Recoverable Quantized Tier" (INT2): per token, per KV
+    head, per group of 32 consecutive channels of head_dim, for K and V alike:
+
+      mn = min x, mx = max x                               (exact)
+      min16   = fp16_rne(mn)
+      scale16 = fp16_rne(fl32(fl32(mx - mn) / 3))
+      code_j  = clamp(rint_even(fl32(fl32(x_j - min16) / scale16)), 0, 3)
+                (all codes 0 when scale16 == 0)
+
+    x: float32 array [..., 32] holding bf16 values.
+    Returns (codes uint8 [..., 32], scale float16 [...], minimum float16 [...],
+    bad bool [...]) where ``bad`` flags a group with a non-finite input or a
+    scale / minimum that overflows fp16 (the library reports these as a status
+    error and leaves the group's codes at 0).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    assert x.shape[-1] == GROUP
+    finite = np.isfinite(x).all(axis=-1)
+    xs = np.where(np.isfinite(x), x, np.float32(0))
+    mn = xs.min(axis=-1)
+    mx = xs.max(axis=-1)
+    mn16 = half_round(mn)
+    with np.errstate(over="ignore", invalid="ignore"):
+        rng = (mx - mn).astype(np.float32)
+        s32 = (rng / np.float32(LEVELS)).astype(np.float32)
+    s16 = half_round(s32)
+    bad = ~finite | ~np.isfinite(mn16) | ~np.isfinite(s16)
+    s32q = s16.astype(np.float32)
+    m32q = mn16.astype(np.float32)
+    zero = (s32q == 0) | bad
+    den = np.where(zero, np.float32(1), s32q)
+    with np.errstate(over="ignore", invalid="ignore"):
+        diff = (xs - m32q[..., None]).astype(np.float32)
+        qt = (diff / den[..., None]).astype(np.float32)
+    codes = np.clip(np.rint(qt), 0, LEVELS)
+    codes = np.where(zero[..., None], 0, codes).astype(np.uint8)
+    s16 = np.where(bad, np.float16(0), s16)
+    mn16 = np.where(bad, np.float16(0), mn16)
+    return codes, s16.astype(np.float16), mn16.astype(np.float16), bad
+
+
+def dequant_exact(codes, scale16, min16):
+    """Real value min + code * scale of each code (float64, exact for fp16 meta).
+
+    Used inside attention: the quantised tier is attended in place, without
+    rounding the reconstruction.
+    """
+    c = np.asarray(codes, dtype=np.float64)
+    s = np.asarray(scale16, dtype=np.float64)[..., None]
+    m = np.asarray(min16, dtype=np.float64)[..., None]
+    return m + c * s
+
+
+def dequant_promote(codes, scale16, min16):
+    """Promotion back to the full-precision tier: bf16_rne(fl32(code * scale + min)).
+
+    code * scale + min is exact in float64 for fp16 scale / min and codes 0..3,
+    so the float32 cast below is the single rounding of a fused multiply-add.
+    """
+    exact = dequant_exact(codes, scale16, min16)
+    return bf16_round(exact.astype(np.float32))
+
+
+# --------------------------------------------------------------------------
+# Budget and routing
+# --------------------------------------------------------------------------
+
+def window_costs(w: int, Hkv: int, d: int):
+    """Bytes one window occupies per sequence in each visible tier.
+
+    full precision: K and V bf16, w * Hkv * d * 2 * 2;
+    INT2: K and V codes (d / 4 bytes per token and head) plus one fp16 scale
+    and one fp16 minimum per group of 32 channels.
+    """
+    c_fp = w * Hkv * d * 4
+    c_q = w * Hkv * 2 * (d // 4 + 4 * (d // GROUP))
+    return c_fp, c_q
+
+
+def budget_bytes(L: int, Hkv: int, d: int, beta: float) -> int:
+    """B_t = floor(beta * F_t), F_t = bytes of the full bf16 K/V cache at length L."""
+    F = L * Hkv * d * 4
+    return int(math.floor(beta * F))
+
+
+def fp_budget_windows(Bt: int, c_fp: int, rho: float) -> int:
+    """floor(rho * B_t / c_fp): full-precision windows the FP share of the budget buys."""
+    return int(math.floor((rho * Bt) / c_fp))
+
+
+def route_counts(n_cand: int, L: int, w: int, Hkv: int, d: int, beta: float, rho: float):
+    """(n_fp, n_q) for one sequence at length L with n_cand non-evicted windows."""
+    c_fp, c_q = window_costs(w, Hkv, d)
+    Bt = budget_bytes(L, Hkv, d, beta)
+    if Bt < c_fp:
+        raise BudgetError(f"budget {Bt} B cannot hold the open window ({c_fp} B)")
+    n_fp = min(n_cand, max(1, fp_budget_windows(Bt, c_fp, rho)))
+    n_q = min(n_cand - n_fp, (Bt - n_fp * c_fp) // c_q)
+    return n_fp, n_q
+
+
+def route_tiers(S, tiers, L: int, w: int, Hkv: int, d: int, beta: float, rho: float):
+    """Budgeted tier assignment for one sequence (QEvict "Kernmechanismen").
+
+    Candidates are the windows that are not evicted (eviction is permanent).
+    The last window (the one appends go into) is forced to full precision
+    when it is a candidate. The rest are ranked by cumulative score, highest
+    first, ties to the lower window index; the top n_fp (including the forced
+    window) stay / become full precision, the next n_q INT2, the rest are
+    evicted.
+    Returns the new tier array (uint8).
+    """
+    W = -(-L // w)
+    tiers = np.asarray(tiers, dtype=np.uint8)
+    cand = [i for i in range(W) if tiers[i] != TIER_E]
+    if not cand:
+        return tiers.copy()
+    vals = [float(S[i]) for i in cand]
+    if not all(math.isfinite(v) for v in vals):
+        raise OracleError("non-finite score among routing candidates")
+    n_fp, n_q = route_counts(len(cand), L, w, Hkv, d, beta, rho)
+    forced = W - 1
+    order = sorted(cand, key=lambda i: (i != forced, -float(S[i]), i))
+    new = tiers.copy()
+    for r, i in enumerate(order):
+        new[i] = TIER_FP if r < n_fp else (TIER_Q if r < n_fp + n_q else TIER_E)
+    return new
+
+
+# --------------------------------------------------------------------------
+# Attention over the tiered cache
+# --------------------------------------------------------------------------
+
+def softmax_attention(q, keys, values):
+    """o = softmax(q k^T / sqrt(d)) v for one head, in float64; also returns p."""
+    q = np.asarray(q, dtype=np.float64)
+    s = (np.asarray(keys, dtype=np.float64) @ q) / math.sqrt(q.shape[-1])
+    s = s - s.max()
+    e = np.exp(s)
+    p = e / e.sum()
+    return p @ np.asarray(values, dtype=np.float64), p
+
+
+# --------------------------------------------------------------------------
+# The cache as a state machine
+# --------------------------------------------------------------------------
+
+class Window:
+    __slots__ = ("tier", "k", "v", "ledger", "ledger_writes", "ntok")
+
+    def __init__(self, Hkv, w, d):
+        self.tier = TIER_FP
+        self.k = np.zeros((Hkv, w, d), np.float32)   # bf16 values
+        self.v = np.zeros((Hkv, w, d), np.float32)
+        self.ledger = None        # (codes_k, scale_k, min_k, codes_v, scale_v, min_v)
+        self.ledger_writes = 0
+        self.ntok = 0
+
+
+class OracleCache:
+    """One layer of the tiered cache for a batch of B sequences of equal length."""
+
+    def __init__(self, B, Hq, Hkv, d, w, beta=1.0, rho=0.5):
+        assert Hq % Hkv == 0 and d % GROUP == 0
+        self.B, self.Hq, self.Hkv, self.d, self.w = B, Hq, Hkv, d, w
+        self.beta, self.rho = beta, rho
+        self.L = 0
+        self.win = [[] for _ in range(B)]
+        self.S = [np.zeros(0, np.float64) for _ in range(B)]
+        self.stats = dict(demotions=0, promotions=0, evictions=0, ledger_writes=0,
+                          ledger_reuses=0)
+
+    # ---- helpers --------------------------------------------------------
+    @property
+    def W(self):
+        return -(-self.L // self.w)
+
+    def tiers(self):
+        return np.array([[win.tier for win in self.win[b]] for b in range(self.B)], np.uint8).reshape(self.B, self.W)
+
+    def scores(self):
+        return np.stack(self.S) if self.B else np.zeros((0, 0))
+
+    # ---- appends (window partitioning) ------------------------------------
+    def append(self, k, v):
+        """Append n tokens' K, V ([B][n][Hkv][d], bf16 values) to every sequence.
+
+        History is partitioned into consecutive windows of w tokens; a token at
+        position p lands in window p // w, row p % w. A window opens in the
+        full-precision tier when its first token arrives.
+        """
+        k = np.asarray(k, np.float32)
+        v = np.asarray(v, np.float32)
+        n = k.shape[1]
+        for i in range(n):
+            p = self.L + i
+            wi, row = divmod(p, self.w)
+            for b in range(self.B):
+                if row == 0:
+                    self.win[b].append(Window(self.Hkv, self.w, self.d))
+                    self.S[b] = np.append(self.S[b], 0.0)
+                win = self.win[b][wi]
+                if win.tier != TIER_FP:
+                    raise StateError("append into a window that is not full precision")
+                win.k[:, row, :] = k[b, i]
+                win.v[:, row, :] = v[b, i]
+                win.ntok = row + 1
+        self.L += n
+
+    # ---- transitions (recoverable hierarchy + ledger) ----------------------
+    def _evict(self, b, wi):
+        win = self.win[b][wi]
+        win.tier = TIER_E
+        win.k = win.v = None
+        win.ledger = None
+        self.stats["evictions"] += 1
+
+    def _demote(self, b, wi):
+        """FP -> INT2. Quantise only if the window has no ledger entry yet."""
+        win = self.win[b][wi]
+        if win.tier != TIER_FP or win.ntok != self.w:
+            raise StateError("demotion needs a full full-precision window")
+        if win.ledger is None:
+            ck, sk, mk, bk = quantize_groups(win.k.reshape(self.Hkv, self.w, -1, GROUP))
+            cv, sv, mv, bv = quantize_groups(win.v.reshape(self.Hkv, self.w, -1, GROUP))
+            if bk.any() or bv.any():
+                raise QuantError("non-finite value or fp16 overflow in a quantisation group")
+            win.ledger = (ck.reshape(self.Hkv, self.w, self.d), sk, mk,
+                          cv.reshape(self.Hkv, self.w, self.d), sv, mv)
+            win.ledger_writes += 1
+            self.stats["ledger_writes"] += 1
+        else:
+            self.stats["ledger_reuses"] += 1
+        win.tier = TIER_Q
+        win.k = win.v = None
+        self.stats["demotions"] += 1
+
+    def _promote(self, b, wi):
+        """INT2 -> FP: dequantise the ledger codes to bf16; the ledger is kept."""
+        win = self.win[b][wi]
+        if win.tier != TIER_Q:
+            raise StateError("promotion needs an INT2 window")
+        ck, sk, mk, cv, sv, mv = win.ledger
+        g = lambda c: c.reshape(self.Hkv, self.w, -1, GROUP)
+        win.k = dequant_promote(g(ck), sk, mk).reshape(self.Hkv, self.w, self.d)
+        win.v = dequant_promote(g(cv), sv, mv).reshape(self.Hkv, self.w, self.d)
+        win.tier = TIER_FP
+        self.stats["promotions"] += 1
+
+    def apply_tiers(self, b, new):
+        """Move sequence b's windows to tiers ``new``: evict, then demote, then promote."""
+        cur = [win.tier for win in self.win[b]]
+        for wi, (c, t) in enumerate(zip(cur, new)):
+            if c == TIER_E and t != TIER_E:
+                raise StateError("an evicted window cannot come back")
+            if c != t and wi == self.W - 1 and self.win[b][wi].ntok < self.w:
+                raise StateError("the partially filled last window stays full precision")
+        for wi, (c, t) in enumerate(zip(cur, new)):
+            if c != TIER_E and t == TIER_E:
+                self._evict(b, wi)
+        for wi, (c, t) in enumerate(zip(cur, new)):
+            if c == TIER_FP and t == TIER_Q:
+                self._demote(b, wi)
+        for wi, (c, t) in enumerate(zip(cur, new)):
+            if c == TIER_Q and t == TIER_FP:
+                self._promote(b, wi)
+
+    def set_tiers(self, tiers):
+        tiers = np.asarray(tiers, np.uint8)
+        for b in range(self.B):
+            self.apply_tiers(b, tiers[b])
+
+    def route(self, scores_override=None, score_mult=None):
+        """A routing event: optionally replace / scale the scores, rank, move tiers."""
+        if scores_override is not None:
+            ov = np.asarray(scores_override, np.float64)
+            self.S = [ov[b, :self.W].copy() for b in range(self.B)]
+        if score_mult is not None:
+            mu = np.asarray(score_mult, np.float64)
+            self.S = [self.S[b] * mu[b, :self.W] for b in range(self.B)]
+        for b in range(self.B):
+            new = route_tiers(self.S[b], [x.tier for x in self.win[b]], self.L, self.w,
+                              self.Hkv, self.d, self.beta, self.rho)
+            self.apply_tiers(b, new)
+
+    def prefill(self, k, v, scores=None, tiers=None):
+        """Fill an empty cache with L tokens (all full precision), then route or set tiers."""
+        assert self.L == 0
+        self.append(k, v)
+        if scores is not None:
+            self.route(scores_override=scores)
+        elif tiers is not None:
+            self.set_tiers(tiers)
+
+    def demote(self, pairs):
+        for b, wi in pairs:
+            self._demote(b, wi)
+
+    def promote(self, pairs):
+        for b, wi in pairs:
+            self._promote(b, wi)
+
+    # ---- decode attention + cumulative scoring ----------------------------
+    def window_kv(self, b, wi, kvh):
+        """K, V rows (float64) a query attends to in window wi for KV head kvh, or None."""
+        win = self.win[b][wi]
+        if win.tier == TIER_E:
+            return None
+        n = win.ntok
+        if win.tier == TIER_FP:
+            return (win.k[kvh, :n].astype(np.float64), win.v[kvh, :n].astype(np.float64))
+        ck, sk, mk, cv, sv, mv = win.ledger
+        g = lambda c: c[kvh].reshape(self.w, -1, GROUP)
+        kk = dequant_exact(g(ck), sk[kvh], mk[kvh]).reshape(self.w, self.d)
+        vv = dequant_exact(g(cv), sv[kvh], mv[kvh]).reshape(self.w, self.d)
+        return kk[:n], vv[:n]
+
+    def decode(self, q, accumulate=True):
+        """One decode step of single-token GQA attention over the tiered cache.
+
+        q: [B][Hq][d] (bf16 values). Query head h reads KV head h // (Hq / Hkv).
+        Full-precision windows are read as stored, INT2 windows as their exact
+        reconstruction min + code * scale, evicted windows not at all (they
+        leave the softmax denominator). Returns (out [B][Hq][d], mass
+        [B][Hq][W]) in float64; mass[b, h, w] is the softmax probability the
+        head puts on window w. With ``accumulate`` the window score grows by
+        the mean of the masses over the Hq query heads.
+        """
+        q = np.asarray(q, np.float64)
+        G = self.Hq // self.Hkv
+        W = self.W
+        out = np.zeros((self.B, self.Hq, self.d))
+        mass = np.zeros((self.B, self.Hq, W))
+        for b in range(self.B):
+            for kvh in range(self.Hkv):
+                ks, vs, owner = [], [], []
+                for wi in range(W):
+                    kv = self.window_kv(b, wi, kvh)
+                    if kv is None:
+                        continue
+                    ks.append(kv[0])
+                    vs.append(kv[1])
+                    owner.append(np.full(kv[0].shape[0], wi))
+                if not ks:
+                    continue
+                K = np.concatenate(ks)
+                V = np.concatenate(vs)
+                own = np.concatenate(owner)
+                for h in range(kvh * G, (kvh + 1) * G):
+                    o, p = softmax_attention(q[b, h], K, V)
+                    out[b, h] = o
+                    mass[b, h] = np.bincount(own, weights=p, minlength=W)
+            if accumulate:
+                self.S[b] = self.S[b] + mass[b].mean(axis=0)
+        return out, mass
+
+
+def tiered_bytes(cache: OracleCache) -> int:
+    """Attention-visible bytes resident for all sequences (FP c_fp, INT2 c_q, E 0)."""
+    c_fp, c_q = window_costs(cache.w, cache.Hkv, cache.d)
+    t = cache.tiers()
+    return int((t == TIER_FP).sum() * c_fp + (t == TIER_Q).sum() * c_q)

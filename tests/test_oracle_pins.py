@@ -1,0 +1,433 @@
+"""Pins that tie the CPU oracle to something other than itself.
+
+Each test checks the oracle against a hand-derived value, a closed form, an
+invariant, a library routine for a special case, or brute force on a tiny
+input. None of them needs a GPU.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tiered_kv_cache_decode_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- rounding
+
+def _f32_sweep(n=200000, seed=1):
+    rng = np.random.default_rng(seed)
+    bitsv = rng.integers(0, 2 ** 32, size=n, dtype=np.uint64).astype(np.uint32)
+    x = bitsv.view(np.float32)
+    # exact ties for bf16 (low 16 bits = 0x8000) and fp16 (low 13 bits = 0x1000)
+    tb = (bitsv & np.uint32(0xFFFF0000)) | np.uint32(0x8000)
+    th = (bitsv & np.uint32(0xFFFFE000)) | np.uint32(0x1000)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, 65504.0, 65520.0, 65519.99, 6e-8, 3e-8,
+                        2.0 ** -24, 2.0 ** -25, 3.4e38, 1.0, -1.0], np.float32)
+    return np.concatenate([x, tb.view(np.float32), th.view(np.float32), special])
+
+
+def test_bf16_round_matches_torch_conversion():
+    x = _f32_sweep()
+    x = x[~np.isnan(x)]
+    mine = O.bf16_round(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(mine.view(np.uint32), ref.view(np.uint32))
+
+
+def test_half_round_matches_torch_conversion():
+    x = _f32_sweep()
+    x = x[~np.isnan(x)]
+    mine = O.half_round(x).view(np.uint16)
+    ref = torch.from_numpy(x).to(torch.float16).numpy().view(np.uint16)
+    assert np.array_equal(mine, ref)
+
+
+# ---------------------------------------------------------------- quantiser
+
+def _parse_golden_groups():
+    groups, cur = [], {}
+    for line in open(os.path.join(GOLDEN, "quant_groups.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, val = [s.strip() for s in line.split(":", 1)]
+        cur[key] = val
+        if key == "codes":
+            groups.append(cur)
+            cur = {}
+    out = []
+    for g in groups:
+        xs = g["x"].rstrip("*").strip()
+        vals = [sum(float(t) for t in tok.split("+")) for tok in xs.split(",")]
+        x = (vals * 32)[:32]
+        cs = g["codes"].rstrip("*").strip()
+        codes = [int(c) for c in (cs * 32)[:32]]
+        out.append((g["name"], np.array(x, np.float32), int(g["scale16"], 16),
+                    int(g["min16"], 16), np.array(codes, np.uint8)))
+    return out
+
+
+@pytest.mark.parametrize("name,x,s16,m16,codes", _parse_golden_groups())
+def test_quantizer_hand_derived_groups(name, x, s16, m16, codes):
+    assert np.array_equal(O.bf16_round(x), x), "fixture values must be bf16"
+    c, s, m, bad = O.quantize_groups(x[None])
+    assert not bad[0]
+    assert int(s.view(np.uint16)[0]) == s16
+    assert int(m.view(np.uint16)[0]) == m16
+    assert np.array_equal(c[0], codes)
+
+
+def _random_groups(n, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(n, 32, generator=g, dtype=torch.float64) * scale
+    x[:, :3] *= 8.0
+    return x.to(torch.float32).to(torch.bfloat16).to(torch.float32).numpy()
+
+
+def test_quantizer_exact_grid_has_zero_error():
+    rng = np.random.default_rng(3)
+    for _ in range(500):
+        e = rng.integers(-6, 4)
+        s = np.float32(2.0 ** e * rng.choice([1.0, 1.5, 1.25, 1.75]))
+        m = np.float32(rng.integers(-64, 64) * 2.0 ** (e - 1))
+        k = rng.integers(0, 4, size=32)
+        k[0], k[1] = 0, 3
+        x = (m + k * s).astype(np.float32)
+        assert np.array_equal(O.bf16_round(x), x) and np.float16(s) == s and np.float16(m) == m
+        c, s16, m16, bad = O.quantize_groups(x[None])
+        assert not bad[0]
+        assert np.array_equal(c[0], k)
+        assert np.array_equal(O.dequant_exact(c, s16, m16)[0], x.astype(np.float64))
+
+
+def test_quantizer_constant_group():
+    for v in [0.0, 1.5, -3.25, 1e-3, 200.0]:
+        x = np.full((1, 32), O.bf16_round(np.float32(v)), np.float32)
+        c, s, m, bad = O.quantize_groups(x)
+        assert not bad[0] and float(s[0]) == 0.0 and not c.any()
+        assert float(m[0]) == float(np.float16(x[0, 0]))
+
+
+def test_quantizer_codes_are_nearest_levels_and_error_bound():
+    x = _random_groups(4000, 5)
+    c, s16, m16, bad = O.quantize_groups(x)
+    assert not bad.any()
+    s = s16.astype(np.float64)[:, None]
+    m = m16.astype(np.float64)[:, None]
+    xd = x.astype(np.float64)
+    levels = m[..., None] + np.arange(4)[None, None, :] * s[..., None]
+    dist = np.abs(xd[..., None] - levels)
+    best = dist.min(axis=-1)
+    chosen = np.take_along_axis(dist, c[..., None].astype(np.int64), axis=-1)[..., 0]
+    # chosen level is a nearest one, up to the float32 rounding of the quotient
+    slack = 4 * np.finfo(np.float32).eps * (np.abs(xd - m) + s)
+    assert np.all(chosen <= best + slack)
+    # error bound: half a step plus the fp16 rounding of the meta data
+    mn = x.min(axis=1).astype(np.float64)[:, None]
+    mx = x.max(axis=1).astype(np.float64)[:, None]
+    bound = s / 2 + np.abs(mn - m) + 3 * np.abs((mx - mn) / 3 - s) + slack
+    err = np.abs(xd - O.dequant_exact(c, s16, m16))
+    assert np.all(err <= bound)
+    # when the meta data round exactly, the error is at most half a step
+    exact_meta = (np.abs(mn - m) == 0) & (np.abs((mx - mn) / 3 - s) == 0)
+    if exact_meta.any():
+        assert np.all(err[exact_meta[:, 0]] <= s[exact_meta[:, 0]] / 2 + slack[exact_meta[:, 0]])
+
+
+def test_quantizer_flags_nonfinite_and_fp16_overflow():
+    x = _random_groups(3, 7)
+    x[0, 4] = np.inf
+    x[1, 5] = np.float32(O.bf16_round(np.float32(3e5)))   # range / 3 > 65504
+    x[2, :] = np.float32(O.bf16_round(np.float32(-7e4)))   # min below -65504
+    _, _, _, bad = O.quantize_groups(x)
+    assert bad.all()
+
+
+def test_promote_dequant_single_rounding():
+    x = _random_groups(2000, 11)
+    c, s16, m16, _ = O.quantize_groups(x)
+    p = O.dequant_promote(c, s16, m16)
+    exact = O.dequant_exact(c, s16, m16)
+    # result is a bf16 value within half a bf16 ulp of the float32-rounded exact value
+    assert np.array_equal(O.bf16_round(p), p)
+    f32 = exact.astype(np.float32).astype(np.float64)
+    ulp = np.spacing(np.abs(p).astype(np.float32)).astype(np.float64) * 2 ** 16
+    assert np.all(np.abs(p - f32) <= ulp / 2 + 1e-300)
+
+
+# ---------------------------------------------------------------- routing
+
+def _golden_counts():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "route_counts.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        a, b = line.split("|")
+        Hkv, d, w, L, beta, rho = a.split()
+        Bt, nfp, nq, ne, res = map(int, b.split())
+        rows.append((int(Hkv), int(d), int(w), int(L), float(beta), float(rho), Bt, nfp, nq, ne, res))
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_counts())
+def test_route_counts_hand_derived(row):
+    Hkv, d, w, L, beta, rho, Bt, nfp, nq, ne, res = row
+    W = L // w
+    assert O.budget_bytes(L, Hkv, d, beta) == Bt
+    assert O.route_counts(W, L, w, Hkv, d, beta, rho) == (nfp, nq)
+    assert W - nfp - nq == ne
+    c_fp, c_q = O.window_costs(w, Hkv, d)
+    assert nfp * c_fp + nq * c_q == res <= Bt
+
+
+def _brute_force_route(S, tiers, L, w, Hkv, d, beta, rho):
+    """Enumerate every assignment; keep those with the closed-form counts inside
+    the budget, forced last window and absorbing evictions; pick the best by
+    (sum of FP scores, sum of retained scores), then the lowest window indices."""
+    W = len(tiers)
+    cand = [i for i in range(W) if tiers[i] != O.TIER_E]
+    n_fp, n_q = O.route_counts(len(cand), L, w, Hkv, d, beta, rho)
+    c_fp, c_q = O.window_costs(w, Hkv, d)
+    Bt = O.budget_bytes(L, Hkv, d, beta)
+    best, best_key = None, None
+    for assign in itertools.product((O.TIER_FP, O.TIER_Q, O.TIER_E), repeat=len(cand)):
+        t = np.array(tiers, np.uint8).copy()
+        for i, a in zip(cand, assign):
+            t[i] = a
+        fp = [i for i in range(W) if t[i] == O.TIER_FP]
+        qq = [i for i in range(W) if t[i] == O.TIER_Q]
+        if len(fp) != n_fp or len(qq) != n_q:
+            continue
+        if (W - 1) in cand and t[W - 1] != O.TIER_FP:
+            continue
+        if len(fp) * c_fp + len(qq) * c_q > Bt:
+            continue
+        key = (sum(S[i] for i in fp if i != W - 1), sum(S[i] for i in fp + qq if i != W - 1),
+               [-i for i in sorted(fp)], [-i for i in sorted(fp + qq)])
+        if best_key is None or key > best_key:
+            best, best_key = t, key
+    return best
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_route_matches_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    W = int(rng.integers(2, 8))
+    w, Hkv, d = 4, 1, 32
+    L = W * w - int(rng.integers(0, w))
+    beta = float(rng.choice([0.3, 0.45, 0.6, 0.8]))
+    rho = float(rng.choice([0.3, 0.5, 0.7]))
+    # scores with deliberate ties
+    S = rng.choice([0.1, 0.2, 0.2, 0.5, 0.7, 1.0], size=W).astype(np.float64)
+    tiers = rng.choice([O.TIER_FP, O.TIER_Q, O.TIER_E], size=W, p=[0.5, 0.3, 0.2]).astype(np.uint8)
+    tiers[W - 1] = O.TIER_FP
+    try:
+        got = O.route_tiers(S, tiers, L, w, Hkv, d, beta, rho)
+    except O.BudgetError:
+        c_fp, _ = O.window_costs(w, Hkv, d)
+        assert O.budget_bytes(L, Hkv, d, beta) < c_fp
+        return
+    ref = _brute_force_route(S, tiers, L, w, Hkv, d, beta, rho)
+    assert np.array_equal(got, ref)
+
+
+def test_route_never_readmits_evicted_and_respects_budget():
+    rng = np.random.default_rng(9)
+    for _ in range(200):
+        W = int(rng.integers(1, 40))
+        w, Hkv, d = 8, 2, 64
+        L = W * w
+        S = rng.random(W)
+        tiers = rng.choice([0, 1, 2], size=W).astype(np.uint8)
+        tiers[-1] = 0
+        try:
+            new = O.route_tiers(S, tiers, L, w, Hkv, d, 0.3, 0.5)
+        except O.BudgetError:
+            continue
+        assert np.all(new[tiers == O.TIER_E] == O.TIER_E)
+        c_fp, c_q = O.window_costs(w, Hkv, d)
+        used = (new == 0).sum() * c_fp + (new == 1).sum() * c_q
+        assert used <= O.budget_bytes(L, Hkv, d, 0.3)
+        assert new[-1] == O.TIER_FP
+
+
+# ---------------------------------------------------------------- attention
+
+def _cache_with(B, Hq, Hkv, d, w, L, seed=0, outliers="heavy"):
+    k, v = synth.kv_tokens(seed, 0, B, 0, L, Hkv, d, outliers)
+    c = O.OracleCache(B, Hq, Hkv, d, w, beta=1.0)
+    c.append(k.float().numpy(), v.float().numpy())
+    return c, k, v
+
+
+def test_all_full_precision_equals_dense_sdpa():
+    B, Hq, Hkv, d, w, L = 2, 8, 2, 128, 16, 100
+    c, k, v = _cache_with(B, Hq, Hkv, d, w, L)
+    q = synth.queries(0, 0, 0, B, Hq, d)
+    out, mass = c.decode(q.float().numpy(), accumulate=False)
+    G = Hq // Hkv
+    kk = k.double().permute(0, 2, 1, 3).repeat_interleave(G, dim=1)   # [B][Hq][L][d]
+    vv = v.double().permute(0, 2, 1, 3).repeat_interleave(G, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(q.double()[:, :, None, :], kk, vv)[:, :, 0]
+    assert np.abs(out - ref.numpy()).max() < 1e-12
+    assert np.abs(mass.sum(-1) - 1).max() < 1e-12
+
+
+def test_masses_evicted_zero_and_single_window():
+    B, Hq, Hkv, d, w, L = 1, 4, 1, 64, 8, 64
+    c, k, v = _cache_with(B, Hq, Hkv, d, w, L)
+    tiers = np.full((1, 8), O.TIER_E, np.uint8)
+    tiers[0, 3] = O.TIER_FP
+    c.set_tiers(tiers)
+    q = synth.queries(0, 0, 1, B, Hq, d)
+    out, mass = c.decode(q.float().numpy(), accumulate=False)
+    assert np.all(mass[0, :, [0, 1, 2, 4, 5, 6, 7]] == 0)
+    assert np.allclose(mass[0, :, 3], 1.0, atol=1e-14)
+    # attention over that window alone, by the dense special case
+    kk = k.double()[0, 24:32, 0]
+    vv = v.double()[0, 24:32, 0]
+    ref = torch.softmax(q.double()[0] @ kk.T / math.sqrt(d), dim=-1) @ vv
+    assert np.abs(out[0] - ref.numpy()).max() < 1e-12
+
+
+def test_constant_keys_give_token_count_masses_and_scores():
+    B, Hq, Hkv, d, w, L = 1, 4, 2, 64, 8, 60   # last window holds 4 tokens
+    c = O.OracleCache(B, Hq, Hkv, d, w)
+    k = np.ones((B, L, Hkv, d), np.float32)
+    v = np.asarray(synth.kv_tokens(1, 0, B, 0, L, Hkv, d, "none")[1].float())
+    c.append(k, v)
+    tiers = np.zeros((1, 8), np.uint8)
+    tiers[0, [1, 5]] = O.TIER_E
+    tiers[0, 2] = O.TIER_Q
+    c.set_tiers(tiers)
+    T = 5
+    for t in range(T):
+        q = synth.queries(2, 0, t, B, Hq, d).float().numpy()
+        _, mass = c.decode(q, accumulate=True)
+    ntok = np.array([8, 0, 8, 8, 8, 0, 8, 4], np.float64)
+    expect = ntok / ntok.sum()
+    assert np.abs(mass[0] - expect[None]).max() < 1e-12
+    assert np.abs(c.S[0] - T * expect).max() < 1e-12
+
+
+def test_order_of_tokens_does_not_change_attention():
+    rng = np.random.default_rng(0)
+    K = rng.standard_normal((50, 32))
+    V = rng.standard_normal((50, 32))
+    q = rng.standard_normal(32)
+    perm = rng.permutation(50)
+    o1, p1 = O.softmax_attention(q, K, V)
+    o2, p2 = O.softmax_attention(q, K[perm], V[perm])
+    assert np.abs(o1 - o2).max() < 1e-13 and np.abs(p1[perm] - p2).max() < 1e-15
+
+
+def test_quantised_window_attends_to_exact_reconstruction():
+    B, Hq, Hkv, d, w, L = 1, 2, 1, 64, 8, 16
+    c, k, v = _cache_with(B, Hq, Hkv, d, w, L)
+    c.set_tiers(np.array([[O.TIER_Q, O.TIER_FP]], np.uint8))
+    ck, sk, mk, cv, sv, mv = c.win[0][0].ledger
+    kk = O.dequant_exact(ck[0].reshape(w, -1, 32), sk[0], mk[0]).reshape(w, d)
+    vv = O.dequant_exact(cv[0].reshape(w, -1, 32), sv[0], mv[0]).reshape(w, d)
+    K = np.concatenate([kk, k.double().numpy()[0, 8:16, 0]])
+    V = np.concatenate([vv, v.double().numpy()[0, 8:16, 0]])
+    q = synth.queries(0, 0, 3, B, Hq, d).float().numpy()
+    out, _ = c.decode(q, accumulate=False)
+    for h in range(Hq):
+        ref, _ = O.softmax_attention(q[0, h], K, V)
+        assert np.abs(out[0, h] - ref).max() < 1e-13
+
+
+# ---------------------------------------------------------------- ledger / state machine
+
+def test_ledger_write_once_over_cycles_and_control_drift():
+    B, Hq, Hkv, d, w, L = 1, 4, 2, 128, 16, 64
+    c, k, v = _cache_with(B, Hq, Hkv, d, w, L, seed=4)
+    c.demote([(0, 1)])
+    led0 = [a.copy() for a in c.win[0][1].ledger]
+    c.promote([(0, 1)])
+    fp0 = (c.win[0][1].k.copy(), c.win[0][1].v.copy())
+    for _ in range(3):
+        c.demote([(0, 1)])
+        assert all(np.array_equal(a, b) for a, b in zip(led0, c.win[0][1].ledger))
+        c.promote([(0, 1)])
+        assert np.array_equal(c.win[0][1].k, fp0[0]) and np.array_equal(c.win[0][1].v, fp0[1])
+    assert c.win[0][1].ledger_writes == 1
+    assert c.stats["ledger_writes"] == 1 and c.stats["ledger_reuses"] == 3
+    # Control: what the ledger avoids is re-quantising the promoted bf16. For
+    # N(0,1)-scale data this min/max quantiser happens to reproduce its own
+    # codes; near the fp16 subnormal range (values ~1e-5) it does not, and the
+    # re-quantised codes / meta drift from the first ones.
+    rng = np.random.default_rng(0)
+    x = O.bf16_round((1e-5 + 1e-5 * rng.standard_normal((4000, 32))).astype(np.float32))
+    c1, s1, m1, _ = O.quantize_groups(x)
+    c2, s2, m2, _ = O.quantize_groups(O.dequant_promote(c1, s1, m1))
+    drift = (c2 != c1).any(axis=1) | (s2 != s1) | (m2 != m1)
+    assert drift.sum() > 0
+    cache = O.OracleCache(1, 1, 1, 32, 4)
+    g = x[np.nonzero(drift)[0][:4]]                        # 4 drifting groups as 4 tokens
+    kv = g.reshape(1, 4, 1, 32)
+    cache.append(kv, kv)
+    cache.append(np.zeros((1, 1, 1, 32), np.float32), np.zeros((1, 1, 1, 32), np.float32))
+    cache.demote([(0, 0)])
+    first = [a.copy() for a in cache.win[0][0].ledger]
+    for _ in range(3):
+        cache.promote([(0, 0)])
+        cache.demote([(0, 0)])
+        assert all(np.array_equal(a, b) for a, b in zip(first, cache.win[0][0].ledger))
+    assert not np.array_equal(first[0].reshape(4, 32), c2[np.nonzero(drift)[0][:4]]) or \
+        not np.array_equal(first[1].ravel(), s2[np.nonzero(drift)[0][:4]]) or \
+        not np.array_equal(first[2].ravel(), m2[np.nonzero(drift)[0][:4]])
+
+
+def test_illegal_transitions_rejected():
+    c, _, _ = _cache_with(1, 2, 1, 64, 8, 20)
+    with pytest.raises(O.StateError):
+        c.demote([(0, 2)])                      # partially filled last window
+    with pytest.raises(O.StateError):
+        c.promote([(0, 0)])                     # not quantised
+    c.set_tiers(np.array([[O.TIER_E, O.TIER_Q, O.TIER_FP]], np.uint8))
+    with pytest.raises(O.StateError):
+        c.set_tiers(np.array([[O.TIER_FP, O.TIER_Q, O.TIER_FP]], np.uint8))
+    with pytest.raises(O.StateError):
+        c.demote([(0, 0)])                      # evicted
+
+
+def test_route_budget_error_when_open_window_does_not_fit():
+    c, _, _ = _cache_with(1, 2, 1, 64, 8, 64)
+    c.beta = 0.05   # 5 % of 8 windows < one full-precision window
+    with pytest.raises(O.BudgetError):
+        c.route(scores_override=np.ones((1, 8)))
+
+
+def test_multistep_invariants():
+    B, Hq, Hkv, d, w = 2, 4, 2, 64, 8
+    L0 = 160
+    c = O.OracleCache(B, Hq, Hkv, d, w, beta=0.3, rho=0.5)
+    k, v = synth.kv_tokens(5, 0, B, 0, L0, Hkv, d)
+    c.prefill(k.float().numpy(), v.float().numpy(),
+              scores=synth.zipf_scores(5, 0, B, L0 // w).numpy())
+    seen_e = np.zeros((B, 0), bool)
+    for step in range(40):
+        kn, vn = synth.kv_tokens(5, 0, B, c.L, 1, Hkv, d)
+        c.append(kn.float().numpy(), vn.float().numpy())
+        c.decode(synth.queries(5, 0, step, B, Hq, d).float().numpy(), accumulate=True)
+        if step % 8 == 7:
+            c.route(score_mult=synth.drift_factors(5, 0, step, B, c.W).numpy())
+            t = c.tiers()
+            c_fp, c_q = O.window_costs(w, Hkv, d)
+            for b in range(B):
+                used = (t[b] == 0).sum() * c_fp + (t[b] == 1).sum() * c_q
+                assert used <= O.budget_bytes(c.L, Hkv, d, 0.3)
+            pad = np.zeros((B, t.shape[1] - seen_e.shape[1]), bool)
+            seen_e = np.concatenate([seen_e, pad], axis=1)
+            assert np.all(t[seen_e] == O.TIER_E)
+            seen_e |= (t == O.TIER_E)
+    assert all(win.ledger_writes <= 1 for b in range(B) for win in c.win[b])
+    assert c.stats["promotions"] > 0 and c.stats["demotions"] > 0
