@@ -1,0 +1,281 @@
+/*
+ * qevict.h - C ABI of a GB300 (sm_103a) library for single-token GQA decode
+ * attention over QEvict's recoverable three-tier KV cache.
+ *
+ * Method: "Technische Samenvatting: QEvict" (gist.science/nl/paper/2608.05326;
+ * Chinese twin gist.science/zh/paper/2608.05326). Sections "Methodologie:
+ * QEvict" (history split into consecutive windows, each kept in full precision,
+ * in a recoverable INT2 tier, or evicted, inside one fixed byte budget) and
+ * "Kernmechanismen" (window-level routing, cumulative attention scoring,
+ * demotion, promotion, the write-once quantisation ledger, GQA support).
+ * Evicted tokens leave the softmax normalisation ("Technische Samenvatting:
+ * LogQuant", Methodologie 3) and the order of cache entries does not change
+ * the attention output (same page, Methodologie 4), which lets the kernels
+ * store and visit the tiers in any order.
+ *
+ * Conventions for every call:
+ *  - Tensors are dense, row-major, on the device of the cache (device
+ *    pointers) unless a parameter says "host". bf16 is IEEE bfloat16.
+ *  - Every call that takes a `stream` (a cudaStream_t, NULL = legacy default
+ *    stream) only enqueues work on it and returns without synchronising,
+ *    except qevict_get_status / qevict_get_stats / qevict_cache_create /
+ *    qevict_cache_destroy, which synchronise that stream.
+ *  - Errors the host can see (bad arguments, a budget that cannot hold the
+ *    open window, a full context) return a status at once and enqueue
+ *    nothing; the cache is unchanged. Errors only the device can see (a
+ *    slot pool running out, an illegal tier transition named by the caller,
+ *    a non-finite score or K/V value, an fp16 overflow of the INT2 scale)
+ *    set a sticky device status word, skip the offending work and are
+ *    reported by qevict_get_status. No kernel traps or asserts.
+ *  - Calls on one cache must be issued on one stream (or be ordered by the
+ *    caller); different layers may not run concurrently on different
+ *    streams because the sticky status and statistics are shared. Not
+ *    thread-safe.
+ *  - qevict_last_error() returns a thread-local message for the last host
+ *    error of the calling thread.
+ */
+#ifndef QEVICT_H
+#define QEVICT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qevict_status {
+    QEVICT_OK = 0,
+    QEVICT_ERR_INVALID_ARG = 1,   /* a parameter is out of range or NULL */
+    QEVICT_ERR_OUT_OF_MEMORY = 2, /* the allocator returned NULL */
+    QEVICT_ERR_BUDGET = 3,        /* the byte budget cannot hold the open window */
+    QEVICT_ERR_STATE = 4,         /* illegal tier transition / append into a non-FP window */
+    QEVICT_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    QEVICT_ERR_TIMEOUT = 6,       /* a bounded device wait gave up */
+    QEVICT_ERR_DEVICE = 7,        /* non-finite value or fp16 overflow met on the device */
+    QEVICT_ERR_CAPACITY = 8       /* a device slot pool ran out */
+} qevict_status;
+
+/* Window tiers (QEvict "Methodologie: QEvict", items 1-3). */
+enum { QEVICT_TIER_FP = 0, QEVICT_TIER_Q = 1, QEVICT_TIER_E = 2 };
+
+/* Optional device-memory allocator. alloc(bytes, stream, ctx) returns a
+ * device pointer (aligned to >= 256 B) or NULL; free(ptr, stream, ctx)
+ * releases it. With a NULL allocator the library uses cudaMalloc/cudaFree. */
+typedef struct qevict_allocator {
+    void *(*alloc)(size_t bytes, void *stream, void *ctx);
+    void (*free)(void *ptr, void *stream, void *ctx);
+    void *ctx;
+} qevict_allocator;
+
+/* Cache geometry and budget. All sequences of the batch share one length.
+ *  head_dim      must be 128; INT2 groups are 32 consecutive channels.
+ *  num_q_heads   a multiple of num_kv_heads with at most 8 query heads per
+ *                KV head (GQA, QEvict "Kernmechanismen", Implementatie).
+ *  window        tokens per window w: a multiple of 16 in [16, 128].
+ *  max_context   the longest length the cache will reach (sizes the tables).
+ *  budget_frac   beta in (0, 1]: the visible tiers of each (sequence, layer)
+ *                hold at most floor(beta * L * Hkv * d * 4) bytes after a
+ *                routing event ("5% tot 20% van de volledige KV-cache").
+ *  fp_share      rho in (0, 1]: the share of that budget that buys
+ *                full-precision windows (the pages fix no split; 0.5 default).
+ *  fp_capacity / ledger_capacity
+ *                full-precision / INT2-ledger window slots per (sequence,
+ *                layer); 0 derives them from the budget at max_context
+ *                (plus fp_slack full-precision slots for windows that open
+ *                between routing events; fp_slack 0 means 4).
+ */
+typedef struct qevict_config {
+    int32_t batch;
+    int32_t num_layers;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t window;
+    int32_t max_context;
+    int32_t fp_capacity;
+    int32_t ledger_capacity;
+    int32_t fp_slack;
+    double budget_frac;
+    double fp_share;
+} qevict_config;
+
+typedef struct qevict_cache qevict_cache;
+
+/* Device layout of one layer, for inspection by tests and tools. Pointers
+ * are device pointers owned by the cache; they stay valid until destroy.
+ *  tier[b * max_windows + w]       uint8 tier of window w of sequence b
+ *  fp_slot / ledger_slot[b*max_windows + w]
+ *                                  int32 slot index or -1
+ *  ledger_writes[b*max_windows+w]  int32 times window w was quantised (<= 1)
+ *  fp_pool + slot * fp_slot_bytes  a full-precision window:
+ *        bf16 [Hkv][2 (K, V)][window][head_dim]
+ *  ledger_pool + slot * ledger_slot_bytes   an INT2 window, per KV head and
+ *        K/V a part of window*48 bytes at head_dim 128: part index
+ *        (kvh * 2 + kv), each part = codes (window * head_dim / 4 bytes)
+ *        followed by meta (window * head_dim / 32 half2 {scale, min}):
+ *        K codes: [token][head_dim / 4] bytes, channel j in byte j / 4,
+ *                 bits 2 * (j % 4);
+ *        V codes: [token / 16][head_dim] uint32 words, token t of a
+ *                 16-token tile in bits 2 * (t % 16);
+ *        meta:    [token][head_dim / 32] half2, .x = scale, .y = min.
+ *  length                          current context length (host copy). */
+typedef struct qevict_view {
+    int32_t batch, num_q_heads, num_kv_heads, head_dim, window;
+    int32_t max_windows, num_windows;
+    int32_t fp_capacity, ledger_capacity;   /* per sequence */
+    int64_t length;
+    int64_t fp_slot_bytes, ledger_slot_bytes;
+    const uint8_t *tier;
+    const int32_t *fp_slot;
+    const int32_t *ledger_slot;
+    const int32_t *ledger_writes;
+    const uint8_t *fp_pool;
+    const uint8_t *ledger_pool;
+} qevict_view;
+
+typedef struct qevict_stats {
+    uint64_t demotions;       /* FP -> INT2 transitions */
+    uint64_t promotions;      /* INT2 -> FP transitions */
+    uint64_t evictions;       /* FP/INT2 -> evicted */
+    uint64_t ledger_writes;   /* quantisations (first demotion of a window) */
+    uint64_t ledger_reuses;   /* demotions that reused the ledger entry */
+    int64_t device_bytes;     /* bytes the cache allocated */
+} qevict_stats;
+
+/* Create a cache: allocates every layer's slot pools, tables and decode
+ * scratch through `allocator` (NULL = cudaMalloc) on the current device and
+ * initialises them on `stream`; synchronises `stream`. *out receives the
+ * handle. INVALID_ARG for an unsupported geometry, OUT_OF_MEMORY when an
+ * allocation fails (nothing leaks). */
+qevict_status qevict_cache_create(const qevict_config *config, const qevict_allocator *allocator,
+                                  void *stream, qevict_cache **out);
+
+/* Synchronise the stream the cache was created on and release everything. */
+qevict_status qevict_cache_destroy(qevict_cache *cache);
+
+/* Fill an empty layer with n_tokens tokens and set its first tiers.
+ * Semantically: append all tokens as full-precision windows, then either
+ * route on `scores` ([batch][ceil(n/window)] fp32, the initial cumulative
+ * window scores) or move to the tiers `tiers` ([batch][ceil(n/window)]
+ * uint8). Exactly one of scores / tiers is non-NULL. Windows that end up
+ * INT2 are quantised straight from k / v (their one ledger write); evicted
+ * windows are never stored, so the layer never holds more than its pools.
+ * k, v: bf16 [batch][n_tokens][Hkv][head_dim], read-only, caller-owned.
+ * STATE if the layer is not empty; BUDGET if routing cannot hold the open
+ * window. */
+qevict_status qevict_prefill(qevict_cache *cache, int32_t layer, const void *k, const void *v,
+                             int32_t n_tokens, const float *scores, const uint8_t *tiers,
+                             void *stream);
+
+/* Append n_new tokens to every sequence of a layer (QEvict
+ * "Kernmechanismen", window-level partitioning). Token at position p goes to
+ * window p / window, row p % window; a window opens in the full-precision
+ * tier when its first token arrives (a slot comes from the device free
+ * list; CAPACITY on the device if none is left).
+ * k, v: bf16 [batch][n_new][Hkv][head_dim], caller-owned.
+ * INVALID_ARG if the context would pass max_context. */
+qevict_status qevict_append_kv(qevict_cache *cache, int32_t layer, const void *k, const void *v,
+                               int32_t n_new, void *stream);
+
+/* One decode step of single-token GQA attention over the tiered cache of a
+ * layer, with the per-window mass that drives cumulative scoring.
+ *  q     bf16 [batch][Hq][head_dim]; query head h reads KV head
+ *        h / (Hq / Hkv).
+ *  out   fp32 [batch][Hq][head_dim]: softmax(q K^T / sqrt(d)) V over the
+ *        retained tokens. Full-precision windows are read as stored, INT2
+ *        windows as min + code * scale (fp32 fma, not rounded to bf16),
+ *        evicted windows are skipped and are not in the softmax denominator.
+ *  mass  fp32 [batch][Hq][ceil(length/window)] or NULL: probability mass
+ *        each head puts on each window (0 for evicted windows).
+ *  accumulate_scores  nonzero: every window's cumulative score grows by the
+ *        mean of its mass over the Hq query heads (QEvict "Cumulatieve
+ *        Scoring"; RDKV 2.1 defines a token's importance as the attention it
+ *        receives summed over queries).
+ * INVALID_ARG for an empty layer. */
+qevict_status qevict_decode_attention(qevict_cache *cache, int32_t layer, const void *q,
+                                      float *out, float *mass, int32_t accumulate_scores,
+                                      void *stream);
+
+/* A routing event for a layer (QEvict "Kernmechanismen": rank windows by
+ * cumulative score and move them between tiers under the byte budget).
+ * Optional inputs, [batch][ceil(length/window)] fp32 or NULL:
+ *  scores_override  replaces the cumulative scores before ranking;
+ *  score_mult       multiplies them (drift or decay) before ranking.
+ * Rule: candidates are the non-evicted windows (eviction is permanent); the
+ * last window, which appends go into, stays full precision; B = floor(beta *
+ * length * Hkv * d * 4); n_fp = min(C, max(1, floor(rho * B / c_fp))),
+ * n_q = min(C - n_fp, floor((B - n_fp * c_fp) / c_q)) with c_fp = window *
+ * Hkv * d * 4 and c_q = window * Hkv * 2 * (d / 4 + 4 * d / 32); rank by
+ * score, highest first, ties to the lower window index; the top n_fp are
+ * full precision, the next n_q INT2, the rest evicted. Transitions run
+ * evict -> demote -> promote. A demotion quantises only a window without a
+ * ledger entry (write-once ledger); a promotion dequantises the ledger codes
+ * to bf16 (bf16_rne(fmaf(code, scale, min))) and keeps the ledger entry.
+ * BUDGET if B < c_fp. A non-finite score among the candidates sets the
+ * device status DEVICE and leaves the tiers unchanged. */
+qevict_status qevict_route(qevict_cache *cache, int32_t layer, const float *scores_override,
+                           const float *score_mult, void *stream);
+
+/* Demote the listed windows FP -> INT2 (QEvict "Demotie"), in list order.
+ * bw_ids: int32 [n][2] device array of (sequence, window) pairs. A window
+ * without a ledger entry is quantised per token, KV head and group of 32
+ * channels: min16 = fp16(min), scale16 = fp16(fl32(fl32(max - min) / 3)),
+ * code = clamp(rint(fl32(fl32(x - min16) / scale16)), 0, 3) (all codes 0 if
+ * scale16 is 0); a window with a ledger entry reuses it. An entry naming a
+ * window that is not full precision, or the partially filled last window,
+ * sets STATE on the device and is skipped. */
+qevict_status qevict_demote_quantize(qevict_cache *cache, int32_t layer, const int32_t *bw_ids,
+                                     int32_t n, void *stream);
+
+/* Promote the listed windows INT2 -> FP (QEvict "Promotie"), in list order:
+ * x = bf16_rne(fmaf(code, scale, min)) into a new full-precision slot; the
+ * ledger entry is kept for later demotions. bw_ids as above; an entry naming
+ * a window that is not INT2 sets STATE and is skipped. */
+qevict_status qevict_promote_dequantize(qevict_cache *cache, int32_t layer, const int32_t *bw_ids,
+                                        int32_t n, void *stream);
+
+/* Move a layer's windows to explicit tiers (uint8 [batch][ceil(length /
+ * window)]), with the same transition rules as a routing event but no
+ * budget. E -> FP/INT2 and a change of the partially filled last window set
+ * STATE on the device and leave the tiers unchanged. */
+qevict_status qevict_set_tiers(qevict_cache *cache, int32_t layer, const uint8_t *tiers,
+                               void *stream);
+
+/* Write a layer's cumulative window scores, fp32 [batch][ceil(length /
+ * window)], to `scores`. */
+qevict_status qevict_get_scores(qevict_cache *cache, int32_t layer, float *scores, void *stream);
+
+/* Fill *view with the device layout of a layer (host call, no stream work). */
+qevict_status qevict_get_view(const qevict_cache *cache, int32_t layer, qevict_view *view);
+
+/* Synchronise `stream` and return the sticky device status (QEVICT_OK if no
+ * device error happened since the last qevict_clear_status). */
+qevict_status qevict_get_status(qevict_cache *cache, void *stream);
+
+/* Reset the sticky device status to QEVICT_OK (enqueued on `stream`). */
+qevict_status qevict_clear_status(qevict_cache *cache, void *stream);
+
+/* Synchronise `stream` and copy the transition counters to *stats (host). */
+qevict_status qevict_get_stats(qevict_cache *cache, qevict_stats *stats, void *stream);
+
+/* The kernels keep each layer's context length in device memory and read it
+ * when they run, so a CUDA graph captured from these calls can be replayed:
+ * every replay appends, attends and routes at the device-side length of the
+ * moment. The host keeps a copy of each length for argument checks and
+ * output shapes (mass and score rows are ceil(length / window) long at the
+ * time the kernel runs). After replaying graphs, call qevict_refresh_lengths
+ * (synchronises `stream`) to copy the device lengths back to the host. */
+qevict_status qevict_refresh_lengths(qevict_cache *cache, void *stream);
+
+/* Current context length of a layer (host copy), or -1 for a bad layer. */
+int64_t qevict_length(const qevict_cache *cache, int32_t layer);
+
+/* Thread-local text of the last host-side error of this thread. */
+const char *qevict_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QEVICT_H */

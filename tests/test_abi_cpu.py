@@ -1,0 +1,93 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+function include/qevict.h declares, and host-side argument checks answer
+without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiered_kv_cache_decode_gb300 import binding
+from tiered_kv_cache_decode_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return binding.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "qevict.h")).read()
+    return sorted(set(re.findall(r"\b(qevict_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_what_binding_exports():
+    assert _declared() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_struct_layouts_match_header_sizes():
+    # int32 x 10 + double x 2 = 56 bytes
+    assert ctypes.sizeof(binding.Config) == 56
+    assert ctypes.sizeof(binding.Stats) == 48
+    assert ctypes.sizeof(binding.View) == 9 * 4 + 4 + 3 * 8 + 6 * 8
+
+
+def _cfg(**kw):
+    base = dict(batch=1, num_layers=1, num_q_heads=8, num_kv_heads=2, head_dim=128, window=32,
+                max_context=2048, fp_capacity=0, ledger_capacity=0, fp_slack=0,
+                budget_frac=0.2, fp_share=0.5)
+    base.update(kw)
+    return binding.Config(**base)
+
+
+@pytest.mark.parametrize("bad", [dict(head_dim=64), dict(window=24), dict(window=256),
+                                 dict(num_q_heads=9), dict(num_q_heads=32, num_kv_heads=2),
+                                 dict(budget_frac=0.0), dict(budget_frac=1.5), dict(fp_share=0.0),
+                                 dict(batch=0), dict(max_context=0), dict(max_context=4096 * 32 + 1)])
+def test_create_rejects_bad_config_on_host(lib, bad):
+    h = ctypes.c_void_p()
+    rc = lib.qevict_cache_create(ctypes.byref(_cfg(**bad)), None, None, ctypes.byref(h))
+    assert rc == 1, (bad, rc)
+    assert not h.value
+    assert lib.qevict_last_error()
+
+
+def test_calls_on_null_cache_fail_cleanly(lib):
+    assert lib.qevict_decode_attention(None, 0, None, None, None, 0, None) == 1
+    assert lib.qevict_route(None, 0, None, None, None) == 1
+    assert lib.qevict_length(None, 0) == -1
+    assert lib.qevict_cache_destroy(None) == 1
+
+
+@pytest.mark.parametrize("fail_at", [0, 1, 2, 3])
+def test_failing_allocator_reports_oom_and_frees_everything(lib, fail_at):
+    """Host-side fault injection: the allocator returns NULL on its n-th call."""
+    live, calls = set(), [0]
+
+    def _a(size, stream, ctx):
+        i = calls[0]
+        calls[0] += 1
+        if i == fail_at:
+            return None
+        p = 0x10000000 + 0x100000 * i
+        live.add(p)
+        return p
+
+    def _f(ptr, stream, ctx):
+        live.remove(ptr)
+
+    al = binding.Allocator(binding.ALLOC_FN(_a), binding.FREE_FN(_f), None)
+    h = ctypes.c_void_p()
+    rc = lib.qevict_cache_create(ctypes.byref(_cfg(num_layers=4)), ctypes.byref(al), None, ctypes.byref(h))
+    assert rc == 2 and not h.value
+    assert calls[0] == fail_at + 1
+    assert not live

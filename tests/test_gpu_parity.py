@@ -1,0 +1,206 @@
+"""CUDA path against the CPU oracle, through the C ABI, on the same seeded inputs.
+
+Bit-exact: tiers, stored bf16 windows, INT2 codes, fp16 scale/min, ledger
+write counts, transition statistics. Within max|d| <= 2e-3 and relative L2 <=
+1e-3: attention outputs, window masses, cumulative scores.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tiered_kv_cache_decode_gb300 import binding, synth
+from parity_util import check_decode, check_state, check_stats, close, make_pair
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from tiered_kv_cache_decode_gb300 import build
+    build.build()
+    binding.load()
+
+
+def test_tiny_decode_step_drawn_tiers():
+    """Batch 1, 8/2 heads, 2048 tokens in 64 windows of 32, 16 FP / 32 INT2 / 16 evicted."""
+    W = 64
+    tiers = synth.drawn_tiers(0, 0, 1, W, 16, 32)
+    cache, (ref,) = make_pair(1, 8, 2, 32, 2048, outliers="tiny", tiers=[tiers],
+                              fp_capacity=W, ledger_capacity=W)
+    check_state(cache, 0, ref)
+    check_decode(cache, 0, ref, synth.queries(0, 0, 0, 1, 8, 128))
+    check_stats(cache, [ref])
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,w,L", [(1, 8, 2, 32, 1000), (2, 32, 8, 64, 777), (3, 28, 4, 16, 333),
+                                           (1, 4, 4, 128, 129), (2, 8, 1, 64, 1)])
+def test_all_full_precision_matches_oracle(B, Hq, Hkv, w, L):
+    W = -(-L // w)
+    tiers = torch.zeros(B, W, dtype=torch.uint8)
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, tiers=[tiers], fp_capacity=W, ledger_capacity=1)
+    check_state(cache, 0, ref)
+    for step in range(2):
+        check_decode(cache, 0, ref, synth.queries(1, 0, step, B, Hq, 128))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,w,L,beta", [(1, 32, 8, 64, 4096, 0.2), (2, 28, 4, 64, 3000, 0.1),
+                                                (4, 32, 8, 32, 2048, 0.05), (1, 8, 2, 128, 5000, 0.2)])
+def test_prefill_routing_quantises_and_attends(B, Hq, Hkv, w, L, beta):
+    W = -(-L // w)
+    scores = synth.zipf_scores(3, 0, B, W)
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, beta=beta, scores=[scores])
+    check_state(cache, 0, ref)
+    t = ref.tiers()
+    assert (t == O.TIER_Q).any() and (t == O.TIER_E).any()
+    check_decode(cache, 0, ref, synth.queries(3, 0, 0, B, Hq, 128))
+    check_stats(cache, [ref])
+
+
+def test_quantiser_edge_groups_bit_exact():
+    """Constant groups, exact grids, tiny (fp16-subnormal) values and heavy outliers."""
+    B, Hkv, w, L = 1, 2, 16, 64
+    k, v = synth.kv_tokens(5, 0, B, 0, L, Hkv, 128, "heavy")
+    k = k.clone()
+    v = v.clone()
+    k[0, 0:16, 0, :32] = 0.75                          # constant group
+    k[0, 0:16, 1, 32:64] = torch.tensor([-1, -0.5, 0, 0.5] * 8, dtype=torch.bfloat16)   # exact grid
+    v[0, 16:32, 0, :] = (v[0, 16:32, 0, :].float() * 1e-5 + 1e-5).to(torch.bfloat16)  # subnormal range
+    v[0, 32:48, 1, 64:96] = (v[0, 32:48, 1, 64:96].float() * 300).to(torch.bfloat16)   # wide range
+    tiers = torch.tensor([[1, 1, 1, 0]], dtype=torch.uint8)
+    cache = binding.TieredCache(B, 1, 4, Hkv, w, L, fp_capacity=4, ledger_capacity=4)
+    cache.prefill(0, k.cuda(), v.cuda(), tiers=tiers.cuda())
+    ref = O.OracleCache(B, 4, Hkv, 128, w)
+    ref.prefill(k.float().numpy(), v.float().numpy(), tiers=tiers.numpy())
+    check_state(cache, 0, ref)
+    check_decode(cache, 0, ref, synth.queries(5, 0, 0, B, 4, 128))
+
+
+def test_ledger_write_once_through_cycles():
+    B, Hq, Hkv, w, L = 2, 8, 2, 32, 320
+    W = L // w
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, tiers=[torch.zeros(B, W, dtype=torch.uint8)],
+                              fp_capacity=W, ledger_capacity=W)
+    pairs = torch.tensor([[0, 1], [1, 3], [0, 4], [1, 0]], dtype=torch.int32)
+    for cycle in range(3):
+        cache.demote(0, pairs.cuda())
+        ref.demote(pairs.tolist())
+        check_state(cache, 0, ref)
+        check_decode(cache, 0, ref, synth.queries(6, 0, cycle, B, Hq, 128), accumulate=False)
+        cache.promote(0, pairs.cuda())
+        ref.promote(pairs.tolist())
+        check_state(cache, 0, ref)
+    check_stats(cache, [ref])
+    s = cache.stats()
+    assert s["ledger_writes"] == 4 and s["ledger_reuses"] == 8
+
+
+def test_multistep_appends_decodes_routes_teacher_forced():
+    """Appends, decode steps with score accumulation and routing events with drift.
+    At each routing event the oracle routes on the GPU's scores (teacher forcing)
+    after the GPU scores are checked against the oracle's."""
+    B, Hq, Hkv, w, L0, beta = 2, 32, 8, 64, 2048, 0.25
+    steps, every = 160, 32
+    W0 = L0 // w
+    scores = synth.zipf_scores(7, 0, B, W0)
+    maxc = L0 + steps
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L0, beta=beta, scores=[scores], max_context=maxc, seed=7)
+    check_state(cache, 0, ref)
+    for step in range(steps):
+        kn, vn = synth.kv_tokens(7, 0, B, L0 + step, 1, Hkv, 128)
+        cache.append(0, kn.cuda(), vn.cuda())
+        ref.append(kn.float().numpy(), vn.float().numpy())
+        check_decode(cache, 0, ref, synth.queries(7, 0, step, B, Hq, 128))
+        if step % every == every - 1:
+            gs = cache.scores(0).cpu().numpy()
+            close(gs, np.stack(ref.S), "cumulative scores")
+            drift = synth.drift_factors(7, 0, step, B, cache.num_windows(0))
+            cache.route(0, score_mult=drift.cuda())
+            forced = (gs.astype(np.float32) * drift.numpy()).astype(np.float64)
+            ref.route(scores_override=np.asarray(cache.scores(0).cpu().numpy(), np.float64))
+            # the GPU scores after the event are its pre-event scores times the drift
+            assert np.array_equal(cache.scores(0).cpu().numpy().astype(np.float64), forced)
+            check_state(cache, 0, ref)
+    check_stats(cache, [ref])
+    assert cache.stats()["promotions"] > 0
+
+
+def test_full_size_llama_b1_32k_20pct_one_layer():
+    """The full-size Llama-3.1-8B-shaped layer: 32/8 heads, 32768 tokens, 64-token windows, 20 %."""
+    B, Hq, Hkv, w, L, beta = 1, 32, 8, 64, 32768, 0.2
+    W = L // w
+    scores = synth.zipf_scores(0, 0, B, W)
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, beta=beta, scores=[scores])
+    t = ref.tiers()
+    assert ((t == 0).sum(), (t == 1).sum(), (t == 2).sum()) == (51, 274, 187)
+    check_state(cache, 0, ref)
+    check_decode(cache, 0, ref, synth.queries(0, 0, 0, B, Hq, 128))
+
+
+def test_device_errors_set_status_without_faulting():
+    B, Hq, Hkv, w, L = 1, 8, 2, 32, 100
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, tiers=[torch.zeros(B, 4, dtype=torch.uint8)],
+                              fp_capacity=5, ledger_capacity=1)
+    # demoting the partially filled last window is illegal
+    cache.demote(0, torch.tensor([[0, 3]], dtype=torch.int32).cuda())
+    assert binding.STATUS[cache.status()] == "STATE"
+    cache.clear_status()
+    # two first demotions with a single ledger slot: the second runs out of capacity
+    cache.demote(0, torch.tensor([[0, 0], [0, 1]], dtype=torch.int32).cuda())
+    assert binding.STATUS[cache.status()] == "CAPACITY"
+    cache.clear_status()
+    # evicted windows cannot come back
+    cache.set_tiers(0, torch.tensor([[2, 1, 0, 0]], dtype=torch.uint8).cuda())
+    assert cache.status() == 0
+    cache.set_tiers(0, torch.tensor([[0, 1, 0, 0]], dtype=torch.uint8).cuda())
+    assert binding.STATUS[cache.status()] == "STATE"
+    cache.clear_status()
+    # a non-finite score among the candidates
+    bad = torch.tensor([[1.0, float("nan"), 0.5, 0.1]]).cuda()
+    cache.route(0, scores_override=bad)
+    assert binding.STATUS[cache.status()] == "DEVICE"
+    cache.clear_status()
+    # host-side: budget too small for the open window
+    small = binding.TieredCache(1, 1, 8, 2, 32, 64, budget_frac=0.05)
+    small.append(0, *[x.cuda() for x in synth.kv_tokens(0, 0, 1, 0, 64, 2, 128)])
+    with pytest.raises(binding.QevictError) as ei:
+        small.route(0)
+    assert ei.value.name == "BUDGET"
+
+
+def test_graph_replay_advances_device_length():
+    """A CUDA graph of (append, decode) replayed N times equals N eager steps."""
+    B, Hq, Hkv, w, L0 = 1, 8, 2, 32, 200
+    W = -(-L0 // w)
+    steps = 40
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L0, tiers=[torch.zeros(B, W, dtype=torch.uint8)],
+                              max_context=L0 + steps + 1, fp_capacity=16, ledger_capacity=4)
+    kbuf = torch.empty(B, 1, Hkv, 128, dtype=torch.bfloat16, device="cuda")
+    vbuf = torch.empty_like(kbuf)
+    qbuf = torch.empty(B, Hq, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            cache.append(0, kbuf, vbuf, stream=s)
+            cache.decode(0, qbuf, out=out, want_mass=False, stream=s)
+    torch.cuda.synchronize()
+    for step in range(steps):
+        kn, vn = synth.kv_tokens(9, 0, B, L0 + step, 1, Hkv, 128)
+        q = synth.queries(9, 0, step, B, Hq, 128)
+        kbuf.copy_(kn)
+        vbuf.copy_(vn)
+        qbuf.copy_(q)
+        g.replay()
+        ref.append(kn.float().numpy(), vn.float().numpy())
+        ro, _ = ref.decode(q.float().numpy())
+        torch.cuda.synchronize()
+        close(out.cpu().numpy(), ro, f"graph step {step}")
+    cache.refresh_lengths()
+    assert cache.length(0) == L0 + steps
+    assert cache.status() == 0
+    gs = cache.scores(0).cpu().numpy()
+    close(gs, np.stack(ref.S), "scores after graph replays")
+    check_state(cache, 0, ref)

@@ -1,0 +1,295 @@
+"""Thin ctypes binding over the C ABI in include/qevict.h (libqevict.so).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels behind the ABI. PyTorch supplies device memory (through the
+allocator callbacks, or the caller's tensors) and the current stream. There
+is no fallback: if the shared library is missing or a call fails, a Python
+exception says so.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqevict.so")
+
+TIER_FP, TIER_Q, TIER_E = 0, 1, 2
+HEAD_DIM = 128
+
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_MEMORY", 3: "BUDGET", 4: "STATE", 5: "CUDA",
+          6: "TIMEOUT", 7: "DEVICE", 8: "CAPACITY"}
+
+# every function the header declares
+EXPORTS = ["qevict_cache_create", "qevict_cache_destroy", "qevict_prefill", "qevict_append_kv",
+           "qevict_decode_attention", "qevict_route", "qevict_demote_quantize",
+           "qevict_promote_dequantize", "qevict_set_tiers", "qevict_get_scores", "qevict_get_view",
+           "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_refresh_lengths",
+           "qevict_length",
+           "qevict_last_error"]
+
+
+class QevictError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_layers", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("max_context", ctypes.c_int32), ("fp_capacity", ctypes.c_int32),
+                ("ledger_capacity", ctypes.c_int32), ("fp_slack", ctypes.c_int32),
+                ("budget_frac", ctypes.c_double), ("fp_share", ctypes.c_double)]
+
+
+ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
+FREE_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
+
+
+class Allocator(ctypes.Structure):
+    _fields_ = [("alloc", ALLOC_FN), ("free", FREE_FN), ("ctx", ctypes.c_void_p)]
+
+
+class View(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("max_windows", ctypes.c_int32),
+                ("num_windows", ctypes.c_int32), ("fp_capacity", ctypes.c_int32),
+                ("ledger_capacity", ctypes.c_int32), ("length", ctypes.c_int64),
+                ("fp_slot_bytes", ctypes.c_int64), ("ledger_slot_bytes", ctypes.c_int64),
+                ("tier", ctypes.c_void_p), ("fp_slot", ctypes.c_void_p),
+                ("ledger_slot", ctypes.c_void_p), ("ledger_writes", ctypes.c_void_p),
+                ("fp_pool", ctypes.c_void_p), ("ledger_pool", ctypes.c_void_p)]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [("demotions", ctypes.c_uint64), ("promotions", ctypes.c_uint64),
+                ("evictions", ctypes.c_uint64), ("ledger_writes", ctypes.c_uint64),
+                ("ledger_reuses", ctypes.c_uint64), ("device_bytes", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libqevict.so (built by ``__graft_entry__.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it first (python -m "
+                           "tiered_kv_cache_decode_gb300.build)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "qevict_cache_create": [ctypes.POINTER(Config), ctypes.POINTER(Allocator), P, ctypes.POINTER(P)],
+        "qevict_cache_destroy": [P],
+        "qevict_prefill": [P, I32, P, P, I32, P, P, P],
+        "qevict_append_kv": [P, I32, P, P, I32, P],
+        "qevict_decode_attention": [P, I32, P, P, P, I32, P],
+        "qevict_route": [P, I32, P, P, P],
+        "qevict_demote_quantize": [P, I32, P, I32, P],
+        "qevict_promote_dequantize": [P, I32, P, I32, P],
+        "qevict_set_tiers": [P, I32, P, P],
+        "qevict_get_scores": [P, I32, P, P],
+        "qevict_get_view": [P, I32, ctypes.POINTER(View)],
+        "qevict_get_status": [P, P],
+        "qevict_clear_status": [P, P],
+        "qevict_get_stats": [P, ctypes.POINTER(Stats), P],
+        "qevict_refresh_lengths": [P, P],
+        "qevict_length": [P, I32],
+        "qevict_last_error": [],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.qevict_length.restype = I64
+    lib.qevict_last_error.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class _DeviceArray:
+    """Exposes a device pointer owned by the cache through __cuda_array_interface__."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+def device_tensor(ptr: int, shape, typestr: str) -> torch.Tensor:
+    return torch.as_tensor(_DeviceArray(ptr, shape, typestr), device="cuda")
+
+
+class TieredCache:
+    """A multi-layer tiered KV cache living on the current CUDA device."""
+
+    def __init__(self, batch, num_layers, num_q_heads, num_kv_heads, window, max_context,
+                 budget_frac=1.0, fp_share=0.5, fp_capacity=0, ledger_capacity=0, fp_slack=0,
+                 head_dim=HEAD_DIM, torch_allocator=True):
+        self.lib = load()
+        self.cfg = Config(batch, num_layers, num_q_heads, num_kv_heads, head_dim, window, max_context,
+                          fp_capacity, ledger_capacity, fp_slack, float(budget_frac), float(fp_share))
+        self.B, self.Hq, self.Hkv, self.w = batch, num_q_heads, num_kv_heads, window
+        self.layers = num_layers
+        self.device = torch.cuda.current_device()
+        self._alloc = None
+        if torch_allocator:
+            dev = self.device
+
+            def _a(size, stream, ctx):
+                try:
+                    return torch.cuda.caching_allocator_alloc(int(size), dev, stream or 0)
+                except Exception:
+                    return None
+
+            def _f(ptr, stream, ctx):
+                torch.cuda.caching_allocator_delete(ptr)
+
+            self._alloc = Allocator(ALLOC_FN(_a), FREE_FN(_f), None)
+        self.handle = ctypes.c_void_p()
+        rc = self.lib.qevict_cache_create(ctypes.byref(self.cfg),
+                                          ctypes.byref(self._alloc) if self._alloc else None,
+                                          _stream(), ctypes.byref(self.handle))
+        self._check(rc)
+
+    # ---- plumbing ----------------------------------------------------------
+    def _check(self, rc):
+        if rc != 0:
+            raise QevictError(rc, self.lib.qevict_last_error().decode())
+
+    def close(self):
+        if self.handle:
+            self._check(self.lib.qevict_cache_destroy(self.handle))
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def refresh_lengths(self, stream=None):
+        self._check(self.lib.qevict_refresh_lengths(self.handle, _stream(stream)))
+
+    def length(self, layer=0) -> int:
+        return int(self.lib.qevict_length(self.handle, layer))
+
+    def num_windows(self, layer=0) -> int:
+        return -(-self.length(layer) // self.w)
+
+    # ---- the path -----------------------------------------------------------
+    def prefill(self, layer, k, v, scores=None, tiers=None, stream=None):
+        n = k.shape[1]
+        self._check(self.lib.qevict_prefill(self.handle, layer, _ptr(k), _ptr(v), n, _ptr(scores),
+                                            _ptr(tiers), _stream(stream)))
+
+    def append(self, layer, k, v, stream=None):
+        self._check(self.lib.qevict_append_kv(self.handle, layer, _ptr(k), _ptr(v), k.shape[1],
+                                              _stream(stream)))
+
+    def decode(self, layer, q, out=None, mass=None, want_mass=True, accumulate=True, stream=None):
+        if out is None:
+            out = torch.empty(self.B, self.Hq, HEAD_DIM, dtype=torch.float32, device=q.device)
+        if mass is None and want_mass:
+            mass = torch.empty(self.B, self.Hq, self.num_windows(layer), dtype=torch.float32,
+                               device=q.device)
+        self._check(self.lib.qevict_decode_attention(self.handle, layer, _ptr(q), _ptr(out), _ptr(mass),
+                                                     1 if accumulate else 0, _stream(stream)))
+        return out, mass
+
+    def route(self, layer, scores_override=None, score_mult=None, stream=None):
+        self._check(self.lib.qevict_route(self.handle, layer, _ptr(scores_override), _ptr(score_mult),
+                                          _stream(stream)))
+
+    def demote(self, layer, pairs, stream=None):
+        self._check(self.lib.qevict_demote_quantize(self.handle, layer, _ptr(pairs), pairs.shape[0],
+                                                    _stream(stream)))
+
+    def promote(self, layer, pairs, stream=None):
+        self._check(self.lib.qevict_promote_dequantize(self.handle, layer, _ptr(pairs), pairs.shape[0],
+                                                       _stream(stream)))
+
+    def set_tiers(self, layer, tiers, stream=None):
+        self._check(self.lib.qevict_set_tiers(self.handle, layer, _ptr(tiers), _stream(stream)))
+
+    def scores(self, layer, stream=None):
+        out = torch.empty(self.B, self.num_windows(layer), dtype=torch.float32, device="cuda")
+        self._check(self.lib.qevict_get_scores(self.handle, layer, _ptr(out), _stream(stream)))
+        return out
+
+    # ---- inspection ---------------------------------------------------------
+    def view(self, layer) -> View:
+        v = View()
+        self._check(self.lib.qevict_get_view(self.handle, layer, ctypes.byref(v)))
+        return v
+
+    def status(self, stream=None) -> int:
+        return int(self.lib.qevict_get_status(self.handle, _stream(stream)))
+
+    def last_error(self) -> str:
+        return self.lib.qevict_last_error().decode()
+
+    def clear_status(self, stream=None):
+        self._check(self.lib.qevict_clear_status(self.handle, _stream(stream)))
+
+    def stats(self, stream=None) -> dict:
+        s = Stats()
+        self._check(self.lib.qevict_get_stats(self.handle, ctypes.byref(s), _stream(stream)))
+        return {f: getattr(s, f) for f, _ in Stats._fields_}
+
+    def tables(self, layer):
+        """(tier, fp_slot, ledger_slot, ledger_writes) of the current windows, copied to host."""
+        v = self.view(layer)
+        W, Wm, B = v.num_windows, v.max_windows, v.batch
+        get = lambda p, t: device_tensor(p, (B, Wm), t)[:, :W].cpu()
+        return (get(v.tier, "|u1"), get(v.fp_slot, "<i4"), get(v.ledger_slot, "<i4"),
+                get(v.ledger_writes, "<i4"))
+
+    def fp_window(self, layer, slot):
+        """bf16 [Hkv][2][w][d] content of a full-precision slot (host copy)."""
+        v = self.view(layer)
+        raw = device_tensor(v.fp_pool + slot * v.fp_slot_bytes, (v.fp_slot_bytes,), "|u1").cpu()
+        return raw.view(torch.bfloat16).view(self.Hkv, 2, self.w, HEAD_DIM)
+
+    def ledger_window(self, layer, slot):
+        """Decoded ledger slot: codes uint8 [Hkv][2][w][d], scale/min fp16 [Hkv][2][w][d/32]."""
+        v = self.view(layer)
+        raw = device_tensor(v.ledger_pool + slot * v.ledger_slot_bytes, (v.ledger_slot_bytes,), "|u1").cpu()
+        return decode_ledger_slot(raw, self.Hkv, self.w)
+
+
+def decode_ledger_slot(raw: torch.Tensor, Hkv: int, w: int):
+    """Unpack the documented ledger slot layout (see include/qevict.h) on the host."""
+    d = HEAD_DIM
+    part = w * (d // 4) + w * (d // 32) * 4
+    raw = raw.view(Hkv, 2, part)
+    codes = torch.empty(Hkv, 2, w, d, dtype=torch.uint8)
+    shifts = torch.arange(16, dtype=torch.int64) * 2
+    for kv in range(2):
+        words = raw[:, kv, :w * d // 4].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+        if kv == 0:     # [token][d/16 words], channel j at word j//16 bits 2*(j%16)
+            wv = words.view(Hkv, w, d // 16)
+            c = (wv[..., None] >> shifts) & 3          # [Hkv][w][d/16][16]
+            codes[:, 0] = c.reshape(Hkv, w, d).to(torch.uint8)
+        else:           # [token/16][d], token t of the tile at bits 2*(t%16)
+            wv = words.view(Hkv, w // 16, d)
+            c = (wv[..., None] >> shifts) & 3          # [Hkv][tiles][d][16]
+            codes[:, 1] = c.permute(0, 1, 3, 2).reshape(Hkv, w, d).to(torch.uint8)
+    meta = raw[:, :, w * d // 4:].contiguous().view(torch.float16).view(Hkv, 2, w, d // 32, 2)
+    return codes, meta[..., 0].clone(), meta[..., 1].clone()

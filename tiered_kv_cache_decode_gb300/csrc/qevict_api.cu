@@ -1,0 +1,507 @@
+// Host side of the C ABI declared in include/qevict.h: configuration checks,
+// slot-pool sizing from the byte budget, device allocations, host-side error
+// reporting and the launch sequence of every call.
+#include "qevict_internal.cuh"
+
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <string>
+#include <vector>
+
+using namespace qevict;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+qevict_status fail(qevict_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+qevict_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(QEVICT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct LayerHost {
+    LayerDev dev{};
+    int64_t length = 0;
+    void *base = nullptr;
+};
+
+}  // namespace
+
+struct qevict_cache {
+    qevict_config cfg{};
+    qevict_allocator alloc{};
+    bool user_alloc = false;
+    cudaStream_t stream = nullptr;
+    int device = 0;
+    int num_sms = 1;
+    int Wmax = 0, CF = 0, CQ = 0, G = 0;
+    int64_t c_fp = 0, c_q = 0;
+    std::vector<LayerHost> layers;
+    CacheDev cdev{};
+    void *cbase = nullptr;
+    int64_t total_bytes = 0;
+    std::vector<void *> blocks;
+};
+
+namespace {
+
+void *dev_alloc(qevict_cache *c, size_t bytes) {
+    void *p = nullptr;
+    if (c->user_alloc) {
+        p = c->alloc.alloc(bytes, (void *)c->stream, c->alloc.ctx);
+    } else if (cudaMalloc(&p, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        p = nullptr;
+    }
+    if (p) {
+        c->blocks.push_back(p);
+        c->total_bytes += (int64_t)bytes;
+    }
+    return p;
+}
+
+void release_all(qevict_cache *c) {
+    for (void *p : c->blocks) {
+        if (c->user_alloc) c->alloc.free(p, (void *)c->stream, c->alloc.ctx);
+        else cudaFree(p);
+    }
+    c->blocks.clear();
+}
+
+struct Carver {
+    size_t off = 0;
+    size_t take(size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) & ~size_t(255);
+        return o;
+    }
+};
+
+// Window costs per sequence: full-precision K+V bf16, INT2 codes + fp16 meta.
+void window_costs(int w, int Hkv, int64_t *c_fp, int64_t *c_q) {
+    *c_fp = (int64_t)w * Hkv * kHeadDim * 4;
+    *c_q = (int64_t)w * Hkv * 2 * (kHeadDim / 4 + 4 * (kHeadDim / kGroup));
+}
+
+int64_t budget_bytes(const qevict_config &cfg, int64_t L) {
+    const int64_t F = L * cfg.num_kv_heads * kHeadDim * 4;
+    return (int64_t)floor(cfg.budget_frac * (double)F);
+}
+
+int fp_budget_windows(int64_t Bt, int64_t c_fp, double rho) {  // host copy of the plan kernel's rule
+    return (int)floor((rho * (double)Bt) / (double)c_fp);
+}
+
+qevict_status check_layer(const qevict_cache *c, int32_t layer) {
+    if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    if (layer < 0 || layer >= c->cfg.num_layers)
+        return fail(QEVICT_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, c->cfg.num_layers);
+    return QEVICT_OK;
+}
+
+int n_windows(const qevict_cache *c, int64_t L) { return (int)((L + c->cfg.window - 1) / c->cfg.window); }
+
+// Plan + the data movement it queues, in order: quantise (reads full-precision
+// slots released by demotions), then promote / prefill copy (write slots).
+qevict_status run_plan(qevict_cache *c, LayerHost &lh, const PlanArgs &a, const __nv_bfloat16 *k_ext,
+                       const __nv_bfloat16 *v_ext, cudaStream_t s) {
+    cudaError_t e = launch_plan(lh.dev, c->cdev, a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "plan kernel");
+    const int maxq = c->Wmax < c->CQ ? c->Wmax : c->CQ;
+    const int maxf = c->Wmax < c->CF ? c->Wmax : c->CF;
+    const bool prefill = a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_PREFILL_TIERS;
+    if (a.mode != PLAN_PROMOTE) {
+        e = launch_quantize(lh.dev, c->cdev, a.layer, k_ext, v_ext, a.prefill_len, maxq, s);
+        if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");
+    }
+    if (prefill) {
+        e = launch_prefill_copy(lh.dev, k_ext, v_ext, a.prefill_len, maxf, s);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill copy kernel");
+    } else if (a.mode != PLAN_DEMOTE) {
+        e = launch_promote(lh.dev, c->cdev, maxf, s);
+        if (e != cudaSuccess) return cuda_fail(e, "promote kernel");
+    }
+    return QEVICT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qevict_last_error(void) { return g_last_error.c_str(); }
+
+qevict_status qevict_cache_create(const qevict_config *config, const qevict_allocator *allocator, void *stream,
+                                  qevict_cache **out) {
+    if (!config || !out) return fail(QEVICT_ERR_INVALID_ARG, "config and out must not be NULL");
+    *out = nullptr;
+    const qevict_config &cfg = *config;
+    if (cfg.batch < 1 || cfg.num_layers < 1 || cfg.num_kv_heads < 1 || cfg.num_q_heads < 1)
+        return fail(QEVICT_ERR_INVALID_ARG, "batch, layers and head counts must be >= 1");
+    if (cfg.num_q_heads % cfg.num_kv_heads != 0 || cfg.num_q_heads / cfg.num_kv_heads > kMaxG)
+        return fail(QEVICT_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads, at most %d per KV head",
+                    kMaxG);
+    if (cfg.head_dim != kHeadDim) return fail(QEVICT_ERR_INVALID_ARG, "head_dim must be %d", kHeadDim);
+    if (cfg.window < 16 || cfg.window > 128 || cfg.window % kVTile != 0)
+        return fail(QEVICT_ERR_INVALID_ARG, "window must be a multiple of 16 in [16, 128]");
+    if (cfg.max_context < 1) return fail(QEVICT_ERR_INVALID_ARG, "max_context must be >= 1");
+    if (!(cfg.budget_frac > 0.0 && cfg.budget_frac <= 1.0))
+        return fail(QEVICT_ERR_INVALID_ARG, "budget_frac must be in (0, 1]");
+    if (!(cfg.fp_share > 0.0 && cfg.fp_share <= 1.0))
+        return fail(QEVICT_ERR_INVALID_ARG, "fp_share must be in (0, 1]");
+    if (cfg.fp_capacity < 0 || cfg.ledger_capacity < 0 || cfg.fp_slack < 0)
+        return fail(QEVICT_ERR_INVALID_ARG, "capacities must be >= 0");
+    const int Wmax = (cfg.max_context + cfg.window - 1) / cfg.window;
+    if (Wmax > 4096) return fail(QEVICT_ERR_INVALID_ARG, "at most 4096 windows per sequence (got %d)", Wmax);
+    if (allocator && (!allocator->alloc || !allocator->free))
+        return fail(QEVICT_ERR_INVALID_ARG, "allocator needs both alloc and free");
+
+    qevict_cache *c = new qevict_cache();
+    c->cfg = cfg;
+    if (allocator) {
+        c->alloc = *allocator;
+        c->user_alloc = true;
+    }
+    c->stream = (cudaStream_t)stream;
+    cudaGetDevice(&c->device);
+    cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+    c->G = cfg.num_q_heads / cfg.num_kv_heads;
+    c->Wmax = Wmax;
+    window_costs(cfg.window, cfg.num_kv_heads, &c->c_fp, &c->c_q);
+    {
+        const int64_t Bmax = budget_bytes(cfg, cfg.max_context);
+        int nfp = fp_budget_windows(Bmax, c->c_fp, cfg.fp_share);
+        if (nfp < 1) nfp = 1;
+        if (nfp > Wmax) nfp = Wmax;
+        int64_t nq = (Bmax - (int64_t)nfp * c->c_fp) / c->c_q;
+        if (nq < 0) nq = 0;
+        const int slack = cfg.fp_slack > 0 ? cfg.fp_slack : 4;
+        c->CF = cfg.fp_capacity > 0 ? cfg.fp_capacity : (nfp + slack < Wmax ? nfp + slack : Wmax);
+        c->CQ = cfg.ledger_capacity > 0 ? cfg.ledger_capacity : (int)(nfp + nq < Wmax ? nfp + nq : Wmax);
+        if (c->CQ < 1) c->CQ = 1;
+    }
+    const int B = cfg.batch, Hkv = cfg.num_kv_heads, Hq = cfg.num_q_heads, w = cfg.window;
+    const int64_t fps = (int64_t)Hkv * 2 * w * kHeadDim * 2;
+    const int64_t lgs = (int64_t)Hkv * 2 * lg_part_bytes(w);
+
+    cudaError_t err = cudaSuccess;
+    // cache-wide status and statistics
+    c->cbase = dev_alloc(c, 256);
+    if (!c->cbase) {
+        release_all(c);
+        delete c;
+        return fail(QEVICT_ERR_OUT_OF_MEMORY, "allocation of 256 B failed");
+    }
+    c->cdev.status = reinterpret_cast<int32_t *>(c->cbase);
+    c->cdev.stats = reinterpret_cast<unsigned long long *>((uint8_t *)c->cbase + 64);
+
+    // every allocation first, so that a failing allocator leaves nothing behind
+    c->layers.resize(cfg.num_layers);
+    for (int l = 0; l < cfg.num_layers; ++l) {
+        LayerDev &D = c->layers[l].dev;
+        D.B = B;
+        D.Hq = Hq;
+        D.Hkv = Hkv;
+        D.G = c->G;
+        D.w = w;
+        D.Wmax = Wmax;
+        D.CF = c->CF;
+        D.CQ = c->CQ;
+        D.max_context = cfg.max_context;
+        D.beta = cfg.budget_frac;
+        D.rho = cfg.fp_share;
+        D.c_fp = c->c_fp;
+        D.c_q = c->c_q;
+        D.fp_slot_bytes = fps;
+        D.lg_slot_bytes = lgs;
+        Carver cv;
+        const size_t o_fp = cv.take((size_t)B * c->CF * fps);
+        const size_t o_lg = cv.take((size_t)B * c->CQ * lgs);
+        const size_t o_tier = cv.take((size_t)B * Wmax);
+        const size_t o_fps = cv.take((size_t)B * Wmax * 4);
+        const size_t o_lgs = cv.take((size_t)B * Wmax * 4);
+        const size_t o_lw = cv.take((size_t)B * Wmax * 4);
+        const size_t o_sc = cv.take((size_t)B * Hkv * Wmax * 4);
+        const size_t o_ff = cv.take((size_t)B * c->CF * 4);
+        const size_t o_lf = cv.take((size_t)B * c->CQ * 4);
+        const size_t o_fl = cv.take((size_t)B * c->CF * 8);
+        const size_t o_ql = cv.take((size_t)B * c->CQ * 8);
+        const size_t o_ctr = cv.take((size_t)B * kCtrN * 4);
+        const size_t o_wq = cv.take((size_t)B * Wmax * 16);
+        const size_t o_wp = cv.take((size_t)B * Wmax * 16);
+        const size_t o_wc = cv.take((size_t)B * Wmax * 16);
+        const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * (2 + kHeadDim) * 4);
+        const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
+        const size_t o_arr = cv.take((size_t)B * Hkv * 4);
+        uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
+        if (!base) {
+            const size_t need = cv.off;
+            release_all(c);
+            delete c;
+            return fail(QEVICT_ERR_OUT_OF_MEMORY, "allocation of %zu B for layer %d failed", need, l);
+        }
+        c->layers[l].base = base;
+        D.fp_pool = base + o_fp;
+        D.lg_pool = base + o_lg;
+        D.tier = base + o_tier;
+        D.fp_slot = (int32_t *)(base + o_fps);
+        D.lg_slot = (int32_t *)(base + o_lgs);
+        D.lwrites = (int32_t *)(base + o_lw);
+        D.score_part = (float *)(base + o_sc);
+        D.fp_free = (int32_t *)(base + o_ff);
+        D.lg_free = (int32_t *)(base + o_lf);
+        D.fp_list = (int2 *)(base + o_fl);
+        D.q_list = (int2 *)(base + o_ql);
+        D.ctr = (int32_t *)(base + o_ctr);
+        D.work_q = (int4 *)(base + o_wq);
+        D.work_p = (int4 *)(base + o_wp);
+        D.work_c = (int4 *)(base + o_wc);
+        D.part = (float *)(base + o_part);
+        D.wstat = (float2 *)(base + o_ws);
+        D.arrive = (uint32_t *)(base + o_arr);
+    }
+    err = cudaMemsetAsync(c->cbase, 0, 256, c->stream);
+    for (int l = 0; l < cfg.num_layers && err == cudaSuccess; ++l) err = launch_init_layer(c->layers[l].dev, c->stream);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(c->stream);
+    if (err != cudaSuccess) {
+        release_all(c);
+        delete c;
+        return cuda_fail(err, "cache initialisation");
+    }
+    *out = c;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_cache_destroy(qevict_cache *cache) {
+    if (!cache) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    cudaStreamSynchronize(cache->stream);
+    release_all(cache);
+    delete cache;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_prefill(qevict_cache *c, int32_t layer, const void *k, const void *v, int32_t n_tokens,
+                             const float *scores, const uint8_t *tiers, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (!k || !v) return fail(QEVICT_ERR_INVALID_ARG, "k and v must not be NULL");
+    if ((scores == nullptr) == (tiers == nullptr))
+        return fail(QEVICT_ERR_INVALID_ARG, "give exactly one of scores and tiers");
+    if (n_tokens < 1 || n_tokens > c->cfg.max_context)
+        return fail(QEVICT_ERR_INVALID_ARG, "n_tokens %d out of [1, %d]", n_tokens, c->cfg.max_context);
+    if (lh.length != 0) return fail(QEVICT_ERR_STATE, "prefill needs an empty layer (length %lld)", (long long)lh.length);
+    PlanArgs a{};
+    a.mode = scores ? PLAN_PREFILL_SCORES : PLAN_PREFILL_TIERS;
+    a.layer = layer;
+    a.prefill_len = n_tokens;
+    a.scores = scores;
+    a.tiers = tiers;
+    if (scores) {
+        const int64_t Bt = budget_bytes(c->cfg, n_tokens);
+        if (Bt < c->c_fp)
+            return fail(QEVICT_ERR_BUDGET, "budget %lld B cannot hold the open window (%lld B)", (long long)Bt,
+                        (long long)c->c_fp);
+    }
+    st = run_plan(c, lh, a, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, (cudaStream_t)stream);
+    if (st) return st;
+    lh.length = n_tokens;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_append_kv(qevict_cache *c, int32_t layer, const void *k, const void *v, int32_t n_new,
+                               void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (!k || !v) return fail(QEVICT_ERR_INVALID_ARG, "k and v must not be NULL");
+    if (n_new < 1) return fail(QEVICT_ERR_INVALID_ARG, "n_new must be >= 1");
+    if (lh.length + n_new > c->cfg.max_context)
+        return fail(QEVICT_ERR_INVALID_ARG, "context %lld + %d passes max_context %d", (long long)lh.length, n_new,
+                    c->cfg.max_context);
+    cudaError_t e = launch_append(lh.dev, c->cdev, layer, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, n_new,
+                                  (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "append kernel");
+    lh.length += n_new;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_decode_attention(qevict_cache *c, int32_t layer, const void *q, float *out, float *mass,
+                                      int32_t accumulate_scores, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (!q || !out) return fail(QEVICT_ERR_INVALID_ARG, "q and out must not be NULL");
+    if (lh.length < 1) return fail(QEVICT_ERR_INVALID_ARG, "layer %d is empty", layer);
+    const int bk = c->cfg.batch * c->cfg.num_kv_heads;
+    int splits = (2 * c->num_sms + bk - 1) / bk;
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    if (splits < 1) splits = 1;
+    cudaError_t e = launch_decode(lh.dev, c->cdev, layer, (const __nv_bfloat16 *)q, out, mass, accumulate_scores,
+                                  splits, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    return QEVICT_OK;
+}
+
+qevict_status qevict_route(qevict_cache *c, int32_t layer, const float *scores_override, const float *score_mult,
+                           void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (lh.length == 0) return QEVICT_OK;
+    PlanArgs a{};
+    a.mode = PLAN_ROUTE;
+    a.layer = layer;
+    a.scores = scores_override;
+    a.mult = score_mult;
+    const int64_t Bt = budget_bytes(c->cfg, lh.length);
+    if (Bt < c->c_fp)
+        return fail(QEVICT_ERR_BUDGET, "budget %lld B cannot hold the open window (%lld B)", (long long)Bt,
+                    (long long)c->c_fp);
+    return run_plan(c, lh, a, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+static qevict_status listed(qevict_cache *c, int32_t layer, const int32_t *bw, int32_t n, int mode, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (n < 0) return fail(QEVICT_ERR_INVALID_ARG, "n must be >= 0");
+    if (n == 0 || lh.length == 0) return QEVICT_OK;
+    if (!bw) return fail(QEVICT_ERR_INVALID_ARG, "bw_ids must not be NULL");
+    PlanArgs a{};
+    a.mode = mode;
+    a.layer = layer;
+    a.pairs = bw;
+    a.n_pairs = n;
+    return run_plan(c, lh, a, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+qevict_status qevict_demote_quantize(qevict_cache *c, int32_t layer, const int32_t *bw_ids, int32_t n, void *stream) {
+    return listed(c, layer, bw_ids, n, PLAN_DEMOTE, stream);
+}
+
+qevict_status qevict_promote_dequantize(qevict_cache *c, int32_t layer, const int32_t *bw_ids, int32_t n,
+                                        void *stream) {
+    return listed(c, layer, bw_ids, n, PLAN_PROMOTE, stream);
+}
+
+qevict_status qevict_set_tiers(qevict_cache *c, int32_t layer, const uint8_t *tiers, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (!tiers) return fail(QEVICT_ERR_INVALID_ARG, "tiers must not be NULL");
+    if (lh.length == 0) return QEVICT_OK;
+    PlanArgs a{};
+    a.mode = PLAN_TIERS;
+    a.layer = layer;
+    a.tiers = tiers;
+    return run_plan(c, lh, a, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+qevict_status qevict_get_scores(qevict_cache *c, int32_t layer, float *scores, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!scores) return fail(QEVICT_ERR_INVALID_ARG, "scores must not be NULL");
+    LayerHost &lh = c->layers[layer];
+    const int nw = n_windows(c, lh.length);
+    if (nw == 0) return QEVICT_OK;
+    cudaError_t e = launch_scores(lh.dev, nw, scores, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "scores kernel");
+    return QEVICT_OK;
+}
+
+qevict_status qevict_get_view(const qevict_cache *c, int32_t layer, qevict_view *v) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!v) return fail(QEVICT_ERR_INVALID_ARG, "view must not be NULL");
+    const LayerHost &lh = c->layers[layer];
+    const LayerDev &D = lh.dev;
+    v->batch = D.B;
+    v->num_q_heads = D.Hq;
+    v->num_kv_heads = D.Hkv;
+    v->head_dim = kHeadDim;
+    v->window = D.w;
+    v->max_windows = D.Wmax;
+    v->num_windows = n_windows(c, lh.length);
+    v->fp_capacity = D.CF;
+    v->ledger_capacity = D.CQ;
+    v->length = lh.length;
+    v->fp_slot_bytes = D.fp_slot_bytes;
+    v->ledger_slot_bytes = D.lg_slot_bytes;
+    v->tier = D.tier;
+    v->fp_slot = D.fp_slot;
+    v->ledger_slot = D.lg_slot;
+    v->ledger_writes = D.lwrites;
+    v->fp_pool = D.fp_pool;
+    v->ledger_pool = D.lg_pool;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_get_status(qevict_cache *c, void *stream) {
+    if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+    int32_t s[4];
+    e = cudaMemcpy(s, c->cdev.status, sizeof s, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "status copy");
+    if (s[0] != 0) {
+        g_last_error = "device status " + std::to_string(s[0]) + " at layer " + std::to_string(s[1]) +
+                       " (sequence " + std::to_string(s[2]) + ", item " + std::to_string(s[3]) + ")";
+    }
+    return (qevict_status)s[0];
+}
+
+qevict_status qevict_clear_status(qevict_cache *c, void *stream) {
+    if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    cudaError_t e = cudaMemsetAsync(c->cdev.status, 0, 16, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    return QEVICT_OK;
+}
+
+qevict_status qevict_get_stats(qevict_cache *c, qevict_stats *out, void *stream) {
+    if (!c || !out) return fail(QEVICT_ERR_INVALID_ARG, "cache and stats must not be NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronise");
+    unsigned long long s[ST_N];
+    e = cudaMemcpy(s, c->cdev.stats, sizeof s, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "stats copy");
+    out->demotions = s[ST_DEMOTE];
+    out->promotions = s[ST_PROMOTE];
+    out->evictions = s[ST_EVICT];
+    out->ledger_writes = s[ST_LWRITE];
+    out->ledger_reuses = s[ST_LREUSE];
+    out->device_bytes = c->total_bytes;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_refresh_lengths(qevict_cache *c, void *stream) {
+    if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t *dbuf = reinterpret_cast<int32_t *>((uint8_t *)c->cbase + 128);
+    for (int l = 0; l < c->cfg.num_layers; ++l) {
+        cudaError_t e = launch_read_lengths(c->layers[l].dev, dbuf, s);
+        int32_t len = 0;
+        if (e == cudaSuccess) e = cudaMemcpyAsync(&len, dbuf, sizeof len, cudaMemcpyDeviceToHost, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "length refresh");
+        c->layers[l].length = len;
+    }
+    return QEVICT_OK;
+}
+
+int64_t qevict_length(const qevict_cache *c, int32_t layer) {
+    if (!c || layer < 0 || layer >= c->cfg.num_layers) return -1;
+    return c->layers[layer].length;
+}
+
+}  // extern "C"

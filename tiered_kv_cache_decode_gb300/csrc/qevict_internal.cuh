@@ -1,0 +1,112 @@
+// Internal declarations shared by the translation units of the library:
+// the device view of one layer, launch entry points, and small PTX helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qevict.h"
+
+namespace qevict {
+
+constexpr int kHeadDim = 128;          // d
+constexpr int kGroup = 32;             // channels per INT2 group
+constexpr int kGroups = kHeadDim / kGroup;
+constexpr int kMaxG = 8;               // query heads per KV head
+constexpr int kMaxSplits = 64;         // decode splits per (sequence, KV head)
+constexpr int kVTile = 16;             // tokens per transposed V-code word
+constexpr int kCtrN = 8;               // counters per sequence
+
+// counter slots (per sequence)
+enum { CTR_NFP = 0, CTR_NQ = 1, CTR_FP_TOP = 2, CTR_LG_TOP = 3, CTR_WQ = 4, CTR_WP = 5,
+       CTR_WC = 6, CTR_LEN = 7 };
+
+// device stats slots
+enum { ST_DEMOTE = 0, ST_PROMOTE = 1, ST_EVICT = 2, ST_LWRITE = 3, ST_LREUSE = 4, ST_N = 8 };
+
+// Bytes of one INT2 part (one KV head, K or V) of a ledger window.
+__host__ __device__ inline int64_t lg_part_bytes(int w) {
+    return (int64_t)w * (kHeadDim / 4) + (int64_t)w * kGroups * 4;
+}
+__host__ __device__ inline int64_t lg_codes_bytes(int w) { return (int64_t)w * (kHeadDim / 4); }
+
+// Everything a kernel needs about one layer of the cache (passed by value).
+struct LayerDev {
+    int B, Hq, Hkv, G, w, Wmax, CF, CQ;
+    int max_context;
+    double beta, rho;           // budget fraction and its full-precision share
+    int64_t c_fp, c_q;          // bytes of one window per sequence in each visible tier
+    int64_t fp_slot_bytes, lg_slot_bytes;
+    uint8_t *fp_pool;     // [B*CF][fp_slot_bytes]   bf16 [Hkv][2][w][d]
+    uint8_t *lg_pool;     // [B*CQ][lg_slot_bytes]   parts [Hkv][2]
+    uint8_t *tier;        // [B][Wmax]
+    int32_t *fp_slot;     // [B][Wmax]
+    int32_t *lg_slot;     // [B][Wmax]
+    int32_t *lwrites;     // [B][Wmax]
+    float *score_part;    // [B][Hkv][Wmax] per-KV-head-group partial cumulative scores
+    int32_t *fp_free;     // [B][CF] stack of free slot indices
+    int32_t *lg_free;     // [B][CQ]
+    int2 *fp_list;        // [B][CF] {window, slot} of full-precision windows
+    int2 *q_list;         // [B][CQ] {window, slot} of INT2 windows
+    int32_t *ctr;         // [B][kCtrN]; CTR_LEN is the context length the kernels use
+    int4 *work_q;         // [B][Wmax] quantise: {window, src fp slot or -1 (external), dst ledger slot, 0}
+    int4 *work_p;         // [B][Wmax] promote: {window, src ledger slot, dst fp slot, 0}
+    int4 *work_c;         // [B][Wmax] prefill copy: {window, dst fp slot, 0, 0}
+    float *part;          // [B][Hkv][kMaxSplits][G][2 + d] decode split partials
+    float2 *wstat;        // [B][Hq][Wmax] (window max, window exp-sum), log2 domain
+    uint32_t *arrive;     // [B][Hkv] split arrival counters (kept at 0 between launches)
+};
+
+struct CacheDev {
+    int32_t *status;              // [4]: code, layer, info0, info1
+    unsigned long long *stats;    // [ST_N]
+};
+
+enum PlanMode { PLAN_ROUTE = 0, PLAN_TIERS = 1, PLAN_PREFILL_SCORES = 2, PLAN_PREFILL_TIERS = 3,
+                PLAN_DEMOTE = 4, PLAN_PROMOTE = 5 };
+
+struct PlanArgs {
+    int mode;
+    int layer;
+    int64_t prefill_len;  // tokens a prefill brings (prefill modes only)
+    const float *scores;  // override / prefill scores [B][n_win]
+    const float *mult;    // [B][n_win]
+    const uint8_t *tiers; // [B][n_win]
+    const int32_t *pairs; // [n][2]
+    int n_pairs;
+};
+
+// ---- launchers (each enqueues on `s`, returns the launch error) -----------
+cudaError_t launch_init_layer(const LayerDev &L, cudaStream_t s);
+cudaError_t launch_append(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *k,
+                          const __nv_bfloat16 *v, int n_new, cudaStream_t s);
+cudaError_t launch_plan(const LayerDev &L, const CacheDev &C, const PlanArgs &a, cudaStream_t s);
+cudaError_t launch_quantize(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *k_ext,
+                            const __nv_bfloat16 *v_ext, int64_t ext_len, int max_entries,
+                            cudaStream_t s);
+cudaError_t launch_promote(const LayerDev &L, const CacheDev &C, int max_entries, cudaStream_t s);
+cudaError_t launch_prefill_copy(const LayerDev &L, const __nv_bfloat16 *k_ext,
+                                const __nv_bfloat16 *v_ext, int64_t ext_len, int max_entries,
+                                cudaStream_t s);
+cudaError_t launch_scores(const LayerDev &L, int n_win, float *out, cudaStream_t s);
+cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *q,
+                          float *out, float *mass, int accumulate, int splits, cudaStream_t s);
+cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s);
+int decode_smem_bytes(int w, int G);
+
+// ---- device helpers -------------------------------------------------------
+__device__ __forceinline__ void set_status(const CacheDev &C, int code, int layer, int i0, int i1) {
+    if (atomicCAS(C.status, 0, code) == 0) {
+        C.status[1] = layer;
+        C.status[2] = i0;
+        C.status[3] = i1;
+    }
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+}  // namespace qevict

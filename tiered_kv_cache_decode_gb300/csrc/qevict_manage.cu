@@ -1,0 +1,689 @@
+// Cache management kernels: layer initialisation, appends, the tier plan
+// (routing, explicit tiers, prefill, listed demotions / promotions), the
+// INT2 quantiser, the promotion dequantiser and the score reduction.
+//
+// Method: "Technische Samenvatting: QEvict" (gist.science 2608.05326),
+// "Methodologie: QEvict" and "Kernmechanismen" (window routing under a byte
+// budget, cumulative scoring, demotion, promotion, write-once ledger).
+#include "qevict_internal.cuh"
+
+#include <math.h>
+
+namespace qevict {
+
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanMaxW = 4096;
+
+// ---------------------------------------------------------------- init
+__global__ void init_layer_kernel(LayerDev D) {
+    const int64_t nW = (int64_t)D.B * D.Wmax;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t i = i0; i < nW; i += stride) {
+        D.tier[i] = QEVICT_TIER_E;
+        D.fp_slot[i] = -1;
+        D.lg_slot[i] = -1;
+        D.lwrites[i] = 0;
+    }
+    for (int64_t i = i0; i < nW * D.Hkv; i += stride) D.score_part[i] = 0.f;
+    for (int64_t i = i0; i < (int64_t)D.B * D.CF; i += stride) {
+        const int b = (int)(i / D.CF), j = (int)(i % D.CF);
+        D.fp_free[i] = b * D.CF + (D.CF - 1 - j);   // top of the stack pops slot b*CF first
+    }
+    for (int64_t i = i0; i < (int64_t)D.B * D.CQ; i += stride) {
+        const int b = (int)(i / D.CQ), j = (int)(i % D.CQ);
+        D.lg_free[i] = b * D.CQ + (D.CQ - 1 - j);
+    }
+    for (int64_t i = i0; i < D.B; i += stride) {
+        int32_t *c = D.ctr + i * kCtrN;
+        for (int k = 0; k < kCtrN; ++k) c[k] = 0;
+        c[CTR_FP_TOP] = D.CF;
+        c[CTR_LG_TOP] = D.CQ;
+    }
+    for (int64_t i = i0; i < (int64_t)D.B * D.Hkv; i += stride) D.arrive[i] = 0;
+}
+
+// ---------------------------------------------------------------- append
+// One CTA per sequence: thread 0 opens the windows that start inside the
+// appended range (a slot from the free list each), then the CTA copies the
+// tokens' K and V rows into their windows' full-precision slots.
+__global__ void append_kernel(LayerDev D, CacheDev C, int layer, const __nv_bfloat16 *__restrict__ k,
+                              const __nv_bfloat16 *__restrict__ v, int n_new) {
+    const int b = blockIdx.x;
+    const int w = D.w;
+    const int64_t wb = (int64_t)b * D.Wmax;
+    __shared__ int s_bad;
+    __shared__ int s_len;
+    if (threadIdx.x == 0) {
+        s_bad = 0;
+        int32_t *ctr = D.ctr + b * kCtrN;
+        const int64_t L0 = ctr[CTR_LEN];
+        s_len = (int)L0;
+        if (L0 + n_new > D.max_context) {
+            set_status(C, QEVICT_ERR_INVALID_ARG, layer, b, (int)L0);
+            s_bad = 1;
+        } else if (L0 % w != 0) {
+            const int wi = (int)(L0 / w);
+            if (D.tier[wb + wi] != QEVICT_TIER_FP || D.fp_slot[wb + wi] < 0) {
+                set_status(C, QEVICT_ERR_STATE, layer, b, wi);
+                s_bad = 1;
+            }
+        }
+        if (!s_bad) {
+            for (int64_t p = ((L0 + w - 1) / w) * w; p < L0 + n_new; p += w) {
+                const int wi = (int)(p / w);
+                const int top = ctr[CTR_FP_TOP];
+                int slot = -1;
+                if (top > 0) {
+                    slot = D.fp_free[b * D.CF + top - 1];
+                    ctr[CTR_FP_TOP] = top - 1;
+                } else {
+                    set_status(C, QEVICT_ERR_CAPACITY, layer, b, wi);
+                }
+                D.tier[wb + wi] = slot >= 0 ? QEVICT_TIER_FP : QEVICT_TIER_E;
+                D.fp_slot[wb + wi] = slot;
+                D.lg_slot[wb + wi] = -1;
+                D.lwrites[wb + wi] = 0;
+                for (int h = 0; h < D.Hkv; ++h) D.score_part[((int64_t)b * D.Hkv + h) * D.Wmax + wi] = 0.f;
+                if (slot >= 0) {
+                    const int n = ctr[CTR_NFP];
+                    D.fp_list[b * D.CF + n] = make_int2(wi, slot);
+                    ctr[CTR_NFP] = n + 1;
+                }
+            }
+            ctr[CTR_LEN] = (int)(L0 + n_new);
+        }
+    }
+    __syncthreads();
+    if (s_bad) return;
+    const int64_t L0 = s_len;
+    constexpr int kChunks = kHeadDim * 2 / 16;   // 16-byte chunks per row
+    const int64_t total = (int64_t)n_new * D.Hkv * 2 * kChunks;
+    for (int64_t i = threadIdx.x; i < total; i += blockDim.x) {
+        const int c = (int)(i % kChunks);
+        int64_t r = i / kChunks;
+        const int kv = (int)(r % 2);
+        r /= 2;
+        const int h = (int)(r % D.Hkv);
+        const int t = (int)(r / D.Hkv);
+        const int64_t p = L0 + t;
+        const int wi = (int)(p / w), row = (int)(p % w);
+        const int slot = D.fp_slot[wb + wi];
+        if (slot < 0) continue;
+        const __nv_bfloat16 *src = (kv ? v : k) + (((int64_t)b * n_new + t) * D.Hkv + h) * kHeadDim;
+        uint8_t *dst = D.fp_pool + (int64_t)slot * D.fp_slot_bytes +
+                       (((int64_t)(h * 2 + kv) * w + row) * kHeadDim) * 2;
+        reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
+    }
+}
+
+// ---------------------------------------------------------------- plan
+__device__ __forceinline__ uint32_t orderable(float f) {
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix sum over the block of one int per thread; *total gets the sum.
+__device__ int block_scan(int v, int *total, int *s_warp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int nwarp = kPlanThreads / 32;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int ws = lane < nwarp ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, ws, o);
+            if (lane >= o) ws += y;
+        }
+        if (lane < nwarp) s_warp[lane] = ws;
+    }
+    __syncthreads();
+    const int excl = x - v + (warp > 0 ? s_warp[warp - 1] : 0);
+    *total = s_warp[nwarp - 1];
+    __syncthreads();
+    return excl;
+}
+
+// One CTA per sequence. Computes the target tier of every window (by ranking
+// the cumulative scores under the budget, or from explicit tiers), then
+// applies the transitions: free the slots of evicted / demoted windows, take
+// slots for promotions and first quantisations, update the window table,
+// queue the data movement (quantise, dequantise, prefill copy) and rebuild
+// the per-tier window lists the decode kernel walks.
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev C, PlanArgs a) {
+    __shared__ unsigned long long s_key[kPlanMaxW];
+    __shared__ uint8_t s_cur[kPlanMaxW];
+    __shared__ uint8_t s_tgt[kPlanMaxW];
+    __shared__ int s_warp[kPlanThreads / 32 + 1];
+
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const int64_t wb = (int64_t)b * D.Wmax;
+    int32_t *ctr = D.ctr + b * kCtrN;
+    const bool prefill = a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_PREFILL_TIERS;
+    const int64_t length = prefill ? a.prefill_len : (int64_t)ctr[CTR_LEN];
+    const int nw = (int)((length + D.w - 1) / D.w);
+    const bool partial_last = (length % D.w) != 0;
+    if (tid == 0) {   // nothing queued unless this plan queues it
+        ctr[CTR_WQ] = 0;
+        ctr[CTR_WP] = 0;
+        ctr[CTR_WC] = 0;
+    }
+    if (nw == 0) return;
+    // byte budget at this length: B_t = floor(beta * L * Hkv * d * 4)
+    const int64_t budget = (int64_t)floor(D.beta * (double)(length * D.Hkv * kHeadDim * 4));
+    const int nfp_budget = (int)floor((D.rho * (double)budget) / (double)D.c_fp);
+    if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES) && budget < D.c_fp) {
+        if (tid == 0) set_status(C, QEVICT_ERR_BUDGET, a.layer, b, (int)length);
+        return;
+    }
+
+    for (int i = tid; i < nw; i += kPlanThreads) s_cur[i] = prefill ? QEVICT_TIER_FP : D.tier[wb + i];
+    __syncthreads();
+
+    if (a.mode == PLAN_DEMOTE || a.mode == PLAN_PROMOTE) {
+        // Listed transitions, applied one by one in list order.
+        if (tid == 0) {
+            int nq = 0, np = 0;
+            for (int i = 0; i < a.n_pairs; ++i) {
+                const int bb = a.pairs[2 * i], wi = a.pairs[2 * i + 1];
+                if (bb != b) continue;
+                if (wi < 0 || wi >= nw) {
+                    set_status(C, QEVICT_ERR_STATE, a.layer, b, wi);
+                    continue;
+                }
+                if (a.mode == PLAN_DEMOTE) {
+                    if (s_cur[wi] != QEVICT_TIER_FP || (wi == nw - 1 && partial_last)) {
+                        set_status(C, QEVICT_ERR_STATE, a.layer, b, wi);
+                        continue;
+                    }
+                    const int old_fp = D.fp_slot[wb + wi];
+                    int lg = D.lg_slot[wb + wi];
+                    if (lg < 0) {
+                        const int top = ctr[CTR_LG_TOP];
+                        if (top == 0) {
+                            set_status(C, QEVICT_ERR_CAPACITY, a.layer, b, wi);
+                            continue;
+                        }
+                        lg = D.lg_free[b * D.CQ + top - 1];
+                        ctr[CTR_LG_TOP] = top - 1;
+                        D.lg_slot[wb + wi] = lg;
+                        D.lwrites[wb + wi] += 1;
+                        D.work_q[wb + nq++] = make_int4(wi, old_fp, lg, 0);
+                        atomicAdd(&C.stats[ST_LWRITE], 1ull);
+                    } else {
+                        atomicAdd(&C.stats[ST_LREUSE], 1ull);
+                    }
+                    const int top = ctr[CTR_FP_TOP];
+                    D.fp_free[b * D.CF + top] = old_fp;
+                    ctr[CTR_FP_TOP] = top + 1;
+                    D.fp_slot[wb + wi] = -1;
+                    D.tier[wb + wi] = QEVICT_TIER_Q;
+                    s_cur[wi] = QEVICT_TIER_Q;
+                    atomicAdd(&C.stats[ST_DEMOTE], 1ull);
+                } else {
+                    if (s_cur[wi] != QEVICT_TIER_Q) {
+                        set_status(C, QEVICT_ERR_STATE, a.layer, b, wi);
+                        continue;
+                    }
+                    const int top = ctr[CTR_FP_TOP];
+                    if (top == 0) {
+                        set_status(C, QEVICT_ERR_CAPACITY, a.layer, b, wi);
+                        continue;
+                    }
+                    const int fp = D.fp_free[b * D.CF + top - 1];
+                    ctr[CTR_FP_TOP] = top - 1;
+                    D.fp_slot[wb + wi] = fp;
+                    D.tier[wb + wi] = QEVICT_TIER_FP;
+                    D.work_p[wb + np++] = make_int4(wi, D.lg_slot[wb + wi], fp, 0);
+                    s_cur[wi] = QEVICT_TIER_FP;
+                    atomicAdd(&C.stats[ST_PROMOTE], 1ull);
+                }
+            }
+            ctr[CTR_WQ] = nq;
+            ctr[CTR_WP] = np;
+        }
+        __syncthreads();
+        for (int i = tid; i < nw; i += kPlanThreads) s_tgt[i] = s_cur[i];
+        __syncthreads();
+    } else {
+        // ---- target tiers
+        for (int i = tid; i < nw; i += kPlanThreads) s_tgt[i] = s_cur[i];
+        int bad = 0;
+        if (a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES) {
+            int P = 1;
+            while (P < nw) P <<= 1;
+            for (int i = tid; i < P; i += kPlanThreads) {
+                unsigned long long key = ~0ull;
+                if (i < nw) {
+                    float S;
+                    if (a.scores) {
+                        S = a.scores[(int64_t)b * nw + i];
+                    } else {
+                        S = 0.f;
+                        for (int h = 0; h < D.Hkv; ++h) S += D.score_part[((int64_t)b * D.Hkv + h) * D.Wmax + i];
+                    }
+                    if (a.mult) S = S * a.mult[(int64_t)b * nw + i];
+                    if (S == 0.f) S = 0.f;   // one zero: -0 and +0 rank as equal
+                    for (int h = 0; h < D.Hkv; ++h)
+                        D.score_part[((int64_t)b * D.Hkv + h) * D.Wmax + i] = h == 0 ? S : 0.f;
+                    if (s_cur[i] != QEVICT_TIER_E) {
+                        if (!isfinite(S)) bad = 1;
+                        key = (i == nw - 1) ? (unsigned long long)i
+                                            : (((unsigned long long)(~orderable(S))) << 32) | (unsigned)i;
+                    }
+                }
+                s_key[i] = key;
+            }
+            if (__syncthreads_or(bad)) {
+                if (tid == 0) set_status(C, QEVICT_ERR_DEVICE, a.layer, b, -1);
+                return;
+            }
+            // bitonic sort, ascending: forced window first, then score desc, index asc
+            for (int kk = 2; kk <= P; kk <<= 1) {
+                for (int j = kk >> 1; j > 0; j >>= 1) {
+                    for (int i = tid; i < P; i += kPlanThreads) {
+                        const int ixj = i ^ j;
+                        if (ixj > i) {
+                            const unsigned long long x = s_key[i], y = s_key[ixj];
+                            const bool up = (i & kk) == 0;
+                            if ((x > y) == up) {
+                                s_key[i] = y;
+                                s_key[ixj] = x;
+                            }
+                        }
+                    }
+                    __syncthreads();
+                }
+            }
+            int ncand_local = 0;
+            for (int i = tid; i < nw; i += kPlanThreads) ncand_local += s_cur[i] != QEVICT_TIER_E;
+            int ncand;
+            block_scan(ncand_local, &ncand, s_warp);
+            const int n_fp = min(ncand, max(1, nfp_budget));
+            const int64_t rem = budget - (int64_t)n_fp * D.c_fp;
+            const int n_q = (int)min((int64_t)(ncand - n_fp), rem > 0 ? rem / D.c_q : 0);
+            for (int r = tid; r < ncand; r += kPlanThreads) {
+                const int wi = (int)(s_key[r] & 0xffffffffu);
+                s_tgt[wi] = r < n_fp ? QEVICT_TIER_FP : (r < n_fp + n_q ? QEVICT_TIER_Q : QEVICT_TIER_E);
+            }
+            __syncthreads();
+        } else {
+            for (int i = tid; i < nw; i += kPlanThreads) {
+                const uint8_t t = a.tiers[(int64_t)b * nw + i];
+                const uint8_t c = s_cur[i];
+                if (t > QEVICT_TIER_E || (c == QEVICT_TIER_E && t != QEVICT_TIER_E) ||
+                    (i == nw - 1 && partial_last && t != c))
+                    bad = 1;
+                s_tgt[i] = t;
+            }
+            if (__syncthreads_or(bad)) {
+                if (tid == 0) set_status(C, QEVICT_ERR_STATE, a.layer, b, -1);
+                return;
+            }
+        }
+
+        // ---- capacity check
+        const int per = (nw + kPlanThreads - 1) / kPlanThreads;
+        const int w0 = tid * per, w1 = min(nw, w0 + per);
+        int free_fp = 0, free_lg = 0, need_fp = 0, need_lg = 0;
+        for (int i = w0; i < w1; ++i) {
+            const uint8_t c = s_cur[i], t = s_tgt[i];
+            const int lg = prefill ? -1 : D.lg_slot[wb + i];
+            if (!prefill && c == QEVICT_TIER_FP && t != QEVICT_TIER_FP) ++free_fp;
+            if (c != QEVICT_TIER_E && t == QEVICT_TIER_E && lg >= 0) ++free_lg;
+            if (c == QEVICT_TIER_FP && t == QEVICT_TIER_Q && lg < 0) ++need_lg;
+            if ((c == QEVICT_TIER_Q && t == QEVICT_TIER_FP) || (prefill && t == QEVICT_TIER_FP)) ++need_fp;
+        }
+        int tot_free_fp, tot_free_lg, tot_need_fp, tot_need_lg;
+        const int off_free_fp = block_scan(free_fp, &tot_free_fp, s_warp);
+        const int off_free_lg = block_scan(free_lg, &tot_free_lg, s_warp);
+        const int off_need_fp = block_scan(need_fp, &tot_need_fp, s_warp);
+        const int off_need_lg = block_scan(need_lg, &tot_need_lg, s_warp);
+        const int fp_top = ctr[CTR_FP_TOP], lg_top = ctr[CTR_LG_TOP];
+        if (fp_top + tot_free_fp < tot_need_fp || lg_top + tot_free_lg < tot_need_lg) {
+            if (tid == 0) set_status(C, QEVICT_ERR_CAPACITY, a.layer, b, -1);
+            return;
+        }
+        // ---- phase A: release slots
+        {
+            int of = off_free_fp, ol = off_free_lg;
+            for (int i = w0; i < w1; ++i) {
+                const uint8_t c = s_cur[i], t = s_tgt[i];
+                if (!prefill && c == QEVICT_TIER_FP && t != QEVICT_TIER_FP)
+                    D.fp_free[b * D.CF + fp_top + of++] = D.fp_slot[wb + i];
+                const int lg = prefill ? -1 : D.lg_slot[wb + i];
+                if (c != QEVICT_TIER_E && t == QEVICT_TIER_E && lg >= 0)
+                    D.lg_free[b * D.CQ + lg_top + ol++] = lg;
+            }
+        }
+        __syncthreads();
+        const int fp_mid = fp_top + tot_free_fp, lg_mid = lg_top + tot_free_lg;
+        // ---- phase B: take slots, update the table, queue data movement
+        int nq_local = 0, np_local = 0, nc_local = 0;
+        for (int i = w0; i < w1; ++i) {
+            const uint8_t c = s_cur[i], t = s_tgt[i];
+            nq_local += (c == QEVICT_TIER_FP && t == QEVICT_TIER_Q && (prefill || D.lg_slot[wb + i] < 0));
+            np_local += (!prefill && c == QEVICT_TIER_Q && t == QEVICT_TIER_FP);
+            nc_local += (prefill && t == QEVICT_TIER_FP);
+        }
+        int tq, tp, tc;
+        int oq = block_scan(nq_local, &tq, s_warp);
+        int op = block_scan(np_local, &tp, s_warp);
+        int oc = block_scan(nc_local, &tc, s_warp);
+        int nf = off_need_fp, nl = off_need_lg;
+        unsigned long long st_dem = 0, st_pro = 0, st_evi = 0, st_lw = 0, st_lr = 0;
+        for (int i = w0; i < w1; ++i) {
+            const uint8_t c = s_cur[i], t = s_tgt[i];
+            const int64_t e = wb + i;
+            if (prefill) {
+                D.lwrites[e] = 0;
+                D.lg_slot[e] = -1;
+                D.fp_slot[e] = -1;
+                if (t == QEVICT_TIER_FP) {
+                    const int fp = D.fp_free[b * D.CF + fp_mid - 1 - nf++];
+                    D.fp_slot[e] = fp;
+                    D.work_c[wb + oc++] = make_int4(i, fp, 0, 0);
+                } else if (t == QEVICT_TIER_Q) {
+                    const int lg = D.lg_free[b * D.CQ + lg_mid - 1 - nl++];
+                    D.lg_slot[e] = lg;
+                    D.lwrites[e] = 1;
+                    D.work_q[wb + oq++] = make_int4(i, -1, lg, 0);
+                    ++st_dem;
+                    ++st_lw;
+                } else {
+                    ++st_evi;
+                }
+                D.tier[e] = t;
+                for (int h = 0; h < D.Hkv; ++h)
+                    if (a.mode == PLAN_PREFILL_TIERS) D.score_part[((int64_t)b * D.Hkv + h) * D.Wmax + i] = 0.f;
+                continue;
+            }
+            if (c == t) continue;
+            if (t == QEVICT_TIER_E) {
+                D.fp_slot[e] = -1;
+                D.lg_slot[e] = -1;
+                ++st_evi;
+            } else if (c == QEVICT_TIER_FP && t == QEVICT_TIER_Q) {
+                const int old_fp = D.fp_slot[e];
+                if (D.lg_slot[e] < 0) {
+                    const int lg = D.lg_free[b * D.CQ + lg_mid - 1 - nl++];
+                    D.lg_slot[e] = lg;
+                    D.lwrites[e] += 1;
+                    D.work_q[wb + oq++] = make_int4(i, old_fp, lg, 0);
+                    ++st_lw;
+                } else {
+                    ++st_lr;
+                }
+                D.fp_slot[e] = -1;
+                ++st_dem;
+            } else if (c == QEVICT_TIER_Q && t == QEVICT_TIER_FP) {
+                const int fp = D.fp_free[b * D.CF + fp_mid - 1 - nf++];
+                D.fp_slot[e] = fp;
+                D.work_p[wb + op++] = make_int4(i, D.lg_slot[e], fp, 0);
+                ++st_pro;
+            }
+            D.tier[e] = t;
+        }
+        if (st_dem) atomicAdd(&C.stats[ST_DEMOTE], st_dem);
+        if (st_pro) atomicAdd(&C.stats[ST_PROMOTE], st_pro);
+        if (st_evi) atomicAdd(&C.stats[ST_EVICT], st_evi);
+        if (st_lw) atomicAdd(&C.stats[ST_LWRITE], st_lw);
+        if (st_lr) atomicAdd(&C.stats[ST_LREUSE], st_lr);
+        if (tid == 0) {
+            ctr[CTR_FP_TOP] = fp_mid - tot_need_fp;
+            ctr[CTR_LG_TOP] = lg_mid - tot_need_lg;
+            ctr[CTR_WQ] = tq;
+            ctr[CTR_WP] = tp;
+            ctr[CTR_WC] = tc;
+        }
+        __syncthreads();
+    }
+
+    // ---- rebuild the per-tier window lists
+    const int per = (nw + kPlanThreads - 1) / kPlanThreads;
+    const int w0 = tid * per, w1 = min(nw, w0 + per);
+    int nfp_local = 0, nq_local = 0;
+    for (int i = w0; i < w1; ++i) {
+        nfp_local += s_tgt[i] == QEVICT_TIER_FP;
+        nq_local += s_tgt[i] == QEVICT_TIER_Q;
+    }
+    int tf, tq;
+    int of = block_scan(nfp_local, &tf, s_warp);
+    int oq = block_scan(nq_local, &tq, s_warp);
+    for (int i = w0; i < w1; ++i) {
+        if (s_tgt[i] == QEVICT_TIER_FP) D.fp_list[b * D.CF + of++] = make_int2(i, D.fp_slot[wb + i]);
+        if (s_tgt[i] == QEVICT_TIER_Q) D.q_list[b * D.CQ + oq++] = make_int2(i, D.lg_slot[wb + i]);
+    }
+    if (tid == 0) {
+        ctr[CTR_NFP] = tf;
+        ctr[CTR_NQ] = tq;
+        if (prefill) ctr[CTR_LEN] = (int)length;
+    }
+}
+
+// ---------------------------------------------------------------- quantise
+// INT2 quantisation of one window part (entry, KV head, K or V): per token and
+// group of 32 channels, min16 = fp16(min), scale16 = fp16(fl32(fl32(max-min)/3)),
+// code = clamp(rint(fl32(fl32(x - min16) / scale16)), 0, 3).
+__global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, int layer,
+                                                        const __nv_bfloat16 *__restrict__ k_ext,
+                                                        const __nv_bfloat16 *__restrict__ v_ext,
+                                                        int64_t ext_len) {
+    extern __shared__ uint8_t s_codes[];   // [w][d]
+    const int b = blockIdx.z;
+    const int h = blockIdx.y >> 1, kv = blockIdx.y & 1;
+    const int w = D.w;
+    const int n = D.ctr[b * kCtrN + CTR_WQ];
+    for (int e = blockIdx.x; e < n; e += gridDim.x) {
+        const int4 job = D.work_q[(int64_t)b * D.Wmax + e];
+        const int wi = job.x, src_slot = job.y, dst = job.z;
+        uint8_t *part = D.lg_pool + (int64_t)dst * D.lg_slot_bytes + (int64_t)(h * 2 + kv) * lg_part_bytes(w);
+        __half2 *meta = reinterpret_cast<__half2 *>(part + lg_codes_bytes(w));
+        for (int it = threadIdx.x; it < w * kGroups; it += blockDim.x) {
+            const int t = it / kGroups, g = it % kGroups;
+            const __nv_bfloat16 *src;
+            if (src_slot >= 0) {
+                src = reinterpret_cast<const __nv_bfloat16 *>(D.fp_pool + (int64_t)src_slot * D.fp_slot_bytes) +
+                      ((int64_t)(h * 2 + kv) * w + t) * kHeadDim + g * kGroup;
+            } else {
+                src = (kv ? v_ext : k_ext) + (((int64_t)b * ext_len + (int64_t)wi * w + t) * D.Hkv + h) * kHeadDim +
+                      g * kGroup;
+            }
+            float x[kGroup];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 u = reinterpret_cast<const uint4 *>(src)[c];
+                const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __bfloat1622float2(p2[j]);
+                    x[c * 8 + 2 * j] = f.x;
+                    x[c * 8 + 2 * j + 1] = f.y;
+                }
+            }
+            bool finite = true;
+            float mn = x[0], mx = x[0];
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j) {
+                finite &= isfinite(x[j]);
+                mn = fminf(mn, x[j]);
+                mx = fmaxf(mx, x[j]);
+            }
+            const __half mn16 = __float2half_rn(mn);
+            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+            const float mq = __half2float(mn16), sq = __half2float(s16);
+            const bool bad = !finite || isinf(mq) || isinf(sq);
+            if (bad) set_status(C, QEVICT_ERR_DEVICE, layer, b, wi);
+            const bool zero = bad || sq == 0.f;
+            uint8_t *cs = s_codes + t * kHeadDim + g * kGroup;
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j) {
+                float c = zero ? 0.f : rintf(__fdiv_rn(__fsub_rn(x[j], mq), zero ? 1.f : sq));
+                c = fminf(fmaxf(c, 0.f), 3.f);
+                cs[j] = (uint8_t)c;
+            }
+            meta[t * kGroups + g] = bad ? __halves2half2(__float2half_rn(0.f), __float2half_rn(0.f))
+                                        : __halves2half2(s16, mn16);
+        }
+        __syncthreads();
+        uint32_t *words = reinterpret_cast<uint32_t *>(part);
+        if (kv == 0) {
+            // K: [token][d/4] bytes, channel j in byte j/4 at bits 2*(j%4); 16 channels per word
+            for (int i = threadIdx.x; i < w * (kHeadDim / 16); i += blockDim.x) {
+                const int t = i / (kHeadDim / 16), q = i % (kHeadDim / 16);
+                const uint8_t *cs = s_codes + t * kHeadDim + q * 16;
+                uint32_t word = 0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) word |= (uint32_t)cs[j] << (2 * j);
+                words[i] = word;
+            }
+        } else {
+            // V: [token/16][d] words, token t of the tile at bits 2*(t%16)
+            for (int i = threadIdx.x; i < (w / kVTile) * kHeadDim; i += blockDim.x) {
+                const int tile = i / kHeadDim, j = i % kHeadDim;
+                uint32_t word = 0;
+#pragma unroll
+                for (int t = 0; t < kVTile; ++t) word |= (uint32_t)s_codes[(tile * kVTile + t) * kHeadDim + j] << (2 * t);
+                words[i] = word;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- promote
+// bf16_rne(fmaf(code, scale, min)) from a ledger part into a full-precision slot.
+__global__ void __launch_bounds__(128) promote_kernel(LayerDev D) {
+    const int b = blockIdx.z;
+    const int h = blockIdx.y >> 1, kv = blockIdx.y & 1;
+    const int w = D.w;
+    const int n = D.ctr[b * kCtrN + CTR_WP];
+    for (int e = blockIdx.x; e < n; e += gridDim.x) {
+        const int4 job = D.work_p[(int64_t)b * D.Wmax + e];
+        const uint8_t *part = D.lg_pool + (int64_t)job.y * D.lg_slot_bytes + (int64_t)(h * 2 + kv) * lg_part_bytes(w);
+        const uint32_t *words = reinterpret_cast<const uint32_t *>(part);
+        const __half2 *meta = reinterpret_cast<const __half2 *>(part + lg_codes_bytes(w));
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)job.z * D.fp_slot_bytes) +
+                             (int64_t)(h * 2 + kv) * w * kHeadDim;
+        for (int it = threadIdx.x; it < w * kGroups; it += blockDim.x) {
+            const int t = it / kGroups, g = it % kGroups;
+            const __half2 m2 = meta[t * kGroups + g];
+            const float s = __low2float(m2), mn = __high2float(m2);
+            __align__(16) __nv_bfloat16 outv[kGroup];
+#pragma unroll
+            for (int j = 0; j < kGroup; ++j) {
+                const int ch = g * kGroup + j;
+                uint32_t c;
+                if (kv == 0) c = (words[t * (kHeadDim / 16) + ch / 16] >> (2 * (ch % 16))) & 3u;
+                else c = (words[(t / kVTile) * kHeadDim + ch] >> (2 * (t % kVTile))) & 3u;
+                outv[j] = __float2bfloat16_rn(fmaf((float)c, s, mn));
+            }
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + (int64_t)t * kHeadDim + g * kGroup);
+            const uint4 *s4 = reinterpret_cast<const uint4 *>(outv);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) d4[c] = s4[c];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- prefill copy
+__global__ void __launch_bounds__(128) prefill_copy_kernel(LayerDev D, const __nv_bfloat16 *__restrict__ k_ext,
+                                                            const __nv_bfloat16 *__restrict__ v_ext,
+                                                            int64_t ext_len) {
+    const int b = blockIdx.z;
+    const int h = blockIdx.y >> 1, kv = blockIdx.y & 1;
+    const int w = D.w;
+    const int n = D.ctr[b * kCtrN + CTR_WC];
+    constexpr int kChunks = kHeadDim * 2 / 16;
+    for (int e = blockIdx.x; e < n; e += gridDim.x) {
+        const int4 job = D.work_c[(int64_t)b * D.Wmax + e];
+        const int wi = job.x;
+        const int ntok = (int)min((int64_t)w, ext_len - (int64_t)wi * w);
+        uint8_t *dst = D.fp_pool + (int64_t)job.y * D.fp_slot_bytes + (int64_t)(h * 2 + kv) * w * kHeadDim * 2;
+        const __nv_bfloat16 *srcb = kv ? v_ext : k_ext;
+        for (int i = threadIdx.x; i < ntok * kChunks; i += blockDim.x) {
+            const int t = i / kChunks, c = i % kChunks;
+            const __nv_bfloat16 *src = srcb + (((int64_t)b * ext_len + (int64_t)wi * w + t) * D.Hkv + h) * kHeadDim;
+            reinterpret_cast<uint4 *>(dst + (int64_t)t * kHeadDim * 2)[c] = reinterpret_cast<const uint4 *>(src)[c];
+        }
+    }
+}
+
+// Every sequence of the batch has the same length; report sequence 0's.
+__global__ void read_lengths_kernel(LayerDev D, int32_t *out) {
+    if (threadIdx.x == 0) out[0] = D.ctr[CTR_LEN];
+}
+
+__global__ void scores_kernel(LayerDev D, int n_win, float *out) {
+    const int64_t n = (int64_t)D.B * n_win;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int b = (int)(i / n_win), wi = (int)(i % n_win);
+        float s = 0.f;
+        for (int h = 0; h < D.Hkv; ++h) s += D.score_part[((int64_t)b * D.Hkv + h) * D.Wmax + wi];
+        out[i] = s;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_init_layer(const LayerDev &L, cudaStream_t s) {
+    init_layer_kernel<<<256, 256, 0, s>>>(L);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *k,
+                          const __nv_bfloat16 *v, int n_new, cudaStream_t s) {
+    append_kernel<<<L.B, 256, 0, s>>>(L, C, layer, k, v, n_new);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const LayerDev &L, const CacheDev &C, const PlanArgs &a, cudaStream_t s) {
+    plan_kernel<<<L.B, kPlanThreads, 0, s>>>(L, C, a);
+    return cudaGetLastError();
+}
+
+static dim3 work_grid(const LayerDev &L, int max_entries) {
+    int gx = max_entries < 1 ? 1 : max_entries;
+    if (gx > 64) gx = 64;
+    return dim3(gx, L.Hkv * 2, L.B);
+}
+
+cudaError_t launch_quantize(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *k_ext,
+                            const __nv_bfloat16 *v_ext, int64_t ext_len, int max_entries, cudaStream_t s) {
+    const int smem = L.w * kHeadDim;
+    quantize_kernel<<<work_grid(L, max_entries), 128, smem, s>>>(L, C, layer, k_ext, v_ext, ext_len);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_promote(const LayerDev &L, const CacheDev &C, int max_entries, cudaStream_t s) {
+    (void)C;
+    promote_kernel<<<work_grid(L, max_entries), 128, 0, s>>>(L);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_copy(const LayerDev &L, const __nv_bfloat16 *k_ext, const __nv_bfloat16 *v_ext,
+                                int64_t ext_len, int max_entries, cudaStream_t s) {
+    prefill_copy_kernel<<<work_grid(L, max_entries), 128, 0, s>>>(L, k_ext, v_ext, ext_len);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s) {
+    read_lengths_kernel<<<1, 32, 0, s>>>(L, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scores(const LayerDev &L, int n_win, float *out, cudaStream_t s) {
+    scores_kernel<<<64, 256, 0, s>>>(L, n_win, out);
+    return cudaGetLastError();
+}
+
+}  // namespace qevict
