@@ -1,0 +1,474 @@
+#!/usr/bin/env python
+"""Tiered decode attention benchmark (QEvict three-tier KV cache, decode path).
+
+Workload: the Llama-3.1-8B-shaped cache of 32 layers, 32 query / 8 KV heads,
+head_dim 128, batch 1, 32768-token context in 64-token windows, a 20 % byte
+budget (tiers from routing on seeded Zipf(1.1) scores), synthetic bf16 K/V
+N(0, 1) with 1 % Student-t(3) outlier channels. Inputs are seeded and resident
+in HBM before timing; the 32 layers hold about 860 MB of tiered cache, far
+more than the 129 MB L2, so no layer is served from L2 when it comes round.
+
+One step = one decode token through all 32 layers: per layer one fused call
+that appends the token's K/V and runs tiered decode attention with the
+per-window mass added to the cumulative scores; every 64th step ends with a
+routing event on every layer (rank, evict, demote with the write-once ledger,
+promote). Steps are replayed as CUDA graphs captured from the C ABI calls.
+
+Prints one JSON line. ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama8b_b1_32k_20pct"
+METRIC = "tiered decode attention µs/layer-step and effective HBM GB/s (% of GB300 peak)"
+ROUTE_EVERY = 64
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------- helpers
+
+def workload():
+    from tiered_kv_cache_decode_gb300 import synth
+    return dict(synth.WORKLOADS[WORKLOAD])
+
+
+def costs(wl):
+    d = 128
+    c_fp = wl["w"] * wl["Hkv"] * d * 4
+    c_q = wl["w"] * wl["Hkv"] * 2 * (d // 4 + 4 * (d // 32))
+    return c_fp, c_q
+
+
+def route_counts(wl, n_cand, L):
+    """(n_fp, n_q) a routing event yields at length L (same rule as the kernels)."""
+    c_fp, c_q = costs(wl)
+    Bt = math.floor(wl["beta"] * (L * wl["Hkv"] * 128 * 4))
+    n_fp = min(n_cand, max(1, math.floor((wl["rho"] * Bt) / c_fp)))
+    n_q = min(n_cand - n_fp, (Bt - n_fp * c_fp) // c_q)
+    return n_fp, n_q
+
+
+class TierTracker:
+    """Host-side bookkeeping of how many windows each tier holds (per layer;
+    every layer and sequence has the same counts), to count algorithmic bytes."""
+
+    def __init__(self, wl, L):
+        self.wl, self.L = wl, L
+        W = -(-L // wl["w"])
+        self.n_fp, self.n_q = route_counts(wl, W, L)
+
+    def append(self):
+        if self.L % self.wl["w"] == 0:
+            self.n_fp += 1
+        self.L += 1
+
+    def route(self):
+        self.n_fp, self.n_q = route_counts(self.wl, self.n_fp + self.n_q, self.L)
+
+    def decode_bytes(self):
+        """Algorithmic bytes of one decode launch (one layer, all sequences):
+        resident tiered cache (the open window at its token count), the query,
+        the fp32 output and the read + write of one cumulative score per window."""
+        wl = self.wl
+        c_fp, c_q = costs(wl)
+        W = -(-self.L // wl["w"])
+        ntok = self.L - (W - 1) * wl["w"]
+        resident = (self.n_fp - 1) * c_fp + ntok * wl["Hkv"] * 128 * 4 + self.n_q * c_q
+        aux = wl["Hq"] * 128 * 2 + wl["Hq"] * 128 * 4 + W * 8
+        return wl["B"] * (resident + aux)
+
+    def append_bytes(self):
+        return self.wl["B"] * self.wl["Hkv"] * 128 * 4 * 2     # read the token, write it to its slot
+
+
+def sample_clocks():
+    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    try:
+        return subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "200"],
+                                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+    except OSError:
+        return None
+
+
+def finish_clocks(proc, gpu_index):
+    if proc is None:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    proc.terminate()
+    try:
+        out, _ = proc.communicate(timeout=5)
+    except subprocess.TimeoutExpired:
+        proc.kill()
+        out, _ = proc.communicate()
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in out.splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9 or f[0] != str(gpu_index):
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx.append(float(f[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in p:
+                v = p[key]
+                if isinstance(v, dict):
+                    v = v.get("value") or v.get("gbs")
+                return float(v), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    src = os.path.join(ROOT, "tiered_kv_cache_decode_gb300", "csrc", "qevict_decode.cu")
+    summ = os.path.join(ROOT, "profiles", f"decode_{WORKLOAD}.md")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        fields = {}
+        for line in open(summ):
+            if ":" in line and line.strip().startswith(("kernel_sha", "dram_bytes_per_launch")):
+                k, v = line.split(":", 1)
+                fields[k.strip(" -*`")] = v.strip(" `\n")
+        if fields.get("kernel_sha") == sha:
+            return int(float(fields["dram_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------- CPU oracle leg
+
+def _oracle_worker(args):
+    """One layer of the workload on the CPU oracle: prefill, then timed decode
+    steps (append + attention + score accumulation) for about `budget_s` s."""
+    layer, budget_s, max_steps = args
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    import torch
+    torch.set_num_threads(1)
+    import oracle as O
+    from tiered_kv_cache_decode_gb300 import synth
+    wl = workload()
+    B, Hq, Hkv, w, L = wl["B"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"]
+    k, v = synth.kv_tokens(0, layer, B, 0, L, Hkv, 128, wl["outliers"])
+    c = O.OracleCache(B, Hq, Hkv, 128, w, beta=wl["beta"], rho=wl["rho"])
+    c.prefill(k.float().numpy(), v.float().numpy(), scores=synth.zipf_scores(0, layer, B, L // w).numpy())
+    del k, v
+    tr = TierTracker(wl, L)
+    done, nbytes, spent = 0, 0, 0.0
+    while done < max_steps and (spent < budget_s or done == 0):
+        kn, vn = synth.kv_tokens(0, layer, B, c.L, 1, Hkv, 128, wl["outliers"])
+        q = synth.queries(0, layer, done, B, Hq, 128).float().numpy()
+        kn, vn = kn.float().numpy(), vn.float().numpy()
+        t0 = time.perf_counter()
+        c.append(kn, vn)
+        c.decode(q, accumulate=True)
+        spent += time.perf_counter() - t0
+        tr.append()
+        nbytes += tr.decode_bytes() + tr.append_bytes()
+        done += 1
+    return nbytes, spent, done
+
+
+def oracle_throughput(n_workers, budget_s, max_steps):
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(n_workers) as pool:
+        res = pool.map(_oracle_worker, [(l, budget_s, max_steps) for l in range(n_workers)])
+    wall = time.perf_counter() - t0
+    nbytes = sum(r[0] for r in res)
+    spent = max(r[1] for r in res)
+    steps = sum(r[2] for r in res)
+    return nbytes / spent / 1e9, spent, steps, wall
+
+
+# --------------------------------------------------------------------------- native arm
+
+def run_native(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    from tiered_kv_cache_decode_gb300 import binding, synth
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = workload()
+    B, NL, Hq, Hkv, w, L0 = wl["B"], wl["layers"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"]
+    if args.layers:
+        NL = args.layers
+    d = 128
+    K, Wm = args.steps, args.warmup
+    total_steps = Wm + 2 * K + 8
+    maxc = L0 + total_steps + 64
+    seed = 0
+
+    # Start the CPU oracle pool first (spawned workers never touch the GPU).
+    cpu = None
+    pool_async = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import multiprocessing as mp
+        nw = max(1, min(8, (os.cpu_count() or 2) // 2))
+        ctx = mp.get_context("spawn")
+        cpu_pool = ctx.Pool(nw)
+        pool_async = (cpu_pool, nw, cpu_pool.map_async(_oracle_worker, [(l, args.cpu_seconds, 200) for l in range(nw)]),
+                      time.perf_counter())
+
+    cache = binding.TieredCache(B, NL, Hq, Hkv, w, maxc, budget_frac=wl["beta"], fp_share=wl["rho"])
+    # inside the step graph every decode follows the previous layer's decode kernel
+    cache.set_launch_overlap(True)
+    W0 = L0 // w
+    for layer in range(NL):
+        k, v = synth.kv_tokens(seed, layer, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
+        sc = synth.zipf_scores(seed, layer, B, W0, device=dev)
+        cache.prefill(layer, k, v, scores=sc)
+        del k, v
+    torch.cuda.synchronize()
+    assert cache.status() == 0, cache.last_error()
+
+    # per-step inputs, resident in HBM: [step][layer][q | k | v] bf16
+    nq, nkv = B * Hq * d, B * Hkv * d
+    per_layer = nq + 2 * nkv
+    pool = torch.empty(total_steps, NL, per_layer, dtype=torch.bfloat16, device=dev)
+    for layer in range(NL):
+        kn, vn = synth.kv_tokens(seed, layer, B, L0, total_steps, Hkv, d, wl["outliers"], device=dev)
+        for s in range(total_steps):
+            pool[s, layer, :nq] = synth.queries(seed, layer, s, B, Hq, d, device=dev).reshape(-1)
+            pool[s, layer, nq:nq + nkv] = kn[:, s].reshape(-1)
+            pool[s, layer, nq + nkv:] = vn[:, s].reshape(-1)
+    xin = torch.empty(NL, per_layer, dtype=torch.bfloat16, device=dev)
+    xout = torch.empty(NL, B, Hq, d, dtype=torch.float32, device=dev)
+    qv = [xin[l, :nq].view(B, Hq, d) for l in range(NL)]
+    kv_ = [xin[l, nq:nq + nkv].view(B, Hkv, d) for l in range(NL)]
+    vv = [xin[l, nq + nkv:].view(B, Hkv, d) for l in range(NL)]
+
+    stream = torch.cuda.Stream(device=dev)
+    g_step, g_route, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_step, stream=stream):
+            for l in range(NL):
+                cache.decode_step(l, qv[l], kv_[l], vv[l], out=xout[l], want_mass=False, accumulate=True,
+                                  stream=stream)
+        with torch.cuda.graph(g_route, stream=stream):
+            for l in range(NL):
+                cache.route(l, stream=stream)
+        with torch.cuda.graph(g_decode, stream=stream):
+            for l in range(NL):
+                cache.decode(l, qv[l], out=xout[l], want_mass=False, accumulate=True, stream=stream)
+    torch.cuda.synchronize()
+
+    tracker = TierTracker(wl, L0)
+    gstep = [0]
+
+    def one_step(s_idx, host_in=None, host_out=None):
+        if host_in is not None:
+            xin.copy_(host_in, non_blocking=True)
+        else:
+            xin.copy_(pool[s_idx], non_blocking=True)
+        g_step.replay()
+        tracker.append()
+        nbytes = NL * (tracker.decode_bytes() + tracker.append_bytes())
+        launches = NL
+        gstep[0] += 1
+        if gstep[0] % ROUTE_EVERY == 0:
+            g_route.replay()
+            tracker.route()
+            launches += 3 * NL
+        if host_out is not None:
+            host_out.copy_(xout, non_blocking=True)
+        return nbytes, launches
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for s in range(Wm):
+            one_step(s)
+        barrier()
+        clk = sample_clocks()
+        time.sleep(0.3)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        ev0.record(stream)
+        nbytes, launches = 0, 0
+        for s in range(K):
+            b_, l_ = one_step(Wm + s)
+            nbytes += b_
+            launches += l_
+        ev1.record(stream)
+        barrier()
+        clocks = finish_clocks(clk, local_rank)
+        ms = ev0.elapsed_time(ev1)
+
+        # the dominant kernel alone: decode over all 32 layers, no appends
+        dec_bytes = tracker.decode_bytes()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(K):
+            g_decode.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dec_ms = e0.elapsed_time(e1) / (K * NL)
+
+        # end to end: inputs from pinned host memory, outputs back to the host every step
+        if args.no_e2e:
+            host_pool = None
+        else:
+            host_pool = pool[Wm + K:Wm + 2 * K].cpu().pin_memory()
+        host_out = torch.empty(NL, B, Hq, d, dtype=torch.float32).pin_memory()
+        barrier()
+        t0 = time.perf_counter()
+        e2e_bytes = 0
+        for s in range(0 if args.no_e2e else K):
+            b_, _ = one_step(Wm + K + s, host_in=host_pool[s], host_out=host_out)
+            e2e_bytes += b_
+            stream.synchronize()
+        e2e_s = max(time.perf_counter() - t0, 1e-9)
+    torch.cuda.synchronize()
+    st = cache.status()
+    assert st == 0, f"device status {st}: {cache.last_error()}"
+    cache.refresh_lengths()
+
+    if world > 1:
+        t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_s = float(t[0]), float(t[1])
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    value = world * nbytes / (ms / 1e3) / 1e9
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": round(ms / K, 5),
+        "us_per_layer_step": round(ms / K / NL * 1e3, 4),
+        "pct_of_hbm_peak": round(100 * (value / world) / peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD if NL == wl["layers"] else f"{WORKLOAD} ({NL} of {wl['layers']} layers)",
+                   "batch": B, "layers": NL, "q_heads": Hq, "kv_heads": Hkv,
+                   "head_dim": d, "context": L0, "window": w, "budget_frac": wl["beta"], "fp_share": wl["rho"],
+                   "route_every": ROUTE_EVERY, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2 ({NL} layers x ~26.8 MB of tiered cache)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
+                     "kernel": "decode_kernel (tiered split-K decode + combine + score + append)",
+                     "peak_source": peak_kind, "us_per_launch": round(dec_ms * 1e3, 3),
+                     "bytes_per_launch": dec_bytes},
+        "e2e": None if args.no_e2e else {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(NL * per_layer * 2), "d2h_bytes_per_step": int(xout.numel() * 4),
+                "ms_per_step": round(e2e_s / K * 1e3, 4)},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if pool_async is not None:
+        cpu_pool, nw, res, t_start = pool_async
+        out = res.get()
+        cpu_pool.close()
+        nb = sum(r[0] for r in out)
+        spent = max(r[1] for r in out)
+        line["cpu_baseline"] = {"value": round(nb / spent / 1e9, 4), "unit": "GB/s", "cores": nw, "kind": "oracle",
+                                "sample": f"{nw} layers of the workload, one per single-threaded process, "
+                                          f"{sum(r[2] for r in out)} decode steps in total (append + fp64 attention "
+                                          f"+ score accumulation) after a 32K-token prefill"}
+    return line
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    nw = max(1, min(8, (os.cpu_count() or 2) // 2))
+    per_step = max(1, args.steps + args.warmup)
+    gbs, spent, steps, wall = oracle_throughput(nw, budget_s=1e9, max_steps=per_step)
+    wl = workload()
+    sample = (f"{nw} of the {wl['layers']} layers, one per single-threaded process; {per_step} decode steps "
+              f"each (append + fp64 attention + score accumulation) after a 32K-token prefill")
+    return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(spent / max(1, per_step) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sampled_layers": nw},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nw, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run fewer layers of the same per-layer workload (profiling captures)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        line = run_native(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -116,8 +116,10 @@ typedef struct qevict_cache qevict_cache;
  *        followed by meta (window * head_dim / 32 half2 {scale, min}):
  *        K codes: [token][head_dim / 4] bytes, channel j in byte j / 4,
  *                 bits 2 * (j % 4);
- *        V codes: [token / 16][head_dim] uint32 words, token t of a
- *                 16-token tile in bits 2 * (t % 16);
+ *        V codes: [token / 16][128] uint32 words per 16-token tile; word
+ *                 i = (g * 8 + mt) * 2 + h (g, mt in 0..7, h in 0..1) holds
+ *                 channel 16 * mt + g + 8 * h, token t of the tile in bits
+ *                 2 * (t % 16);
  *        meta:    [token][head_dim / 32] half2, .x = scale, .y = min.
  *  length                          current context length (host copy). */
 typedef struct qevict_view {
@@ -142,6 +144,18 @@ typedef struct qevict_stats {
     uint64_t ledger_reuses;   /* demotions that reused the ledger entry */
     int64_t device_bytes;     /* bytes the cache allocated */
 } qevict_stats;
+
+/* Host-only: the per-sequence full-precision and INT2-ledger slot counts a
+ * cache created with *config gets (fp_capacity / ledger_capacity of the view)
+ * and the bytes of one layer's two slot pools for the whole batch (may be
+ * NULL). No routing event at any length up to max_context needs more slots:
+ * full precision at most max(1, floor(rho B / c_fp)) windows (plus
+ * fp_slack + 1 for windows opened between routing events and the one kept in
+ * reserve for the next window), the ledger at most
+ * floor(B (1 - rho) / c_q + rho B / c_fp + c_fp / c_q - 1) + 1, with B the
+ * budget at max_context. INVALID_ARG for an unsupported config. */
+qevict_status qevict_pool_capacity(const qevict_config *config, int32_t *fp_capacity,
+                                   int32_t *ledger_capacity, int64_t *pool_bytes_per_layer);
 
 /* Create a cache: allocates every layer's slot pools, tables and decode
  * scratch through `allocator` (NULL = cudaMalloc) on the current device and
@@ -196,6 +210,18 @@ qevict_status qevict_append_kv(qevict_cache *cache, int32_t layer, const void *k
 qevict_status qevict_decode_attention(qevict_cache *cache, int32_t layer, const void *q,
                                       float *out, float *mass, int32_t accumulate_scores,
                                       void *stream);
+
+/* One decode step with this step's token fused in: equivalent to
+ * qevict_append_kv(layer, k_new, v_new, n_new = 1) followed by
+ * qevict_decode_attention(layer, q, out, mass, accumulate_scores), in one
+ * launch. k_new, v_new: bf16 [batch][Hkv][head_dim]. mass rows are
+ * ceil((length + 1) / window) long. The attention reads the cache as it was
+ * plus the new token; the token is written into its window (opening one in
+ * the full-precision tier when needed) after the attention, by the last CTA
+ * of each sequence. INVALID_ARG if the context would pass max_context. */
+qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void *q, const void *k_new,
+                                 const void *v_new, float *out, float *mass, int32_t accumulate_scores,
+                                 void *stream);
 
 /* A routing event for a layer (QEvict "Kernmechanismen": rank windows by
  * cumulative score and move them between tiers under the byte budget).
@@ -258,6 +284,17 @@ qevict_status qevict_clear_status(qevict_cache *cache, void *stream);
 
 /* Synchronise `stream` and copy the transition counters to *stats (host). */
 qevict_status qevict_get_stats(qevict_cache *cache, qevict_stats *stats, void *stream);
+
+/* Let a decode launch overlap the end of the kernel before it in the stream
+ * (programmatic dependent launch): the decode kernel starts loading this
+ * layer's cache while the previous kernel finishes, and waits for that kernel
+ * before it reads q, k_new and v_new. The library enables it only for a
+ * decode whose previous call on this cache was on another layer and on the
+ * same stream. Enable it only if the operation just before each such decode
+ * in the stream is a kernel (for example a graph of consecutive decode steps,
+ * or the projection that produces q): a copy or memset directly before the
+ * launch is not waited for. Off by default. */
+qevict_status qevict_set_launch_overlap(qevict_cache *cache, int32_t enable);
 
 /* The kernels keep each layer's context length in device memory and read it
  * when they run, so a CUDA graph captured from these calls can be replayed:

@@ -91,3 +91,28 @@ def test_failing_allocator_reports_oom_and_frees_everything(lib, fail_at):
     assert rc == 2 and not h.value
     assert calls[0] == fail_at + 1
     assert not live
+
+
+@pytest.mark.parametrize("Hkv,w,maxc,beta,rho", [(8, 64, 32768 + 300, 0.20, 0.5), (8, 64, 32768 + 300, 0.05, 0.5),
+                                                 (4, 64, 16640, 0.10, 0.5), (4, 32, 1070, 0.30, 0.5),
+                                                 (8, 32, 8192 + 64, 0.05, 0.5), (8, 128, 8192 + 64, 0.05, 0.3),
+                                                 (2, 16, 3000, 0.6, 0.8), (8, 64, 131072, 0.2, 0.5)])
+def test_pool_capacity_covers_every_routing_event(lib, Hkv, w, maxc, beta, rho):
+    """Brute force over every context length: the routed tier counts of the oracle
+    never exceed the pools the library sizes for the config."""
+    import oracle as O
+    cfg = _cfg(num_kv_heads=Hkv, num_q_heads=Hkv * 4, window=w, max_context=maxc, budget_frac=beta,
+               fp_share=rho)
+    cf, cq, nbytes = binding.pool_capacity(cfg)
+    c_fp, c_q = O.window_costs(w, Hkv, 128)
+    worst_fp = worst_led = 0
+    for L in range(1, maxc + 1):
+        if O.budget_bytes(L, Hkv, 128, beta) < c_fp:
+            continue
+        W = -(-L // w)
+        n_fp, n_q = O.route_counts(W, L, w, Hkv, 128, beta, rho)
+        worst_fp = max(worst_fp, n_fp)
+        worst_led = max(worst_led, n_fp + n_q)
+    assert worst_fp + 1 <= cf          # one more for the slot kept for the next window
+    assert worst_led <= cq
+    assert nbytes == cf * c_fp + cq * c_q

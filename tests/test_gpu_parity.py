@@ -141,7 +141,7 @@ def test_full_size_llama_b1_32k_20pct_one_layer():
 def test_device_errors_set_status_without_faulting():
     B, Hq, Hkv, w, L = 1, 8, 2, 32, 100
     cache, (ref,) = make_pair(B, Hq, Hkv, w, L, tiers=[torch.zeros(B, 4, dtype=torch.uint8)],
-                              fp_capacity=5, ledger_capacity=1)
+                              fp_capacity=6, ledger_capacity=1)
     # demoting the partially filled last window is illegal
     cache.demote(0, torch.tensor([[0, 3]], dtype=torch.int32).cuda())
     assert binding.STATUS[cache.status()] == "STATE"
@@ -169,38 +169,126 @@ def test_device_errors_set_status_without_faulting():
     assert ei.value.name == "BUDGET"
 
 
+def test_decode_step_fused_append_matches_oracle_over_layers():
+    """decode_step (append one token + attention, one launch) on 3 interleaved layers,
+    so consecutive launches touch different layers (the programmatic-launch path);
+    windows open along the way and a routing event runs in between."""
+    B, Hq, Hkv, w, L0, beta, NL = 2, 28, 4, 32, 1000, 0.3, 3
+    W0 = -(-L0 // w)
+    steps = 70
+    scores = [synth.zipf_scores(11, l, B, W0) for l in range(NL)]
+    cache, refs = make_pair(B, Hq, Hkv, w, L0, layers=NL, beta=beta, scores=scores, max_context=L0 + steps,
+                            seed=11)
+    for step in range(steps):
+        for l in range(NL):
+            kn, vn = synth.kv_tokens(11, l, B, L0 + step, 1, Hkv, 128)
+            q = synth.queries(11, l, step, B, Hq, 128)
+            out, mass = cache.decode_step(l, q.cuda(), kn[:, 0].contiguous().cuda(), vn[:, 0].contiguous().cuda())
+            refs[l].append(kn.float().numpy(), vn.float().numpy())
+            ro, rm = refs[l].decode(q.float().numpy())
+            torch.cuda.synchronize()
+            close(out.cpu().numpy(), ro, f"out layer {l} step {step}")
+            close(mass.cpu().numpy(), rm, f"mass layer {l} step {step}")
+        if step == 40:
+            for l in range(NL):
+                cache.route(l)
+                refs[l].route(scores_override=np.asarray(cache.scores(l).cpu().numpy(), np.float64))
+            assert cache.status() == 0, cache.last_error()
+            for l in range(NL):
+                check_state(cache, l, refs[l])
+    assert cache.status() == 0, cache.last_error()
+    for l in range(NL):
+        close(cache.scores(l).cpu().numpy(), np.stack(refs[l].S), f"scores layer {l}")
+        check_state(cache, l, refs[l])
+    check_stats(cache, refs)
+
+
+def test_decode_step_on_empty_layer_and_window_edges():
+    B, Hq, Hkv, w = 1, 8, 2, 16
+    cache = binding.TieredCache(B, 1, Hq, Hkv, w, 64, budget_frac=1.0, fp_capacity=8, ledger_capacity=2)
+    ref = O.OracleCache(B, Hq, Hkv, 128, w)
+    for step in range(40):     # from an empty layer across two window boundaries
+        kn, vn = synth.kv_tokens(13, 0, B, step, 1, Hkv, 128)
+        q = synth.queries(13, 0, step, B, Hq, 128)
+        out, mass = cache.decode_step(0, q.cuda(), kn[:, 0].contiguous().cuda(), vn[:, 0].contiguous().cuda())
+        ref.append(kn.float().numpy(), vn.float().numpy())
+        ro, rm = ref.decode(q.float().numpy())
+        torch.cuda.synchronize()
+        close(out.cpu().numpy(), ro, f"out step {step}")
+        close(mass.cpu().numpy(), rm, f"mass step {step}")
+    assert cache.status() == 0, cache.last_error()
+    check_state(cache, 0, ref)
+
+
 def test_graph_replay_advances_device_length():
-    """A CUDA graph of (append, decode) replayed N times equals N eager steps."""
-    B, Hq, Hkv, w, L0 = 1, 8, 2, 32, 200
+    """A CUDA graph of fused decode steps over two layers, replayed N times, equals N eager steps."""
+    B, Hq, Hkv, w, L0, NL = 1, 8, 2, 32, 200, 2
     W = -(-L0 // w)
     steps = 40
-    cache, (ref,) = make_pair(B, Hq, Hkv, w, L0, tiers=[torch.zeros(B, W, dtype=torch.uint8)],
-                              max_context=L0 + steps + 1, fp_capacity=16, ledger_capacity=4)
-    kbuf = torch.empty(B, 1, Hkv, 128, dtype=torch.bfloat16, device="cuda")
-    vbuf = torch.empty_like(kbuf)
-    qbuf = torch.empty(B, Hq, 128, dtype=torch.bfloat16, device="cuda")
-    out = torch.empty(B, Hq, 128, dtype=torch.float32, device="cuda")
+    cache, refs = make_pair(B, Hq, Hkv, w, L0, layers=NL, tiers=[torch.zeros(B, W, dtype=torch.uint8)] * NL,
+                            max_context=L0 + steps + 1, fp_capacity=16, ledger_capacity=4)
+    kbuf = [torch.empty(B, Hkv, 128, dtype=torch.bfloat16, device="cuda") for _ in range(NL)]
+    vbuf = [torch.empty_like(kbuf[0]) for _ in range(NL)]
+    qbuf = [torch.empty(B, Hq, 128, dtype=torch.bfloat16, device="cuda") for _ in range(NL)]
+    out = [torch.empty(B, Hq, 128, dtype=torch.float32, device="cuda") for _ in range(NL)]
     s = torch.cuda.Stream()
     g = torch.cuda.CUDAGraph()
+    cache.set_launch_overlap(True)   # layer 1's decode follows layer 0's decode kernel in the graph
+    torch.cuda.synchronize()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            cache.append(0, kbuf, vbuf, stream=s)
-            cache.decode(0, qbuf, out=out, want_mass=False, stream=s)
+            for l in range(NL):
+                cache.decode_step(l, qbuf[l], kbuf[l], vbuf[l], out=out[l], want_mass=False, stream=s)
     torch.cuda.synchronize()
     for step in range(steps):
-        kn, vn = synth.kv_tokens(9, 0, B, L0 + step, 1, Hkv, 128)
-        q = synth.queries(9, 0, step, B, Hq, 128)
-        kbuf.copy_(kn)
-        vbuf.copy_(vn)
-        qbuf.copy_(q)
+        for l in range(NL):
+            kn, vn = synth.kv_tokens(9, l, B, L0 + step, 1, Hkv, 128)
+            q = synth.queries(9, l, step, B, Hq, 128)
+            kbuf[l].copy_(kn[:, 0])
+            vbuf[l].copy_(vn[:, 0])
+            qbuf[l].copy_(q)
         g.replay()
-        ref.append(kn.float().numpy(), vn.float().numpy())
-        ro, _ = ref.decode(q.float().numpy())
         torch.cuda.synchronize()
-        close(out.cpu().numpy(), ro, f"graph step {step}")
+        for l in range(NL):
+            kn, vn = synth.kv_tokens(9, l, B, L0 + step, 1, Hkv, 128)
+            q = synth.queries(9, l, step, B, Hq, 128)
+            refs[l].append(kn.float().numpy(), vn.float().numpy())
+            ro, _ = refs[l].decode(q.float().numpy())
+            close(out[l].cpu().numpy(), ro, f"graph step {step} layer {l}")
     cache.refresh_lengths()
     assert cache.length(0) == L0 + steps
     assert cache.status() == 0
-    gs = cache.scores(0).cpu().numpy()
-    close(gs, np.stack(ref.S), "scores after graph replays")
-    check_state(cache, 0, ref)
+    for l in range(NL):
+        close(cache.scores(l).cpu().numpy(), np.stack(refs[l].S), "scores after graph replays")
+        check_state(cache, l, refs[l])
+
+
+@pytest.mark.parametrize("L", [1000, 1001, 1015, 1017])
+def test_stale_rows_of_open_window_never_reach_the_output(L):
+    """The slot of a partially filled window keeps whatever its rows held before.
+    Poison the whole full-precision pool with NaN first: attention must still
+    equal the oracle's over the tokens that exist."""
+    B, Hq, Hkv, w = 2, 16, 4, 16
+    W = -(-L // w)
+    cache = binding.TieredCache(B, 1, Hq, Hkv, w, L + 40, fp_capacity=W + 8, ledger_capacity=W)
+    v = cache.view(0)
+    pool = binding.device_tensor(v.fp_pool, (B * v.fp_capacity * v.fp_slot_bytes // 2,), "<i2")
+    pool.fill_(-1)                                         # 0xFFFF: a bf16 NaN in every row
+    torch.cuda.synchronize()
+    k, vv = synth.kv_tokens(17, 0, B, 0, L, Hkv, 128)
+    tiers = torch.zeros(B, W, dtype=torch.uint8)
+    tiers[:, : W // 3] = 1
+    cache.prefill(0, k.cuda(), vv.cuda(), tiers=tiers.cuda())
+    ref = O.OracleCache(B, Hq, Hkv, 128, w)
+    ref.prefill(k.float().numpy(), vv.float().numpy(), tiers=tiers.numpy())
+    check_decode(cache, 0, ref, synth.queries(17, 0, 0, B, Hq, 128))
+    for step in range(20):
+        kn, vn = synth.kv_tokens(17, 0, B, L + step, 1, Hkv, 128)
+        q = synth.queries(17, 0, step + 1, B, Hq, 128)
+        out, mass = cache.decode_step(0, q.cuda(), kn[:, 0].contiguous().cuda(), vn[:, 0].contiguous().cuda())
+        ref.append(kn.float().numpy(), vn.float().numpy())
+        ro, rm = ref.decode(q.float().numpy())
+        torch.cuda.synchronize()
+        close(out.cpu().numpy(), ro, f"out step {step}")
+        close(mass.cpu().numpy(), rm, f"mass step {step}")
+    assert cache.status() == 0

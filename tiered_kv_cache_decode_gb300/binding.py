@@ -23,10 +23,11 @@ STATUS = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_MEMORY", 3: "BUDGET", 4: "STATE"
           6: "TIMEOUT", 7: "DEVICE", 8: "CAPACITY"}
 
 # every function the header declares
-EXPORTS = ["qevict_cache_create", "qevict_cache_destroy", "qevict_prefill", "qevict_append_kv",
-           "qevict_decode_attention", "qevict_route", "qevict_demote_quantize",
+EXPORTS = ["qevict_pool_capacity", "qevict_cache_create", "qevict_cache_destroy", "qevict_prefill", "qevict_append_kv",
+           "qevict_decode_attention", "qevict_decode_step", "qevict_route", "qevict_demote_quantize",
            "qevict_promote_dequantize", "qevict_set_tiers", "qevict_get_scores", "qevict_get_view",
-           "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_refresh_lengths",
+           "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_set_launch_overlap",
+           "qevict_refresh_lengths",
            "qevict_length",
            "qevict_last_error"]
 
@@ -87,11 +88,14 @@ def load() -> ctypes.CDLL:
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     sig = {
+        "qevict_pool_capacity": [ctypes.POINTER(Config), ctypes.POINTER(I32), ctypes.POINTER(I32),
+                                 ctypes.POINTER(I64)],
         "qevict_cache_create": [ctypes.POINTER(Config), ctypes.POINTER(Allocator), P, ctypes.POINTER(P)],
         "qevict_cache_destroy": [P],
         "qevict_prefill": [P, I32, P, P, I32, P, P, P],
         "qevict_append_kv": [P, I32, P, P, I32, P],
         "qevict_decode_attention": [P, I32, P, P, P, I32, P],
+        "qevict_decode_step": [P, I32, P, P, P, P, P, I32, P],
         "qevict_route": [P, I32, P, P, P],
         "qevict_demote_quantize": [P, I32, P, I32, P],
         "qevict_promote_dequantize": [P, I32, P, I32, P],
@@ -101,6 +105,7 @@ def load() -> ctypes.CDLL:
         "qevict_get_status": [P, P],
         "qevict_clear_status": [P, P],
         "qevict_get_stats": [P, ctypes.POINTER(Stats), P],
+        "qevict_set_launch_overlap": [P, I32],
         "qevict_refresh_lengths": [P, P],
         "qevict_length": [P, I32],
         "qevict_last_error": [],
@@ -113,6 +118,16 @@ def load() -> ctypes.CDLL:
     lib.qevict_last_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
+
+
+def pool_capacity(cfg: Config):
+    """(fp_capacity, ledger_capacity, pool bytes per layer) a cache with this config gets."""
+    lib = load()
+    a, b_, n = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+    rc = lib.qevict_pool_capacity(ctypes.byref(cfg), ctypes.byref(a), ctypes.byref(b_), ctypes.byref(n))
+    if rc != 0:
+        raise QevictError(rc, lib.qevict_last_error().decode())
+    return a.value, b_.value, n.value
 
 
 def _ptr(t):
@@ -184,6 +199,9 @@ class TieredCache:
         except Exception:
             pass
 
+    def set_launch_overlap(self, enable=True):
+        self._check(self.lib.qevict_set_launch_overlap(self.handle, 1 if enable else 0))
+
     def refresh_lengths(self, stream=None):
         self._check(self.lib.qevict_refresh_lengths(self.handle, _stream(stream)))
 
@@ -211,6 +229,18 @@ class TieredCache:
                                device=q.device)
         self._check(self.lib.qevict_decode_attention(self.handle, layer, _ptr(q), _ptr(out), _ptr(mass),
                                                      1 if accumulate else 0, _stream(stream)))
+        return out, mass
+
+    def decode_step(self, layer, q, k_new, v_new, out=None, mass=None, want_mass=True, accumulate=True,
+                    stream=None):
+        """Append one token ([B][Hkv][d] or [B][1][Hkv][d]) and decode, in one launch."""
+        if out is None:
+            out = torch.empty(self.B, self.Hq, HEAD_DIM, dtype=torch.float32, device=q.device)
+        if mass is None and want_mass:
+            W = -(-(self.length(layer) + 1) // self.w)
+            mass = torch.empty(self.B, self.Hq, W, dtype=torch.float32, device=q.device)
+        self._check(self.lib.qevict_decode_step(self.handle, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                                _ptr(mass), 1 if accumulate else 0, _stream(stream)))
         return out, mass
 
     def route(self, layer, scores_override=None, score_mult=None, stream=None):
@@ -287,9 +317,13 @@ def decode_ledger_slot(raw: torch.Tensor, Hkv: int, w: int):
             wv = words.view(Hkv, w, d // 16)
             c = (wv[..., None] >> shifts) & 3          # [Hkv][w][d/16][16]
             codes[:, 0] = c.reshape(Hkv, w, d).to(torch.uint8)
-        else:           # [token/16][d], token t of the tile at bits 2*(t%16)
+        else:           # [token/16][128 words], word i holds channel vword_dim(i)
             wv = words.view(Hkv, w // 16, d)
-            c = (wv[..., None] >> shifts) & 3          # [Hkv][tiles][d][16]
-            codes[:, 1] = c.permute(0, 1, 3, 2).reshape(Hkv, w, d).to(torch.uint8)
+            c = (wv[..., None] >> shifts) & 3          # [Hkv][tiles][word][16]
+            i = torch.arange(d)
+            ch = 16 * ((i >> 1) & 7) + (i >> 4) + 8 * (i & 1)
+            c2 = torch.empty_like(c)
+            c2[:, :, ch] = c
+            codes[:, 1] = c2.permute(0, 1, 3, 2).reshape(Hkv, w, d).to(torch.uint8)
     meta = raw[:, :, w * d // 4:].contiguous().view(torch.float16).view(Hkv, 2, w, d // 32, 2)
     return codes, meta[..., 0].clone(), meta[..., 1].clone()

@@ -32,9 +32,29 @@ qevict_status cuda_fail(cudaError_t e, const char *what) {
 
 struct LayerHost {
     LayerDev dev{};
+    CUtensorMap tmap{};     // 2-D tiled view of the full-precision pool: [rows][128] bf16, 64 x 16 boxes
     int64_t length = 0;
     void *base = nullptr;
 };
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
 
 }  // namespace
 
@@ -49,9 +69,17 @@ struct qevict_cache {
     int64_t c_fp = 0, c_q = 0;
     std::vector<LayerHost> layers;
     CacheDev cdev{};
+    DecodeScratch scratch{};
     void *cbase = nullptr;
     int64_t total_bytes = 0;
     std::vector<void *> blocks;
+    // the last operation enqueued: programmatic dependent launch is used for a
+    // decode only when that operation was on another layer and on the same stream
+    int prev_layer = -1;
+    void *prev_stream = nullptr;
+    void *scratch_base = nullptr;
+    size_t scratch_bytes = 0;
+    bool allow_pdl = false;    // qevict_set_launch_overlap
 };
 
 namespace {
@@ -112,6 +140,11 @@ qevict_status check_layer(const qevict_cache *c, int32_t layer) {
 
 int n_windows(const qevict_cache *c, int64_t L) { return (int)((L + c->cfg.window - 1) / c->cfg.window); }
 
+void note_op(qevict_cache *c, int layer, void *stream) {
+    c->prev_layer = layer;
+    c->prev_stream = stream;
+}
+
 // Plan + the data movement it queues, in order: quantise (reads full-precision
 // slots released by demotions), then promote / prefill copy (write slots).
 qevict_status run_plan(qevict_cache *c, LayerHost &lh, const PlanArgs &a, const __nv_bfloat16 *k_ext,
@@ -132,20 +165,32 @@ qevict_status run_plan(qevict_cache *c, LayerHost &lh, const PlanArgs &a, const 
         e = launch_promote(lh.dev, c->cdev, maxf, s);
         if (e != cudaSuccess) return cuda_fail(e, "promote kernel");
     }
+    note_op(c, a.layer, (void *)s);
     return QEVICT_OK;
 }
 
-}  // namespace
+// Pool sizes that no routing event up to max_context can exceed. The budget
+// grows with the length, so the full-precision count peaks at max_context;
+// n_fp + n_q does not (it drops when n_fp steps up), so the ledger uses the
+// bound n_fp + n_q <= B (1 - rho) / c_q + rho B / c_fp + c_fp / c_q - 1, which
+// follows from n_fp c_fp + n_q c_q <= B and n_fp >= rho B / c_fp - 1 and
+// increases with B.
+void pool_capacity(const qevict_config &cfg, int Wmax, int64_t c_fp, int64_t c_q, int *CF, int *CQ) {
+    const int64_t Bmax = budget_bytes(cfg, cfg.max_context);
+    int nfp = fp_budget_windows(Bmax, c_fp, cfg.fp_share);
+    if (nfp < 1) nfp = 1;
+    if (nfp > Wmax) nfp = Wmax;
+    const double rho = cfg.fp_share, Bd = (double)Bmax;
+    const double lq = Bd * (1.0 - rho) / (double)c_q + rho * Bd / (double)c_fp + (double)c_fp / (double)c_q - 1.0;
+    int64_t nl = (int64_t)floor(lq) + 1;
+    if (nl > Wmax) nl = Wmax;
+    if (nl < 1) nl = 1;
+    const int slack = cfg.fp_slack > 0 ? cfg.fp_slack : 4;
+    *CF = cfg.fp_capacity > 0 ? cfg.fp_capacity : (nfp + slack + 1 < Wmax ? nfp + slack + 1 : Wmax);
+    *CQ = cfg.ledger_capacity > 0 ? cfg.ledger_capacity : (int)nl;
+}
 
-extern "C" {
-
-const char *qevict_last_error(void) { return g_last_error.c_str(); }
-
-qevict_status qevict_cache_create(const qevict_config *config, const qevict_allocator *allocator, void *stream,
-                                  qevict_cache **out) {
-    if (!config || !out) return fail(QEVICT_ERR_INVALID_ARG, "config and out must not be NULL");
-    *out = nullptr;
-    const qevict_config &cfg = *config;
+qevict_status check_config(const qevict_config &cfg) {
     if (cfg.batch < 1 || cfg.num_layers < 1 || cfg.num_kv_heads < 1 || cfg.num_q_heads < 1)
         return fail(QEVICT_ERR_INVALID_ARG, "batch, layers and head counts must be >= 1");
     if (cfg.num_q_heads % cfg.num_kv_heads != 0 || cfg.num_q_heads / cfg.num_kv_heads > kMaxG)
@@ -163,6 +208,43 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         return fail(QEVICT_ERR_INVALID_ARG, "capacities must be >= 0");
     const int Wmax = (cfg.max_context + cfg.window - 1) / cfg.window;
     if (Wmax > 4096) return fail(QEVICT_ERR_INVALID_ARG, "at most 4096 windows per sequence (got %d)", Wmax);
+    return QEVICT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qevict_status qevict_pool_capacity(const qevict_config *config, int32_t *fp_capacity, int32_t *ledger_capacity,
+                                   int64_t *pool_bytes_per_layer) {
+    if (!config || !fp_capacity || !ledger_capacity) return fail(QEVICT_ERR_INVALID_ARG, "NULL argument");
+    qevict_status st = check_config(*config);
+    if (st) return st;
+    const qevict_config &cfg = *config;
+    const int Wmax = (cfg.max_context + cfg.window - 1) / cfg.window;
+    int64_t c_fp, c_q;
+    window_costs(cfg.window, cfg.num_kv_heads, &c_fp, &c_q);
+    int CF, CQ;
+    pool_capacity(cfg, Wmax, c_fp, c_q, &CF, &CQ);
+    *fp_capacity = CF;
+    *ledger_capacity = CQ;
+    if (pool_bytes_per_layer)
+        *pool_bytes_per_layer = (int64_t)cfg.batch * (CF * c_fp + CQ * c_q);
+    return QEVICT_OK;
+}
+
+const char *qevict_last_error(void) { return g_last_error.c_str(); }
+
+qevict_status qevict_cache_create(const qevict_config *config, const qevict_allocator *allocator, void *stream,
+                                  qevict_cache **out) {
+    if (!config || !out) return fail(QEVICT_ERR_INVALID_ARG, "config and out must not be NULL");
+    *out = nullptr;
+    const qevict_config &cfg = *config;
+    {
+        const qevict_status cs = check_config(cfg);
+        if (cs) return cs;
+    }
+    const int Wmax = (cfg.max_context + cfg.window - 1) / cfg.window;
     if (allocator && (!allocator->alloc || !allocator->free))
         return fail(QEVICT_ERR_INVALID_ARG, "allocator needs both alloc and free");
 
@@ -178,18 +260,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     c->G = cfg.num_q_heads / cfg.num_kv_heads;
     c->Wmax = Wmax;
     window_costs(cfg.window, cfg.num_kv_heads, &c->c_fp, &c->c_q);
-    {
-        const int64_t Bmax = budget_bytes(cfg, cfg.max_context);
-        int nfp = fp_budget_windows(Bmax, c->c_fp, cfg.fp_share);
-        if (nfp < 1) nfp = 1;
-        if (nfp > Wmax) nfp = Wmax;
-        int64_t nq = (Bmax - (int64_t)nfp * c->c_fp) / c->c_q;
-        if (nq < 0) nq = 0;
-        const int slack = cfg.fp_slack > 0 ? cfg.fp_slack : 4;
-        c->CF = cfg.fp_capacity > 0 ? cfg.fp_capacity : (nfp + slack < Wmax ? nfp + slack : Wmax);
-        c->CQ = cfg.ledger_capacity > 0 ? cfg.ledger_capacity : (int)(nfp + nq < Wmax ? nfp + nq : Wmax);
-        if (c->CQ < 1) c->CQ = 1;
-    }
+    pool_capacity(cfg, Wmax, c->c_fp, c->c_q, &c->CF, &c->CQ);
     const int B = cfg.batch, Hkv = cfg.num_kv_heads, Hq = cfg.num_q_heads, w = cfg.window;
     const int64_t fps = (int64_t)Hkv * 2 * w * kHeadDim * 2;
     const int64_t lgs = (int64_t)Hkv * 2 * lg_part_bytes(w);
@@ -206,6 +277,28 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     c->cdev.stats = reinterpret_cast<unsigned long long *>((uint8_t *)c->cbase + 64);
 
     // every allocation first, so that a failing allocator leaves nothing behind
+    {
+        Carver cv;
+        const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * (2 + kHeadDim) * 4);
+        const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
+        const size_t o_us = cv.take((size_t)B * Hq * Wmax * (w / 16) * 8);
+        const size_t o_ar = cv.take((size_t)B * Hkv * 4);
+        const size_t o_ab = cv.take((size_t)B * 4);
+        uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
+        if (!base) {
+            const size_t need = cv.off;
+            release_all(c);
+            delete c;
+            return fail(QEVICT_ERR_OUT_OF_MEMORY, "allocation of %zu B of decode scratch failed", need);
+        }
+        c->scratch.part = (float *)(base + o_part);
+        c->scratch.wstat = (float2 *)(base + o_ws);
+        c->scratch.ustat = (float2 *)(base + o_us);
+        c->scratch.arrive = (uint32_t *)(base + o_ar);
+        c->scratch.arrive_b = (uint32_t *)(base + o_ab);
+        c->scratch_bytes = cv.off;
+        c->scratch_base = base;
+    }
     c->layers.resize(cfg.num_layers);
     for (int l = 0; l < cfg.num_layers; ++l) {
         LayerDev &D = c->layers[l].dev;
@@ -240,9 +333,6 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         const size_t o_wq = cv.take((size_t)B * Wmax * 16);
         const size_t o_wp = cv.take((size_t)B * Wmax * 16);
         const size_t o_wc = cv.take((size_t)B * Wmax * 16);
-        const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * (2 + kHeadDim) * 4);
-        const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
-        const size_t o_arr = cv.take((size_t)B * Hkv * 4);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
         if (!base) {
             const size_t need = cv.off;
@@ -266,11 +356,26 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         D.work_q = (int4 *)(base + o_wq);
         D.work_p = (int4 *)(base + o_wp);
         D.work_c = (int4 *)(base + o_wc);
-        D.part = (float *)(base + o_part);
-        D.wstat = (float2 *)(base + o_ws);
-        D.arrive = (uint32_t *)(base + o_arr);
     }
-    err = cudaMemsetAsync(c->cbase, 0, 256, c->stream);
+    err = prepare_decode();
+    EncodeTiledFn enc = encode_tiled();
+    for (int l = 0; l < cfg.num_layers && err == cudaSuccess; ++l) {
+        if (!enc) {
+            err = cudaErrorNotSupported;
+            break;
+        }
+        const LayerDev &D = c->layers[l].dev;
+        const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)B * c->CF * Hkv * 2 * w};
+        const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+        const cuuint32_t box[2] = {64, 16};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = enc(&c->layers[l].tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D.fp_pool, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) err = cudaErrorInvalidValue;
+    }
+    if (err == cudaSuccess) err = cudaMemsetAsync(c->cbase, 0, 256, c->stream);
+    if (err == cudaSuccess) err = cudaMemsetAsync(c->scratch_base, 0, c->scratch_bytes, c->stream);
     for (int l = 0; l < cfg.num_layers && err == cudaSuccess; ++l) err = launch_init_layer(c->layers[l].dev, c->stream);
     if (err == cudaSuccess) err = cudaStreamSynchronize(c->stream);
     if (err != cudaSuccess) {
@@ -333,24 +438,46 @@ qevict_status qevict_append_kv(qevict_cache *c, int32_t layer, const void *k, co
                                   (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "append kernel");
     lh.length += n_new;
+    note_op(c, layer, stream);
+    return QEVICT_OK;
+}
+
+static qevict_status decode_common(qevict_cache *c, int32_t layer, const void *q, const void *k_new, const void *v_new,
+                                   float *out, float *mass, int32_t accumulate, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (!q || !out) return fail(QEVICT_ERR_INVALID_ARG, "q and out must not be NULL");
+    if (k_new) {
+        if (lh.length + 1 > c->cfg.max_context)
+            return fail(QEVICT_ERR_INVALID_ARG, "context %lld + 1 passes max_context %d", (long long)lh.length,
+                        c->cfg.max_context);
+    } else if (lh.length < 1) {
+        return fail(QEVICT_ERR_INVALID_ARG, "layer %d is empty", layer);
+    }
+    const int splits = decode_splits(c->cfg.batch * c->cfg.num_kv_heads, c->num_sms);
+    const bool pdl = c->allow_pdl && c->prev_layer >= 0 && c->prev_layer != layer && c->prev_stream == stream;
+    cudaError_t e = launch_decode(lh.dev, c->cdev, c->scratch, lh.tmap, layer, (const __nv_bfloat16 *)q,
+                                  (const __nv_bfloat16 *)k_new, (const __nv_bfloat16 *)v_new, out, mass,
+                                  accumulate, splits, pdl, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    if (k_new) lh.length += 1;
     return QEVICT_OK;
 }
 
 qevict_status qevict_decode_attention(qevict_cache *c, int32_t layer, const void *q, float *out, float *mass,
                                       int32_t accumulate_scores, void *stream) {
-    qevict_status st = check_layer(c, layer);
-    if (st) return st;
-    LayerHost &lh = c->layers[layer];
-    if (!q || !out) return fail(QEVICT_ERR_INVALID_ARG, "q and out must not be NULL");
-    if (lh.length < 1) return fail(QEVICT_ERR_INVALID_ARG, "layer %d is empty", layer);
-    const int bk = c->cfg.batch * c->cfg.num_kv_heads;
-    int splits = (2 * c->num_sms + bk - 1) / bk;
-    if (splits > kMaxSplits) splits = kMaxSplits;
-    if (splits < 1) splits = 1;
-    cudaError_t e = launch_decode(lh.dev, c->cdev, layer, (const __nv_bfloat16 *)q, out, mass, accumulate_scores,
-                                  splits, (cudaStream_t)stream);
-    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
-    return QEVICT_OK;
+    qevict_status st = decode_common(c, layer, q, nullptr, nullptr, out, mass, accumulate_scores, stream);
+    if (!st) note_op(c, layer, stream);
+    return st;
+}
+
+qevict_status qevict_decode_step(qevict_cache *c, int32_t layer, const void *q, const void *k_new, const void *v_new,
+                                 float *out, float *mass, int32_t accumulate_scores, void *stream) {
+    if (!k_new || !v_new) return fail(QEVICT_ERR_INVALID_ARG, "k_new and v_new must not be NULL");
+    qevict_status st = decode_common(c, layer, q, k_new, v_new, out, mass, accumulate_scores, stream);
+    if (!st) note_op(c, layer, stream);
+    return st;
 }
 
 qevict_status qevict_route(qevict_cache *c, int32_t layer, const float *scores_override, const float *score_mult,
@@ -417,6 +544,7 @@ qevict_status qevict_get_scores(qevict_cache *c, int32_t layer, float *scores, v
     if (nw == 0) return QEVICT_OK;
     cudaError_t e = launch_scores(lh.dev, nw, scores, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "scores kernel");
+    note_op(c, layer, stream);
     return QEVICT_OK;
 }
 
@@ -481,6 +609,12 @@ qevict_status qevict_get_stats(qevict_cache *c, qevict_stats *out, void *stream)
     out->ledger_writes = s[ST_LWRITE];
     out->ledger_reuses = s[ST_LREUSE];
     out->device_bytes = c->total_bytes;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_set_launch_overlap(qevict_cache *c, int32_t enable) {
+    if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    c->allow_pdl = enable != 0;
     return QEVICT_OK;
 }
 

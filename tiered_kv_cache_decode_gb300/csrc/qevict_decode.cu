@@ -1,363 +1,782 @@
 // Split-K single-token GQA decode attention over the three-tier cache, with
-// the per-window softmax mass and the cumulative-score update fused in.
+// the per-window softmax mass, the cumulative-score update and (optionally)
+// the append of this step's token fused in.
 //
 // Method: "Technische Samenvatting: QEvict" (gist.science 2608.05326),
 // "Methodologie: QEvict" (full-precision and INT2 windows stay visible to
 // attention, evicted windows do not) and "Kernmechanismen" (cumulative
 // scoring, GQA). "Technische Samenvatting: LogQuant" (gist.science
 // 2503.19950), Methodologie 3 and 4: evicted tokens leave the softmax
-// normalisation, and entries may be visited in any order, which is what lets
-// a split walk its full-precision windows first and its INT2 windows after.
+// normalisation, and cache entries may be visited in any order.
 //
-// Grid (splits, B * Hkv). A CTA owns one (sequence, KV head) and a byte-
-// balanced contiguous run of that sequence's window list (full-precision
-// windows, then INT2 windows). Each window's K+V for the KV head is one
-// contiguous block in HBM and arrives by one cp.async.bulk into a stage of
-// a shared-memory ring tracked by mbarriers. The CTA keeps, for each of its G
-// query heads, the running max, the running exp-sum and the output
-// accumulator, and records every window's own (max, exp-sum). The last CTA
-// of a (sequence, KV head) to finish merges the splits (log-sum-exp), writes
-// the output, turns the window records into masses and adds their mean over
-// the Hq heads into the KV head's partial cumulative score.
+// Layout of the work. Grid (splits, B * Hkv); a CTA owns one (sequence, KV
+// head) and a cost-balanced contiguous run of that sequence's window list
+// (full-precision windows first, then INT2 windows). Its windows are cut
+// into 16-token units that its four warps take round-robin. Every warp feeds
+// itself: lane 0 keeps a ring of in-flight units in shared memory (a
+// full-precision unit is four TMA tile loads of K/V, 128-byte swizzled; an
+// INT2 unit is four bulk copies of codes and fp16 scale/min) and issues the
+// next units as soon as it has consumed one.
+//
+// Per unit a warp computes the GQA query group's logits and P.V on the
+// tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation):
+//  - QK: S[head][token] = Q[head][:] . K[token][:]; the G query heads are the
+//    M rows (padded to 16), 8 tokens per N tile. INT2 codes 0..3 are exact in
+//    bf16 and built in registers (code | 0x4300 is 128 + code; minus 128),
+//    one accumulator per group of 32 channels, then
+//    logit = sum_g scale_g * acc_g + min_g * sum(q over group g): the exact
+//    reconstruction min + code * scale, never rounded.
+//  - PV: O^T[channel][head] += V^T[channel][token] . P^T[token][head]; P is
+//    split into bf16 hi + lo parts (two MMAs) so it keeps ~16 bits; for INT2
+//    the scale folds into P per group and the min term is a CUDA-core sum.
+//  The token order inside an INT2 unit is permuted (pairs t, t+8 share a
+//  32-bit code word) and the same permutation is used on both sides of each
+//  product, which leaves every sum unchanged.
+// The last CTA of a (sequence, KV head) merges the splits by log-sum-exp,
+// adds this step's token when one is given, writes the output, turns the
+// per-window (max, exp-sum) records into masses and adds their mean over the
+// Hq heads into the KV head's partial cumulative score; the last of the
+// sequence's KV heads then opens the new window / advances the length.
+//
+// With programmatic dependent launch the kernel starts loading cache units
+// before the previous kernel in the stream has finished and waits for it
+// only before it reads the query (griddepcontrol.wait); the host enables
+// this only when that previous kernel did not change this layer's cache.
 #include "qevict_internal.cuh"
 
 namespace qevict {
 
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kWarps = 4;                 // consumer warps per CTA
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;                // shared-memory stages per warp
+constexpr int kStage = 8192;              // bytes per stage
+constexpr int kRing = kStages * kStage;   // bytes per warp
+constexpr int kFPUnit = 8192;             // 16 tokens x (K, V) x 256 B: one per stage
+constexpr int kQUnit = 1536;              // 16 tokens: K codes 512, K meta 256, V codes 512, V meta 256
+constexpr int kQPerStage = kStage / kQUnit;   // INT2 units batched into one stage (5)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kWaitCycles = 4000000000ll;   // about two seconds at GB300 clocks
 
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
-
-// Bounded wait on a stage barrier: false after about two seconds.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// bounded wait: false after about two seconds
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait(bar, parity))
         if (clock64() - t0 > kWaitCycles) return false;
-    }
     return true;
 }
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                    uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+// Two 2-bit codes (bits 1:0 and 17:16 of x) as an exact bf16 pair.
+__device__ __forceinline__ uint32_t codes2(uint32_t x) {
+    uint32_t r = (x & 0x00030003u) | 0x43004300u;     // bf16 128 + code in each half
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r);
+    v = __hsub2(v, __floats2bfloat162_rn(128.f, 128.f));
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+// hi = bf16(x), lo = bf16(x - hi) for a pair
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+    __nv_bfloat162 hv;
+    hv.x = h0;
+    hv.y = h1;
+    hi = *reinterpret_cast<uint32_t *>(&hv);
+    lo = pack2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+}
+__device__ __forceinline__ float2 h2f(uint32_t u) {
+    const __half2 h = *reinterpret_cast<const __half2 *>(&u);
+    return __half22float2(h);
+}
+__device__ __forceinline__ uint32_t pick(const uint4 &v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
 
-// Smallest list entry whose first byte is at or after unit offset u, in the
-// concatenated list (n_fp full-precision windows of u_fp bytes, then n_q
-// INT2 windows of u_q bytes).
-__device__ __forceinline__ int entry_at(int64_t u, int n_fp, int n_q, int64_t u_fp, int64_t u_q) {
-    const int64_t fp_total = (int64_t)n_fp * u_fp;
-    if (u <= fp_total) return (int)((u + u_fp - 1) / u_fp);
-    const int64_t e = n_fp + (u - fp_total + u_q - 1) / u_q;
-    return (int)min(e, (int64_t)(n_fp + n_q));
+// (max, exp-sum relative to max) pairs
+__device__ __forceinline__ float2 stat_merge(float2 a, float2 b) {
+    if (a.y <= 0.f) return b;
+    if (b.y <= 0.f) return a;
+    const float m = fmaxf(a.x, b.x);
+    return make_float2(m, a.y * exp2f(a.x - m) + b.y * exp2f(b.x - m));
+}
+
+// A split's share of the window list: full-precision entries [f0, f1) and
+// INT2 entries [q0, q1) (indices within each tier's list). Every split gets a
+// proportional share of each tier, so memory-bound and ALU-bound work mix
+// evenly over the CTAs.
+struct Range {
+    int f0, f1, q0, q1;
+};
+
+__device__ __forceinline__ Range split_range(int split, int splits, int n_fp, int n_q) {
+    return Range{(int)((int64_t)n_fp * split / splits), (int)((int64_t)n_fp * (split + 1) / splits),
+                 (int)((int64_t)n_q * split / splits), (int)((int64_t)n_q * (split + 1) / splits)};
 }
 
 template <int G>
-__global__ void __launch_bounds__(kThreads) decode_kernel(LayerDev D, CacheDev C, int layer,
-                                                           const __nv_bfloat16 *__restrict__ q,
-                                                           float *__restrict__ out, float *__restrict__ mass,
-                                                           int accumulate, int splits, int nst,
-                                                           int stage_bytes) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int w = D.w;
-    uint8_t *stages = smem;
-    float *q_s = reinterpret_cast<float *>(smem + (size_t)nst * stage_bytes);   // [G][d]
-    float *p_s = q_s + G * kHeadDim;                                             // [G][w]
-    float *run_m = p_s + G * w;                                                  // [G]
-    float *run_l = run_m + kMaxG;
-    float *s_alpha = run_l + kMaxG;
-    float *s_M = s_alpha + kMaxG;
-    float *s_il = s_M + kMaxG;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(s_il + kMaxG);                // [nst]
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_kernel(const LayerDev D, const CacheDev C, const DecodeScratch S, const __grid_constant__ CUtensorMap tmap,
+                  int layer, const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *knew,
+                  const __nv_bfloat16 *vnew, float *__restrict__ out, float *__restrict__ mass, int accumulate,
+                  int splits) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 128-byte-swizzled TMA tiles need 1024-byte aligned destinations
+    uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t bars[kWarps][kStages];
+    __shared__ int st_first[kWarps][kStages], st_n[kWarps][kStages];   // warp-local first unit, unit count
     __shared__ int s_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int split = blockIdx.x;
-    const int bk = blockIdx.y;
-    const int b = bk / D.Hkv, kvh = bk % D.Hkv;
-    const int Hq = D.Hq;
+    const int g = lane >> 2, t = lane & 3;
+    const int split = blockIdx.x, bk = blockIdx.y;
+    const int Hkv = D.Hkv, Hq = D.Hq, w = D.w, mu = w / 16;
+    const int b = bk / Hkv, kvh = bk % Hkv;
     const int64_t wb = (int64_t)b * D.Wmax;
-    const int64_t length = D.ctr[b * kCtrN + CTR_LEN];
+    const int32_t *ctr = D.ctr + b * kCtrN;
+    const int64_t length = ctr[CTR_LEN];
+    if (knew != nullptr && length >= D.max_context) {   // replayed past the end of the tables
+        if (tid == 0 && split == 0) set_status(C, QEVICT_ERR_INVALID_ARG, layer, b, (int)length);
+        knew = nullptr;
+        vnew = nullptr;
+    }
     const int n_win = (int)((length + w - 1) / w);
+    const int n_fp = ctr[CTR_NFP], n_q = ctr[CTR_NQ];
+    const Range R = split_range(split, splits, n_fp, n_q);
+    const int nfw = R.f1 - R.f0;                       // full-precision windows of this split
+    const int nwin = nfw + (R.q1 - R.q0);              // windows of this split
+    const int nunits = nwin * mu;
+    const int lmu = mu == 1 ? 0 : mu == 2 ? 1 : mu == 4 ? 2 : mu == 8 ? 3 : 31 - __clz(mu);
+    const uint32_t ring_s = smem_u32(smem + warp * kRing);
 
-    // query, pre-scaled so that logits are in the log2 domain
-    const float qscale = kLog2e * rsqrtf((float)kHeadDim);
-    for (int i = tid; i < G * kHeadDim; i += kThreads) {
-        const int g = i / kHeadDim, j = i % kHeadDim;
-        q_s[i] = __bfloat162float(q[((int64_t)b * Hq + kvh * G + g) * kHeadDim + j]) * qscale;
-    }
-    if (tid < kMaxG) {
-        run_m[tid] = -INFINITY;
-        run_l[tid] = 0.f;
-    }
-
-    // this split's run of the window list
-    const int n_fp = D.ctr[b * kCtrN + CTR_NFP];
-    const int n_q = D.ctr[b * kCtrN + CTR_NQ];
-    const int64_t u_fp = (int64_t)w * kHeadDim * 4;          // K + V bf16 for one KV head
-    const int64_t u_q = 2 * lg_part_bytes(w);                // K + V codes + meta
-    const int64_t U = n_fp * u_fp + n_q * u_q;
-    const int e0 = entry_at(U * split / splits, n_fp, n_q, u_fp, u_q);
-    const int e1 = entry_at(U * (split + 1) / splits, n_fp, n_q, u_fp, u_q);
-
-    if (tid == 0) {
-        s_flag = 0;
-        for (int i = 0; i < nst; ++i) mbar_init(&bars[i], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
+    if (tid == 0) s_flag = 0;
+    if (lane == 0)
+        for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
 
-    auto issue = [&](int e, int st) {
-        const bool fp = e < n_fp;
-        const int2 ent = fp ? D.fp_list[b * D.CF + e] : D.q_list[b * D.CQ + (e - n_fp)];
-        const uint8_t *src;
-        uint32_t bytes;
-        if (fp) {
-            src = D.fp_pool + (int64_t)ent.y * D.fp_slot_bytes + (int64_t)kvh * u_fp;
-            bytes = (uint32_t)u_fp;
-        } else {
-            src = D.lg_pool + (int64_t)ent.y * D.lg_slot_bytes + (int64_t)kvh * u_q;
-            bytes = (uint32_t)u_q;
-        }
-        mbar_expect_tx(&bars[st], bytes);
-        bulk_g2s(stages + (size_t)st * stage_bytes, src, bytes, &bars[st]);
+    // ---- unit bookkeeping (all lanes run it; lane 0 issues the copies). This
+    // warp takes units warp, warp + 4, ... of the CTA's run; a unit is the j-th
+    // 16-token slice of a window. A stage holds one full-precision unit or up to
+    // five consecutive INT2 units of the warp.
+    // local window index i -> global list entry e (full-precision entries first, then INT2)
+    auto gentry = [&](int i) -> int { return i < nfw ? R.f0 + i : n_fp + R.q0 + (i - nfw); };
+    auto entry = [&](int e) -> int2 { return e < n_fp ? D.fp_list[b * D.CF + e] : D.q_list[b * D.CQ + (e - n_fp)]; };
+    auto unit_tokens = [&](int wi, int j) -> int {
+        const int ntok = (wi == n_win - 1) ? (int)(length - (int64_t)wi * w) : w;
+        return min(16, ntok - 16 * j);
     };
-    int issued_end = e0;   // thread 0: entries [e0, issued_end) have been issued
-    if (tid == 0) {
-        for (int i = 0; i < nst && e0 + i < e1; ++i) issue(e0 + i, i);
-        issued_end = min(e1, e0 + nst);
-    }
+    const int my_units = nunits > warp ? (nunits - warp + kWarps - 1) / kWarps : 0;
+    int next_unit = 0;               // next warp-local unit to put in a stage
+    int issued = 0, consumed = 0;    // stages issued / consumed so far
+    auto unit_e = [&](int k) { return gentry((warp + k * kWarps) >> lmu); };
+    auto unit_j = [&](int k) { return (warp + k * kWarps) & (mu - 1); };
+    auto try_issue = [&]() {
+        while (next_unit < my_units && issued - consumed < kStages) {
+            int e = unit_e(next_unit), j = unit_j(next_unit);
+            int2 ent = entry(e);
+            if (unit_tokens(ent.x, j) <= 0) {   // past the end of the open window
+                ++next_unit;
+                continue;
+            }
+            const int st = issued % kStages;
+            const uint32_t bar = smem_u32(&bars[warp][st]);
+            const uint32_t dst = ring_s + st * kStage;
+            if (e < n_fp) {
+                if (lane == 0) {
+                    st_first[warp][st] = next_unit;
+                    st_n[warp][st] = 1;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(bar, (uint32_t)kFPUnit);
+                    const int row = ((ent.y * Hkv + kvh) * 2) * w + 16 * j;
+                    tma_2d(dst, &tmap, 0, row, bar);
+                    tma_2d(dst + 2048, &tmap, 64, row, bar);
+                    tma_2d(dst + 4096, &tmap, 0, row + w, bar);
+                    tma_2d(dst + 6144, &tmap, 64, row + w, bar);
+                }
+                ++next_unit;
+            } else {
+                // INT2 windows come after every full-precision one and are always full
+                const int n = min(kQPerStage, my_units - next_unit);
+                if (lane == 0) {
+                    st_first[warp][st] = next_unit;
+                    st_n[warp][st] = n;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(bar, (uint32_t)(n * kQUnit));
+                    for (int i = 0; i < n; ++i) {
+                        const int2 en = entry(unit_e(next_unit + i));
+                        const int jj = unit_j(next_unit + i);
+                        const uint8_t *kp =
+                            D.lg_pool + (int64_t)en.y * D.lg_slot_bytes + (int64_t)(kvh * 2) * lg_part_bytes(w);
+                        const uint8_t *vp = kp + lg_part_bytes(w);
+                        const uint32_t d = dst + i * kQUnit;
+                        bulk_g2s(d, kp + 16 * jj * 32, 512, bar);
+                        bulk_g2s(d + 512, kp + lg_codes_bytes(w) + 16 * jj * 16, 256, bar);
+                        bulk_g2s(d + 768, vp + jj * 512, 512, bar);
+                        bulk_g2s(d + 1280, vp + lg_codes_bytes(w) + 16 * jj * 16, 256, bar);
+                    }
+                }
+                next_unit += n;
+            }
+            ++issued;
+        }
+    };
+    try_issue();   // cache data only: safe before the dependency wait
 
-    float acc[G];
+    // ---- wait for the previous kernel, then let the next one start
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // ---- query fragments (A operand: G heads as rows, rest zero)
+    const uint32_t *qw =
+        reinterpret_cast<const uint32_t *>(q + ((int64_t)b * Hq + kvh * G + (g < G ? g : 0)) * kHeadDim);
+    uint32_t Af0[8], Af2[8], Aq0[8], Aq2[8];
+    float qsum[kGroups] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = 0.f;
+    for (int ks = 0; ks < 8; ++ks) {
+        uint32_t lo = 0, hi = 0;   // channels (16ks+2t, +1) and (16ks+2t+8, +9)
+        if (g < G) {
+            lo = qw[(16 * ks + 2 * t) / 2];
+            hi = qw[(16 * ks + 2 * t + 8) / 2];
+        }
+        Af0[ks] = lo;
+        Af2[ks] = hi;
+        Aq0[ks] = (lo & 0xffffu) | (hi << 16);       // channels 2t, 2t+8
+        Aq2[ks] = (lo >> 16) | (hi & 0xffff0000u);   // channels 2t+1, 2t+9
+        const float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&lo));
+        const float2 c = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&hi));
+        qsum[ks >> 1] += (a.x + a.y) + (c.x + c.y);
+    }
+#pragma unroll
+    for (int i = 0; i < kGroups; ++i) {
+        qsum[i] += __shfl_xor_sync(0xffffffffu, qsum[i], 1);
+        qsum[i] += __shfl_xor_sync(0xffffffffu, qsum[i], 2);
+    }
+    const float qk_scale = kLog2e * rsqrtf((float)kHeadDim);
 
-    for (int e = e0; e < e1; ++e) {
-        const int it = e - e0;
-        const int st = it % nst;
-        const uint32_t parity = (uint32_t)((it / nst) & 1);
-        const bool ok = mbar_wait(&bars[st], parity);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                set_status(C, QEVICT_ERR_TIMEOUT, layer, b, e);
-                // let the copies still in flight land before the CTA moves on
-                for (int r = e; r < issued_end; ++r)
-                    (void)mbar_wait(&bars[(r - e0) % nst], (uint32_t)(((r - e0) / nst) & 1));
+    // ---- per-warp online softmax state (lane: head g for m/l, heads 2t, 2t+1 in O)
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float minacc[kGroups] = {0.f, 0.f, 0.f, 0.f};
+    float2 *ustat = S.ustat + ((int64_t)b * Hq + kvh * G) * ((int64_t)D.Wmax * mu);
+
+    // ldmatrix row addressing (same for K and V tiles): token and 8-channel half of this lane's row
+    const int lm_tok = ((lane >> 4) << 3) + (lane & 7);
+    const int lm_hi = (lane >> 3) & 1;
+
+    // online-softmax update with 4 logits of head g (masked ones -inf); turns x into P
+    auto softmax4 = [&](float (&x)[4], float2 &ust) {
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = exp2f(m_run - m_new);
+        const float beta = exp2f(mx - m_new);
+        float e[4], es = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            e[i] = exp2f(x[i] - mx);
+            es += e[i];
+        }
+        es += __shfl_xor_sync(0xffffffffu, es, 1);
+        es += __shfl_xor_sync(0xffffffffu, es, 2);
+        ust = make_float2(mx, es);
+        l_run = l_run * alpha + es * beta;
+        m_run = m_new;
+        const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * t);
+        const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
+        if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                o[i][0] *= a_lo;
+                o[i][1] *= a_hi;
+                o[i][2] *= a_lo;
+                o[i][3] *= a_hi;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) minacc[i] *= alpha;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) x[i] = (g < G) ? e[i] * beta : 0.f;
+    };
+
+    while (consumed < issued) {
+        const int st = consumed % kStages;
+        const bool ok = mbar_wait(smem_u32(&bars[warp][st]), (uint32_t)((consumed / kStages) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            if (lane == 0) {
+                set_status(C, QEVICT_ERR_TIMEOUT, layer, b, consumed);
+                for (int r = consumed + 1; r < issued; ++r)
+                    (void)mbar_wait(smem_u32(&bars[warp][r % kStages]), (uint32_t)((r / kStages) & 1));
             }
             break;
         }
-        const bool fp = e < n_fp;
-        const int2 ent = fp ? D.fp_list[b * D.CF + e] : D.q_list[b * D.CQ + (e - n_fp)];
-        const int wi = ent.x;
-        const int ntok = (wi == n_win - 1) ? (int)(length - (int64_t)wi * w) : w;
-        const uint8_t *sb = stages + (size_t)st * stage_bytes;
-
-        // ---- logits: warp per token, lane per 4 channels
-        for (int t = warp; t < w; t += kThreads / 32) {
-            float k4[4];
-            if (fp) {
-                const uint2 u = reinterpret_cast<const uint2 *>(sb + (size_t)t * kHeadDim * 2)[lane];
-                const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
-                const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
-                k4[0] = a.x; k4[1] = a.y; k4[2] = c.x; k4[3] = c.y;
-            } else {
-                const uint32_t byte = sb[(size_t)t * (kHeadDim / 4) + lane];
-                const __half2 m2 = reinterpret_cast<const __half2 *>(sb + lg_codes_bytes(w))[t * kGroups + lane / 8];
-                const float s = __low2float(m2), mn = __high2float(m2);
+        __syncwarp();
+        const int first = st_first[warp][st], nb = st_n[warp][st];
+        for (int ib = 0; ib < nb; ++ib) {
+        const int k = first + ib;
+        const int e = unit_e(k), j = unit_j(k);
+        const int wi = entry(e).x;
+        const int ntu = unit_tokens(wi, j);
+        const uint32_t base = ring_s + st * kStage + ib * kQUnit;
+        float2 ust;
+        if (e < n_fp) {
+            // ---------------- full-precision unit
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) k4[i] = fmaf((float)((byte >> (2 * i)) & 3u), s, mn);
+            for (int ks = 0; ks < 8; ++ks) {
+                const int chunk = 2 * (ks & 3) + lm_hi;
+                const uint32_t addr = base + (ks >> 2) * 2048 + lm_tok * 128 + ((chunk ^ (lm_tok & 7)) << 4);
+                uint32_t b00, b01, b10, b11;
+                ldsm_x4(addr, b00, b01, b10, b11);
+                mma(s0, Af0[ks], 0u, Af2[ks], 0u, b00, b01);
+                mma(s1, Af0[ks], 0u, Af2[ks], 0u, b10, b11);
             }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float4 qv = reinterpret_cast<const float4 *>(q_s + g * kHeadDim)[lane];
-                float dot = qv.x * k4[0] + qv.y * k4[1] + qv.z * k4[2] + qv.w * k4[3];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                if (lane == 0) p_s[g * w + t] = t < ntok ? dot : -INFINITY;
-            }
-        }
-        __syncthreads();
-
-        // ---- window statistics and probabilities (warp per head)
-        for (int g = warp; g < G; g += kThreads / 32) {
-            float mw = -INFINITY;
-            for (int t = lane; t < ntok; t += 32) mw = fmaxf(mw, p_s[g * w + t]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-            const float m_old = run_m[g];
-            const float m_new = fmaxf(m_old, mw);
-            const float beta = exp2f(mw - m_new);
-            float es = 0.f;
-            for (int t = lane; t < w; t += 32) {
-                const float ex = t < ntok ? exp2f(p_s[g * w + t] - mw) : 0.f;
-                es += ex;
-                p_s[g * w + t] = ex * beta;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) es += __shfl_xor_sync(0xffffffffu, es, o);
-            if (lane == 0) {
-                const float alpha = m_old == -INFINITY ? 0.f : exp2f(m_old - m_new);
-                run_l[g] = run_l[g] * alpha + es * beta;
-                run_m[g] = m_new;
-                s_alpha[g] = alpha;
-                D.wstat[((int64_t)b * Hq + kvh * G + g) * D.Wmax + wi] = make_float2(mw, es);
-            }
-        }
-        __syncthreads();
-
-        // ---- P.V: thread per channel
-        {
-            const int j = tid;
-#pragma unroll
-            for (int g = 0; g < G; ++g) acc[g] *= s_alpha[g];
-            if (fp) {
-                const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(sb) + (size_t)w * kHeadDim;
-                for (int t = 0; t < ntok; ++t) {
-                    const float vv = __bfloat162float(vb[(size_t)t * kHeadDim + j]);
-#pragma unroll
-                    for (int g = 0; g < G; ++g) acc[g] = fmaf(p_s[g * w + t], vv, acc[g]);
+            float x[4] = {s0[0] * qk_scale, s0[1] * qk_scale, s1[0] * qk_scale, s1[1] * qk_scale};
+            if (ntu < 16) {
+                // rows past the open window's last token hold stale slot memory: P is 0
+                // there, but 0 * NaN would still poison the P.V product, so zero them
+                for (int c = lane; c < (16 - ntu) * 16; c += 32) {
+                    const int row = ntu + (c >> 4), half = (c >> 3) & 1, ch = c & 7;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + 4096 + half * 2048 +
+                                                                                  row * 128 + ch * 16),
+                                 "r"(0u)
+                                 : "memory");
                 }
-            } else {
-                const uint8_t *vpart = sb + lg_part_bytes(w);
-                const uint32_t *vw = reinterpret_cast<const uint32_t *>(vpart);
-                const __half2 *vm = reinterpret_cast<const __half2 *>(vpart + lg_codes_bytes(w));
-                for (int t = 0; t < ntok; ++t) {
-                    const uint32_t c = (vw[(t / kVTile) * kHeadDim + j] >> (2 * (t % kVTile))) & 3u;
-                    const __half2 m2 = vm[t * kGroups + j / kGroup];
-                    const float vv = fmaf((float)c, __low2float(m2), __high2float(m2));
+                __syncwarp();
+                if (2 * t >= ntu) x[0] = -INFINITY;
+                if (2 * t + 1 >= ntu) x[1] = -INFINITY;
+                if (8 + 2 * t >= ntu) x[2] = -INFINITY;
+                if (9 + 2 * t >= ntu) x[3] = -INFINITY;
+            }
+            softmax4(x, ust);
+            uint32_t b0h, b0l, b1h, b1l;
+            split2(x[0], x[1], b0h, b0l);
+            split2(x[2], x[3], b1h, b1l);
 #pragma unroll
-                    for (int g = 0; g < G; ++g) acc[g] = fmaf(p_s[g * w + t], vv, acc[g]);
+            for (int mt = 0; mt < 8; ++mt) {
+                const int chunk = 2 * (mt & 3) + lm_hi;
+                const uint32_t addr = base + 4096 + (mt >> 2) * 2048 + lm_tok * 128 + ((chunk ^ (lm_tok & 7)) << 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(addr, a0, a1, a2, a3);
+                mma(o[mt], a0, a1, a2, a3, b0h, b1h);
+                mma(o[mt], a0, a1, a2, a3, b0l, b1l);
+            }
+        } else {
+            // ---------------- INT2 unit
+            const uint32_t kc = base, km = base + 512, vc = base + 768, vm = base + 1280;
+            // QK: column g of N tile 0 is token tA, of tile 1 token tB
+            const int tA = (g & 1) ? g + 7 : g;
+            const int tB = (g & 1) ? g + 8 : g + 1;
+            const uint4 kA0 = lds128(kc + tA * 32), kA1 = lds128(kc + tA * 32 + 16);
+            const uint4 kB0 = lds128(kc + tB * 32), kB1 = lds128(kc + tB * 32 + 16);
+            // this lane's logit / probability tokens: 2t, 2t+8 (tile 0), 2t+1, 2t+9 (tile 1)
+            uint4 kmeta[4];
+            kmeta[0] = lds128(km + (2 * t) * 16);
+            kmeta[1] = lds128(km + (2 * t + 8) * 16);
+            kmeta[2] = lds128(km + (2 * t + 1) * 16);
+            kmeta[3] = lds128(km + (2 * t + 9) * 16);
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int grp = 0; grp < kGroups; ++grp) {
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int ks = 2 * grp + kk;
+                    const uint32_t xa = pick(ks < 4 ? kA0 : kA1, ks & 3) >> (4 * t);
+                    const uint32_t xb = pick(ks < 4 ? kB0 : kB1, ks & 3) >> (4 * t);
+                    mma(c0, Aq0[ks], 0u, Aq2[ks], 0u, codes2(xa), codes2(xa >> 2));
+                    mma(c1, Aq0[ks], 0u, Aq2[ks], 0u, codes2(xb), codes2(xb >> 2));
+                }
+                const float acc[4] = {c0[0], c0[1], c1[0], c1[1]};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 sm = h2f(pick(kmeta[i], grp));   // .x scale, .y min
+                    x[i] = fmaf(sm.x, acc[i], fmaf(sm.y, qsum[grp], x[i]));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[i] *= qk_scale;
+            softmax4(x, ust);
+            uint4 vmeta[4];
+            vmeta[0] = lds128(vm + (2 * t) * 16);
+            vmeta[1] = lds128(vm + (2 * t + 8) * 16);
+            vmeta[2] = lds128(vm + (2 * t + 1) * 16);
+            vmeta[3] = lds128(vm + (2 * t + 9) * 16);
+            const uint4 v0 = lds128(vc + g * 64), v1 = lds128(vc + g * 64 + 16);
+            const uint4 v2 = lds128(vc + g * 64 + 32), v3 = lds128(vc + g * 64 + 48);
+#pragma unroll
+            for (int grp = 0; grp < kGroups; ++grp) {
+                float val[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 sm = h2f(pick(vmeta[i], grp));
+                    val[i] = x[i] * sm.x;
+                    minacc[grp] = fmaf(x[i], sm.y, minacc[grp]);
+                }
+                uint32_t b0h, b0l, b1h, b1l;
+                split2(val[0], val[1], b0h, b0l);
+                split2(val[2], val[3], b1h, b1l);
+                // words of this lane's channels: mt = 2 grp, 2 grp + 1; h = 0 (channel g), 1 (g + 8)
+                const uint4 &vv = grp == 0 ? v0 : grp == 1 ? v1 : grp == 2 ? v2 : v3;
+#pragma unroll
+                for (int mm = 0; mm < 2; ++mm) {
+                    const int mt = 2 * grp + mm;
+                    const uint32_t x0 = pick(vv, 2 * mm) >> (4 * t), x1 = pick(vv, 2 * mm + 1) >> (4 * t);
+                    const uint32_t a0 = codes2(x0), a1 = codes2(x1), a2 = codes2(x0 >> 2), a3 = codes2(x1 >> 2);
+                    mma(o[mt], a0, a1, a2, a3, b0h, b1h);
+                    mma(o[mt], a0, a1, a2, a3, b0l, b1l);
                 }
             }
         }
-        __syncthreads();
-        if (tid == 0 && e + nst < e1) {
-            issue(e + nst, st);
-            issued_end = e + nst + 1;
+        if (t == 0 && g < G) ustat[(int64_t)g * D.Wmax * mu + (int64_t)wi * mu + j] = ust;
+        }
+        __syncwarp();
+        ++consumed;
+        try_issue();
+    }
+    __syncthreads();
+
+    // ---- merge the warps (the rings are free now)
+    float *Ow = reinterpret_cast<float *>(smem);                 // [warp][8 heads][128]
+    float *mw_s = Ow + kWarps * 8 * kHeadDim;                    // [warp][8]
+    float *lw_s = mw_s + kWarps * 8;
+    float *minw = lw_s + kWarps * 8;                             // [warp][8][4]
+    {
+        float *ob = Ow + warp * 8 * kHeadDim;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            ob[(2 * t) * kHeadDim + 16 * mt + g] = o[mt][0];
+            ob[(2 * t + 1) * kHeadDim + 16 * mt + g] = o[mt][1];
+            ob[(2 * t) * kHeadDim + 16 * mt + g + 8] = o[mt][2];
+            ob[(2 * t + 1) * kHeadDim + 16 * mt + g + 8] = o[mt][3];
         }
     }
-
-    // ---- split partials
-    float *part = D.part + (((int64_t)b * D.Hkv + kvh) * kMaxSplits + split) * G * (2 + kHeadDim);
 #pragma unroll
-    for (int g = 0; g < G; ++g) part[g * (2 + kHeadDim) + 2 + tid] = acc[g];
-    if (tid < G) {
-        part[tid * (2 + kHeadDim)] = run_m[tid];
-        part[tid * (2 + kHeadDim) + 1] = run_l[tid];
+    for (int i = 0; i < kGroups; ++i) {
+        minacc[i] += __shfl_xor_sync(0xffffffffu, minacc[i], 1);
+        minacc[i] += __shfl_xor_sync(0xffffffffu, minacc[i], 2);
+    }
+    if (t == 0) {
+        mw_s[warp * 8 + g] = m_run;
+        lw_s[warp * 8 + g] = l_run;
+#pragma unroll
+        for (int i = 0; i < kGroups; ++i) minw[(warp * 8 + g) * 4 + i] = minacc[i];
+    }
+    __syncthreads();
+    float *part = S.part + ((int64_t)bk * kMaxSplits + split) * G * (2 + kHeadDim);
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + hh]);
+        float acc = 0.f, l = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int ww = 0; ww < kWarps; ++ww) {
+                const float f = exp2f(mw_s[ww * 8 + hh] - M);
+                acc += f * (Ow[(ww * 8 + hh) * kHeadDim + tid] + minw[(ww * 8 + hh) * 4 + tid / kGroup]);
+                l += f * lw_s[ww * 8 + hh];
+            }
+        }
+        part[hh * (2 + kHeadDim) + 2 + tid] = acc;
+        if (tid == 0) {
+            part[hh * (2 + kHeadDim)] = M;
+            part[hh * (2 + kHeadDim) + 1] = l;
+        }
+    }
+    // per-window statistics from the unit records of this split
+    float2 *wstat = S.wstat + ((int64_t)b * Hq + kvh * G) * D.Wmax;
+    for (int i = tid; i < nwin * G; i += kThreads) {
+        const int e = gentry(i / G), hh = i % G;
+        const int wi = entry(e).x;
+        const float2 *us = ustat + (int64_t)hh * D.Wmax * mu + (int64_t)wi * mu;
+        float2 v[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            v[jj] = (jj < mu && unit_tokens(wi, jj) > 0) ? __ldcg(us + jj) : make_float2(-INFINITY, 0.f);
+        float2 st = v[0];
+#pragma unroll
+        for (int jj = 1; jj < 8; ++jj) st = stat_merge(st, v[jj]);
+        wstat[(int64_t)hh * D.Wmax + wi] = st;
     }
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        const unsigned prev = atomicAdd(&D.arrive[bk], 1u);
+        const unsigned prev = atomicAdd(&S.arrive[bk], 1u);
         s_flag = prev == (unsigned)(splits - 1);
     }
     __syncthreads();
     if (!s_flag) return;
     __threadfence();
 
-    // ---- last CTA: log-sum-exp merge of the splits
-    const float *pb = D.part + ((int64_t)b * D.Hkv + kvh) * kMaxSplits * G * (2 + kHeadDim);
-    if (tid < G) {
-        float M = -INFINITY;
-        for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(pb + ((int64_t)s * G + tid) * (2 + kHeadDim)));
-        float l = 0.f;
-        if (M != -INFINITY) {
-            for (int s = 0; s < splits; ++s) {
-                const float ms = __ldcg(pb + ((int64_t)s * G + tid) * (2 + kHeadDim));
-                const float ls = __ldcg(pb + ((int64_t)s * G + tid) * (2 + kHeadDim) + 1);
-                if (ms != -INFINITY) l += ls * exp2f(ms - M);
-            }
+    // ================= last CTA of this (sequence, KV head): merge the splits
+    float *sM = reinterpret_cast<float *>(smem);                  // [splits][G]
+    float *sL = sM + kMaxSplits * G;
+    float *sF = sL + kMaxSplits * G;                              // scale factor per split
+    float *hM = sF + kMaxSplits * G;                              // [G] global max
+    float *hIL = hM + 8;                                          // [G] 1 / L
+    float *hNew = hIL + 8;                                        // [G] new-token logit
+    float *hFN = hNew + 8;                                        // [G] new-token factor
+    const float *pb = S.part + (int64_t)bk * kMaxSplits * G * (2 + kHeadDim);
+    for (int i = tid; i < splits * G; i += kThreads) {
+        sM[i] = __ldcg(pb + (int64_t)i * (2 + kHeadDim));
+        sL[i] = __ldcg(pb + (int64_t)i * (2 + kHeadDim) + 1);
+    }
+    const bool has_new = knew != nullptr;
+    const __nv_bfloat16 *kn = has_new ? knew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
+    const __nv_bfloat16 *vn = has_new ? vnew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
+    if (has_new) {
+        for (int hh = warp; hh < G; hh += kWarps) {
+            const __nv_bfloat16 *qq = q + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim;
+            float d = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                d = fmaf(__bfloat162float(qq[lane * 4 + i]), __bfloat162float(kn[lane * 4 + i]), d);
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o2);
+            if (lane == 0) hNew[hh] = d * qk_scale;
         }
-        s_M[tid] = M;
-        s_il[tid] = l > 0.f ? 1.f / l : 0.f;
     }
     __syncthreads();
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        float o = 0.f;
-        const float M = s_M[g];
-        if (M != -INFINITY) {
-            for (int s = 0; s < splits; ++s) {
-                const float ms = __ldcg(pb + ((int64_t)s * G + g) * (2 + kHeadDim));
-                if (ms == -INFINITY) continue;
-                o = fmaf(__ldcg(pb + ((int64_t)s * G + g) * (2 + kHeadDim) + 2 + tid), exp2f(ms - M), o);
-            }
+    if (tid < G) {
+        float M = has_new ? hNew[tid] : -INFINITY;
+        for (int s = 0; s < splits; ++s) M = fmaxf(M, sM[s * G + tid]);
+        float L = 0.f;
+        for (int s = 0; s < splits; ++s) {
+            const float f = (M == -INFINITY || sM[s * G + tid] == -INFINITY) ? 0.f : exp2f(sM[s * G + tid] - M);
+            sF[s * G + tid] = f;
+            L += f * sL[s * G + tid];
         }
-        out[((int64_t)b * Hq + kvh * G + g) * kHeadDim + tid] = o * s_il[g];
+        const float fn = has_new ? exp2f(hNew[tid] - M) : 0.f;
+        L += fn;
+        hM[tid] = M;
+        hIL[tid] = L > 0.f ? 1.f / L : 0.f;
+        hFN[tid] = fn;
     }
-    // masses and the cumulative score
+    __syncthreads();
+    {
+        float acc[G];
+        const float vnv = has_new ? __bfloat162float(vn[tid]) : 0.f;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) acc[hh] = hFN[hh] * vnv;
+        for (int s0 = 0; s0 < splits; s0 += 8) {
+            float v[8][G];
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+                    v[s][hh] = s0 + s < splits ? __ldcg(pb + ((int64_t)(s0 + s) * G + hh) * (2 + kHeadDim) + 2 + tid)
+                                               : 0.f;
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+                    if (s0 + s < splits) acc[hh] = fmaf(sF[(s0 + s) * G + hh], v[s][hh], acc[hh]);
+        }
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) out[((int64_t)b * Hq + kvh * G + hh) * kHeadDim + tid] = acc[hh] * hIL[hh];
+    }
+
+    // ---- masses and the cumulative score; the new token counts in its window
+    const int64_t Lnew = has_new ? length + 1 : length;
+    const int n_out = (int)((Lnew + w - 1) / w);
+    const int wnew = (int)(length / w);
+    const bool opens = has_new && (length % w == 0);
     const float inv_hq = 1.f / (float)Hq;
-    for (int wi = tid; wi < n_win; wi += kThreads) {
-        const bool live = D.tier[wb + wi] != QEVICT_TIER_E;
-        float sum = 0.f;
+    float *sp = D.score_part + ((int64_t)b * Hkv + kvh) * D.Wmax;
+    for (int w0 = 0; w0 < n_out; w0 += 4 * kThreads) {
+        float2 st[4][G];
+        bool live[4];
+        float old[4];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float m = 0.f;
-            if (live && s_M[g] != -INFINITY) {
-                const float2 ws = __ldcg(&D.wstat[((int64_t)b * Hq + kvh * G + g) * D.Wmax + wi]);
-                m = ws.y * exp2f(ws.x - s_M[g]) * s_il[g];
-            }
-            if (mass) mass[((int64_t)b * Hq + kvh * G + g) * n_win + wi] = m;
-            sum += m;
+        for (int c = 0; c < 4; ++c) {
+            const int wi = w0 + c * kThreads + tid;
+            const bool in = wi < n_out;
+            const bool fresh = opens && wi == wnew;
+            live[c] = in && (fresh || D.tier[wb + wi] != QEVICT_TIER_E);
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh)
+                st[c][hh] = (live[c] && !fresh) ? __ldcg(&wstat[(int64_t)hh * D.Wmax + wi]) : make_float2(-INFINITY, 0.f);
+            old[c] = (in && accumulate) ? sp[wi] : 0.f;
         }
-        if (accumulate) D.score_part[((int64_t)b * D.Hkv + kvh) * D.Wmax + wi] += sum * inv_hq;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int wi = w0 + c * kThreads + tid;
+            if (wi >= n_out) continue;
+            float sum = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                float2 stt = st[c][hh];
+                if (has_new && wi == wnew) stt = stat_merge(stt, make_float2(hNew[hh], 1.f));
+                const float m =
+                    (live[c] && hM[hh] != -INFINITY && stt.y > 0.f) ? stt.y * exp2f(stt.x - hM[hh]) * hIL[hh] : 0.f;
+                if (mass) mass[((int64_t)b * Hq + kvh * G + hh) * n_out + wi] = m;
+                sum += m;
+            }
+            if (accumulate) sp[wi] = old[c] + sum * inv_hq;
+        }
     }
-    if (tid == 0) D.arrive[bk] = 0u;
+
+    // ---- append this step's token (this KV head's K and V rows)
+    if (has_new) {
+        const int slot = opens ? ctr[CTR_NEXT] : D.fp_slot[wb + wnew];
+        if (slot >= 0 && tid < 32) {
+            const int row = (int)(length % w);
+            const int kv = tid >> 4, c = tid & 15;
+            const __nv_bfloat16 *src = kv ? vn : kn;
+            uint8_t *dst =
+                D.fp_pool + (int64_t)slot * D.fp_slot_bytes + (((int64_t)(kvh * 2 + kv) * w + row) * kHeadDim) * 2;
+            reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned prev = atomicAdd(&S.arrive_b[b], 1u);
+            if (prev == (unsigned)(Hkv - 1)) {
+                // last KV head of this sequence: table bookkeeping for the new token
+                __threadfence();
+                int32_t *c = D.ctr + b * kCtrN;
+                if (opens) {
+                    const int slotn = c[CTR_NEXT];
+                    if (slotn < 0) {
+                        set_status(C, QEVICT_ERR_CAPACITY, layer, b, wnew);
+                    } else {
+                        D.tier[wb + wnew] = QEVICT_TIER_FP;
+                        D.fp_slot[wb + wnew] = slotn;
+                        D.lg_slot[wb + wnew] = -1;
+                        D.lwrites[wb + wnew] = 0;
+                        const int n = c[CTR_NFP];
+                        D.fp_list[b * D.CF + n] = make_int2(wnew, slotn);
+                        c[CTR_NFP] = n + 1;
+                        const int top = c[CTR_FP_TOP];
+                        if (top > 0) {
+                            c[CTR_NEXT] = D.fp_free[b * D.CF + top - 1];
+                            c[CTR_FP_TOP] = top - 1;
+                        } else {
+                            c[CTR_NEXT] = -1;
+                        }
+                    }
+                }
+                c[CTR_LEN] = (int)Lnew;
+                S.arrive_b[b] = 0u;
+            }
+        }
+    }
+    if (tid == 0) S.arrive[bk] = 0u;
+}
+
+template <int G>
+cudaError_t raise_smem_limit(int optin) {
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<G>);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - (int)fa.sharedSizeBytes);
 }
 
 }  // namespace
 
-int decode_smem_bytes(int w, int G) {
-    (void)G;
-    const int stage = w * kHeadDim * 4;
-    const int extra = kMaxG * kHeadDim * 4 + kMaxG * w * 4 + 5 * kMaxG * 4 + 8 * 8 + 128;
-    int nst = (200 * 1024 - extra) / stage;
-    if (nst > 4) nst = 4;
-    if (nst < 2) nst = 2;
-    return nst * stage + extra;
+// Raise the dynamic shared-memory limit of every decode instantiation once
+// (called at cache creation, outside any stream capture).
+cudaError_t prepare_decode() {
+    static bool done = false;
+    if (done) return cudaSuccess;
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = raise_smem_limit<1>(optin);
+    if (e == cudaSuccess) e = raise_smem_limit<2>(optin);
+    if (e == cudaSuccess) e = raise_smem_limit<3>(optin);
+    if (e == cudaSuccess) e = raise_smem_limit<4>(optin);
+    if (e == cudaSuccess) e = raise_smem_limit<5>(optin);
+    if (e == cudaSuccess) e = raise_smem_limit<6>(optin);
+    if (e == cudaSuccess) e = raise_smem_limit<7>(optin);
+    if (e == cudaSuccess) e = raise_smem_limit<8>(optin);
+    if (e == cudaSuccess) done = true;
+    return e;
 }
 
-cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *q, float *out,
-                          float *mass, int accumulate, int splits, cudaStream_t s) {
-    const int stage = L.w * kHeadDim * 4;
-    const int smem = decode_smem_bytes(L.w, L.G);
-    const int extra = kMaxG * kHeadDim * 4 + kMaxG * L.w * 4 + 5 * kMaxG * 4 + 8 * 8 + 128;
-    const int nst = (smem - extra) / stage;
-    dim3 grid(splits, L.B * L.Hkv);
-#define QV_CASE(GG)                                                                                    \
-    case GG: {                                                                                         \
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                             smem);                                                    \
-        if (e != cudaSuccess) return e;                                                                \
-        decode_kernel<GG><<<grid, kThreads, smem, s>>>(L, C, layer, q, out, mass, accumulate, splits, nst,    \
-                                                       stage);                            \
-        break;                                                                                         \
-    }
+// Splits per (sequence, KV head): about two CTAs per SM in one wave.
+int decode_splits(int pairs, int num_sms) {
+    int s = (2 * num_sms + pairs - 1) / pairs;
+    if (s > kMaxSplits) s = kMaxSplits;
+    if (s < 1) s = 1;
+    return s;
+}
+
+cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, const CUtensorMap &tmap,
+                          int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
+                          float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(splits, L.B * L.Hkv);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kWarps * kRing + 1024;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+#define QV_CASE(GG)                                                                                          \
+    case GG:                                                                                                 \
+        return cudaLaunchKernelEx(&cfg, decode_kernel<GG>, L, C, S, tmap, layer, q, knew, vnew, out, mass,  \
+                                  accumulate, splits);
     switch (L.G) {
         QV_CASE(1)
         QV_CASE(2)
@@ -371,7 +790,6 @@ cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, int layer, const
             return cudaErrorInvalidValue;
     }
 #undef QV_CASE
-    return cudaGetLastError();
 }
 
 }  // namespace qevict

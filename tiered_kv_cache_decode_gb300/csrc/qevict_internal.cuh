@@ -2,6 +2,7 @@
 // the device view of one layer, launch entry points, and small PTX helpers.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -17,11 +18,12 @@ constexpr int kGroups = kHeadDim / kGroup;
 constexpr int kMaxG = 8;               // query heads per KV head
 constexpr int kMaxSplits = 64;         // decode splits per (sequence, KV head)
 constexpr int kVTile = 16;             // tokens per transposed V-code word
-constexpr int kCtrN = 8;               // counters per sequence
+constexpr int kCtrN = 16;              // counters per sequence
 
-// counter slots (per sequence)
+// counter slots (per sequence). CTR_NEXT is a full-precision slot taken off the
+// free list ahead of time for the next window to open (-1 if none was free).
 enum { CTR_NFP = 0, CTR_NQ = 1, CTR_FP_TOP = 2, CTR_LG_TOP = 3, CTR_WQ = 4, CTR_WP = 5,
-       CTR_WC = 6, CTR_LEN = 7 };
+       CTR_WC = 6, CTR_LEN = 7, CTR_NEXT = 8 };
 
 // device stats slots
 enum { ST_DEMOTE = 0, ST_PROMOTE = 1, ST_EVICT = 2, ST_LWRITE = 3, ST_LREUSE = 4, ST_N = 8 };
@@ -31,6 +33,18 @@ __host__ __device__ inline int64_t lg_part_bytes(int w) {
     return (int64_t)w * (kHeadDim / 4) + (int64_t)w * kGroups * 4;
 }
 __host__ __device__ inline int64_t lg_codes_bytes(int w) { return (int64_t)w * (kHeadDim / 4); }
+
+// V codes of a 16-token tile are 128 uint32 words, word i = (g * 8 + mt) * 2 + h
+// holding channel 16 * mt + g + 8 * h (g, mt in 0..7, h in 0..1). This puts the
+// 16 words one MMA lane group needs for the transposed-V operand side by side.
+__host__ __device__ inline int vword_dim(int i) {
+    const int g = i >> 4, mt = (i >> 1) & 7, h = i & 1;
+    return 16 * mt + g + 8 * h;
+}
+__host__ __device__ inline int vword_index(int ch) {
+    const int mt = ch >> 4, r = ch & 15, g = r & 7, h = r >> 3;
+    return (g * 8 + mt) * 2 + h;
+}
 
 // Everything a kernel needs about one layer of the cache (passed by value).
 struct LayerDev {
@@ -54,9 +68,16 @@ struct LayerDev {
     int4 *work_q;         // [B][Wmax] quantise: {window, src fp slot or -1 (external), dst ledger slot, 0}
     int4 *work_p;         // [B][Wmax] promote: {window, src ledger slot, dst fp slot, 0}
     int4 *work_c;         // [B][Wmax] prefill copy: {window, dst fp slot, 0, 0}
-    float *part;          // [B][Hkv][kMaxSplits][G][2 + d] decode split partials
+};
+
+// Decode scratch, shared by all layers of a cache: a decode launch touches it
+// only after its dependency wait, so consecutive launches never overlap in it.
+struct DecodeScratch {
+    float *part;          // [B*Hkv][kMaxSplits][G][2 + d] split partials (max, sum, acc)
     float2 *wstat;        // [B][Hq][Wmax] (window max, window exp-sum), log2 domain
-    uint32_t *arrive;     // [B][Hkv] split arrival counters (kept at 0 between launches)
+    float2 *ustat;        // [B][Hq][Wmax][w/16] the same per 16-token unit
+    uint32_t *arrive;     // [B*Hkv] split arrival counters (kept at 0 between launches)
+    uint32_t *arrive_b;   // [B] KV-head arrival counters for the fused append
 };
 
 struct CacheDev {
@@ -91,10 +112,12 @@ cudaError_t launch_prefill_copy(const LayerDev &L, const __nv_bfloat16 *k_ext,
                                 const __nv_bfloat16 *v_ext, int64_t ext_len, int max_entries,
                                 cudaStream_t s);
 cudaError_t launch_scores(const LayerDev &L, int n_win, float *out, cudaStream_t s);
-cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *q,
-                          float *out, float *mass, int accumulate, int splits, cudaStream_t s);
+cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, const CUtensorMap &tmap,
+                          int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
+                          float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s);
 cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s);
-int decode_smem_bytes(int w, int G);
+int decode_splits(int pairs, int num_sms);
+cudaError_t prepare_decode();
 
 // ---- device helpers -------------------------------------------------------
 __device__ __forceinline__ void set_status(const CacheDev &C, int code, int layer, int i0, int i1) {

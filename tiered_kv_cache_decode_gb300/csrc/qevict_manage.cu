@@ -39,10 +39,10 @@ __global__ void init_layer_kernel(LayerDev D) {
     for (int64_t i = i0; i < D.B; i += stride) {
         int32_t *c = D.ctr + i * kCtrN;
         for (int k = 0; k < kCtrN; ++k) c[k] = 0;
-        c[CTR_FP_TOP] = D.CF;
+        c[CTR_NEXT] = (int)i * D.CF;      // slot b*CF, the top of the stack, is taken ahead
+        c[CTR_FP_TOP] = D.CF - 1;
         c[CTR_LG_TOP] = D.CQ;
     }
-    for (int64_t i = i0; i < (int64_t)D.B * D.Hkv; i += stride) D.arrive[i] = 0;
 }
 
 // ---------------------------------------------------------------- append
@@ -74,14 +74,15 @@ __global__ void append_kernel(LayerDev D, CacheDev C, int layer, const __nv_bflo
         if (!s_bad) {
             for (int64_t p = ((L0 + w - 1) / w) * w; p < L0 + n_new; p += w) {
                 const int wi = (int)(p / w);
+                const int slot = ctr[CTR_NEXT];
                 const int top = ctr[CTR_FP_TOP];
-                int slot = -1;
                 if (top > 0) {
-                    slot = D.fp_free[b * D.CF + top - 1];
+                    ctr[CTR_NEXT] = D.fp_free[b * D.CF + top - 1];
                     ctr[CTR_FP_TOP] = top - 1;
                 } else {
-                    set_status(C, QEVICT_ERR_CAPACITY, layer, b, wi);
+                    ctr[CTR_NEXT] = -1;
                 }
+                if (slot < 0) set_status(C, QEVICT_ERR_CAPACITY, layer, b, wi);
                 D.tier[wb + wi] = slot >= 0 ? QEVICT_TIER_FP : QEVICT_TIER_E;
                 D.fp_slot[wb + wi] = slot;
                 D.lg_slot[wb + wi] = -1;
@@ -120,6 +121,15 @@ __global__ void append_kernel(LayerDev D, CacheDev C, int layer, const __nv_bflo
 }
 
 // ---------------------------------------------------------------- plan
+// Take a free full-precision slot ahead of time for the next window to open.
+__device__ __forceinline__ void reserve_next(const LayerDev &D, int32_t *ctr, int b) {
+    if (ctr[CTR_NEXT] < 0 && ctr[CTR_FP_TOP] > 0) {
+        const int top = ctr[CTR_FP_TOP] - 1;
+        ctr[CTR_NEXT] = D.fp_free[b * D.CF + top];
+        ctr[CTR_FP_TOP] = top;
+    }
+}
+
 __device__ __forceinline__ uint32_t orderable(float f) {
     const uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
@@ -176,13 +186,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         ctr[CTR_WQ] = 0;
         ctr[CTR_WP] = 0;
         ctr[CTR_WC] = 0;
+        // the slot reserved for the next window goes back on the free list for the plan
+        const int nx = ctr[CTR_NEXT];
+        if (nx >= 0) {
+            D.fp_free[b * D.CF + ctr[CTR_FP_TOP]] = nx;
+            ctr[CTR_FP_TOP] += 1;
+            ctr[CTR_NEXT] = -1;
+        }
     }
-    if (nw == 0) return;
+    __syncthreads();
+    if (nw == 0) {
+        if (tid == 0) reserve_next(D, ctr, b);
+        return;
+    }
     // byte budget at this length: B_t = floor(beta * L * Hkv * d * 4)
     const int64_t budget = (int64_t)floor(D.beta * (double)(length * D.Hkv * kHeadDim * 4));
     const int nfp_budget = (int)floor((D.rho * (double)budget) / (double)D.c_fp);
     if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES) && budget < D.c_fp) {
-        if (tid == 0) set_status(C, QEVICT_ERR_BUDGET, a.layer, b, (int)length);
+        if (tid == 0) {
+            set_status(C, QEVICT_ERR_BUDGET, a.layer, b, (int)length);
+            reserve_next(D, ctr, b);
+        }
         return;
     }
 
@@ -284,7 +308,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                 s_key[i] = key;
             }
             if (__syncthreads_or(bad)) {
-                if (tid == 0) set_status(C, QEVICT_ERR_DEVICE, a.layer, b, -1);
+                if (tid == 0) {
+                    set_status(C, QEVICT_ERR_DEVICE, a.layer, b, -1);
+                    reserve_next(D, ctr, b);
+                }
                 return;
             }
             // bitonic sort, ascending: forced window first, then score desc, index asc
@@ -326,7 +353,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                 s_tgt[i] = t;
             }
             if (__syncthreads_or(bad)) {
-                if (tid == 0) set_status(C, QEVICT_ERR_STATE, a.layer, b, -1);
+                if (tid == 0) {
+                    set_status(C, QEVICT_ERR_STATE, a.layer, b, -1);
+                    reserve_next(D, ctr, b);
+                }
                 return;
             }
         }
@@ -350,7 +380,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         const int off_need_lg = block_scan(need_lg, &tot_need_lg, s_warp);
         const int fp_top = ctr[CTR_FP_TOP], lg_top = ctr[CTR_LG_TOP];
         if (fp_top + tot_free_fp < tot_need_fp || lg_top + tot_free_lg < tot_need_lg) {
-            if (tid == 0) set_status(C, QEVICT_ERR_CAPACITY, a.layer, b, -1);
+            if (tid == 0) {
+                set_status(C, QEVICT_ERR_CAPACITY, a.layer, b, -1);
+                reserve_next(D, ctr, b);
+            }
             return;
         }
         // ---- phase A: release slots
@@ -467,6 +500,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         ctr[CTR_NFP] = tf;
         ctr[CTR_NQ] = tq;
         if (prefill) ctr[CTR_LEN] = (int)length;
+        reserve_next(D, ctr, b);
     }
 }
 
@@ -547,9 +581,10 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
                 words[i] = word;
             }
         } else {
-            // V: [token/16][d] words, token t of the tile at bits 2*(t%16)
+            // V: per 16-token tile 128 words; word i holds channel vword_dim(i), token t of
+            // the tile at bits 2*(t%16)
             for (int i = threadIdx.x; i < (w / kVTile) * kHeadDim; i += blockDim.x) {
-                const int tile = i / kHeadDim, j = i % kHeadDim;
+                const int tile = i / kHeadDim, j = vword_dim(i % kHeadDim);
                 uint32_t word = 0;
 #pragma unroll
                 for (int t = 0; t < kVTile; ++t) word |= (uint32_t)s_codes[(tile * kVTile + t) * kHeadDim + j] << (2 * t);
@@ -584,7 +619,7 @@ __global__ void __launch_bounds__(128) promote_kernel(LayerDev D) {
                 const int ch = g * kGroup + j;
                 uint32_t c;
                 if (kv == 0) c = (words[t * (kHeadDim / 16) + ch / 16] >> (2 * (ch % 16))) & 3u;
-                else c = (words[(t / kVTile) * kHeadDim + ch] >> (2 * (t % kVTile))) & 3u;
+                else c = (words[(t / kVTile) * kHeadDim + vword_index(ch)] >> (2 * (t % kVTile))) & 3u;
                 outv[j] = __float2bfloat16_rn(fmaf((float)c, s, mn));
             }
             uint4 *d4 = reinterpret_cast<uint4 *>(dst + (int64_t)t * kHeadDim + g * kGroup);
