@@ -109,18 +109,16 @@ typedef struct qevict_cache qevict_cache;
  *                                  int32 slot index or -1
  *  ledger_writes[b*max_windows+w]  int32 times window w was quantised (<= 1)
  *  fp_pool + slot * fp_slot_bytes  a full-precision window:
- *        bf16 [Hkv][2 (K, V)][window][head_dim]
- *  ledger_pool + slot * ledger_slot_bytes   an INT2 window, per KV head and
- *        K/V a part of window*48 bytes at head_dim 128: part index
- *        (kvh * 2 + kv), each part = codes (window * head_dim / 4 bytes)
- *        followed by meta (window * head_dim / 32 half2 {scale, min}):
- *        K codes: [token][head_dim / 4] bytes, channel j in byte j / 4,
- *                 bits 2 * (j % 4);
- *        V codes: [token / 16][128] uint32 words per 16-token tile; word
- *                 i = (g * 8 + mt) * 2 + h (g, mt in 0..7, h in 0..1) holds
- *                 channel 16 * mt + g + 8 * h, token t of the tile in bits
- *                 2 * (t % 16);
- *        meta:    [token][head_dim / 32] half2, .x = scale, .y = min.
+ *        bf16 [Hkv][2 (K, V)][2 (channels 0-63, 64-127)][window][64]
+ *  ledger_pool + slot * ledger_slot_bytes   an INT2 window: [Hkv][window /
+ *        16] tiles of 16 tokens, 1536 bytes each (head_dim 128):
+ *        K codes at 0: [16 tokens][8] uint32, word q of a token holds
+ *                 channels 16 q .. 16 q + 15, channel j at bits 2 * (j % 16);
+ *        K meta at 512: [16 tokens][4 groups] half2, .x = scale, .y = min;
+ *        V codes at 768: 128 uint32 words; word i = (g * 8 + mt) * 2 + h
+ *                 (g, mt in 0..7, h in 0..1) holds channel 16 * mt + g + 8 h,
+ *                 token t of the tile at bits 2 * t;
+ *        V meta at 1280: [16 tokens][4 groups] half2.
  *  length                          current context length (host copy). */
 typedef struct qevict_view {
     int32_t batch, num_q_heads, num_kv_heads, head_dim, window;

@@ -292,10 +292,11 @@ class TieredCache:
                 get(v.ledger_writes, "<i4"))
 
     def fp_window(self, layer, slot):
-        """bf16 [Hkv][2][w][d] content of a full-precision slot (host copy)."""
+        """bf16 [Hkv][2 (K, V)][w][d] content of a full-precision slot (host copy)."""
         v = self.view(layer)
         raw = device_tensor(v.fp_pool + slot * v.fp_slot_bytes, (v.fp_slot_bytes,), "|u1").cpu()
-        return raw.view(torch.bfloat16).view(self.Hkv, 2, self.w, HEAD_DIM)
+        x = raw.view(torch.bfloat16).view(self.Hkv, 2, 2, self.w, 64)     # [kvh][kv][half][token][64]
+        return x.permute(0, 1, 3, 2, 4).reshape(self.Hkv, 2, self.w, HEAD_DIM)
 
     def ledger_window(self, layer, slot):
         """Decoded ledger slot: codes uint8 [Hkv][2][w][d], scale/min fp16 [Hkv][2][w][d/32]."""
@@ -305,25 +306,26 @@ class TieredCache:
 
 
 def decode_ledger_slot(raw: torch.Tensor, Hkv: int, w: int):
-    """Unpack the documented ledger slot layout (see include/qevict.h) on the host."""
+    """Unpack the documented ledger slot layout (see include/qevict.h) on the host.
+
+    Returns codes uint8 [Hkv][2 (K, V)][w][d] and scale, min fp16 [Hkv][2][w][d/32].
+    """
     d = HEAD_DIM
-    part = w * (d // 4) + w * (d // 32) * 4
-    raw = raw.view(Hkv, 2, part)
-    codes = torch.empty(Hkv, 2, w, d, dtype=torch.uint8)
+    nt = w // 16
+    raw = raw.view(Hkv, nt, 1536)
     shifts = torch.arange(16, dtype=torch.int64) * 2
-    for kv in range(2):
-        words = raw[:, kv, :w * d // 4].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF
-        if kv == 0:     # [token][d/16 words], channel j at word j//16 bits 2*(j%16)
-            wv = words.view(Hkv, w, d // 16)
-            c = (wv[..., None] >> shifts) & 3          # [Hkv][w][d/16][16]
-            codes[:, 0] = c.reshape(Hkv, w, d).to(torch.uint8)
-        else:           # [token/16][128 words], word i holds channel vword_dim(i)
-            wv = words.view(Hkv, w // 16, d)
-            c = (wv[..., None] >> shifts) & 3          # [Hkv][tiles][word][16]
-            i = torch.arange(d)
-            ch = 16 * ((i >> 1) & 7) + (i >> 4) + 8 * (i & 1)
-            c2 = torch.empty_like(c)
-            c2[:, :, ch] = c
-            codes[:, 1] = c2.permute(0, 1, 3, 2).reshape(Hkv, w, d).to(torch.uint8)
-    meta = raw[:, :, w * d // 4:].contiguous().view(torch.float16).view(Hkv, 2, w, d // 32, 2)
+    kw = raw[:, :, :512].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF   # [Hkv][nt][16*8]
+    kc = (kw.view(Hkv, nt, 16, 8)[..., None] >> shifts) & 3                           # [Hkv][nt][tok][q][16]
+    kcodes = kc.reshape(Hkv, nt * 16, d)
+    vw = raw[:, :, 768:1280].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF   # [Hkv][nt][128]
+    vc = (vw[..., None] >> shifts) & 3                                                   # [Hkv][nt][word][tok]
+    i = torch.arange(d)
+    ch = 16 * ((i >> 1) & 7) + (i >> 4) + 8 * (i & 1)                                   # channel of word i
+    vcodes = torch.empty(Hkv, nt, d, 16, dtype=torch.int64)
+    vcodes[:, :, ch] = vc
+    vcodes = vcodes.permute(0, 1, 3, 2).reshape(Hkv, nt * 16, d)
+    codes = torch.stack([kcodes, vcodes], dim=1).to(torch.uint8)
+    km = raw[:, :, 512:768].contiguous().view(torch.float16).view(Hkv, nt * 16, 4, 2)
+    vm = raw[:, :, 1280:1536].contiguous().view(torch.float16).view(Hkv, nt * 16, 4, 2)
+    meta = torch.stack([km, vm], dim=1)
     return codes, meta[..., 0].clone(), meta[..., 1].clone()

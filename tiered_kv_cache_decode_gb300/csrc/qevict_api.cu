@@ -32,7 +32,7 @@ qevict_status cuda_fail(cudaError_t e, const char *what) {
 
 struct LayerHost {
     LayerDev dev{};
-    CUtensorMap tmap{};     // 2-D tiled view of the full-precision pool: [rows][128] bf16, 64 x 16 boxes
+    CUtensorMap tmap{};     // 4-D tiled view of the full-precision pool, 64 x 16 x 4 boxes
     int64_t length = 0;
     void *base = nullptr;
 };
@@ -263,7 +263,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     pool_capacity(cfg, Wmax, c->c_fp, c->c_q, &c->CF, &c->CQ);
     const int B = cfg.batch, Hkv = cfg.num_kv_heads, Hq = cfg.num_q_heads, w = cfg.window;
     const int64_t fps = (int64_t)Hkv * 2 * w * kHeadDim * 2;
-    const int64_t lgs = (int64_t)Hkv * 2 * lg_part_bytes(w);
+    const int64_t lgs = (int64_t)Hkv * (w / 16) * kQTile;
 
     cudaError_t err = cudaSuccess;
     // cache-wide status and statistics
@@ -279,9 +279,9 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     // every allocation first, so that a failing allocator leaves nothing behind
     {
         Carver cv;
-        const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * (2 + kHeadDim) * 4);
+        const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * kHeadDim * 4);
+        const size_t o_pml = cv.take((size_t)B * Hkv * kMaxSplits * c->G * 8);
         const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
-        const size_t o_us = cv.take((size_t)B * Hq * Wmax * (w / 16) * 8);
         const size_t o_ar = cv.take((size_t)B * Hkv * 4);
         const size_t o_ab = cv.take((size_t)B * 4);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
@@ -292,8 +292,8 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
             return fail(QEVICT_ERR_OUT_OF_MEMORY, "allocation of %zu B of decode scratch failed", need);
         }
         c->scratch.part = (float *)(base + o_part);
+        c->scratch.part_ml = (float2 *)(base + o_pml);
         c->scratch.wstat = (float2 *)(base + o_ws);
-        c->scratch.ustat = (float2 *)(base + o_us);
         c->scratch.arrive = (uint32_t *)(base + o_ar);
         c->scratch.arrive_b = (uint32_t *)(base + o_ab);
         c->scratch_bytes = cv.off;
@@ -364,12 +364,13 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
             err = cudaErrorNotSupported;
             break;
         }
+        // the full-precision pool as [slot * Hkv + kvh][K0, K1, V0, V1][token][64 channels]
         const LayerDev &D = c->layers[l].dev;
-        const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)B * c->CF * Hkv * 2 * w};
-        const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
-        const cuuint32_t box[2] = {64, 16};
-        const cuuint32_t estr[2] = {1, 1};
-        CUresult r = enc(&c->layers[l].tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D.fp_pool, dims, strides, box, estr,
+        const cuuint64_t dims[4] = {64, (cuuint64_t)w, 4, (cuuint64_t)B * c->CF * Hkv};
+        const cuuint64_t strides[3] = {128, (cuuint64_t)w * 128, (cuuint64_t)w * 512};
+        const cuuint32_t box[4] = {64, 16, 4, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult r = enc(&c->layers[l].tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, D.fp_pool, dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) err = cudaErrorInvalidValue;
@@ -455,7 +456,7 @@ static qevict_status decode_common(qevict_cache *c, int32_t layer, const void *q
     } else if (lh.length < 1) {
         return fail(QEVICT_ERR_INVALID_ARG, "layer %d is empty", layer);
     }
-    const int splits = decode_splits(c->cfg.batch * c->cfg.num_kv_heads, c->num_sms);
+    const int splits = decode_splits(c->cfg.batch * c->cfg.num_kv_heads, c->num_sms, c->G);
     const bool pdl = c->allow_pdl && c->prev_layer >= 0 && c->prev_layer != layer && c->prev_stream == stream;
     cudaError_t e = launch_decode(lh.dev, c->cdev, c->scratch, lh.tmap, layer, (const __nv_bfloat16 *)q,
                                   (const __nv_bfloat16 *)k_new, (const __nv_bfloat16 *)v_new, out, mass,

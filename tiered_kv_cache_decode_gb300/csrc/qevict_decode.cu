@@ -13,10 +13,10 @@
 // head) and a cost-balanced contiguous run of that sequence's window list
 // (full-precision windows first, then INT2 windows). Its windows are cut
 // into 16-token units that its four warps take round-robin. Every warp feeds
-// itself: lane 0 keeps a ring of in-flight units in shared memory (a
-// full-precision unit is four TMA tile loads of K/V, 128-byte swizzled; an
-// INT2 unit is four bulk copies of codes and fp16 scale/min) and issues the
-// next units as soon as it has consumed one.
+// itself: lane 0 keeps three shared-memory stages in flight (a full-precision
+// unit is one 4-D TMA tile load of its K and V, 128-byte swizzled; a stage
+// takes up to five INT2 units, one bulk copy each of the unit's codes and
+// fp16 scale/min) and refills a stage as soon as it has consumed it.
 //
 // Per unit a warp computes the GQA query group's logits and P.V on the
 // tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulation):
@@ -29,6 +29,8 @@
 //  - PV: O^T[channel][head] += V^T[channel][token] . P^T[token][head]; P is
 //    split into bf16 hi + lo parts (two MMAs) so it keeps ~16 bits; for INT2
 //    the scale folds into P per group and the min term is a CUDA-core sum.
+//    (An fp16 P * scale with one MMA keeps only 11 bits: heavy-tailed V
+//    groups then miss a 2e-3 absolute bound.)
 //  The token order inside an INT2 unit is permuted (pairs t, t+8 share a
 //  32-bit code word) and the same permutation is used on both sides of each
 //  product, which leaves every sum unchanged.
@@ -48,15 +50,17 @@ namespace qevict {
 
 namespace {
 
-constexpr int kWarps = 4;                 // consumer warps per CTA
+constexpr int kWarps = 6;                 // consumer warps per CTA
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;                // shared-memory stages per warp
+constexpr int kStages = 2;                // shared-memory stages per warp
 constexpr int kStage = 8192;              // bytes per stage
 constexpr int kRing = kStages * kStage;   // bytes per warp
 constexpr int kFPUnit = 8192;             // 16 tokens x (K, V) x 256 B: one per stage
 constexpr int kQUnit = 1536;              // 16 tokens: K codes 512, K meta 256, V codes 512, V meta 256
 constexpr int kQPerStage = kStage / kQUnit;   // INT2 units batched into one stage (5)
+constexpr int kEntTab = 1024;             // window-list entries of a split cached in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazy = 8.f;              // log2 headroom before the running max moves
 constexpr long long kWaitCycles = 4000000000ll;   // about two seconds at GB300 clocks
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -65,14 +69,15 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// try_wait suspends the thread until the phase completes or about 20 us pass
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(20000u)
         : "memory");
     return ok != 0;
 }
@@ -88,11 +93,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int u,
+                                       uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(u), "r"(bar)
         : "memory");
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -129,14 +135,12 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
 }
-// hi = bf16(x), lo = bf16(x - hi) for a pair
+// hi = x truncated to bf16 (its top 16 bits), lo = bf16_rn(x - hi) for a pair:
+// hi + lo carries x to within 2^-16 relative.
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-    __nv_bfloat162 hv;
-    hv.x = h0;
-    hv.y = h1;
-    hi = *reinterpret_cast<uint32_t *>(&hv);
-    lo = pack2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+    const uint32_t u0 = __float_as_uint(x0), u1 = __float_as_uint(x1);
+    hi = __byte_perm(u0, u1, 0x7632);
+    lo = pack2(x0 - __uint_as_float(u0 & 0xffff0000u), x1 - __uint_as_float(u1 & 0xffff0000u));
 }
 __device__ __forceinline__ float2 h2f(uint32_t u) {
     const __half2 h = *reinterpret_cast<const __half2 *>(&u);
@@ -176,8 +180,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 128-byte-swizzled TMA tiles need 1024-byte aligned destinations
     uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    int2 *s_ent = reinterpret_cast<int2 *>(smem + kWarps * kRing);   // this split's {window, slot} list
+    // query A fragments per lane: [path (0 natural, 1 INT2 channel order)][k-step][lane] {a0, a2}
+    uint2 *s_qf = reinterpret_cast<uint2 *>(smem + kWarps * kRing + kEntTab * 8);
     __shared__ uint64_t bars[kWarps][kStages];
-    __shared__ int st_first[kWarps][kStages], st_n[kWarps][kStages];   // warp-local first unit, unit count
+    __shared__ int st_n[kWarps][kStages];                    // units in a stage
+    __shared__ int st_fp[kWarps][kStages];                   // 1: a full-precision unit
+    __shared__ int st_wi[kWarps][kStages][kQPerStage];       // window of each unit
+    __shared__ int st_j[kWarps][kStages][kQPerStage];        // 16-token unit index inside the window
+    __shared__ int st_nt[kWarps][kStages][kQPerStage];       // tokens in the unit
+    __shared__ int st_last[kWarps][kStages][kQPerStage];     // 1: the window's last unit
     __shared__ int s_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -198,78 +210,84 @@ __global__ void __launch_bounds__(kThreads, 2)
     const Range R = split_range(split, splits, n_fp, n_q);
     const int nfw = R.f1 - R.f0;                       // full-precision windows of this split
     const int nwin = nfw + (R.q1 - R.q0);              // windows of this split
-    const int nunits = nwin * mu;
-    const int lmu = mu == 1 ? 0 : mu == 2 ? 1 : mu == 4 ? 2 : mu == 8 ? 3 : 31 - __clz(mu);
     const uint32_t ring_s = smem_u32(smem + warp * kRing);
 
+    // ---- this split's windows: local index i (full-precision first, then INT2)
+    auto lentry = [&](int i) -> int2 {
+        return i < nfw ? D.fp_list[b * D.CF + R.f0 + i] : D.q_list[b * D.CQ + R.q0 + (i - nfw)];
+    };
+    for (int i = tid; i < min(nwin, kEntTab); i += kThreads) s_ent[i] = lentry(i);
     if (tid == 0) s_flag = 0;
     if (lane == 0)
         for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
+    auto ent = [&](int i) -> int2 { return i < kEntTab ? s_ent[i] : lentry(i); };
+    auto ntok_of = [&](int wi) -> int { return (wi == n_win - 1) ? (int)(length - (int64_t)wi * w) : w; };
 
-    // ---- unit bookkeeping (all lanes run it; lane 0 issues the copies). This
-    // warp takes units warp, warp + 4, ... of the CTA's run; a unit is the j-th
-    // 16-token slice of a window. A stage holds one full-precision unit or up to
-    // five consecutive INT2 units of the warp.
-    // local window index i -> global list entry e (full-precision entries first, then INT2)
-    auto gentry = [&](int i) -> int { return i < nfw ? R.f0 + i : n_fp + R.q0 + (i - nfw); };
-    auto entry = [&](int e) -> int2 { return e < n_fp ? D.fp_list[b * D.CF + e] : D.q_list[b * D.CQ + (e - n_fp)]; };
-    auto unit_tokens = [&](int wi, int j) -> int {
-        const int ntok = (wi == n_win - 1) ? (int)(length - (int64_t)wi * w) : w;
-        return min(16, ntok - 16 * j);
-    };
-    const int my_units = nunits > warp ? (nunits - warp + kWarps - 1) / kWarps : 0;
-    int next_unit = 0;               // next warp-local unit to put in a stage
-    int issued = 0, consumed = 0;    // stages issued / consumed so far
-    auto unit_e = [&](int k) { return gentry((warp + k * kWarps) >> lmu); };
-    auto unit_j = [&](int k) { return (warp + k * kWarps) & (mu - 1); };
+    // ---- issue bookkeeping (all lanes run it; lane 0 issues the copies). This
+    // warp takes windows warp, warp + kWarps, ... of the split, all units of a window
+    // in order. A stage holds one full-precision unit, or up to five 16-token
+    // tiles of INT2 windows (one bulk copy per window's run of tiles).
+    const int my_wins = nwin > warp ? (nwin - warp + kWarps - 1) / kWarps : 0;
+    int iw = 0, ij = 0;              // next (warp-local window, unit) to issue
+    int issued = 0, consumed = 0;    // stages issued / consumed
     auto try_issue = [&]() {
-        while (next_unit < my_units && issued - consumed < kStages) {
-            int e = unit_e(next_unit), j = unit_j(next_unit);
-            int2 ent = entry(e);
-            if (unit_tokens(ent.x, j) <= 0) {   // past the end of the open window
-                ++next_unit;
-                continue;
-            }
+        while (iw < my_wins && issued - consumed < kStages) {
+            const int li = warp + iw * kWarps;
             const int st = issued % kStages;
             const uint32_t bar = smem_u32(&bars[warp][st]);
             const uint32_t dst = ring_s + st * kStage;
-            if (e < n_fp) {
+            if (li < nfw) {
+                const int2 en = ent(li);
+                const int nt = ntok_of(en.x);
+                const int nu = (nt + 15) >> 4;   // units that hold tokens
                 if (lane == 0) {
-                    st_first[warp][st] = next_unit;
                     st_n[warp][st] = 1;
+                    st_fp[warp][st] = 1;
+                    st_wi[warp][st][0] = en.x;
+                    st_j[warp][st][0] = ij;
+                    st_nt[warp][st][0] = min(16, nt - 16 * ij);
+                    st_last[warp][st][0] = ij == nu - 1;
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     mbar_expect_tx(bar, (uint32_t)kFPUnit);
-                    const int row = ((ent.y * Hkv + kvh) * 2) * w + 16 * j;
-                    tma_2d(dst, &tmap, 0, row, bar);
-                    tma_2d(dst + 2048, &tmap, 64, row, bar);
-                    tma_2d(dst + 4096, &tmap, 0, row + w, bar);
-                    tma_2d(dst + 6144, &tmap, 64, row + w, bar);
+                    tma_4d(dst, &tmap, 0, 16 * ij, 0, en.y * Hkv + kvh, bar);
                 }
-                ++next_unit;
+                if (++ij == nu) {
+                    ij = 0;
+                    ++iw;
+                }
             } else {
-                // INT2 windows come after every full-precision one and are always full
-                const int n = min(kQPerStage, my_units - next_unit);
+                // every later window of this warp is INT2 and full (mu tiles)
+                const int n = min(kQPerStage, (mu - ij) + (my_wins - iw - 1) * mu);
                 if (lane == 0) {
-                    st_first[warp][st] = next_unit;
                     st_n[warp][st] = n;
+                    st_fp[warp][st] = 0;
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     mbar_expect_tx(bar, (uint32_t)(n * kQUnit));
-                    for (int i = 0; i < n; ++i) {
-                        const int2 en = entry(unit_e(next_unit + i));
-                        const int jj = unit_j(next_unit + i);
-                        const uint8_t *kp =
-                            D.lg_pool + (int64_t)en.y * D.lg_slot_bytes + (int64_t)(kvh * 2) * lg_part_bytes(w);
-                        const uint8_t *vp = kp + lg_part_bytes(w);
-                        const uint32_t d = dst + i * kQUnit;
-                        bulk_g2s(d, kp + 16 * jj * 32, 512, bar);
-                        bulk_g2s(d + 512, kp + lg_codes_bytes(w) + 16 * jj * 16, 256, bar);
-                        bulk_g2s(d + 768, vp + jj * 512, 512, bar);
-                        bulk_g2s(d + 1280, vp + lg_codes_bytes(w) + 16 * jj * 16, 256, bar);
+                }
+                int done = 0;
+                while (done < n) {
+                    const int2 en = ent(warp + iw * kWarps);
+                    const int run = min(mu - ij, n - done);
+                    if (lane == 0) {
+                        for (int r = 0; r < run; ++r) {
+                            st_wi[warp][st][done + r] = en.x;
+                            st_j[warp][st][done + r] = ij + r;
+                            st_nt[warp][st][done + r] = 16;
+                            st_last[warp][st][done + r] = ij + r == mu - 1;
+                        }
+                        bulk_g2s(dst + done * kQUnit,
+                                 D.lg_pool + (int64_t)en.y * D.lg_slot_bytes + lg_tile_off(kvh, w, ij),
+                                 (uint32_t)(run * kQUnit), bar);
+                    }
+                    done += run;
+                    ij += run;
+                    if (ij == mu) {
+                        ij = 0;
+                        ++iw;
                     }
                 }
-                next_unit += n;
             }
             ++issued;
         }
@@ -283,7 +301,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     // ---- query fragments (A operand: G heads as rows, rest zero)
     const uint32_t *qw =
         reinterpret_cast<const uint32_t *>(q + ((int64_t)b * Hq + kvh * G + (g < G ? g : 0)) * kHeadDim);
-    uint32_t Af0[8], Af2[8], Aq0[8], Aq2[8];
     float qsum[kGroups] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
@@ -292,14 +309,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             lo = qw[(16 * ks + 2 * t) / 2];
             hi = qw[(16 * ks + 2 * t + 8) / 2];
         }
-        Af0[ks] = lo;
-        Af2[ks] = hi;
-        Aq0[ks] = (lo & 0xffffu) | (hi << 16);       // channels 2t, 2t+8
-        Aq2[ks] = (lo >> 16) | (hi & 0xffff0000u);   // channels 2t+1, 2t+9
+        if (warp == 0) {
+            s_qf[ks * 32 + lane] = make_uint2(lo, hi);
+            s_qf[(8 + ks) * 32 + lane] = make_uint2((lo & 0xffffu) | (hi << 16),       // channels 2t, 2t+8
+                                                    (lo >> 16) | (hi & 0xffff0000u));  // channels 2t+1, 2t+9
+        }
         const float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&lo));
         const float2 c = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&hi));
         qsum[ks >> 1] += (a.x + a.y) + (c.x + c.y);
     }
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < kGroups; ++i) {
         qsum[i] += __shfl_xor_sync(0xffffffffu, qsum[i], 1);
@@ -308,39 +327,39 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float qk_scale = kLog2e * rsqrtf((float)kHeadDim);
 
     // ---- per-warp online softmax state (lane: head g for m/l, heads 2t, 2t+1 in O)
-    float m_run = -INFINITY, l_run = 0.f;
+    float m_run = -INFINITY, l_part = 0.f, w_part = 0.f;
     float o[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float minacc[kGroups] = {0.f, 0.f, 0.f, 0.f};
-    float2 *ustat = S.ustat + ((int64_t)b * Hq + kvh * G) * ((int64_t)D.Wmax * mu);
+    float2 *wstat = S.wstat + ((int64_t)b * Hq + kvh * G) * D.Wmax;
 
     // ldmatrix row addressing (same for K and V tiles): token and 8-channel half of this lane's row
     const int lm_tok = ((lane >> 4) << 3) + (lane & 7);
     const int lm_hi = (lane >> 3) & 1;
 
     // online-softmax update with 4 logits of head g (masked ones -inf); turns x into P
-    auto softmax4 = [&](float (&x)[4], float2 &ust) {
-        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = exp2f(m_run - m_new);
-        const float beta = exp2f(mx - m_new);
-        float e[4], es = 0.f;
+    // Online softmax, lazily rescaled: lanes keep partial exp-sums over their own
+    // tokens (l_part for the whole run, w_part for the window in progress), both
+    // relative to the head's running max m_run, which moves (with a rescale of
+    // O, the partial sums and the min accumulators) only when a logit passes it
+    // by more than 2^8. Turns the 4 logits of head g in x (masked ones -inf)
+    // into P.
+    auto softmax4 = [&](float (&x)[4]) {
+        const float lmx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        if (__any_sync(0xffffffffu, lmx > m_run + kLazy)) {
+            float hmx = fmaxf(lmx, __shfl_xor_sync(0xffffffffu, lmx, 1));
+            hmx = fmaxf(hmx, __shfl_xor_sync(0xffffffffu, hmx, 2));
+            const float m_new = fmaxf(m_run, hmx);
+            const float alpha = exp2f(m_run - m_new);
+            m_run = m_new;
+            l_part *= alpha;
+            w_part *= alpha;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            e[i] = exp2f(x[i] - mx);
-            es += e[i];
-        }
-        es += __shfl_xor_sync(0xffffffffu, es, 1);
-        es += __shfl_xor_sync(0xffffffffu, es, 2);
-        ust = make_float2(mx, es);
-        l_run = l_run * alpha + es * beta;
-        m_run = m_new;
-        const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * t);
-        const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
-        if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
+            for (int i = 0; i < kGroups; ++i) minacc[i] *= alpha;
+            // O columns are heads 2t, 2t+1, whose alphas live in lanes 8t and 8t+4
+            const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * t);
+            const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * t + 4);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 o[i][0] *= a_lo;
@@ -349,10 +368,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                 o[i][3] *= a_hi;
             }
         }
+        float es = 0.f;
 #pragma unroll
-        for (int i = 0; i < kGroups; ++i) minacc[i] *= alpha;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[i] = (g < G) ? e[i] * beta : 0.f;
+        for (int i = 0; i < 4; ++i) {
+            const float e = exp2f(x[i] - m_run);
+            es += e;
+            x[i] = (g < G) ? e : 0.f;
+        }
+        l_part += es;
+        w_part += es;
     };
 
     while (consumed < issued) {
@@ -367,15 +391,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
         }
         __syncwarp();
-        const int first = st_first[warp][st], nb = st_n[warp][st];
+        const int nb = st_n[warp][st];
+        const bool is_fp = st_fp[warp][st] != 0;
         for (int ib = 0; ib < nb; ++ib) {
-        const int k = first + ib;
-        const int e = unit_e(k), j = unit_j(k);
-        const int wi = entry(e).x;
-        const int ntu = unit_tokens(wi, j);
+        const int wi = st_wi[warp][st][ib], ntu = st_nt[warp][st][ib];
+        const bool last = st_last[warp][st][ib] != 0;
         const uint32_t base = ring_s + st * kStage + ib * kQUnit;
-        float2 ust;
-        if (e < n_fp) {
+        if (is_fp) {
             // ---------------- full-precision unit
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -384,8 +406,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t addr = base + (ks >> 2) * 2048 + lm_tok * 128 + ((chunk ^ (lm_tok & 7)) << 4);
                 uint32_t b00, b01, b10, b11;
                 ldsm_x4(addr, b00, b01, b10, b11);
-                mma(s0, Af0[ks], 0u, Af2[ks], 0u, b00, b01);
-                mma(s1, Af0[ks], 0u, Af2[ks], 0u, b10, b11);
+                const uint2 af = s_qf[ks * 32 + lane];
+                mma(s0, af.x, 0u, af.y, 0u, b00, b01);
+                mma(s1, af.x, 0u, af.y, 0u, b10, b11);
             }
             float x[4] = {s0[0] * qk_scale, s0[1] * qk_scale, s1[0] * qk_scale, s1[1] * qk_scale};
             if (ntu < 16) {
@@ -404,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (8 + 2 * t >= ntu) x[2] = -INFINITY;
                 if (9 + 2 * t >= ntu) x[3] = -INFINITY;
             }
-            softmax4(x, ust);
+            softmax4(x);
             uint32_t b0h, b0l, b1h, b1l;
             split2(x[0], x[1], b0h, b0l);
             split2(x[2], x[3], b1h, b1l);
@@ -440,8 +463,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int ks = 2 * grp + kk;
                     const uint32_t xa = pick(ks < 4 ? kA0 : kA1, ks & 3) >> (4 * t);
                     const uint32_t xb = pick(ks < 4 ? kB0 : kB1, ks & 3) >> (4 * t);
-                    mma(c0, Aq0[ks], 0u, Aq2[ks], 0u, codes2(xa), codes2(xa >> 2));
-                    mma(c1, Aq0[ks], 0u, Aq2[ks], 0u, codes2(xb), codes2(xb >> 2));
+                    const uint2 aq = s_qf[(8 + ks) * 32 + lane];
+                    mma(c0, aq.x, 0u, aq.y, 0u, codes2(xa), codes2(xa >> 2));
+                    mma(c1, aq.x, 0u, aq.y, 0u, codes2(xb), codes2(xb >> 2));
                 }
                 const float acc[4] = {c0[0], c0[1], c1[0], c1[1]};
 #pragma unroll
@@ -452,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) x[i] *= qk_scale;
-            softmax4(x, ust);
+            softmax4(x);
             uint4 vmeta[4];
             vmeta[0] = lds128(vm + (2 * t) * 16);
             vmeta[1] = lds128(vm + (2 * t + 8) * 16);
@@ -484,7 +508,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
-        if (t == 0 && g < G) ustat[(int64_t)g * D.Wmax * mu + (int64_t)wi * mu + j] = ust;
+        if (last) {   // the window is complete: (reference max, exp-sum over its tokens) for head g
+            float ws = w_part + __shfl_xor_sync(0xffffffffu, w_part, 1);
+            ws += __shfl_xor_sync(0xffffffffu, ws, 2);
+            if (t == 0 && g < G) wstat[(int64_t)g * D.Wmax + wi] = make_float2(m_run, ws);
+            w_part = 0.f;
+        }
         }
         __syncwarp();
         ++consumed;
@@ -512,48 +541,35 @@ __global__ void __launch_bounds__(kThreads, 2)
         minacc[i] += __shfl_xor_sync(0xffffffffu, minacc[i], 1);
         minacc[i] += __shfl_xor_sync(0xffffffffu, minacc[i], 2);
     }
+    l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
+    l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
     if (t == 0) {
         mw_s[warp * 8 + g] = m_run;
-        lw_s[warp * 8 + g] = l_run;
+        lw_s[warp * 8 + g] = l_part;
 #pragma unroll
         for (int i = 0; i < kGroups; ++i) minw[(warp * 8 + g) * 4 + i] = minacc[i];
     }
     __syncthreads();
-    float *part = S.part + ((int64_t)bk * kMaxSplits + split) * G * (2 + kHeadDim);
+    float *pacc = S.part + ((int64_t)bk * kMaxSplits + split) * G * kHeadDim;
+    float2 *pml = S.part_ml + ((int64_t)bk * kMaxSplits + split) * G;
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
         float M = -INFINITY;
 #pragma unroll
         for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + hh]);
-        float acc = 0.f, l = 0.f;
-        if (M != -INFINITY) {
+        if (tid < kHeadDim) {
+            float acc = 0.f, l = 0.f;
+            if (M != -INFINITY) {
 #pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) {
-                const float f = exp2f(mw_s[ww * 8 + hh] - M);
-                acc += f * (Ow[(ww * 8 + hh) * kHeadDim + tid] + minw[(ww * 8 + hh) * 4 + tid / kGroup]);
-                l += f * lw_s[ww * 8 + hh];
+                for (int ww = 0; ww < kWarps; ++ww) {
+                    const float f = exp2f(mw_s[ww * 8 + hh] - M);
+                    acc += f * (Ow[(ww * 8 + hh) * kHeadDim + tid] + minw[(ww * 8 + hh) * 4 + tid / kGroup]);
+                    l += f * lw_s[ww * 8 + hh];
+                }
             }
+            pacc[hh * kHeadDim + tid] = acc;
+            if (tid == 0) pml[hh] = make_float2(M, l);
         }
-        part[hh * (2 + kHeadDim) + 2 + tid] = acc;
-        if (tid == 0) {
-            part[hh * (2 + kHeadDim)] = M;
-            part[hh * (2 + kHeadDim) + 1] = l;
-        }
-    }
-    // per-window statistics from the unit records of this split
-    float2 *wstat = S.wstat + ((int64_t)b * Hq + kvh * G) * D.Wmax;
-    for (int i = tid; i < nwin * G; i += kThreads) {
-        const int e = gentry(i / G), hh = i % G;
-        const int wi = entry(e).x;
-        const float2 *us = ustat + (int64_t)hh * D.Wmax * mu + (int64_t)wi * mu;
-        float2 v[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            v[jj] = (jj < mu && unit_tokens(wi, jj) > 0) ? __ldcg(us + jj) : make_float2(-INFINITY, 0.f);
-        float2 st = v[0];
-#pragma unroll
-        for (int jj = 1; jj < 8; ++jj) st = stat_merge(st, v[jj]);
-        wstat[(int64_t)hh * D.Wmax + wi] = st;
     }
     __threadfence();
     __syncthreads();
@@ -573,10 +589,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *hIL = hM + 8;                                          // [G] 1 / L
     float *hNew = hIL + 8;                                        // [G] new-token logit
     float *hFN = hNew + 8;                                        // [G] new-token factor
-    const float *pb = S.part + (int64_t)bk * kMaxSplits * G * (2 + kHeadDim);
+    const float2 *ml = S.part_ml + (int64_t)bk * kMaxSplits * G;
+    // the splits' partial outputs, one bulk copy into shared memory when they fit
+    float *sAcc = hFN + 8;                                        // [splits][G][128]
+    const uint32_t acc_bytes = (uint32_t)splits * G * kHeadDim * 4;
+    const bool bulk_acc = (uint8_t *)sAcc + acc_bytes <= smem + kWarps * kRing;
+    const uint32_t tbar = smem_u32(&bars[0][0]);
+    if (bulk_acc && tid == 0) {
+        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tbar) : "memory");
+        mbar_init(tbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async;" ::: "memory");   // generic writes of the other splits -> bulk read
+        mbar_expect_tx(tbar, acc_bytes);
+        bulk_g2s(smem_u32(sAcc), S.part + (int64_t)bk * kMaxSplits * G * kHeadDim, acc_bytes, tbar);
+    }
     for (int i = tid; i < splits * G; i += kThreads) {
-        sM[i] = __ldcg(pb + (int64_t)i * (2 + kHeadDim));
-        sL[i] = __ldcg(pb + (int64_t)i * (2 + kHeadDim) + 1);
+        const float2 v = __ldcg(ml + i);
+        sM[i] = v.x;
+        sL[i] = v.y;
     }
     const bool has_new = knew != nullptr;
     const __nv_bfloat16 *kn = has_new ? knew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
@@ -610,27 +640,63 @@ __global__ void __launch_bounds__(kThreads, 2)
         hFN[tid] = fn;
     }
     __syncthreads();
-    {
-        float acc[G];
-        const float vnv = has_new ? __bfloat162float(vn[tid]) : 0.f;
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) acc[hh] = hFN[hh] * vnv;
-        for (int s0 = 0; s0 < splits; s0 += 8) {
-            float v[8][G];
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh)
-                    v[s][hh] = s0 + s < splits ? __ldcg(pb + ((int64_t)(s0 + s) * G + hh) * (2 + kHeadDim) + 2 + tid)
-                                               : 0.f;
-#pragma unroll
-            for (int s = 0; s < 8; ++s)
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh)
-                    if (s0 + s < splits) acc[hh] = fmaf(sF[(s0 + s) * G + hh], v[s][hh], acc[hh]);
+    // output: each thread owns 4 channels of one head
+    if (bulk_acc) {
+        bool ok = true;
+        if (tid == 0) ok = mbar_wait(tbar, 0);
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -2);
         }
+        const float4 *pa = reinterpret_cast<const float4 *>(sAcc);
+        for (int oi = tid; oi < G * (kHeadDim / 4); oi += kThreads) {
+            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has_new) {
+                const float fn = hFN[hh];
+                acc = make_float4(fn * __bfloat162float(vn[4 * c4]), fn * __bfloat162float(vn[4 * c4 + 1]),
+                                  fn * __bfloat162float(vn[4 * c4 + 2]), fn * __bfloat162float(vn[4 * c4 + 3]));
+            }
+            for (int s = 0; s < splits; ++s) {
+                const float f = sF[s * G + hh];
+                const float4 v = pa[(s * G + hh) * (kHeadDim / 4) + c4];
+                acc.x = fmaf(f, v.x, acc.x);
+                acc.y = fmaf(f, v.y, acc.y);
+                acc.z = fmaf(f, v.z, acc.z);
+                acc.w = fmaf(f, v.w, acc.w);
+            }
+            const float il = hIL[hh];
+            reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
+                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        }
+    } else {
+        const float4 *pa = reinterpret_cast<const float4 *>(S.part + (int64_t)bk * kMaxSplits * G * kHeadDim);
+        for (int oi = tid; oi < G * (kHeadDim / 4); oi += kThreads) {
+            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has_new) {
+                const float fn = hFN[hh];
+                acc = make_float4(fn * __bfloat162float(vn[4 * c4]), fn * __bfloat162float(vn[4 * c4 + 1]),
+                                  fn * __bfloat162float(vn[4 * c4 + 2]), fn * __bfloat162float(vn[4 * c4 + 3]));
+            }
+            for (int s0 = 0; s0 < splits; s0 += 16) {
+                float4 v[16];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) out[((int64_t)b * Hq + kvh * G + hh) * kHeadDim + tid] = acc[hh] * hIL[hh];
+                for (int s = 0; s < 16; ++s)
+                    v[s] = s0 + s < splits ? __ldcg(pa + ((int64_t)(s0 + s) * G + hh) * (kHeadDim / 4) + c4)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int s = 0; s < 16; ++s) {
+                    const float f = s0 + s < splits ? sF[(s0 + s) * G + hh] : 0.f;
+                    acc.x = fmaf(f, v[s].x, acc.x);
+                    acc.y = fmaf(f, v[s].y, acc.y);
+                    acc.z = fmaf(f, v[s].z, acc.z);
+                    acc.w = fmaf(f, v[s].w, acc.w);
+                }
+            }
+            const float il = hIL[hh];
+            reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
+                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        }
     }
 
     // ---- masses and the cumulative score; the new token counts in its window
@@ -680,9 +746,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int row = (int)(length % w);
             const int kv = tid >> 4, c = tid & 15;
             const __nv_bfloat16 *src = kv ? vn : kn;
-            uint8_t *dst =
-                D.fp_pool + (int64_t)slot * D.fp_slot_bytes + (((int64_t)(kvh * 2 + kv) * w + row) * kHeadDim) * 2;
-            reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)slot * D.fp_slot_bytes) +
+                                 fp_off(kvh, kv, w, row, 8 * c);
+            *reinterpret_cast<uint4 *>(dst) = reinterpret_cast<const uint4 *>(src)[c];
         }
         __threadfence();
         __syncthreads();
@@ -721,13 +787,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0) S.arrive[bk] = 0u;
 }
 
+// CTAs of decode_kernel<G> that fit on one SM, filled in by prepare_decode.
+int g_ctas_per_sm[kMaxG + 1];
+
+constexpr int kDynSmem = kWarps * kRing + kEntTab * 8 + 16 * 32 * 8 + 1024;
+
 template <int G>
-cudaError_t raise_smem_limit(int optin) {
+cudaError_t raise_smem_limit(int optin, int *ctas_per_sm) {
     cudaFuncAttributes fa{};
     cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<G>);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                optin - (int)fa.sharedSizeBytes);
+    e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)fa.sharedSizeBytes);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_kernel<G>, kThreads, kDynSmem);
 }
 
 }  // namespace
@@ -740,21 +813,22 @@ cudaError_t prepare_decode() {
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess) e = raise_smem_limit<1>(optin);
-    if (e == cudaSuccess) e = raise_smem_limit<2>(optin);
-    if (e == cudaSuccess) e = raise_smem_limit<3>(optin);
-    if (e == cudaSuccess) e = raise_smem_limit<4>(optin);
-    if (e == cudaSuccess) e = raise_smem_limit<5>(optin);
-    if (e == cudaSuccess) e = raise_smem_limit<6>(optin);
-    if (e == cudaSuccess) e = raise_smem_limit<7>(optin);
-    if (e == cudaSuccess) e = raise_smem_limit<8>(optin);
+    if (e == cudaSuccess) e = raise_smem_limit<1>(optin, &g_ctas_per_sm[1]);
+    if (e == cudaSuccess) e = raise_smem_limit<2>(optin, &g_ctas_per_sm[2]);
+    if (e == cudaSuccess) e = raise_smem_limit<3>(optin, &g_ctas_per_sm[3]);
+    if (e == cudaSuccess) e = raise_smem_limit<4>(optin, &g_ctas_per_sm[4]);
+    if (e == cudaSuccess) e = raise_smem_limit<5>(optin, &g_ctas_per_sm[5]);
+    if (e == cudaSuccess) e = raise_smem_limit<6>(optin, &g_ctas_per_sm[6]);
+    if (e == cudaSuccess) e = raise_smem_limit<7>(optin, &g_ctas_per_sm[7]);
+    if (e == cudaSuccess) e = raise_smem_limit<8>(optin, &g_ctas_per_sm[8]);
     if (e == cudaSuccess) done = true;
     return e;
 }
 
-// Splits per (sequence, KV head): about two CTAs per SM in one wave.
-int decode_splits(int pairs, int num_sms) {
-    int s = (2 * num_sms + pairs - 1) / pairs;
+// Splits per (sequence, KV head): one wave of as many CTAs as fit on the SMs.
+int decode_splits(int pairs, int num_sms, int G) {
+    const int per_sm = (G >= 1 && G <= kMaxG && g_ctas_per_sm[G] > 0) ? g_ctas_per_sm[G] : 1;
+    int s = (per_sm * num_sms + pairs - 1) / pairs;
     if (s > kMaxSplits) s = kMaxSplits;
     if (s < 1) s = 1;
     return s;
@@ -766,7 +840,7 @@ cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScra
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(splits, L.B * L.Hkv);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kWarps * kRing + 1024;
+    cfg.dynamicSmemBytes = kDynSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

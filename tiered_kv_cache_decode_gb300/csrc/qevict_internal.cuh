@@ -28,11 +28,20 @@ enum { CTR_NFP = 0, CTR_NQ = 1, CTR_FP_TOP = 2, CTR_LG_TOP = 3, CTR_WQ = 4, CTR_
 // device stats slots
 enum { ST_DEMOTE = 0, ST_PROMOTE = 1, ST_EVICT = 2, ST_LWRITE = 3, ST_LREUSE = 4, ST_N = 8 };
 
-// Bytes of one INT2 part (one KV head, K or V) of a ledger window.
-__host__ __device__ inline int64_t lg_part_bytes(int w) {
-    return (int64_t)w * (kHeadDim / 4) + (int64_t)w * kGroups * 4;
+// Full-precision slot: bf16 [Hkv][2 (K, V)][2 (channels 0-63, 64-127)][w][64].
+// Element offset of channel c of token t of (KV head kvh, K or V).
+__host__ __device__ inline int64_t fp_off(int kvh, int kv, int w, int t, int c) {
+    return ((((int64_t)(kvh * 2 + kv) * 2 + (c >> 6)) * w + t) * 64) + (c & 63);
 }
-__host__ __device__ inline int64_t lg_codes_bytes(int w) { return (int64_t)w * (kHeadDim / 4); }
+
+// Ledger slot: per KV head, w / 16 tiles of 16 tokens, each tile kQTile bytes:
+// K codes [16][32 B] at 0, K meta [16][4] half2 at 512, V codes (128 words) at
+// 768, V meta [16][4] half2 at 1280.
+constexpr int kQTile = 1536;
+constexpr int kTileKMeta = 512, kTileVCodes = 768, kTileVMeta = 1280;
+__host__ __device__ inline int64_t lg_tile_off(int kvh, int w, int tile) {
+    return ((int64_t)kvh * (w / 16) + tile) * kQTile;
+}
 
 // V codes of a 16-token tile are 128 uint32 words, word i = (g * 8 + mt) * 2 + h
 // holding channel 16 * mt + g + 8 * h (g, mt in 0..7, h in 0..1). This puts the
@@ -53,8 +62,8 @@ struct LayerDev {
     double beta, rho;           // budget fraction and its full-precision share
     int64_t c_fp, c_q;          // bytes of one window per sequence in each visible tier
     int64_t fp_slot_bytes, lg_slot_bytes;
-    uint8_t *fp_pool;     // [B*CF][fp_slot_bytes]   bf16 [Hkv][2][w][d]
-    uint8_t *lg_pool;     // [B*CQ][lg_slot_bytes]   parts [Hkv][2]
+    uint8_t *fp_pool;     // [B*CF][fp_slot_bytes]   see fp_off
+    uint8_t *lg_pool;     // [B*CQ][lg_slot_bytes]   see lg_tile_off
     uint8_t *tier;        // [B][Wmax]
     int32_t *fp_slot;     // [B][Wmax]
     int32_t *lg_slot;     // [B][Wmax]
@@ -73,9 +82,9 @@ struct LayerDev {
 // Decode scratch, shared by all layers of a cache: a decode launch touches it
 // only after its dependency wait, so consecutive launches never overlap in it.
 struct DecodeScratch {
-    float *part;          // [B*Hkv][kMaxSplits][G][2 + d] split partials (max, sum, acc)
+    float *part;          // [B*Hkv][kMaxSplits][G][d] split partial outputs
+    float2 *part_ml;      // [B*Hkv][kMaxSplits][G] split (max, exp-sum), log2 domain
     float2 *wstat;        // [B][Hq][Wmax] (window max, window exp-sum), log2 domain
-    float2 *ustat;        // [B][Hq][Wmax][w/16] the same per 16-token unit
     uint32_t *arrive;     // [B*Hkv] split arrival counters (kept at 0 between launches)
     uint32_t *arrive_b;   // [B] KV-head arrival counters for the fused append
 };
@@ -116,7 +125,7 @@ cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScra
                           int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
                           float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s);
 cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s);
-int decode_splits(int pairs, int num_sms);
+int decode_splits(int pairs, int num_sms, int G);
 cudaError_t prepare_decode();
 
 // ---- device helpers -------------------------------------------------------

@@ -114,9 +114,9 @@ __global__ void append_kernel(LayerDev D, CacheDev C, int layer, const __nv_bflo
         const int slot = D.fp_slot[wb + wi];
         if (slot < 0) continue;
         const __nv_bfloat16 *src = (kv ? v : k) + (((int64_t)b * n_new + t) * D.Hkv + h) * kHeadDim;
-        uint8_t *dst = D.fp_pool + (int64_t)slot * D.fp_slot_bytes +
-                       (((int64_t)(h * 2 + kv) * w + row) * kHeadDim) * 2;
-        reinterpret_cast<uint4 *>(dst)[c] = reinterpret_cast<const uint4 *>(src)[c];
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)slot * D.fp_slot_bytes) +
+                             fp_off(h, kv, w, row, 8 * c);
+        *reinterpret_cast<uint4 *>(dst) = reinterpret_cast<const uint4 *>(src)[c];
     }
 }
 
@@ -520,14 +520,13 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int4 job = D.work_q[(int64_t)b * D.Wmax + e];
         const int wi = job.x, src_slot = job.y, dst = job.z;
-        uint8_t *part = D.lg_pool + (int64_t)dst * D.lg_slot_bytes + (int64_t)(h * 2 + kv) * lg_part_bytes(w);
-        __half2 *meta = reinterpret_cast<__half2 *>(part + lg_codes_bytes(w));
+        uint8_t *slotp = D.lg_pool + (int64_t)dst * D.lg_slot_bytes;
         for (int it = threadIdx.x; it < w * kGroups; it += blockDim.x) {
             const int t = it / kGroups, g = it % kGroups;
             const __nv_bfloat16 *src;
             if (src_slot >= 0) {
                 src = reinterpret_cast<const __nv_bfloat16 *>(D.fp_pool + (int64_t)src_slot * D.fp_slot_bytes) +
-                      ((int64_t)(h * 2 + kv) * w + t) * kHeadDim + g * kGroup;
+                      fp_off(h, kv, w, t, g * kGroup);
             } else {
                 src = (kv ? v_ext : k_ext) + (((int64_t)b * ext_len + (int64_t)wi * w + t) * D.Hkv + h) * kHeadDim +
                       g * kGroup;
@@ -565,20 +564,21 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
                 c = fminf(fmaxf(c, 0.f), 3.f);
                 cs[j] = (uint8_t)c;
             }
-            meta[t * kGroups + g] = bad ? __halves2half2(__float2half_rn(0.f), __float2half_rn(0.f))
-                                        : __halves2half2(s16, mn16);
+            __half2 *meta = reinterpret_cast<__half2 *>(slotp + lg_tile_off(h, w, t / 16) +
+                                                        (kv ? kTileVMeta : kTileKMeta)) +
+                            (t % 16) * kGroups + g;
+            *meta = bad ? __halves2half2(__float2half_rn(0.f), __float2half_rn(0.f)) : __halves2half2(s16, mn16);
         }
         __syncthreads();
-        uint32_t *words = reinterpret_cast<uint32_t *>(part);
         if (kv == 0) {
-            // K: [token][d/4] bytes, channel j in byte j/4 at bits 2*(j%4); 16 channels per word
+            // K: per token 8 words of 16 channels, channel j of the word at bits 2*(j%16)
             for (int i = threadIdx.x; i < w * (kHeadDim / 16); i += blockDim.x) {
                 const int t = i / (kHeadDim / 16), q = i % (kHeadDim / 16);
                 const uint8_t *cs = s_codes + t * kHeadDim + q * 16;
                 uint32_t word = 0;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) word |= (uint32_t)cs[j] << (2 * j);
-                words[i] = word;
+                reinterpret_cast<uint32_t *>(slotp + lg_tile_off(h, w, t / 16))[(t % 16) * 8 + q] = word;
             }
         } else {
             // V: per 16-token tile 128 words; word i holds channel vword_dim(i), token t of
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
                 uint32_t word = 0;
 #pragma unroll
                 for (int t = 0; t < kVTile; ++t) word |= (uint32_t)s_codes[(tile * kVTile + t) * kHeadDim + j] << (2 * t);
-                words[i] = word;
+                reinterpret_cast<uint32_t *>(slotp + lg_tile_off(h, w, tile) + kTileVCodes)[i % kHeadDim] = word;
             }
         }
         __syncthreads();
@@ -604,25 +604,24 @@ __global__ void __launch_bounds__(128) promote_kernel(LayerDev D) {
     const int n = D.ctr[b * kCtrN + CTR_WP];
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int4 job = D.work_p[(int64_t)b * D.Wmax + e];
-        const uint8_t *part = D.lg_pool + (int64_t)job.y * D.lg_slot_bytes + (int64_t)(h * 2 + kv) * lg_part_bytes(w);
-        const uint32_t *words = reinterpret_cast<const uint32_t *>(part);
-        const __half2 *meta = reinterpret_cast<const __half2 *>(part + lg_codes_bytes(w));
-        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)job.z * D.fp_slot_bytes) +
-                             (int64_t)(h * 2 + kv) * w * kHeadDim;
+        const uint8_t *slotp = D.lg_pool + (int64_t)job.y * D.lg_slot_bytes;
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)job.z * D.fp_slot_bytes);
         for (int it = threadIdx.x; it < w * kGroups; it += blockDim.x) {
             const int t = it / kGroups, g = it % kGroups;
-            const __half2 m2 = meta[t * kGroups + g];
+            const uint8_t *tile = slotp + lg_tile_off(h, w, t / 16);
+            const uint32_t *words = reinterpret_cast<const uint32_t *>(tile + (kv ? kTileVCodes : 0));
+            const __half2 m2 = reinterpret_cast<const __half2 *>(tile + (kv ? kTileVMeta : kTileKMeta))[(t % 16) * kGroups + g];
             const float s = __low2float(m2), mn = __high2float(m2);
             __align__(16) __nv_bfloat16 outv[kGroup];
 #pragma unroll
             for (int j = 0; j < kGroup; ++j) {
                 const int ch = g * kGroup + j;
                 uint32_t c;
-                if (kv == 0) c = (words[t * (kHeadDim / 16) + ch / 16] >> (2 * (ch % 16))) & 3u;
-                else c = (words[(t / kVTile) * kHeadDim + vword_index(ch)] >> (2 * (t % kVTile))) & 3u;
+                if (kv == 0) c = (words[(t % 16) * 8 + ch / 16] >> (2 * (ch % 16))) & 3u;
+                else c = (words[vword_index(ch)] >> (2 * (t % kVTile))) & 3u;
                 outv[j] = __float2bfloat16_rn(fmaf((float)c, s, mn));
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + (int64_t)t * kHeadDim + g * kGroup);
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst + fp_off(h, kv, w, t, g * kGroup));
             const uint4 *s4 = reinterpret_cast<const uint4 *>(outv);
 #pragma unroll
             for (int c = 0; c < 4; ++c) d4[c] = s4[c];
@@ -643,12 +642,12 @@ __global__ void __launch_bounds__(128) prefill_copy_kernel(LayerDev D, const __n
         const int4 job = D.work_c[(int64_t)b * D.Wmax + e];
         const int wi = job.x;
         const int ntok = (int)min((int64_t)w, ext_len - (int64_t)wi * w);
-        uint8_t *dst = D.fp_pool + (int64_t)job.y * D.fp_slot_bytes + (int64_t)(h * 2 + kv) * w * kHeadDim * 2;
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)job.y * D.fp_slot_bytes);
         const __nv_bfloat16 *srcb = kv ? v_ext : k_ext;
         for (int i = threadIdx.x; i < ntok * kChunks; i += blockDim.x) {
             const int t = i / kChunks, c = i % kChunks;
             const __nv_bfloat16 *src = srcb + (((int64_t)b * ext_len + (int64_t)wi * w + t) * D.Hkv + h) * kHeadDim;
-            reinterpret_cast<uint4 *>(dst + (int64_t)t * kHeadDim * 2)[c] = reinterpret_cast<const uint4 *>(src)[c];
+            *reinterpret_cast<uint4 *>(dst + fp_off(h, kv, w, t, 8 * c)) = reinterpret_cast<const uint4 *>(src)[c];
         }
     }
 }
