@@ -306,6 +306,39 @@ qevict_status qevict_refresh_lengths(qevict_cache *cache, void *stream);
 /* Current context length of a layer (host copy), or -1 for a bad layer. */
 int64_t qevict_length(const qevict_cache *cache, int32_t layer);
 
+/* Bytes of device scratch that qevict_decode_attention_static_scratch can
+ * use: 4 MiB, one array per device, owned by the library. */
+#define QEVICT_STATIC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/* qevict_decode_attention with the kernel's per-call scratch taken from a
+ * fixed 4 MiB device array that the library holds, instead of the scratch
+ * block the cache drew from its allocator. The call allocates nothing: no
+ * cudaMalloc, no allocator callback, no library routine that allocates.
+ * The QEvict pages have no counterpart of this call; it exists for callers
+ * that cannot reach an allocator when they decode, for example an engine
+ * that has handed all free device memory to its own pools after set-up, or
+ * a host thread that must not block on an allocator's lock.
+ *
+ * Arguments, outputs and errors are those of qevict_decode_attention.
+ * The scratch a call needs grows with batch x Hkv x (Hq / Hkv) (split
+ * partials, 64 splits of 512 B per query head) and batch x Hq x the window
+ * count (window statistics); a cache whose need passes
+ * QEVICT_STATIC_SCRATCH_BYTES is rejected with INVALID_ARG before anything
+ * is enqueued, and the error text gives both sizes. The cache's device must
+ * be current (INVALID_ARG otherwise).
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's address and clears it (the split arrival counters in it must start
+ * at zero; each launch leaves them at zero). That first call synchronises
+ * the device, so make it before any stream capture begins.
+ *
+ * One array serves every cache and stream on a device: calls whose kernels
+ * can overlap (other streams, other host threads, other caches) race on it
+ * and give wrong results. Order them on one stream or by events. */
+qevict_status qevict_decode_attention_static_scratch(qevict_cache *cache, int32_t layer, const void *q,
+                                                     float *out, float *mass, int32_t accumulate_scores,
+                                                     void *stream);
+
 /* Thread-local text of the last host-side error of this thread. */
 const char *qevict_last_error(void);
 

@@ -27,7 +27,7 @@ EXPORTS = ["qevict_pool_capacity", "qevict_cache_create", "qevict_cache_destroy"
            "qevict_decode_attention", "qevict_decode_step", "qevict_route", "qevict_demote_quantize",
            "qevict_promote_dequantize", "qevict_set_tiers", "qevict_get_scores", "qevict_get_view",
            "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_set_launch_overlap",
-           "qevict_refresh_lengths",
+           "qevict_refresh_lengths", "qevict_decode_attention_static_scratch",
            "qevict_length",
            "qevict_last_error"]
 
@@ -107,6 +107,7 @@ def load() -> ctypes.CDLL:
         "qevict_get_stats": [P, ctypes.POINTER(Stats), P],
         "qevict_set_launch_overlap": [P, I32],
         "qevict_refresh_lengths": [P, P],
+        "qevict_decode_attention_static_scratch": [P, I32, P, P, P, I32, P],
         "qevict_length": [P, I32],
         "qevict_last_error": [],
     }
@@ -229,6 +230,14 @@ class TieredCache:
                                device=q.device)
         self._check(self.lib.qevict_decode_attention(self.handle, layer, _ptr(q), _ptr(out), _ptr(mass),
                                                      1 if accumulate else 0, _stream(stream)))
+        return out, mass
+
+    def decode_static_scratch(self, layer, q, out, mass=None, accumulate=True, stream=None):
+        """decode() on the library's static device scratch; out (and mass, if
+        wanted) are caller-owned, so nothing is allocated on this call."""
+        self._check(self.lib.qevict_decode_attention_static_scratch(self.handle, layer, _ptr(q), _ptr(out),
+                                                                    _ptr(mass), 1 if accumulate else 0,
+                                                                    _stream(stream)))
         return out, mass
 
     def decode_step(self, layer, q, k_new, v_new, out=None, mass=None, want_mass=True, accumulate=True,

@@ -7,6 +7,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -637,6 +638,105 @@ qevict_status qevict_refresh_lengths(qevict_cache *c, void *stream) {
 int64_t qevict_length(const qevict_cache *c, int32_t layer) {
     if (!c || layer < 0 || layer >= c->cfg.num_layers) return -1;
     return c->layers[layer].length;
+}
+
+}  // extern "C"
+
+// ---- decode with library-owned static scratch ------------------------------
+// The decode kernel needs per-call scratch (split partials, window statistics,
+// arrival counters). qevict_decode_attention_static_scratch takes it from the
+// fixed device array below instead of the cache's own block, so the call
+// allocates nothing. Its address is looked up once per device, with that
+// device current, and then passed to the kernel as a plain pointer.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = QEVICT_STATIC_SCRATCH_BYTES;
+constexpr int kStaticMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void *g_static_ptr[kStaticMaxDevices];
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Scratch layout of one call (the kernel indexes split partials with a stride
+// of kMaxSplits splits, whatever the split count). Counters come first.
+struct StaticLayout {
+    size_t o_ar, o_ab, o_pml, o_part, o_ws, total;
+};
+
+StaticLayout static_layout(const qevict_cache *c) {
+    const size_t B = (size_t)c->cfg.batch, Hkv = (size_t)c->cfg.num_kv_heads, Hq = (size_t)c->cfg.num_q_heads;
+    StaticLayout s{};
+    s.o_ar = 0;
+    s.o_ab = s.o_ar + round256(B * Hkv * 4);
+    s.o_pml = s.o_ab + round256(B * 4);
+    s.o_part = s.o_pml + round256(B * Hkv * kMaxSplits * (size_t)c->G * 8);
+    s.o_ws = s.o_part + round256(B * Hkv * kMaxSplits * (size_t)c->G * kHeadDim * 4);
+    s.total = s.o_ws + round256(B * Hq * (size_t)c->Wmax * 8);
+    return s;
+}
+
+// First use on a device: look up the array's address and clear it (the
+// arrival counters must start at zero; each launch leaves them at zero).
+qevict_status static_scratch_setup(int dev, void **out) {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "static scratch address lookup");
+        e = cudaMemset(p, 0, kStaticScratchBytes);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return cuda_fail(e, "static scratch clear");
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return QEVICT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qevict_status qevict_decode_attention_static_scratch(qevict_cache *c, int32_t layer, const void *q, float *out,
+                                                     float *mass, int32_t accumulate_scores, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (!q || !out) return fail(QEVICT_ERR_INVALID_ARG, "q and out must not be NULL");
+    if (lh.length < 1) return fail(QEVICT_ERR_INVALID_ARG, "layer %d is empty", layer);
+    const StaticLayout ly = static_layout(c);
+    if (ly.total > kStaticScratchBytes)
+        return fail(QEVICT_ERR_INVALID_ARG,
+                    "this cache needs %zu B of decode scratch; the static scratch holds %zu B "
+                    "(use qevict_decode_attention)",
+                    ly.total, kStaticScratchBytes);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != c->device)
+        return fail(QEVICT_ERR_INVALID_ARG, "device %d is current but the cache lives on device %d", dev, c->device);
+    if (dev < 0 || dev >= kStaticMaxDevices)
+        return fail(QEVICT_ERR_INVALID_ARG, "device index %d passes the static scratch table (%d)", dev,
+                    kStaticMaxDevices);
+    void *base = nullptr;
+    st = static_scratch_setup(dev, &base);
+    if (st) return st;
+    uint8_t *p = (uint8_t *)base;
+    DecodeScratch S{};
+    S.arrive = (uint32_t *)(p + ly.o_ar);
+    S.arrive_b = (uint32_t *)(p + ly.o_ab);
+    S.part_ml = (float2 *)(p + ly.o_pml);
+    S.part = (float *)(p + ly.o_part);
+    S.wstat = (float2 *)(p + ly.o_ws);
+    const int splits = decode_splits(c->cfg.batch * c->cfg.num_kv_heads, c->num_sms, c->G);
+    e = launch_decode(lh.dev, c->cdev, S, lh.tmap, layer, (const __nv_bfloat16 *)q, nullptr, nullptr, out, mass,
+                      accumulate_scores, splits, false, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
+    note_op(c, layer, stream);
+    return QEVICT_OK;
 }
 
 }  // extern "C"
