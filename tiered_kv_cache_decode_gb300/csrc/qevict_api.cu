@@ -282,7 +282,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         Carver cv;
         const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * kHeadDim * 4);
         const size_t o_pml = cv.take((size_t)B * Hkv * kMaxSplits * c->G * 8);
-        const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
+        const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8 + 16);   // the decode's bulk reads may pass a row end by 8 B
         const size_t o_ar = cv.take((size_t)B * Hkv * 4);
         const size_t o_ab = cv.take((size_t)B * 4);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
@@ -675,7 +675,7 @@ StaticLayout static_layout(const qevict_cache *c) {
     s.o_pml = s.o_ab + round256(B * 4);
     s.o_part = s.o_pml + round256(B * Hkv * kMaxSplits * (size_t)c->G * 8);
     s.o_ws = s.o_part + round256(B * Hkv * kMaxSplits * (size_t)c->G * kHeadDim * 4);
-    s.total = s.o_ws + round256(B * Hq * (size_t)c->Wmax * 8);
+    s.total = s.o_ws + round256(B * Hq * (size_t)c->Wmax * 8 + 16);
     return s;
 }
 

@@ -52,6 +52,7 @@ namespace {
 
 constexpr int kWarps = 6;                 // consumer warps per CTA
 constexpr int kThreads = kWarps * 32;
+constexpr int kTailThreads = (kWarps - 1) * 32;   // merge threads of the last CTA (the last warp appends)
 constexpr int kStages = 2;                // shared-memory stages per warp
 constexpr int kStage = 8192;              // bytes per stage
 constexpr int kRing = kStages * kStage;   // bytes per warp
@@ -119,6 +120,32 @@ __device__ __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1, uin
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// D = A B + C with C from separate registers: {c0, c0, c1, c1}
+__device__ __forceinline__ void mma_c(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                      uint32_t b1, float c0, float c1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %11, %11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+// 2^x (PTX ex2.approx; results below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// barrier among the merge warps of the last CTA (named barrier 1)
+__device__ __forceinline__ void tail_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTailThreads) : "memory"); }
+__device__ __forceinline__ bool tail_sync_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kTailThreads)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -131,6 +158,12 @@ __device__ __forceinline__ uint32_t codes2(uint32_t x) {
     v = __hsub2(v, __floats2bfloat162_rn(128.f, 128.f));
     return *reinterpret_cast<uint32_t *>(&v);
 }
+// K codes of a QK k-step as bf16 pairs with the offset kept: bits 1:0 and
+// 17:16 give 128 + code, bits 3:2 and 19:18 give 128 + 4 code (both exact).
+// The query values that meet the second pair are stored divided by 4, and
+// the offsets' contribution is taken out through the accumulator's start value.
+__device__ __forceinline__ uint32_t kcodes_lo(uint32_t x) { return (x & 0x00030003u) | 0x43004300u; }
+__device__ __forceinline__ uint32_t kcodes_hi(uint32_t x) { return (x & 0x000C000Cu) | 0x43004300u; }
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -189,7 +222,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ int st_wi[kWarps][kStages][kQPerStage];       // window of each unit
     __shared__ int st_j[kWarps][kStages][kQPerStage];        // 16-token unit index inside the window
     __shared__ int st_nt[kWarps][kStages][kQPerStage];       // tokens in the unit
-    __shared__ int st_last[kWarps][kStages][kQPerStage];     // 1: the window's last unit
+    __shared__ int st_emit[kWarps][kStages][kQPerStage];     // window statistics after the unit: 1 whole, 2 partial
+    __shared__ int pt_win[kWarps][2];                        // windows this warp saw only part of
+    __shared__ float2 pt_st[kWarps][2][8];                   // their (max, exp-sum) per head
     __shared__ int s_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -207,6 +242,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int n_win = (int)((length + w - 1) / w);
     const int n_fp = ctr[CTR_NFP], n_q = ctr[CTR_NQ];
+    // full-precision slot that receives this step's token, read before this CTA
+    // arrives (the sequence's last CTA moves CTR_NEXT afterwards)
+    const int slot_new = knew == nullptr ? -1
+                         : (length % w == 0) ? *(volatile const int32_t *)&ctr[CTR_NEXT]
+                                             : *(volatile const int32_t *)&D.fp_slot[wb + length / w];
     const Range R = split_range(split, splits, n_fp, n_q);
     const int nfw = R.f1 - R.f0;                       // full-precision windows of this split
     const int nwin = nfw + (R.q1 - R.q0);              // windows of this split
@@ -218,23 +258,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     };
     for (int i = tid; i < min(nwin, kEntTab); i += kThreads) s_ent[i] = lentry(i);
     if (tid == 0) s_flag = 0;
-    if (lane == 0)
+    if (lane == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
+        pt_win[warp][0] = pt_win[warp][1] = -1;
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
     auto ent = [&](int i) -> int2 { return i < kEntTab ? s_ent[i] : lentry(i); };
     auto ntok_of = [&](int wi) -> int { return (wi == n_win - 1) ? (int)(length - (int64_t)wi * w) : w; };
 
-    // ---- issue bookkeeping (all lanes run it; lane 0 issues the copies). This
-    // warp takes windows warp, warp + kWarps, ... of the split, all units of a window
-    // in order. A stage holds one full-precision unit, or up to five 16-token
-    // tiles of INT2 windows (one bulk copy per window's run of tiles).
-    const int my_wins = nwin > warp ? (nwin - warp + kWarps - 1) / kWarps : 0;
-    int iw = 0, ij = 0;              // next (warp-local window, unit) to issue
+    // ---- issue bookkeeping (all lanes run it; lane 0 issues the copies). The
+    // split's windows are cut into 16-token units (w / 16 per window; the open
+    // window's units past its last token are skipped) and each warp takes a
+    // contiguous range of them. A stage holds one full-precision unit, or up
+    // to five INT2 tiles (one bulk copy per window's run of tiles). A window
+    // whose units all lie in this warp's range gets its statistics written
+    // after its last unit; a window cut by a range boundary leaves a partial
+    // entry, merged with its neighbour's after the loop.
+    const int n_units = nwin * mu;
+    const int u_beg = (int)((int64_t)n_units * warp / kWarps);
+    const int u_end = (int)((int64_t)n_units * (warp + 1) / kWarps);
+    int iu = u_beg;                  // next unit to issue
     int issued = 0, consumed = 0;    // stages issued / consumed
     auto try_issue = [&]() {
-        while (iw < my_wins && issued - consumed < kStages) {
-            const int li = warp + iw * kWarps;
+        while (iu < u_end && issued - consumed < kStages) {
+            const int li = iu / mu, j = iu - li * mu;
             const int st = issued % kStages;
             const uint32_t bar = smem_u32(&bars[warp][st]);
             const uint32_t dst = ring_s + st * kStage;
@@ -242,24 +290,26 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int2 en = ent(li);
                 const int nt = ntok_of(en.x);
                 const int nu = (nt + 15) >> 4;   // units that hold tokens
+                if (j >= nu) {                   // past the open window's last token
+                    iu = (li + 1) * mu;
+                    continue;
+                }
                 if (lane == 0) {
+                    const bool whole = li * mu >= u_beg && li * mu + nu <= u_end;
                     st_n[warp][st] = 1;
                     st_fp[warp][st] = 1;
                     st_wi[warp][st][0] = en.x;
-                    st_j[warp][st][0] = ij;
-                    st_nt[warp][st][0] = min(16, nt - 16 * ij);
-                    st_last[warp][st][0] = ij == nu - 1;
+                    st_j[warp][st][0] = j;
+                    st_nt[warp][st][0] = min(16, nt - 16 * j);
+                    st_emit[warp][st][0] = (j == nu - 1 || iu + 1 == u_end) ? (whole ? 1 : 2) : 0;
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     mbar_expect_tx(bar, (uint32_t)kFPUnit);
-                    tma_4d(dst, &tmap, 0, 16 * ij, 0, en.y * Hkv + kvh, bar);
+                    tma_4d(dst, &tmap, 0, 16 * j, 0, en.y * Hkv + kvh, bar);
                 }
-                if (++ij == nu) {
-                    ij = 0;
-                    ++iw;
-                }
+                ++iu;
             } else {
-                // every later window of this warp is INT2 and full (mu tiles)
-                const int n = min(kQPerStage, (mu - ij) + (my_wins - iw - 1) * mu);
+                // INT2 windows are always full (mu tiles)
+                const int n = min(kQPerStage, u_end - iu);
                 if (lane == 0) {
                     st_n[warp][st] = n;
                     st_fp[warp][st] = 0;
@@ -268,25 +318,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 int done = 0;
                 while (done < n) {
-                    const int2 en = ent(warp + iw * kWarps);
-                    const int run = min(mu - ij, n - done);
+                    const int lq = iu / mu, jq = iu - lq * mu;
+                    const int2 en = ent(lq);
+                    const int run = min(mu - jq, n - done);
                     if (lane == 0) {
+                        const bool whole = lq * mu >= u_beg && (lq + 1) * mu <= u_end;
                         for (int r = 0; r < run; ++r) {
                             st_wi[warp][st][done + r] = en.x;
-                            st_j[warp][st][done + r] = ij + r;
+                            st_j[warp][st][done + r] = jq + r;
                             st_nt[warp][st][done + r] = 16;
-                            st_last[warp][st][done + r] = ij + r == mu - 1;
+                            st_emit[warp][st][done + r] =
+                                (jq + r == mu - 1 || iu + r + 1 == u_end) ? (whole ? 1 : 2) : 0;
                         }
                         bulk_g2s(dst + done * kQUnit,
-                                 D.lg_pool + (int64_t)en.y * D.lg_slot_bytes + lg_tile_off(kvh, w, ij),
+                                 D.lg_pool + (int64_t)en.y * D.lg_slot_bytes + lg_tile_off(kvh, w, jq),
                                  (uint32_t)(run * kQUnit), bar);
                     }
                     done += run;
-                    ij += run;
-                    if (ij == mu) {
-                        ij = 0;
-                        ++iw;
-                    }
+                    iu += run;
                 }
             }
             ++issued;
@@ -302,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t *qw =
         reinterpret_cast<const uint32_t *>(q + ((int64_t)b * Hq + kvh * G + (g < G ? g : 0)) * kHeadDim);
     float qsum[kGroups] = {0.f, 0.f, 0.f, 0.f};
+    float qbias[kGroups] = {0.f, 0.f, 0.f, 0.f};   // -128 x the INT2-path fragment values, per group
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
         uint32_t lo = 0, hi = 0;   // channels (16ks+2t, +1) and (16ks+2t+8, +9)
@@ -309,25 +359,33 @@ __global__ void __launch_bounds__(kThreads, 2)
             lo = qw[(16 * ks + 2 * t) / 2];
             hi = qw[(16 * ks + 2 * t + 8) / 2];
         }
-        if (warp == 0) {
-            s_qf[ks * 32 + lane] = make_uint2(lo, hi);
-            s_qf[(8 + ks) * 32 + lane] = make_uint2((lo & 0xffffu) | (hi << 16),       // channels 2t, 2t+8
-                                                    (lo >> 16) | (hi & 0xffff0000u));  // channels 2t+1, 2t+9
-        }
         const float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&lo));
         const float2 c = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&hi));
+        // INT2 path: channels 2t, 2t+8 meet 128 + code; channels 2t+1, 2t+9
+        // meet 128 + 4 code and are stored divided by 4 (exact in bf16)
+        const uint32_t x0 = (lo & 0xffffu) | (hi << 16);
+        const uint32_t x1 = pack2(a.y * 0.25f, c.y * 0.25f);
+        if (warp == 0) {
+            s_qf[ks * 32 + lane] = make_uint2(lo, hi);
+            s_qf[(8 + ks) * 32 + lane] = make_uint2(x0, x1);
+        }
+        const float2 y1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&x1));
         qsum[ks >> 1] += (a.x + a.y) + (c.x + c.y);
+        qbias[ks >> 1] -= 128.f * ((a.x + c.x) + (y1.x + y1.y));
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kGroups; ++i) {
         qsum[i] += __shfl_xor_sync(0xffffffffu, qsum[i], 1);
         qsum[i] += __shfl_xor_sync(0xffffffffu, qsum[i], 2);
+        qbias[i] += __shfl_xor_sync(0xffffffffu, qbias[i], 1);
+        qbias[i] += __shfl_xor_sync(0xffffffffu, qbias[i], 2);
     }
     const float qk_scale = kLog2e * rsqrtf((float)kHeadDim);
 
     // ---- per-warp online softmax state (lane: head g for m/l, heads 2t, 2t+1 in O)
     float m_run = -INFINITY, l_part = 0.f, w_part = 0.f;
+    int n_part = 0;   // partial window entries left by this warp (at most 2)
     float o[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -351,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             float hmx = fmaxf(lmx, __shfl_xor_sync(0xffffffffu, lmx, 1));
             hmx = fmaxf(hmx, __shfl_xor_sync(0xffffffffu, hmx, 2));
             const float m_new = fmaxf(m_run, hmx);
-            const float alpha = exp2f(m_run - m_new);
+            const float alpha = ex2(m_run - m_new);
             m_run = m_new;
             l_part *= alpha;
             w_part *= alpha;
@@ -371,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         float es = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float e = exp2f(x[i] - m_run);
+            const float e = ex2(x[i] - m_run);
             es += e;
             x[i] = (g < G) ? e : 0.f;
         }
@@ -395,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool is_fp = st_fp[warp][st] != 0;
         for (int ib = 0; ib < nb; ++ib) {
         const int wi = st_wi[warp][st][ib], ntu = st_nt[warp][st][ib];
-        const bool last = st_last[warp][st][ib] != 0;
+        const int emit = st_emit[warp][st][ib];
         const uint32_t base = ring_s + st * kStage + ib * kQUnit;
         if (is_fp) {
             // ---------------- full-precision unit
@@ -457,15 +515,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             float x[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int grp = 0; grp < kGroups; ++grp) {
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                float c0[4], c1[4];
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const int ks = 2 * grp + kk;
                     const uint32_t xa = pick(ks < 4 ? kA0 : kA1, ks & 3) >> (4 * t);
                     const uint32_t xb = pick(ks < 4 ? kB0 : kB1, ks & 3) >> (4 * t);
                     const uint2 aq = s_qf[(8 + ks) * 32 + lane];
-                    mma(c0, aq.x, 0u, aq.y, 0u, codes2(xa), codes2(xa >> 2));
-                    mma(c1, aq.x, 0u, aq.y, 0u, codes2(xb), codes2(xb >> 2));
+                    if (kk == 0) {   // start from minus the offsets' share (rows g; rows g + 8 are padding)
+                        mma_c(c0, aq.x, 0u, aq.y, 0u, kcodes_lo(xa), kcodes_hi(xa), qbias[grp], 0.f);
+                        mma_c(c1, aq.x, 0u, aq.y, 0u, kcodes_lo(xb), kcodes_hi(xb), qbias[grp], 0.f);
+                    } else {
+                        mma(c0, aq.x, 0u, aq.y, 0u, kcodes_lo(xa), kcodes_hi(xa));
+                        mma(c1, aq.x, 0u, aq.y, 0u, kcodes_lo(xb), kcodes_hi(xb));
+                    }
                 }
                 const float acc[4] = {c0[0], c0[1], c1[0], c1[1]};
 #pragma unroll
@@ -508,10 +571,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
-        if (last) {   // the window is complete: (reference max, exp-sum over its tokens) for head g
+        if (emit) {   // (reference max, exp-sum over the window's tokens seen here) for head g
             float ws = w_part + __shfl_xor_sync(0xffffffffu, w_part, 1);
             ws += __shfl_xor_sync(0xffffffffu, ws, 2);
-            if (t == 0 && g < G) wstat[(int64_t)g * D.Wmax + wi] = make_float2(m_run, ws);
+            if (emit == 1) {
+                if (t == 0 && g < G) wstat[(int64_t)g * D.Wmax + wi] = make_float2(m_run, ws);
+            } else {
+                if (t == 0 && g < G) pt_st[warp][n_part][g] = make_float2(m_run, ws);
+                if (lane == 0) pt_win[warp][n_part] = wi;
+                ++n_part;
+            }
             w_part = 0.f;
         }
         }
@@ -520,6 +589,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         try_issue();
     }
     __syncthreads();
+    // windows cut between warps: merge the partial entries in unit order
+    if (warp == 0 && lane < G) {
+        int cur = -1;
+        float2 acc = make_float2(-INFINITY, 0.f);
+        for (int ww = 0; ww < kWarps; ++ww)
+            for (int k = 0; k < 2; ++k) {
+                const int wn = pt_win[ww][k];
+                if (wn < 0) continue;
+                if (wn != cur) {
+                    if (cur >= 0) wstat[(int64_t)lane * D.Wmax + cur] = acc;
+                    cur = wn;
+                    acc = pt_st[ww][k][lane];
+                } else {
+                    acc = stat_merge(acc, pt_st[ww][k][lane]);
+                }
+            }
+        if (cur >= 0) wstat[(int64_t)lane * D.Wmax + cur] = acc;
+    }
 
     // ---- merge the warps (the rings are free now)
     float *Ow = reinterpret_cast<float *>(smem);                 // [warp][8 heads][128]
@@ -581,181 +668,36 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!s_flag) return;
     __threadfence();
 
-    // ================= last CTA of this (sequence, KV head): merge the splits
-    float *sM = reinterpret_cast<float *>(smem);                  // [splits][G]
-    float *sL = sM + kMaxSplits * G;
-    float *sF = sL + kMaxSplits * G;                              // scale factor per split
-    float *hM = sF + kMaxSplits * G;                              // [G] global max
-    float *hIL = hM + 8;                                          // [G] 1 / L
-    float *hNew = hIL + 8;                                        // [G] new-token logit
-    float *hFN = hNew + 8;                                        // [G] new-token factor
-    const float2 *ml = S.part_ml + (int64_t)bk * kMaxSplits * G;
-    // the splits' partial outputs, one bulk copy into shared memory when they fit
-    float *sAcc = hFN + 8;                                        // [splits][G][128]
-    const uint32_t acc_bytes = (uint32_t)splits * G * kHeadDim * 4;
-    const bool bulk_acc = (uint8_t *)sAcc + acc_bytes <= smem + kWarps * kRing;
-    const uint32_t tbar = smem_u32(&bars[0][0]);
-    if (bulk_acc && tid == 0) {
-        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tbar) : "memory");
-        mbar_init(tbar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async;" ::: "memory");   // generic writes of the other splits -> bulk read
-        mbar_expect_tx(tbar, acc_bytes);
-        bulk_g2s(smem_u32(sAcc), S.part + (int64_t)bk * kMaxSplits * G * kHeadDim, acc_bytes, tbar);
-    }
-    for (int i = tid; i < splits * G; i += kThreads) {
-        const float2 v = __ldcg(ml + i);
-        sM[i] = v.x;
-        sL[i] = v.y;
-    }
+    // ================= last CTA of this (sequence, KV head): merge the splits.
+    // Every input of the merge is requested before the first wait: the split
+    // partials and the window statistics by bulk copy into shared memory when
+    // they fit, the split maxima/sums, tiers, old scores and the new token by
+    // plain loads. The last warp stays out of the merge: it appends this
+    // step's token and, in the last such CTA of the sequence, moves the
+    // sequence's tables forward while the other warps merge.
     const bool has_new = knew != nullptr;
     const __nv_bfloat16 *kn = has_new ? knew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
     const __nv_bfloat16 *vn = has_new ? vnew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
-    if (has_new) {
-        for (int hh = warp; hh < G; hh += kWarps) {
-            const __nv_bfloat16 *qq = q + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim;
-            float d = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                d = fmaf(__bfloat162float(qq[lane * 4 + i]), __bfloat162float(kn[lane * 4 + i]), d);
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o2);
-            if (lane == 0) hNew[hh] = d * qk_scale;
-        }
-    }
-    __syncthreads();
-    if (tid < G) {
-        float M = has_new ? hNew[tid] : -INFINITY;
-        for (int s = 0; s < splits; ++s) M = fmaxf(M, sM[s * G + tid]);
-        float L = 0.f;
-        for (int s = 0; s < splits; ++s) {
-            const float f = (M == -INFINITY || sM[s * G + tid] == -INFINITY) ? 0.f : exp2f(sM[s * G + tid] - M);
-            sF[s * G + tid] = f;
-            L += f * sL[s * G + tid];
-        }
-        const float fn = has_new ? exp2f(hNew[tid] - M) : 0.f;
-        L += fn;
-        hM[tid] = M;
-        hIL[tid] = L > 0.f ? 1.f / L : 0.f;
-        hFN[tid] = fn;
-    }
-    __syncthreads();
-    // output: each thread owns 4 channels of one head
-    if (bulk_acc) {
-        bool ok = true;
-        if (tid == 0) ok = mbar_wait(tbar, 0);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -2);
-        }
-        const float4 *pa = reinterpret_cast<const float4 *>(sAcc);
-        for (int oi = tid; oi < G * (kHeadDim / 4); oi += kThreads) {
-            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has_new) {
-                const float fn = hFN[hh];
-                acc = make_float4(fn * __bfloat162float(vn[4 * c4]), fn * __bfloat162float(vn[4 * c4 + 1]),
-                                  fn * __bfloat162float(vn[4 * c4 + 2]), fn * __bfloat162float(vn[4 * c4 + 3]));
-            }
-            for (int s = 0; s < splits; ++s) {
-                const float f = sF[s * G + hh];
-                const float4 v = pa[(s * G + hh) * (kHeadDim / 4) + c4];
-                acc.x = fmaf(f, v.x, acc.x);
-                acc.y = fmaf(f, v.y, acc.y);
-                acc.z = fmaf(f, v.z, acc.z);
-                acc.w = fmaf(f, v.w, acc.w);
-            }
-            const float il = hIL[hh];
-            reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
-                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
-        }
-    } else {
-        const float4 *pa = reinterpret_cast<const float4 *>(S.part + (int64_t)bk * kMaxSplits * G * kHeadDim);
-        for (int oi = tid; oi < G * (kHeadDim / 4); oi += kThreads) {
-            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has_new) {
-                const float fn = hFN[hh];
-                acc = make_float4(fn * __bfloat162float(vn[4 * c4]), fn * __bfloat162float(vn[4 * c4 + 1]),
-                                  fn * __bfloat162float(vn[4 * c4 + 2]), fn * __bfloat162float(vn[4 * c4 + 3]));
-            }
-            for (int s0 = 0; s0 < splits; s0 += 16) {
-                float4 v[16];
-#pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    v[s] = s0 + s < splits ? __ldcg(pa + ((int64_t)(s0 + s) * G + hh) * (kHeadDim / 4) + c4)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int s = 0; s < 16; ++s) {
-                    const float f = s0 + s < splits ? sF[(s0 + s) * G + hh] : 0.f;
-                    acc.x = fmaf(f, v[s].x, acc.x);
-                    acc.y = fmaf(f, v[s].y, acc.y);
-                    acc.z = fmaf(f, v[s].z, acc.z);
-                    acc.w = fmaf(f, v[s].w, acc.w);
-                }
-            }
-            const float il = hIL[hh];
-            reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
-                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
-        }
-    }
-
-    // ---- masses and the cumulative score; the new token counts in its window
     const int64_t Lnew = has_new ? length + 1 : length;
     const int n_out = (int)((Lnew + w - 1) / w);
     const int wnew = (int)(length / w);
     const bool opens = has_new && (length % w == 0);
-    const float inv_hq = 1.f / (float)Hq;
-    float *sp = D.score_part + ((int64_t)b * Hkv + kvh) * D.Wmax;
-    for (int w0 = 0; w0 < n_out; w0 += 4 * kThreads) {
-        float2 st[4][G];
-        bool live[4];
-        float old[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int wi = w0 + c * kThreads + tid;
-            const bool in = wi < n_out;
-            const bool fresh = opens && wi == wnew;
-            live[c] = in && (fresh || D.tier[wb + wi] != QEVICT_TIER_E);
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh)
-                st[c][hh] = (live[c] && !fresh) ? __ldcg(&wstat[(int64_t)hh * D.Wmax + wi]) : make_float2(-INFINITY, 0.f);
-            old[c] = (in && accumulate) ? sp[wi] : 0.f;
-        }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int wi = w0 + c * kThreads + tid;
-            if (wi >= n_out) continue;
-            float sum = 0.f;
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                float2 stt = st[c][hh];
-                if (has_new && wi == wnew) stt = stat_merge(stt, make_float2(hNew[hh], 1.f));
-                const float m =
-                    (live[c] && hM[hh] != -INFINITY && stt.y > 0.f) ? stt.y * exp2f(stt.x - hM[hh]) * hIL[hh] : 0.f;
-                if (mass) mass[((int64_t)b * Hq + kvh * G + hh) * n_out + wi] = m;
-                sum += m;
-            }
-            if (accumulate) sp[wi] = old[c] + sum * inv_hq;
-        }
-    }
 
-    // ---- append this step's token (this KV head's K and V rows)
-    if (has_new) {
-        const int slot = opens ? ctr[CTR_NEXT] : D.fp_slot[wb + wnew];
-        if (slot >= 0 && tid < 32) {
+    if (warp == kWarps - 1) {
+        if (!has_new) return;
+        // this KV head's K and V rows of the new token
+        if (slot_new >= 0) {
             const int row = (int)(length % w);
-            const int kv = tid >> 4, c = tid & 15;
+            const int kv = lane >> 4, c = lane & 15;
             const __nv_bfloat16 *src = kv ? vn : kn;
-            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)slot * D.fp_slot_bytes) +
+            __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)slot_new * D.fp_slot_bytes) +
                                  fp_off(kvh, kv, w, row, 8 * c);
             *reinterpret_cast<uint4 *>(dst) = reinterpret_cast<const uint4 *>(src)[c];
         }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
+        if (lane == 0) {
             const unsigned prev = atomicAdd(&S.arrive_b[b], 1u);
             if (prev == (unsigned)(Hkv - 1)) {
-                // last KV head of this sequence: table bookkeeping for the new token
+                // every CTA of this sequence has read its tables: move them forward
                 __threadfence();
                 int32_t *c = D.ctr + b * kCtrN;
                 if (opens) {
@@ -783,7 +725,177 @@ __global__ void __launch_bounds__(kThreads, 2)
                 S.arrive_b[b] = 0u;
             }
         }
+        return;
     }
+
+    float *sM = reinterpret_cast<float *>(smem);                  // [kMaxSplits][G]
+    float *sL = sM + kMaxSplits * G;
+    float *sF = sL + kMaxSplits * G;                              // scale factor per split
+    float *hM = sF + kMaxSplits * G;                              // [G] global max
+    float *hIL = hM + 8;                                          // [G] 1 / L
+    float *hNew = hIL + 8;                                        // [G] new-token logit
+    float *hFN = hNew + 8;                                        // [G] new-token factor
+    float *sVn = hFN + 8;                                         // [128] new token's V row
+    float *sAcc = sVn + kHeadDim;                                 // [splits][G][128]
+    uint8_t *const tail_end = smem + kWarps * kRing + kEntTab * 8 + 16 * 32 * 8;
+    const uint32_t acc_bytes = (uint32_t)splits * G * kHeadDim * 4;
+    const bool bulk_acc = (uint8_t *)sAcc + acc_bytes <= tail_end;
+    // window statistics: one row per head; a row starts on a 16-byte boundary
+    // in shared memory and holds the global row from the 16-byte boundary at
+    // or below its start (its first entry at offset wofs)
+    const int ws_row = (n_out + 2) & ~1;
+    float2 *sWs = reinterpret_cast<float2 *>(bulk_acc ? sAcc + splits * G * kHeadDim : sAcc);
+    const bool bulk_ws = (uint8_t *)(sWs + G * ws_row) <= tail_end;
+    auto wofs = [&](int hh) -> int {
+        return (int)((reinterpret_cast<uintptr_t>(wstat + (int64_t)hh * D.Wmax) >> 3) & 1);
+    };
+    const uint32_t tbar = smem_u32(&bars[0][0]);
+    const bool use_bar = bulk_acc || bulk_ws;
+    if (use_bar && tid == 0) {
+        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tbar) : "memory");
+        mbar_init(tbar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async;" ::: "memory");   // generic writes of the splits -> bulk reads
+        uint32_t total = bulk_acc ? acc_bytes : 0u;
+        if (bulk_ws)
+            for (int hh = 0; hh < G; ++hh) total += (uint32_t)(((wofs(hh) + n_out) * 8 + 15) & ~15);
+        mbar_expect_tx(tbar, total);
+        if (bulk_acc) bulk_g2s(smem_u32(sAcc), S.part + (int64_t)bk * kMaxSplits * G * kHeadDim, acc_bytes, tbar);
+        if (bulk_ws)
+            for (int hh = 0; hh < G; ++hh) {
+                const int o = wofs(hh);
+                bulk_g2s(smem_u32(sWs + hh * ws_row), wstat + (int64_t)hh * D.Wmax - o,
+                         (uint32_t)(((o + n_out) * 8 + 15) & ~15), tbar);
+            }
+    }
+    const float2 *ml = S.part_ml + (int64_t)bk * kMaxSplits * G;
+    for (int i = tid; i < splits * G; i += kTailThreads) {
+        const float2 v = __ldcg(ml + i);
+        sM[i] = v.x;
+        sL[i] = v.y;
+    }
+    if (has_new) {
+        for (int hh = warp; hh < G; hh += kWarps - 1) {
+            const __nv_bfloat16 *qq = q + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim;
+            float d = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                d = fmaf(__bfloat162float(qq[lane * 4 + i]), __bfloat162float(kn[lane * 4 + i]), d);
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o2);
+            if (lane == 0) hNew[hh] = d * qk_scale;
+        }
+        if (tid < kHeadDim) sVn[tid] = __bfloat162float(vn[tid]);
+    }
+    // tiers and old scores of this thread's first windows
+    float *sp = D.score_part + ((int64_t)b * Hkv + kvh) * D.Wmax;
+    uint8_t tr0[4];
+    float old0[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int wi = c * kTailThreads + tid;
+        tr0[c] = wi < n_out ? D.tier[wb + wi] : (uint8_t)QEVICT_TIER_E;
+        old0[c] = (wi < n_out && accumulate) ? sp[wi] : 0.f;
+    }
+    tail_sync();
+    // global max and exp-sum per head, one warp per head
+    for (int hh = warp; hh < G; hh += kWarps - 1) {
+        float m = -INFINITY;
+        for (int s = lane; s < splits; s += 32) m = fmaxf(m, sM[s * G + hh]);
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
+        const float M = has_new ? fmaxf(m, hNew[hh]) : m;
+        float l = 0.f;
+        for (int s = lane; s < splits; s += 32) {
+            const float ms = sM[s * G + hh];
+            const float f = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
+            sF[s * G + hh] = f;
+            l = fmaf(f, sL[s * G + hh], l);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o2);
+        if (lane == 0) {
+            const float fn = has_new ? exp2f(hNew[hh] - M) : 0.f;
+            l += fn;
+            hM[hh] = M;
+            hIL[hh] = l > 0.f ? 1.f / l : 0.f;
+            hFN[hh] = fn;
+        }
+    }
+    {
+        bool ok = true;
+        if (use_bar && tid == 0) ok = mbar_wait(tbar, 0);
+        if (tail_sync_or(!ok)) {
+            if (tid == 0) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -2);
+        }
+    }
+    // output: each thread owns 4 channels of one head
+    for (int oi = tid; oi < G * (kHeadDim / 4); oi += kTailThreads) {
+        const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (has_new) {
+            const float fn = hFN[hh];
+            acc = make_float4(fn * sVn[4 * c4], fn * sVn[4 * c4 + 1], fn * sVn[4 * c4 + 2], fn * sVn[4 * c4 + 3]);
+        }
+        if (bulk_acc) {
+            const float4 *pa = reinterpret_cast<const float4 *>(sAcc);
+            for (int s = 0; s < splits; ++s) {
+                const float f = sF[s * G + hh];
+                const float4 v = pa[(s * G + hh) * (kHeadDim / 4) + c4];
+                acc.x = fmaf(f, v.x, acc.x);
+                acc.y = fmaf(f, v.y, acc.y);
+                acc.z = fmaf(f, v.z, acc.z);
+                acc.w = fmaf(f, v.w, acc.w);
+            }
+        } else {
+            const float4 *pa = reinterpret_cast<const float4 *>(S.part + (int64_t)bk * kMaxSplits * G * kHeadDim);
+            for (int s0 = 0; s0 < splits; s0 += 16) {
+                float4 v[16];
+#pragma unroll
+                for (int s = 0; s < 16; ++s)
+                    v[s] = s0 + s < splits ? __ldcg(pa + ((int64_t)(s0 + s) * G + hh) * (kHeadDim / 4) + c4)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int s = 0; s < 16; ++s) {
+                    const float f = s0 + s < splits ? sF[(s0 + s) * G + hh] : 0.f;
+                    acc.x = fmaf(f, v[s].x, acc.x);
+                    acc.y = fmaf(f, v[s].y, acc.y);
+                    acc.z = fmaf(f, v[s].z, acc.z);
+                    acc.w = fmaf(f, v[s].w, acc.w);
+                }
+            }
+        }
+        const float il = hIL[hh];
+        reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
+            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+    }
+
+    // ---- masses and the cumulative score; the new token counts in its window
+    const float inv_hq = 1.f / (float)Hq;
+    for (int w0 = 0; w0 < n_out; w0 += 4 * kTailThreads) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int wi = w0 + c * kTailThreads + tid;
+            if (wi >= n_out) continue;
+            const bool fresh = opens && wi == wnew;
+            const uint8_t tw = w0 == 0 ? tr0[c] : D.tier[wb + wi];
+            const bool live = fresh || tw != QEVICT_TIER_E;
+            float sum = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < G; ++hh) {
+                float2 stt = make_float2(-INFINITY, 0.f);
+                if (live && !fresh)
+                    stt = bulk_ws ? sWs[hh * ws_row + wofs(hh) + wi] : __ldcg(&wstat[(int64_t)hh * D.Wmax + wi]);
+                if (has_new && wi == wnew) stt = stat_merge(stt, make_float2(hNew[hh], 1.f));
+                const float m =
+                    (live && hM[hh] != -INFINITY && stt.y > 0.f) ? stt.y * exp2f(stt.x - hM[hh]) * hIL[hh] : 0.f;
+                if (mass) mass[((int64_t)b * Hq + kvh * G + hh) * n_out + wi] = m;
+                sum += m;
+            }
+            if (accumulate) sp[wi] = (w0 == 0 ? old0[c] : sp[wi]) + sum * inv_hq;
+        }
+    }
+
     if (tid == 0) S.arrive[bk] = 0u;
 }
 
