@@ -320,16 +320,17 @@ int64_t qevict_length(const qevict_cache *cache, int32_t layer);
  * a host thread that must not block on an allocator's lock.
  *
  * Arguments, outputs and errors are those of qevict_decode_attention.
- * The scratch a call needs grows with batch x Hkv x (Hq / Hkv) (split
- * partials, 64 splits of 512 B per query head) and batch x Hq x the window
- * count (window statistics); a cache whose need passes
+ * The scratch a call needs is 8 B of window statistics per (sequence,
+ * query head, window of max_context), (512 + 8) B per query head for each
+ * decode split of each (sequence, KV head) (up to 32 splits, as many as fit
+ * the GPU in one wave), and a few counters; a cache whose need passes
  * QEVICT_STATIC_SCRATCH_BYTES is rejected with INVALID_ARG before anything
  * is enqueued, and the error text gives both sizes. The cache's device must
  * be current (INVALID_ARG otherwise).
  *
  * Set-up: the first call on a device, with that device current, looks up the
- * array's address and clears it (the split arrival counters in it must start
- * at zero; each launch leaves them at zero). That first call synchronises
+ * array's address and clears it (the arrival counters in it must start at
+ * zero; each launch leaves them at zero). That first call synchronises
  * the device, so make it before any stream capture begins.
  *
  * One array serves every cache and stream on a device: calls whose kernels

@@ -68,8 +68,8 @@ def test_static_scratch_without_mass():
 
 
 def test_static_scratch_rejects_a_cache_that_needs_more():
-    # 16 sequences x 8 KV heads x 4 query heads x 64 splits x 512 B of split partials alone is 16 MiB
-    cache = binding.TieredCache(16, 1, 32, 8, 64, 256, budget_frac=1.0, fp_share=1.0)
+    # 16 sequences x 32 query heads x 1024 windows x 8 B of window statistics is 4 MiB, plus the counters
+    cache = binding.TieredCache(16, 1, 32, 8, 16, 16384, budget_frac=0.05, fp_share=0.5)
     k, v = synth.kv_tokens(13, 0, 16, 0, 100, 8, 128, "heavy", device="cuda")
     cache.append(0, k, v)
     q = synth.queries(13, 0, 0, 16, 32, 128).cuda()

@@ -282,8 +282,8 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         Carver cv;
         const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * kHeadDim * 4);
         const size_t o_pml = cv.take((size_t)B * Hkv * kMaxSplits * c->G * 8);
-        const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8 + 16);   // the decode's bulk reads may pass a row end by 8 B
-        const size_t o_ar = cv.take((size_t)B * Hkv * 4);
+        const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
+        const size_t o_bar = cv.take((size_t)B * Hkv * 8);
         const size_t o_ab = cv.take((size_t)B * 4);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
         if (!base) {
@@ -295,7 +295,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         c->scratch.part = (float *)(base + o_part);
         c->scratch.part_ml = (float2 *)(base + o_pml);
         c->scratch.wstat = (float2 *)(base + o_ws);
-        c->scratch.arrive = (uint32_t *)(base + o_ar);
+        c->scratch.bar = (uint32_t *)(base + o_bar);
         c->scratch.arrive_b = (uint32_t *)(base + o_ab);
         c->scratch_bytes = cv.off;
         c->scratch_base = base;
@@ -643,8 +643,8 @@ int64_t qevict_length(const qevict_cache *c, int32_t layer) {
 }  // extern "C"
 
 // ---- decode with library-owned static scratch ------------------------------
-// The decode kernel needs per-call scratch (split partials, window statistics,
-// arrival counters). qevict_decode_attention_static_scratch takes it from the
+// The decode kernel needs per-call scratch (split partials, window
+// statistics, barrier and arrival counters). qevict_decode_attention_static_scratch takes it from the
 // fixed device array below instead of the cache's own block, so the call
 // allocates nothing. Its address is looked up once per device, with that
 // device current, and then passed to the kernel as a plain pointer.
@@ -661,21 +661,21 @@ void *g_static_ptr[kStaticMaxDevices];
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Scratch layout of one call (the kernel indexes split partials with a stride
-// of kMaxSplits splits, whatever the split count). Counters come first.
+// Scratch layout of one call: counters first (they must start at zero),
+// then split partials for `splits` splits and the window statistics.
 struct StaticLayout {
-    size_t o_ar, o_ab, o_pml, o_part, o_ws, total;
+    size_t o_ab, o_bar, o_pml, o_part, o_ws, total;
 };
 
-StaticLayout static_layout(const qevict_cache *c) {
+StaticLayout static_layout(const qevict_cache *c, int splits) {
     const size_t B = (size_t)c->cfg.batch, Hkv = (size_t)c->cfg.num_kv_heads, Hq = (size_t)c->cfg.num_q_heads;
     StaticLayout s{};
-    s.o_ar = 0;
-    s.o_ab = s.o_ar + round256(B * Hkv * 4);
-    s.o_pml = s.o_ab + round256(B * 4);
-    s.o_part = s.o_pml + round256(B * Hkv * kMaxSplits * (size_t)c->G * 8);
-    s.o_ws = s.o_part + round256(B * Hkv * kMaxSplits * (size_t)c->G * kHeadDim * 4);
-    s.total = s.o_ws + round256(B * Hq * (size_t)c->Wmax * 8 + 16);
+    s.o_ab = 0;
+    s.o_bar = s.o_ab + round256(B * 4);
+    s.o_pml = s.o_bar + round256(B * Hkv * 8);
+    s.o_part = s.o_pml + round256(B * Hkv * (size_t)splits * c->G * 8);
+    s.o_ws = s.o_part + round256(B * Hkv * (size_t)splits * c->G * kHeadDim * 4);
+    s.total = s.o_ws + round256(B * Hq * (size_t)c->Wmax * 8);
     return s;
 }
 
@@ -707,7 +707,8 @@ qevict_status qevict_decode_attention_static_scratch(qevict_cache *c, int32_t la
     LayerHost &lh = c->layers[layer];
     if (!q || !out) return fail(QEVICT_ERR_INVALID_ARG, "q and out must not be NULL");
     if (lh.length < 1) return fail(QEVICT_ERR_INVALID_ARG, "layer %d is empty", layer);
-    const StaticLayout ly = static_layout(c);
+    const int splits = decode_splits(c->cfg.batch * c->cfg.num_kv_heads, c->num_sms, c->G);
+    const StaticLayout ly = static_layout(c, splits);
     if (ly.total > kStaticScratchBytes)
         return fail(QEVICT_ERR_INVALID_ARG,
                     "this cache needs %zu B of decode scratch; the static scratch holds %zu B "
@@ -726,12 +727,11 @@ qevict_status qevict_decode_attention_static_scratch(qevict_cache *c, int32_t la
     if (st) return st;
     uint8_t *p = (uint8_t *)base;
     DecodeScratch S{};
-    S.arrive = (uint32_t *)(p + ly.o_ar);
     S.arrive_b = (uint32_t *)(p + ly.o_ab);
+    S.bar = (uint32_t *)(p + ly.o_bar);
     S.part_ml = (float2 *)(p + ly.o_pml);
     S.part = (float *)(p + ly.o_part);
     S.wstat = (float2 *)(p + ly.o_ws);
-    const int splits = decode_splits(c->cfg.batch * c->cfg.num_kv_heads, c->num_sms, c->G);
     e = launch_decode(lh.dev, c->cdev, S, lh.tmap, layer, (const __nv_bfloat16 *)q, nullptr, nullptr, out, mass,
                       accumulate_scores, splits, false, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");

@@ -50,9 +50,12 @@ namespace qevict {
 
 namespace {
 
-constexpr int kWarps = 6;                 // consumer warps per CTA
+constexpr int kWarps = 12;                // warps per CTA (one CTA per SM)
 constexpr int kThreads = kWarps * 32;
-constexpr int kTailThreads = (kWarps - 1) * 32;   // merge threads of the last CTA (the last warp appends)
+constexpr int kTailThreads = (kWarps - 1) * 32;   // threads of the split merge (the last warp appends)
+// shared-memory offsets used after the main loop (inside the free rings)
+constexpr int kFwtOff = 52 * 1024;     // [warp][8] weight of each warp's partial
+constexpr int kHeadOff = 54 * 1024;    // per-head merge results, per-split weights, new token's V row
 constexpr int kStages = 2;                // shared-memory stages per warp
 constexpr int kStage = 8192;              // bytes per stage
 constexpr int kRing = kStages * kStage;   // bytes per warp
@@ -89,17 +92,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         if (clock64() - t0 > kWaitCycles) return false;
     return true;
 }
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
+// L2 policy for data read once per launch: evicted first, so that it does not
+// push the kernel's code, tables and scratch out of L2
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
 }
 __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, int u,
-                                       uint32_t bar) {
+                                       uint32_t bar, uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-        "%5}], [%6];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(u), "r"(bar)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(u), "r"(bar), "l"(pol)
         : "memory");
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -129,23 +141,8 @@ __device__ __forceinline__ void mma_c(float (&d)[4], uint32_t a0, uint32_t a1, u
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
 }
-// 2^x (PTX ex2.approx; results below 2^-126 flush to zero)
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 // barrier among the merge warps of the last CTA (named barrier 1)
 __device__ __forceinline__ void tail_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTailThreads) : "memory"); }
-__device__ __forceinline__ bool tail_sync_or(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v), "n"(kTailThreads)
-        : "memory");
-    return r != 0;
-}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -183,12 +180,18 @@ __device__ __forceinline__ uint32_t pick(const uint4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// 2^x (PTX ex2.approx; results below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // (max, exp-sum relative to max) pairs
 __device__ __forceinline__ float2 stat_merge(float2 a, float2 b) {
     if (a.y <= 0.f) return b;
     if (b.y <= 0.f) return a;
     const float m = fmaxf(a.x, b.x);
-    return make_float2(m, a.y * exp2f(a.x - m) + b.y * exp2f(b.x - m));
+    return make_float2(m, a.y * ex2(a.x - m) + b.y * ex2(b.x - m));
 }
 
 // A split's share of the window list: full-precision entries [f0, f1) and
@@ -205,7 +208,7 @@ __device__ __forceinline__ Range split_range(int split, int splits, int n_fp, in
 }
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const LayerDev D, const CacheDev C, const DecodeScratch S, const __grid_constant__ CUtensorMap tmap,
                   int layer, const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *knew,
                   const __nv_bfloat16 *vnew, float *__restrict__ out, float *__restrict__ mass, int accumulate,
@@ -225,7 +228,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     __shared__ int st_emit[kWarps][kStages][kQPerStage];     // window statistics after the unit: 1 whole, 2 partial
     __shared__ int pt_win[kWarps][2];                        // windows this warp saw only part of
     __shared__ float2 pt_st[kWarps][2][8];                   // their (max, exp-sum) per head
-    __shared__ int s_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -257,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         return i < nfw ? D.fp_list[b * D.CF + R.f0 + i] : D.q_list[b * D.CQ + R.q0 + (i - nfw)];
     };
     for (int i = tid; i < min(nwin, kEntTab); i += kThreads) s_ent[i] = lentry(i);
-    if (tid == 0) s_flag = 0;
     if (lane == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
         pt_win[warp][0] = pt_win[warp][1] = -1;
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // whose units all lie in this warp's range gets its statistics written
     // after its last unit; a window cut by a range boundary leaves a partial
     // entry, merged with its neighbour's after the loop.
+    const uint64_t l2_stream = evict_first_policy();
     const int n_units = nwin * mu;
     const int u_beg = (int)((int64_t)n_units * warp / kWarps);
     const int u_end = (int)((int64_t)n_units * (warp + 1) / kWarps);
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     st_emit[warp][st][0] = (j == nu - 1 || iu + 1 == u_end) ? (whole ? 1 : 2) : 0;
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     mbar_expect_tx(bar, (uint32_t)kFPUnit);
-                    tma_4d(dst, &tmap, 0, 16 * j, 0, en.y * Hkv + kvh, bar);
+                    tma_4d(dst, &tmap, 0, 16 * j, 0, en.y * Hkv + kvh, bar, l2_stream);
                 }
                 ++iu;
             } else {
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         }
                         bulk_g2s(dst + done * kQUnit,
                                  D.lg_pool + (int64_t)en.y * D.lg_slot_bytes + lg_tile_off(kvh, w, jq),
-                                 (uint32_t)(run * kQUnit), bar);
+                                 (uint32_t)(run * kQUnit), bar, l2_stream);
                     }
                     done += run;
                     iu += run;
@@ -589,23 +591,26 @@ __global__ void __launch_bounds__(kThreads, 2)
         try_issue();
     }
     __syncthreads();
-    // windows cut between warps: merge the partial entries in unit order
-    if (warp == 0 && lane < G) {
-        int cur = -1;
-        float2 acc = make_float2(-INFINITY, 0.f);
-        for (int ww = 0; ww < kWarps; ++ww)
-            for (int k = 0; k < 2; ++k) {
-                const int wn = pt_win[ww][k];
-                if (wn < 0) continue;
-                if (wn != cur) {
-                    if (cur >= 0) wstat[(int64_t)lane * D.Wmax + cur] = acc;
-                    cur = wn;
-                    acc = pt_st[ww][k][lane];
-                } else {
-                    acc = stat_merge(acc, pt_st[ww][k][lane]);
+    // windows cut between warps: entry e = 2 warp + slot; the entries of one
+    // window are consecutive among the used ones. One thread per (entry,
+    // head) starts at each window's first entry and merges the rest.
+    if (tid < 2 * kWarps * 8) {
+        const int e = tid >> 3, hh = tid & 7;
+        const int wn = pt_win[e >> 1][e & 1];
+        if (hh < G && wn >= 0) {
+            int pe = e - 1;
+            while (pe >= 0 && pt_win[pe >> 1][pe & 1] < 0) --pe;
+            if (pe < 0 || pt_win[pe >> 1][pe & 1] != wn) {
+                float2 acc = pt_st[e >> 1][e & 1][hh];
+                for (int ne = e + 1; ne < 2 * kWarps; ++ne) {
+                    const int wv = pt_win[ne >> 1][ne & 1];
+                    if (wv < 0) continue;
+                    if (wv != wn) break;
+                    acc = stat_merge(acc, pt_st[ne >> 1][ne & 1][hh]);
                 }
+                wstat[(int64_t)hh * D.Wmax + wn] = acc;
             }
-        if (cur >= 0) wstat[(int64_t)lane * D.Wmax + cur] = acc;
+        }
     }
 
     // ---- merge the warps (the rings are free now)
@@ -636,45 +641,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int i = 0; i < kGroups; ++i) minw[(warp * 8 + g) * 4 + i] = minacc[i];
     }
-    __syncthreads();
-    float *pacc = S.part + ((int64_t)bk * kMaxSplits + split) * G * kHeadDim;
-    float2 *pml = S.part_ml + ((int64_t)bk * kMaxSplits + split) * G;
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + hh]);
-        if (tid < kHeadDim) {
-            float acc = 0.f, l = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int ww = 0; ww < kWarps; ++ww) {
-                    const float f = exp2f(mw_s[ww * 8 + hh] - M);
-                    acc += f * (Ow[(ww * 8 + hh) * kHeadDim + tid] + minw[(ww * 8 + hh) * 4 + tid / kGroup]);
-                    l += f * lw_s[ww * 8 + hh];
-                }
-            }
-            pacc[hh * kHeadDim + tid] = acc;
-            if (tid == 0) pml[hh] = make_float2(M, l);
-        }
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(&S.arrive[bk], 1u);
-        s_flag = prev == (unsigned)(splits - 1);
-    }
-    __syncthreads();
-    if (!s_flag) return;
-    __threadfence();
-
-    // ================= last CTA of this (sequence, KV head): merge the splits.
-    // Every input of the merge is requested before the first wait: the split
-    // partials and the window statistics by bulk copy into shared memory when
-    // they fit, the split maxima/sums, tiers, old scores and the new token by
-    // plain loads. The last warp stays out of the merge: it appends this
-    // step's token and, in the last such CTA of the sequence, moves the
-    // sequence's tables forward while the other warps merge.
+    // per-head merge results and the new token, in the free rings
+    float *fwt = reinterpret_cast<float *>(smem + kFwtOff);                    // [warp][8]
+    float *hM = reinterpret_cast<float *>(smem + kHeadOff);                    // [8] max over the splits
+    float *hIL = hM + 8;                                                       // [8] 1 / exp-sum
+    float *hNew = hIL + 8;                                                     // [8] new token's logit
+    float *hFN = hNew + 8;                                                     // [8] new token's weight
+    float *Frk = hFN + 8;                                                      // [kMaxSplits][8] weight of each split
+    float *sVn = Frk + kMaxSplits * 8;                                         // [128] new token's V row
     const bool has_new = knew != nullptr;
     const __nv_bfloat16 *kn = has_new ? knew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
     const __nv_bfloat16 *vn = has_new ? vnew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
@@ -682,9 +656,88 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int n_out = (int)((Lnew + w - 1) / w);
     const int wnew = (int)(length / w);
     const bool opens = has_new && (length % w == 0);
+    if (has_new) {
+        for (int hh = warp; hh < G; hh += kWarps) {
+            const __nv_bfloat16 *qq = q + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim;
+            float d = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                d = fmaf(__bfloat162float(qq[lane * 4 + i]), __bfloat162float(kn[lane * 4 + i]), d);
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o2);
+            if (lane == 0) hNew[hh] = d * qk_scale;
+        }
+        if (tid < kHeadDim) sVn[tid] = __bfloat162float(vn[tid]);
+    }
+    __syncthreads();
+    // this split's partial: output [G][128] (unnormalised, relative to its
+    // own max) and (max, exp-sum) [G], to global memory for the other splits
+    float *pacc = S.part + ((int64_t)bk * splits + split) * G * kHeadDim;
+    float2 *pml = S.part_ml + ((int64_t)bk * splits + split) * G;
+    if (tid < G) {
+        float M = -INFINITY;
+        for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + tid]);
+        float l = 0.f;
+        for (int ww = 0; ww < kWarps; ++ww) {
+            const float f = M == -INFINITY ? 0.f : ex2(mw_s[ww * 8 + tid] - M);
+            fwt[ww * 8 + tid] = f;
+            l = fmaf(f, lw_s[ww * 8 + tid], l);
+        }
+        pml[tid] = make_float2(M, l);
+    }
+    __syncthreads();
+    for (int i = tid; i < G * kHeadDim; i += kThreads) {
+        const int hh = i / kHeadDim, c = i % kHeadDim;
+        float acc = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww)
+            acc = fmaf(fwt[ww * 8 + hh], Ow[(ww * 8 + hh) * kHeadDim + c] + minw[(ww * 8 + hh) * 4 + c / kGroup], acc);
+        pacc[i] = acc;
+    }
+    // statistics of this thread's first window (written to global memory by
+    // this CTA's warps), its old score, and the tier of its window in this
+    // split's slice of the window range, fetched while the splits gather
+    float *sp = D.score_part + ((int64_t)b * Hkv + kvh) * D.Wmax;
+    int pwi = -1;
+    float pold = 0.f;
+    float2 pst[G];
+    if (tid < nwin) {
+        pwi = ent(tid).x;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) pst[hh] = wstat[(int64_t)hh * D.Wmax + pwi];
+        pold = accumulate ? sp[pwi] : 0.f;
+    }
+    const int z0 = (int)((int64_t)split * n_out / splits), z1 = (int)((int64_t)(split + 1) * n_out / splits);
+    const uint8_t ztier = z0 + tid < z1 ? D.tier[wb + z0 + tid] : (uint8_t)QEVICT_TIER_E;
 
+    // ================= barrier over the splits of this (sequence, KV head).
+    // Every CTA of the grid is resident at once (one wave), so the wait ends
+    // as soon as the last split arrives; it gives up after about two seconds.
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t *cnt = S.bar + 2 * bk, *gen = cnt + 1;
+        const uint32_t g0 = *(volatile uint32_t *)gen;
+        __threadfence();
+        const uint32_t prev = atomicAdd(cnt, 1u);
+        if (prev == (uint32_t)(splits - 1)) {
+            *(volatile uint32_t *)cnt = 0u;
+            __threadfence();
+            atomicAdd(gen, 1u);
+        } else {
+            const long long t0 = clock64();
+            while (*(volatile uint32_t *)gen == g0) {
+                if (clock64() - t0 > kWaitCycles) {
+                    set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -3);
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
     if (warp == kWarps - 1) {
-        if (!has_new) return;
+        if (split != 0 || !has_new) return;
         // this KV head's K and V rows of the new token
         if (slot_new >= 0) {
             const int row = (int)(length % w);
@@ -727,220 +780,148 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         return;
     }
-
-    float *sM = reinterpret_cast<float *>(smem);                  // [kMaxSplits][G]
-    float *sL = sM + kMaxSplits * G;
-    float *sF = sL + kMaxSplits * G;                              // scale factor per split
-    float *hM = sF + kMaxSplits * G;                              // [G] global max
-    float *hIL = hM + 8;                                          // [G] 1 / L
-    float *hNew = hIL + 8;                                        // [G] new-token logit
-    float *hFN = hNew + 8;                                        // [G] new-token factor
-    float *sVn = hFN + 8;                                         // [128] new token's V row
-    float *sAcc = sVn + kHeadDim;                                 // [splits][G][128]
-    uint8_t *const tail_end = smem + kWarps * kRing + kEntTab * 8 + 16 * 32 * 8;
-    const uint32_t acc_bytes = (uint32_t)splits * G * kHeadDim * 4;
-    const bool bulk_acc = (uint8_t *)sAcc + acc_bytes <= tail_end;
-    // window statistics: one row per head; a row starts on a 16-byte boundary
-    // in shared memory and holds the global row from the 16-byte boundary at
-    // or below its start (its first entry at offset wofs)
-    const int ws_row = (n_out + 2) & ~1;
-    float2 *sWs = reinterpret_cast<float2 *>(bulk_acc ? sAcc + splits * G * kHeadDim : sAcc);
-    const bool bulk_ws = (uint8_t *)(sWs + G * ws_row) <= tail_end;
-    auto wofs = [&](int hh) -> int {
-        return (int)((reinterpret_cast<uintptr_t>(wstat + (int64_t)hh * D.Wmax) >> 3) & 1);
-    };
-    const uint32_t tbar = smem_u32(&bars[0][0]);
-    const bool use_bar = bulk_acc || bulk_ws;
-    if (use_bar && tid == 0) {
-        asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(tbar) : "memory");
-        mbar_init(tbar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async;" ::: "memory");   // generic writes of the splits -> bulk reads
-        uint32_t total = bulk_acc ? acc_bytes : 0u;
-        if (bulk_ws)
-            for (int hh = 0; hh < G; ++hh) total += (uint32_t)(((wofs(hh) + n_out) * 8 + 15) & ~15);
-        mbar_expect_tx(tbar, total);
-        if (bulk_acc) bulk_g2s(smem_u32(sAcc), S.part + (int64_t)bk * kMaxSplits * G * kHeadDim, acc_bytes, tbar);
-        if (bulk_ws)
-            for (int hh = 0; hh < G; ++hh) {
-                const int o = wofs(hh);
-                bulk_g2s(smem_u32(sWs + hh * ws_row), wstat + (int64_t)hh * D.Wmax - o,
-                         (uint32_t)(((o + n_out) * 8 + 15) & ~15), tbar);
-            }
-    }
-    const float2 *ml = S.part_ml + (int64_t)bk * kMaxSplits * G;
-    for (int i = tid; i < splits * G; i += kTailThreads) {
-        const float2 v = __ldcg(ml + i);
-        sM[i] = v.x;
-        sL[i] = v.y;
-    }
-    if (has_new) {
-        for (int hh = warp; hh < G; hh += kWarps - 1) {
-            const __nv_bfloat16 *qq = q + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim;
-            float d = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                d = fmaf(__bfloat162float(qq[lane * 4 + i]), __bfloat162float(kn[lane * 4 + i]), d);
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o2);
-            if (lane == 0) hNew[hh] = d * qk_scale;
-        }
-        if (tid < kHeadDim) sVn[tid] = __bfloat162float(vn[tid]);
-    }
-    // tiers and old scores of this thread's first windows
-    float *sp = D.score_part + ((int64_t)b * Hkv + kvh) * D.Wmax;
-    uint8_t tr0[4];
-    float old0[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int wi = c * kTailThreads + tid;
-        tr0[c] = wi < n_out ? D.tier[wb + wi] : (uint8_t)QEVICT_TIER_E;
-        old0[c] = (wi < n_out && accumulate) ? sp[wi] : 0.f;
-    }
-    tail_sync();
-    // global max and exp-sum per head, one warp per head
+    // max and exp-sum over the splits, per head (every CTA computes the same)
+    const float2 *ml_all = S.part_ml + (int64_t)bk * splits * G;
     for (int hh = warp; hh < G; hh += kWarps - 1) {
-        float m = -INFINITY;
-        for (int s = lane; s < splits; s += 32) m = fmaxf(m, sM[s * G + hh]);
+        float2 v = make_float2(-INFINITY, 0.f);
+        if (lane < splits) v = __ldcg(ml_all + lane * G + hh);
+        float M = v.x;
 #pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o2));
-        const float M = has_new ? fmaxf(m, hNew[hh]) : m;
-        float l = 0.f;
-        for (int s = lane; s < splits; s += 32) {
-            const float ms = sM[s * G + hh];
-            const float f = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
-            sF[s * G + hh] = f;
-            l = fmaf(f, sL[s * G + hh], l);
-        }
+        for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+        if (has_new) M = fmaxf(M, hNew[hh]);
+        const float f = (lane < splits && M != -INFINITY && v.x != -INFINITY) ? ex2(v.x - M) : 0.f;
+        if (lane < splits) Frk[lane * 8 + hh] = f;
+        float l = f * v.y;
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o2);
         if (lane == 0) {
-            const float fn = has_new ? exp2f(hNew[hh] - M) : 0.f;
+            const float fn = has_new ? ex2(hNew[hh] - M) : 0.f;
             l += fn;
             hM[hh] = M;
             hIL[hh] = l > 0.f ? 1.f / l : 0.f;
             hFN[hh] = fn;
         }
     }
+    tail_sync();
+    // output: this split's slice of the [G][32] float4 outputs, each summed over the splits' partials
     {
-        bool ok = true;
-        if (use_bar && tid == 0) ok = mbar_wait(tbar, 0);
-        if (tail_sync_or(!ok)) {
-            if (tid == 0) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -2);
-        }
-    }
-    // output: each thread owns 4 channels of one head
-    for (int oi = tid; oi < G * (kHeadDim / 4); oi += kTailThreads) {
-        const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (has_new) {
-            const float fn = hFN[hh];
-            acc = make_float4(fn * sVn[4 * c4], fn * sVn[4 * c4 + 1], fn * sVn[4 * c4 + 2], fn * sVn[4 * c4 + 3]);
-        }
-        if (bulk_acc) {
-            const float4 *pa = reinterpret_cast<const float4 *>(sAcc);
-            for (int s = 0; s < splits; ++s) {
-                const float f = sF[s * G + hh];
-                const float4 v = pa[(s * G + hh) * (kHeadDim / 4) + c4];
-                acc.x = fmaf(f, v.x, acc.x);
-                acc.y = fmaf(f, v.y, acc.y);
-                acc.z = fmaf(f, v.z, acc.z);
-                acc.w = fmaf(f, v.w, acc.w);
+        const int n4 = G * (kHeadDim / 4);
+        const int o0 = split * n4 / splits, o1 = (split + 1) * n4 / splits;
+        const float4 *pa = reinterpret_cast<const float4 *>(S.part + (int64_t)bk * splits * G * kHeadDim);
+        for (int oi = o0 + tid; oi < o1; oi += kTailThreads) {
+            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has_new) {
+                const float fn = hFN[hh];
+                acc = make_float4(fn * sVn[4 * c4], fn * sVn[4 * c4 + 1], fn * sVn[4 * c4 + 2], fn * sVn[4 * c4 + 3]);
             }
-        } else {
-            const float4 *pa = reinterpret_cast<const float4 *>(S.part + (int64_t)bk * kMaxSplits * G * kHeadDim);
-            for (int s0 = 0; s0 < splits; s0 += 16) {
-                float4 v[16];
+            for (int s0 = 0; s0 < splits; s0 += 8) {
+                float4 v[8];
 #pragma unroll
-                for (int s = 0; s < 16; ++s)
-                    v[s] = s0 + s < splits ? __ldcg(pa + ((int64_t)(s0 + s) * G + hh) * (kHeadDim / 4) + c4)
+                for (int r = 0; r < 8; ++r)
+                    v[r] = s0 + r < splits ? __ldcg(pa + ((int64_t)(s0 + r) * G + hh) * (kHeadDim / 4) + c4)
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int s = 0; s < 16; ++s) {
-                    const float f = s0 + s < splits ? sF[(s0 + s) * G + hh] : 0.f;
-                    acc.x = fmaf(f, v[s].x, acc.x);
-                    acc.y = fmaf(f, v[s].y, acc.y);
-                    acc.z = fmaf(f, v[s].z, acc.z);
-                    acc.w = fmaf(f, v[s].w, acc.w);
+                for (int r = 0; r < 8; ++r) {
+                    const float f = s0 + r < splits ? Frk[(s0 + r) * 8 + hh] : 0.f;
+                    acc.x = fmaf(f, v[r].x, acc.x);
+                    acc.y = fmaf(f, v[r].y, acc.y);
+                    acc.z = fmaf(f, v[r].z, acc.z);
+                    acc.w = fmaf(f, v[r].w, acc.w);
                 }
             }
+            const float il = hIL[hh];
+            reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
+                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
         }
-        const float il = hIL[hh];
-        reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
-            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
     }
 
-    // ---- masses and the cumulative score; the new token counts in its window
+    // ---- masses and cumulative scores of this split's windows
     const float inv_hq = 1.f / (float)Hq;
-    for (int w0 = 0; w0 < n_out; w0 += 4 * kTailThreads) {
+    for (int li = tid; li < nwin; li += kTailThreads) {
+        int wi = pwi;
+        float old = pold;
+        float2 st[G];
+        if (li == tid) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int wi = w0 + c * kTailThreads + tid;
-            if (wi >= n_out) continue;
-            const bool fresh = opens && wi == wnew;
-            const uint8_t tw = w0 == 0 ? tr0[c] : D.tier[wb + wi];
-            const bool live = fresh || tw != QEVICT_TIER_E;
-            float sum = 0.f;
+            for (int hh = 0; hh < G; ++hh) st[hh] = pst[hh];
+        } else {
+            wi = ent(li).x;
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                float2 stt = make_float2(-INFINITY, 0.f);
-                if (live && !fresh)
-                    stt = bulk_ws ? sWs[hh * ws_row + wofs(hh) + wi] : __ldcg(&wstat[(int64_t)hh * D.Wmax + wi]);
-                if (has_new && wi == wnew) stt = stat_merge(stt, make_float2(hNew[hh], 1.f));
-                const float m =
-                    (live && hM[hh] != -INFINITY && stt.y > 0.f) ? stt.y * exp2f(stt.x - hM[hh]) * hIL[hh] : 0.f;
-                if (mass) mass[((int64_t)b * Hq + kvh * G + hh) * n_out + wi] = m;
-                sum += m;
-            }
-            if (accumulate) sp[wi] = (w0 == 0 ? old0[c] : sp[wi]) + sum * inv_hq;
+            for (int hh = 0; hh < G; ++hh) st[hh] = wstat[(int64_t)hh * D.Wmax + wi];
+            old = accumulate ? sp[wi] : 0.f;
         }
+        float sum = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            float2 stt = st[hh];
+            if (has_new && wi == wnew) stt = stat_merge(stt, make_float2(hNew[hh], 1.f));   // the new token's window
+            const float m = (hM[hh] != -INFINITY && stt.y > 0.f) ? stt.y * ex2(stt.x - hM[hh]) * hIL[hh] : 0.f;
+            if (mass) mass[((int64_t)b * Hq + kvh * G + hh) * n_out + wi] = m;
+            sum += m;
+        }
+        if (accumulate) sp[wi] = old + sum * inv_hq;
     }
-
-    if (tid == 0) S.arrive[bk] = 0u;
+    // windows no split holds: evicted ones (mass 0) and a window this step
+    // opens; the window range is sliced over the splits
+    for (int wi = z0 + tid; wi < z1; wi += kTailThreads) {
+        const bool fresh = opens && wi == wnew;
+        if (!fresh && (wi == z0 + tid ? ztier : D.tier[wb + wi]) != QEVICT_TIER_E) continue;
+        float sum = 0.f;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            const float m = (fresh && hM[hh] != -INFINITY) ? ex2(hNew[hh] - hM[hh]) * hIL[hh] : 0.f;
+            if (mass) mass[((int64_t)b * Hq + kvh * G + hh) * n_out + wi] = m;
+            sum += m;
+        }
+        if (accumulate && fresh) sp[wi] += sum * inv_hq;
+    }
 }
+
+constexpr int kDynSmem = kWarps * kRing + kEntTab * 8 + 16 * 32 * 8 + 1024;
 
 // CTAs of decode_kernel<G> that fit on one SM, filled in by prepare_decode.
 int g_ctas_per_sm[kMaxG + 1];
 
-constexpr int kDynSmem = kWarps * kRing + kEntTab * 8 + 16 * 32 * 8 + 1024;
-
 template <int G>
-cudaError_t raise_smem_limit(int optin, int *ctas_per_sm) {
+cudaError_t prepare_one(int optin) {
     cudaFuncAttributes fa{};
     cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<G>);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              optin - (int)fa.sharedSizeBytes);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_kernel<G>, kThreads, kDynSmem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_ctas_per_sm[G], decode_kernel<G>, kThreads, kDynSmem);
 }
 
 }  // namespace
 
-// Raise the dynamic shared-memory limit of every decode instantiation once
-// (called at cache creation, outside any stream capture).
+// Raise the dynamic shared-memory limit of every decode instantiation and
+// record how many of its CTAs fit on one SM (called at cache creation,
+// outside any stream capture).
 cudaError_t prepare_decode() {
     static bool done = false;
     if (done) return cudaSuccess;
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess) e = raise_smem_limit<1>(optin, &g_ctas_per_sm[1]);
-    if (e == cudaSuccess) e = raise_smem_limit<2>(optin, &g_ctas_per_sm[2]);
-    if (e == cudaSuccess) e = raise_smem_limit<3>(optin, &g_ctas_per_sm[3]);
-    if (e == cudaSuccess) e = raise_smem_limit<4>(optin, &g_ctas_per_sm[4]);
-    if (e == cudaSuccess) e = raise_smem_limit<5>(optin, &g_ctas_per_sm[5]);
-    if (e == cudaSuccess) e = raise_smem_limit<6>(optin, &g_ctas_per_sm[6]);
-    if (e == cudaSuccess) e = raise_smem_limit<7>(optin, &g_ctas_per_sm[7]);
-    if (e == cudaSuccess) e = raise_smem_limit<8>(optin, &g_ctas_per_sm[8]);
+    if (e == cudaSuccess) e = prepare_one<1>(optin);
+    if (e == cudaSuccess) e = prepare_one<2>(optin);
+    if (e == cudaSuccess) e = prepare_one<3>(optin);
+    if (e == cudaSuccess) e = prepare_one<4>(optin);
+    if (e == cudaSuccess) e = prepare_one<5>(optin);
+    if (e == cudaSuccess) e = prepare_one<6>(optin);
+    if (e == cudaSuccess) e = prepare_one<7>(optin);
+    if (e == cudaSuccess) e = prepare_one<8>(optin);
     if (e == cudaSuccess) done = true;
     return e;
 }
 
-// Splits per (sequence, KV head): one wave of as many CTAs as fit on the SMs.
+// Splits per (sequence, KV head): as many as keep the whole grid resident at
+// once (the splits of a pair wait for one another), at most kMaxSplits.
 int decode_splits(int pairs, int num_sms, int G) {
     const int per_sm = (G >= 1 && G <= kMaxG && g_ctas_per_sm[G] > 0) ? g_ctas_per_sm[G] : 1;
-    int s = (per_sm * num_sms + pairs - 1) / pairs;
+    int s = per_sm * num_sms / (pairs > 0 ? pairs : 1);
     if (s > kMaxSplits) s = kMaxSplits;
     if (s < 1) s = 1;
     return s;

@@ -16,7 +16,7 @@ constexpr int kHeadDim = 128;          // d
 constexpr int kGroup = 32;             // channels per INT2 group
 constexpr int kGroups = kHeadDim / kGroup;
 constexpr int kMaxG = 8;               // query heads per KV head
-constexpr int kMaxSplits = 64;         // decode splits per (sequence, KV head)
+constexpr int kMaxSplits = 32;         // decode CTAs per (sequence, KV head)
 constexpr int kVTile = 16;             // tokens per transposed V-code word
 constexpr int kCtrN = 16;              // counters per sequence
 
@@ -82,11 +82,11 @@ struct LayerDev {
 // Decode scratch, shared by all layers of a cache: a decode launch touches it
 // only after its dependency wait, so consecutive launches never overlap in it.
 struct DecodeScratch {
-    float *part;          // [B*Hkv][kMaxSplits][G][d] split partial outputs
-    float2 *part_ml;      // [B*Hkv][kMaxSplits][G] split (max, exp-sum), log2 domain
+    float *part;          // [B*Hkv][splits][G][d] split partial outputs
+    float2 *part_ml;      // [B*Hkv][splits][G] split (max, exp-sum), log2 domain
     float2 *wstat;        // [B][Hq][Wmax] (window max, window exp-sum), log2 domain
-    uint32_t *arrive;     // [B*Hkv] split arrival counters (kept at 0 between launches)
-    uint32_t *arrive_b;   // [B] KV-head arrival counters for the fused append
+    uint32_t *bar;        // [B*Hkv][2] split barrier: arrival count (0 between launches), generation
+    uint32_t *arrive_b;   // [B] KV-head arrival counters for the fused append (0 between launches)
 };
 
 struct CacheDev {
