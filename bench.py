@@ -147,6 +147,20 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def combine_ranks(ms, e2e_s, nbytes, e2e_bytes, world, device):
+    """Whole-job figures over the ranks (each runs its own replica): the
+    slowest rank's times and the bytes of all ranks."""
+    if world == 1:
+        return ms, e2e_s, float(nbytes), float(e2e_bytes)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([float(nbytes), float(e2e_bytes)], dtype=torch.float64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t[0]), float(t[1]), float(n[0]), float(n[1])
+
+
 def profiled_traffic():
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current decode kernel source (else None)."""
@@ -156,8 +170,9 @@ def profiled_traffic():
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         fields = {}
         for line in open(summ):
-            if ":" in line and line.strip().startswith(("kernel_sha", "dram_bytes_per_launch")):
-                k, v = line.split(":", 1)
+            item = line.strip().lstrip("-* ").strip()
+            if ":" in item and item.startswith(("kernel_sha", "dram_bytes_per_launch")):
+                k, v = item.split(":", 1)
                 fields[k.strip(" -*`")] = v.strip(" `\n")
         if fields.get("kernel_sha") == sha:
             return int(float(fields["dram_bytes_per_launch"]))
@@ -363,15 +378,12 @@ def run_native(args, rank, world, local_rank):
     assert st == 0, f"device status {st}: {cache.last_error()}"
     cache.refresh_lengths()
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_s = float(t[0]), float(t[1])
+    ms, e2e_s, tot_bytes, tot_e2e_bytes = combine_ranks(ms, e2e_s, nbytes, e2e_bytes, world, dev)
 
     if rank != 0:
         return None
     peak, peak_kind = measured_peak()
-    value = world * nbytes / (ms / 1e3) / 1e9
+    value = tot_bytes / (ms / 1e3) / 1e9
     achieved = dec_bytes / (dec_ms / 1e3) / 1e9
     line = {
         "metric": METRIC,
@@ -386,7 +398,7 @@ def run_native(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD if NL == wl["layers"] else f"{WORKLOAD} ({NL} of {wl['layers']} layers)",
                    "batch": B, "layers": NL, "q_heads": Hq, "kv_heads": Hkv,
@@ -398,7 +410,7 @@ def run_native(args, rank, world, local_rank):
                      "kernel": "decode_kernel (tiered split-K decode + combine + score + append)",
                      "peak_source": peak_kind, "us_per_launch": round(dec_ms * 1e3, 3),
                      "bytes_per_launch": dec_bytes},
-        "e2e": None if args.no_e2e else {"value": round(e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
+        "e2e": None if args.no_e2e else {"value": round(tot_e2e_bytes / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(NL * per_layer * 2), "d2h_bytes_per_step": int(xout.numel() * 4),
                 "ms_per_step": round(e2e_s / K * 1e3, 4)},
         "gpu_launches": launches,

@@ -76,7 +76,8 @@ typedef struct qevict_allocator {
  *  max_context   the longest length the cache will reach (sizes the tables).
  *  budget_frac   beta in (0, 1]: the visible tiers of each (sequence, layer)
  *                hold at most floor(beta * L * Hkv * d * 4) bytes after a
- *                routing event ("5% tot 20% van de volledige KV-cache").
+ *                routing event (QEvict, Methodologie: a budget of a few to
+ *                twenty percent of the full cache).
  *  fp_share      rho in (0, 1]: the share of that budget that buys
  *                full-precision windows (the pages fix no split; 0.5 default).
  *  fp_capacity / ledger_capacity
