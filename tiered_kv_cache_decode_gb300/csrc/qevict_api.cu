@@ -281,7 +281,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     {
         Carver cv;
         const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * kHeadDim * 4);
-        const size_t o_pml = cv.take((size_t)B * Hkv * kMaxSplits * c->G * 8);
+        const size_t o_rec = cv.take((size_t)B * Hkv * kMaxSplits * kMaxG * 16);
         const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
         const size_t o_bar = cv.take((size_t)B * Hkv * 8);
         const size_t o_ab = cv.take((size_t)B * 4);
@@ -293,7 +293,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
             return fail(QEVICT_ERR_OUT_OF_MEMORY, "allocation of %zu B of decode scratch failed", need);
         }
         c->scratch.part = (float *)(base + o_part);
-        c->scratch.part_ml = (float2 *)(base + o_pml);
+        c->scratch.rec = (unsigned long long *)(base + o_rec);
         c->scratch.wstat = (float2 *)(base + o_ws);
         c->scratch.bar = (uint32_t *)(base + o_bar);
         c->scratch.arrive_b = (uint32_t *)(base + o_ab);
@@ -661,10 +661,12 @@ void *g_static_ptr[kStaticMaxDevices];
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Scratch layout of one call: counters first (they must start at zero),
-// then split partials for `splits` splits and the window statistics.
+// Scratch layout of one call: counters first (the arrival counts must start
+// at zero), the tagged split records (fixed stride, so that every cache maps a
+// (sequence, KV head, split) to the same words), split partials for `splits`
+// splits, and the window statistics.
 struct StaticLayout {
-    size_t o_ab, o_bar, o_pml, o_part, o_ws, total;
+    size_t o_ab, o_bar, o_rec, o_part, o_ws, total;
 };
 
 StaticLayout static_layout(const qevict_cache *c, int splits) {
@@ -672,8 +674,8 @@ StaticLayout static_layout(const qevict_cache *c, int splits) {
     StaticLayout s{};
     s.o_ab = 0;
     s.o_bar = s.o_ab + round256(B * 4);
-    s.o_pml = s.o_bar + round256(B * Hkv * 8);
-    s.o_part = s.o_pml + round256(B * Hkv * (size_t)splits * c->G * 8);
+    s.o_rec = s.o_bar + round256(B * Hkv * 8);
+    s.o_part = s.o_rec + round256(B * Hkv * (size_t)kMaxSplits * kMaxG * 16);
     s.o_ws = s.o_part + round256(B * Hkv * (size_t)splits * c->G * kHeadDim * 4);
     s.total = s.o_ws + round256(B * Hq * (size_t)c->Wmax * 8);
     return s;
@@ -729,7 +731,7 @@ qevict_status qevict_decode_attention_static_scratch(qevict_cache *c, int32_t la
     DecodeScratch S{};
     S.arrive_b = (uint32_t *)(p + ly.o_ab);
     S.bar = (uint32_t *)(p + ly.o_bar);
-    S.part_ml = (float2 *)(p + ly.o_pml);
+    S.rec = (unsigned long long *)(p + ly.o_rec);
     S.part = (float *)(p + ly.o_part);
     S.wstat = (float2 *)(p + ly.o_ws);
     e = launch_decode(lh.dev, c->cdev, S, lh.tmap, layer, (const __nv_bfloat16 *)q, nullptr, nullptr, out, mass,

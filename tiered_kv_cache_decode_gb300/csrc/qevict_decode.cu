@@ -220,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // query A fragments per lane: [path (0 natural, 1 INT2 channel order)][k-step][lane] {a0, a2}
     uint2 *s_qf = reinterpret_cast<uint2 *>(smem + kWarps * kRing + kEntTab * 8);
     __shared__ uint64_t bars[kWarps][kStages];
+    __shared__ uint32_t s_gen;                               // split-record generation of this launch
     __shared__ int st_n[kWarps][kStages];                    // units in a stage
     __shared__ int st_fp[kWarps][kStages];                   // 1: a full-precision unit
     __shared__ int st_wi[kWarps][kStages][kQPerStage];       // window of each unit
@@ -347,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- wait for the previous kernel, then let the next one start
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (tid == 0) s_gen = *(volatile const uint32_t *)(S.bar + 2 * bk + 1);
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- query fragments (A operand: G heads as rows, rest zero)
@@ -649,6 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *hFN = hNew + 8;                                                     // [8] new token's weight
     float *Frk = hFN + 8;                                                      // [kMaxSplits][8] weight of each split
     float *sVn = Frk + kMaxSplits * 8;                                         // [128] new token's V row
+    float2 *sOwn = reinterpret_cast<float2 *>(sVn + kHeadDim);                 // [8] this split's (max, exp-sum)
     const bool has_new = knew != nullptr;
     const __nv_bfloat16 *kn = has_new ? knew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
     const __nv_bfloat16 *vn = has_new ? vnew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
@@ -656,24 +659,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_out = (int)((Lnew + w - 1) / w);
     const int wnew = (int)(length / w);
     const bool opens = has_new && (length % w == 0);
+    // the new token's inputs, requested now and used after the splits meet
+    uint2 nq_raw = make_uint2(0u, 0u), nk_raw = make_uint2(0u, 0u);
+    __nv_bfloat16 nv_raw = __float2bfloat16(0.f);
     if (has_new) {
-        for (int hh = warp; hh < G; hh += kWarps) {
-            const __nv_bfloat16 *qq = q + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim;
-            float d = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                d = fmaf(__bfloat162float(qq[lane * 4 + i]), __bfloat162float(kn[lane * 4 + i]), d);
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o2);
-            if (lane == 0) hNew[hh] = d * qk_scale;
+        if (warp < G) {
+            nq_raw = reinterpret_cast<const uint2 *>(q + ((int64_t)b * Hq + kvh * G + warp) * kHeadDim)[lane];
+            nk_raw = reinterpret_cast<const uint2 *>(kn)[lane];
         }
-        if (tid < kHeadDim) sVn[tid] = __bfloat162float(vn[tid]);
+        if (tid < kHeadDim) nv_raw = vn[tid];
     }
     __syncthreads();
     // this split's partial: output [G][128] (unnormalised, relative to its
     // own max) and (max, exp-sum) [G], to global memory for the other splits
     float *pacc = S.part + ((int64_t)bk * splits + split) * G * kHeadDim;
-    float2 *pml = S.part_ml + ((int64_t)bk * splits + split) * G;
     if (tid < G) {
         float M = -INFINITY;
         for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + tid]);
@@ -683,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fwt[ww * 8 + tid] = f;
             l = fmaf(f, lw_s[ww * 8 + tid], l);
         }
-        pml[tid] = make_float2(M, l);
+        sOwn[tid] = make_float2(M, l);
     }
     __syncthreads();
     for (int i = tid; i < G * kHeadDim; i += kThreads) {
@@ -696,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // statistics of this thread's first window (written to global memory by
     // this CTA's warps), its old score, and the tier of its window in this
-    // split's slice of the window range, fetched while the splits gather
+    // split's slice of the window range, fetched while the splits meet
     float *sp = D.score_part + ((int64_t)b * Hkv + kvh) * D.Wmax;
     int pwi = -1;
     float pold = 0.f;
@@ -710,36 +709,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int z0 = (int)((int64_t)split * n_out / splits), z1 = (int)((int64_t)(split + 1) * n_out / splits);
     const uint8_t ztier = z0 + tid < z1 ? D.tier[wb + z0 + tid] : (uint8_t)QEVICT_TIER_E;
 
-    // ================= barrier over the splits of this (sequence, KV head).
-    // Every CTA of the grid is resident at once (one wave), so the wait ends
-    // as soon as the last split arrives; it gives up after about two seconds.
+    // ================= the splits of this (sequence, KV head) meet. Each
+    // publishes its per-head (max, exp-sum) as 64-bit words tagged with this
+    // launch's generation, after a fence that makes its partial output
+    // visible; every split reads all records once their tags are current.
+    // The wait gives up after about two seconds (TIMEOUT).
+    const uint32_t tag = s_gen + 1u;
     __syncthreads();
     if (tid == 0) {
-        uint32_t *cnt = S.bar + 2 * bk, *gen = cnt + 1;
-        const uint32_t g0 = *(volatile uint32_t *)gen;
         __threadfence();
-        const uint32_t prev = atomicAdd(cnt, 1u);
-        if (prev == (uint32_t)(splits - 1)) {
-            *(volatile uint32_t *)cnt = 0u;
-            __threadfence();
-            atomicAdd(gen, 1u);
-        } else {
-            const long long t0 = clock64();
-            while (*(volatile uint32_t *)gen == g0) {
-                if (clock64() - t0 > kWaitCycles) {
-                    set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -3);
-                    break;
-                }
-                __nanosleep(64);
+        for (int hh = 0; hh < G; ++hh) {
+            unsigned long long *r = S.rec + ((int64_t)bk * kMaxSplits + split) * kMaxG * 2 + hh * 2;
+            const unsigned long long m64 = ((unsigned long long)tag << 32) | __float_as_uint(sOwn[hh].x);
+            const unsigned long long l64 = ((unsigned long long)tag << 32) | __float_as_uint(sOwn[hh].y);
+            asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(r), "l"(m64), "l"(l64) : "memory");
+        }
+    }
+    if (warp == kWarps - 1) {
+        // arrival count: the last split to arrive moves the generation on for
+        // the next launch (every split read it before its loop)
+        if (lane == 0) {
+            uint32_t *cnt = S.bar + 2 * bk, *gen = cnt + 1;
+            const uint32_t prev = atomicAdd(cnt, 1u);
+            if (prev == (uint32_t)(splits - 1)) {
+                *(volatile uint32_t *)cnt = 0u;
+                *(volatile uint32_t *)gen = tag;
             }
         }
-        __threadfence();
-    }
-    __syncthreads();
-    if (warp == kWarps - 1) {
-        if (split != 0 || !has_new) return;
-        // this KV head's K and V rows of the new token
-        if (slot_new >= 0) {
+        if (!has_new) return;
+        // this KV head's K and V rows of the new token (split 0)
+        if (split == 0 && slot_new >= 0) {
             const int row = (int)(length % w);
             const int kv = lane >> 4, c = lane & 15;
             const __nv_bfloat16 *src = kv ? vn : kn;
@@ -748,9 +747,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(dst) = reinterpret_cast<const uint4 *>(src)[c];
         }
         if (lane == 0) {
+            // every CTA of this sequence has read its tables once all have
+            // arrived here: the last one moves them forward
             const unsigned prev = atomicAdd(&S.arrive_b[b], 1u);
-            if (prev == (unsigned)(Hkv - 1)) {
-                // every CTA of this sequence has read its tables: move them forward
+            if (prev == (unsigned)(Hkv * splits - 1)) {
                 __threadfence();
                 int32_t *c = D.ctr + b * kCtrN;
                 if (opens) {
@@ -780,28 +780,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return;
     }
-    // max and exp-sum over the splits, per head (every CTA computes the same)
-    const float2 *ml_all = S.part_ml + (int64_t)bk * splits * G;
-    for (int hh = warp; hh < G; hh += kWarps - 1) {
+    // max and exp-sum over the splits: warp hh polls head hh's records (lane = split)
+    if (warp < G) {
+        const int hh = warp;
+        float nl = -INFINITY;   // the new token's logit
+        if (has_new) {
+            const float2 q0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&nq_raw.x));
+            const float2 q1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&nq_raw.y));
+            const float2 k0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&nk_raw.x));
+            const float2 k1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&nk_raw.y));
+            float d = fmaf(q0.x, k0.x, fmaf(q0.y, k0.y, fmaf(q1.x, k1.x, q1.y * k1.y)));
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o2);
+            nl = d * qk_scale;
+        }
         float2 v = make_float2(-INFINITY, 0.f);
-        if (lane < splits) v = __ldcg(ml_all + lane * G + hh);
+        bool ok = true;
+        if (lane < splits) {
+            const unsigned long long *r = S.rec + ((int64_t)bk * kMaxSplits + lane) * kMaxG * 2 + hh * 2;
+            unsigned long long m64, l64;
+            const long long t0 = clock64();
+            while (true) {
+                asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(m64), "=l"(l64) : "l"(r) : "memory");
+                if ((uint32_t)(m64 >> 32) == tag && (uint32_t)(l64 >> 32) == tag) break;
+                if (clock64() - t0 > kWaitCycles) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(32);
+            }
+            v = ok ? make_float2(__uint_as_float((uint32_t)m64), __uint_as_float((uint32_t)l64))
+                   : make_float2(-INFINITY, 0.f);
+        }
+        if (__any_sync(0xffffffffu, !ok) && lane == 0) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -3);
+        __threadfence();   // the partial outputs written before the records are visible now
         float M = v.x;
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-        if (has_new) M = fmaxf(M, hNew[hh]);
+        if (has_new) M = fmaxf(M, nl);
         const float f = (lane < splits && M != -INFINITY && v.x != -INFINITY) ? ex2(v.x - M) : 0.f;
         if (lane < splits) Frk[lane * 8 + hh] = f;
         float l = f * v.y;
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o2);
         if (lane == 0) {
-            const float fn = has_new ? ex2(hNew[hh] - M) : 0.f;
+            const float fn = has_new ? ex2(nl - M) : 0.f;
             l += fn;
             hM[hh] = M;
             hIL[hh] = l > 0.f ? 1.f / l : 0.f;
             hFN[hh] = fn;
+            hNew[hh] = nl;
         }
     }
+    if (has_new && tid < kHeadDim) sVn[tid] = __bfloat162float(nv_raw);
     tail_sync();
     // output: this split's slice of the [G][32] float4 outputs, each summed over the splits' partials
     {
@@ -877,6 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (accumulate && fresh) sp[wi] += sum * inv_hq;
     }
 }
+
 
 constexpr int kDynSmem = kWarps * kRing + kEntTab * 8 + 16 * 32 * 8 + 1024;
 

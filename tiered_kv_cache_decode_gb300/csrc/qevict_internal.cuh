@@ -83,9 +83,10 @@ struct LayerDev {
 // only after its dependency wait, so consecutive launches never overlap in it.
 struct DecodeScratch {
     float *part;          // [B*Hkv][splits][G][d] split partial outputs
-    float2 *part_ml;      // [B*Hkv][splits][G] split (max, exp-sum), log2 domain
+    unsigned long long *rec;   // [B*Hkv][kMaxSplits][kMaxG][2] split (max, exp-sum), log2 domain, each
+                               // float in the low half of a word whose high half is the launch's tag
     float2 *wstat;        // [B][Hq][Wmax] (window max, window exp-sum), log2 domain
-    uint32_t *bar;        // [B*Hkv][2] split barrier: arrival count (0 between launches), generation
+    uint32_t *bar;        // [B*Hkv][2] split arrival count (0 between launches), record generation
     uint32_t *arrive_b;   // [B] KV-head arrival counters for the fused append (0 between launches)
 };
 
