@@ -322,7 +322,7 @@ int64_t qevict_length(const qevict_cache *cache, int32_t layer);
  *
  * Arguments, outputs and errors are those of qevict_decode_attention.
  * The scratch a call needs is 8 B of window statistics per (sequence,
- * query head, window of max_context), 512 B per query head for each decode
+ * query head, window of max_context), 1 KiB per query head for each decode
  * split of each (sequence, KV head) (up to 32 splits, as many as fit the GPU
  * in one wave), 4 KiB of split records per (sequence, KV head) and a few
  * counters; a cache whose need passes

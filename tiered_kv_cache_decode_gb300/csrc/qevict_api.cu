@@ -280,7 +280,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     // every allocation first, so that a failing allocator leaves nothing behind
     {
         Carver cv;
-        const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * kHeadDim * 4);
+        const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * kHeadDim * 8);
         const size_t o_rec = cv.take((size_t)B * Hkv * kMaxSplits * kMaxG * 16);
         const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
         const size_t o_bar = cv.take((size_t)B * Hkv * 8);
@@ -292,7 +292,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
             delete c;
             return fail(QEVICT_ERR_OUT_OF_MEMORY, "allocation of %zu B of decode scratch failed", need);
         }
-        c->scratch.part = (float *)(base + o_part);
+        c->scratch.part = (unsigned long long *)(base + o_part);
         c->scratch.rec = (unsigned long long *)(base + o_rec);
         c->scratch.wstat = (float2 *)(base + o_ws);
         c->scratch.bar = (uint32_t *)(base + o_bar);
@@ -676,7 +676,7 @@ StaticLayout static_layout(const qevict_cache *c, int splits) {
     s.o_bar = s.o_ab + round256(B * 4);
     s.o_rec = s.o_bar + round256(B * Hkv * 8);
     s.o_part = s.o_rec + round256(B * Hkv * (size_t)kMaxSplits * kMaxG * 16);
-    s.o_ws = s.o_part + round256(B * Hkv * (size_t)splits * c->G * kHeadDim * 4);
+    s.o_ws = s.o_part + round256(B * Hkv * (size_t)splits * c->G * kHeadDim * 8);
     s.total = s.o_ws + round256(B * Hq * (size_t)c->Wmax * 8);
     return s;
 }
@@ -732,7 +732,7 @@ qevict_status qevict_decode_attention_static_scratch(qevict_cache *c, int32_t la
     S.arrive_b = (uint32_t *)(p + ly.o_ab);
     S.bar = (uint32_t *)(p + ly.o_bar);
     S.rec = (unsigned long long *)(p + ly.o_rec);
-    S.part = (float *)(p + ly.o_part);
+    S.part = (unsigned long long *)(p + ly.o_part);
     S.wstat = (float2 *)(p + ly.o_ws);
     e = launch_decode(lh.dev, c->cdev, S, lh.tmap, layer, (const __nv_bfloat16 *)q, nullptr, nullptr, out, mass,
                       accumulate_scores, splits, false, (cudaStream_t)stream);

@@ -56,6 +56,7 @@ constexpr int kTailThreads = (kWarps - 1) * 32;   // threads of the split merge 
 // shared-memory offsets used after the main loop (inside the free rings)
 constexpr int kFwtOff = 52 * 1024;     // [warp][8] weight of each warp's partial
 constexpr int kHeadOff = 54 * 1024;    // per-head merge results, per-split weights, new token's V row
+constexpr int kRedOff = 58 * 1024;     // [<= 288] float4 weighted split partials of this CTA's output slice
 constexpr int kStages = 2;                // shared-memory stages per warp
 constexpr int kStage = 8192;              // bytes per stage
 constexpr int kRing = kStages * kStage;   // bytes per warp
@@ -671,8 +672,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     // this split's partial: output [G][128] (unnormalised, relative to its
-    // own max) and (max, exp-sum) [G], to global memory for the other splits
-    float *pacc = S.part + ((int64_t)bk * splits + split) * G * kHeadDim;
+    // own max) and (max, exp-sum) [G], to global memory for the other splits.
+    // Every value goes out as a 64-bit word whose high half is this launch's
+    // tag, so a reader can tell a current value from a stale one by itself.
+    const uint32_t tag = s_gen + 1u;
+    unsigned long long *pacc = S.part + ((int64_t)bk * splits + split) * G * kHeadDim;
     if (tid < G) {
         float M = -INFINITY;
         for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + tid]);
@@ -691,7 +695,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ww = 0; ww < kWarps; ++ww)
             acc = fmaf(fwt[ww * 8 + hh], Ow[(ww * 8 + hh) * kHeadDim + c] + minw[(ww * 8 + hh) * 4 + c / kGroup], acc);
-        pacc[i] = acc;
+        const unsigned long long word = ((unsigned long long)tag << 32) | __float_as_uint(acc);
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(pacc + i), "l"(word) : "memory");
     }
     // statistics of this thread's first window (written to global memory by
     // this CTA's warps), its old score, and the tier of its window in this
@@ -710,14 +715,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint8_t ztier = z0 + tid < z1 ? D.tier[wb + z0 + tid] : (uint8_t)QEVICT_TIER_E;
 
     // ================= the splits of this (sequence, KV head) meet. Each
-    // publishes its per-head (max, exp-sum) as 64-bit words tagged with this
-    // launch's generation, after a fence that makes its partial output
-    // visible; every split reads all records once their tags are current.
-    // The wait gives up after about two seconds (TIMEOUT).
-    const uint32_t tag = s_gen + 1u;
+    // publishes its per-head (max, exp-sum) as tagged 64-bit words; every
+    // split reads all records, and later the partial outputs of its slice,
+    // once their tags are current. Each wait gives up after about two
+    // seconds (TIMEOUT).
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
         for (int hh = 0; hh < G; ++hh) {
             unsigned long long *r = S.rec + ((int64_t)bk * kMaxSplits + split) * kMaxG * 2 + hh * 2;
             const unsigned long long m64 = ((unsigned long long)tag << 32) | __float_as_uint(sOwn[hh].x);
@@ -813,7 +816,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : make_float2(-INFINITY, 0.f);
         }
         if (__any_sync(0xffffffffu, !ok) && lane == 0) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -3);
-        __threadfence();   // the partial outputs written before the records are visible now
         float M = v.x;
 #pragma unroll
         for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
@@ -834,32 +836,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (has_new && tid < kHeadDim) sVn[tid] = __bfloat162float(nv_raw);
     tail_sync();
-    // output: this split's slice of the [G][32] float4 outputs, each summed over the splits' partials
+    // output: this split's slice of the [G][32] float4 outputs. One thread
+    // per (output, split) reads that split's tagged words (waiting until they
+    // are current), weights them, and the slice's threads then sum over the
+    // splits in shared memory.
     {
         const int n4 = G * (kHeadDim / 4);
         const int o0 = split * n4 / splits, o1 = (split + 1) * n4 / splits;
-        const float4 *pa = reinterpret_cast<const float4 *>(S.part + (int64_t)bk * splits * G * kHeadDim);
-        for (int oi = o0 + tid; oi < o1; oi += kTailThreads) {
+        const int nwork = (o1 - o0) * splits;
+        float4 *red = reinterpret_cast<float4 *>(smem + kRedOff);   // [outputs of the slice][splits]
+        const unsigned long long *pw = S.part + (int64_t)bk * splits * G * kHeadDim;
+        bool ok = true;
+        for (int t = tid; t < nwork; t += kTailThreads) {
+            const int oi = o0 + t / splits, r = t % splits;
+            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
+            const unsigned long long *a4 = pw + ((int64_t)r * G + hh) * kHeadDim + 4 * c4;
+            unsigned long long u0, u1, u2, u3;
+            const long long t0 = clock64();
+            while (true) {
+                asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(u0), "=l"(u1) : "l"(a4) : "memory");
+                asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(u2), "=l"(u3) : "l"(a4 + 2) : "memory");
+                if ((uint32_t)(u0 >> 32) == tag && (uint32_t)(u1 >> 32) == tag && (uint32_t)(u2 >> 32) == tag &&
+                    (uint32_t)(u3 >> 32) == tag)
+                    break;
+                if (clock64() - t0 > kWaitCycles) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(32);
+            }
+            const float f = ok ? Frk[r * 8 + hh] : 0.f;
+            red[t] = make_float4(f * __uint_as_float((uint32_t)u0), f * __uint_as_float((uint32_t)u1),
+                                 f * __uint_as_float((uint32_t)u2), f * __uint_as_float((uint32_t)u3));
+        }
+        if (!ok) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -4);
+        tail_sync();
+        for (int t = tid; t < o1 - o0; t += kTailThreads) {
+            const int oi = o0 + t;
             const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             if (has_new) {
                 const float fn = hFN[hh];
                 acc = make_float4(fn * sVn[4 * c4], fn * sVn[4 * c4 + 1], fn * sVn[4 * c4 + 2], fn * sVn[4 * c4 + 3]);
             }
-            for (int s0 = 0; s0 < splits; s0 += 8) {
-                float4 v[8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    v[r] = s0 + r < splits ? __ldcg(pa + ((int64_t)(s0 + r) * G + hh) * (kHeadDim / 4) + c4)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const float f = s0 + r < splits ? Frk[(s0 + r) * 8 + hh] : 0.f;
-                    acc.x = fmaf(f, v[r].x, acc.x);
-                    acc.y = fmaf(f, v[r].y, acc.y);
-                    acc.z = fmaf(f, v[r].z, acc.z);
-                    acc.w = fmaf(f, v[r].w, acc.w);
-                }
+            for (int r = 0; r < splits; ++r) {
+                const float4 v = red[t * splits + r];
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
             }
             const float il = hIL[hh];
             reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =

@@ -82,7 +82,8 @@ struct LayerDev {
 // Decode scratch, shared by all layers of a cache: a decode launch touches it
 // only after its dependency wait, so consecutive launches never overlap in it.
 struct DecodeScratch {
-    float *part;          // [B*Hkv][splits][G][d] split partial outputs
+    unsigned long long *part;  // [B*Hkv][splits][G][d] split partial outputs: float in the low half,
+                               // the launch's tag in the high half of each word
     unsigned long long *rec;   // [B*Hkv][kMaxSplits][kMaxG][2] split (max, exp-sum), log2 domain, each
                                // float in the low half of a word whose high half is the launch's tag
     float2 *wstat;        // [B][Hq][Wmax] (window max, window exp-sum), log2 domain
