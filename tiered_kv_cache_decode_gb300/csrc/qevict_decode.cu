@@ -54,7 +54,6 @@ constexpr int kWarps = 12;                // warps per CTA (one CTA per SM)
 constexpr int kThreads = kWarps * 32;
 constexpr int kTailThreads = (kWarps - 1) * 32;   // threads of the split merge (the last warp appends)
 // shared-memory offsets used after the main loop (inside the free rings)
-constexpr int kFwtOff = 52 * 1024;     // [warp][8] weight of each warp's partial
 constexpr int kHeadOff = 54 * 1024;    // per-head merge results, per-split weights, new token's V row
 constexpr int kRedOff = 58 * 1024;     // [<= 288] float4 weighted split partials of this CTA's output slice
 constexpr int kStages = 2;                // shared-memory stages per warp
@@ -594,41 +593,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         try_issue();
     }
     __syncthreads();
-    // windows cut between warps: entry e = 2 warp + slot; the entries of one
-    // window are consecutive among the used ones. One thread per (entry,
-    // head) starts at each window's first entry and merges the rest.
-    if (tid < 2 * kWarps * 8) {
-        const int e = tid >> 3, hh = tid & 7;
-        const int wn = pt_win[e >> 1][e & 1];
-        if (hh < G && wn >= 0) {
-            int pe = e - 1;
-            while (pe >= 0 && pt_win[pe >> 1][pe & 1] < 0) --pe;
-            if (pe < 0 || pt_win[pe >> 1][pe & 1] != wn) {
-                float2 acc = pt_st[e >> 1][e & 1][hh];
-                for (int ne = e + 1; ne < 2 * kWarps; ++ne) {
-                    const int wv = pt_win[ne >> 1][ne & 1];
-                    if (wv < 0) continue;
-                    if (wv != wn) break;
-                    acc = stat_merge(acc, pt_st[ne >> 1][ne & 1][hh]);
-                }
-                wstat[(int64_t)hh * D.Wmax + wn] = acc;
-            }
-        }
-    }
-
-    // ---- merge the warps (the rings are free now)
-    float *Ow = reinterpret_cast<float *>(smem);                 // [warp][8 heads][128]
-    float *mw_s = Ow + kWarps * 8 * kHeadDim;                    // [warp][8]
+    // ---- merge the warps (the rings are free now); rows padded by 4 floats
+    // so that the fragment stores hit 32 different banks
+    constexpr int kOwStride = kHeadDim + 4;
+    float *Ow = reinterpret_cast<float *>(smem);                 // [warp][8 heads][kOwStride]
+    float *mw_s = Ow + kWarps * 8 * kOwStride;                   // [warp][8]
     float *lw_s = mw_s + kWarps * 8;
     float *minw = lw_s + kWarps * 8;                             // [warp][8][4]
     {
-        float *ob = Ow + warp * 8 * kHeadDim;
+        float *ob = Ow + warp * 8 * kOwStride;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            ob[(2 * t) * kHeadDim + 16 * mt + g] = o[mt][0];
-            ob[(2 * t + 1) * kHeadDim + 16 * mt + g] = o[mt][1];
-            ob[(2 * t) * kHeadDim + 16 * mt + g + 8] = o[mt][2];
-            ob[(2 * t + 1) * kHeadDim + 16 * mt + g + 8] = o[mt][3];
+            ob[(2 * t) * kOwStride + 16 * mt + g] = o[mt][0];
+            ob[(2 * t + 1) * kOwStride + 16 * mt + g] = o[mt][1];
+            ob[(2 * t) * kOwStride + 16 * mt + g + 8] = o[mt][2];
+            ob[(2 * t + 1) * kOwStride + 16 * mt + g + 8] = o[mt][3];
         }
     }
 #pragma unroll
@@ -645,14 +624,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kGroups; ++i) minw[(warp * 8 + g) * 4 + i] = minacc[i];
     }
     // per-head merge results and the new token, in the free rings
-    float *fwt = reinterpret_cast<float *>(smem + kFwtOff);                    // [warp][8]
     float *hM = reinterpret_cast<float *>(smem + kHeadOff);                    // [8] max over the splits
     float *hIL = hM + 8;                                                       // [8] 1 / exp-sum
     float *hNew = hIL + 8;                                                     // [8] new token's logit
     float *hFN = hNew + 8;                                                     // [8] new token's weight
     float *Frk = hFN + 8;                                                      // [kMaxSplits][8] weight of each split
     float *sVn = Frk + kMaxSplits * 8;                                         // [128] new token's V row
-    float2 *sOwn = reinterpret_cast<float2 *>(sVn + kHeadDim);                 // [8] this split's (max, exp-sum)
     const bool has_new = knew != nullptr;
     const __nv_bfloat16 *kn = has_new ? knew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
     const __nv_bfloat16 *vn = has_new ? vnew + ((int64_t)b * Hkv + kvh) * kHeadDim : nullptr;
@@ -670,64 +647,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (tid < kHeadDim) nv_raw = vn[tid];
     }
-    __syncthreads();
-    // this split's partial: output [G][128] (unnormalised, relative to its
-    // own max) and (max, exp-sum) [G], to global memory for the other splits.
-    // Every value goes out as a 64-bit word whose high half is this launch's
-    // tag, so a reader can tell a current value from a stale one by itself.
+    // Every value this split hands to the others leaves as a 64-bit word whose
+    // high half is this launch's tag, so a reader tells a current value from a
+    // stale one by itself and no fence is needed.
     const uint32_t tag = s_gen + 1u;
-    unsigned long long *pacc = S.part + ((int64_t)bk * splits + split) * G * kHeadDim;
-    if (tid < G) {
-        float M = -INFINITY;
-        for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + tid]);
-        float l = 0.f;
-        for (int ww = 0; ww < kWarps; ++ww) {
-            const float f = M == -INFINITY ? 0.f : ex2(mw_s[ww * 8 + tid] - M);
-            fwt[ww * 8 + tid] = f;
-            l = fmaf(f, lw_s[ww * 8 + tid], l);
-        }
-        sOwn[tid] = make_float2(M, l);
-    }
     __syncthreads();
-    for (int i = tid; i < G * kHeadDim; i += kThreads) {
-        const int hh = i / kHeadDim, c = i % kHeadDim;
-        float acc = 0.f;
+    // ---- this split's partial output [G][128] (unnormalised, relative to its
+    // own max), one thread per (head, channel); the channel-0 thread of each
+    // head also publishes the head's (max, exp-sum) record
+    {
+        unsigned long long *pacc = S.part + ((int64_t)bk * splits + split) * G * kHeadDim;
+        for (int i = tid; i < G * kHeadDim; i += kThreads) {
+            const int hh = i / kHeadDim, c = i % kHeadDim;
+            float M = -INFINITY;
 #pragma unroll
-        for (int ww = 0; ww < kWarps; ++ww)
-            acc = fmaf(fwt[ww * 8 + hh], Ow[(ww * 8 + hh) * kHeadDim + c] + minw[(ww * 8 + hh) * 4 + c / kGroup], acc);
-        const unsigned long long word = ((unsigned long long)tag << 32) | __float_as_uint(acc);
-        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(pacc + i), "l"(word) : "memory");
+            for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + hh]);
+            float acc = 0.f, l = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int ww = 0; ww < kWarps; ++ww) {
+                    const float f = ex2(mw_s[ww * 8 + hh] - M);
+                    acc = fmaf(f, Ow[(ww * 8 + hh) * kOwStride + c] + minw[(ww * 8 + hh) * 4 + c / kGroup], acc);
+                    l = fmaf(f, lw_s[ww * 8 + hh], l);
+                }
+            }
+            const unsigned long long word = ((unsigned long long)tag << 32) | __float_as_uint(acc);
+            asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(pacc + i), "l"(word) : "memory");
+            if (c == 0) {
+                unsigned long long *r = S.rec + ((int64_t)bk * kMaxSplits + split) * kMaxG * 2 + hh * 2;
+                const unsigned long long m64 = ((unsigned long long)tag << 32) | __float_as_uint(M);
+                const unsigned long long l64 = ((unsigned long long)tag << 32) | __float_as_uint(l);
+                asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(r), "l"(m64), "l"(l64) : "memory");
+            }
+        }
     }
-    // statistics of this thread's first window (written to global memory by
-    // this CTA's warps), its old score, and the tier of its window in this
-    // split's slice of the window range, fetched while the splits meet
     float *sp = D.score_part + ((int64_t)b * Hkv + kvh) * D.Wmax;
-    int pwi = -1;
-    float pold = 0.f;
-    float2 pst[G];
-    if (tid < nwin) {
-        pwi = ent(tid).x;
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) pst[hh] = wstat[(int64_t)hh * D.Wmax + pwi];
-        pold = accumulate ? sp[pwi] : 0.f;
-    }
     const int z0 = (int)((int64_t)split * n_out / splits), z1 = (int)((int64_t)(split + 1) * n_out / splits);
-    const uint8_t ztier = z0 + tid < z1 ? D.tier[wb + z0 + tid] : (uint8_t)QEVICT_TIER_E;
-
-    // ================= the splits of this (sequence, KV head) meet. Each
-    // publishes its per-head (max, exp-sum) as tagged 64-bit words; every
-    // split reads all records, and later the partial outputs of its slice,
-    // once their tags are current. Each wait gives up after about two
-    // seconds (TIMEOUT).
-    __syncthreads();
-    if (tid == 0) {
-        for (int hh = 0; hh < G; ++hh) {
-            unsigned long long *r = S.rec + ((int64_t)bk * kMaxSplits + split) * kMaxG * 2 + hh * 2;
-            const unsigned long long m64 = ((unsigned long long)tag << 32) | __float_as_uint(sOwn[hh].x);
-            const unsigned long long l64 = ((unsigned long long)tag << 32) | __float_as_uint(sOwn[hh].y);
-            asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(r), "l"(m64), "l"(l64) : "memory");
-        }
-    }
+    // masses are computed from the top warps down (mt), beside the output
+    // work of the low warps
+    const int mt = kTailThreads - 1 - tid;
+    const uint8_t ztier = (mt >= 0 && z0 + mt < z1) ? D.tier[wb + z0 + mt] : (uint8_t)QEVICT_TIER_E;
     if (warp == kWarps - 1) {
         // arrival count: the last split to arrive moves the generation on for
         // the next launch (every split read it before its loop)
@@ -782,6 +741,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         return;
+    }
+    if (warp >= G) {
+        // windows cut between warps: entry e = 2 warp + slot; the entries of
+        // one window are consecutive among the used ones. One thread per
+        // (entry, head) starts at each window's first entry and merges the
+        // rest. Done by the warps that do not poll, while the splits meet.
+        const int nmw = (kWarps - 1 - G) * 32;
+        for (int sl = tid - G * 32; sl < 2 * kWarps * G; sl += nmw) {
+            const int e = sl / G, hh = sl % G;
+            const int wn = pt_win[e >> 1][e & 1];
+            if (wn < 0) continue;
+            int pe = e - 1;
+            while (pe >= 0 && pt_win[pe >> 1][pe & 1] < 0) --pe;
+            if (pe >= 0 && pt_win[pe >> 1][pe & 1] == wn) continue;
+            float2 acc = pt_st[e >> 1][e & 1][hh];
+            for (int ne = e + 1; ne < 2 * kWarps; ++ne) {
+                const int wv = pt_win[ne >> 1][ne & 1];
+                if (wv < 0) continue;
+                if (wv != wn) break;
+                acc = stat_merge(acc, pt_st[ne >> 1][ne & 1][hh]);
+            }
+            wstat[(int64_t)hh * D.Wmax + wn] = acc;
+        }
+        asm volatile("bar.sync 2, %0;" ::"r"(nmw) : "memory");
+    }
+    // statistics of the first window of each mass thread of those warps (all
+    // in global memory now) and its old score, fetched while the splits meet
+    const bool pre = warp >= G && mt < nwin;
+    int pwi = -1;
+    float pold = 0.f;
+    float2 pst[G];
+    if (pre) {
+        pwi = ent(mt).x;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) pst[hh] = wstat[(int64_t)hh * D.Wmax + pwi];
+        pold = accumulate ? sp[pwi] : 0.f;
     }
     // max and exp-sum over the splits: warp hh polls head hh's records (lane = split)
     if (warp < G) {
@@ -840,14 +835,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // per (output, split) reads that split's tagged words (waiting until they
     // are current), weights them, and the slice's threads then sum over the
     // splits in shared memory.
-    {
+    if (warp < (((split + 1) * G * (kHeadDim / 4) / splits - split * G * (kHeadDim / 4) / splits) * splits + 31) / 32) {
         const int n4 = G * (kHeadDim / 4);
         const int o0 = split * n4 / splits, o1 = (split + 1) * n4 / splits;
         const int nwork = (o1 - o0) * splits;
+        const int out_warps = (nwork + 31) / 32;   // warps that take part (named barrier 3)
         float4 *red = reinterpret_cast<float4 *>(smem + kRedOff);   // [outputs of the slice][splits]
         const unsigned long long *pw = S.part + (int64_t)bk * splits * G * kHeadDim;
         bool ok = true;
-        for (int t = tid; t < nwork; t += kTailThreads) {
+        for (int t = tid; t < nwork; t += out_warps * 32) {
             const int oi = o0 + t / splits, r = t % splits;
             const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
             const unsigned long long *a4 = pw + ((int64_t)r * G + hh) * kHeadDim + 4 * c4;
@@ -870,8 +866,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  f * __uint_as_float((uint32_t)u2), f * __uint_as_float((uint32_t)u3));
         }
         if (!ok) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -4);
-        tail_sync();
-        for (int t = tid; t < o1 - o0; t += kTailThreads) {
+        asm volatile("bar.sync 3, %0;" ::"r"(out_warps * 32) : "memory");
+        for (int t = tid; t < o1 - o0; t += out_warps * 32) {
             const int oi = o0 + t;
             const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -894,11 +890,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- masses and cumulative scores of this split's windows
     const float inv_hq = 1.f / (float)Hq;
-    for (int li = tid; li < nwin; li += kTailThreads) {
+    for (int li = mt; li < nwin; li += kTailThreads) {
         int wi = pwi;
         float old = pold;
         float2 st[G];
-        if (li == tid) {
+        if (li == mt && pre) {
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) st[hh] = pst[hh];
         } else {
@@ -920,9 +916,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // windows no split holds: evicted ones (mass 0) and a window this step
     // opens; the window range is sliced over the splits
-    for (int wi = z0 + tid; wi < z1; wi += kTailThreads) {
+    for (int wi = z0 + mt; wi < z1; wi += kTailThreads) {
         const bool fresh = opens && wi == wnew;
-        if (!fresh && (wi == z0 + tid ? ztier : D.tier[wb + wi]) != QEVICT_TIER_E) continue;
+        if (!fresh && (wi == z0 + mt ? ztier : D.tier[wb + wi]) != QEVICT_TIER_E) continue;
         float sum = 0.f;
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
@@ -933,7 +929,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (accumulate && fresh) sp[wi] += sum * inv_hq;
     }
 }
-
 
 constexpr int kDynSmem = kWarps * kRing + kEntTab * 8 + 16 * 32 * 8 + 1024;
 
