@@ -138,6 +138,25 @@ def test_full_size_llama_b1_32k_20pct_one_layer():
     check_decode(cache, 0, ref, synth.queries(0, 0, 0, B, Hq, 128))
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,w,L,beta", [
+    (8, 32, 8, 64, 32768, 0.05),    # Llama-8B-shaped batch 8: 64 (sequence, KV head) pairs, 2 splits each
+    (16, 28, 4, 64, 16384, 0.10),   # Qwen-7B-shaped batch 16: G = 7, 64 pairs
+    (4, 32, 8, 32, 8192, 0.20),     # a Mistral-7B-shaped sweep point: 32-token windows
+])
+def test_full_size_batched_workloads_one_layer(B, Hq, Hkv, w, L, beta):
+    """One full-size layer of the batched workloads, decoded twice (the second
+    decode follows the first on the same scratch, so stale records from the
+    first must not be taken for the second's)."""
+    W = L // w
+    scores = synth.zipf_scores(5, 0, B, W)
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, beta=beta, scores=[scores], seed=5)
+    t = ref.tiers()
+    assert (t == O.TIER_Q).any() and (t == O.TIER_E).any()
+    check_state(cache, 0, ref)
+    for step in range(2):
+        check_decode(cache, 0, ref, synth.queries(5, 0, step, B, Hq, 128))
+
+
 def test_device_errors_set_status_without_faulting():
     B, Hq, Hkv, w, L = 1, 8, 2, 32, 100
     cache, (ref,) = make_pair(B, Hq, Hkv, w, L, tiers=[torch.zeros(B, 4, dtype=torch.uint8)],
