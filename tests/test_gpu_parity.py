@@ -68,6 +68,8 @@ def test_quantiser_edge_groups_bit_exact():
     k[0, 0:16, 1, 32:64] = torch.tensor([-1, -0.5, 0, 0.5] * 8, dtype=torch.bfloat16)   # exact grid
     v[0, 16:32, 0, :] = (v[0, 16:32, 0, :].float() * 1e-5 + 1e-5).to(torch.bfloat16)  # subnormal range
     v[0, 32:48, 1, 64:96] = (v[0, 32:48, 1, 64:96].float() * 300).to(torch.bfloat16)   # wide range
+    k[0, 16:32, 1, 96:128] = (k[0, 16:32, 1, 96:128].float() * 30).to(torch.bfloat16)    # wide keys
+    k[0, 32:48, 0, 0:32] = (k[0, 32:48, 0, 0:32].float() * 300).to(torch.bfloat16)       # very wide keys
     tiers = torch.tensor([[1, 1, 1, 0]], dtype=torch.uint8)
     cache = binding.TieredCache(B, 1, 4, Hkv, w, L, fp_capacity=4, ledger_capacity=4)
     cache.prefill(0, k.cuda(), v.cuda(), tiers=tiers.cuda())
