@@ -279,13 +279,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // entry, merged with its neighbour's after the loop.
     const uint64_t l2_stream = evict_first_policy();
     const int n_units = nwin * mu;
+    // unit -> (window, unit in window): a shift when mu is a power of two
+    const bool mu_pow2 = (mu & (mu - 1)) == 0;
+    const int lmu = 31 - __clz(mu);
+    auto win_of = [&](int u) -> int { return mu_pow2 ? u >> lmu : u / mu; };
     const int u_beg = (int)((int64_t)n_units * warp / kWarps);
     const int u_end = (int)((int64_t)n_units * (warp + 1) / kWarps);
     int iu = u_beg;                  // next unit to issue
     int issued = 0, consumed = 0;    // stages issued / consumed
     auto try_issue = [&]() {
         while (iu < u_end && issued - consumed < kStages) {
-            const int li = iu / mu, j = iu - li * mu;
+            const int li = win_of(iu), j = iu - li * mu;
             const int st = issued % kStages;
             const uint32_t bar = smem_u32(&bars[warp][st]);
             const uint32_t dst = ring_s + st * kStage;
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 int done = 0;
                 while (done < n) {
-                    const int lq = iu / mu, jq = iu - lq * mu;
+                    const int lq = win_of(iu), jq = iu - lq * mu;
                     const int2 en = ent(lq);
                     const int run = min(mu - jq, n - done);
                     if (lane == 0) {
