@@ -12,7 +12,9 @@ One step = one decode token through all 32 layers: per layer one fused call
 that appends the token's K/V and runs tiered decode attention with the
 per-window mass added to the cumulative scores; every 64th step ends with a
 routing event on every layer (rank, evict, demote with the write-once ledger,
-promote). Steps are replayed as CUDA graphs captured from the C ABI calls.
+promote; the layers' routes run side by side on 8 streams, since no layer's
+routing depends on another's). Steps are replayed as CUDA graphs captured
+from the C ABI calls.
 
 Prints one JSON line. ``--impl reference`` times the CPU oracle instead.
 """
@@ -289,6 +291,7 @@ def run_native(args, rank, world, local_rank):
     vv = [xin[l, nq + nkv:].view(B, Hkv, d) for l in range(NL)]
 
     stream = torch.cuda.Stream(device=dev)
+    route_streams = [torch.cuda.Stream(device=dev) for _ in range(8)]
     g_step, g_route, g_decode = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -296,9 +299,19 @@ def run_native(args, rank, world, local_rank):
             for l in range(NL):
                 cache.decode_step(l, qv[l], kv_[l], vv[l], out=xout[l], want_mass=False, accumulate=True,
                                   stream=stream)
+        # a routing event: the layers are independent, so their routes run
+        # side by side on a few streams, forked from and joined back to the step's
         with torch.cuda.graph(g_route, stream=stream):
+            fork = torch.cuda.Event()
+            fork.record(stream)
+            for rs in route_streams:
+                rs.wait_event(fork)
             for l in range(NL):
-                cache.route(l, stream=stream)
+                cache.route(l, stream=route_streams[l % len(route_streams)])
+            for rs in route_streams:
+                join = torch.cuda.Event()
+                join.record(rs)
+                stream.wait_event(join)
         with torch.cuda.graph(g_decode, stream=stream):
             for l in range(NL):
                 cache.decode(l, qv[l], out=xout[l], want_mass=False, accumulate=True, stream=stream)

@@ -159,6 +159,28 @@ def test_full_size_batched_workloads_one_layer(B, Hq, Hkv, w, L, beta):
         check_decode(cache, 0, ref, synth.queries(5, 0, step, B, Hq, 128))
 
 
+def test_layers_route_concurrently_on_separate_streams():
+    """Routing events of different layers share no state: routed side by side
+    on their own streams they give exactly the sequential result."""
+    B, Hq, Hkv, w, L, layers = 2, 16, 4, 64, 2048, 4
+    W = L // w
+    scores = [synth.zipf_scores(7, l, B, W) for l in range(layers)]
+    cache, refs = make_pair(B, Hq, Hkv, w, L, layers=layers, beta=0.5, scores=scores)
+    new_scores = [synth.zipf_scores(8, l, B, W) for l in range(layers)]
+    streams = [torch.cuda.Stream() for _ in range(layers)]
+    torch.cuda.synchronize()
+    for l in range(layers):
+        with torch.cuda.stream(streams[l]):
+            cache.route(l, scores_override=new_scores[l].cuda(), stream=streams[l])
+    torch.cuda.synchronize()
+    assert cache.status() == 0, cache.last_error()
+    for l in range(layers):
+        refs[l].route(scores_override=new_scores[l].numpy())
+        check_state(cache, l, refs[l])
+        check_decode(cache, l, refs[l], synth.queries(8, l, 0, B, Hq, 128))
+    check_stats(cache, refs)
+
+
 def test_device_errors_set_status_without_faulting():
     B, Hq, Hkv, w, L = 1, 8, 2, 32, 100
     cache, (ref,) = make_pair(B, Hq, Hkv, w, L, tiers=[torch.zeros(B, 4, dtype=torch.uint8)],
