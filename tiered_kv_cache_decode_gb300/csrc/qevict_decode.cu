@@ -782,6 +782,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < G; ++hh) pst[hh] = wstat[(int64_t)hh * D.Wmax + pwi];
         pold = accumulate ? sp[pwi] : 0.f;
     }
+    // ---- output gather: this split's slice of the [G][32] float4 outputs,
+    // one (output, split) item per thread of the warps that do not poll. Each
+    // waits until the four tagged words of its item are current and keeps the
+    // raw values; they are weighted and summed once the splits have met.
+    const int n4 = G * (kHeadDim / 4);
+    const int o0 = split * n4 / splits, o1 = (split + 1) * n4 / splits;
+    const int nwork = (o1 - o0) * splits;
+    float4 *red = reinterpret_cast<float4 *>(smem + kRedOff);   // [outputs of the slice][splits]
+    if (warp >= G) {
+        const unsigned long long *pw = S.part + (int64_t)bk * splits * G * kHeadDim;
+        bool ok = true;
+        for (int t = tid - G * 32; t < nwork; t += (kWarps - 1 - G) * 32) {
+            const int oi = o0 + t / splits, r = t % splits;
+            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
+            const unsigned long long *a4 = pw + ((int64_t)r * G + hh) * kHeadDim + 4 * c4;
+            unsigned long long u0, u1, u2, u3;
+            const long long t0 = clock64();
+            while (true) {
+                asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(u0), "=l"(u1) : "l"(a4) : "memory");
+                asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(u2), "=l"(u3) : "l"(a4 + 2) : "memory");
+                if ((uint32_t)(u0 >> 32) == tag && (uint32_t)(u1 >> 32) == tag && (uint32_t)(u2 >> 32) == tag &&
+                    (uint32_t)(u3 >> 32) == tag)
+                    break;
+                if (clock64() - t0 > kWaitCycles) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(32);
+            }
+            red[t] = ok ? make_float4(__uint_as_float((uint32_t)u0), __uint_as_float((uint32_t)u1),
+                                      __uint_as_float((uint32_t)u2), __uint_as_float((uint32_t)u3))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (!ok) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -4);
+    }
     // max and exp-sum over the splits: warp hh polls head hh's records (lane = split)
     if (warp < G) {
         const int hh = warp;
@@ -835,61 +870,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (has_new && tid < kHeadDim) sVn[tid] = __bfloat162float(nv_raw);
     tail_sync();
-    // output: this split's slice of the [G][32] float4 outputs. One thread
-    // per (output, split) reads that split's tagged words (waiting until they
-    // are current), weights them, and the slice's threads then sum over the
-    // splits in shared memory.
-    if (warp < (((split + 1) * G * (kHeadDim / 4) / splits - split * G * (kHeadDim / 4) / splits) * splits + 31) / 32) {
-        const int n4 = G * (kHeadDim / 4);
-        const int o0 = split * n4 / splits, o1 = (split + 1) * n4 / splits;
-        const int nwork = (o1 - o0) * splits;
-        const int out_warps = (nwork + 31) / 32;   // warps that take part (named barrier 3)
-        float4 *red = reinterpret_cast<float4 *>(smem + kRedOff);   // [outputs of the slice][splits]
-        const unsigned long long *pw = S.part + (int64_t)bk * splits * G * kHeadDim;
-        bool ok = true;
-        for (int t = tid; t < nwork; t += out_warps * 32) {
-            const int oi = o0 + t / splits, r = t % splits;
-            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
-            const unsigned long long *a4 = pw + ((int64_t)r * G + hh) * kHeadDim + 4 * c4;
-            unsigned long long u0, u1, u2, u3;
-            const long long t0 = clock64();
-            while (true) {
-                asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(u0), "=l"(u1) : "l"(a4) : "memory");
-                asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(u2), "=l"(u3) : "l"(a4 + 2) : "memory");
-                if ((uint32_t)(u0 >> 32) == tag && (uint32_t)(u1 >> 32) == tag && (uint32_t)(u2 >> 32) == tag &&
-                    (uint32_t)(u3 >> 32) == tag)
-                    break;
-                if (clock64() - t0 > kWaitCycles) {
-                    ok = false;
-                    break;
-                }
-                __nanosleep(32);
-            }
-            const float f = ok ? Frk[r * 8 + hh] : 0.f;
-            red[t] = make_float4(f * __uint_as_float((uint32_t)u0), f * __uint_as_float((uint32_t)u1),
-                                 f * __uint_as_float((uint32_t)u2), f * __uint_as_float((uint32_t)u3));
+    // output: weight the gathered partials by their splits' factors and sum
+    for (int t = tid; t < o1 - o0; t += kTailThreads) {
+        const int oi = o0 + t;
+        const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (has_new) {
+            const float fn = hFN[hh];
+            acc = make_float4(fn * sVn[4 * c4], fn * sVn[4 * c4 + 1], fn * sVn[4 * c4 + 2], fn * sVn[4 * c4 + 3]);
         }
-        if (!ok) set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -4);
-        asm volatile("bar.sync 3, %0;" ::"r"(out_warps * 32) : "memory");
-        for (int t = tid; t < o1 - o0; t += out_warps * 32) {
-            const int oi = o0 + t;
-            const int hh = oi / (kHeadDim / 4), c4 = oi % (kHeadDim / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has_new) {
-                const float fn = hFN[hh];
-                acc = make_float4(fn * sVn[4 * c4], fn * sVn[4 * c4 + 1], fn * sVn[4 * c4 + 2], fn * sVn[4 * c4 + 3]);
-            }
-            for (int r = 0; r < splits; ++r) {
-                const float4 v = red[t * splits + r];
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-            const float il = hIL[hh];
-            reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
-                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        for (int r = 0; r < splits; ++r) {
+            const float f = Frk[r * 8 + hh];
+            const float4 v = red[t * splits + r];
+            acc.x = fmaf(f, v.x, acc.x);
+            acc.y = fmaf(f, v.y, acc.y);
+            acc.z = fmaf(f, v.z, acc.z);
+            acc.w = fmaf(f, v.w, acc.w);
         }
+        const float il = hIL[hh];
+        reinterpret_cast<float4 *>(out + ((int64_t)b * Hq + kvh * G + hh) * kHeadDim)[c4] =
+            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
     }
 
     // ---- masses and cumulative scores of this split's windows
