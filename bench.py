@@ -149,6 +149,15 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def run_config(wl, NL, world):
+    """The workload description both arms print."""
+    return {"workload": WORKLOAD if NL == wl["layers"] else f"{WORKLOAD} ({NL} of {wl['layers']} layers)",
+            "batch": wl["B"], "layers": NL, "q_heads": wl["Hq"], "kv_heads": wl["Hkv"],
+            "head_dim": 128, "context": wl["L"], "window": wl["w"], "budget_frac": wl["beta"],
+            "fp_share": wl["rho"], "route_every": ROUTE_EVERY, "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2 ({NL} layers x ~26.8 MB of tiered cache)"}
+
+
 def combine_ranks(ms, e2e_s, nbytes, e2e_bytes, world, device):
     """Whole-job figures over the ranks (each runs its own replica): the
     slowest rank's times and the bytes of all ranks."""
@@ -413,11 +422,7 @@ def run_native(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD if NL == wl["layers"] else f"{WORKLOAD} ({NL} of {wl['layers']} layers)",
-                   "batch": B, "layers": NL, "q_heads": Hq, "kv_heads": Hkv,
-                   "head_dim": d, "context": L0, "window": w, "budget_frac": wl["beta"], "fp_share": wl["rho"],
-                   "route_every": ROUTE_EVERY, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2 ({NL} layers x ~26.8 MB of tiered cache)"},
+        "config": run_config(wl, NL, world),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "kernel": "decode_kernel (tiered split-K decode + combine + score + append)",
@@ -456,7 +461,7 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(spent / max(1, per_step) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sampled_layers": nw},
+            "config": run_config(wl, wl["layers"], world),
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nw, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
