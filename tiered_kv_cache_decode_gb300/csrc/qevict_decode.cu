@@ -245,11 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int n_win = (int)((length + w - 1) / w);
     const int n_fp = ctr[CTR_NFP], n_q = ctr[CTR_NQ];
-    // full-precision slot that receives this step's token, read before this CTA
-    // arrives (the sequence's last CTA moves CTR_NEXT afterwards)
-    const int slot_new = knew == nullptr ? -1
-                         : (length % w == 0) ? *(volatile const int32_t *)&ctr[CTR_NEXT]
-                                             : *(volatile const int32_t *)&D.fp_slot[wb + length / w];
     const Range R = split_range(split, splits, n_fp, n_q);
     const int nfw = R.f1 - R.f0;                       // full-precision windows of this split
     const int nwin = nfw + (R.q1 - R.q0);              // windows of this split
@@ -692,19 +687,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int mt = kTailThreads - 1 - tid;
     const uint8_t ztier = (mt >= 0 && z0 + mt < z1) ? D.tier[wb + z0 + mt] : (uint8_t)QEVICT_TIER_E;
     if (warp == kWarps - 1) {
-        // arrival count: the last split to arrive moves the generation on for
-        // the next launch (every split read it before its loop)
-        if (lane == 0) {
-            uint32_t *cnt = S.bar + 2 * bk, *gen = cnt + 1;
-            const uint32_t prev = atomicAdd(cnt, 1u);
-            if (prev == (uint32_t)(splits - 1)) {
-                *(volatile uint32_t *)cnt = 0u;
-                *(volatile uint32_t *)gen = tag;
-            }
-        }
-        if (!has_new) return;
-        // this KV head's K and V rows of the new token (split 0)
-        if (split == 0 && slot_new >= 0) {
+        // this KV head's K and V rows of the new token (split 0), into the
+        // slot that receives it: read before this CTA arrives below (the
+        // sequence's last CTA moves CTR_NEXT only after every CTA arrived)
+        const int slot_new = (!has_new || split != 0) ? -1
+                             : opens ? *(volatile const int32_t *)&ctr[CTR_NEXT]
+                                     : *(volatile const int32_t *)&D.fp_slot[wb + wnew];
+        if (slot_new >= 0) {
             const int row = (int)(length % w);
             const int kv = lane >> 4, c = lane & 15;
             const __nv_bfloat16 *src = kv ? vn : kn;
@@ -713,11 +702,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(dst) = reinterpret_cast<const uint4 *>(src)[c];
         }
         if (lane == 0) {
-            // every CTA of this sequence has read its tables once all have
-            // arrived here: the last one moves them forward
-            const unsigned prev = atomicAdd(&S.arrive_b[b], 1u);
-            if (prev == (unsigned)(Hkv * splits - 1)) {
-                __threadfence();
+            // Two arrival counts, requested together. Per (sequence, KV head):
+            // the last split moves the record generation on for the next
+            // launch. Per sequence (fused append only): every CTA of the
+            // sequence has read its tables once all have arrived, so the last
+            // one moves them forward (tables written only by earlier launches).
+            uint32_t *cnt = S.bar + 2 * bk, *gen = cnt + 1;
+            const uint32_t prev = atomicAdd(cnt, 1u);
+            const unsigned prev_b = has_new ? atomicAdd(&S.arrive_b[b], 1u) : 0u;
+            if (prev == (uint32_t)(splits - 1)) {
+                *(volatile uint32_t *)cnt = 0u;
+                *(volatile uint32_t *)gen = tag;
+            }
+            if (has_new && prev_b == (unsigned)(Hkv * splits - 1)) {
                 int32_t *c = D.ctr + b * kCtrN;
                 if (opens) {
                     const int slotn = c[CTR_NEXT];
