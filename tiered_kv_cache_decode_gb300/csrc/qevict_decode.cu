@@ -143,6 +143,11 @@ __device__ __forceinline__ void mma_c(float (&d)[4], uint32_t a0, uint32_t a1, u
 }
 // barrier among the merge warps of the last CTA (named barrier 1)
 __device__ __forceinline__ void tail_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTailThreads) : "memory"); }
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -543,27 +548,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) x[i] *= qk_scale;
             softmax4(x);
-            uint4 vmeta[4];
-            vmeta[0] = lds128(vm + (2 * t) * 16);
-            vmeta[1] = lds128(vm + (2 * t + 8) * 16);
-            vmeta[2] = lds128(vm + (2 * t + 1) * 16);
-            vmeta[3] = lds128(vm + (2 * t + 9) * 16);
-            const uint4 v0 = lds128(vc + g * 64), v1 = lds128(vc + g * 64 + 16);
-            const uint4 v2 = lds128(vc + g * 64 + 32), v3 = lds128(vc + g * 64 + 48);
+            // each group's V codes and meta are loaded where they are used,
+            // which keeps fewer registers live across the unit
+            const int vtok[4] = {2 * t, 2 * t + 8, 2 * t + 1, 2 * t + 9};
 #pragma unroll
             for (int grp = 0; grp < kGroups; ++grp) {
+                const uint4 vv = lds128(vc + g * 64 + grp * 16);
+                uint32_t vmg[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vmg[i] = lds32(vm + vtok[i] * 16 + grp * 4);
                 float val[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float2 sm = h2f(pick(vmeta[i], grp));
+                    const float2 sm = h2f(vmg[i]);
                     val[i] = x[i] * sm.x;
                     minacc[grp] = fmaf(x[i], sm.y, minacc[grp]);
                 }
                 uint32_t b0h, b0l, b1h, b1l;
                 split2(val[0], val[1], b0h, b0l);
                 split2(val[2], val[3], b1h, b1l);
-                // words of this lane's channels: mt = 2 grp, 2 grp + 1; h = 0 (channel g), 1 (g + 8)
-                const uint4 &vv = grp == 0 ? v0 : grp == 1 ? v1 : grp == 2 ? v2 : v3;
+                // words of this lane's channels in vv: mt = 2 grp, 2 grp + 1; h = 0 (channel g), 1 (g + 8)
 #pragma unroll
                 for (int mm = 0; mm < 2; ++mm) {
                     const int mt = 2 * grp + mm;
