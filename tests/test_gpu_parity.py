@@ -159,6 +159,33 @@ def test_full_size_batched_workloads_one_layer(B, Hq, Hkv, w, L, beta):
         check_decode(cache, 0, ref, synth.queries(5, 0, step, B, Hq, 128))
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,w,L,beta", [
+    (2, 64, 8, 48, 3000, 0.2),     # G = 8, windows of 3 units
+    (1, 8, 8, 80, 2000, 0.3),      # G = 1, windows of 5 units
+    (3, 12, 4, 112, 1500, 0.25),   # G = 3, windows of 7 units
+    (2, 20, 4, 96, 2500, 0.15),    # G = 5, windows of 6 units
+])
+def test_uneven_windows_and_group_sizes(B, Hq, Hkv, w, L, beta):
+    """Window sizes whose unit count is not a power of two, and group sizes
+    from 1 to 8, through routing, decode and a fused decode step."""
+    W = -(-L // w)
+    scores = synth.zipf_scores(9, 0, B, W)
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, beta=beta, scores=[scores], max_context=L + 8, seed=9)
+    t = ref.tiers()
+    assert (t == O.TIER_Q).any()
+    check_state(cache, 0, ref)
+    check_decode(cache, 0, ref, synth.queries(9, 0, 0, B, Hq, 128))
+    k, v = synth.kv_tokens(9, 0, B, L, 1, Hkv, 128, "heavy")
+    q = synth.queries(9, 0, 1, B, Hq, 128)
+    out, mass = cache.decode_step(0, q.cuda(), k[:, 0].cuda(), v[:, 0].cuda())
+    torch.cuda.synchronize()
+    ref.append(k.float().numpy(), v.float().numpy())
+    ro, rm = ref.decode(q.float().numpy())
+    close(out.cpu().numpy(), ro, "decode step output")
+    close(mass.cpu().numpy(), rm, "decode step mass")
+    assert cache.status() == 0, cache.last_error()
+
+
 def test_layers_route_concurrently_on_separate_streams():
     """Routing events of different layers share no state: routed side by side
     on their own streams they give exactly the sequential result."""
