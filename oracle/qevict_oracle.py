@@ -366,10 +366,17 @@ class OracleCache:
             if c == TIER_Q and t == TIER_FP:
                 self._promote(b, wi)
 
+    def tiers_now(self, b):
+        return [win.tier for win in self.win[b]]
+
     def set_tiers(self, tiers):
         tiers = np.asarray(tiers, np.uint8)
+        counts = []
         for b in range(self.B):
+            old = self.tiers_now(b)
             self.apply_tiers(b, tiers[b])
+            counts.append(transition_counts(old, self.tiers_now(b)))
+        self.last_counts = np.stack(counts)
 
     def route(self, scores_override=None, score_mult=None):
         """A routing event: optionally replace / scale the scores, rank, move tiers."""
@@ -379,10 +386,13 @@ class OracleCache:
         if score_mult is not None:
             mu = np.asarray(score_mult, np.float64)
             self.S = [self.S[b] * mu[b, :self.W] for b in range(self.B)]
+        counts = []
         for b in range(self.B):
-            new = route_tiers(self.S[b], [x.tier for x in self.win[b]], self.L, self.w,
-                              self.Hkv, self.d, self.beta, self.rho)
+            old = self.tiers_now(b)
+            new = route_tiers(self.S[b], old, self.L, self.w, self.Hkv, self.d, self.beta, self.rho)
             self.apply_tiers(b, new)
+            counts.append(transition_counts(old, self.tiers_now(b)))
+        self.last_counts = np.stack(counts)
 
     def prefill(self, k, v, scores=None, tiers=None):
         """Fill an empty cache with L tokens (all full precision), then route or set tiers."""
@@ -394,12 +404,16 @@ class OracleCache:
             self.set_tiers(tiers)
 
     def demote(self, pairs):
+        old = [self.tiers_now(b) for b in range(self.B)]
         for b, wi in pairs:
             self._demote(b, wi)
+        self.last_counts = np.stack([transition_counts(old[b], self.tiers_now(b)) for b in range(self.B)])
 
     def promote(self, pairs):
+        old = [self.tiers_now(b) for b in range(self.B)]
         for b, wi in pairs:
             self._promote(b, wi)
+        self.last_counts = np.stack([transition_counts(old[b], self.tiers_now(b)) for b in range(self.B)])
 
     # ---- decode attention + cumulative scoring ----------------------------
     def window_kv(self, b, wi, kvh):
@@ -454,6 +468,47 @@ class OracleCache:
             if accumulate:
                 self.S[b] = self.S[b] + mass[b].mean(axis=0)
         return out, mass
+
+
+def transition_counts(old, new):
+    """Diagnostics of one move of a sequence's tiers (QEvict, Kernbijdragen:
+    selection churn and latent importance reactivation), with the full
+    precision tier read as the active set:
+    [fp_before, q_before, fp_after, q_after, kept, promoted, demoted, evicted],
+    where kept counts windows full precision before and after, promoted INT2 ->
+    full precision, demoted full precision -> INT2, evicted visible -> evicted.
+    Selection churn = 1 - kept / fp_after; reactivation rate = promoted /
+    q_before."""
+    old = np.asarray(old)
+    new = np.asarray(new)
+    return np.array([
+        int((old == TIER_FP).sum()), int((old == TIER_Q).sum()),
+        int((new == TIER_FP).sum()), int((new == TIER_Q).sum()),
+        int(((old == TIER_FP) & (new == TIER_FP)).sum()),
+        int(((old == TIER_Q) & (new == TIER_FP)).sum()),
+        int(((old == TIER_FP) & (new == TIER_Q)).sum()),
+        int(((old != TIER_E) & (new == TIER_E)).sum()),
+    ], dtype=np.int64)
+
+
+def future_missed_mass(cache, q, k_full):
+    """Future missed mass (QEvict, Kernbijdragen): the share of a query's
+    attention over the full, never-evicted cache that falls on windows the
+    cache has evicted. q [B][Hq][d], k_full [B][L][Hkv][d] (the keys of all L
+    tokens as stored before any tier move); returns [B][Hq] in float64."""
+    q = np.asarray(q, np.float64)
+    k_full = np.asarray(k_full, np.float64)
+    B, L, Hkv, d = k_full.shape
+    G = cache.Hq // Hkv
+    out = np.zeros((B, cache.Hq))
+    for b in range(B):
+        tier_of_tok = np.array([cache.win[b][t // cache.w].tier for t in range(L)])
+        for h in range(cache.Hq):
+            s = k_full[b, :, h // G, :] @ q[b, h] / np.sqrt(d)
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            out[b, h] = p[tier_of_tok == TIER_E].sum()
+    return out
 
 
 def tiered_bytes(cache: OracleCache) -> int:

@@ -431,3 +431,76 @@ def test_multistep_invariants():
             seen_e |= (t == O.TIER_E)
     assert all(win.ledger_writes <= 1 for b in range(B) for win in c.win[b])
     assert c.stats["promotions"] > 0 and c.stats["demotions"] > 0
+
+
+# ---------------------------------------------------------------- diagnostics
+
+def test_transition_counts_hand_derived():
+    """Before FP FP Q Q E FP, after FP Q FP E E FP: 3 FP / 2 INT2 before, 3 / 1
+    after; windows 0 and 5 stay, 2 is promoted, 1 demoted, 3 evicted."""
+    F, Q, E = O.TIER_FP, O.TIER_Q, O.TIER_E
+    c = O.transition_counts([F, F, Q, Q, E, F], [F, Q, F, E, E, F])
+    assert c.tolist() == [3, 2, 3, 1, 2, 1, 1, 1]
+
+
+def test_route_counts_invariants():
+    """Over routing events on random scores: the active set after the event is
+    what stayed plus what was promoted (routing opens no window), what left is
+    what was demoted or evicted, and visible windows never grow."""
+    rng = np.random.default_rng(3)
+    B, Hq, Hkv, w, L = 2, 8, 2, 32, 1024
+    k = rng.standard_normal((B, L, Hkv, 128))
+    c = O.OracleCache(B, Hq, Hkv, 128, w, beta=0.3)
+    c.prefill(k, k, scores=rng.random((B, L // w)))
+    for _ in range(5):
+        c.route(scores_override=rng.random((B, L // w)))
+        for fpb, qb, fpa, qa, kept, prom, dem, ev in c.last_counts:
+            assert fpa == kept + prom
+            fp_evicted = fpb - kept - dem            # left the active set straight to eviction
+            q_evicted = ev - fp_evicted
+            assert fp_evicted >= 0 and 0 <= q_evicted <= qb
+            assert qa == qb - prom - q_evicted + dem  # the INT2 tier is conserved
+            assert 0.0 <= 1 - kept / fpa <= 1.0
+
+
+def test_future_missed_mass_closed_forms():
+    """No window evicted: 0. Constant keys (all logits equal): the evicted share
+    of the tokens. And it equals the mass a fully full-precision twin cache
+    puts on the windows the tiered cache has evicted."""
+    rng = np.random.default_rng(4)
+    B, Hq, Hkv, w, L = 1, 4, 2, 16, 128
+    k = rng.standard_normal((B, L, Hkv, 128)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, 128))
+    W = L // w
+    full = O.OracleCache(B, Hq, Hkv, 128, w)
+    full.prefill(k, k, tiers=np.zeros((B, W), np.uint8))
+    assert np.all(O.future_missed_mass(full, q, k) == 0.0)
+    tiers = np.array([[2, 0, 2, 1, 2, 2, 0, 0]], np.uint8)
+    tiered = O.OracleCache(B, Hq, Hkv, 128, w)
+    tiered.prefill(k, k, tiers=tiers)
+    _, mass_full = full.decode(q, accumulate=False)
+    expect = mass_full[:, :, tiers[0] == 2].sum(axis=2)
+    assert np.allclose(O.future_missed_mass(tiered, q, k), expect, rtol=0, atol=1e-12)
+    const = np.ones((B, L, Hkv, 128), np.float32)
+    tc = O.OracleCache(B, Hq, Hkv, 128, w)
+    tc.prefill(const, const, tiers=tiers)
+    assert np.allclose(O.future_missed_mass(tc, q, const), 4 * w / L, rtol=0, atol=1e-12)
+
+
+def test_future_missed_mass_matches_library_softmax():
+    """Against torch's softmax in float64 on a small random case."""
+    import torch
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, w, L = 2, 6, 3, 16, 80
+    k = rng.standard_normal((B, L, Hkv, 128)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, 128))
+    tiers = np.array([[0, 2, 2, 1, 0], [2, 0, 1, 2, 0]], np.uint8)
+    c = O.OracleCache(B, Hq, Hkv, 128, w)
+    c.prefill(k, k, tiers=tiers)
+    got = O.future_missed_mass(c, q, k)
+    kt, qt = torch.from_numpy(k.astype(np.float64)), torch.from_numpy(q)
+    for b in range(B):
+        ev = torch.from_numpy(np.repeat(tiers[b] == 2, w))
+        for h in range(Hq):
+            p = torch.softmax(kt[b, :, h // (Hq // Hkv)] @ qt[b, h] / math.sqrt(128), dim=0)
+            assert abs(float(p[ev].sum()) - got[b, h]) < 1e-12
