@@ -241,6 +241,57 @@ def oracle_throughput(n_workers, budget_s, max_steps):
 
 # --------------------------------------------------------------------------- native arm
 
+def measure_diagnostics(cache, wl, NL, pool, nq, nkv, stream, reps, dev):
+    """Routing diagnostics after the timed steps: the last routing event's tier
+    moves on every layer (selection churn, reactivation) and the future missed
+    mass of a fresh query over the full keys, timed over four layers in turn
+    (256 MiB of keys, more than L2 holds)."""
+    import torch
+    from tiered_kv_cache_decode_gb300 import synth
+    B, Hq, Hkv, w, L0, d, seed = wl["B"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"], 128, 0
+    cnt = torch.stack([cache.tier_move_counts(l) for l in range(NL)]).double()   # [NL][B][8]
+    churn = (1 - cnt[..., 4] / cnt[..., 2].clamp(min=1)).mean().item()
+    react = (cnt[..., 5] / cnt[..., 1].clamp(min=1)).mean().item()
+    nd = min(NL, 4)
+    Lc = cache.length(0)
+    n_app = Lc - L0
+    kfull, qd = [], []
+    for l in range(nd):
+        k0, _ = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
+        ka = pool[:n_app, l, nq:nq + nkv].reshape(n_app, B, Hkv, d).permute(1, 0, 2, 3)
+        kfull.append(torch.cat([k0, ka], dim=1).contiguous())
+        qd.append(synth.queries(seed + 1, l, 0, B, Hq, d, device=dev))
+        del k0
+    fmm = torch.empty(nd, B, Hq, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for l in range(nd):   # eager first: the launch shape is set up outside the capture
+            cache.future_missed_mass(l, qd[l], kfull[l], out=fmm[l], stream=stream)
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(nd):
+                cache.future_missed_mass(l, qd[l], kfull[l], out=fmm[l], stream=stream)
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for r in range(reps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert cache.status() == 0, cache.last_error()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * nd)
+    # keys and queries read, one tier byte per window read, one float written per query head
+    nbytes = B * Lc * Hkv * d * 2 + B * Hq * d * 2 + B * (-(-Lc // w)) + B * Hq * 4
+    return {
+        "tier_move": {"layers": NL, "churn": round(churn, 4), "reactivation": round(react, 4),
+                      "counts_layer0_seq0": [int(x) for x in cnt[0, 0].tolist()]},
+        "future_missed_mass": {"mean": round(fmm.mean().item(), 5), "max": round(fmm.max().item(), 5),
+                               "us_per_launch": round(us, 3), "bytes_per_launch": int(nbytes),
+                               "gbs": round(nbytes / (us * 1e-6) / 1e9, 2), "context": Lc},
+    }
+
+
 def run_native(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -399,6 +450,7 @@ def run_native(args, rank, world, local_rank):
     st = cache.status()
     assert st == 0, f"device status {st}: {cache.last_error()}"
     cache.refresh_lengths()
+    diagnostics = None if args.no_diag else measure_diagnostics(cache, wl, NL, pool, nq, nkv, stream, K, dev)
 
     ms, e2e_s, tot_bytes, tot_e2e_bytes = combine_ranks(ms, e2e_s, nbytes, e2e_bytes, world, dev)
 
@@ -434,6 +486,9 @@ def run_native(args, rank, world, local_rank):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if diagnostics is not None:
+        diagnostics["future_missed_mass"]["frac_of_peak"] = round(diagnostics["future_missed_mass"]["gbs"] / peak, 4)
+        line["diagnostics"] = diagnostics
     if pool_async is not None:
         cpu_pool, nw, res, t_start = pool_async
         out = res.get()
@@ -477,6 +532,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="run fewer layers of the same per-layer workload (profiling captures)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
+    ap.add_argument("--no-diag", action="store_true", help="skip the routing diagnostics leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -284,6 +284,36 @@ qevict_status qevict_clear_status(qevict_cache *cache, void *stream);
 /* Synchronise `stream` and copy the transition counters to *stats (host). */
 qevict_status qevict_get_stats(qevict_cache *cache, qevict_stats *stats, void *stream);
 
+/* Diagnostics of a layer's last completed tier move (QEvict "Kernbijdragen":
+ * selection churn and latent importance reactivation, reading the
+ * full-precision tier as the active set). A tier move is a routing event, a
+ * prefill with scores or tiers, qevict_set_tiers, qevict_demote_quantize or
+ * qevict_promote_dequantize; appends and decodes are not. Synchronises
+ * `stream`, then writes int32 [batch][8] to the HOST array `counts`, per
+ * sequence:
+ *   [0] full-precision windows before the move   [1] INT2 windows before
+ *   [2] full-precision windows after             [3] INT2 windows after
+ *   [4] kept: full precision before and after    [5] promoted: INT2 -> FP
+ *   [6] demoted: FP -> INT2                      [7] evicted: FP or INT2 -> E
+ * Selection churn = 1 - [4] / [2]; reactivation rate = [5] / [1]. All zero
+ * before the layer's first move. A move that stops on a device error (BUDGET,
+ * STATE, DEVICE) leaves the previous counts. */
+qevict_status qevict_get_tier_move_counts(qevict_cache *cache, int32_t layer, int32_t *counts, void *stream);
+
+/* Future missed mass (QEvict "Kernbijdragen"): for each sequence and query
+ * head, the share of softmax(q K_full^T / sqrt(d)) over all of the layer's
+ * tokens that falls on tokens whose window is evicted now. A measurement, not
+ * part of decoding: the caller keeps the layer's full keys, as they were
+ * stored before any tier move.
+ *  q       bf16 [batch][Hq][head_dim], device, 16-byte aligned.
+ *  k_full  bf16 [batch][n_tokens][Hkv][head_dim], device, 16-byte aligned;
+ *          n_tokens must equal the layer's length (INVALID_ARG otherwise).
+ *  fmm     fp32 [batch][Hq], device; 0 where nothing is evicted.
+ * Logits and sums are fp32. The call uses the cache's decode scratch, so it
+ * must not overlap a decode of the same cache on another stream. */
+qevict_status qevict_future_missed_mass(qevict_cache *cache, int32_t layer, const void *q, const void *k_full,
+                                        int64_t n_tokens, float *fmm, void *stream);
+
 /* Let a decode launch overlap the end of the kernel before it in the stream
  * (programmatic dependent launch): the decode kernel starts loading this
  * layer's cache while the previous kernel finishes, and waits for that kernel

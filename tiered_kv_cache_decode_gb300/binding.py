@@ -28,7 +28,7 @@ EXPORTS = ["qevict_pool_capacity", "qevict_cache_create", "qevict_cache_destroy"
            "qevict_promote_dequantize", "qevict_set_tiers", "qevict_get_scores", "qevict_get_view",
            "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_set_launch_overlap",
            "qevict_refresh_lengths", "qevict_decode_attention_static_scratch",
-           "qevict_length",
+           "qevict_get_tier_move_counts", "qevict_future_missed_mass", "qevict_length",
            "qevict_last_error"]
 
 
@@ -108,6 +108,8 @@ def load() -> ctypes.CDLL:
         "qevict_set_launch_overlap": [P, I32],
         "qevict_refresh_lengths": [P, P],
         "qevict_decode_attention_static_scratch": [P, I32, P, P, P, I32, P],
+        "qevict_get_tier_move_counts": [P, I32, P, P],
+        "qevict_future_missed_mass": [P, I32, P, P, I64, P, P],
         "qevict_length": [P, I32],
         "qevict_last_error": [],
     }
@@ -270,6 +272,24 @@ class TieredCache:
     def scores(self, layer, stream=None):
         out = torch.empty(self.B, self.num_windows(layer), dtype=torch.float32, device="cuda")
         self._check(self.lib.qevict_get_scores(self.handle, layer, _ptr(out), _stream(stream)))
+        return out
+
+    # ---- diagnostics ----------------------------------------------------------
+    def tier_move_counts(self, layer, stream=None):
+        """int32 [B][8] counts of the layer's last tier move: FP and INT2 windows
+        before, the same after, kept, promoted, demoted, evicted (host tensor)."""
+        out = torch.zeros(self.B, 8, dtype=torch.int32)
+        self._check(self.lib.qevict_get_tier_move_counts(self.handle, layer, ctypes.c_void_p(out.data_ptr()),
+                                                         _stream(stream)))
+        return out
+
+    def future_missed_mass(self, layer, q, k_full, out=None, stream=None):
+        """fp32 [B][Hq]: attention share of the full keys k_full [B][L][Hkv][d]
+        (L = the layer's length) that falls on evicted windows."""
+        if out is None:
+            out = torch.empty(self.B, self.Hq, dtype=torch.float32, device=q.device)
+        self._check(self.lib.qevict_future_missed_mass(self.handle, layer, _ptr(q), _ptr(k_full), k_full.shape[1],
+                                                       _ptr(out), _stream(stream)))
         return out
 
     # ---- inspection ---------------------------------------------------------

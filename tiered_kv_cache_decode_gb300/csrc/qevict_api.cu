@@ -334,6 +334,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         const size_t o_wq = cv.take((size_t)B * Wmax * 16);
         const size_t o_wp = cv.take((size_t)B * Wmax * 16);
         const size_t o_wc = cv.take((size_t)B * Wmax * 16);
+        const size_t o_dg = cv.take((size_t)B * 8 * 4);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
         if (!base) {
             const size_t need = cv.off;
@@ -357,6 +358,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         D.work_q = (int4 *)(base + o_wq);
         D.work_p = (int4 *)(base + o_wp);
         D.work_c = (int4 *)(base + o_wc);
+        D.diag = (int32_t *)(base + o_dg);
     }
     err = prepare_decode();
     EncodeTiledFn enc = encode_tiled();
@@ -378,7 +380,10 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     }
     if (err == cudaSuccess) err = cudaMemsetAsync(c->cbase, 0, 256, c->stream);
     if (err == cudaSuccess) err = cudaMemsetAsync(c->scratch_base, 0, c->scratch_bytes, c->stream);
-    for (int l = 0; l < cfg.num_layers && err == cudaSuccess; ++l) err = launch_init_layer(c->layers[l].dev, c->stream);
+    for (int l = 0; l < cfg.num_layers && err == cudaSuccess; ++l) {
+        err = launch_init_layer(c->layers[l].dev, c->stream);
+        if (err == cudaSuccess) err = cudaMemsetAsync(c->layers[l].dev.diag, 0, (size_t)B * 8 * 4, c->stream);
+    }
     if (err == cudaSuccess) err = cudaStreamSynchronize(c->stream);
     if (err != cudaSuccess) {
         release_all(c);
@@ -611,6 +616,37 @@ qevict_status qevict_get_stats(qevict_cache *c, qevict_stats *out, void *stream)
     out->ledger_writes = s[ST_LWRITE];
     out->ledger_reuses = s[ST_LREUSE];
     out->device_bytes = c->total_bytes;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_get_tier_move_counts(qevict_cache *c, int32_t layer, int32_t *counts, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!counts) return fail(QEVICT_ERR_INVALID_ARG, "counts must not be NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(counts, c->layers[layer].dev.diag, (size_t)c->cfg.batch * 8 * sizeof(int32_t),
+                       cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "tier move counts copy");
+    return QEVICT_OK;
+}
+
+qevict_status qevict_future_missed_mass(qevict_cache *c, int32_t layer, const void *q, const void *k_full,
+                                        int64_t n_tokens, float *fmm, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!q || !k_full || !fmm) return fail(QEVICT_ERR_INVALID_ARG, "q, k_full and fmm must not be NULL");
+    if (((uintptr_t)q | (uintptr_t)k_full) & 15) return fail(QEVICT_ERR_INVALID_ARG, "q and k_full must be 16-byte aligned");
+    LayerHost &lh = c->layers[layer];
+    if (lh.length < 1) return fail(QEVICT_ERR_INVALID_ARG, "layer %d is empty", layer);
+    if (n_tokens != lh.length)
+        return fail(QEVICT_ERR_INVALID_ARG, "n_tokens %lld differs from the layer's length %lld", (long long)n_tokens,
+                    (long long)lh.length);
+    cudaError_t e = launch_future_missed_mass(lh.dev, c->cdev, c->scratch, layer, (const __nv_bfloat16 *)q,
+                                              (const __nv_bfloat16 *)k_full, (int)n_tokens, fmm, c->num_sms,
+                                              (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "future missed mass kernels");
+    note_op(c, layer, stream);
     return QEVICT_OK;
 }
 

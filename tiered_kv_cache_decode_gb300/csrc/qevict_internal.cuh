@@ -77,6 +77,7 @@ struct LayerDev {
     int4 *work_q;         // [B][Wmax] quantise: {window, src fp slot or -1 (external), dst ledger slot, 0}
     int4 *work_p;         // [B][Wmax] promote: {window, src ledger slot, dst fp slot, 0}
     int4 *work_c;         // [B][Wmax] prefill copy: {window, dst fp slot, 0, 0}
+    int32_t *diag;        // [B][8] counts of the last completed tier move (see qevict_get_tier_move_counts)
 };
 
 // Decode scratch, shared by all layers of a cache: a decode launch touches it
@@ -127,6 +128,9 @@ cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScra
                           int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
                           float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s);
 cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s);
+cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, int layer,
+                                      const __nv_bfloat16 *q, const __nv_bfloat16 *k_full, int n_tokens, float *fmm,
+                                      int num_sms, cudaStream_t s);
 int decode_splits(int pairs, int num_sms, int G);
 cudaError_t prepare_decode();
 

@@ -173,7 +173,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     __shared__ unsigned long long s_key[kPlanMaxW];
     __shared__ uint8_t s_cur[kPlanMaxW];
     __shared__ uint8_t s_tgt[kPlanMaxW];
+    __shared__ uint8_t s_old[kPlanMaxW];   // tiers before this plan, for the move's counts
     __shared__ int s_warp[kPlanThreads / 32 + 1];
+    __shared__ int s_cnt[8];
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int64_t wb = (int64_t)b * D.Wmax;
@@ -182,6 +184,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     const int64_t length = prefill ? a.prefill_len : (int64_t)ctr[CTR_LEN];
     const int nw = (int)((length + D.w - 1) / D.w);
     const bool partial_last = (length % D.w) != 0;
+    if (tid < 8) s_cnt[tid] = 0;
     if (tid == 0) {   // nothing queued unless this plan queues it
         ctr[CTR_WQ] = 0;
         ctr[CTR_WP] = 0;
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         return;
     }
 
-    for (int i = tid; i < nw; i += kPlanThreads) s_cur[i] = prefill ? QEVICT_TIER_FP : D.tier[wb + i];
+    for (int i = tid; i < nw; i += kPlanThreads) s_old[i] = s_cur[i] = prefill ? QEVICT_TIER_FP : D.tier[wb + i];
     __syncthreads();
 
     if (a.mode == PLAN_DEMOTE || a.mode == PLAN_PROMOTE) {
@@ -495,6 +498,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     for (int i = w0; i < w1; ++i) {
         if (s_tgt[i] == QEVICT_TIER_FP) D.fp_list[b * D.CF + of++] = make_int2(i, D.fp_slot[wb + i]);
         if (s_tgt[i] == QEVICT_TIER_Q) D.q_list[b * D.CQ + oq++] = make_int2(i, D.lg_slot[wb + i]);
+    }
+    // ---- the move's counts (the full-precision tier read as the active set):
+    // tier sizes before and after, kept, promoted, demoted, evicted
+    {
+        int cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int i = w0; i < w1; ++i) {
+            const uint8_t o = s_old[i], n = s_tgt[i];
+            cnt[0] += o == QEVICT_TIER_FP;
+            cnt[1] += o == QEVICT_TIER_Q;
+            cnt[2] += n == QEVICT_TIER_FP;
+            cnt[3] += n == QEVICT_TIER_Q;
+            cnt[4] += o == QEVICT_TIER_FP && n == QEVICT_TIER_FP;
+            cnt[5] += o == QEVICT_TIER_Q && n == QEVICT_TIER_FP;
+            cnt[6] += o == QEVICT_TIER_FP && n == QEVICT_TIER_Q;
+            cnt[7] += o != QEVICT_TIER_E && n == QEVICT_TIER_E;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (cnt[j]) atomicAdd(&s_cnt[j], cnt[j]);
+        __syncthreads();
+        if (tid < 8) D.diag[b * 8 + tid] = s_cnt[tid];
     }
     if (tid == 0) {
         ctr[CTR_NFP] = tf;
