@@ -11,7 +11,7 @@ import torch
 
 import oracle as O
 from tiered_kv_cache_decode_gb300 import binding, synth
-from parity_util import close, make_pair
+from parity_util import check_decode, close, make_pair
 
 pytestmark = pytest.mark.gpu
 
@@ -117,6 +117,8 @@ def fmm_case(B, Hq, Hkv, w, L, beta, seed, appended=0):
     assert cache.status() == 0, cache.last_error()
     want = O.future_missed_mass(ref, q.float().numpy(), k_full.float().numpy())
     close(got.cpu().numpy(), want, "future missed mass")
+    # the measurement shares the decode scratch: decoding after it is unaffected
+    check_decode(cache, 0, ref, synth.queries(seed, 0, 1, B, Hq, 128))
     return got.cpu().numpy(), want
 
 
@@ -145,3 +147,17 @@ def test_future_missed_mass_rejects_a_wrong_length():
     with pytest.raises(binding.QevictError) as e:
         cache.future_missed_mass(0, q, k)
     assert e.value.name == "INVALID_ARG"
+
+
+def test_future_missed_mass_single_window_cache():
+    """max_context below one window: one window per sequence, nothing evicted."""
+    B, Hq, Hkv, w, L = 8, 8, 2, 32, 20
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, tiers=[torch.zeros(B, 1, dtype=torch.uint8)], seed=28)
+    k, _ = synth.kv_tokens(28, 0, B, 0, L, Hkv, 128, "heavy")
+    q = synth.queries(28, 0, 0, B, Hq, 128)
+    got = cache.future_missed_mass(0, q.cuda(), k.cuda())
+    torch.cuda.synchronize()
+    assert cache.status() == 0, cache.last_error()
+    want = O.future_missed_mass(ref, q.float().numpy(), k.float().numpy())
+    assert not want.any() and not got.cpu().numpy().any()
+    check_decode(cache, 0, ref, q)

@@ -282,7 +282,8 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         Carver cv;
         const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * kHeadDim * 8);
         const size_t o_rec = cv.take((size_t)B * Hkv * kMaxSplits * kMaxG * 16);
-        const size_t o_ws = cv.take((size_t)B * Hq * Wmax * 8);
+        // window statistics; also the future-missed-mass partials (12 B per split and query head)
+        const size_t o_ws = cv.take((size_t)B * Hq * (Wmax * 8 > 12 ? Wmax * 8 : 12));
         const size_t o_bar = cv.take((size_t)B * Hkv * 8);
         const size_t o_ab = cv.take((size_t)B * 4);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
@@ -642,9 +643,23 @@ qevict_status qevict_future_missed_mass(qevict_cache *c, int32_t layer, const vo
     if (n_tokens != lh.length)
         return fail(QEVICT_ERR_INVALID_ARG, "n_tokens %lld differs from the layer's length %lld", (long long)n_tokens,
                     (long long)lh.length);
-    cudaError_t e = launch_future_missed_mass(lh.dev, c->cdev, c->scratch, layer, (const __nv_bfloat16 *)q,
-                                              (const __nv_bfloat16 *)k_full, (int)n_tokens, fmm, c->num_sms,
-                                              (cudaStream_t)stream);
+    if ((int64_t)c->cfg.batch * n_tokens > INT32_MAX)
+        return fail(QEVICT_ERR_INVALID_ARG, "batch x n_tokens passes 2^31 - 1");
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return fail(QEVICT_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    // k_full as [B * n_tokens][Hkv][128]: boxes of 64 channels x 1 KV head x 16 tokens
+    CUtensorMap kmap{};
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)c->cfg.num_kv_heads,
+                                (cuuint64_t)c->cfg.batch * (cuuint64_t)n_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)c->cfg.num_kv_heads * kHeadDim * 2};
+    const cuuint32_t box[3] = {64, 1, 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k_full), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return fail(QEVICT_ERR_INVALID_ARG, "k_full cannot be described as a tensor map");
+    cudaError_t e = launch_future_missed_mass(lh.dev, c->cdev, c->scratch, layer, kmap, (const __nv_bfloat16 *)q,
+                                              (int)n_tokens, fmm, c->num_sms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "future missed mass kernels");
     note_op(c, layer, stream);
     return QEVICT_OK;

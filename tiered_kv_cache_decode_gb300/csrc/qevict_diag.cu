@@ -37,106 +37,179 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint4 &a, uint32_t
         : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void fmm_add(FmmStat &st, float x, bool evicted) {
-    if (x > st.m) {
-        const float f = exp2f(st.m - x);
-        st.la *= f;
-        st.le *= f;
-        st.m = x;
-    }
-    const float e = exp2f(x - st.m);
-    st.la += e;
-    if (evicted) st.le += e;
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-// One CTA per (split of the token range, sequence and KV head). A warp takes
-// chunks of 16 tokens and computes their logits on the tensor cores
-// (mma.sync m16n8k16, bf16 operands, fp32 sums): tokens are the M rows, the
-// query heads of the group the N columns (padded to 8), channels the K
-// dimension in 8 steps of 16. Lane (g, c) = (lane / 4, lane % 4) loads, for
-// tokens g and g + 8, the 16-byte pieces at bytes 16 c + 64 i (i = 0..3) of
-// the token's 256-byte key row, so the 32 lanes of one load read 8 whole
-// 64-byte runs. Inside a 16-channel step the channel order is permuted the
-// same way for K and q (lane c's k indices 2c, 2c+1, 2c+8, 2c+9 are its 4
-// consecutive channels), which leaves every dot product unchanged and lets
-// the loaded words serve as the A fragment as they are. The next chunk's
-// keys and tiers are loaded before the current chunk's arithmetic. Each lane
-// keeps a running (max, sums) for heads 2c and 2c + 1.
+constexpr long long kFmmWaitCycles = 4000000000ll;   // about two seconds at GB300 clocks
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// suspends the thread until the phase completes or about 20 us pass
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+// bounded wait: false after about two seconds
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kFmmWaitCycles) return false;
+    return true;
+}
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar,
+                                       uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint4 &r) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+}
+
+// Running (max, sums) of one head over two more logits (log2 domain).
+__device__ __forceinline__ void fmm_add2(FmmStat &st, float x0, float x1, bool ok0, bool ok1, bool evicted) {
+    x0 = ok0 ? x0 : -INFINITY;
+    x1 = ok1 ? x1 : -INFINITY;
+    const float m = fmaxf(st.m, fmaxf(x0, x1));
+    if (m == -INFINITY) return;
+    const float f = ex2(st.m - m), e = ex2(x0 - m) + ex2(x1 - m);
+    st.la = fmaf(st.la, f, e);
+    st.le = st.le * f + (evicted ? e : 0.f);
+    st.m = m;
+}
+
+// Each warp streams chunks of 16 tokens through its own ring of kFmmStages
+// stages in shared memory. A stage holds the chunk's keys as two TMA boxes of
+// 16 tokens x 64 channels (channels 0-63, then 64-127), 128-byte rows with
+// the 128-byte swizzle, so that ldmatrix reads them without bank conflicts.
+constexpr int kFmmStages = 6;
+constexpr int kFmmThreads = kFmmWarps * 32;
+constexpr int kFmmStage = 4096;
+constexpr int kFmmRing = kFmmWarps * kFmmStages * kFmmStage;
+constexpr int kFmmSmem = kFmmRing + kFmmWarps * kFmmStages * 8 + 1024;   // + barriers, + alignment
+
+// One CTA per (split of the token range, sequence and KV head), one CTA per
+// SM; splits start on 16-token boundaries, so a chunk of 16 tokens lies
+// inside one window (a window is a multiple of 16 tokens) and takes one tier
+// byte. A warp takes every 8th chunk: lane 0 issues the chunk's two TMA
+// copies kFmmStages - 1 chunks ahead, and the warp computes the logits on the
+// tensor cores (mma.sync m16n8k16, bf16 operands, fp32 sums) with the tokens
+// as the M rows (A from ldmatrix), the query heads of the group as the N
+// columns (padded to 8) and the channels as K in 8 steps of 16. Lane
+// (g, c) = (lane / 4, lane % 4) keeps a running (max, sums) for heads 2c and
+// 2c + 1.
+//
+// The CTA's statistics per head go to `part`; the last CTA of each (sequence,
+// KV head) to arrive on `cnt` (zero between launches, reset by that CTA)
+// merges all splits and writes the missed mass of the group's heads.
 template <int G>
-__global__ void __launch_bounds__(kFmmWarps * 32) fmm_partial_kernel(const LayerDev D, const __nv_bfloat16 *q,
-                                                                     const __nv_bfloat16 *k_full, int L,
-                                                                     float *part, int splits) {
+__global__ void __launch_bounds__(kFmmThreads, 1) fmm_kernel(const LayerDev D, const CacheDev C,
+                                                             const __grid_constant__ CUtensorMap kmap, int layer,
+                                                             const __nv_bfloat16 *q, int L, float *part,
+                                                             int splits, uint32_t *cnt, float *fmm) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
     const int split = blockIdx.x, bk = blockIdx.y;
     const int b = bk / D.Hkv, kvh = bk % D.Hkv;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, c = lane & 3;
     const float scale = kLog2eF * rsqrtf((float)kHeadDim);
+    const uint32_t sraw = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    const uint32_t ring = (sraw + 1023u) & ~1023u;   // swizzled TMA boxes want 1024-byte alignment
+    const uint32_t wring = ring + warp * kFmmStages * kFmmStage;
+    const uint32_t bars = ring + kFmmRing + warp * kFmmStages * 8;
 
-    // B fragments (q^T): step kk uses channels 8c + 32 (kk / 2) + 4 (kk % 2) + 0..3 of head g
+    const int nch = (L + 15) / 16;
+    const int t0 = 16 * (int)((int64_t)nch * split / splits);
+    const int t1 = min(L, 16 * (int)((int64_t)nch * (split + 1) / splits));
+    const uint8_t *tier = D.tier + (int64_t)b * D.Wmax;
+    auto chunk0 = [&](int k) { return t0 + (warp + k * kFmmWarps) * 16; };
+
+    if (lane == 0)
+        for (int i = 0; i < kFmmStages; ++i) mbar_init(bars + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+    const uint64_t pol = evict_first_policy();
+    auto issue = [&](int k) {   // lane 0
+        const int st = k % kFmmStages, c0 = chunk0(k);
+        const uint32_t bar = bars + 8 * st, dst = wring + st * kFmmStage;
+        mbar_expect_tx(bar, (uint32_t)kFmmStage);
+        tma_3d(dst, &kmap, 0, kvh, b * L + c0, bar, pol);
+        tma_3d(dst + 2048, &kmap, 64, kvh, b * L + c0, bar, pol);
+    };
+    int issued = 0;
+    if (lane == 0)
+        for (; issued < kFmmStages - 1 && chunk0(issued) < t1; ++issued) issue(issued);
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+
+    // B fragments (q^T): step ks, (k = 2c, 2c+1) and (k = 2c+8, 2c+9) of head g
     uint32_t qb[8][2];
     {
-        uint4 r[4] = {};
-        if (g < G) {
-            const uint4 *qp = reinterpret_cast<const uint4 *>(q + ((int64_t)b * D.Hq + kvh * G + g) * kHeadDim);
+        const uint32_t *qp = reinterpret_cast<const uint32_t *>(q + ((int64_t)b * D.Hq + kvh * G + g) * kHeadDim);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) r[i] = qp[c + 4 * i];
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            qb[2 * i][0] = r[i].x;
-            qb[2 * i][1] = r[i].y;
-            qb[2 * i + 1][0] = r[i].z;
-            qb[2 * i + 1][1] = r[i].w;
+        for (int ks = 0; ks < 8; ++ks) {
+            qb[ks][0] = g < G ? qp[8 * ks + c] : 0u;
+            qb[ks][1] = g < G ? qp[8 * ks + 4 + c] : 0u;
         }
     }
     FmmStat st[2] = {{-INFINITY, 0.f, 0.f}, {-INFINITY, 0.f, 0.f}};
+    // ldmatrix row of this lane: matrix m = lane / 8 gives tokens 0-7 or 8-15 and k 0-7 or 8-15
+    const int lm_tok = (lane & 7) + 8 * ((lane >> 3) & 1), lm_hi = lane >> 4;
 
-    const int t0 = (int)((int64_t)L * split / splits), t1 = (int)((int64_t)L * (split + 1) / splits);
-    const int64_t row = (int64_t)D.Hkv * kHeadDim;   // elements between consecutive tokens
-    const uint4 *kb = reinterpret_cast<const uint4 *>(k_full + ((int64_t)b * L * D.Hkv + kvh) * kHeadDim) + c;
-    const uint8_t *tier = D.tier + (int64_t)b * D.Wmax;
-    // r[h][i]: token g + 8 h, piece i; ev[h]: that token is evicted
-    auto load_chunk = [&](int c0, uint4 (&r)[2][4], bool (&ev)[2]) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int t = c0 + g + 8 * h;
-            const bool in = t < t1;
-            const uint4 *p = kb + (int64_t)t * (row / 8);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) r[h][i] = in ? __ldg(p + 4 * i) : make_uint4(0, 0, 0, 0);
-            ev[h] = in && __ldg(tier + t / D.w) == QEVICT_TIER_E;
+    for (int k = 0; k < issued; ++k) {
+        const int sidx = k % kFmmStages, c0 = chunk0(k);
+        const bool ev = tier[c0 / D.w] == QEVICT_TIER_E;
+        const bool ok = mbar_wait(bars + 8 * sidx, (uint32_t)((k / kFmmStages) & 1));
+        if (__any_sync(0xffffffffu, !ok)) {
+            if (lane == 0) {
+                set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -5);
+                // the copies still in flight land before the CTA leaves
+                for (int r = k; r < issued; ++r)
+                    (void)mbar_wait(bars + 8 * (r % kFmmStages), (uint32_t)((r / kFmmStages) & 1));
+            }
+            break;
         }
-    };
-    uint4 cur[2][4], nxt[2][4];
-    bool ecur[2], enxt[2];
-    int c0 = t0 + warp * 16;
-    constexpr int stride = kFmmWarps * 16;
-    if (c0 < t1) load_chunk(c0, cur, ecur);
-    for (; c0 < t1; c0 += stride) {
-        if (c0 + stride < t1) load_chunk(c0 + stride, nxt, enxt);
+        const uint32_t base = wring + sidx * kFmmStage;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            // A fragment: (token g, k 2c..2c+1), (token g+8, same), (token g, k 2c+8..9), (token g+8, same)
-            mma_bf16(acc, make_uint4(cur[0][i].x, cur[1][i].x, cur[0][i].y, cur[1][i].y), qb[2 * i][0],
-                     qb[2 * i][1]);
-            mma_bf16(acc, make_uint4(cur[0][i].z, cur[1][i].z, cur[0][i].w, cur[1][i].w), qb[2 * i + 1][0],
-                     qb[2 * i + 1][1]);
+        for (int ks = 0; ks < 8; ++ks) {
+            const int chunk = 2 * (ks & 3) + lm_hi;
+            uint4 a;
+            ldsm_x4(base + (ks >> 2) * 2048 + lm_tok * 128 + ((chunk ^ (lm_tok & 7)) << 4), a);
+            mma_bf16(acc, a, qb[ks][0], qb[ks][1]);
         }
+        __syncwarp();   // every lane has read the stage before it is refilled
+        if (lane == 0 && chunk0(issued) < t1) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(issued);
+        }
+        issued = (chunk0(issued) < t1) ? issued + 1 : issued;
         // acc: (token g, head 2c), (token g, head 2c+1), (token g+8, head 2c), (token g+8, head 2c+1)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (c0 + g + 8 * h < t1) {
-                if (2 * c < G) fmm_add(st[0], acc[2 * h] * scale, ecur[h]);
-                if (2 * c + 1 < G) fmm_add(st[1], acc[2 * h + 1] * scale, ecur[h]);
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            ecur[h] = enxt[h];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) cur[h][i] = nxt[h][i];
-        }
+        const bool ok0 = c0 + g < t1, ok1 = c0 + g + 8 < t1;
+        if (2 * c < G) fmm_add2(st[0], acc[0] * scale, acc[2] * scale, ok0, ok1, ev);
+        if (2 * c + 1 < G) fmm_add2(st[1], acc[1] * scale, acc[3] * scale, ok0, ok1, ev);
     }
 
     // per head: merge the 8 lanes that share c, then the warps
@@ -160,60 +233,66 @@ __global__ void __launch_bounds__(kFmmWarps * 32) fmm_partial_kernel(const Layer
         o[0] = acc.m;
         o[1] = acc.la;
         o[2] = acc.le;
+        __threadfence();
     }
-}
-
-// One warp per (sequence, query head): lanes take the splits in turn, then
-// the lanes' statistics are merged across the warp.
-__global__ void fmm_merge_kernel(const LayerDev D, const float *part, int splits, float *fmm) {
-    const int i = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (i >= D.B * D.Hq) return;
-    const int b = i / D.Hq, h = i % D.Hq, kvh = h / D.G, hh = h % D.G;
-    const int bk = b * D.Hkv + kvh;
-    FmmStat acc{-INFINITY, 0.f, 0.f};
-    for (int s = lane; s < splits; s += 32) {
-        const float *o = part + (((int64_t)bk * splits + s) * D.G + hh) * 3;
-        acc = fmm_merge(acc, FmmStat{o[0], o[1], o[2]});
-    }
+    __shared__ bool s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&cnt[2 * bk], 1u) == (unsigned)splits - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    // warp hh merges head hh over the splits, lanes taking splits in turn
+    if (warp < G) {
+        FmmStat a{-INFINITY, 0.f, 0.f};
+        for (int sp = lane; sp < splits; sp += 32) {
+            const float *o = part + (((int64_t)bk * splits + sp) * G + warp) * 3;
+            a = fmm_merge(a, FmmStat{__ldcg(o), __ldcg(o + 1), __ldcg(o + 2)});
+        }
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const FmmStat p{__shfl_xor_sync(0xffffffffu, acc.m, o), __shfl_xor_sync(0xffffffffu, acc.la, o),
-                        __shfl_xor_sync(0xffffffffu, acc.le, o)};
-        acc = fmm_merge(acc, p);
+        for (int o = 16; o >= 1; o >>= 1) {
+            const FmmStat p{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.la, o),
+                            __shfl_xor_sync(0xffffffffu, a.le, o)};
+            a = fmm_merge(a, p);
+        }
+        if (lane == 0) fmm[(int64_t)b * D.Hq + kvh * G + warp] = a.la > 0.f ? a.le / a.la : 0.f;
     }
-    if (lane == 0) fmm[i] = acc.la > 0.f ? acc.le / acc.la : 0.f;
+    if (threadIdx.x == 0) cnt[2 * bk] = 0;
 }
 
 }  // namespace
 
 cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, int layer,
-                                      const __nv_bfloat16 *q, const __nv_bfloat16 *k_full, int n_tokens, float *fmm,
+                                      const CUtensorMap &kmap, const __nv_bfloat16 *q, int n_tokens, float *fmm,
                                       int num_sms, cudaStream_t s) {
-    (void)C;
-    (void)layer;
     const int pairs = L.B * L.Hkv;
     // Partials (3 floats per split and query head) go to the window-statistics
-    // area of the decode scratch, which holds 2 * Wmax floats per query head
-    // and carries nothing from one decode launch to the next. (The partial
-    // output area is not used: its words carry arrival tags.)
+    // area of the decode scratch, which holds 8 Wmax bytes (at least 12) per
+    // query head and carries nothing from one decode launch to the next. (The
+    // partial output area is not used: its words carry arrival tags.)
     float *part = reinterpret_cast<float *>(S.wstat);
-    // as many CTAs as fit the GPU at once, spread over the (sequence, KV head) pairs
+    // The split arrival counters of the decode scratch (zero between launches)
+    // count this launch's arrivals too; every launch leaves them at zero.
+    uint32_t *cnt = S.bar;   // [B*Hkv][2]; the kernel counts on entry 2 * bk
+    // one CTA per SM, spread over the (sequence, KV head) pairs
     auto grid_for = [&](const void *fn) {
-        static int per_sm[kMaxG + 1] = {};
-        if (!per_sm[L.G] && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[L.G], fn, kFmmWarps * 32, 0) !=
-                                cudaSuccess)
-            per_sm[L.G] = 1;
-        int splits = (max(1, per_sm[L.G]) * num_sms + pairs - 1) / pairs;
+        static bool attr[kMaxG + 1] = {};
+        if (!attr[L.G]) {
+            const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFmmSmem);
+            if (e != cudaSuccess) return -1;
+            attr[L.G] = true;
+        }
+        const int splits = (num_sms + pairs - 1) / pairs;
         return max(1, min(splits, min(256, 2 * L.Wmax / 3)));
     };
-    int splits = 1;
     switch (L.G) {
 #define QV_CASE(GG)                                                                                          \
-    case GG:                                                                                                 \
-        splits = grid_for((const void *)fmm_partial_kernel<GG>);                                             \
-        fmm_partial_kernel<GG><<<dim3(splits, pairs), kFmmWarps * 32, 0, s>>>(L, q, k_full, n_tokens, part,  \
-                                                                              splits);                       \
-        break;
+    case GG: {                                                                                               \
+        const int splits = grid_for((const void *)fmm_kernel<GG>);                                           \
+        if (splits < 0) return cudaGetLastError();                                                           \
+        fmm_kernel<GG><<<dim3(splits, pairs), kFmmThreads, kFmmSmem, s>>>(L, C, kmap, layer, q, n_tokens,    \
+                                                                           part, splits, cnt, fmm);          \
+        break;                                                                                               \
+    }
         QV_CASE(1)
         QV_CASE(2)
         QV_CASE(3)
@@ -226,10 +305,6 @@ cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, cons
         default:
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int n = L.B * L.Hq;
-    fmm_merge_kernel<<<(n + 3) / 4, 128, 0, s>>>(L, part, splits, fmm);
     return cudaGetLastError();
 }
 

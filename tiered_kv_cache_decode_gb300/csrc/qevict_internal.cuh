@@ -128,8 +128,10 @@ cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScra
                           int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
                           float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s);
 cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s);
+// kmap: k_full [B * n_tokens][Hkv][128] bf16 as a 3-D tiled map, boxes of
+// 64 channels x 1 KV head x 16 tokens, 128-byte swizzle
 cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, int layer,
-                                      const __nv_bfloat16 *q, const __nv_bfloat16 *k_full, int n_tokens, float *fmm,
+                                      const CUtensorMap &kmap, const __nv_bfloat16 *q, int n_tokens, float *fmm,
                                       int num_sms, cudaStream_t s);
 int decode_splits(int pairs, int num_sms, int G);
 cudaError_t prepare_decode();
