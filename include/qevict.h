@@ -85,6 +85,21 @@ typedef struct qevict_allocator {
  *                layer); 0 derives them from the budget at max_context
  *                (plus fp_slack full-precision slots for windows that open
  *                between routing events; fp_slack 0 means 4).
+ *  tier_per_kv_head
+ *                0: one tier per (sequence, layer, window), shared by the KV
+ *                heads. Nonzero: one tier per (sequence, KV head, layer,
+ *                window) (the head-specific cache sizes of "Technische
+ *                Samenvatting: DBTrimKV", Implementatie). Each (sequence, KV
+ *                head) pair is then a unit with its own windows, cumulative
+ *                scores (the mean mass of the head's G query heads), slot
+ *                pools and budget floor(beta * L * d * 4), and its own
+ *                routing. Token inputs keep their [batch][n][Hkv][head_dim]
+ *                layout and q, out and mass theirs; what is per sequence in
+ *                the shared mode is per unit here, unit u = b * Hkv + kvh:
+ *                scores and tiers are [batch * Hkv][windows], (sequence,
+ *                window) pairs name (unit, window), tier-move counts are
+ *                [batch * Hkv][8], and qevict_get_view shows batch * Hkv
+ *                units of 1 KV head and G query heads.
  */
 typedef struct qevict_config {
     int32_t batch;
@@ -99,6 +114,7 @@ typedef struct qevict_config {
     int32_t fp_slack;
     double budget_frac;
     double fp_share;
+    int32_t tier_per_kv_head;
 } qevict_config;
 
 typedef struct qevict_cache qevict_cache;

@@ -511,6 +511,38 @@ def future_missed_mass(cache, q, k_full):
     return out
 
 
+# ---- per-KV-head tiers (an option) -------------------------------------------
+#
+# The default reading shares one tier per window between the KV heads. As an
+# option each KV head keeps a cache of its own size ("Technische Samenvatting:
+# DBTrimKV", Implementatie: head-specific cache sizes). Every (sequence, KV
+# head) pair is then a unit routed on its own: its own windows and tiers, its
+# own cumulative score (the mean mass of the G query heads that read it), and
+# its own budget floor(beta * L * d * 4), the pair's share of the sequence's
+# bytes. A query head attends only to its own KV head, so a unit is exactly a
+# one-KV-head cache with G query heads, and that is how it is built here.
+
+def per_head_cache(B, Hq, Hkv, d, w, beta=1.0, rho=0.5):
+    """The per-head form of a cache of B sequences: B * Hkv units, unit
+    u = b * Hkv + kvh, each with 1 KV head and Hq / Hkv query heads."""
+    assert Hq % Hkv == 0
+    return OracleCache(B * Hkv, Hq // Hkv, 1, d, w, beta, rho)
+
+
+def to_units(x):
+    """Token rows [B][n][Hkv][d] as unit rows [B * Hkv][n][1][d]."""
+    x = np.asarray(x)
+    B, n, H, d = x.shape
+    return x.transpose(0, 2, 1, 3).reshape(B * H, n, 1, d)
+
+
+def queries_to_units(q, Hkv):
+    """Queries [B][Hq][d] as [B * Hkv][Hq / Hkv][d] (query head h reads KV head h // G)."""
+    q = np.asarray(q)
+    B, Hq, d = q.shape
+    return q.reshape(B * Hkv, Hq // Hkv, d)
+
+
 def tiered_bytes(cache: OracleCache) -> int:
     """Attention-visible bytes resident for all sequences (FP c_fp, INT2 c_q, E 0)."""
     c_fp, c_q = window_costs(cache.w, cache.Hkv, cache.d)

@@ -35,8 +35,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match_header_sizes():
-    # int32 x 10 + double x 2 = 56 bytes
-    assert ctypes.sizeof(binding.Config) == 56
+    # int32 x 10 + double x 2 + int32 + 4 bytes of tail padding = 64 bytes
+    assert ctypes.sizeof(binding.Config) == 64
+    assert binding.Config.tier_per_kv_head.offset == 56
     assert ctypes.sizeof(binding.Stats) == 48
     assert ctypes.sizeof(binding.View) == 9 * 4 + 4 + 3 * 8 + 6 * 8
 
@@ -116,3 +117,24 @@ def test_pool_capacity_covers_every_routing_event(lib, Hkv, w, maxc, beta, rho):
     assert worst_fp + 1 <= cf          # one more for the slot kept for the next window
     assert worst_led <= cq
     assert nbytes == cf * c_fp + cq * c_q
+
+
+def test_per_head_pools_match_the_shared_pools(lib):
+    """With per-head tiers a unit is one (sequence, KV head): its budget and
+    window costs are the sequence's divided by Hkv, so it gets the shared
+    mode's slot counts and the layer's pool bytes do not change."""
+    out = []
+    for per_head in (0, 1):
+        cf, cq, nb = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+        cfg = _cfg(batch=3, num_q_heads=32, num_kv_heads=8, window=64, max_context=32768, budget_frac=0.25,
+                   tier_per_kv_head=per_head)
+        assert lib.qevict_pool_capacity(ctypes.byref(cfg), ctypes.byref(cf), ctypes.byref(cq), ctypes.byref(nb)) == 0
+        out.append((cf.value, cq.value, nb.value))
+    assert out[0] == out[1]
+
+
+def test_per_head_rejects_too_many_units(lib):
+    h = ctypes.c_void_p()
+    cfg = _cfg(batch=16384, num_q_heads=8, num_kv_heads=8, max_context=64, tier_per_kv_head=1)
+    assert lib.qevict_cache_create(ctypes.byref(cfg), None, None, ctypes.byref(h)) == 1
+    assert b"65535" in lib.qevict_last_error()

@@ -504,3 +504,60 @@ def test_future_missed_mass_matches_library_softmax():
         for h in range(Hq):
             p = torch.softmax(kt[b, :, h // (Hq // Hkv)] @ qt[b, h] / math.sqrt(128), dim=0)
             assert abs(float(p[ev].sum()) - got[b, h]) < 1e-12
+
+
+# ---------------------------------------------------------------- per-KV-head tiers
+
+def test_per_head_with_equal_scores_is_the_shared_cache():
+    """Heads of a sequence ranked on the same scores keep the same windows as
+    the shared-tier cache: a unit's budget and its window costs are both the
+    sequence's divided by Hkv (exactly, with beta * L * d * 4 an integer), so
+    the counts agree. The attention outputs and masses are then the same."""
+    rng = np.random.default_rng(6)
+    B, Hq, Hkv, w, L, beta = 2, 8, 2, 16, 200, 0.25
+    k = O.bf16_round(rng.standard_normal((B, L, Hkv, 128)))
+    v = O.bf16_round(rng.standard_normal((B, L, Hkv, 128)))
+    W = -(-L // w)
+    S = rng.random((B, W))
+    shared = O.OracleCache(B, Hq, Hkv, 128, w, beta=beta)
+    shared.prefill(k, v, scores=S)
+    ph = O.per_head_cache(B, Hq, Hkv, 128, w, beta=beta)
+    ph.prefill(O.to_units(k), O.to_units(v), scores=np.repeat(S, Hkv, axis=0))
+    t = shared.tiers()
+    assert (t == O.TIER_Q).any() and (t == O.TIER_E).any()
+    assert np.array_equal(ph.tiers(), np.repeat(t, Hkv, axis=0))
+    q = O.bf16_round(rng.standard_normal((B, Hq, 128)))
+    o1, m1 = shared.decode(q, accumulate=False)
+    o2, m2 = ph.decode(O.queries_to_units(q, Hkv), accumulate=False)
+    assert np.allclose(o2.reshape(B, Hq, 128), o1, rtol=0, atol=1e-12)
+    assert np.allclose(m2.reshape(B, Hq, W), m1, rtol=0, atol=1e-12)
+
+
+def test_per_head_attention_reads_only_its_own_windows():
+    """Each KV head keeps its own full-precision windows: a query head's output
+    is dense softmax attention over exactly the tokens of its KV head's kept
+    windows, written out here from the raw K, V."""
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, w, L = 2, 6, 3, 16, 96
+    G, W = Hq // Hkv, L // w
+    k = O.bf16_round(rng.standard_normal((B, L, Hkv, 128)))
+    v = O.bf16_round(rng.standard_normal((B, L, Hkv, 128)))
+    tiers = np.full((B * Hkv, W), O.TIER_E, np.uint8)
+    for u in range(B * Hkv):
+        keep = rng.choice(W - 1, size=2, replace=False)
+        tiers[u, keep] = O.TIER_FP
+        tiers[u, W - 1] = O.TIER_FP
+    ph = O.per_head_cache(B, Hq, Hkv, 128, w)
+    ph.prefill(O.to_units(k), O.to_units(v), tiers=tiers)
+    q = O.bf16_round(rng.standard_normal((B, Hq, 128)))
+    out, _ = ph.decode(O.queries_to_units(q, Hkv), accumulate=False)
+    out = out.reshape(B, Hq, 128)
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // G
+            toks = np.concatenate([np.arange(wi * w, (wi + 1) * w) for wi in range(W)
+                                   if tiers[b * Hkv + kvh, wi] == O.TIER_FP])
+            s = k[b, toks, kvh].astype(np.float64) @ q[b, h].astype(np.float64) / np.sqrt(128)
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            assert np.allclose(out[b, h], p @ v[b, toks, kvh].astype(np.float64), rtol=0, atol=1e-12)

@@ -45,7 +45,8 @@ class Config(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("window", ctypes.c_int32),
                 ("max_context", ctypes.c_int32), ("fp_capacity", ctypes.c_int32),
                 ("ledger_capacity", ctypes.c_int32), ("fp_slack", ctypes.c_int32),
-                ("budget_frac", ctypes.c_double), ("fp_share", ctypes.c_double)]
+                ("budget_frac", ctypes.c_double), ("fp_share", ctypes.c_double),
+                ("tier_per_kv_head", ctypes.c_int32)]
 
 
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
@@ -159,11 +160,16 @@ class TieredCache:
 
     def __init__(self, batch, num_layers, num_q_heads, num_kv_heads, window, max_context,
                  budget_frac=1.0, fp_share=0.5, fp_capacity=0, ledger_capacity=0, fp_slack=0,
-                 head_dim=HEAD_DIM, torch_allocator=True):
+                 head_dim=HEAD_DIM, torch_allocator=True, per_head=False):
+        """per_head: one tier per (sequence, KV head, window); scores, tiers and
+        tier-move counts then have one row per unit b * num_kv_heads + kvh."""
         self.lib = load()
         self.cfg = Config(batch, num_layers, num_q_heads, num_kv_heads, head_dim, window, max_context,
-                          fp_capacity, ledger_capacity, fp_slack, float(budget_frac), float(fp_share))
+                          fp_capacity, ledger_capacity, fp_slack, float(budget_frac), float(fp_share),
+                          1 if per_head else 0)
         self.B, self.Hq, self.Hkv, self.w = batch, num_q_heads, num_kv_heads, window
+        self.per_head = bool(per_head)
+        self.units = batch * num_kv_heads if per_head else batch
         self.layers = num_layers
         self.device = torch.cuda.current_device()
         self._alloc = None
@@ -270,7 +276,7 @@ class TieredCache:
         self._check(self.lib.qevict_set_tiers(self.handle, layer, _ptr(tiers), _stream(stream)))
 
     def scores(self, layer, stream=None):
-        out = torch.empty(self.B, self.num_windows(layer), dtype=torch.float32, device="cuda")
+        out = torch.empty(self.units, self.num_windows(layer), dtype=torch.float32, device="cuda")
         self._check(self.lib.qevict_get_scores(self.handle, layer, _ptr(out), _stream(stream)))
         return out
 
@@ -278,7 +284,7 @@ class TieredCache:
     def tier_move_counts(self, layer, stream=None):
         """int32 [B][8] counts of the layer's last tier move: FP and INT2 windows
         before, the same after, kept, promoted, demoted, evicted (host tensor)."""
-        out = torch.zeros(self.B, 8, dtype=torch.int32)
+        out = torch.zeros(self.units, 8, dtype=torch.int32)
         self._check(self.lib.qevict_get_tier_move_counts(self.handle, layer, ctypes.c_void_p(out.data_ptr()),
                                                          _stream(stream)))
         return out
@@ -324,14 +330,15 @@ class TieredCache:
         """bf16 [Hkv][2 (K, V)][w][d] content of a full-precision slot (host copy)."""
         v = self.view(layer)
         raw = device_tensor(v.fp_pool + slot * v.fp_slot_bytes, (v.fp_slot_bytes,), "|u1").cpu()
-        x = raw.view(torch.bfloat16).view(self.Hkv, 2, 2, self.w, 64)     # [kvh][kv][half][token][64]
-        return x.permute(0, 1, 3, 2, 4).reshape(self.Hkv, 2, self.w, HEAD_DIM)
+        H = v.num_kv_heads   # KV heads of a unit: 1 with per-head tiers
+        x = raw.view(torch.bfloat16).view(H, 2, 2, self.w, 64)     # [kvh][kv][half][token][64]
+        return x.permute(0, 1, 3, 2, 4).reshape(H, 2, self.w, HEAD_DIM)
 
     def ledger_window(self, layer, slot):
         """Decoded ledger slot: codes uint8 [Hkv][2][w][d], scale/min fp16 [Hkv][2][w][d/32]."""
         v = self.view(layer)
         raw = device_tensor(v.ledger_pool + slot * v.ledger_slot_bytes, (v.ledger_slot_bytes,), "|u1").cpu()
-        return decode_ledger_slot(raw, self.Hkv, self.w)
+        return decode_ledger_slot(raw, v.num_kv_heads, self.w)
 
 
 def decode_ledger_slot(raw: torch.Tensor, Hkv: int, w: int):

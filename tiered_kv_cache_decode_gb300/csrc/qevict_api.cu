@@ -209,7 +209,21 @@ qevict_status check_config(const qevict_config &cfg) {
         return fail(QEVICT_ERR_INVALID_ARG, "capacities must be >= 0");
     const int Wmax = (cfg.max_context + cfg.window - 1) / cfg.window;
     if (Wmax > 4096) return fail(QEVICT_ERR_INVALID_ARG, "at most 4096 windows per sequence (got %d)", Wmax);
+    if (cfg.tier_per_kv_head && (int64_t)cfg.batch * cfg.num_kv_heads > 65535)
+        return fail(QEVICT_ERR_INVALID_ARG, "with per-head tiers batch x num_kv_heads must be at most 65535");
     return QEVICT_OK;
+}
+
+// The configuration the cache works with: with per-head tiers every
+// (sequence, KV head) pair is a unit of 1 KV head and G query heads.
+qevict_config unit_config(const qevict_config &cfg) {
+    qevict_config u = cfg;
+    if (cfg.tier_per_kv_head) {
+        u.batch = cfg.batch * cfg.num_kv_heads;
+        u.num_q_heads = cfg.num_q_heads / cfg.num_kv_heads;
+        u.num_kv_heads = 1;
+    }
+    return u;
 }
 
 }  // namespace
@@ -221,7 +235,7 @@ qevict_status qevict_pool_capacity(const qevict_config *config, int32_t *fp_capa
     if (!config || !fp_capacity || !ledger_capacity) return fail(QEVICT_ERR_INVALID_ARG, "NULL argument");
     qevict_status st = check_config(*config);
     if (st) return st;
-    const qevict_config &cfg = *config;
+    const qevict_config cfg = unit_config(*config);
     const int Wmax = (cfg.max_context + cfg.window - 1) / cfg.window;
     int64_t c_fp, c_q;
     window_costs(cfg.window, cfg.num_kv_heads, &c_fp, &c_q);
@@ -240,11 +254,12 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
                                   qevict_cache **out) {
     if (!config || !out) return fail(QEVICT_ERR_INVALID_ARG, "config and out must not be NULL");
     *out = nullptr;
-    const qevict_config &cfg = *config;
     {
-        const qevict_status cs = check_config(cfg);
+        const qevict_status cs = check_config(*config);
         if (cs) return cs;
     }
+    const qevict_config cfg = unit_config(*config);
+    const int hs = config->tier_per_kv_head ? config->num_kv_heads : 1;
     const int Wmax = (cfg.max_context + cfg.window - 1) / cfg.window;
     if (allocator && (!allocator->alloc || !allocator->free))
         return fail(QEVICT_ERR_INVALID_ARG, "allocator needs both alloc and free");
@@ -305,6 +320,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     for (int l = 0; l < cfg.num_layers; ++l) {
         LayerDev &D = c->layers[l].dev;
         D.B = B;
+        D.hs = hs;
         D.Hq = Hq;
         D.Hkv = Hkv;
         D.G = c->G;
@@ -647,11 +663,12 @@ qevict_status qevict_future_missed_mass(qevict_cache *c, int32_t layer, const vo
         return fail(QEVICT_ERR_INVALID_ARG, "batch x n_tokens passes 2^31 - 1");
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return fail(QEVICT_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-    // k_full as [B * n_tokens][Hkv][128]: boxes of 64 channels x 1 KV head x 16 tokens
+    // k_full as [sequences * n_tokens][model KV heads][128]: boxes of 64 channels x 1 KV head x 16 tokens
     CUtensorMap kmap{};
-    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)c->cfg.num_kv_heads,
-                                (cuuint64_t)c->cfg.batch * (cuuint64_t)n_tokens};
-    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)c->cfg.num_kv_heads * kHeadDim * 2};
+    const int hs = lh.dev.hs;
+    const cuuint64_t heads = (cuuint64_t)c->cfg.num_kv_heads * hs;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, heads, (cuuint64_t)(c->cfg.batch / hs) * (cuuint64_t)n_tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, heads * kHeadDim * 2};
     const cuuint32_t box[3] = {64, 1, 16};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(k_full), dims, strides, box, estr,

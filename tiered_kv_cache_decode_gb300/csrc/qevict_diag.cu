@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(kFmmThreads, 1) fmm_kernel(const LayerDev D, c
     const int t1 = min(L, 16 * (int)((int64_t)nch * (split + 1) / splits));
     const uint8_t *tier = D.tier + (int64_t)b * D.Wmax;
     auto chunk0 = [&](int k) { return t0 + (warp + k * kFmmWarps) * 16; };
+    // the unit's KV head and first token in the map (a unit may be a (sequence, KV head) pair)
+    const int ky = (b % D.hs) * D.Hkv + kvh, kz = (b / D.hs) * L;
 
     if (lane == 0)
         for (int i = 0; i < kFmmStages; ++i) mbar_init(bars + 8 * i, 1);
@@ -156,8 +158,8 @@ __global__ void __launch_bounds__(kFmmThreads, 1) fmm_kernel(const LayerDev D, c
         const int st = k % kFmmStages, c0 = chunk0(k);
         const uint32_t bar = bars + 8 * st, dst = wring + st * kFmmStage;
         mbar_expect_tx(bar, (uint32_t)kFmmStage);
-        tma_3d(dst, &kmap, 0, kvh, b * L + c0, bar, pol);
-        tma_3d(dst + 2048, &kmap, 64, kvh, b * L + c0, bar, pol);
+        tma_3d(dst, &kmap, 0, ky, kz + c0, bar, pol);
+        tma_3d(dst + 2048, &kmap, 64, ky, kz + c0, bar, pol);
     };
     int issued = 0;
     if (lane == 0)

@@ -57,7 +57,8 @@ __host__ __device__ inline int vword_index(int ch) {
 
 // Everything a kernel needs about one layer of the cache (passed by value).
 struct LayerDev {
-    int B, Hq, Hkv, G, w, Wmax, CF, CQ;
+    int B, Hq, Hkv, G, w, Wmax, CF, CQ;   // per unit: a sequence, or a (sequence, KV head) pair
+    int hs;                     // KV heads folded into units: 1, or the model's Hkv with per-head tiers
     int max_context;
     double beta, rho;           // budget fraction and its full-precision share
     int64_t c_fp, c_q;          // bytes of one window per sequence in each visible tier
@@ -79,6 +80,12 @@ struct LayerDev {
     int4 *work_c;         // [B][Wmax] prefill copy: {window, dst fp slot, 0, 0}
     int32_t *diag;        // [B][8] counts of the last completed tier move (see qevict_get_tier_move_counts)
 };
+
+// Row of token t of unit u in a caller's [units / hs][n][Hkv * hs][d] token array
+// (a unit is a sequence, or with per-head tiers a (sequence, KV head) pair)
+__device__ __forceinline__ int64_t src_row(const LayerDev &D, int u, int64_t n, int64_t t, int h) {
+    return (((int64_t)(u / D.hs) * n + t) * D.hs + u % D.hs) * D.Hkv + h;
+}
 
 // Decode scratch, shared by all layers of a cache: a decode launch touches it
 // only after its dependency wait, so consecutive launches never overlap in it.
@@ -128,8 +135,8 @@ cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScra
                           int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
                           float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s);
 cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s);
-// kmap: k_full [B * n_tokens][Hkv][128] bf16 as a 3-D tiled map, boxes of
-// 64 channels x 1 KV head x 16 tokens, 128-byte swizzle
+// kmap: k_full [sequences * n_tokens][Hkv * hs][128] bf16 as a 3-D tiled map,
+// boxes of 64 channels x 1 KV head x 16 tokens, 128-byte swizzle
 cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, int layer,
                                       const CUtensorMap &kmap, const __nv_bfloat16 *q, int n_tokens, float *fmm,
                                       int num_sms, cudaStream_t s);

@@ -113,7 +113,7 @@ __global__ void append_kernel(LayerDev D, CacheDev C, int layer, const __nv_bflo
         const int wi = (int)(p / w), row = (int)(p % w);
         const int slot = D.fp_slot[wb + wi];
         if (slot < 0) continue;
-        const __nv_bfloat16 *src = (kv ? v : k) + (((int64_t)b * n_new + t) * D.Hkv + h) * kHeadDim;
+        const __nv_bfloat16 *src = (kv ? v : k) + src_row(D, b, n_new, t, h) * kHeadDim;
         __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)slot * D.fp_slot_bytes) +
                              fp_off(h, kv, w, row, 8 * c);
         *reinterpret_cast<uint4 *>(dst) = reinterpret_cast<const uint4 *>(src)[c];
@@ -552,8 +552,7 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
                 src = reinterpret_cast<const __nv_bfloat16 *>(D.fp_pool + (int64_t)src_slot * D.fp_slot_bytes) +
                       fp_off(h, kv, w, t, g * kGroup);
             } else {
-                src = (kv ? v_ext : k_ext) + (((int64_t)b * ext_len + (int64_t)wi * w + t) * D.Hkv + h) * kHeadDim +
-                      g * kGroup;
+                src = (kv ? v_ext : k_ext) + src_row(D, b, ext_len, (int64_t)wi * w + t, h) * kHeadDim + g * kGroup;
             }
             float x[kGroup];
 #pragma unroll
@@ -670,7 +669,7 @@ __global__ void __launch_bounds__(128) prefill_copy_kernel(LayerDev D, const __n
         const __nv_bfloat16 *srcb = kv ? v_ext : k_ext;
         for (int i = threadIdx.x; i < ntok * kChunks; i += blockDim.x) {
             const int t = i / kChunks, c = i % kChunks;
-            const __nv_bfloat16 *src = srcb + (((int64_t)b * ext_len + (int64_t)wi * w + t) * D.Hkv + h) * kHeadDim;
+            const __nv_bfloat16 *src = srcb + src_row(D, b, ext_len, (int64_t)wi * w + t, h) * kHeadDim;
             *reinterpret_cast<uint4 *>(dst + fp_off(h, kv, w, t, 8 * c)) = reinterpret_cast<const uint4 *>(src)[c];
         }
     }
