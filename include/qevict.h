@@ -258,6 +258,34 @@ qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void 
 qevict_status qevict_route(qevict_cache *cache, int32_t layer, const float *scores_override,
                            const float *score_mult, void *stream);
 
+/* One routing event over all layers of the cache under one byte budget per
+ * sequence ("Technische Samenvatting: DBTrimKV", section 3: one global budget
+ * instead of budgets per layer or head, every cached entry ranked globally
+ * by one utility score; the utility here is the cumulative attention score,
+ * on one scale across layers because each layer spreads one unit of mass per
+ * query head per decode step). The per-layer rule of qevict_route is applied
+ * with the candidates, the budget and the forced windows widened to all
+ * layers (and KV heads, with per-head tiers) of a sequence:
+ *   budget B = floor(beta * sum over layers and units of L * Hkv * d * 4);
+ *   the last window of every unit of every layer is forced full precision;
+ *   n_fp = min(C, max(forced, floor(rho * B / c_fp))),
+ *   n_q = min(C - n_fp, floor((B - n_fp * c_fp) / c_q)), c_fp and c_q of one
+ *   unit's window; rank by score descending, then (layer, unit, window)
+ *   ascending; the top n_fp full precision, the next n_q INT2, the rest
+ *   evicted, with the transitions of qevict_route in every layer.
+ * Layers may end up with different numbers of windows, so a layer can need
+ * more slots than its pools were sized for from its own budget share: size
+ * fp_capacity and ledger_capacity for it (a layer whose pool runs out sets
+ * CAPACITY and keeps its tiers).
+ *  scores_override  NULL, or a HOST array of num_layers pointers, each NULL
+ *                   or a device fp32 [units][ceil(length / window)] array
+ *                   that replaces that layer's cumulative scores first.
+ * BUDGET (host) if the forced windows alone pass the budget. A non-finite
+ * score among the candidates sets DEVICE and leaves every layer's tiers
+ * unchanged. Uses one table of ranking keys per cache: do not overlap two
+ * global events of one cache. */
+qevict_status qevict_route_global(qevict_cache *cache, const float *const *scores_override, void *stream);
+
 /* Demote the listed windows FP -> INT2 (QEvict "Demotie"), in list order.
  * bw_ids: int32 [n][2] device array of (sequence, window) pairs. A window
  * without a ledger entry is quantised per token, KV head and group of 32

@@ -543,6 +543,73 @@ def queries_to_units(q, Hkv):
     return q.reshape(B * Hkv, Hq // Hkv, d)
 
 
+# ---- one budget across layers and KV heads (an option) ------------------------
+#
+# "Technische Samenvatting: DBTrimKV", section 3 (global budget): instead of a
+# budget per layer or head, one budget M_global for the whole cache, every
+# cached entry ranked globally by one utility score and the top ones kept.
+# Here the utility is the cumulative attention score: every layer spreads one
+# unit of mass per query head per decode step over its windows, so the
+# layers' scores share a scale without learned gates. The QEvict rule is
+# applied unchanged with the candidate set, the budget and the forced windows
+# widened to all layers (and, with per-head units, all KV heads) of a
+# sequence:
+#   budget   B_g = floor(beta * sum over the layers and units of L * Hkv * d * 4)
+#   forced   the last window of every unit of every layer (full precision)
+#   counts   n_fp = min(C, max(n_forced, floor(rho * B_g / c_fp))),
+#            n_q  = min(C - n_fp, floor((B_g - n_fp * c_fp) / c_q))
+#   ranking  forced first, then score descending, then (layer, unit, window)
+#            ascending; top n_fp full precision, next n_q INT2, rest evicted.
+
+def route_global(layers, hs=1, scores_override=None):
+    """One routing event over several layers under one byte budget per
+    sequence. `layers`: OracleCache per layer with the same units and window;
+    `hs`: units per sequence (1, or Hkv with per-head units); scores_override:
+    optional list (per layer) of [units][W] arrays replacing the scores.
+    Moves every layer's tiers (evict, demote, promote per unit) and sets each
+    layer's last_counts; raises BudgetError if the forced windows do not fit."""
+    if scores_override is not None:
+        for c, ov in zip(layers, scores_override):
+            ov = np.asarray(ov, np.float64)
+            c.S = [ov[u, :c.W].copy() for u in range(c.B)]
+    first = layers[0]
+    U, w, d = first.B, first.w, first.d
+    c_fp, c_q = window_costs(w, first.Hkv, d)
+    new = [c.tiers().copy() for c in layers]
+    for b in range(U // hs):
+        units = range(b * hs, (b + 1) * hs)
+        F = sum(c.L * c.Hkv * d * 4 for c in layers for _ in units)
+        Bg = int(math.floor(first.beta * F))
+        forced, cand = [], []
+        for li, c in enumerate(layers):
+            for j, u in enumerate(units):
+                W = c.W
+                for wi in range(W):
+                    if c.win[u][wi].tier == TIER_E:
+                        continue
+                    s = float(c.S[u][wi])
+                    if not math.isfinite(s):
+                        raise OracleError("non-finite score among routing candidates")
+                    (forced if wi == W - 1 else cand).append((li, j, wi, s))
+        if not forced and not cand:
+            continue
+        if len(forced) * c_fp > Bg:
+            raise BudgetError(f"budget {Bg} B cannot hold the {len(forced)} open windows")
+        C = len(forced) + len(cand)
+        n_fp = min(C, max(len(forced), fp_budget_windows(Bg, c_fp, first.rho)))
+        n_q = min(C - n_fp, (Bg - n_fp * c_fp) // c_q)
+        order = sorted(forced, key=lambda e: e[:3]) + sorted(cand, key=lambda e: (-e[3], e[0], e[1], e[2]))
+        for r, (li, j, wi, _) in enumerate(order):
+            new[li][b * hs + j, wi] = TIER_FP if r < n_fp else (TIER_Q if r < n_fp + n_q else TIER_E)
+    for li, c in enumerate(layers):
+        counts = []
+        for u in range(U):
+            old = c.tiers_now(u)
+            c.apply_tiers(u, new[li][u])
+            counts.append(transition_counts(old, c.tiers_now(u)))
+        c.last_counts = np.stack(counts)
+
+
 def tiered_bytes(cache: OracleCache) -> int:
     """Attention-visible bytes resident for all sequences (FP c_fp, INT2 c_q, E 0)."""
     c_fp, c_q = window_costs(cache.w, cache.Hkv, cache.d)

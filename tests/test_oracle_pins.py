@@ -561,3 +561,115 @@ def test_per_head_attention_reads_only_its_own_windows():
             p = np.exp(s - s.max())
             p /= p.sum()
             assert np.allclose(out[b, h], p @ v[b, toks, kvh].astype(np.float64), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- one budget across layers and heads
+
+def _layers(n_layers, B, Hq, Hkv, w, L, beta, rng, per_head=False):
+    out = []
+    for _ in range(n_layers):
+        k = O.bf16_round(rng.standard_normal((B, L, Hkv, 128)))
+        if per_head:
+            c = O.per_head_cache(B, Hq, Hkv, 128, w, beta=beta)
+            c.prefill(O.to_units(k), O.to_units(k), tiers=np.zeros((B * Hkv, -(-L // w)), np.uint8))
+        else:
+            c = O.OracleCache(B, Hq, Hkv, 128, w, beta=beta)
+            c.prefill(k, k, tiers=np.zeros((B, -(-L // w)), np.uint8))
+        out.append(c)
+    return out
+
+
+def test_global_route_over_one_layer_is_the_layer_route():
+    rng = np.random.default_rng(8)
+    B, Hq, Hkv, w, L, beta = 3, 8, 2, 16, 300, 0.2
+    a = _layers(1, B, Hq, Hkv, w, L, beta, rng)
+    b = _layers(1, B, Hq, Hkv, w, L, beta, np.random.default_rng(8))
+    for _ in range(3):
+        S = rng.random((B, -(-L // w)))
+        a[0].route(scores_override=S)
+        O.route_global(b, scores_override=[S])
+        assert np.array_equal(a[0].tiers(), b[0].tiers())
+        assert np.array_equal(a[0].last_counts, b[0].last_counts)
+
+
+def _brute_global(layers, hs, b):
+    """Every assignment of the sequence's non-forced candidates with the
+    closed-form counts inside the budget; the best by (sum of FP scores, sum of
+    retained scores), then the lowest (layer, unit, window) indices."""
+    first = layers[0]
+    c_fp, c_q = O.window_costs(first.w, first.Hkv, first.d)
+    units = range(b * hs, (b + 1) * hs)
+    Bg = int(math.floor(first.beta * sum(c.L * c.Hkv * c.d * 4 for c in layers for _ in units)))
+    forced, cand = [], []
+    for li, c in enumerate(layers):
+        for j, u in enumerate(units):
+            for wi in range(c.W):
+                if c.win[u][wi].tier != O.TIER_E:
+                    (forced if wi == c.W - 1 else cand).append((li, j, wi, float(c.S[u][wi])))
+    C = len(forced) + len(cand)
+    n_fp = min(C, max(len(forced), O.fp_budget_windows(Bg, c_fp, first.rho)))
+    n_q = min(C - n_fp, (Bg - n_fp * c_fp) // c_q)
+    best, best_key = None, None
+    for assign in itertools.product((O.TIER_FP, O.TIER_Q, O.TIER_E), repeat=len(cand)):
+        fp = [e for e, a in zip(cand, assign) if a == O.TIER_FP]
+        qq = [e for e, a in zip(cand, assign) if a == O.TIER_Q]
+        if len(fp) + len(forced) != n_fp or len(qq) != n_q:
+            continue
+        if (len(fp) + len(forced)) * c_fp + len(qq) * c_q > Bg:
+            continue
+        key = (sum(e[3] for e in fp), sum(e[3] for e in fp + qq),
+               [tuple(-x for x in e[:3]) for e in sorted(fp)], [tuple(-x for x in e[:3]) for e in sorted(fp + qq)])
+        if best_key is None or key > best_key:
+            best, best_key = {e[:3]: a for e, a in zip(cand, assign)}, key
+    return best
+
+
+@pytest.mark.parametrize("n_layers,Hkv,per_head,Ls", [(2, 2, False, (96, 96)), (3, 1, False, (64, 80, 48)),
+                                                      (1, 2, True, (96,)), (2, 2, True, (64, 64))])
+def test_global_route_matches_brute_force(n_layers, Hkv, per_head, Ls):
+    rng = np.random.default_rng(9)
+    w, beta = 16, 0.35
+    hs = Hkv if per_head else 1
+    layers = []
+    for li in range(n_layers):
+        layers += _layers(1, 1, 2 * Hkv, Hkv, w, Ls[li], beta, rng, per_head=per_head)
+    for event in range(3):
+        S = [rng.integers(0, 4, size=(c.B, c.W)).astype(np.float64) for c in layers]   # ties on purpose
+        for c, s in zip(layers, S):
+            c.S = [s[u].copy() for u in range(c.B)]
+        want = _brute_global(layers, hs, 0)
+        O.route_global(layers, hs=hs)
+        for (li, j, wi), a in want.items():
+            assert layers[li].win[j][wi].tier == a, (event, li, j, wi)
+
+
+def test_global_route_invariants_and_counts():
+    """Bytes kept within the one budget; among the non-forced candidates every
+    full-precision score >= every INT2 score >= every newly evicted score;
+    layers may keep different numbers of windows."""
+    rng = np.random.default_rng(10)
+    B, Hq, Hkv, w, beta = 2, 8, 2, 16, 0.2
+    layers = [c for L in (320, 320, 320) for c in _layers(1, B, Hq, Hkv, w, L, beta, rng)]
+    c_fp, c_q = O.window_costs(w, Hkv, 128)
+    for event in range(4):
+        S = [rng.random((B, c.W)) * (1 + 3 * li) for li, c in enumerate(layers)]
+        before = [c.tiers().copy() for c in layers]
+        O.route_global(layers, scores_override=S)
+        per_layer_fp = []
+        for b in range(B):
+            Bg = int(math.floor(beta * sum(c.L * Hkv * 128 * 4 for c in layers)))
+            used = sum(c_fp * (c.tiers()[b] == O.TIER_FP).sum() + c_q * (c.tiers()[b] == O.TIER_Q).sum()
+                       for c in layers)
+            assert used <= Bg
+            tiers_of = {}
+            for li, c in enumerate(layers):
+                for wi in range(c.W - 1):
+                    if before[li][b, wi] != O.TIER_E:
+                        tiers_of.setdefault(c.tiers()[b, wi], []).append(S[li][b, wi])
+                per_layer_fp.append((c.tiers()[b] == O.TIER_FP).sum())
+            fp, q, e = (tiers_of.get(t, []) for t in (O.TIER_FP, O.TIER_Q, O.TIER_E))
+            if fp and q:
+                assert min(fp) >= max(q)
+            if q and e:
+                assert min(q) >= max(e)
+        assert len(set(per_layer_fp)) > 1   # the budget moves between layers

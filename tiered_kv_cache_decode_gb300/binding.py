@@ -28,7 +28,7 @@ EXPORTS = ["qevict_pool_capacity", "qevict_cache_create", "qevict_cache_destroy"
            "qevict_promote_dequantize", "qevict_set_tiers", "qevict_get_scores", "qevict_get_view",
            "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_set_launch_overlap",
            "qevict_refresh_lengths", "qevict_decode_attention_static_scratch",
-           "qevict_get_tier_move_counts", "qevict_future_missed_mass", "qevict_length",
+           "qevict_get_tier_move_counts", "qevict_future_missed_mass", "qevict_route_global", "qevict_length",
            "qevict_last_error"]
 
 
@@ -110,6 +110,7 @@ def load() -> ctypes.CDLL:
         "qevict_refresh_lengths": [P, P],
         "qevict_decode_attention_static_scratch": [P, I32, P, P, P, I32, P],
         "qevict_get_tier_move_counts": [P, I32, P, P],
+        "qevict_route_global": [P, P, P],
         "qevict_future_missed_mass": [P, I32, P, P, I64, P, P],
         "qevict_length": [P, I32],
         "qevict_last_error": [],
@@ -263,6 +264,14 @@ class TieredCache:
     def route(self, layer, scores_override=None, score_mult=None, stream=None):
         self._check(self.lib.qevict_route(self.handle, layer, _ptr(scores_override), _ptr(score_mult),
                                           _stream(stream)))
+
+    def route_global(self, scores_override=None, stream=None):
+        """One routing event over all layers under one budget per sequence;
+        scores_override: None or a list (per layer) of None / device [units][W] fp32."""
+        arr = None
+        if scores_override is not None:
+            arr = (ctypes.c_void_p * self.layers)(*[None if t is None else t.data_ptr() for t in scores_override])
+        self._check(self.lib.qevict_route_global(self.handle, arr, _stream(stream)))
 
     def demote(self, layer, pairs, stream=None):
         self._check(self.lib.qevict_demote_quantize(self.handle, layer, _ptr(pairs), pairs.shape[0],

@@ -80,6 +80,11 @@ struct qevict_cache {
     void *prev_stream = nullptr;
     void *scratch_base = nullptr;
     size_t scratch_bytes = 0;
+    // global routing: the layers' device descriptors, ranking keys, thresholds, flags
+    int hs = 1;   // KV heads folded into each unit (per-head tiers), else 1
+    LayerDev *ldev = nullptr;
+    unsigned long long *gkeys = nullptr, *gthr = nullptr;
+    int32_t *gflag = nullptr;
     bool allow_pdl = false;    // qevict_set_launch_overlap
 };
 
@@ -209,6 +214,8 @@ qevict_status check_config(const qevict_config &cfg) {
         return fail(QEVICT_ERR_INVALID_ARG, "capacities must be >= 0");
     const int Wmax = (cfg.max_context + cfg.window - 1) / cfg.window;
     if (Wmax > 4096) return fail(QEVICT_ERR_INVALID_ARG, "at most 4096 windows per sequence (got %d)", Wmax);
+    if ((int64_t)cfg.num_layers * (cfg.tier_per_kv_head ? cfg.num_kv_heads : 1) * Wmax > 0xffffffffll)
+        return fail(QEVICT_ERR_INVALID_ARG, "layers x windows (x KV heads with per-head tiers) must be below 2^32");
     if (cfg.tier_per_kv_head && (int64_t)cfg.batch * cfg.num_kv_heads > 65535)
         return fail(QEVICT_ERR_INVALID_ARG, "with per-head tiers batch x num_kv_heads must be at most 65535");
     return QEVICT_OK;
@@ -316,6 +323,26 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         c->scratch_bytes = cv.off;
         c->scratch_base = base;
     }
+    c->hs = hs;
+    {
+        const int S = B / hs;
+        Carver cv;
+        const size_t o_ld = cv.take((size_t)cfg.num_layers * sizeof(LayerDev));
+        const size_t o_gk = cv.take((size_t)S * cfg.num_layers * hs * Wmax * 8);
+        const size_t o_gt = cv.take((size_t)S * 16);
+        const size_t o_gf = cv.take((size_t)S * 4);
+        uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
+        if (!base) {
+            const size_t need = cv.off;
+            release_all(c);
+            delete c;
+            return fail(QEVICT_ERR_OUT_OF_MEMORY, "allocation of %zu B of routing tables failed", need);
+        }
+        c->ldev = (LayerDev *)(base + o_ld);
+        c->gkeys = (unsigned long long *)(base + o_gk);
+        c->gthr = (unsigned long long *)(base + o_gt);
+        c->gflag = (int32_t *)(base + o_gf);
+    }
     c->layers.resize(cfg.num_layers);
     for (int l = 0; l < cfg.num_layers; ++l) {
         LayerDev &D = c->layers[l].dev;
@@ -397,6 +424,11 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     }
     if (err == cudaSuccess) err = cudaMemsetAsync(c->cbase, 0, 256, c->stream);
     if (err == cudaSuccess) err = cudaMemsetAsync(c->scratch_base, 0, c->scratch_bytes, c->stream);
+    std::vector<LayerDev> ltab(cfg.num_layers);   // alive until the synchronisation below
+    for (int l = 0; l < cfg.num_layers; ++l) ltab[l] = c->layers[l].dev;
+    if (err == cudaSuccess)
+        err = cudaMemcpyAsync(c->ldev, ltab.data(), ltab.size() * sizeof(LayerDev), cudaMemcpyHostToDevice,
+                              c->stream);
     for (int l = 0; l < cfg.num_layers && err == cudaSuccess; ++l) {
         err = launch_init_layer(c->layers[l].dev, c->stream);
         if (err == cudaSuccess) err = cudaMemsetAsync(c->layers[l].dev.diag, 0, (size_t)B * 8 * 4, c->stream);
@@ -502,6 +534,59 @@ qevict_status qevict_decode_step(qevict_cache *c, int32_t layer, const void *q, 
     qevict_status st = decode_common(c, layer, q, k_new, v_new, out, mass, accumulate_scores, stream);
     if (!st) note_op(c, layer, stream);
     return st;
+}
+
+qevict_status qevict_route_global(qevict_cache *c, const float *const *scores_override, void *stream) {
+    if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    const qevict_config &cfg = c->cfg;
+    cudaStream_t s = (cudaStream_t)stream;
+    // host check of the one budget against the forced windows (host lengths)
+    int64_t F = 0;
+    int forced = 0;
+    for (int l = 0; l < cfg.num_layers; ++l) {
+        F += (int64_t)c->hs * c->layers[l].length * cfg.num_kv_heads * kHeadDim * 4;
+        forced += c->layers[l].length > 0 ? c->hs : 0;
+    }
+    if (forced == 0) return QEVICT_OK;
+    const int64_t Bg = (int64_t)floor(cfg.budget_frac * (double)F);
+    if ((int64_t)forced * c->c_fp > Bg)
+        return fail(QEVICT_ERR_BUDGET, "budget %lld B cannot hold the %d open windows (%lld B each)", (long long)Bg,
+                    forced, (long long)c->c_fp);
+    cudaError_t e = cudaSuccess;
+    if (scores_override)
+        for (int l = 0; l < cfg.num_layers && e == cudaSuccess; ++l)
+            if (scores_override[l] && c->layers[l].length > 0)
+                e = launch_set_scores(c->layers[l].dev, scores_override[l], n_windows(c, c->layers[l].length), s);
+    if (e != cudaSuccess) return cuda_fail(e, "score override kernel");
+    GlobalArgs g{};
+    g.layers = c->ldev;
+    g.num_layers = cfg.num_layers;
+    g.hs = c->hs;
+    g.Wmax = c->Wmax;
+    g.w = cfg.window;
+    g.beta = cfg.budget_frac;
+    g.rho = cfg.fp_share;
+    g.c_fp = c->c_fp;
+    g.c_q = c->c_q;
+    g.keys = c->gkeys;
+    g.thr = c->gthr;
+    g.flag = c->gflag;
+    e = launch_global_select(g, c->cdev, cfg.batch / c->hs, s);
+    if (e != cudaSuccess) return cuda_fail(e, "global select kernel");
+    for (int l = 0; l < cfg.num_layers; ++l) {
+        LayerHost &lh = c->layers[l];
+        if (lh.length == 0) continue;
+        PlanArgs a{};
+        a.mode = PLAN_GLOBAL;
+        a.layer = l;
+        a.gkeys = c->gkeys;
+        a.gthr = c->gthr;
+        a.gflag = c->gflag;
+        a.glayers = cfg.num_layers;
+        const qevict_status st = run_plan(c, lh, a, nullptr, nullptr, s);
+        if (st) return st;
+    }
+    return QEVICT_OK;
 }
 
 qevict_status qevict_route(qevict_cache *c, int32_t layer, const float *scores_override, const float *score_mult,

@@ -105,7 +105,7 @@ struct CacheDev {
 };
 
 enum PlanMode { PLAN_ROUTE = 0, PLAN_TIERS = 1, PLAN_PREFILL_SCORES = 2, PLAN_PREFILL_TIERS = 3,
-                PLAN_DEMOTE = 4, PLAN_PROMOTE = 5 };
+                PLAN_DEMOTE = 4, PLAN_PROMOTE = 5, PLAN_GLOBAL = 6 };
 
 struct PlanArgs {
     int mode;
@@ -116,10 +116,30 @@ struct PlanArgs {
     const uint8_t *tiers; // [B][n_win]
     const int32_t *pairs; // [n][2]
     int n_pairs;
+    // PLAN_GLOBAL: the ranking keys and thresholds of one routing event over all layers
+    const unsigned long long *gkeys;   // [sequences][layers][hs][Wmax], 0 for non-candidates
+    const unsigned long long *gthr;    // [sequences][2]: keys >= [0] full precision, >= [1] INT2
+    const int32_t *gflag;              // [sequences]: 0 = leave this sequence's tiers unchanged
+    int glayers;                       // layers in the key table
+};
+
+// One routing event over all layers of a cache under one budget per sequence.
+struct GlobalArgs {
+    const LayerDev *layers;            // device table [num_layers]
+    int num_layers, hs, Wmax, w;
+    double beta, rho;
+    int64_t c_fp, c_q;                 // window costs of one unit
+    unsigned long long *keys;          // as PlanArgs::gkeys
+    unsigned long long *thr;
+    int32_t *flag;
 };
 
 // ---- launchers (each enqueues on `s`, returns the launch error) -----------
 cudaError_t launch_init_layer(const LayerDev &L, cudaStream_t s);
+// Keys, budget, counts and the two thresholds of a global routing event (one CTA per sequence)
+cudaError_t launch_global_select(const GlobalArgs &g, const CacheDev &C, int sequences, cudaStream_t s);
+// Replace a layer's cumulative scores by scores [units][n_win] (the override of a global event)
+cudaError_t launch_set_scores(const LayerDev &L, const float *scores, int n_win, cudaStream_t s);
 cudaError_t launch_append(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *k,
                           const __nv_bfloat16 *v, int n_new, cudaStream_t s);
 cudaError_t launch_plan(const LayerDev &L, const CacheDev &C, const PlanArgs &a, cudaStream_t s);

@@ -346,6 +346,23 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                 s_tgt[wi] = r < n_fp ? QEVICT_TIER_FP : (r < n_fp + n_q ? QEVICT_TIER_Q : QEVICT_TIER_E);
             }
             __syncthreads();
+        } else if (a.mode == PLAN_GLOBAL) {
+            // the sequence's keys across all layers were ranked by global_select_kernel:
+            // classify this layer's candidates against its two thresholds
+            const int seq = b / D.hs, j = b % D.hs;
+            if (a.gflag[seq] == 0) {   // the event stopped on an error, reported by the select kernel
+                if (tid == 0) reserve_next(D, ctr, b);
+                return;
+            }
+            const unsigned long long t_fp = a.gthr[2 * seq], t_q = a.gthr[2 * seq + 1];
+            const unsigned long long *keys =
+                a.gkeys + ((int64_t)seq * a.glayers * D.hs + (int64_t)a.layer * D.hs + j) * D.Wmax;
+            for (int i = tid; i < nw; i += kPlanThreads) {
+                if (s_cur[i] == QEVICT_TIER_E) continue;
+                const unsigned long long k = keys[i];
+                s_tgt[i] = k >= t_fp ? QEVICT_TIER_FP : (k >= t_q ? QEVICT_TIER_Q : QEVICT_TIER_E);
+            }
+            __syncthreads();
         } else {
             for (int i = tid; i < nw; i += kPlanThreads) {
                 const uint8_t t = a.tiers[(int64_t)b * nw + i];
@@ -690,7 +707,180 @@ __global__ void scores_kernel(LayerDev D, int n_win, float *out) {
     }
 }
 
+// ---------------------------------------------------------------- global routing
+// Ranking key of a candidate window of a global routing event: larger ranks
+// first. Forced (the last window of each unit of each layer) above everything,
+// then the score, then the lower (layer, unit, window) index. Unique within a
+// sequence, and never 0 (0 marks a non-candidate).
+__device__ __forceinline__ unsigned long long global_key(float S, bool forced, uint32_t gidx) {
+    return ((unsigned long long)(forced ? 0xffffffffu : orderable(S)) << 32) | (0xffffffffu - gidx);
+}
+
+// Of the 256 digit bins (counts h[d]), the digit of the K-th largest key among
+// those in the bins, with *rem = K on entry and K's rank inside that bin on
+// exit. Warp-wide: lane L sums bins 255 - 8L down to 248 - 8L.
+__device__ __forceinline__ int top_bin(const unsigned *h, long long *rem, int lane) {
+    unsigned part = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part += h[255 - 8 * lane - i];
+    unsigned incl = part;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const long long r = *rem;
+    const unsigned ball = __ballot_sync(0xffffffffu, (long long)incl >= r);
+    const int L = __ffs(ball) - 1;   // the first lane whose bins reach rank r
+    int digit = 0;
+    long long left = 0;
+    if (lane == L) {
+        long long cum = (long long)(incl - part);
+        for (int i = 0; i < 8; ++i) {
+            const int d = 255 - 8 * lane - i;
+            if (cum + h[d] >= r) {
+                digit = d;
+                left = r - cum;
+                break;
+            }
+            cum += h[d];
+        }
+    }
+    digit = __shfl_sync(0xffffffffu, digit, L);
+    left = __shfl_sync(0xffffffffu, left, L);
+    *rem = left;
+    return digit;
+}
+
+// One CTA per sequence: writes the sequence's ranking keys for every layer,
+// unit and window (collapsing each score's per-KV-head partials into one
+// value, as a per-layer route does), computes the one budget and the counts,
+// and finds by radix selection the n_fp-th and (n_fp + n_q)-th largest keys.
+__global__ void __launch_bounds__(1024) global_select_kernel(GlobalArgs g, CacheDev C) {
+    const int seq = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ unsigned s_h[2][256];
+    __shared__ int s_cand, s_forced, s_bad;
+    __shared__ unsigned long long s_pre[2];
+    __shared__ long long s_rem[2];
+    const int64_t per_unit = g.Wmax, per_layer = (int64_t)g.hs * g.Wmax;
+    unsigned long long *keys = g.keys + (int64_t)seq * g.num_layers * per_layer;
+    if (tid == 0) {
+        s_cand = 0;
+        s_forced = 0;
+        s_bad = 0;
+    }
+    __syncthreads();
+    int cand = 0, forced = 0, bad = 0;
+    for (int l = 0; l < g.num_layers; ++l) {
+        const LayerDev &D = g.layers[l];
+        const int u0 = seq * g.hs;
+        const int64_t len = D.ctr[u0 * kCtrN + CTR_LEN];
+        const int nw = (int)((len + g.w - 1) / g.w);
+        for (int64_t i = tid; i < per_layer; i += blockDim.x) {
+            const int j = (int)(i / per_unit), wi = (int)(i % per_unit), u = u0 + j;
+            unsigned long long key = 0;
+            if (wi < nw && D.tier[(int64_t)u * D.Wmax + wi] != QEVICT_TIER_E) {
+                float S = 0.f;
+                for (int h = 0; h < D.Hkv; ++h) S += D.score_part[((int64_t)u * D.Hkv + h) * D.Wmax + wi];
+                if (S == 0.f) S = 0.f;   // one zero: -0 and +0 rank as equal
+                for (int h = 0; h < D.Hkv; ++h) D.score_part[((int64_t)u * D.Hkv + h) * D.Wmax + wi] = h == 0 ? S : 0.f;
+                if (!isfinite(S)) bad = 1;
+                const bool f = wi == nw - 1;
+                key = global_key(S, f, (uint32_t)(l * per_layer + i));
+                ++cand;
+                forced += f;
+            }
+            keys[l * per_layer + i] = key;
+        }
+    }
+    if (cand) atomicAdd(&s_cand, cand);
+    if (forced) atomicAdd(&s_forced, forced);
+    if (bad) s_bad = 1;
+    __syncthreads();
+    if (tid == 0) {
+        int go = 1;
+        int64_t F = 0;
+        for (int l = 0; l < g.num_layers; ++l) {
+            const LayerDev &D = g.layers[l];
+            F += (int64_t)g.hs * D.ctr[seq * g.hs * kCtrN + CTR_LEN] * D.Hkv * kHeadDim * 4;
+        }
+        const int64_t Bg = (int64_t)floor(g.beta * (double)F);
+        const int C_ = s_cand, nf = s_forced;
+        int n_fp = 0, n_q = 0;
+        if (s_bad) {
+            set_status(C, QEVICT_ERR_DEVICE, -1, seq, -1);
+            go = 0;
+        } else if ((int64_t)nf * g.c_fp > Bg) {
+            set_status(C, QEVICT_ERR_BUDGET, -1, seq, nf);
+            go = 0;
+        } else {
+            const int nfp_budget = (int)floor((g.rho * (double)Bg) / (double)g.c_fp);
+            n_fp = min(C_, max(nf, nfp_budget));
+            const int64_t rem = Bg - (int64_t)n_fp * g.c_fp;
+            n_q = (int)min((int64_t)(C_ - n_fp), rem > 0 ? rem / g.c_q : 0);
+        }
+        g.flag[seq] = go;
+        s_rem[0] = n_fp;
+        s_rem[1] = (long long)n_fp + n_q;
+        s_pre[0] = 0;
+        s_pre[1] = 0;
+        s_bad = go;
+    }
+    __syncthreads();
+    if (!s_bad) return;
+    // ranks 0 (no full precision at all) and beyond the candidates select nothing
+    const bool want0 = s_rem[0] > 0, want1 = s_rem[1] > 0;
+    unsigned long long mask = 0;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 512; i += blockDim.x) (&s_h[0][0])[i] = 0;
+        __syncthreads();
+        const unsigned long long p0 = s_pre[0], p1 = s_pre[1];
+        for (int64_t i = tid; i < (int64_t)g.num_layers * per_layer; i += blockDim.x) {
+            const unsigned long long k = keys[i];
+            if (!k) continue;
+            const unsigned d = (unsigned)(k >> shift) & 255u;
+            if ((k & mask) == p0) atomicAdd(&s_h[0][d], 1u);
+            if ((k & mask) == p1) atomicAdd(&s_h[1][d], 1u);
+        }
+        __syncthreads();
+        if (warp < 2 && (warp == 0 ? want0 : want1)) {
+            long long r = s_rem[warp];
+            const int d = top_bin(s_h[warp], &r, lane);
+            if (lane == 0) {
+                s_rem[warp] = r;
+                s_pre[warp] |= (unsigned long long)d << shift;
+            }
+        }
+        mask |= 0xffull << shift;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        // no rank asked: a threshold above every key
+        g.thr[2 * seq] = want0 ? s_pre[0] : ~0ull;
+        g.thr[2 * seq + 1] = want1 ? s_pre[1] : ~0ull;
+    }
+}
+
+__global__ void set_scores_kernel(LayerDev D, const float *scores, int n_win) {
+    const int64_t n = (int64_t)D.B * n_win;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int u = (int)(i / n_win), wi = (int)(i % n_win);
+        for (int h = 0; h < D.Hkv; ++h)
+            D.score_part[((int64_t)u * D.Hkv + h) * D.Wmax + wi] = h == 0 ? scores[i] : 0.f;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_global_select(const GlobalArgs &g, const CacheDev &C, int sequences, cudaStream_t s) {
+    global_select_kernel<<<sequences, 1024, 0, s>>>(g, C);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_scores(const LayerDev &L, const float *scores, int n_win, cudaStream_t s) {
+    set_scores_kernel<<<64, 256, 0, s>>>(L, scores, n_win);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_init_layer(const LayerDev &L, cudaStream_t s) {
     init_layer_kernel<<<256, 256, 0, s>>>(L);
