@@ -292,6 +292,79 @@ def measure_diagnostics(cache, wl, NL, pool, nq, nkv, stream, reps, dev):
     }
 
 
+def measure_variants(wl, NL, reps, dev, peak):
+    """The workload with per-KV-head tiers: every (sequence, KV head) routed on
+    its own seeded scores. Times the decode kernel over all layers (CUDA graph,
+    the same algorithmic bytes as the shared mode plus one score per window per
+    extra KV head), then routing events on fresh seeded scores: one event under
+    one budget across all layers and KV heads (qevict_route_global) against one
+    routing per layer, both captured as CUDA graphs on one stream."""
+    import torch
+    from tiered_kv_cache_decode_gb300 import binding, synth
+    B, Hq, Hkv, w, L0, d, seed = wl["B"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"], 128, 0
+    W0 = L0 // w
+    units = B * Hkv
+    # pools for every window: a global event may give one layer more than its own share
+    ph = binding.TieredCache(B, NL, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"], per_head=True,
+                             fp_capacity=W0, ledger_capacity=W0)
+    ph.set_launch_overlap(True)
+    for l in range(NL):
+        k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
+        ph.prefill(l, k, v, scores=synth.zipf_scores(seed, l, units, W0, device=dev))
+        del k, v
+    q = [synth.queries(seed, l, 0, B, Hq, d, device=dev) for l in range(NL)]
+    xo = torch.empty(NL, B, Hq, d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    ovs = [torch.empty(units, W0, dtype=torch.float32, device=dev) for _ in range(NL)]
+    g_dec, g_glob, g_layer = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_dec, stream=stream):
+            for l in range(NL):
+                ph.decode(l, q[l], out=xo[l], want_mass=False, accumulate=True, stream=stream)
+        with torch.cuda.graph(g_glob, stream=stream):
+            ph.route_global(ovs, stream=stream)
+        with torch.cuda.graph(g_layer, stream=stream):
+            for l in range(NL):
+                ph.route(l, scores_override=ovs[l], stream=stream)
+        for _ in range(3):
+            g_dec.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g_dec.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us_dec = e0.elapsed_time(e1) * 1e3 / (reps * NL)
+    nbytes = TierTracker(wl, L0).decode_bytes() + B * (Hkv - 1) * W0 * 8
+    route_us = {}
+    for name, g in (("global", g_glob), ("per_layer", g_layer)):
+        tot = 0.0
+        for r in range(8):
+            for l in range(NL):
+                ovs[l].copy_(synth.zipf_scores(seed + 100 + r, l, units, W0, device=dev) * (1.0 + 0.02 * l))
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1) * 1e3
+        route_us[name] = round(tot / 8, 2)
+    st = ph.status()
+    assert st == 0, f"device status {st}: {ph.last_error()}"
+    kept = [int((ph.tables(l)[0] != 2).sum()) for l in range(NL)]
+    return {
+        "per_kv_head_decode": {"us_per_launch": round(us_dec, 3), "bytes_per_launch": int(nbytes),
+                               "gbs": round(nbytes / (us_dec * 1e-6) / 1e9, 2),
+                               "frac_of_peak": round(nbytes / (us_dec * 1e-6) / 1e9 / peak, 4)},
+        "routing_event_us": {"global_all_layers_and_heads": route_us["global"],
+                             "one_per_layer": route_us["per_layer"], "layers": NL,
+                             "keys_per_sequence": NL * Hkv * W0,
+                             "windows_kept_per_layer_min_max": [min(kept), max(kept)]},
+    }
+
+
 def run_native(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -489,6 +562,10 @@ def run_native(args, rank, world, local_rank):
     if diagnostics is not None:
         diagnostics["future_missed_mass"]["frac_of_peak"] = round(diagnostics["future_missed_mass"]["gbs"] / peak, 4)
         line["diagnostics"] = diagnostics
+    if not args.no_variants:
+        del cache, pool
+        torch.cuda.empty_cache()
+        line["variants"] = measure_variants(wl, NL, K, dev, peak)
     if pool_async is not None:
         cpu_pool, nw, res, t_start = pool_async
         out = res.get()
@@ -533,6 +610,8 @@ def main():
                     help="run fewer layers of the same per-layer workload (profiling captures)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) leg")
     ap.add_argument("--no-diag", action="store_true", help="skip the routing diagnostics leg")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the per-KV-head and global-routing leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -82,9 +82,11 @@ struct qevict_cache {
     size_t scratch_bytes = 0;
     // global routing: the layers' device descriptors, ranking keys, thresholds, flags
     int hs = 1;   // KV heads folded into each unit (per-head tiers), else 1
+    void *groute_base = nullptr;
+    size_t groute_bytes = 0;
     LayerDev *ldev = nullptr;
     unsigned long long *gkeys = nullptr, *gthr = nullptr;
-    int32_t *gflag = nullptr;
+    int32_t *gflag = nullptr, *gcnt = nullptr;
     bool allow_pdl = false;    // qevict_set_launch_overlap
 };
 
@@ -331,6 +333,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         const size_t o_gk = cv.take((size_t)S * cfg.num_layers * hs * Wmax * 8);
         const size_t o_gt = cv.take((size_t)S * 16);
         const size_t o_gf = cv.take((size_t)S * 4);
+        const size_t o_gc = cv.take((size_t)S * 16);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
         if (!base) {
             const size_t need = cv.off;
@@ -342,6 +345,9 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         c->gkeys = (unsigned long long *)(base + o_gk);
         c->gthr = (unsigned long long *)(base + o_gt);
         c->gflag = (int32_t *)(base + o_gf);
+        c->gcnt = (int32_t *)(base + o_gc);
+        c->groute_base = base;
+        c->groute_bytes = cv.off;
     }
     c->layers.resize(cfg.num_layers);
     for (int l = 0; l < cfg.num_layers; ++l) {
@@ -424,6 +430,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     }
     if (err == cudaSuccess) err = cudaMemsetAsync(c->cbase, 0, 256, c->stream);
     if (err == cudaSuccess) err = cudaMemsetAsync(c->scratch_base, 0, c->scratch_bytes, c->stream);
+    if (err == cudaSuccess) err = cudaMemsetAsync(c->groute_base, 0, c->groute_bytes, c->stream);
     std::vector<LayerDev> ltab(cfg.num_layers);   // alive until the synchronisation below
     for (int l = 0; l < cfg.num_layers; ++l) ltab[l] = c->layers[l].dev;
     if (err == cudaSuccess)
@@ -548,6 +555,7 @@ qevict_status qevict_route_global(qevict_cache *c, const float *const *scores_ov
         forced += c->layers[l].length > 0 ? c->hs : 0;
     }
     if (forced == 0) return QEVICT_OK;
+    if (cfg.batch / c->hs > 65535) return fail(QEVICT_ERR_INVALID_ARG, "a global event takes at most 65535 sequences");
     const int64_t Bg = (int64_t)floor(cfg.budget_frac * (double)F);
     if ((int64_t)forced * c->c_fp > Bg)
         return fail(QEVICT_ERR_BUDGET, "budget %lld B cannot hold the %d open windows (%lld B each)", (long long)Bg,
@@ -571,6 +579,7 @@ qevict_status qevict_route_global(qevict_cache *c, const float *const *scores_ov
     g.keys = c->gkeys;
     g.thr = c->gthr;
     g.flag = c->gflag;
+    g.cnt = c->gcnt;
     e = launch_global_select(g, c->cdev, cfg.batch / c->hs, s);
     if (e != cudaSuccess) return cuda_fail(e, "global select kernel");
     for (int l = 0; l < cfg.num_layers; ++l) {

@@ -132,11 +132,13 @@ struct GlobalArgs {
     unsigned long long *keys;          // as PlanArgs::gkeys
     unsigned long long *thr;
     int32_t *flag;
+    int32_t *cnt;                      // [sequences][4]: candidates, forced, non-finite (0 between events)
 };
 
 // ---- launchers (each enqueues on `s`, returns the launch error) -----------
 cudaError_t launch_init_layer(const LayerDev &L, cudaStream_t s);
-// Keys, budget, counts and the two thresholds of a global routing event (one CTA per sequence)
+// Keys (all layers in parallel), then budget, counts and the two thresholds of
+// a global routing event (one CTA per sequence)
 cudaError_t launch_global_select(const GlobalArgs &g, const CacheDev &C, int sequences, cudaStream_t s);
 // Replace a layer's cumulative scores by scores [units][n_win] (the override of a global event)
 cudaError_t launch_set_scores(const LayerDev &L, const float *scores, int n_win, cudaStream_t s);

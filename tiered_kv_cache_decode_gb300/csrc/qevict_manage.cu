@@ -752,51 +752,58 @@ __device__ __forceinline__ int top_bin(const unsigned *h, long long *rem, int la
     return digit;
 }
 
-// One CTA per sequence: writes the sequence's ranking keys for every layer,
-// unit and window (collapsing each score's per-KV-head partials into one
-// value, as a per-layer route does), computes the one budget and the counts,
-// and finds by radix selection the n_fp-th and (n_fp + n_q)-th largest keys.
+// Keys of a global routing event: one CTA per (range of 1024 entries of a
+// layer's [hs][Wmax] table, layer, sequence). Writes the ranking key of every
+// candidate window (0 elsewhere), collapsing each score's per-KV-head
+// partials into one value as a per-layer route does, and adds the sequence's
+// candidate, forced and non-finite counts to g.cnt.
+__global__ void __launch_bounds__(1024) global_keys_kernel(GlobalArgs g) {
+    const int l = blockIdx.y, seq = blockIdx.z, tid = threadIdx.x;
+    const int64_t per_layer = (int64_t)g.hs * g.Wmax;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + tid;
+    const LayerDev &D = g.layers[l];
+    const int u0 = seq * g.hs;
+    const int64_t len = D.ctr[u0 * kCtrN + CTR_LEN];
+    const int nw = (int)((len + g.w - 1) / g.w);
+    int cand = 0, forced = 0, bad = 0;
+    if (i < per_layer) {
+        const int j = (int)(i / g.Wmax), wi = (int)(i % g.Wmax), u = u0 + j;
+        unsigned long long key = 0;
+        if (wi < nw && D.tier[(int64_t)u * D.Wmax + wi] != QEVICT_TIER_E) {
+            float S = 0.f;
+            for (int h = 0; h < D.Hkv; ++h) S += D.score_part[((int64_t)u * D.Hkv + h) * D.Wmax + wi];
+            if (S == 0.f) S = 0.f;   // one zero: -0 and +0 rank as equal
+            for (int h = 0; h < D.Hkv; ++h) D.score_part[((int64_t)u * D.Hkv + h) * D.Wmax + wi] = h == 0 ? S : 0.f;
+            bad = !isfinite(S);
+            const bool f = wi == nw - 1;
+            key = global_key(S, f, (uint32_t)(l * per_layer + i));
+            cand = 1;
+            forced = f;
+        }
+        g.keys[((int64_t)seq * g.num_layers + l) * per_layer + i] = key;
+    }
+    cand = __reduce_add_sync(0xffffffffu, cand);
+    forced = __reduce_add_sync(0xffffffffu, forced);
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if ((tid & 31) == 0 && (cand | bad)) {
+        atomicAdd(&g.cnt[4 * seq], cand);
+        atomicAdd(&g.cnt[4 * seq + 1], forced);
+        if (bad) atomicOr(&g.cnt[4 * seq + 2], 1);
+    }
+}
+
+// One CTA per sequence, after global_keys_kernel: the one budget and the
+// counts, then the n_fp-th and (n_fp + n_q)-th largest keys by radix
+// selection (8 passes of 8 bits over the sequence's key table). Leaves the
+// sequence's counters at zero for the next event.
 __global__ void __launch_bounds__(1024) global_select_kernel(GlobalArgs g, CacheDev C) {
     const int seq = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ unsigned s_h[2][256];
-    __shared__ int s_cand, s_forced, s_bad;
+    __shared__ int s_go;
     __shared__ unsigned long long s_pre[2];
     __shared__ long long s_rem[2];
-    const int64_t per_unit = g.Wmax, per_layer = (int64_t)g.hs * g.Wmax;
-    unsigned long long *keys = g.keys + (int64_t)seq * g.num_layers * per_layer;
-    if (tid == 0) {
-        s_cand = 0;
-        s_forced = 0;
-        s_bad = 0;
-    }
-    __syncthreads();
-    int cand = 0, forced = 0, bad = 0;
-    for (int l = 0; l < g.num_layers; ++l) {
-        const LayerDev &D = g.layers[l];
-        const int u0 = seq * g.hs;
-        const int64_t len = D.ctr[u0 * kCtrN + CTR_LEN];
-        const int nw = (int)((len + g.w - 1) / g.w);
-        for (int64_t i = tid; i < per_layer; i += blockDim.x) {
-            const int j = (int)(i / per_unit), wi = (int)(i % per_unit), u = u0 + j;
-            unsigned long long key = 0;
-            if (wi < nw && D.tier[(int64_t)u * D.Wmax + wi] != QEVICT_TIER_E) {
-                float S = 0.f;
-                for (int h = 0; h < D.Hkv; ++h) S += D.score_part[((int64_t)u * D.Hkv + h) * D.Wmax + wi];
-                if (S == 0.f) S = 0.f;   // one zero: -0 and +0 rank as equal
-                for (int h = 0; h < D.Hkv; ++h) D.score_part[((int64_t)u * D.Hkv + h) * D.Wmax + wi] = h == 0 ? S : 0.f;
-                if (!isfinite(S)) bad = 1;
-                const bool f = wi == nw - 1;
-                key = global_key(S, f, (uint32_t)(l * per_layer + i));
-                ++cand;
-                forced += f;
-            }
-            keys[l * per_layer + i] = key;
-        }
-    }
-    if (cand) atomicAdd(&s_cand, cand);
-    if (forced) atomicAdd(&s_forced, forced);
-    if (bad) s_bad = 1;
-    __syncthreads();
+    const int64_t per_seq = (int64_t)g.num_layers * g.hs * g.Wmax;
+    const unsigned long long *keys = g.keys + (int64_t)seq * per_seq;
     if (tid == 0) {
         int go = 1;
         int64_t F = 0;
@@ -805,9 +812,12 @@ __global__ void __launch_bounds__(1024) global_select_kernel(GlobalArgs g, Cache
             F += (int64_t)g.hs * D.ctr[seq * g.hs * kCtrN + CTR_LEN] * D.Hkv * kHeadDim * 4;
         }
         const int64_t Bg = (int64_t)floor(g.beta * (double)F);
-        const int C_ = s_cand, nf = s_forced;
+        const int C_ = g.cnt[4 * seq], nf = g.cnt[4 * seq + 1], bad = g.cnt[4 * seq + 2];
+        g.cnt[4 * seq] = 0;
+        g.cnt[4 * seq + 1] = 0;
+        g.cnt[4 * seq + 2] = 0;
         int n_fp = 0, n_q = 0;
-        if (s_bad) {
+        if (bad) {
             set_status(C, QEVICT_ERR_DEVICE, -1, seq, -1);
             go = 0;
         } else if ((int64_t)nf * g.c_fp > Bg) {
@@ -824,23 +834,33 @@ __global__ void __launch_bounds__(1024) global_select_kernel(GlobalArgs g, Cache
         s_rem[1] = (long long)n_fp + n_q;
         s_pre[0] = 0;
         s_pre[1] = 0;
-        s_bad = go;
+        s_go = go;
     }
     __syncthreads();
-    if (!s_bad) return;
-    // ranks 0 (no full precision at all) and beyond the candidates select nothing
+    if (!s_go) return;
+    // rank 0 (no full precision at all: no candidates) selects nothing
     const bool want0 = s_rem[0] > 0, want1 = s_rem[1] > 0;
     unsigned long long mask = 0;
     for (int shift = 56; shift >= 0; shift -= 8) {
         for (int i = tid; i < 512; i += blockDim.x) (&s_h[0][0])[i] = 0;
         __syncthreads();
         const unsigned long long p0 = s_pre[0], p1 = s_pre[1];
-        for (int64_t i = tid; i < (int64_t)g.num_layers * per_layer; i += blockDim.x) {
-            const unsigned long long k = keys[i];
-            if (!k) continue;
-            const unsigned d = (unsigned)(k >> shift) & 255u;
-            if ((k & mask) == p0) atomicAdd(&s_h[0][d], 1u);
-            if ((k & mask) == p1) atomicAdd(&s_h[1][d], 1u);
+        // 8 keys in flight per thread
+        for (int64_t i0 = tid; i0 < per_seq; i0 += 8 * (int64_t)blockDim.x) {
+            unsigned long long kk[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t i = i0 + (int64_t)u * blockDim.x;
+                kk[u] = i < per_seq ? __ldcg(keys + i) : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const unsigned long long k = kk[u];
+                if (!k) continue;
+                const unsigned d = (unsigned)(k >> shift) & 255u;
+                if ((k & mask) == p0) atomicAdd(&s_h[0][d], 1u);
+                if ((k & mask) == p1) atomicAdd(&s_h[1][d], 1u);
+            }
         }
         __syncthreads();
         if (warp < 2 && (warp == 0 ? want0 : want1)) {
@@ -873,6 +893,10 @@ __global__ void set_scores_kernel(LayerDev D, const float *scores, int n_win) {
 }  // namespace
 
 cudaError_t launch_global_select(const GlobalArgs &g, const CacheDev &C, int sequences, cudaStream_t s) {
+    const int64_t per_layer = (int64_t)g.hs * g.Wmax;
+    global_keys_kernel<<<dim3((unsigned)((per_layer + 1023) / 1024), g.num_layers, sequences), 1024, 0, s>>>(g);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     global_select_kernel<<<sequences, 1024, 0, s>>>(g, C);
     return cudaGetLastError();
 }
