@@ -316,7 +316,8 @@ def measure_variants(wl, NL, reps, dev, peak):
     xo = torch.empty(NL, B, Hq, d, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     ovs = [torch.empty(units, W0, dtype=torch.float32, device=dev) for _ in range(NL)]
-    g_dec, g_glob, g_layer = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_dec, g_glob, g_layer, g_ls = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                    torch.cuda.CUDAGraph())
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g_dec, stream=stream):
@@ -327,6 +328,9 @@ def measure_variants(wl, NL, reps, dev, peak):
         with torch.cuda.graph(g_layer, stream=stream):
             for l in range(NL):
                 ph.route(l, scores_override=ovs[l], stream=stream)
+        with torch.cuda.graph(g_ls, stream=stream):
+            for l in range(NL):
+                ph.route_logsparse(l, recent=2, stream=stream)
         for _ in range(3):
             g_dec.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -351,17 +355,43 @@ def measure_variants(wl, NL, reps, dev, peak):
             torch.cuda.synchronize()
             tot += e0.elapsed_time(e1) * 1e3
         route_us[name] = round(tot / 8, 2)
+        if name == "global":   # windows each layer keeps after a global event
+            kept = [int((ph.tables(l)[0] != 2).sum()) for l in range(NL)]
+    # log-sparse events: positions do not move between replays, so each timed
+    # event follows an untimed global event on fresh scores that scrambles the tiers
+    tot = 0.0
+    for r in range(8):
+        for l in range(NL):
+            ovs[l].copy_(synth.zipf_scores(seed + 200 + r, l, units, W0, device=dev))
+        with torch.cuda.stream(stream):
+            g_glob.replay()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g_ls.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1) * 1e3
+    route_us["logsparse"] = round(tot / 8, 2)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g_dec.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us_dec_ls = e0.elapsed_time(e1) * 1e3 / (reps * NL)
     st = ph.status()
     assert st == 0, f"device status {st}: {ph.last_error()}"
-    kept = [int((ph.tables(l)[0] != 2).sum()) for l in range(NL)]
     return {
         "per_kv_head_decode": {"us_per_launch": round(us_dec, 3), "bytes_per_launch": int(nbytes),
                                "gbs": round(nbytes / (us_dec * 1e-6) / 1e9, 2),
-                               "frac_of_peak": round(nbytes / (us_dec * 1e-6) / 1e9 / peak, 4)},
+                               "frac_of_peak": round(nbytes / (us_dec * 1e-6) / 1e9 / peak, 4),
+                               "us_per_launch_after_logsparse_route": round(us_dec_ls, 3)},
         "routing_event_us": {"global_all_layers_and_heads": route_us["global"],
-                             "one_per_layer": route_us["per_layer"], "layers": NL,
+                             "one_per_layer": route_us["per_layer"],
+                             "logsparse_one_per_layer": route_us["logsparse"], "layers": NL,
                              "keys_per_sequence": NL * Hkv * W0,
-                             "windows_kept_per_layer_min_max": [min(kept), max(kept)]},
+                             "windows_kept_per_layer_after_global_min_max": [min(kept), max(kept)]},
     }
 
 

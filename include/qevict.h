@@ -258,6 +258,21 @@ qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void 
 qevict_status qevict_route(qevict_cache *cache, int32_t layer, const float *scores_override,
                            const float *score_mult, void *stream);
 
+/* A routing event by position instead of score ("Technische Samenvatting:
+ * LogQuant", Methodologie 1-2: attention peaks thin out logarithmically with
+ * the distance to the current token, so the kept positions thin out the same
+ * way). Windows are ranked by age (0 = the open window): the recent_windows
+ * newest are dense; before them, region l = 1, 2, ... covers ages
+ * [R 2^(l-1), R 2^l) (R = recent_windows) and its windows join at spacing
+ * 2^l in the first round and at half the previous spacing in each later
+ * round; the rank is (round, region, age), lowest first. The budget, the
+ * counts and the transitions are qevict_route's, with this rank in place of
+ * the score: the first n_fp windows of the order (the open one always among
+ * them) stay or become full precision, the next n_q INT2, the rest evicted.
+ * The cumulative scores are neither read nor changed. INVALID_ARG if
+ * recent_windows < 1, BUDGET as qevict_route. */
+qevict_status qevict_route_logsparse(qevict_cache *cache, int32_t layer, int32_t recent_windows, void *stream);
+
 /* One routing event over all layers of the cache under one byte budget per
  * sequence ("Technische Samenvatting: DBTrimKV", section 3: one global budget
  * instead of budgets per layer or head, every cached entry ranked globally

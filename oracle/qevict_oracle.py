@@ -543,6 +543,51 @@ def queries_to_units(q, Hkv):
     return q.reshape(B * Hkv, Hq // Hkv, d)
 
 
+# ---- a positional router (an option) ----------------------------------------
+#
+# "Technische Samenvatting: LogQuant", Methodologie 1-2: high-attention
+# positions thin out logarithmically with the distance to the current token,
+# so LogQuant keeps the most recent tokens at full precision and, further
+# back, tokens at a density that halves from region to region; the rest are
+# 2-bit. The summary's numbers are garbled ("2W" and "3W" recent tokens), so
+# at window granularity the reading is: the R most recent windows are dense;
+# before them, region l = 1, 2, ... covers ages [R 2^(l-1), R 2^l) (age 0 is
+# the open window) and first contributes the windows at spacing 2^l, then, in
+# later rounds, the ones at half that spacing, and so on. A window's rank is
+# (round, region, age), lowest first, so every top-k set is log-spaced and
+# each includes the smaller ones. The budget counts and the evict / demote /
+# promote moves are the score-based route's.
+
+def logsparse_rank(age: int, recent: int):
+    """(round, region, age) of a window `age` windows before the open one."""
+    if age < recent:
+        return (0, 0, age)
+    region = 1
+    while age >= recent << region:
+        region += 1
+    m = age - (recent << (region - 1))
+    tz = region if m == 0 else min(region, (m & -m).bit_length() - 1)
+    return (1 + region - tz, region, age)
+
+
+def route_logsparse(cache, recent: int = 2):
+    """A routing event of every sequence by log-sparse position instead of
+    score: the windows' ranks replace the scores in route_tiers (the scores
+    themselves are left as they are)."""
+    counts = []
+    W = cache.W
+    order = sorted(range(W), key=lambda i: logsparse_rank(W - 1 - i, recent))
+    pseudo = np.zeros(W)
+    for r, i in enumerate(order):
+        pseudo[i] = -float(r)    # higher = earlier in the order
+    for b in range(cache.B):
+        old = cache.tiers_now(b)
+        new = route_tiers(pseudo, old, cache.L, cache.w, cache.Hkv, cache.d, cache.beta, cache.rho)
+        cache.apply_tiers(b, new)
+        counts.append(transition_counts(old, cache.tiers_now(b)))
+    cache.last_counts = np.stack(counts)
+
+
 # ---- one budget across layers and KV heads (an option) ------------------------
 #
 # "Technische Samenvatting: DBTrimKV", section 3 (global budget): instead of a

@@ -673,3 +673,66 @@ def test_global_route_invariants_and_counts():
             if q and e:
                 assert min(q) >= max(e)
         assert len(set(per_layer_fp)) > 1   # the budget moves between layers
+
+
+# ---------------------------------------------------------------- log-sparse positional router
+
+def _golden_logsparse():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "logsparse_order.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        a, b = line.split("|")
+        R, W = map(int, a.split())
+        rows.append((R, W, [int(x) for x in b.split()]))
+    return rows
+
+
+@pytest.mark.parametrize("R,W,order", _golden_logsparse())
+def test_logsparse_order_hand_derived(R, W, order):
+    assert sorted(range(W), key=lambda a: O.logsparse_rank(a, R)) == order
+
+
+def test_logsparse_keeps_log_spaced_windows():
+    """Past the dense recent windows, the first round keeps one window per
+    region, regions doubling in length: the windows it keeps within distance D
+    grow like log2(D)."""
+    R, W = 2, 1024
+    order = sorted(range(W), key=lambda a: O.logsparse_rank(a, R))
+    first_round = [a for a in order if O.logsparse_rank(a, R)[0] == 1]
+    assert first_round == [R << (l - 1) for l in range(1, len(first_round) + 1)]
+    assert len(first_round) == int(math.log2(W / R))
+
+
+def test_route_logsparse_keeps_the_top_ranks_under_the_budget():
+    """The score-free route keeps the first n_fp windows of the log-sparse
+    order in full precision and the next n_q in INT2, whatever the scores."""
+    rng = np.random.default_rng(11)
+    B, Hq, Hkv, w, L, beta = 2, 8, 2, 16, 1024, 0.1
+    W = L // w
+    k = O.bf16_round(rng.standard_normal((B, L, Hkv, 128)))
+    c = O.OracleCache(B, Hq, Hkv, 128, w, beta=beta)
+    c.prefill(k, k, scores=rng.random((B, W)))
+    S_before = [s.copy() for s in c.S]
+    O.route_logsparse(c, recent=2)
+    n_fp, n_q = O.route_counts(int((c.tiers()[0] != O.TIER_E).sum()), L, w, Hkv, 128, beta, 0.5)
+    assert all(np.array_equal(a, b) for a, b in zip(S_before, c.S))   # scores untouched
+    # the previous route evicted windows the positional order may want: it
+    # can only choose among the windows still visible
+    for b in range(B):
+        t = c.tiers()[b]
+        visible = [a for a in sorted(range(W), key=lambda a: O.logsparse_rank(a, 2))
+                   if t[W - 1 - a] != O.TIER_E]
+        assert [t[W - 1 - a] for a in visible[:n_fp]] == [O.TIER_FP] * n_fp
+        assert all(t[W - 1 - a] == O.TIER_Q for a in visible[n_fp:])
+    # from an all-full-precision cache it keeps exactly the top of the order
+    c2 = O.OracleCache(B, Hq, Hkv, 128, w, beta=beta)
+    c2.prefill(k, k, tiers=np.zeros((B, W), np.uint8))
+    O.route_logsparse(c2, recent=2)
+    nf, nq = O.route_counts(W, L, w, Hkv, 128, beta, 0.5)
+    order = sorted(range(W), key=lambda a: O.logsparse_rank(a, 2))
+    want = np.full(W, O.TIER_E, np.uint8)
+    for r, a in enumerate(order):
+        want[W - 1 - a] = O.TIER_FP if r < nf else (O.TIER_Q if r < nf + nq else O.TIER_E)
+    assert np.array_equal(c2.tiers(), np.stack([want] * B))

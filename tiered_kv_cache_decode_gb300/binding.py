@@ -28,7 +28,8 @@ EXPORTS = ["qevict_pool_capacity", "qevict_cache_create", "qevict_cache_destroy"
            "qevict_promote_dequantize", "qevict_set_tiers", "qevict_get_scores", "qevict_get_view",
            "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_set_launch_overlap",
            "qevict_refresh_lengths", "qevict_decode_attention_static_scratch",
-           "qevict_get_tier_move_counts", "qevict_future_missed_mass", "qevict_route_global", "qevict_length",
+           "qevict_get_tier_move_counts", "qevict_future_missed_mass", "qevict_route_global", "qevict_route_logsparse",
+           "qevict_length",
            "qevict_last_error"]
 
 
@@ -111,6 +112,7 @@ def load() -> ctypes.CDLL:
         "qevict_decode_attention_static_scratch": [P, I32, P, P, P, I32, P],
         "qevict_get_tier_move_counts": [P, I32, P, P],
         "qevict_route_global": [P, P, P],
+        "qevict_route_logsparse": [P, I32, I32, P],
         "qevict_future_missed_mass": [P, I32, P, P, I64, P, P],
         "qevict_length": [P, I32],
         "qevict_last_error": [],
@@ -264,6 +266,10 @@ class TieredCache:
     def route(self, layer, scores_override=None, score_mult=None, stream=None):
         self._check(self.lib.qevict_route(self.handle, layer, _ptr(scores_override), _ptr(score_mult),
                                           _stream(stream)))
+
+    def route_logsparse(self, layer, recent=2, stream=None):
+        """Route a layer by log-sparse position (the scores are not used)."""
+        self._check(self.lib.qevict_route_logsparse(self.handle, layer, recent, _stream(stream)))
 
     def route_global(self, scores_override=None, stream=None):
         """One routing event over all layers under one budget per sequence;

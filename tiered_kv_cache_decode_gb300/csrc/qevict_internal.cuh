@@ -105,7 +105,7 @@ struct CacheDev {
 };
 
 enum PlanMode { PLAN_ROUTE = 0, PLAN_TIERS = 1, PLAN_PREFILL_SCORES = 2, PLAN_PREFILL_TIERS = 3,
-                PLAN_DEMOTE = 4, PLAN_PROMOTE = 5, PLAN_GLOBAL = 6 };
+                PLAN_DEMOTE = 4, PLAN_PROMOTE = 5, PLAN_GLOBAL = 6, PLAN_LOGSPARSE = 7 };
 
 struct PlanArgs {
     int mode;
@@ -116,6 +116,7 @@ struct PlanArgs {
     const uint8_t *tiers; // [B][n_win]
     const int32_t *pairs; // [n][2]
     int n_pairs;
+    int recent;           // PLAN_LOGSPARSE: dense recent windows
     // PLAN_GLOBAL: the ranking keys and thresholds of one routing event over all layers
     const unsigned long long *gkeys;   // [sequences][layers][hs][Wmax], 0 for non-candidates
     const unsigned long long *gthr;    // [sequences][2]: keys >= [0] full precision, >= [1] INT2

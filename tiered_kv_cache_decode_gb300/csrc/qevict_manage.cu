@@ -135,6 +135,21 @@ __device__ __forceinline__ uint32_t orderable(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Rank of a window `age` windows before the open one under the log-sparse
+// positional order, lowest first: (round, region, age) packed into 24 bits.
+// The `recent` newest windows are dense (round 0); region l >= 1 covers ages
+// [recent 2^(l-1), recent 2^l) and its offset m joins in round
+// 1 + l - min(l, trailing zeros of m) (m = 0 counts as l trailing zeros):
+// spacing 2^l in round 1, half of it in each later round.
+__device__ __forceinline__ uint32_t logsparse_rank(int age, int recent) {
+    if (age < recent) return (uint32_t)age;
+    int region = 1;
+    while (age >= (recent << region)) ++region;
+    const int m = age - (recent << (region - 1));
+    const int tz = m == 0 ? region : min(region, __ffs(m) - 1);
+    return ((uint32_t)(1 + region - tz) << 20) | ((uint32_t)region << 12) | (uint32_t)age;
+}
+
 // Exclusive prefix sum over the block of one int per thread; *total gets the sum.
 __device__ int block_scan(int v, int *total, int *s_warp) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -205,7 +220,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     // byte budget at this length: B_t = floor(beta * L * Hkv * d * 4)
     const int64_t budget = (int64_t)floor(D.beta * (double)(length * D.Hkv * kHeadDim * 4));
     const int nfp_budget = (int)floor((D.rho * (double)budget) / (double)D.c_fp);
-    if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES) && budget < D.c_fp) {
+    if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE) && budget < D.c_fp) {
         if (tid == 0) {
             set_status(C, QEVICT_ERR_BUDGET, a.layer, b, (int)length);
             reserve_next(D, ctr, b);
@@ -285,12 +300,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         // ---- target tiers
         for (int i = tid; i < nw; i += kPlanThreads) s_tgt[i] = s_cur[i];
         int bad = 0;
-        if (a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES) {
+        if (a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE) {
             int P = 1;
             while (P < nw) P <<= 1;
             for (int i = tid; i < P; i += kPlanThreads) {
                 unsigned long long key = ~0ull;
-                if (i < nw) {
+                if (i < nw && a.mode == PLAN_LOGSPARSE) {
+                    // by position alone; the open window (age 0) ranks first; scores untouched
+                    if (s_cur[i] != QEVICT_TIER_E)
+                        key = ((unsigned long long)logsparse_rank(nw - 1 - i, a.recent) << 32) | (unsigned)i;
+                } else if (i < nw) {
                     float S;
                     if (a.scores) {
                         S = a.scores[(int64_t)b * nw + i];
