@@ -258,6 +258,23 @@ qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void 
 qevict_status qevict_route(qevict_cache *cache, int32_t layer, const float *scores_override,
                            const float *score_mult, void *stream);
 
+/* A routing event whose tier counts come from a rate-distortion allocation
+ * ("Technische Samenvatting: RDKV", 2.1-2.2: minimise sum w_u 2^(-b_u) over
+ * bit widths b_u under a byte budget by Lagrangian relaxation over discrete
+ * widths) instead of the fp_share split. Units are windows, widths the tiers'
+ * (0 evicted, 2 INT2, 16 bf16), the weight w_u the window's cumulative score
+ * (the attention it has received). The open window is full precision first;
+ * then upgrades E -> INT2 (removing 3/4 w_u, costing c_q bytes) and INT2 ->
+ * FP (removing 1/4 - 2^-16 of w_u, costing c_fp - c_q) are taken in order of
+ * distortion removed per byte, highest first (E -> INT2 first on a tie, then
+ * by window rank), while the gain is positive, until the first that does not
+ * fit the budget floor(beta * L * Hkv * d * 4). That fixes n_fp and n_q; the
+ * windows are then assigned by score rank and moved as in qevict_route
+ * (same scores_override / score_mult, same errors). The comparisons are done
+ * in float64. */
+qevict_status qevict_route_rd(qevict_cache *cache, int32_t layer, const float *scores_override,
+                              const float *score_mult, void *stream);
+
 /* A routing event by position instead of score ("Technische Samenvatting:
  * LogQuant", Methodologie 1-2: attention peaks thin out logarithmically with
  * the distance to the current token, so the kept positions thin out the same

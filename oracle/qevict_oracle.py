@@ -543,6 +543,78 @@ def queries_to_units(q, Hkv):
     return q.reshape(B * Hkv, Hq // Hkv, d)
 
 
+# ---- rate-distortion routing (an option) ------------------------------------
+#
+# "Technische Samenvatting: RDKV", 2.1-2.2: minimise sum_u w_u sigma_u 2^(-b_u)
+# over bit widths b_u under a byte budget, solved by Lagrangian relaxation
+# (reverse water-filling) over discrete widths. Here the units are windows,
+# the widths the ones the tiers have (0 evicted, 2 INT2, 16 bf16), the weight
+# w_u is the window's cumulative attention score (RDKV's weight of a V token
+# is the attention it receives summed over queries) and sigma_u = 1. Each
+# window has two upgrades: E -> INT2 removes 3/4 w_u of distortion for c_q
+# bytes, INT2 -> FP removes (1/4 - 2^-16) w_u for c_fp - c_q bytes. The open
+# window is full precision first; the other upgrades are taken in order of
+# distortion removed per byte, highest first (E -> INT2 before INT2 -> FP on a
+# tie, then the window rank of the score route), only while positive, and
+# the first one that does not fit ends the allocation (a single multiplier).
+# The result decides (n_fp, n_q); the windows are then assigned by score rank
+# as in the score route.
+
+RD_EQ = 1.0 - 2.0 ** -2            # distortion removed by E -> INT2, per unit weight
+RD_QF = 2.0 ** -2 - 2.0 ** -16     # by INT2 -> FP
+
+
+def rd_counts(S_desc, L: int, w: int, Hkv: int, d: int, beta: float):
+    """(n_fp, n_q) of the rate-distortion allocation for one sequence; S_desc
+    are the scores of the candidate windows other than the open one, in rank
+    order (highest first)."""
+    c_fp, c_q = window_costs(w, Hkv, d)
+    Bt = budget_bytes(L, Hkv, d, beta)
+    if Bt < c_fp:
+        raise BudgetError(f"budget {Bt} B cannot hold the open window ({c_fp} B)")
+    alpha = RD_EQ / c_q
+    gamma = RD_QF / (c_fp - c_q)
+    used, a, f, n = c_fp, 0, 0, len(S_desc)
+    while True:
+        eq = alpha * float(S_desc[a]) if a < n else -math.inf
+        qf = gamma * float(S_desc[f]) if f < a else -math.inf
+        if max(eq, qf) <= 0.0:
+            break
+        cost = c_q if eq >= qf else c_fp - c_q
+        if used + cost > Bt:
+            break
+        used += cost
+        if eq >= qf:
+            a += 1
+        else:
+            f += 1
+    return 1 + f, a - f
+
+
+def route_rd(cache, scores_override=None):
+    """A routing event by the rate-distortion allocation (scores as in route)."""
+    if scores_override is not None:
+        ov = np.asarray(scores_override, np.float64)
+        cache.S = [ov[b, :cache.W].copy() for b in range(cache.B)]
+    counts = []
+    W = cache.W
+    for b in range(cache.B):
+        old = cache.tiers_now(b)
+        S = cache.S[b]
+        cand = [i for i in range(W) if old[i] != TIER_E]
+        if not all(math.isfinite(float(S[i])) for i in cand):
+            raise OracleError("non-finite score among routing candidates")
+        forced = W - 1
+        order = sorted(cand, key=lambda i: (i != forced, -float(S[i]), i))
+        n_fp, n_q = rd_counts([S[i] for i in order[1:]], cache.L, cache.w, cache.Hkv, cache.d, cache.beta)
+        new = np.array(old, np.uint8)
+        for r, i in enumerate(order):
+            new[i] = TIER_FP if r < n_fp else (TIER_Q if r < n_fp + n_q else TIER_E)
+        cache.apply_tiers(b, new)
+        counts.append(transition_counts(old, cache.tiers_now(b)))
+    cache.last_counts = np.stack(counts)
+
+
 # ---- a positional router (an option) ----------------------------------------
 #
 # "Technische Samenvatting: LogQuant", Methodologie 1-2: high-attention

@@ -736,3 +736,72 @@ def test_route_logsparse_keeps_the_top_ranks_under_the_budget():
     for r, a in enumerate(order):
         want[W - 1 - a] = O.TIER_FP if r < nf else (O.TIER_Q if r < nf + nq else O.TIER_E)
     assert np.array_equal(c2.tiers(), np.stack([want] * B))
+
+
+# ---------------------------------------------------------------- rate-distortion router
+
+def _golden_rd():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "rd_counts.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        a, b, c = line.split("|")
+        Hkv, w, L, beta = a.split()
+        S = []
+        for part in b.split():
+            n, v = part.split("x")
+            S += [float(v)] * int(n)
+        nfp, nq, ne, res = map(int, c.split())
+        rows.append((int(Hkv), int(w), int(L), float(beta), S, nfp, nq, ne, res))
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_rd())
+def test_rd_counts_hand_derived(row):
+    Hkv, w, L, beta, S, nfp, nq, ne, res = row
+    assert O.rd_counts(S, L, w, Hkv, 128, beta) == (nfp, nq)
+    assert len(S) + 1 - nfp - nq == ne
+    c_fp, c_q = O.window_costs(w, Hkv, 128)
+    assert nfp * c_fp + nq * c_q == res <= O.budget_bytes(L, Hkv, 128, beta)
+
+
+def test_rd_allocation_is_a_lagrangian_solution():
+    """With lam the per-byte gain of the first upgrade that did not fit (0 if
+    none was refused), every window's tier minimises w 2^-b + lam * cost(b)
+    over b in {0, 2, 16}, up to ties at lam; and the budget holds."""
+    rng = np.random.default_rng(12)
+    Hkv, w, d = 2, 16, 128
+    c_fp, c_q = O.window_costs(w, Hkv, d)
+    for trial in range(40):
+        L = int(rng.integers(200, 1200))
+        beta = float(rng.uniform(max(0.03, 1.2 * w / L), 0.6))   # the open window always fits
+        W = -(-L // w)
+        S = sorted((rng.pareto(1.2, W - 1) * rng.uniform(0.1, 10)).tolist(), reverse=True)
+        n_fp, n_q = O.rd_counts(S, L, w, Hkv, d, beta)
+        Bt = O.budget_bytes(L, Hkv, d, beta)
+        assert n_fp * c_fp + n_q * c_q <= Bt
+        tiers = [16] * (n_fp - 1) + [2] * n_q + [0] * (W - n_fp - n_q)
+        gains = [O.RD_EQ * s / c_q for s, t in zip(S, tiers) if t == 0] + \
+                [O.RD_QF * s / (c_fp - c_q) for s, t in zip(S, tiers) if t == 2]
+        lam = max(gains) if gains else 0.0
+        cost = {0: 0, 2: c_q, 16: c_fp}
+        for s, t in zip(S, tiers):
+            obj = {b: s * 2.0 ** -b + lam * cost[b] for b in (0, 2, 16)}
+            assert obj[t] <= min(obj.values()) * (1 + 1e-12) + 1e-300, (trial, s, t, lam)
+
+
+def test_route_rd_assigns_by_rank():
+    rng = np.random.default_rng(13)
+    B, Hq, Hkv, w, L, beta = 2, 8, 2, 16, 640, 0.15
+    W = L // w
+    k = O.bf16_round(rng.standard_normal((B, L, Hkv, 128)))
+    c = O.OracleCache(B, Hq, Hkv, 128, w, beta=beta)
+    c.prefill(k, k, tiers=np.zeros((B, W), np.uint8))
+    S = rng.pareto(1.1, (B, W))
+    O.route_rd(c, scores_override=S)
+    for b in range(B):
+        order = sorted(range(W), key=lambda i: (i != W - 1, -S[b, i], i))
+        n_fp, n_q = O.rd_counts([S[b, i] for i in order[1:]], L, w, Hkv, 128, beta)
+        t = c.tiers()[b]
+        assert [t[i] for i in order] == [O.TIER_FP] * n_fp + [O.TIER_Q] * n_q + [O.TIER_E] * (W - n_fp - n_q)

@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     __shared__ uint8_t s_old[kPlanMaxW];   // tiers before this plan, for the move's counts
     __shared__ int s_warp[kPlanThreads / 32 + 1];
     __shared__ int s_cnt[8];
+    __shared__ int s_rd[2];
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int64_t wb = (int64_t)b * D.Wmax;
@@ -220,7 +221,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     // byte budget at this length: B_t = floor(beta * L * Hkv * d * 4)
     const int64_t budget = (int64_t)floor(D.beta * (double)(length * D.Hkv * kHeadDim * 4));
     const int nfp_budget = (int)floor((D.rho * (double)budget) / (double)D.c_fp);
-    if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE) && budget < D.c_fp) {
+    if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD) &&
+        budget < D.c_fp) {
         if (tid == 0) {
             set_status(C, QEVICT_ERR_BUDGET, a.layer, b, (int)length);
             reserve_next(D, ctr, b);
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         // ---- target tiers
         for (int i = tid; i < nw; i += kPlanThreads) s_tgt[i] = s_cur[i];
         int bad = 0;
-        if (a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE) {
+        if (a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD) {
             int P = 1;
             while (P < nw) P <<= 1;
             for (int i = tid; i < P; i += kPlanThreads) {
@@ -357,9 +359,46 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             for (int i = tid; i < nw; i += kPlanThreads) ncand_local += s_cur[i] != QEVICT_TIER_E;
             int ncand;
             block_scan(ncand_local, &ncand, s_warp);
-            const int n_fp = min(ncand, max(1, nfp_budget));
-            const int64_t rem = budget - (int64_t)n_fp * D.c_fp;
-            const int n_q = (int)min((int64_t)(ncand - n_fp), rem > 0 ? rem / D.c_q : 0);
+            int n_fp, n_q;
+            if (a.mode == PLAN_RD) {
+                // Rate-distortion counts: after the open window (rank 0), upgrades E -> INT2
+                // (3/4 of the score, c_q bytes) and INT2 -> FP (1/4 - 2^-16, c_fp - c_q bytes)
+                // in order of distortion removed per byte, while positive, until the first
+                // that does not fit. float64, as the counts' reference computes them.
+                if (tid == 0) {
+                    const double alpha = 0.75 / (double)D.c_q;
+                    const double gamma = (0.25 - 1.52587890625e-05) / (double)(D.c_fp - D.c_q);
+                    auto score_at = [&](int r) {   // score of rank r >= 1, back from its sort key
+                        const uint32_t o = ~(uint32_t)(s_key[r] >> 32);
+                        const uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+                        return (double)__uint_as_float(u);
+                    };
+                    const int n = ncand - 1;
+                    int64_t used = D.c_fp;
+                    int up = 0, fp = 0;
+                    while (true) {
+                        const double eq = up < n ? alpha * score_at(1 + up) : -INFINITY;
+                        const double qf = fp < up ? gamma * score_at(1 + fp) : -INFINITY;
+                        if (fmax(eq, qf) <= 0.0) break;
+                        const int64_t cost = eq >= qf ? D.c_q : D.c_fp - D.c_q;
+                        if (used + cost > budget) break;
+                        used += cost;
+                        if (eq >= qf)
+                            ++up;
+                        else
+                            ++fp;
+                    }
+                    s_rd[0] = ncand > 0 ? 1 + fp : 0;
+                    s_rd[1] = up - fp;
+                }
+                __syncthreads();
+                n_fp = s_rd[0];
+                n_q = s_rd[1];
+            } else {
+                n_fp = min(ncand, max(1, nfp_budget));
+                const int64_t rem = budget - (int64_t)n_fp * D.c_fp;
+                n_q = (int)min((int64_t)(ncand - n_fp), rem > 0 ? rem / D.c_q : 0);
+            }
             for (int r = tid; r < ncand; r += kPlanThreads) {
                 const int wi = (int)(s_key[r] & 0xffffffffu);
                 s_tgt[wi] = r < n_fp ? QEVICT_TIER_FP : (r < n_fp + n_q ? QEVICT_TIER_Q : QEVICT_TIER_E);
