@@ -316,8 +316,8 @@ def measure_variants(wl, NL, reps, dev, peak):
     xo = torch.empty(NL, B, Hq, d, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     ovs = [torch.empty(units, W0, dtype=torch.float32, device=dev) for _ in range(NL)]
-    g_dec, g_glob, g_layer, g_ls = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
-                                    torch.cuda.CUDAGraph())
+    g_dec, g_glob, g_layer, g_ls, g_rd = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                          torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph())
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g_dec, stream=stream):
@@ -331,6 +331,9 @@ def measure_variants(wl, NL, reps, dev, peak):
         with torch.cuda.graph(g_ls, stream=stream):
             for l in range(NL):
                 ph.route_logsparse(l, recent=2, stream=stream)
+        with torch.cuda.graph(g_rd, stream=stream):
+            for l in range(NL):
+                ph.route_rd(l, scores_override=ovs[l], stream=stream)
         for _ in range(3):
             g_dec.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -342,7 +345,7 @@ def measure_variants(wl, NL, reps, dev, peak):
     us_dec = e0.elapsed_time(e1) * 1e3 / (reps * NL)
     nbytes = TierTracker(wl, L0).decode_bytes() + B * (Hkv - 1) * W0 * 8
     route_us = {}
-    for name, g in (("global", g_glob), ("per_layer", g_layer)):
+    for name, g in (("global", g_glob), ("per_layer", g_layer), ("rd", g_rd)):
         tot = 0.0
         for r in range(8):
             for l in range(NL):
@@ -373,6 +376,25 @@ def measure_variants(wl, NL, reps, dev, peak):
         torch.cuda.synchronize()
         tot += e0.elapsed_time(e1) * 1e3
     route_us["logsparse"] = round(tot / 8, 2)
+    # decode on the tiers of a rate-distortion event (its counts differ from the fp_share split)
+    for l in range(NL):
+        ovs[l].copy_(synth.zipf_scores(seed + 300, l, units, W0, device=dev))
+    with torch.cuda.stream(stream):
+        g_rd.replay()
+        for _ in range(3):
+            g_dec.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g_dec.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us_dec_rd = e0.elapsed_time(e1) * 1e3 / (reps * NL)
+    c_fp_u, c_q_u = w * d * 4, w * 2 * (d // 4 + 4 * (d // 32))
+    tiers_rd = torch.stack([ph.tables(l)[0] for l in range(NL)])   # [NL][units][W]
+    n_fp_rd = (tiers_rd == 0).sum(dim=2).double()
+    n_q_rd = (tiers_rd == 1).sum(dim=2).double()
+    bytes_rd = ((n_fp_rd * c_fp_u + n_q_rd * c_q_u).sum(dim=1).mean().item()
+                + B * (Hq * d * 2 + Hq * d * 4 + Hkv * W0 * 8))
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(reps):
@@ -387,6 +409,14 @@ def measure_variants(wl, NL, reps, dev, peak):
                                "gbs": round(nbytes / (us_dec * 1e-6) / 1e9, 2),
                                "frac_of_peak": round(nbytes / (us_dec * 1e-6) / 1e9 / peak, 4),
                                "us_per_launch_after_logsparse_route": round(us_dec_ls, 3)},
+        "rate_distortion": {"route_us_per_event_32_layers": route_us["rd"],
+                            "fp_int2_evicted_per_unit_mean": [round(n_fp_rd.mean().item(), 2),
+                                                              round(n_q_rd.mean().item(), 2),
+                                                              round(W0 - n_fp_rd.mean().item() - n_q_rd.mean().item(),
+                                                                    2)],
+                            "decode_us_per_launch": round(us_dec_rd, 3), "decode_bytes_per_launch": int(bytes_rd),
+                            "decode_gbs": round(bytes_rd / (us_dec_rd * 1e-6) / 1e9, 2),
+                            "decode_frac_of_peak": round(bytes_rd / (us_dec_rd * 1e-6) / 1e9 / peak, 4)},
         "routing_event_us": {"global_all_layers_and_heads": route_us["global"],
                              "one_per_layer": route_us["per_layer"],
                              "logsparse_one_per_layer": route_us["logsparse"], "layers": NL,

@@ -191,7 +191,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     __shared__ uint8_t s_old[kPlanMaxW];   // tiers before this plan, for the move's counts
     __shared__ int s_warp[kPlanThreads / 32 + 1];
     __shared__ int s_cnt[8];
-    __shared__ int s_rd[2];
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int64_t wb = (int64_t)b * D.Wmax;
@@ -361,39 +360,53 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             block_scan(ncand_local, &ncand, s_warp);
             int n_fp, n_q;
             if (a.mode == PLAN_RD) {
-                // Rate-distortion counts: after the open window (rank 0), upgrades E -> INT2
-                // (3/4 of the score, c_q bytes) and INT2 -> FP (1/4 - 2^-16, c_fp - c_q bytes)
-                // in order of distortion removed per byte, while positive, until the first
-                // that does not fit. float64, as the counts' reference computes them.
-                if (tid == 0) {
-                    const double alpha = 0.75 / (double)D.c_q;
-                    const double gamma = (0.25 - 1.52587890625e-05) / (double)(D.c_fp - D.c_q);
-                    auto score_at = [&](int r) {   // score of rank r >= 1, back from its sort key
-                        const uint32_t o = ~(uint32_t)(s_key[r] >> 32);
-                        const uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
-                        return (double)__uint_as_float(u);
-                    };
-                    const int n = ncand - 1;
-                    int64_t used = D.c_fp;
-                    int up = 0, fp = 0;
-                    while (true) {
-                        const double eq = up < n ? alpha * score_at(1 + up) : -INFINITY;
-                        const double qf = fp < up ? gamma * score_at(1 + fp) : -INFINITY;
-                        if (fmax(eq, qf) <= 0.0) break;
-                        const int64_t cost = eq >= qf ? D.c_q : D.c_fp - D.c_q;
-                        if (used + cost > budget) break;
-                        used += cost;
-                        if (eq >= qf)
-                            ++up;
+                // Rate-distortion counts. After the open window (rank 0) come upgrades
+                // E -> INT2 of rank-i window (gain A[i] = alpha s_i, c_q bytes) and INT2 -> FP
+                // (Q[i] = gamma s_i, c_fp - c_q bytes), taken in the merged order of the two
+                // non-increasing lists (A first on a tie, then by rank) while positive, until the
+                // first that does not fit. The taken ones are a prefix of the merged order, so each
+                // upgrade finds its merged rank by binary search in the other list, adds up the cost
+                // of the prefix through itself and decides alone. float64 gains, as the counts'
+                // reference computes them.
+                const double alpha = 0.75 / (double)D.c_q;
+                const double gamma = (0.25 - 1.52587890625e-05) / (double)(D.c_fp - D.c_q);
+                auto score_at = [&](int i) {   // score of rank i + 1, back from its sort key
+                    const uint32_t o = ~(uint32_t)(s_key[1 + i] >> 32);
+                    const uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+                    return (double)__uint_as_float(u);
+                };
+                const int n = ncand - 1;
+                const int64_t room = budget - D.c_fp;
+                int up_local = 0, fp_local = 0;
+                for (int e = tid; e < 2 * n; e += kPlanThreads) {
+                    const bool is_q = e >= n;
+                    const int i = is_q ? e - n : e;
+                    const double v = (is_q ? gamma : alpha) * score_at(i);
+                    if (!(v > 0.0)) continue;
+                    // how many of the other list come before this one
+                    int lo = 0, hi = n;
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        const double o = (is_q ? alpha : gamma) * score_at(mid);
+                        if (is_q ? (o >= v) : (o > v))
+                            lo = mid + 1;
                         else
-                            ++fp;
+                            hi = mid;
                     }
-                    s_rd[0] = ncand > 0 ? 1 + fp : 0;
-                    s_rd[1] = up - fp;
+                    // prefix through this upgrade: EQ count and QF count
+                    const int64_t n_eq = is_q ? lo : i + 1, n_qf = is_q ? i + 1 : lo;
+                    if (n_eq * D.c_q + n_qf * (D.c_fp - D.c_q) <= room) {
+                        if (is_q)
+                            ++fp_local;
+                        else
+                            ++up_local;
+                    }
                 }
-                __syncthreads();
-                n_fp = s_rd[0];
-                n_q = s_rd[1];
+                int up, fp;
+                block_scan(up_local, &up, s_warp);
+                block_scan(fp_local, &fp, s_warp);
+                n_fp = ncand > 0 ? 1 + fp : 0;
+                n_q = up - fp;
             } else {
                 n_fp = min(ncand, max(1, nfp_budget));
                 const int64_t rem = budget - (int64_t)n_fp * D.c_fp;
