@@ -7,6 +7,9 @@
 // budget, cumulative scoring, demotion, promotion, write-once ledger).
 #include "qevict_internal.cuh"
 
+#include <cooperative_groups.h>
+namespace cg = cooperative_groups;
+
 #include <math.h>
 
 namespace qevict {
@@ -863,19 +866,27 @@ __global__ void __launch_bounds__(1024) global_keys_kernel(GlobalArgs g) {
     }
 }
 
-// One CTA per sequence, after global_keys_kernel: the one budget and the
-// counts, then the n_fp-th and (n_fp + n_q)-th largest keys by radix
-// selection (8 passes of 8 bits over the sequence's key table). Leaves the
-// sequence's counters at zero for the next event.
-__global__ void __launch_bounds__(1024) global_select_kernel(GlobalArgs g, CacheDev C) {
-    const int seq = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    __shared__ unsigned s_h[2][256];
+// One cluster of kSelCtas CTAs per sequence, after global_keys_kernel: the
+// one budget and the counts, then the n_fp-th and (n_fp + n_q)-th largest
+// keys by radix selection (8 passes of 8 bits). Each CTA histograms its
+// eighth of the sequence's key table in its own shared memory and adds it
+// into rank 0's through distributed shared memory; rank 0 picks each pass's
+// digits. Leaves the sequence's counters at zero for the next event.
+constexpr int kSelCtas = 8;
+
+__global__ void __cluster_dims__(kSelCtas, 1, 1) __launch_bounds__(1024)
+    global_select_kernel(GlobalArgs g, CacheDev C) {
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int seq = blockIdx.x / kSelCtas, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ unsigned s_h[2][256];    // this CTA's histograms
+    __shared__ unsigned s_hc[2][256];   // rank 0: the cluster's
     __shared__ int s_go;
     __shared__ unsigned long long s_pre[2];
     __shared__ long long s_rem[2];
     const int64_t per_seq = (int64_t)g.num_layers * g.hs * g.Wmax;
     const unsigned long long *keys = g.keys + (int64_t)seq * per_seq;
-    if (tid == 0) {
+    if (rank == 0 && tid == 0) {
         int go = 1;
         int64_t F = 0;
         for (int l = 0; l < g.num_layers; ++l) {
@@ -907,22 +918,31 @@ __global__ void __launch_bounds__(1024) global_select_kernel(GlobalArgs g, Cache
         s_pre[1] = 0;
         s_go = go;
     }
-    __syncthreads();
-    if (!s_go) return;
-    // rank 0 (no full precision at all: no candidates) selects nothing
-    const bool want0 = s_rem[0] > 0, want1 = s_rem[1] > 0;
+    cl.sync();
+    int *go0 = cl.map_shared_rank(&s_go, 0);
+    long long *rem0 = cl.map_shared_rank(&s_rem[0], 0);
+    unsigned long long *pre0 = cl.map_shared_rank(&s_pre[0], 0);
+    unsigned *hc0 = cl.map_shared_rank(&s_hc[0][0], 0);
+    const bool go = *go0 != 0;
+    // rank 0 zero (no candidates) selects nothing
+    const bool want0 = rem0[0] > 0, want1 = rem0[1] > 0;
+    cl.sync();   // every CTA has read rank 0's start values
+    if (!go) return;
+    const int64_t i_lo = per_seq * rank / kSelCtas, i_hi = per_seq * (rank + 1) / kSelCtas;
     unsigned long long mask = 0;
     for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 512; i += blockDim.x) (&s_h[0][0])[i] = 0;
-        __syncthreads();
-        const unsigned long long p0 = s_pre[0], p1 = s_pre[1];
-        // 8 keys in flight per thread
-        for (int64_t i0 = tid; i0 < per_seq; i0 += 8 * (int64_t)blockDim.x) {
+        for (int i = tid; i < 512; i += blockDim.x) {
+            (&s_h[0][0])[i] = 0;
+            if (rank == 0) (&s_hc[0][0])[i] = 0;
+        }
+        const unsigned long long p0 = pre0[0], p1 = pre0[1];
+        cl.sync();   // rank 0's bins are zero before anyone adds
+        for (int64_t i0 = i_lo + tid; i0 < i_hi; i0 += 8 * (int64_t)blockDim.x) {
             unsigned long long kk[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int64_t i = i0 + (int64_t)u * blockDim.x;
-                kk[u] = i < per_seq ? __ldcg(keys + i) : 0ull;
+                kk[u] = i < i_hi ? __ldcg(keys + i) : 0ull;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -934,18 +954,23 @@ __global__ void __launch_bounds__(1024) global_select_kernel(GlobalArgs g, Cache
             }
         }
         __syncthreads();
-        if (warp < 2 && (warp == 0 ? want0 : want1)) {
+        for (int i = tid; i < 512; i += blockDim.x) {
+            const unsigned v = (&s_h[0][0])[i];
+            if (v) atomicAdd(hc0 + i, v);
+        }
+        cl.sync();   // the cluster's histograms are complete
+        if (rank == 0 && warp < 2 && (warp == 0 ? want0 : want1)) {
             long long r = s_rem[warp];
-            const int d = top_bin(s_h[warp], &r, lane);
+            const int d = top_bin(s_hc[warp], &r, lane);
             if (lane == 0) {
                 s_rem[warp] = r;
                 s_pre[warp] |= (unsigned long long)d << shift;
             }
         }
         mask |= 0xffull << shift;
-        __syncthreads();
+        cl.sync();   // the digits are in rank 0's shared memory
     }
-    if (tid == 0) {
+    if (rank == 0 && tid == 0) {
         // no rank asked: a threshold above every key
         g.thr[2 * seq] = want0 ? s_pre[0] : ~0ull;
         g.thr[2 * seq + 1] = want1 ? s_pre[1] : ~0ull;
@@ -968,7 +993,7 @@ cudaError_t launch_global_select(const GlobalArgs &g, const CacheDev &C, int seq
     global_keys_kernel<<<dim3((unsigned)((per_layer + 1023) / 1024), g.num_layers, sequences), 1024, 0, s>>>(g);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    global_select_kernel<<<sequences, 1024, 0, s>>>(g, C);
+    global_select_kernel<<<sequences * kSelCtas, 1024, 0, s>>>(g, C);
     return cudaGetLastError();
 }
 
