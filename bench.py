@@ -292,6 +292,65 @@ def measure_diagnostics(cache, wl, NL, pool, nq, nkv, stream, reps, dev):
     }
 
 
+def measure_management(cache, wl, NL, g_route, stream, dev):
+    """Routing events and the tier moves they make, on the headline workload.
+    One 32-layer routing event of the main cache after the timed steps (its
+    CUDA graph, 8 streams). Then the quantise (K4) and dequantise (K5) paths,
+    timed through routing events on a fresh 4-layer cache whose windows start
+    in full precision: a first event on seeded scores quantises every window
+    it demotes for the first time; a second event on re-drawn scores promotes
+    INT2 windows back and quantises the full-precision windows it demotes.
+    Each call (plan + quantise + promote kernels) is timed with CUDA events;
+    bytes are the window rows moved, counted from the statistics counters: a
+    first quantisation reads 512 B and writes 96 B per token and KV head, a
+    promotion reads 96 B and writes 512 B (evictions and ledger reuses move
+    no data)."""
+    import torch
+    from tiered_kv_cache_decode_gb300 import binding, synth
+    B, Hq, Hkv, w, L0, d, seed = wl["B"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"], 128, 0
+    W0 = L0 // w
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g_route.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    route_us = e0.elapsed_time(e1) * 1e3
+    st = cache.status()
+    assert st == 0, f"device status {st}: {cache.last_error()}"
+    nl = 4
+    mc = binding.TieredCache(B, nl, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"],
+                             fp_capacity=W0, ledger_capacity=W0)
+    for l in range(nl):
+        k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
+        mc.prefill(l, k, v, tiers=torch.zeros(B, W0, dtype=torch.uint8, device=dev))
+        del k, v
+    row = Hkv * w * (512 + 96)
+    out = {"route_event_us_32_layers": round(route_us, 2)}
+    for name, sd in (("route_first_quantisations", seed + 400), ("route_promotions", seed + 401)):
+        ov = [synth.zipf_scores(sd, l, B, W0, device=dev) for l in range(nl)]
+        s0 = mc.stats()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for l in range(nl):
+                mc.route(l, scores_override=ov[l], stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3
+        s1 = mc.stats()
+        nq = s1["ledger_writes"] - s0["ledger_writes"]
+        npr = s1["promotions"] - s0["promotions"]
+        nbytes = (nq + npr) * row
+        out[name] = {"quantised_per_layer": nq / nl, "promoted_per_layer": npr / nl,
+                     "us_per_layer_event": round(us / nl, 2), "bytes_per_layer_event": int(nbytes // nl),
+                     "gbs": round(nbytes / (us * 1e-6) / 1e9, 2)}
+    st = mc.status()
+    assert st == 0, f"device status {st}: {mc.last_error()}"
+    mc.close()
+    return out
+
+
 def measure_variants(wl, NL, reps, dev, peak):
     """The workload with per-KV-head tiers: every (sequence, KV head) routed on
     its own seeded scores. Times the decode kernel over all layers (CUDA graph,
@@ -584,6 +643,7 @@ def run_native(args, rank, world, local_rank):
     assert st == 0, f"device status {st}: {cache.last_error()}"
     cache.refresh_lengths()
     diagnostics = None if args.no_diag else measure_diagnostics(cache, wl, NL, pool, nq, nkv, stream, K, dev)
+    management = None if args.no_diag else measure_management(cache, wl, NL, g_route, stream, dev)
 
     ms, e2e_s, tot_bytes, tot_e2e_bytes = combine_ranks(ms, e2e_s, nbytes, e2e_bytes, world, dev)
 
@@ -622,6 +682,8 @@ def run_native(args, rank, world, local_rank):
     if diagnostics is not None:
         diagnostics["future_missed_mass"]["frac_of_peak"] = round(diagnostics["future_missed_mass"]["gbs"] / peak, 4)
         line["diagnostics"] = diagnostics
+    if management is not None:
+        line["management"] = management
     if not args.no_variants:
         del cache, pool
         torch.cuda.empty_cache()

@@ -716,29 +716,37 @@ __global__ void __launch_bounds__(128) promote_kernel(LayerDev D) {
     const int h = blockIdx.y >> 1, kv = blockIdx.y & 1;
     const int w = D.w;
     const int n = D.ctr[b * kCtrN + CTR_WP];
+    // one 16-token tile of this (KV head, K or V) at a time: its 128 code words
+    // and 64 (scale, min) pairs staged with coalesced loads
+    __shared__ uint32_t s_codes[128];
+    __shared__ __half2 s_meta[64];
+    const int tid = threadIdx.x;
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int4 job = D.work_p[(int64_t)b * D.Wmax + e];
         const uint8_t *slotp = D.lg_pool + (int64_t)job.y * D.lg_slot_bytes;
         __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)job.z * D.fp_slot_bytes);
-        for (int it = threadIdx.x; it < w * kGroups; it += blockDim.x) {
-            const int t = it / kGroups, g = it % kGroups;
-            const uint8_t *tile = slotp + lg_tile_off(h, w, t / 16);
-            const uint32_t *words = reinterpret_cast<const uint32_t *>(tile + (kv ? kTileVCodes : 0));
-            const __half2 m2 = reinterpret_cast<const __half2 *>(tile + (kv ? kTileVMeta : kTileKMeta))[(t % 16) * kGroups + g];
-            const float s = __low2float(m2), mn = __high2float(m2);
-            __align__(16) __nv_bfloat16 outv[kGroup];
+        for (int tile = 0; tile < w / 16; ++tile) {
+            const uint8_t *tp = slotp + lg_tile_off(h, w, tile);
+            __syncthreads();   // the previous tile's values are used up
+            s_codes[tid] = reinterpret_cast<const uint32_t *>(tp + (kv ? kTileVCodes : 0))[tid];
+            if (tid < 64) s_meta[tid] = reinterpret_cast<const __half2 *>(tp + (kv ? kTileVMeta : kTileKMeta))[tid];
+            __syncthreads();
+            // 16 tokens x 16 runs of 8 channels: two (token, run) items per thread
+            for (int it = tid; it < 16 * 16; it += 128) {
+                const int t = it >> 4, ch0 = (it & 15) * 8;
+                const __half2 m2 = s_meta[t * kGroups + ch0 / kGroup];
+                const float sc = __low2float(m2), mn = __high2float(m2);
+                __align__(16) __nv_bfloat16 outv[8];
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j) {
-                const int ch = g * kGroup + j;
-                uint32_t c;
-                if (kv == 0) c = (words[(t % 16) * 8 + ch / 16] >> (2 * (ch % 16))) & 3u;
-                else c = (words[vword_index(ch)] >> (2 * (t % kVTile))) & 3u;
-                outv[j] = __float2bfloat16_rn(fmaf((float)c, s, mn));
+                for (int j = 0; j < 8; ++j) {
+                    const int ch = ch0 + j;
+                    const uint32_t c = kv == 0 ? (s_codes[t * 8 + ch / 16] >> (2 * (ch % 16))) & 3u
+                                               : (s_codes[vword_index(ch)] >> (2 * (t % kVTile))) & 3u;
+                    outv[j] = __float2bfloat16_rn(fmaf((float)c, sc, mn));
+                }
+                *reinterpret_cast<uint4 *>(dst + fp_off(h, kv, w, tile * 16 + t, ch0)) =
+                    *reinterpret_cast<const uint4 *>(outv);
             }
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst + fp_off(h, kv, w, t, g * kGroup));
-            const uint4 *s4 = reinterpret_cast<const uint4 *>(outv);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) d4[c] = s4[c];
         }
     }
 }
