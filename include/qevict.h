@@ -18,8 +18,9 @@
  *    pointers) unless a parameter says "host". bf16 is IEEE bfloat16.
  *  - Every call that takes a `stream` (a cudaStream_t, NULL = legacy default
  *    stream) only enqueues work on it and returns without synchronising,
- *    except qevict_get_status / qevict_get_stats / qevict_cache_create /
- *    qevict_cache_destroy, which synchronise that stream.
+ *    except qevict_get_status / qevict_get_stats /
+ *    qevict_get_tier_move_counts / qevict_refresh_lengths /
+ *    qevict_cache_create / qevict_cache_destroy, which synchronise it.
  *  - Errors the host can see (bad arguments, a budget that cannot hold the
  *    open window, a full context) return a status at once and enqueue
  *    nothing; the cache is unchanged. Errors only the device can see (a
@@ -27,10 +28,12 @@
  *    a non-finite score or K/V value, an fp16 overflow of the INT2 scale)
  *    set a sticky device status word, skip the offending work and are
  *    reported by qevict_get_status. No kernel traps or asserts.
- *  - Calls on one cache must be issued on one stream (or be ordered by the
- *    caller); different layers may not run concurrently on different
- *    streams because the sticky status and statistics are shared. Not
- *    thread-safe.
+ *  - Calls on one layer must be ordered (one stream, or events). Routing and
+ *    tier moves of different layers may run concurrently on different
+ *    streams: the shared status word and statistics are updated atomically.
+ *    Calls that use the cache-wide decode scratch (the decode calls and
+ *    qevict_future_missed_mass) must not overlap one another, nor may two
+ *    qevict_route_global events. The host side is not thread-safe.
  *  - qevict_last_error() returns a thread-local message for the last host
  *    error of the calling thread.
  */
