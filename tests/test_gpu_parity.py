@@ -362,3 +362,31 @@ def test_stale_rows_of_open_window_never_reach_the_output(L):
         close(out.cpu().numpy(), ro, f"out step {step}")
         close(mass.cpu().numpy(), rm, f"mass step {step}")
     assert cache.status() == 0
+
+
+def test_max_windows_128k_context_every_router():
+    """The largest table a sequence can have: 131,072 tokens in 32-token
+    windows (4,096 windows, the size the plan kernel sorts and the 12 age bits
+    of the log-sparse rank), Mistral-7B-shaped heads, 10 % budget. Score,
+    log-sparse and rate-distortion routes over all of it."""
+    B, Hq, Hkv, w, L, beta = 1, 32, 8, 32, 131072, 0.1
+    W = L // w
+    cache, (ref,) = make_pair(B, Hq, Hkv, w, L, beta=beta, scores=[synth.zipf_scores(70, 0, B, W)], seed=70,
+                              fp_capacity=W, ledger_capacity=W)
+    t = ref.tiers()
+    assert t.shape[1] == 4096 and (t == O.TIER_Q).any() and (t == O.TIER_E).any()
+    check_state(cache, 0, ref)
+    check_decode(cache, 0, ref, synth.queries(70, 0, 0, B, Hq, 128))
+    sc = synth.zipf_scores(71, 0, B, W)
+    cache.route(0, scores_override=sc.cuda())
+    ref.route(scores_override=sc.numpy())
+    check_state(cache, 0, ref)
+    cache.route_logsparse(0, recent=2)
+    O.route_logsparse(ref, recent=2)
+    check_state(cache, 0, ref)
+    sc = synth.zipf_scores(72, 0, B, W)
+    cache.route_rd(0, scores_override=sc.cuda())
+    O.route_rd(ref, scores_override=sc.numpy())
+    check_state(cache, 0, ref)
+    check_decode(cache, 0, ref, synth.queries(70, 0, 1, B, Hq, 128))
+    check_stats(cache, [ref])
