@@ -1,8 +1,6 @@
 import os
 import sys
 
-import pytest
-
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -12,8 +10,3 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: takes more than a few seconds on CPU")
 
-
-def pytest_collection_modifyitems(config, items):
-    # A GPU test on a machine without a GPU fails loudly instead of skipping, unless
-    # the run deselected GPU tests (-m "not gpu").
-    pass

@@ -4,8 +4,6 @@ time and the sum of the bytes."""
 import os
 import socket
 
-import pytest
-import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 

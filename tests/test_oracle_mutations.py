@@ -7,8 +7,6 @@ denominator must make at least one of them fail.
 import math
 
 import numpy as np
-import pytest
-
 import oracle as O
 from oracle import qevict_oracle as QO
 import test_oracle_pins as P
