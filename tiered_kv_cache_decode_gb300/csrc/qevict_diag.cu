@@ -105,14 +105,15 @@ __device__ __forceinline__ void fmm_add2(FmmStat &st, float x0, float x1, bool o
 // stages in shared memory. A stage holds the chunk's keys as two TMA boxes of
 // 16 tokens x 64 channels (channels 0-63, then 64-127), 128-byte rows with
 // the 128-byte swizzle, so that ldmatrix reads them without bank conflicts.
-constexpr int kFmmStages = 6;
+constexpr int kFmmStages = 3;
 constexpr int kFmmThreads = kFmmWarps * 32;
 constexpr int kFmmStage = 4096;
 constexpr int kFmmRing = kFmmWarps * kFmmStages * kFmmStage;
 constexpr int kFmmSmem = kFmmRing + kFmmWarps * kFmmStages * 8 + 1024;   // + barriers, + alignment
 
-// One CTA per (split of the token range, sequence and KV head), one CTA per
-// SM; splits start on 16-token boundaries, so a chunk of 16 tokens lies
+// One CTA per (split of the token range, sequence and KV head), two CTAs per
+// SM (one's first chunks and merge overlap the other's streaming); splits
+// start on 16-token boundaries, so a chunk of 16 tokens lies
 // inside one window (a window is a multiple of 16 tokens) and takes one tier
 // byte. A warp takes every 8th chunk: lane 0 issues the chunk's two TMA
 // copies kFmmStages - 1 chunks ahead, and the warp computes the logits on the
@@ -126,7 +127,7 @@ constexpr int kFmmSmem = kFmmRing + kFmmWarps * kFmmStages * 8 + 1024;   // + ba
 // KV head) to arrive on `cnt` (zero between launches, reset by that CTA)
 // merges all splits and writes the missed mass of the group's heads.
 template <int G>
-__global__ void __launch_bounds__(kFmmThreads, 1) fmm_kernel(const LayerDev D, const CacheDev C,
+__global__ void __launch_bounds__(kFmmThreads, 2) fmm_kernel(const LayerDev D, const CacheDev C,
                                                              const __grid_constant__ CUtensorMap kmap, int layer,
                                                              const __nv_bfloat16 *q, int L, float *part,
                                                              int splits, uint32_t *cnt, float *fmm) {
@@ -275,7 +276,7 @@ cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, cons
     // The split arrival counters of the decode scratch (zero between launches)
     // count this launch's arrivals too; every launch leaves them at zero.
     uint32_t *cnt = S.bar;   // [B*Hkv][2]; the kernel counts on entry 2 * bk
-    // one CTA per SM, spread over the (sequence, KV head) pairs
+    // two CTAs per SM, spread over the (sequence, KV head) pairs
     auto grid_for = [&](const void *fn) {
         static bool attr[kMaxG + 1] = {};
         if (!attr[L.G]) {
@@ -283,7 +284,7 @@ cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, cons
             if (e != cudaSuccess) return -1;
             attr[L.G] = true;
         }
-        const int splits = (num_sms + pairs - 1) / pairs;
+        const int splits = (2 * num_sms + pairs - 1) / pairs;
         return max(1, min(splits, min(256, 2 * L.Wmax / 3)));
     };
     switch (L.G) {
