@@ -100,7 +100,7 @@ def sample_clocks():
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     try:
-        return subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "200"],
+        return subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100"],
                                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
     except OSError:
         return None
@@ -600,7 +600,15 @@ def run_native(args, rank, world, local_rank):
             one_step(s)
         barrier()
         clk = sample_clocks()
-        time.sleep(0.3)
+        # The timed steps last tens of ms, less than one sampling period, so the
+        # GPU is kept at the same work while the sampler starts: the decode-only
+        # graph (no appends, the context stays put) for about 0.6 s, then the
+        # timed steps. Every sample falls under the decode kernel's load.
+        t_soak = time.perf_counter() + 0.6
+        while time.perf_counter() < t_soak:
+            for _ in range(8):
+                g_decode.replay()
+            stream.synchronize()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         ev0.record(stream)
