@@ -45,8 +45,11 @@ import math
 import numpy as np
 
 TIER_FP, TIER_Q, TIER_E = 0, 1, 2
+TIER_Q4, TIER_Q8 = 3, 4   # the 4- and 8-bit widths of the rate-distortion option (RDKV 2.2)
 GROUP = 32          # channels per INT2 quantisation group
 LEVELS = 3          # 2-bit codes 0..3 -> (max - min) / 3 per step
+BITS_OF_TIER = {TIER_Q: 2, TIER_Q4: 4, TIER_Q8: 8}
+TIER_OF_BITS = {0: TIER_E, 2: TIER_Q, 4: TIER_Q4, 8: TIER_Q8, 16: TIER_FP}
 
 
 class OracleError(Exception):
@@ -96,8 +99,9 @@ def half_round(x) -> np.ndarray:
 # INT2 quantiser (demotion) and dequantisers
 # --------------------------------------------------------------------------
 
-def quantize_groups(x):
-    """Asymmetric 2-bit quantisation of groups of 32 bf16 values.
+def quantize_groups(x, bits: int = 2):
+    """Asymmetric 2-bit (or, for the mixed-width option, 4- or 8-bit)
+    quantisation of groups of 32 bf16 values.
 
     Reading of QEvict "Recoverable Quantized Tier" (INT2): per token, per KV
     head, per group of 32 consecutive channels of head_dim, for K and V alike:
@@ -108,6 +112,9 @@ def quantize_groups(x):
       code_j  = clamp(rint_even(fl32(fl32(x_j - min16) / scale16)), 0, 3)
                 (all codes 0 when scale16 == 0)
 
+    With ``bits`` b the 3 above is 2^b - 1 (RDKV 2.2: widths 2, 4, 8 of one
+    scheme; the pages give no other rule).
+
     x: float32 array [..., 32] holding bf16 values.
     Returns (codes uint8 [..., 32], scale float16 [...], minimum float16 [...],
     bad bool [...]) where ``bad`` flags a group with a non-finite input or a
@@ -115,7 +122,8 @@ def quantize_groups(x):
     error and leaves the group's codes at 0).
     """
     x = np.asarray(x, dtype=np.float32)
-    assert x.shape[-1] == GROUP
+    assert x.shape[-1] == GROUP and bits in (2, 4, 8)
+    levels = (1 << bits) - 1
     finite = np.isfinite(x).all(axis=-1)
     xs = np.where(np.isfinite(x), x, np.float32(0))
     mn = xs.min(axis=-1)
@@ -123,7 +131,7 @@ def quantize_groups(x):
     mn16 = half_round(mn)
     with np.errstate(over="ignore", invalid="ignore"):
         rng = (mx - mn).astype(np.float32)
-        s32 = (rng / np.float32(LEVELS)).astype(np.float32)
+        s32 = (rng / np.float32(levels)).astype(np.float32)
     s16 = half_round(s32)
     bad = ~finite | ~np.isfinite(mn16) | ~np.isfinite(s16)
     s32q = s16.astype(np.float32)
@@ -133,7 +141,7 @@ def quantize_groups(x):
     with np.errstate(over="ignore", invalid="ignore"):
         diff = (xs - m32q[..., None]).astype(np.float32)
         qt = (diff / den[..., None]).astype(np.float32)
-    codes = np.clip(np.rint(qt), 0, LEVELS)
+    codes = np.clip(np.rint(qt), 0, levels)
     codes = np.where(zero[..., None], 0, codes).astype(np.uint8)
     s16 = np.where(bad, np.float16(0), s16)
     mn16 = np.where(bad, np.float16(0), mn16)
@@ -155,8 +163,9 @@ def dequant_exact(codes, scale16, min16):
 def dequant_promote(codes, scale16, min16):
     """Promotion back to the full-precision tier: bf16_rne(fl32(code * scale + min)).
 
-    code * scale + min is exact in float64 for fp16 scale / min and codes 0..3,
-    so the float32 cast below is the single rounding of a fused multiply-add.
+    code * scale + min is exact in float64 for fp16 scale / min and codes up to
+    255 (an 8-bit code times an 11-bit significand, plus an fp16 value), so the
+    float32 cast below is the single rounding of a fused multiply-add.
     """
     exact = dequant_exact(codes, scale16, min16)
     return bf16_round(exact.astype(np.float32))
@@ -247,13 +256,14 @@ def softmax_attention(q, keys, values):
 # --------------------------------------------------------------------------
 
 class Window:
-    __slots__ = ("tier", "k", "v", "ledger", "ledger_writes", "ntok")
+    __slots__ = ("tier", "k", "v", "ledger", "ledger_bits", "ledger_writes", "ntok")
 
     def __init__(self, Hkv, w, d):
         self.tier = TIER_FP
         self.k = np.zeros((Hkv, w, d), np.float32)   # bf16 values
         self.v = np.zeros((Hkv, w, d), np.float32)
         self.ledger = None        # (codes_k, scale_k, min_k, codes_v, scale_v, min_v)
+        self.ledger_bits = 0      # width of the ledger entry: 2, 4 or 8
         self.ledger_writes = 0
         self.ntok = 0
 
@@ -316,31 +326,40 @@ class OracleCache:
         win.ledger = None
         self.stats["evictions"] += 1
 
-    def _demote(self, b, wi):
-        """FP -> INT2. Quantise only if the window has no ledger entry yet."""
+    def _demote(self, b, wi, tier=TIER_Q):
+        """FP -> INT2 (or INT4 / INT8). Quantise only if the window has no
+        ledger entry yet. The write-once ledger fixes a window's width at its
+        first quantisation: a later demotion reuses the entry and must ask for
+        the same width (re-quantising promoted values at another width would
+        compound rounding, which the ledger exists to prevent)."""
         win = self.win[b][wi]
         if win.tier != TIER_FP or win.ntok != self.w:
             raise StateError("demotion needs a full full-precision window")
+        bits = BITS_OF_TIER[tier]
         if win.ledger is None:
-            ck, sk, mk, bk = quantize_groups(win.k.reshape(self.Hkv, self.w, -1, GROUP))
-            cv, sv, mv, bv = quantize_groups(win.v.reshape(self.Hkv, self.w, -1, GROUP))
+            ck, sk, mk, bk = quantize_groups(win.k.reshape(self.Hkv, self.w, -1, GROUP), bits)
+            cv, sv, mv, bv = quantize_groups(win.v.reshape(self.Hkv, self.w, -1, GROUP), bits)
             if bk.any() or bv.any():
                 raise QuantError("non-finite value or fp16 overflow in a quantisation group")
             win.ledger = (ck.reshape(self.Hkv, self.w, self.d), sk, mk,
                           cv.reshape(self.Hkv, self.w, self.d), sv, mv)
+            win.ledger_bits = bits
             win.ledger_writes += 1
             self.stats["ledger_writes"] += 1
+        elif win.ledger_bits != bits:
+            raise StateError("a window's quantised width is fixed by its first quantisation")
         else:
             self.stats["ledger_reuses"] += 1
-        win.tier = TIER_Q
+        win.tier = tier
         win.k = win.v = None
         self.stats["demotions"] += 1
 
     def _promote(self, b, wi):
-        """INT2 -> FP: dequantise the ledger codes to bf16; the ledger is kept."""
+        """INT2 (INT4, INT8) -> FP: dequantise the ledger codes to bf16; the
+        ledger is kept."""
         win = self.win[b][wi]
-        if win.tier != TIER_Q:
-            raise StateError("promotion needs an INT2 window")
+        if win.tier not in BITS_OF_TIER:
+            raise StateError("promotion needs a quantised window")
         ck, sk, mk, cv, sv, mv = win.ledger
         g = lambda c: c.reshape(self.Hkv, self.w, -1, GROUP)
         win.k = dequant_promote(g(ck), sk, mk).reshape(self.Hkv, self.w, self.d)
@@ -354,16 +373,18 @@ class OracleCache:
         for wi, (c, t) in enumerate(zip(cur, new)):
             if c == TIER_E and t != TIER_E:
                 raise StateError("an evicted window cannot come back")
+            if c in BITS_OF_TIER and t in BITS_OF_TIER and c != t:
+                raise StateError("a quantised window keeps its width")
             if c != t and wi == self.W - 1 and self.win[b][wi].ntok < self.w:
                 raise StateError("the partially filled last window stays full precision")
         for wi, (c, t) in enumerate(zip(cur, new)):
             if c != TIER_E and t == TIER_E:
                 self._evict(b, wi)
         for wi, (c, t) in enumerate(zip(cur, new)):
-            if c == TIER_FP and t == TIER_Q:
-                self._demote(b, wi)
+            if c == TIER_FP and t in BITS_OF_TIER:
+                self._demote(b, wi, t)
         for wi, (c, t) in enumerate(zip(cur, new)):
-            if c == TIER_Q and t == TIER_FP:
+            if c in BITS_OF_TIER and t == TIER_FP:
                 self._promote(b, wi)
 
     def tiers_now(self, b):
@@ -403,10 +424,10 @@ class OracleCache:
         elif tiers is not None:
             self.set_tiers(tiers)
 
-    def demote(self, pairs):
+    def demote(self, pairs, tier=TIER_Q):
         old = [self.tiers_now(b) for b in range(self.B)]
         for b, wi in pairs:
-            self._demote(b, wi)
+            self._demote(b, wi, tier)
         self.last_counts = np.stack([transition_counts(old[b], self.tiers_now(b)) for b in range(self.B)])
 
     def promote(self, pairs):
@@ -481,12 +502,13 @@ def transition_counts(old, new):
     q_before."""
     old = np.asarray(old)
     new = np.asarray(new)
+    quant = lambda t: np.isin(t, list(BITS_OF_TIER))   # the recoverable tier, at any width
     return np.array([
-        int((old == TIER_FP).sum()), int((old == TIER_Q).sum()),
-        int((new == TIER_FP).sum()), int((new == TIER_Q).sum()),
+        int((old == TIER_FP).sum()), int(quant(old).sum()),
+        int((new == TIER_FP).sum()), int(quant(new).sum()),
         int(((old == TIER_FP) & (new == TIER_FP)).sum()),
-        int(((old == TIER_Q) & (new == TIER_FP)).sum()),
-        int(((old == TIER_FP) & (new == TIER_Q)).sum()),
+        int((quant(old) & (new == TIER_FP)).sum()),
+        int(((old == TIER_FP) & quant(new)).sum()),
         int(((old != TIER_E) & (new == TIER_E)).sum()),
     ], dtype=np.int64)
 
@@ -615,6 +637,83 @@ def route_rd(cache, scores_override=None):
     cache.last_counts = np.stack(counts)
 
 
+# ---- rate-distortion routing over all widths {0, 2, 4, 8, 16} (an option) ----
+#
+# The same allocation with RDKV's full width set. A window's options form a
+# chain of widths: 0 -> 2 -> 4 -> 8 -> 16 for a window never quantised, and
+# 0 -> b -> 16 for one whose ledger entry has width b (the write-once ledger
+# fixes the width at the first quantisation). Each step of a chain is an
+# upgrade removing (2^-a - 2^-b) w of distortion for cost(b) - cost(a) bytes;
+# its gain per byte is k_step * w with k_step = (2^-a - 2^-b) / (cost(b) -
+# cost(a)) (one float64 product per upgrade). Along every chain k_step falls,
+# so taking the upgrades of all windows in order of gain per byte, highest
+# first (a lower step first on a tie, then the window rank), while positive,
+# until the first that does not fit, takes each chain's steps in order: the
+# Lagrangian solution of the multiple-choice knapsack.
+
+def width_cost(w: int, Hkv: int, d: int, bits: int) -> int:
+    """Bytes of one window at a width: 0 evicted, 16 bf16, else codes + fp16 meta."""
+    if bits == 0:
+        return 0
+    if bits == 16:
+        return w * Hkv * d * 4
+    return w * Hkv * 2 * (d * bits // 8 + 4 * (d // GROUP))
+
+
+def rd_mixed_widths(S_ranked, chains, L: int, w: int, Hkv: int, d: int, beta: float):
+    """Widths of the candidates other than the open window, given in rank
+    order with their chains (lists of widths starting at 0)."""
+    c_fp = width_cost(w, Hkv, d, 16)
+    Bt = budget_bytes(L, Hkv, d, beta)
+    if Bt < c_fp:
+        raise BudgetError(f"budget {Bt} B cannot hold the open window ({c_fp} B)")
+    ups = []
+    for r, (s, ch) in enumerate(zip(S_ranked, chains)):
+        for i in range(len(ch) - 1):
+            a, b = ch[i], ch[i + 1]
+            cost = width_cost(w, Hkv, d, b) - width_cost(w, Hkv, d, a)
+            k = (2.0 ** -a - 2.0 ** -b) / cost
+            ups.append((k * float(s), i, r, cost))
+    ups.sort(key=lambda u: (-u[0], u[1], u[2]))
+    used, steps = c_fp, [0] * len(chains)
+    for gain, i, r, cost in ups:
+        if gain <= 0.0 or used + cost > Bt:
+            break
+        assert steps[r] == i, "a chain's steps come in order"
+        used += cost
+        steps[r] += 1
+    return [ch[st] for ch, st in zip(chains, steps)]
+
+
+def route_rd_mixed(cache, scores_override=None):
+    """A routing event by the rate-distortion allocation over widths
+    {0, 2, 4, 8, 16}; windows keep the width of an existing ledger entry."""
+    if scores_override is not None:
+        ov = np.asarray(scores_override, np.float64)
+        cache.S = [ov[b, :cache.W].copy() for b in range(cache.B)]
+    counts = []
+    W = cache.W
+    for b in range(cache.B):
+        old = cache.tiers_now(b)
+        S = cache.S[b]
+        cand = [i for i in range(W) if old[i] != TIER_E]
+        if not all(math.isfinite(float(S[i])) for i in cand):
+            raise OracleError("non-finite score among routing candidates")
+        forced = W - 1
+        order = sorted(cand, key=lambda i: (i != forced, -float(S[i]), i))
+        rest = order[1:]
+        chains = [[0, 2, 4, 8, 16] if cache.win[b][i].ledger is None else [0, cache.win[b][i].ledger_bits, 16]
+                  for i in rest]
+        widths = rd_mixed_widths([S[i] for i in rest], chains, cache.L, cache.w, cache.Hkv, cache.d, cache.beta)
+        new = np.array(old, np.uint8)
+        new[forced] = TIER_FP
+        for i, bits in zip(rest, widths):
+            new[i] = TIER_OF_BITS[bits]
+        cache.apply_tiers(b, new)
+        counts.append(transition_counts(old, cache.tiers_now(b)))
+    cache.last_counts = np.stack(counts)
+
+
 # ---- a positional router (an option) ----------------------------------------
 #
 # "Technische Samenvatting: LogQuant", Methodologie 1-2: high-attention
@@ -728,7 +827,8 @@ def route_global(layers, hs=1, scores_override=None):
 
 
 def tiered_bytes(cache: OracleCache) -> int:
-    """Attention-visible bytes resident for all sequences (FP c_fp, INT2 c_q, E 0)."""
-    c_fp, c_q = window_costs(cache.w, cache.Hkv, cache.d)
+    """Attention-visible bytes resident for all sequences (FP c_fp, INT2 / INT4 /
+    INT8 their codes and meta, E 0)."""
     t = cache.tiers()
-    return int((t == TIER_FP).sum() * c_fp + (t == TIER_Q).sum() * c_q)
+    return int(sum((t == tier).sum() * width_cost(cache.w, cache.Hkv, cache.d, bits)
+                   for bits, tier in TIER_OF_BITS.items()))

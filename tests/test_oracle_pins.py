@@ -744,7 +744,7 @@ def _golden_rd():
     rows = []
     for line in open(os.path.join(GOLDEN, "rd_counts.txt")):
         line = line.strip()
-        if not line or line.startswith("#"):
+        if not line or line.startswith("#") or line.startswith("MIXED"):
             continue
         a, b, c = line.split("|")
         Hkv, w, L, beta = a.split()
@@ -805,3 +805,145 @@ def test_route_rd_assigns_by_rank():
         n_fp, n_q = O.rd_counts([S[b, i] for i in order[1:]], L, w, Hkv, 128, beta)
         t = c.tiers()[b]
         assert [t[i] for i in order] == [O.TIER_FP] * n_fp + [O.TIER_Q] * n_q + [O.TIER_E] * (W - n_fp - n_q)
+
+
+# ---------------------------------------------------------------- 4- and 8-bit widths
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_wide_quantiser_exact_grid_and_nearest_level(bits):
+    levels = (1 << bits) - 1
+    rng = np.random.default_rng(14 + bits)
+    # exact grid: min and scale exact in fp16, every value exact in bf16, the
+    # lowest and highest level present; such a group quantises with no error
+    done = 0
+    for _ in range(4000):
+        m = float(rng.integers(-64, 64)) * 2.0 ** -int(rng.integers(2, 6))
+        sc = float(2.0 ** -int(rng.integers(1, 9)))
+        k = rng.integers(0, levels + 1, size=32)
+        k[0], k[1] = 0, levels
+        x = (m + k * sc).astype(np.float32)
+        if not np.array_equal(O.bf16_round(x), x) or float(np.float16(m)) != m:
+            continue
+        c, s16, m16, bad = O.quantize_groups(x[None, :], bits)
+        assert not bad.any() and float(s16[0]) == sc and float(m16[0]) == m
+        assert np.array_equal(c[0], k.astype(np.uint8))
+        done += 1
+    assert done >= 100
+    # random bf16 groups: every code is a nearest level of the fp16 grid (up to the
+    # quotient's float32 rounding at a tie), codes within [0, levels]
+    x = O.bf16_round(rng.standard_normal((400, 32)).astype(np.float32) * 3)
+    c, s16, m16, bad = O.quantize_groups(x, bits)
+    assert not bad.any() and c.max() <= levels
+    grid = m16.astype(np.float64)[:, None, None] + np.arange(levels + 1)[None, None, :] * s16.astype(np.float64)[:, None, None]
+    err = np.abs(x.astype(np.float64)[:, :, None] - grid)
+    best = err.min(axis=2)
+    mine = np.take_along_axis(err, c[:, :, None].astype(np.int64), axis=2)[:, :, 0]
+    assert np.all(mine <= best + np.abs(x).max() * 2.0 ** -22)
+    # a constant group: scale 0, codes 0
+    c, s16, _, _ = O.quantize_groups(np.full((1, 32), 0.75, np.float32), bits)
+    assert float(s16[0]) == 0.0 and not c.any()
+
+
+def test_wide_windows_attend_exactly_on_grid_values():
+    """Keys and values on each group's 4- or 8-bit grid survive quantisation
+    exactly, so attention over INT4 / INT8 windows is dense attention."""
+    rng = np.random.default_rng(16)
+    B, Hq, Hkv, w, L = 1, 4, 2, 16, 64
+    W = L // w
+
+    def grid_tokens(bits):
+        levels = (1 << bits) - 1
+        k = rng.integers(0, levels + 1, size=(B, L, Hkv, 128)).astype(np.float64)
+        k[..., 0::32] = 0
+        k[..., 1::32] = levels
+        return (-1.0 + k * 2.0 ** -5).astype(np.float32)
+
+    for tier in (O.TIER_Q4, O.TIER_Q8):
+        bits = O.BITS_OF_TIER[tier]
+        k, v = grid_tokens(bits), grid_tokens(bits)
+        assert np.array_equal(O.bf16_round(k), k)
+        c = O.OracleCache(B, Hq, Hkv, 128, w)
+        c.prefill(k, v, tiers=np.array([[tier, tier, tier, O.TIER_FP]], np.uint8))
+        q = O.bf16_round(rng.standard_normal((B, Hq, 128)).astype(np.float32))
+        out, _ = c.decode(q, accumulate=False)
+        for h in range(Hq):
+            s_ = k[0, :, h // 2].astype(np.float64) @ q[0, h].astype(np.float64) / np.sqrt(128)
+            p = np.exp(s_ - s_.max())
+            p /= p.sum()
+            assert np.allclose(out[0, h], p @ v[0, :, h // 2].astype(np.float64), rtol=0, atol=1e-12)
+
+
+def test_ledger_width_is_fixed_by_the_first_quantisation():
+    rng = np.random.default_rng(17)
+    B, Hq, Hkv, w, L = 1, 4, 2, 16, 64
+    k = O.bf16_round(rng.standard_normal((B, L, Hkv, 128)).astype(np.float32))
+    c = O.OracleCache(B, Hq, Hkv, 128, w)
+    c.prefill(k, k, tiers=np.zeros((B, L // w), np.uint8))
+    c.demote([(0, 1)], O.TIER_Q4)
+    codes = c.win[0][1].ledger[0].copy()
+    c.promote([(0, 1)])
+    c.demote([(0, 1)], O.TIER_Q4)            # the same width: the entry is reused
+    assert c.win[0][1].ledger_writes == 1 and np.array_equal(c.win[0][1].ledger[0], codes)
+    c.promote([(0, 1)])
+    with pytest.raises(O.StateError):
+        c.demote([(0, 1)], O.TIER_Q)         # another width would re-quantise promoted values
+    c2 = O.OracleCache(B, Hq, Hkv, 128, w)
+    c2.prefill(k, k, tiers=np.array([[O.TIER_Q4, 0, 0, 0]], np.uint8))
+    with pytest.raises(O.StateError):
+        c2.set_tiers(np.array([[O.TIER_Q8, 0, 0, 0]], np.uint8))   # INT4 straight to INT8
+
+
+def test_rd_mixed_two_width_chains_are_the_two_width_allocation():
+    rng = np.random.default_rng(18)
+    Hkv, w, d = 2, 16, 128
+    for trial in range(30):
+        L = int(rng.integers(200, 1200))
+        beta = float(rng.uniform(max(0.03, 1.2 * w / L), 0.6))
+        W = -(-L // w)
+        S = sorted((rng.pareto(1.2, W - 1) * rng.uniform(0.1, 10)).tolist(), reverse=True)
+        n_fp, n_q = O.rd_counts(S, L, w, Hkv, d, beta)
+        widths = O.rd_mixed_widths(S, [[0, 2, 16]] * (W - 1), L, w, Hkv, d, beta)
+        assert widths == [16] * (n_fp - 1) + [2] * n_q + [0] * (W - n_fp - n_q), trial
+
+
+def test_rd_mixed_is_a_lagrangian_solution():
+    rng = np.random.default_rng(19)
+    Hkv, w, d = 2, 16, 128
+    for trial in range(40):
+        L = int(rng.integers(200, 1200))
+        beta = float(rng.uniform(max(0.03, 1.2 * w / L), 0.6))
+        W = -(-L // w)
+        S = sorted((rng.pareto(1.2, W - 1) * rng.uniform(0.1, 10)).tolist(), reverse=True)
+        chains = [[0, 2, 4, 8, 16] if rng.random() < 0.6 else [0, int(rng.choice([2, 4, 8])), 16]
+                  for _ in range(W - 1)]
+        widths = O.rd_mixed_widths(S, chains, L, w, Hkv, d, beta)
+        cost = lambda b: O.width_cost(w, Hkv, d, b)
+        assert cost(16) + sum(cost(b) for b in widths) <= O.budget_bytes(L, Hkv, d, beta)
+        refused = []
+        for s_, ch, b in zip(S, chains, widths):
+            i = ch.index(b)
+            if i + 1 < len(ch):
+                a, nb = ch[i], ch[i + 1]
+                refused.append((2.0 ** -a - 2.0 ** -nb) / (cost(nb) - cost(a)) * s_)
+        lam = max(refused) if refused else 0.0
+        for s_, ch, b in zip(S, chains, widths):
+            obj = {x: s_ * 2.0 ** -x + lam * cost(x) for x in ch}
+            assert obj[b] <= min(obj.values()) * (1 + 1e-12) + 1e-300, (trial, s_, ch, b, lam)
+
+
+def test_rd_mixed_hand_derived():
+    for line in open(os.path.join(GOLDEN, "rd_counts.txt")):
+        if not line.startswith("MIXED"):
+            continue
+        a, b, c = line[len("MIXED"):].split("|")
+        Hkv, w, L, beta = a.split()
+        Hkv, w, L, beta = int(Hkv), int(w), int(L), float(beta)
+        S = []
+        for part in b.split():
+            n, v = part.split("x")
+            S += [float(v)] * int(n)
+        n16, n8, n4, n2, n0, res = map(int, c.split())
+        widths = O.rd_mixed_widths(S, [[0, 2, 4, 8, 16]] * len(S), L, w, Hkv, 128, beta)
+        got = [1 + widths.count(16), widths.count(8), widths.count(4), widths.count(2), widths.count(0)]
+        assert got == [n16, n8, n4, n2, n0]
+        assert sum(O.width_cost(w, Hkv, 128, x) for x in widths) + O.width_cost(w, Hkv, 128, 16) == res
