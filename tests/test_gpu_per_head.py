@@ -151,3 +151,30 @@ def test_per_head_demote_promote_set_tiers_and_diagnostics():
     want = O.future_missed_mass(ref, O.queries_to_units(q.float().numpy(), Hkv), O.to_units(k.float().numpy()))
     close(got.cpu().numpy(), want.reshape(B, Hq), "future missed mass per head")
     assert cache.status() == 0, cache.last_error()
+
+
+def test_per_head_full_size_batched_llama_b8_32k_5pct():
+    """Batch 8 of the Llama-8B shape at 5 %, per-head tiers: 64 units of 512 windows."""
+    B, Hq, Hkv, w, L, beta = 8, 32, 8, 64, 32768, 0.05
+    W = L // w
+    scores = synth.zipf_scores(34, 0, B * Hkv, W)
+    cache, ref, _ = make_ph(B, Hq, Hkv, w, L, beta=beta, seed=34, scores=scores)
+    t = ref.tiers()
+    assert all(((r == 0).sum(), (r == 1).sum(), (r == 2).sum()) == (12, 72, 428) for r in t)
+    check_state(cache, 0, ref)
+    for step in range(2):
+        check_decode_ph(cache, ref, synth.queries(34, 0, step, B, Hq, 128))
+
+
+def test_per_head_rate_distortion_route():
+    B, Hq, Hkv, w, L, beta = 2, 16, 4, 32, 2048, 0.15
+    W = L // w
+    cache, ref, _ = make_ph(B, Hq, Hkv, w, L, beta=beta, seed=35, tiers=torch.zeros(B * Hkv, W, dtype=torch.uint8),
+                            fp_capacity=W, ledger_capacity=W)
+    scores = synth.zipf_scores(35, 0, B * Hkv, W)
+    cache.route_rd(0, scores_override=scores.cuda())
+    O.route_rd(ref, scores_override=scores.numpy())
+    assert cache.status() == 0, cache.last_error()
+    check_state(cache, 0, ref)
+    assert np.array_equal(cache.tier_move_counts(0).numpy(), ref.last_counts.astype(np.int32))
+    check_decode_ph(cache, ref, synth.queries(35, 0, 0, B, Hq, 128))
