@@ -59,8 +59,10 @@ typedef enum qevict_status {
     QEVICT_ERR_CAPACITY = 8       /* a device slot pool ran out */
 } qevict_status;
 
-/* Window tiers (QEvict "Methodologie: QEvict", items 1-3). */
-enum { QEVICT_TIER_FP = 0, QEVICT_TIER_Q = 1, QEVICT_TIER_E = 2 };
+/* Window tiers (QEvict "Methodologie: QEvict", items 1-3). INT4 and INT8 are
+ * the wider widths of the rate-distortion option ("Technische Samenvatting:
+ * RDKV", 2.2); a cache allows them only with max_ledger_bits 4 or 8. */
+enum { QEVICT_TIER_FP = 0, QEVICT_TIER_Q = 1, QEVICT_TIER_E = 2, QEVICT_TIER_Q4 = 3, QEVICT_TIER_Q8 = 4 };
 
 /* Optional device-memory allocator. alloc(bytes, stream, ctx) returns a
  * device pointer (aligned to >= 256 B) or NULL; free(ptr, stream, ctx)
@@ -103,6 +105,14 @@ typedef struct qevict_allocator {
  *                window) pairs name (unit, window), tier-move counts are
  *                [batch * Hkv][8], and qevict_get_view shows batch * Hkv
  *                units of 1 KV head and G query heads.
+ *  max_ledger_bits
+ *                0 or 2: windows are quantised to INT2 only. 4 or 8: the INT4
+ *                (and INT8) tiers are allowed too ("Technische Samenvatting:
+ *                RDKV", 2.2, widths {0, 2, 4, 8, 16}); ledger slots are then
+ *                sized for that width. Such a cache moves windows by explicit
+ *                tiers (prefill, qevict_set_tiers), listed moves and
+ *                qevict_route_rd_mixed; the score, log-sparse, rate-distortion
+ *                and global routes, which count INT2 bytes, reject it.
  */
 typedef struct qevict_config {
     int32_t batch;
@@ -118,6 +128,7 @@ typedef struct qevict_config {
     double budget_frac;
     double fp_share;
     int32_t tier_per_kv_head;
+    int32_t max_ledger_bits;
 } qevict_config;
 
 typedef struct qevict_cache qevict_cache;
@@ -139,6 +150,10 @@ typedef struct qevict_cache qevict_cache;
  *                 (g, mt in 0..7, h in 0..1) holds channel 16 * mt + g + 8 h,
  *                 token t of the tile at bits 2 * t;
  *        V meta at 1280: [16 tokens][4 groups] half2.
+ *        An INT4 (INT8) window keeps P = 2 (4) two-bit planes, code =
+ *        sum_p 4^p c_p, each plane in the INT2 code layout; its tiles are
+ *        1024 P + 512 bytes: K planes at 512 p, K meta at 512 P, V planes at
+ *        512 P + 256 + 512 p, V meta at 1024 P + 256.
  *  length                          current context length (host copy). */
 typedef struct qevict_view {
     int32_t batch, num_q_heads, num_kv_heads, head_dim, window;
@@ -152,6 +167,8 @@ typedef struct qevict_view {
     const int32_t *ledger_writes;
     const uint8_t *fp_pool;
     const uint8_t *ledger_pool;
+    const uint8_t *ledger_bits;   /* [b * max_windows + w] width of the ledger entry: 0, 2, 4 or 8 */
+    int32_t max_ledger_bits;
 } qevict_view;
 
 typedef struct qevict_stats {

@@ -49,6 +49,7 @@ def check_state(cache, layer, ref):
     tier, fps, lgs, lw = cache.tables(layer)
     rt = ref.tiers()
     assert np.array_equal(tier.numpy(), rt), "tiers differ"
+    lbits = cache.ledger_bits(layer).numpy()
     for b in range(ref.B):
         for wi, win in enumerate(ref.win[b]):
             assert int(lw[b, wi]) == win.ledger_writes, ("ledger writes", b, wi)
@@ -62,7 +63,8 @@ def check_state(cache, layer, ref):
                 assert np.array_equal(data[:, 0, :n], win.k[:, :n]), ("FP K", b, wi)
                 assert np.array_equal(data[:, 1, :n], win.v[:, :n]), ("FP V", b, wi)
             if win.ledger is not None:
-                codes, scale, mn = cache.ledger_window(layer, int(lgs[b, wi]))
+                assert int(lbits[b, wi]) == win.ledger_bits, ("ledger width", b, wi)
+                codes, scale, mn = cache.ledger_window(layer, int(lgs[b, wi]), win.ledger_bits)
                 ck, sk, mk, cv, sv, mv = win.ledger
                 assert np.array_equal(codes[:, 0].numpy(), ck), ("K codes", b, wi)
                 assert np.array_equal(codes[:, 1].numpy(), cv), ("V codes", b, wi)

@@ -35,11 +35,12 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match_header_sizes():
-    # int32 x 10 + double x 2 + int32 + 4 bytes of tail padding = 64 bytes
+    # int32 x 10 + double x 2 + int32 x 2 = 64 bytes
     assert ctypes.sizeof(binding.Config) == 64
-    assert binding.Config.tier_per_kv_head.offset == 56
+    assert binding.Config.tier_per_kv_head.offset == 56 and binding.Config.max_ledger_bits.offset == 60
     assert ctypes.sizeof(binding.Stats) == 48
-    assert ctypes.sizeof(binding.View) == 9 * 4 + 4 + 3 * 8 + 6 * 8
+    # 9 int32, padding, 3 int64, 7 pointers, int32 and tail padding
+    assert ctypes.sizeof(binding.View) == 9 * 4 + 4 + 3 * 8 + 7 * 8 + 8
 
 
 def _cfg(**kw):

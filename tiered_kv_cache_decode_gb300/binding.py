@@ -47,7 +47,7 @@ class Config(ctypes.Structure):
                 ("max_context", ctypes.c_int32), ("fp_capacity", ctypes.c_int32),
                 ("ledger_capacity", ctypes.c_int32), ("fp_slack", ctypes.c_int32),
                 ("budget_frac", ctypes.c_double), ("fp_share", ctypes.c_double),
-                ("tier_per_kv_head", ctypes.c_int32)]
+                ("tier_per_kv_head", ctypes.c_int32), ("max_ledger_bits", ctypes.c_int32)]
 
 
 ALLOC_FN = ctypes.CFUNCTYPE(ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p)
@@ -67,7 +67,8 @@ class View(ctypes.Structure):
                 ("fp_slot_bytes", ctypes.c_int64), ("ledger_slot_bytes", ctypes.c_int64),
                 ("tier", ctypes.c_void_p), ("fp_slot", ctypes.c_void_p),
                 ("ledger_slot", ctypes.c_void_p), ("ledger_writes", ctypes.c_void_p),
-                ("fp_pool", ctypes.c_void_p), ("ledger_pool", ctypes.c_void_p)]
+                ("fp_pool", ctypes.c_void_p), ("ledger_pool", ctypes.c_void_p),
+                ("ledger_bits", ctypes.c_void_p), ("max_ledger_bits", ctypes.c_int32)]
 
 
 class Stats(ctypes.Structure):
@@ -164,13 +165,14 @@ class TieredCache:
 
     def __init__(self, batch, num_layers, num_q_heads, num_kv_heads, window, max_context,
                  budget_frac=1.0, fp_share=0.5, fp_capacity=0, ledger_capacity=0, fp_slack=0,
-                 head_dim=HEAD_DIM, torch_allocator=True, per_head=False):
+                 head_dim=HEAD_DIM, torch_allocator=True, per_head=False, max_ledger_bits=0):
         """per_head: one tier per (sequence, KV head, window); scores, tiers and
-        tier-move counts then have one row per unit b * num_kv_heads + kvh."""
+        tier-move counts then have one row per unit b * num_kv_heads + kvh.
+        max_ledger_bits 4 or 8 allows the INT4 (and INT8) tiers."""
         self.lib = load()
         self.cfg = Config(batch, num_layers, num_q_heads, num_kv_heads, head_dim, window, max_context,
                           fp_capacity, ledger_capacity, fp_slack, float(budget_frac), float(fp_share),
-                          1 if per_head else 0)
+                          1 if per_head else 0, int(max_ledger_bits))
         self.B, self.Hq, self.Hkv, self.w = batch, num_q_heads, num_kv_heads, window
         self.per_head = bool(per_head)
         self.units = batch * num_kv_heads if per_head else batch
@@ -355,34 +357,48 @@ class TieredCache:
         x = raw.view(torch.bfloat16).view(H, 2, 2, self.w, 64)     # [kvh][kv][half][token][64]
         return x.permute(0, 1, 3, 2, 4).reshape(H, 2, self.w, HEAD_DIM)
 
-    def ledger_window(self, layer, slot):
-        """Decoded ledger slot: codes uint8 [Hkv][2][w][d], scale/min fp16 [Hkv][2][w][d/32]."""
+    def ledger_window(self, layer, slot, bits=2):
+        """Decoded ledger slot of a window quantised to `bits` (2, 4, 8): codes
+        uint8 [Hkv][2][w][d], scale/min fp16 [Hkv][2][w][d/32]."""
         v = self.view(layer)
         raw = device_tensor(v.ledger_pool + slot * v.ledger_slot_bytes, (v.ledger_slot_bytes,), "|u1").cpu()
-        return decode_ledger_slot(raw, v.num_kv_heads, self.w)
+        return decode_ledger_slot(raw, v.num_kv_heads, self.w, bits)
+
+    def ledger_bits(self, layer):
+        """uint8 [units][W]: width of each window's ledger entry (0 none, 2, 4, 8), host copy."""
+        v = self.view(layer)
+        return device_tensor(v.ledger_bits, (v.batch, v.max_windows), "|u1")[:, :v.num_windows].cpu()
 
 
-def decode_ledger_slot(raw: torch.Tensor, Hkv: int, w: int):
+def decode_ledger_slot(raw: torch.Tensor, Hkv: int, w: int, bits: int = 2):
     """Unpack the documented ledger slot layout (see include/qevict.h) on the host.
 
-    Returns codes uint8 [Hkv][2 (K, V)][w][d] and scale, min fp16 [Hkv][2][w][d/32].
+    A window quantised to `bits` keeps P = bits / 2 two-bit planes, code =
+    sum_p 4^p c_p. Returns codes uint8 [Hkv][2 (K, V)][w][d] and scale, min
+    fp16 [Hkv][2][w][d/32].
     """
     d = HEAD_DIM
     nt = w // 16
-    raw = raw.view(Hkv, nt, 1536)
+    P = bits // 2
+    tb = 1024 * P + 512
+    raw = raw[:Hkv * nt * tb].view(Hkv, nt, tb)
     shifts = torch.arange(16, dtype=torch.int64) * 2
-    kw = raw[:, :, :512].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF   # [Hkv][nt][16*8]
-    kc = (kw.view(Hkv, nt, 16, 8)[..., None] >> shifts) & 3                           # [Hkv][nt][tok][q][16]
-    kcodes = kc.reshape(Hkv, nt * 16, d)
-    vw = raw[:, :, 768:1280].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF   # [Hkv][nt][128]
-    vc = (vw[..., None] >> shifts) & 3                                                   # [Hkv][nt][word][tok]
     i = torch.arange(d)
     ch = 16 * ((i >> 1) & 7) + (i >> 4) + 8 * (i & 1)                                   # channel of word i
-    vcodes = torch.empty(Hkv, nt, d, 16, dtype=torch.int64)
-    vcodes[:, :, ch] = vc
-    vcodes = vcodes.permute(0, 1, 3, 2).reshape(Hkv, nt * 16, d)
+    kcodes = torch.zeros(Hkv, nt * 16, d, dtype=torch.int64)
+    vcodes = torch.zeros(Hkv, nt * 16, d, dtype=torch.int64)
+    for p in range(P):
+        kw = raw[:, :, 512 * p:512 * (p + 1)].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+        kc = (kw.view(Hkv, nt, 16, 8)[..., None] >> shifts) & 3                         # [Hkv][nt][tok][q][16]
+        kcodes |= kc.reshape(Hkv, nt * 16, d) << (2 * p)
+        v0 = 512 * P + 256 + 512 * p
+        vw = raw[:, :, v0:v0 + 512].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF   # [Hkv][nt][128]
+        vc = (vw[..., None] >> shifts) & 3                                               # [Hkv][nt][word][tok]
+        vp = torch.empty(Hkv, nt, d, 16, dtype=torch.int64)
+        vp[:, :, ch] = vc
+        vcodes |= vp.permute(0, 1, 3, 2).reshape(Hkv, nt * 16, d) << (2 * p)
     codes = torch.stack([kcodes, vcodes], dim=1).to(torch.uint8)
-    km = raw[:, :, 512:768].contiguous().view(torch.float16).view(Hkv, nt * 16, 4, 2)
-    vm = raw[:, :, 1280:1536].contiguous().view(torch.float16).view(Hkv, nt * 16, 4, 2)
+    km = raw[:, :, 512 * P:512 * P + 256].contiguous().view(torch.float16).view(Hkv, nt * 16, 4, 2)
+    vm = raw[:, :, 1024 * P + 256:1024 * P + 512].contiguous().view(torch.float16).view(Hkv, nt * 16, 4, 2)
     meta = torch.stack([km, vm], dim=1)
     return codes, meta[..., 0].clone(), meta[..., 1].clone()

@@ -148,6 +148,15 @@ qevict_status check_layer(const qevict_cache *c, int32_t layer) {
 
 int n_windows(const qevict_cache *c, int64_t L) { return (int)((L + c->cfg.window - 1) / c->cfg.window); }
 
+// The score, log-sparse, rate-distortion and global routes count INT2 bytes for
+// every quantised window, so a cache that allows wider widths does not take them.
+qevict_status check_int2_only(const qevict_cache *c, const char *what) {
+    if (c->cfg.max_ledger_bits > 2)
+        return fail(QEVICT_ERR_INVALID_ARG, "%s counts INT2 bytes; this cache allows %d-bit windows "
+                    "(route it with qevict_route_rd_mixed or explicit tiers)", what, c->cfg.max_ledger_bits);
+    return QEVICT_OK;
+}
+
 void note_op(qevict_cache *c, int layer, void *stream) {
     c->prev_layer = layer;
     c->prev_stream = stream;
@@ -205,6 +214,8 @@ qevict_status check_config(const qevict_config &cfg) {
         return fail(QEVICT_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads, at most %d per KV head",
                     kMaxG);
     if (cfg.head_dim != kHeadDim) return fail(QEVICT_ERR_INVALID_ARG, "head_dim must be %d", kHeadDim);
+    if (cfg.max_ledger_bits != 0 && cfg.max_ledger_bits != 2 && cfg.max_ledger_bits != 4 && cfg.max_ledger_bits != 8)
+        return fail(QEVICT_ERR_INVALID_ARG, "max_ledger_bits must be 0, 2, 4 or 8");
     if (cfg.window < 16 || cfg.window > 128 || cfg.window % kVTile != 0)
         return fail(QEVICT_ERR_INVALID_ARG, "window must be a multiple of 16 in [16, 128]");
     if (cfg.max_context < 1) return fail(QEVICT_ERR_INVALID_ARG, "max_context must be >= 1");
@@ -252,8 +263,11 @@ qevict_status qevict_pool_capacity(const qevict_config *config, int32_t *fp_capa
     pool_capacity(cfg, Wmax, c_fp, c_q, &CF, &CQ);
     *fp_capacity = CF;
     *ledger_capacity = CQ;
-    if (pool_bytes_per_layer)
-        *pool_bytes_per_layer = (int64_t)cfg.batch * (CF * c_fp + CQ * c_q);
+    if (pool_bytes_per_layer) {
+        const int maxP = cfg.max_ledger_bits > 2 ? cfg.max_ledger_bits / 2 : 1;
+        const int64_t lgs = (int64_t)cfg.num_kv_heads * (cfg.window / 16) * qtile_bytes(maxP);
+        *pool_bytes_per_layer = (int64_t)cfg.batch * (CF * c_fp + CQ * lgs);
+    }
     return QEVICT_OK;
 }
 
@@ -288,7 +302,8 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     pool_capacity(cfg, Wmax, c->c_fp, c->c_q, &c->CF, &c->CQ);
     const int B = cfg.batch, Hkv = cfg.num_kv_heads, Hq = cfg.num_q_heads, w = cfg.window;
     const int64_t fps = (int64_t)Hkv * 2 * w * kHeadDim * 2;
-    const int64_t lgs = (int64_t)Hkv * (w / 16) * kQTile;
+    const int maxP = cfg.max_ledger_bits > 2 ? cfg.max_ledger_bits / 2 : 1;
+    const int64_t lgs = (int64_t)Hkv * (w / 16) * qtile_bytes(maxP);   // ledger slots sized for the widest width
 
     cudaError_t err = cudaSuccess;
     // cache-wide status and statistics
@@ -354,6 +369,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         LayerDev &D = c->layers[l].dev;
         D.B = B;
         D.hs = hs;
+        D.maxP = maxP;
         D.Hq = Hq;
         D.Hkv = Hkv;
         D.G = c->G;
@@ -385,6 +401,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         const size_t o_wp = cv.take((size_t)B * Wmax * 16);
         const size_t o_wc = cv.take((size_t)B * Wmax * 16);
         const size_t o_dg = cv.take((size_t)B * 8 * 4);
+        const size_t o_lb = cv.take((size_t)B * Wmax);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
         if (!base) {
             const size_t need = cv.off;
@@ -409,6 +426,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         D.work_p = (int4 *)(base + o_wp);
         D.work_c = (int4 *)(base + o_wc);
         D.diag = (int32_t *)(base + o_dg);
+        D.lbits = base + o_lb;
     }
     err = prepare_decode();
     EncodeTiledFn enc = encode_tiled();
@@ -466,6 +484,10 @@ qevict_status qevict_prefill(qevict_cache *c, int32_t layer, const void *k, cons
     if (!k || !v) return fail(QEVICT_ERR_INVALID_ARG, "k and v must not be NULL");
     if ((scores == nullptr) == (tiers == nullptr))
         return fail(QEVICT_ERR_INVALID_ARG, "give exactly one of scores and tiers");
+    if (scores) {
+        const qevict_status cs = check_int2_only(c, "a prefill with scores");
+        if (cs) return cs;
+    }
     if (n_tokens < 1 || n_tokens > c->cfg.max_context)
         return fail(QEVICT_ERR_INVALID_ARG, "n_tokens %d out of [1, %d]", n_tokens, c->cfg.max_context);
     if (lh.length != 0) return fail(QEVICT_ERR_STATE, "prefill needs an empty layer (length %lld)", (long long)lh.length);
@@ -511,6 +533,8 @@ static qevict_status decode_common(qevict_cache *c, int32_t layer, const void *q
     if (st) return st;
     LayerHost &lh = c->layers[layer];
     if (!q || !out) return fail(QEVICT_ERR_INVALID_ARG, "q and out must not be NULL");
+    if (c->cfg.max_ledger_bits > 2)
+        return fail(QEVICT_ERR_INVALID_ARG, "decoding a cache with INT4 / INT8 windows is not built yet");
     if (k_new) {
         if (lh.length + 1 > c->cfg.max_context)
             return fail(QEVICT_ERR_INVALID_ARG, "context %lld + 1 passes max_context %d", (long long)lh.length,
@@ -547,6 +571,8 @@ qevict_status qevict_route_rd(qevict_cache *c, int32_t layer, const float *score
                               void *stream) {
     qevict_status st = check_layer(c, layer);
     if (st) return st;
+    st = check_int2_only(c, "the rate-distortion route");
+    if (st) return st;
     LayerHost &lh = c->layers[layer];
     if (lh.length == 0) return QEVICT_OK;
     const int64_t Bt = budget_bytes(c->cfg, lh.length);
@@ -564,6 +590,8 @@ qevict_status qevict_route_rd(qevict_cache *c, int32_t layer, const float *score
 qevict_status qevict_route_logsparse(qevict_cache *c, int32_t layer, int32_t recent_windows, void *stream) {
     qevict_status st = check_layer(c, layer);
     if (st) return st;
+    st = check_int2_only(c, "the log-sparse route");
+    if (st) return st;
     if (recent_windows < 1) return fail(QEVICT_ERR_INVALID_ARG, "recent_windows must be >= 1");
     LayerHost &lh = c->layers[layer];
     if (lh.length == 0) return QEVICT_OK;
@@ -580,6 +608,10 @@ qevict_status qevict_route_logsparse(qevict_cache *c, int32_t layer, int32_t rec
 
 qevict_status qevict_route_global(qevict_cache *c, const float *const *scores_override, void *stream) {
     if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    {
+        const qevict_status st = check_int2_only(c, "the global route");
+        if (st) return st;
+    }
     const qevict_config &cfg = c->cfg;
     cudaStream_t s = (cudaStream_t)stream;
     // host check of the one budget against the forced windows (host lengths)
@@ -636,6 +668,8 @@ qevict_status qevict_route_global(qevict_cache *c, const float *const *scores_ov
 qevict_status qevict_route(qevict_cache *c, int32_t layer, const float *scores_override, const float *score_mult,
                            void *stream) {
     qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    st = check_int2_only(c, "the score route");
     if (st) return st;
     LayerHost &lh = c->layers[layer];
     if (lh.length == 0) return QEVICT_OK;
@@ -725,6 +759,8 @@ qevict_status qevict_get_view(const qevict_cache *c, int32_t layer, qevict_view 
     v->ledger_writes = D.lwrites;
     v->fp_pool = D.fp_pool;
     v->ledger_pool = D.lg_pool;
+    v->ledger_bits = D.lbits;
+    v->max_ledger_bits = 2 * D.maxP;
     return QEVICT_OK;
 }
 

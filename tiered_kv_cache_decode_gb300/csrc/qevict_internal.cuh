@@ -43,6 +43,26 @@ __host__ __device__ inline int64_t lg_tile_off(int kvh, int w, int tile) {
     return ((int64_t)kvh * (w / 16) + tile) * kQTile;
 }
 
+// Wider codes (4 or 8 bits, P = bits / 2 planes): code = sum_p 4^p c_p with
+// 2-bit planes c_p, each plane in the INT2 code layout. A tile holds the K
+// planes at p * 512, the K meta after them, the V planes, then the V meta:
+// 1024 P + 512 bytes; P = 1 is the INT2 tile above.
+__host__ __device__ inline int qtile_bytes(int P) { return 1024 * P + 512; }
+__host__ __device__ inline int qtile_kmeta(int P) { return 512 * P; }
+__host__ __device__ inline int qtile_vcodes(int P) { return 512 * P + 256; }
+__host__ __device__ inline int qtile_vmeta(int P) { return 1024 * P + 256; }
+__host__ __device__ inline int64_t lg_tile_off(int kvh, int w, int tile, int P) {
+    return ((int64_t)kvh * (w / 16) + tile) * qtile_bytes(P);
+}
+// A quantised window list entry's slot field: slot | log2(P) << 24 (0 for INT2).
+constexpr int kSlotBits = 24;
+__host__ __device__ inline bool is_quant_tier(int t) {
+    return t == QEVICT_TIER_Q || t == QEVICT_TIER_Q4 || t == QEVICT_TIER_Q8;
+}
+__host__ __device__ inline int tier_bits(int t) {
+    return t == QEVICT_TIER_Q4 ? 4 : (t == QEVICT_TIER_Q8 ? 8 : 2);
+}
+
 // V codes of a 16-token tile are 128 uint32 words, word i = (g * 8 + mt) * 2 + h
 // holding channel 16 * mt + g + 8 * h (g, mt in 0..7, h in 0..1). This puts the
 // 16 words one MMA lane group needs for the transposed-V operand side by side.
@@ -59,6 +79,7 @@ __host__ __device__ inline int vword_index(int ch) {
 struct LayerDev {
     int B, Hq, Hkv, G, w, Wmax, CF, CQ;   // per unit: a sequence, or a (sequence, KV head) pair
     int hs;                     // KV heads folded into units: 1, or the model's Hkv with per-head tiers
+    int maxP;                   // planes of the widest ledger width allowed: 1 (INT2), 2 (INT4), 4 (INT8)
     int max_context;
     double beta, rho;           // budget fraction and its full-precision share
     int64_t c_fp, c_q;          // bytes of one window per sequence in each visible tier
@@ -79,6 +100,7 @@ struct LayerDev {
     int4 *work_p;         // [B][Wmax] promote: {window, src ledger slot, dst fp slot, 0}
     int4 *work_c;         // [B][Wmax] prefill copy: {window, dst fp slot, 0, 0}
     int32_t *diag;        // [B][8] counts of the last completed tier move (see qevict_get_tier_move_counts)
+    uint8_t *lbits;       // [B][Wmax] width of the window's ledger entry: 0 (none), 2, 4 or 8
 };
 
 // Row of token t of unit u in a caller's [units / hs][n][Hkv * hs][d] token array

@@ -29,6 +29,7 @@ __global__ void init_layer_kernel(LayerDev D) {
         D.fp_slot[i] = -1;
         D.lg_slot[i] = -1;
         D.lwrites[i] = 0;
+        D.lbits[i] = 0;
     }
     for (int64_t i = i0; i < nW * D.Hkv; i += stride) D.score_part[i] = 0.f;
     for (int64_t i = i0; i < (int64_t)D.B * D.CF; i += stride) {
@@ -247,7 +248,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                     continue;
                 }
                 if (a.mode == PLAN_DEMOTE) {
-                    if (s_cur[wi] != QEVICT_TIER_FP || (wi == nw - 1 && partial_last)) {
+                    // a listed demotion is to INT2; a window whose ledger has another width keeps it
+                    if (s_cur[wi] != QEVICT_TIER_FP || (wi == nw - 1 && partial_last) ||
+                        (D.lbits[wb + wi] != 0 && D.lbits[wb + wi] != 2)) {
                         set_status(C, QEVICT_ERR_STATE, a.layer, b, wi);
                         continue;
                     }
@@ -262,8 +265,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                         lg = D.lg_free[b * D.CQ + top - 1];
                         ctr[CTR_LG_TOP] = top - 1;
                         D.lg_slot[wb + wi] = lg;
+                        D.lbits[wb + wi] = 2;
                         D.lwrites[wb + wi] += 1;
-                        D.work_q[wb + nq++] = make_int4(wi, old_fp, lg, 0);
+                        D.work_q[wb + nq++] = make_int4(wi, old_fp, lg, 2);
                         atomicAdd(&C.stats[ST_LWRITE], 1ull);
                     } else {
                         atomicAdd(&C.stats[ST_LREUSE], 1ull);
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                     s_cur[wi] = QEVICT_TIER_Q;
                     atomicAdd(&C.stats[ST_DEMOTE], 1ull);
                 } else {
-                    if (s_cur[wi] != QEVICT_TIER_Q) {
+                    if (!is_quant_tier(s_cur[wi])) {
                         set_status(C, QEVICT_ERR_STATE, a.layer, b, wi);
                         continue;
                     }
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                     ctr[CTR_FP_TOP] = top - 1;
                     D.fp_slot[wb + wi] = fp;
                     D.tier[wb + wi] = QEVICT_TIER_FP;
-                    D.work_p[wb + np++] = make_int4(wi, D.lg_slot[wb + wi], fp, 0);
+                    D.work_p[wb + np++] = make_int4(wi, D.lg_slot[wb + wi], fp, D.lbits[wb + wi]);
                     s_cur[wi] = QEVICT_TIER_FP;
                     atomicAdd(&C.stats[ST_PROMOTE], 1ull);
                 }
@@ -441,8 +445,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             for (int i = tid; i < nw; i += kPlanThreads) {
                 const uint8_t t = a.tiers[(int64_t)b * nw + i];
                 const uint8_t c = s_cur[i];
-                if (t > QEVICT_TIER_E || (c == QEVICT_TIER_E && t != QEVICT_TIER_E) ||
-                    (i == nw - 1 && partial_last && t != c))
+                const int lb = prefill ? 0 : D.lbits[wb + i];
+                const bool allowed = t <= QEVICT_TIER_E || (t == QEVICT_TIER_Q4 && D.maxP >= 2) ||
+                                     (t == QEVICT_TIER_Q8 && D.maxP >= 4);
+                if (!allowed || (c == QEVICT_TIER_E && t != QEVICT_TIER_E) ||
+                    (i == nw - 1 && partial_last && t != c) ||
+                    (is_quant_tier(c) && is_quant_tier(t) && c != t) ||   // a quantised window keeps its width
+                    (c == QEVICT_TIER_FP && is_quant_tier(t) && lb != 0 && lb != tier_bits(t)))   // so does its ledger
                     bad = 1;
                 s_tgt[i] = t;
             }
@@ -464,8 +473,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             const int lg = prefill ? -1 : D.lg_slot[wb + i];
             if (!prefill && c == QEVICT_TIER_FP && t != QEVICT_TIER_FP) ++free_fp;
             if (c != QEVICT_TIER_E && t == QEVICT_TIER_E && lg >= 0) ++free_lg;
-            if (c == QEVICT_TIER_FP && t == QEVICT_TIER_Q && lg < 0) ++need_lg;
-            if ((c == QEVICT_TIER_Q && t == QEVICT_TIER_FP) || (prefill && t == QEVICT_TIER_FP)) ++need_fp;
+            if (c == QEVICT_TIER_FP && is_quant_tier(t) && lg < 0) ++need_lg;
+            if ((is_quant_tier(c) && t == QEVICT_TIER_FP) || (prefill && t == QEVICT_TIER_FP)) ++need_fp;
         }
         int tot_free_fp, tot_free_lg, tot_need_fp, tot_need_lg;
         const int off_free_fp = block_scan(free_fp, &tot_free_fp, s_warp);
@@ -498,8 +507,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         int nq_local = 0, np_local = 0, nc_local = 0;
         for (int i = w0; i < w1; ++i) {
             const uint8_t c = s_cur[i], t = s_tgt[i];
-            nq_local += (c == QEVICT_TIER_FP && t == QEVICT_TIER_Q && (prefill || D.lg_slot[wb + i] < 0));
-            np_local += (!prefill && c == QEVICT_TIER_Q && t == QEVICT_TIER_FP);
+            nq_local += (c == QEVICT_TIER_FP && is_quant_tier(t) && (prefill || D.lg_slot[wb + i] < 0));
+            np_local += (!prefill && is_quant_tier(c) && t == QEVICT_TIER_FP);
             nc_local += (prefill && t == QEVICT_TIER_FP);
         }
         int tq, tp, tc;
@@ -515,15 +524,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                 D.lwrites[e] = 0;
                 D.lg_slot[e] = -1;
                 D.fp_slot[e] = -1;
+                D.lbits[e] = 0;
                 if (t == QEVICT_TIER_FP) {
                     const int fp = D.fp_free[b * D.CF + fp_mid - 1 - nf++];
                     D.fp_slot[e] = fp;
                     D.work_c[wb + oc++] = make_int4(i, fp, 0, 0);
-                } else if (t == QEVICT_TIER_Q) {
+                } else if (is_quant_tier(t)) {
                     const int lg = D.lg_free[b * D.CQ + lg_mid - 1 - nl++];
                     D.lg_slot[e] = lg;
+                    D.lbits[e] = (uint8_t)tier_bits(t);
                     D.lwrites[e] = 1;
-                    D.work_q[wb + oq++] = make_int4(i, -1, lg, 0);
+                    D.work_q[wb + oq++] = make_int4(i, -1, lg, tier_bits(t));
                     ++st_dem;
                     ++st_lw;
                 } else {
@@ -538,24 +549,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             if (t == QEVICT_TIER_E) {
                 D.fp_slot[e] = -1;
                 D.lg_slot[e] = -1;
+                D.lbits[e] = 0;
                 ++st_evi;
-            } else if (c == QEVICT_TIER_FP && t == QEVICT_TIER_Q) {
+            } else if (c == QEVICT_TIER_FP && is_quant_tier(t)) {
                 const int old_fp = D.fp_slot[e];
                 if (D.lg_slot[e] < 0) {
                     const int lg = D.lg_free[b * D.CQ + lg_mid - 1 - nl++];
                     D.lg_slot[e] = lg;
+                    D.lbits[e] = (uint8_t)tier_bits(t);
                     D.lwrites[e] += 1;
-                    D.work_q[wb + oq++] = make_int4(i, old_fp, lg, 0);
+                    D.work_q[wb + oq++] = make_int4(i, old_fp, lg, tier_bits(t));
                     ++st_lw;
                 } else {
                     ++st_lr;
                 }
                 D.fp_slot[e] = -1;
                 ++st_dem;
-            } else if (c == QEVICT_TIER_Q && t == QEVICT_TIER_FP) {
+            } else if (is_quant_tier(c) && t == QEVICT_TIER_FP) {
                 const int fp = D.fp_free[b * D.CF + fp_mid - 1 - nf++];
                 D.fp_slot[e] = fp;
-                D.work_p[wb + op++] = make_int4(i, D.lg_slot[e], fp, 0);
+                D.work_p[wb + op++] = make_int4(i, D.lg_slot[e], fp, D.lbits[e]);
                 ++st_pro;
             }
             D.tier[e] = t;
@@ -581,14 +594,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     int nfp_local = 0, nq_local = 0;
     for (int i = w0; i < w1; ++i) {
         nfp_local += s_tgt[i] == QEVICT_TIER_FP;
-        nq_local += s_tgt[i] == QEVICT_TIER_Q;
+        nq_local += is_quant_tier(s_tgt[i]);
     }
     int tf, tq;
     int of = block_scan(nfp_local, &tf, s_warp);
     int oq = block_scan(nq_local, &tq, s_warp);
     for (int i = w0; i < w1; ++i) {
         if (s_tgt[i] == QEVICT_TIER_FP) D.fp_list[b * D.CF + of++] = make_int2(i, D.fp_slot[wb + i]);
-        if (s_tgt[i] == QEVICT_TIER_Q) D.q_list[b * D.CQ + oq++] = make_int2(i, D.lg_slot[wb + i]);
+        if (is_quant_tier(s_tgt[i])) {   // the slot field carries log2 of the window's planes
+            const int lb = D.lbits[wb + i];
+            D.q_list[b * D.CQ + oq++] = make_int2(i, D.lg_slot[wb + i] | ((lb == 8 ? 2 : lb == 4 ? 1 : 0) << kSlotBits));
+        }
     }
     // ---- the move's counts (the full-precision tier read as the active set):
     // tier sizes before and after, kept, promoted, demoted, evicted
@@ -597,12 +613,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         for (int i = w0; i < w1; ++i) {
             const uint8_t o = s_old[i], n = s_tgt[i];
             cnt[0] += o == QEVICT_TIER_FP;
-            cnt[1] += o == QEVICT_TIER_Q;
+            cnt[1] += is_quant_tier(o);
             cnt[2] += n == QEVICT_TIER_FP;
-            cnt[3] += n == QEVICT_TIER_Q;
+            cnt[3] += is_quant_tier(n);
             cnt[4] += o == QEVICT_TIER_FP && n == QEVICT_TIER_FP;
-            cnt[5] += o == QEVICT_TIER_Q && n == QEVICT_TIER_FP;
-            cnt[6] += o == QEVICT_TIER_FP && n == QEVICT_TIER_Q;
+            cnt[5] += is_quant_tier(o) && n == QEVICT_TIER_FP;
+            cnt[6] += o == QEVICT_TIER_FP && is_quant_tier(n);
             cnt[7] += o != QEVICT_TIER_E && n == QEVICT_TIER_E;
         }
 #pragma unroll
@@ -635,6 +651,9 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int4 job = D.work_q[(int64_t)b * D.Wmax + e];
         const int wi = job.x, src_slot = job.y, dst = job.z;
+        // the width: 2, 4 or 8 bits, written as P 2-bit planes
+        const int bits = job.w == 4 || job.w == 8 ? job.w : 2, P = bits / 2;
+        const float levels = (float)((1 << bits) - 1);
         uint8_t *slotp = D.lg_pool + (int64_t)dst * D.lg_slot_bytes;
         for (int it = threadIdx.x; it < w * kGroups; it += blockDim.x) {
             const int t = it / kGroups, g = it % kGroups;
@@ -666,7 +685,7 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
                 mx = fmaxf(mx, x[j]);
             }
             const __half mn16 = __float2half_rn(mn);
-            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+            const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), levels));
             const float mq = __half2float(mn16), sq = __half2float(s16);
             const bool bad = !finite || isinf(mq) || isinf(sq);
             if (bad) set_status(C, QEVICT_ERR_DEVICE, layer, b, wi);
@@ -675,34 +694,39 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
 #pragma unroll
             for (int j = 0; j < kGroup; ++j) {
                 float c = zero ? 0.f : rintf(__fdiv_rn(__fsub_rn(x[j], mq), zero ? 1.f : sq));
-                c = fminf(fmaxf(c, 0.f), 3.f);
+                c = fminf(fmaxf(c, 0.f), levels);
                 cs[j] = (uint8_t)c;
             }
-            __half2 *meta = reinterpret_cast<__half2 *>(slotp + lg_tile_off(h, w, t / 16) +
-                                                        (kv ? kTileVMeta : kTileKMeta)) +
+            __half2 *meta = reinterpret_cast<__half2 *>(slotp + lg_tile_off(h, w, t / 16, P) +
+                                                        (kv ? qtile_vmeta(P) : qtile_kmeta(P))) +
                             (t % 16) * kGroups + g;
             *meta = bad ? __halves2half2(__float2half_rn(0.f), __float2half_rn(0.f)) : __halves2half2(s16, mn16);
         }
         __syncthreads();
         if (kv == 0) {
-            // K: per token 8 words of 16 channels, channel j of the word at bits 2*(j%16)
-            for (int i = threadIdx.x; i < w * (kHeadDim / 16); i += blockDim.x) {
-                const int t = i / (kHeadDim / 16), q = i % (kHeadDim / 16);
+            // K: per token 8 words of 16 channels, channel j of the word at bits 2*(j%16); plane p
+            // of a wider code holds its bits 2p, 2p + 1
+            for (int i = threadIdx.x; i < P * w * (kHeadDim / 16); i += blockDim.x) {
+                const int p = i / (w * (kHeadDim / 16)), r = i % (w * (kHeadDim / 16));
+                const int t = r / (kHeadDim / 16), q = r % (kHeadDim / 16);
                 const uint8_t *cs = s_codes + t * kHeadDim + q * 16;
                 uint32_t word = 0;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) word |= (uint32_t)cs[j] << (2 * j);
-                reinterpret_cast<uint32_t *>(slotp + lg_tile_off(h, w, t / 16))[(t % 16) * 8 + q] = word;
+                for (int j = 0; j < 16; ++j) word |= (uint32_t)((cs[j] >> (2 * p)) & 3u) << (2 * j);
+                reinterpret_cast<uint32_t *>(slotp + lg_tile_off(h, w, t / 16, P) + 512 * p)[(t % 16) * 8 + q] = word;
             }
         } else {
             // V: per 16-token tile 128 words; word i holds channel vword_dim(i), token t of
-            // the tile at bits 2*(t%16)
-            for (int i = threadIdx.x; i < (w / kVTile) * kHeadDim; i += blockDim.x) {
-                const int tile = i / kHeadDim, j = vword_dim(i % kHeadDim);
+            // the tile at bits 2*(t%16); plane p of a wider code holds its bits 2p, 2p + 1
+            for (int i = threadIdx.x; i < P * (w / kVTile) * kHeadDim; i += blockDim.x) {
+                const int p = i / ((w / kVTile) * kHeadDim), r = i % ((w / kVTile) * kHeadDim);
+                const int tile = r / kHeadDim, j = vword_dim(r % kHeadDim);
                 uint32_t word = 0;
 #pragma unroll
-                for (int t = 0; t < kVTile; ++t) word |= (uint32_t)s_codes[(tile * kVTile + t) * kHeadDim + j] << (2 * t);
-                reinterpret_cast<uint32_t *>(slotp + lg_tile_off(h, w, tile) + kTileVCodes)[i % kHeadDim] = word;
+                for (int t = 0; t < kVTile; ++t)
+                    word |= (uint32_t)((s_codes[(tile * kVTile + t) * kHeadDim + j] >> (2 * p)) & 3u) << (2 * t);
+                reinterpret_cast<uint32_t *>(slotp + lg_tile_off(h, w, tile, P) + qtile_vcodes(P) + 512 * p)[r % kHeadDim] =
+                    word;
             }
         }
         __syncthreads();
@@ -716,20 +740,23 @@ __global__ void __launch_bounds__(128) promote_kernel(LayerDev D) {
     const int h = blockIdx.y >> 1, kv = blockIdx.y & 1;
     const int w = D.w;
     const int n = D.ctr[b * kCtrN + CTR_WP];
-    // one 16-token tile of this (KV head, K or V) at a time: its 128 code words
-    // and 64 (scale, min) pairs staged with coalesced loads
-    __shared__ uint32_t s_codes[128];
+    // one 16-token tile of this (KV head, K or V) at a time: its code words
+    // (128 per plane) and 64 (scale, min) pairs staged with coalesced loads
+    __shared__ uint32_t s_codes[4][128];
     __shared__ __half2 s_meta[64];
     const int tid = threadIdx.x;
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int4 job = D.work_p[(int64_t)b * D.Wmax + e];
+        const int P = job.w == 4 ? 2 : (job.w == 8 ? 4 : 1);   // planes of the window's ledger width
         const uint8_t *slotp = D.lg_pool + (int64_t)job.y * D.lg_slot_bytes;
         __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(D.fp_pool + (int64_t)job.z * D.fp_slot_bytes);
         for (int tile = 0; tile < w / 16; ++tile) {
-            const uint8_t *tp = slotp + lg_tile_off(h, w, tile);
+            const uint8_t *tp = slotp + lg_tile_off(h, w, tile, P);
             __syncthreads();   // the previous tile's values are used up
-            s_codes[tid] = reinterpret_cast<const uint32_t *>(tp + (kv ? kTileVCodes : 0))[tid];
-            if (tid < 64) s_meta[tid] = reinterpret_cast<const __half2 *>(tp + (kv ? kTileVMeta : kTileKMeta))[tid];
+            for (int p = 0; p < P; ++p)
+                s_codes[p][tid] = reinterpret_cast<const uint32_t *>(tp + (kv ? qtile_vcodes(P) : 0) + 512 * p)[tid];
+            if (tid < 64)
+                s_meta[tid] = reinterpret_cast<const __half2 *>(tp + (kv ? qtile_vmeta(P) : qtile_kmeta(P)))[tid];
             __syncthreads();
             // 16 tokens x 16 runs of 8 channels: two (token, run) items per thread
             for (int it = tid; it < 16 * 16; it += 128) {
@@ -740,8 +767,11 @@ __global__ void __launch_bounds__(128) promote_kernel(LayerDev D) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int ch = ch0 + j;
-                    const uint32_t c = kv == 0 ? (s_codes[t * 8 + ch / 16] >> (2 * (ch % 16))) & 3u
-                                               : (s_codes[vword_index(ch)] >> (2 * (t % kVTile))) & 3u;
+                    uint32_t c = 0;
+                    for (int p = 0; p < P; ++p)   // code = sum_p 4^p c_p
+                        c |= (kv == 0 ? (s_codes[p][t * 8 + ch / 16] >> (2 * (ch % 16))) & 3u
+                                      : (s_codes[p][vword_index(ch)] >> (2 * (t % kVTile))) & 3u)
+                             << (2 * p);
                     outv[j] = __float2bfloat16_rn(fmaf((float)c, sc, mn));
                 }
                 *reinterpret_cast<uint4 *>(dst + fp_off(h, kv, w, tile * 16 + t, ch0)) =
