@@ -113,3 +113,55 @@ def test_wide_cache_rejects_the_int2_routes():
         with pytest.raises(binding.QevictError) as e:
             call()
         assert e.value.name == "INVALID_ARG"
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,w,L,bits", [(2, 8, 2, 32, 640, 8), (1, 32, 8, 64, 4096, 8), (3, 28, 4, 16, 777, 4),
+                                               (1, 32, 8, 64, 32768, 8)])
+def test_wide_decode_matches_oracle(B, Hq, Hkv, w, L, bits):
+    from parity_util import check_decode
+    W = -(-L // w)
+    allowed = [O.TIER_FP, O.TIER_Q, O.TIER_Q4, O.TIER_E] + ([O.TIER_Q8] if bits == 8 else [])
+    tiers = mixed_tiers(70 + bits, B, W, allowed)
+    cache, ref = make_wide(B, Hq, Hkv, w, L, bits, tiers, seed=70 + bits)
+    for step in range(2):
+        check_decode(cache, 0, ref, synth.queries(70, 0, step, B, Hq, 128))
+
+
+def test_wide_decode_steps_append_into_a_mixed_cache():
+    B, Hq, Hkv, w, L0, steps = 2, 16, 4, 32, 512, 40
+    W0 = L0 // w
+    tiers = mixed_tiers(80, B, W0, [O.TIER_FP, O.TIER_Q, O.TIER_Q4, O.TIER_Q8, O.TIER_E])
+    Wmax = -(-(L0 + steps) // w)
+    cache = binding.TieredCache(B, 1, Hq, Hkv, w, L0 + steps, max_ledger_bits=8, fp_capacity=Wmax,
+                                ledger_capacity=Wmax)
+    ref = O.OracleCache(B, Hq, Hkv, 128, w)
+    k, v = synth.kv_tokens(80, 0, B, 0, L0, Hkv, 128, "heavy")
+    cache.prefill(0, k.cuda(), v.cuda(), tiers=torch.from_numpy(tiers).cuda())
+    ref.prefill(k.float().numpy(), v.float().numpy(), tiers=tiers)
+    from parity_util import close
+    for step in range(steps):
+        kn, vn = synth.kv_tokens(80, 0, B, L0 + step, 1, Hkv, 128)
+        q = synth.queries(80, 0, step, B, Hq, 128)
+        out, mass = cache.decode_step(0, q.cuda(), kn[:, 0].cuda(), vn[:, 0].cuda())
+        torch.cuda.synchronize()
+        ref.append(kn.float().numpy(), vn.float().numpy())
+        ro, rm = ref.decode(q.float().numpy())
+        close(out.cpu().numpy(), ro, f"output, step {step}")
+        close(mass.cpu().numpy(), rm, f"mass, step {step}")
+    assert cache.status() == 0, cache.last_error()
+    check_state(cache, 0, ref)
+
+
+def test_wide_cache_with_int2_windows_decodes_like_an_int2_cache():
+    B, Hq, Hkv, w, L = 1, 32, 8, 64, 4096
+    W = L // w
+    tiers = mixed_tiers(90, B, W, [O.TIER_FP, O.TIER_Q, O.TIER_E])
+    k, v = synth.kv_tokens(90, 0, B, 0, L, Hkv, 128, "heavy", device="cuda")
+    outs = []
+    for bits in (0, 8):
+        c = binding.TieredCache(B, 1, Hq, Hkv, w, L, max_ledger_bits=bits, fp_capacity=W, ledger_capacity=W)
+        c.prefill(0, k, v, tiers=torch.from_numpy(tiers).cuda())
+        o, m = c.decode(0, synth.queries(90, 0, 0, B, Hq, 128).cuda(), accumulate=False)
+        torch.cuda.synchronize()
+        outs.append((o.cpu(), m.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])

@@ -533,8 +533,6 @@ static qevict_status decode_common(qevict_cache *c, int32_t layer, const void *q
     if (st) return st;
     LayerHost &lh = c->layers[layer];
     if (!q || !out) return fail(QEVICT_ERR_INVALID_ARG, "q and out must not be NULL");
-    if (c->cfg.max_ledger_bits > 2)
-        return fail(QEVICT_ERR_INVALID_ARG, "decoding a cache with INT4 / INT8 windows is not built yet");
     if (k_new) {
         if (lh.length + 1 > c->cfg.max_context)
             return fail(QEVICT_ERR_INVALID_ARG, "context %lld + 1 passes max_context %d", (long long)lh.length,

@@ -212,7 +212,9 @@ __device__ __forceinline__ Range split_range(int split, int splits, int n_fp, in
                  (int)((int64_t)n_q * split / splits), (int)((int64_t)n_q * (split + 1) / splits)};
 }
 
-template <int G>
+// kWide: the cache may hold INT4 / INT8 windows (2 or 4 code planes); the
+// instantiation without it is the INT2 / full-precision kernel as such.
+template <int G, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const LayerDev D, const CacheDev C, const DecodeScratch S, const __grid_constant__ CUtensorMap tmap,
                   int layer, const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *knew,
@@ -228,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t s_gen;                               // split-record generation of this launch
     __shared__ int st_n[kWarps][kStages];                    // units in a stage
     __shared__ int st_fp[kWarps][kStages];                   // 1: a full-precision unit
+    __shared__ int st_p[kWarps][kStages];                    // code planes of a quantised stage (kWide)
     __shared__ int st_wi[kWarps][kStages][kQPerStage];       // window of each unit
     __shared__ int st_j[kWarps][kStages][kQPerStage];        // 16-token unit index inside the window
     __shared__ int st_nt[kWarps][kStages][kQPerStage];       // tokens in the unit
@@ -315,18 +318,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++iu;
             } else {
-                // INT2 windows are always full (mu tiles)
-                const int n = min(kQPerStage, u_end - iu);
+                // quantised windows are always full (mu tiles); with kWide a stage
+                // holds the tiles of one width only (2560 / 4608 B for INT4 / INT8)
+                int P = 1, tb = kQUnit, n = min(kQPerStage, u_end - iu);
+                if (kWide) {
+                    P = 1 << (ent(win_of(iu)).y >> kSlotBits);
+                    tb = qtile_bytes(P);
+                    n = 0;
+                    for (int iu2 = iu; iu2 < u_end && n < kStage / tb;) {
+                        const int lq = win_of(iu2);
+                        if ((1 << (ent(lq).y >> kSlotBits)) != P) break;
+                        const int run = min(min(mu - (iu2 - lq * mu), kStage / tb - n), u_end - iu2);
+                        n += run;
+                        iu2 += run;
+                    }
+                }
                 if (lane == 0) {
                     st_n[warp][st] = n;
                     st_fp[warp][st] = 0;
+                    if (kWide) st_p[warp][st] = P;
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    mbar_expect_tx(bar, (uint32_t)(n * kQUnit));
+                    mbar_expect_tx(bar, (uint32_t)(n * tb));
                 }
                 int done = 0;
                 while (done < n) {
                     const int lq = win_of(iu), jq = iu - lq * mu;
                     const int2 en = ent(lq);
+                    const int slot = kWide ? (en.y & ((1 << kSlotBits) - 1)) : en.y;
                     const int run = min(mu - jq, n - done);
                     if (lane == 0) {
                         const bool whole = lq * mu >= u_beg && (lq + 1) * mu <= u_end;
@@ -337,9 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             st_emit[warp][st][done + r] =
                                 (jq + r == mu - 1 || iu + r + 1 == u_end) ? (whole ? 1 : 2) : 0;
                         }
-                        bulk_g2s(dst + done * kQUnit,
-                                 D.lg_pool + (int64_t)en.y * D.lg_slot_bytes + lg_tile_off(kvh, w, jq),
-                                 (uint32_t)(run * kQUnit), bar, l2_stream);
+                        bulk_g2s(dst + done * tb,
+                                 D.lg_pool + (int64_t)slot * D.lg_slot_bytes +
+                                     (kWide ? lg_tile_off(kvh, w, jq, P) : lg_tile_off(kvh, w, jq)),
+                                 (uint32_t)(run * tb), bar, l2_stream);
                     }
                     done += run;
                     iu += run;
@@ -462,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ib = 0; ib < nb; ++ib) {
         const int wi = st_wi[warp][st][ib], ntu = st_nt[warp][st][ib];
         const int emit = st_emit[warp][st][ib];
-        const uint32_t base = ring_s + st * kStage + ib * kQUnit;
+        const int P = (kWide && !is_fp) ? st_p[warp][st] : 1;
+        const uint32_t base = ring_s + st * kStage + ib * (kWide ? (uint32_t)qtile_bytes(P) : (uint32_t)kQUnit);
         if (is_fp) {
             // ---------------- full-precision unit
             float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -505,6 +525,87 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ldsm_x4_t(addr, a0, a1, a2, a3);
                 mma(o[mt], a0, a1, a2, a3, b0h, b1h);
                 mma(o[mt], a0, a1, a2, a3, b0l, b1l);
+            }
+        } else if (kWide && P > 1) {
+            // ---------------- INT4 / INT8 unit: P planes of 2-bit codes, code = sum_p 4^p c_p.
+            // Each plane goes through the INT2 arithmetic with exact codes (no offset) and
+            // plane p weighted by 4^p on the query (K) and on P.scale (V): exact scalings.
+            const uint32_t kc = base, km = base + qtile_kmeta(P), vc = base + qtile_vcodes(P),
+                           vm = base + qtile_vmeta(P);
+            const int tA = (g & 1) ? g + 7 : g;
+            const int tB = (g & 1) ? g + 8 : g + 1;
+            uint4 kmeta[4];
+            kmeta[0] = lds128(km + (2 * t) * 16);
+            kmeta[1] = lds128(km + (2 * t + 8) * 16);
+            kmeta[2] = lds128(km + (2 * t + 1) * 16);
+            kmeta[3] = lds128(km + (2 * t + 9) * 16);
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int grp = 0; grp < kGroups; ++grp) {
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int p = 0; p < P; ++p) {
+                    const uint32_t kp = kc + 512 * p + (grp >= 2 ? 16 : 0);
+                    const uint4 kA = lds128(kp + tA * 32), kB = lds128(kp + tB * 32);
+                    const __nv_bfloat162 w4 = __float2bfloat162_rn((float)(1 << (2 * p)));
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int ks = 2 * grp + kk;
+                        const uint32_t xa = pick(kA, ks & 3) >> (4 * t);
+                        const uint32_t xb = pick(kB, ks & 3) >> (4 * t);
+                        const uint2 nq = s_qf[ks * 32 + lane];   // natural (q[2t], q[2t+1]), (q[2t+8], q[2t+9])
+                        uint32_t a0 = __byte_perm(nq.x, nq.y, 0x5410), a2 = __byte_perm(nq.x, nq.y, 0x7632);
+                        __nv_bfloat162 v0 = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a0), w4);
+                        __nv_bfloat162 v2 = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a2), w4);
+                        a0 = *reinterpret_cast<uint32_t *>(&v0);
+                        a2 = *reinterpret_cast<uint32_t *>(&v2);
+                        mma(c0, a0, 0u, a2, 0u, codes2(xa), codes2(xa >> 2));
+                        mma(c1, a0, 0u, a2, 0u, codes2(xb), codes2(xb >> 2));
+                    }
+                }
+                const float acc[4] = {c0[0], c0[1], c1[0], c1[1]};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 sm = h2f(pick(kmeta[i], grp));   // .x scale, .y min
+                    x[i] = fmaf(sm.x, acc[i], fmaf(sm.y, qsum[grp], x[i]));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[i] *= qk_scale;
+            softmax4(x);
+            const int vtok[4] = {2 * t, 2 * t + 8, 2 * t + 1, 2 * t + 9};
+#pragma unroll
+            for (int grp = 0; grp < kGroups; ++grp) {
+                uint32_t vmg[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vmg[i] = lds32(vm + vtok[i] * 16 + grp * 4);
+                float val[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 sm = h2f(vmg[i]);
+                    val[i] = x[i] * sm.x;
+                    minacc[grp] = fmaf(x[i], sm.y, minacc[grp]);
+                }
+                uint32_t b0h, b0l, b1h, b1l;
+                split2(val[0], val[1], b0h, b0l);
+                split2(val[2], val[3], b1h, b1l);
+                for (int p = 0; p < P; ++p) {
+                    const uint4 vv = lds128(vc + 512 * p + g * 64 + grp * 16);
+                    const __nv_bfloat162 w4 = __float2bfloat162_rn((float)(1 << (2 * p)));
+                    uint32_t sc[4] = {b0h, b1h, b0l, b1l};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        __nv_bfloat162 v = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&sc[r]), w4);
+                        sc[r] = *reinterpret_cast<uint32_t *>(&v);
+                    }
+#pragma unroll
+                    for (int mm = 0; mm < 2; ++mm) {
+                        const int mt = 2 * grp + mm;
+                        const uint32_t x0 = pick(vv, 2 * mm) >> (4 * t), x1 = pick(vv, 2 * mm + 1) >> (4 * t);
+                        const uint32_t a0 = codes2(x0), a1 = codes2(x1), a2 = codes2(x0 >> 2), a3 = codes2(x1 >> 2);
+                        mma(o[mt], a0, a1, a2, a3, sc[0], sc[1]);
+                        mma(o[mt], a0, a1, a2, a3, sc[2], sc[3]);
+                    }
+                }
             }
         } else {
             // ---------------- INT2 unit
@@ -940,15 +1041,24 @@ constexpr int kDynSmem = kWarps * kRing + kEntTab * 8 + 16 * 32 * 8 + 1024;
 // CTAs of decode_kernel<G> that fit on one SM, filled in by prepare_decode.
 int g_ctas_per_sm[kMaxG + 1];
 
-template <int G>
-cudaError_t prepare_one(int optin) {
+template <int G, bool kWide>
+cudaError_t prepare_inst(int optin, int *per_sm) {
     cudaFuncAttributes fa{};
-    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<G>);
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_kernel<G, kWide>);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_kernel<G, kWide>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              optin - (int)fa.sharedSizeBytes);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_ctas_per_sm[G], decode_kernel<G>, kThreads, kDynSmem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, decode_kernel<G, kWide>, kThreads, kDynSmem);
+}
+// Both instantiations must fit as many CTAs per SM as the split count assumes.
+template <int G>
+cudaError_t prepare_one(int optin) {
+    int a = 0, w = 0;
+    cudaError_t e = prepare_inst<G, false>(optin, &a);
+    if (e == cudaSuccess) e = prepare_inst<G, true>(optin, &w);
+    g_ctas_per_sm[G] = a < w ? a : w;
+    return e;
 }
 
 }  // namespace
@@ -987,6 +1097,7 @@ int decode_splits(int pairs, int num_sms, int G) {
 cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, const CUtensorMap &tmap,
                           int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
                           float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s) {
+    const bool wide = L.maxP > 1;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(splits, L.B * L.Hkv);
     cfg.blockDim = dim3(kThreads);
@@ -999,8 +1110,10 @@ cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScra
     cfg.numAttrs = pdl ? 1 : 0;
 #define QV_CASE(GG)                                                                                          \
     case GG:                                                                                                 \
-        return cudaLaunchKernelEx(&cfg, decode_kernel<GG>, L, C, S, tmap, layer, q, knew, vnew, out, mass,  \
-                                  accumulate, splits);
+        return wide ? cudaLaunchKernelEx(&cfg, decode_kernel<GG, true>, L, C, S, tmap, layer, q, knew, vnew,  \
+                                         out, mass, accumulate, splits)                                      \
+                    : cudaLaunchKernelEx(&cfg, decode_kernel<GG, false>, L, C, S, tmap, layer, q, knew, vnew, \
+                                         out, mass, accumulate, splits);
     switch (L.G) {
         QV_CASE(1)
         QV_CASE(2)
