@@ -484,6 +484,73 @@ def measure_variants(wl, NL, reps, dev, peak):
     }
 
 
+def measure_mixed_widths(wl, NL, reps, dev, peak):
+    """The workload with INT4 and INT8 allowed, routed by the rate-distortion
+    allocation over widths {0, 2, 4, 8, 16} (qevict_route_rd_mixed) on seeded
+    scores: one event per layer captured as a CUDA graph on one stream, timed
+    over 8 fresh score sets, then the decode kernel over all layers on the
+    tiers the last event left (CUDA graph; algorithmic bytes: every kept
+    window at its width, plus the query, output and scores)."""
+    import torch
+    from tiered_kv_cache_decode_gb300 import binding, synth
+    B, Hq, Hkv, w, L0, d, seed = wl["B"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"], 128, 0
+    W0 = L0 // w
+    mc = binding.TieredCache(B, NL, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"], max_ledger_bits=8,
+                             fp_capacity=W0, ledger_capacity=W0)
+    mc.set_launch_overlap(True)
+    zeros = torch.zeros(B, W0, dtype=torch.uint8, device=dev)
+    for l in range(NL):
+        k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
+        mc.prefill(l, k, v, tiers=zeros)
+        del k, v
+    q = [synth.queries(seed, l, 0, B, Hq, d, device=dev) for l in range(NL)]
+    xo = torch.empty(NL, B, Hq, d, dtype=torch.float32, device=dev)
+    ovs = [torch.empty(B, W0, dtype=torch.float32, device=dev) for _ in range(NL)]
+    stream = torch.cuda.Stream(device=dev)
+    g_route, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_route, stream=stream):
+            for l in range(NL):
+                mc.route_rd_mixed(l, scores_override=ovs[l], stream=stream)
+        with torch.cuda.graph(g_dec, stream=stream):
+            for l in range(NL):
+                mc.decode(l, q[l], out=xo[l], want_mass=False, accumulate=True, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tot = 0.0
+    for r in range(8):
+        for l in range(NL):
+            ovs[l].copy_(synth.zipf_scores(seed + 400 + r, l, B, W0, device=dev))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g_route.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        tot += e0.elapsed_time(e1) * 1e3
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g_dec.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g_dec.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us_dec = e0.elapsed_time(e1) * 1e3 / (reps * NL)
+    cost = {0: w * Hkv * d * 4, 1: w * Hkv * 2 * (d // 4 + 16), 3: w * Hkv * 2 * (d // 2 + 16),
+            4: w * Hkv * 2 * (d + 16), 2: 0}
+    tiers = torch.stack([mc.tables(l)[0] for l in range(NL)])   # [NL][B][W]
+    per_tier = {t: (tiers == t).sum().item() / (NL * B) for t in (0, 4, 3, 1, 2)}
+    nbytes = sum(cost[t] * n for t, n in per_tier.items()) * B + B * (Hq * d * 2 + Hq * d * 4 + Hkv * W0 * 8)
+    st = mc.status()
+    assert st == 0, f"device status {st}: {mc.last_error()}"
+    return {"route_us_per_event_all_layers": round(tot / 8, 2), "layers": NL,
+            "windows_bf16_int8_int4_int2_evicted_per_sequence_mean": [round(per_tier[t], 2) for t in (0, 4, 3, 1, 2)],
+            "decode_us_per_launch": round(us_dec, 3), "decode_bytes_per_launch": int(nbytes),
+            "decode_gbs": round(nbytes / (us_dec * 1e-6) / 1e9, 2),
+            "decode_frac_of_peak": round(nbytes / (us_dec * 1e-6) / 1e9 / peak, 4)}
+
+
 def run_native(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -696,6 +763,7 @@ def run_native(args, rank, world, local_rank):
         del cache, pool
         torch.cuda.empty_cache()
         line["variants"] = measure_variants(wl, NL, K, dev, peak)
+        line["variants"]["mixed_widths"] = measure_mixed_widths(wl, NL, K, dev, peak)
     if pool_async is not None:
         cpu_pool, nw, res, t_start = pool_async
         out = res.get()

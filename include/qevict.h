@@ -295,6 +295,29 @@ qevict_status qevict_route(qevict_cache *cache, int32_t layer, const float *scor
 qevict_status qevict_route_rd(qevict_cache *cache, int32_t layer, const float *scores_override,
                               const float *score_mult, void *stream);
 
+/* The rate-distortion routing event over all widths the cache allows
+ * ("Technische Samenvatting: RDKV", 2.1-2.2: widths {0, 2, 4, 8, 16}, the
+ * Lagrangian relaxation of the multiple-choice knapsack). A window's options
+ * form a chain of widths: 0, 2, 4, 8, 16 (the quantised ones up to
+ * max_ledger_bits, INT2 alone when it is 0 or 2) for a window never
+ * quantised, and 0, b, 16 for one whose ledger entry has width b (the
+ * write-once ledger fixes the width). A window of b bits costs
+ * window * Hkv * 2 * (d * b / 8 + 4 * d / 32) bytes (bf16: c_fp). The open
+ * window (the first of the score rank of qevict_route) is full precision;
+ * every other candidate's chain step a -> b is an upgrade whose gain per
+ * byte is (2^-a - 2^-b) / (cost(b) - cost(a)) * s, s its cumulative score,
+ * rounded in float64 as written. Upgrades are taken by gain, highest first (a
+ * lower step, then the higher-ranked window, on a tie), while the gain is
+ * positive, until the first that does not fit the budget
+ * floor(beta * L * Hkv * d * 4). Each window gets the width its taken steps
+ * reach and is moved as in qevict_route (a demotion quantises at that width
+ * when the window has no ledger entry; a promotion dequantises the entry).
+ * On a cache of INT2 only this is the allocation of qevict_route_rd. Same
+ * scores_override / score_mult and errors as qevict_route; allowed at every
+ * max_ledger_bits. */
+qevict_status qevict_route_rd_mixed(qevict_cache *cache, int32_t layer, const float *scores_override,
+                                    const float *score_mult, void *stream);
+
 /* A routing event by position instead of score ("Technische Samenvatting:
  * LogQuant", Methodologie 1-2: attention peaks thin out logarithmically with
  * the distance to the current token, so the kept positions thin out the same

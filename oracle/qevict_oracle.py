@@ -685,9 +685,10 @@ def rd_mixed_widths(S_ranked, chains, L: int, w: int, Hkv: int, d: int, beta: fl
     return [ch[st] for ch, st in zip(chains, steps)]
 
 
-def route_rd_mixed(cache, scores_override=None):
+def route_rd_mixed(cache, scores_override=None, max_bits=8):
     """A routing event by the rate-distortion allocation over widths
-    {0, 2, 4, 8, 16}; windows keep the width of an existing ledger entry."""
+    {0, 2, 4, 8, 16} (those up to max_bits, and 16); windows keep the width of
+    an existing ledger entry."""
     if scores_override is not None:
         ov = np.asarray(scores_override, np.float64)
         cache.S = [ov[b, :cache.W].copy() for b in range(cache.B)]
@@ -702,11 +703,13 @@ def route_rd_mixed(cache, scores_override=None):
         forced = W - 1
         order = sorted(cand, key=lambda i: (i != forced, -float(S[i]), i))
         rest = order[1:]
-        chains = [[0, 2, 4, 8, 16] if cache.win[b][i].ledger is None else [0, cache.win[b][i].ledger_bits, 16]
+        free = [0] + [x for x in (2, 4, 8) if x <= max_bits] + [16]
+        chains = [free if cache.win[b][i].ledger is None else [0, cache.win[b][i].ledger_bits, 16]
                   for i in rest]
         widths = rd_mixed_widths([S[i] for i in rest], chains, cache.L, cache.w, cache.Hkv, cache.d, cache.beta)
         new = np.array(old, np.uint8)
-        new[forced] = TIER_FP
+        if order:   # the first-ranked candidate (the open window) stays full precision, as in route_rd
+            new[order[0]] = TIER_FP
         for i, bits in zip(rest, widths):
             new[i] = TIER_OF_BITS[bits]
         cache.apply_tiers(b, new)

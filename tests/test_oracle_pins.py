@@ -947,3 +947,29 @@ def test_rd_mixed_hand_derived():
         got = [1 + widths.count(16), widths.count(8), widths.count(4), widths.count(2), widths.count(0)]
         assert got == [n16, n8, n4, n2, n0]
         assert sum(O.width_cost(w, Hkv, 128, x) for x in widths) + O.width_cost(w, Hkv, 128, 16) == res
+
+
+def test_rd_mixed_route_on_int2_widths_is_route_rd():
+    """With INT2 the only quantised width every chain is 0-2-16: routing
+    events of the mixed route leave a cache exactly as the two-width route
+    does (tiers, ledger entries, reuse counts), ledgers reused on the third."""
+    B, Hq, Hkv, w, L, beta = 2, 8, 2, 16, 640, 0.25
+    W = L // w
+    rng = np.random.default_rng(20)
+    k = rng.standard_normal((B, L, Hkv, 128)).astype(np.float32)
+    v = rng.standard_normal((B, L, Hkv, 128)).astype(np.float32)
+    caches = []
+    for mixed in (False, True):
+        c = O.OracleCache(B, Hq, Hkv, 128, w, beta=beta)
+        c.prefill(k, v, tiers=np.zeros((B, W), np.uint8))
+        caches.append(c)
+    for event in range(4):
+        S = rng.pareto(1.1, (B, W)) * (1 + event)
+        O.route_rd(caches[0], scores_override=S)
+        O.route_rd_mixed(caches[1], scores_override=S, max_bits=2)
+        assert np.array_equal(caches[0].tiers(), caches[1].tiers()), event
+        assert np.array_equal(caches[0].last_counts, caches[1].last_counts)
+        for b in range(B):
+            for x, y in zip(caches[0].win[b], caches[1].win[b]):
+                assert (x.ledger is None) == (y.ledger is None) and x.ledger_writes == y.ledger_writes
+    assert caches[0].stats == caches[1].stats and caches[1].stats["ledger_reuses"] > 0

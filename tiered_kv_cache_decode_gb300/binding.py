@@ -29,6 +29,7 @@ EXPORTS = ["qevict_pool_capacity", "qevict_cache_create", "qevict_cache_destroy"
            "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_set_launch_overlap",
            "qevict_refresh_lengths", "qevict_decode_attention_static_scratch",
            "qevict_get_tier_move_counts", "qevict_future_missed_mass", "qevict_route_global", "qevict_route_logsparse", "qevict_route_rd",
+           "qevict_route_rd_mixed",
            "qevict_length",
            "qevict_last_error"]
 
@@ -115,6 +116,7 @@ def load() -> ctypes.CDLL:
         "qevict_route_global": [P, P, P],
         "qevict_route_logsparse": [P, I32, I32, P],
         "qevict_route_rd": [P, I32, P, P, P],
+        "qevict_route_rd_mixed": [P, I32, P, P, P],
         "qevict_future_missed_mass": [P, I32, P, P, I64, P, P],
         "qevict_length": [P, I32],
         "qevict_last_error": [],
@@ -274,6 +276,12 @@ class TieredCache:
         """Route a layer with tier counts from the rate-distortion allocation."""
         self._check(self.lib.qevict_route_rd(self.handle, layer, _ptr(scores_override), _ptr(score_mult),
                                              _stream(stream)))
+
+    def route_rd_mixed(self, layer, scores_override=None, score_mult=None, stream=None):
+        """Route a layer by the rate-distortion allocation over the widths the
+        cache allows (0, 2, 4, 8, 16 bits)."""
+        self._check(self.lib.qevict_route_rd_mixed(self.handle, layer, _ptr(scores_override), _ptr(score_mult),
+                                                   _stream(stream)))
 
     def route_logsparse(self, layer, recent=2, stream=None):
         """Route a layer by log-sparse position (the scores are not used)."""

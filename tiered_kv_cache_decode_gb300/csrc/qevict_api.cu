@@ -585,6 +585,24 @@ qevict_status qevict_route_rd(qevict_cache *c, int32_t layer, const float *score
     return run_plan(c, lh, a, nullptr, nullptr, (cudaStream_t)stream);
 }
 
+qevict_status qevict_route_rd_mixed(qevict_cache *c, int32_t layer, const float *scores_override,
+                                    const float *score_mult, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    LayerHost &lh = c->layers[layer];
+    if (lh.length == 0) return QEVICT_OK;
+    const int64_t Bt = budget_bytes(c->cfg, lh.length);
+    if (Bt < c->c_fp)
+        return fail(QEVICT_ERR_BUDGET, "budget %lld B cannot hold the open window (%lld B)", (long long)Bt,
+                    (long long)c->c_fp);
+    PlanArgs a{};
+    a.mode = PLAN_RD_MIXED;
+    a.layer = layer;
+    a.scores = scores_override;
+    a.mult = score_mult;
+    return run_plan(c, lh, a, nullptr, nullptr, (cudaStream_t)stream);
+}
+
 qevict_status qevict_route_logsparse(qevict_cache *c, int32_t layer, int32_t recent_windows, void *stream) {
     qevict_status st = check_layer(c, layer);
     if (st) return st;

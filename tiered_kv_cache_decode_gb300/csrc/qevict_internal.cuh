@@ -127,7 +127,8 @@ struct CacheDev {
 };
 
 enum PlanMode { PLAN_ROUTE = 0, PLAN_TIERS = 1, PLAN_PREFILL_SCORES = 2, PLAN_PREFILL_TIERS = 3,
-                PLAN_DEMOTE = 4, PLAN_PROMOTE = 5, PLAN_GLOBAL = 6, PLAN_LOGSPARSE = 7, PLAN_RD = 8 };
+                PLAN_DEMOTE = 4, PLAN_PROMOTE = 5, PLAN_GLOBAL = 6, PLAN_LOGSPARSE = 7, PLAN_RD = 8,
+                PLAN_RD_MIXED = 9 };
 
 struct PlanArgs {
     int mode;

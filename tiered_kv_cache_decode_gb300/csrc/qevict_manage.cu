@@ -182,6 +182,166 @@ __device__ int block_scan(int v, int *total, int *s_warp) {
     return excl;
 }
 
+// Score of a routing sort key (the float behind ~orderable(S) in the high word).
+__device__ __forceinline__ double key_score(unsigned long long key) {
+    const uint32_t o = ~(uint32_t)(key >> 32);
+    const uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+    return (double)__uint_as_float(u);
+}
+
+// ---------------------------------------------------------------- mixed widths
+// Rate-distortion allocation over widths {0, 2, 4, 8, 16} ("Technische
+// Samenvatting: RDKV", 2.1-2.2, the Lagrangian of the multiple-choice
+// knapsack). A window's options form a chain of widths: 0, 2, 4, 8, 16 (those
+// the ledger can hold) for a window never quantised, 0, b, 16 for one whose
+// ledger entry has width b. Each chain step a -> b is an upgrade with gain
+// (2^-a - 2^-b) / (cost(b) - cost(a)) * s per byte (float64), s the window's
+// score; upgrades are taken by gain, highest first (lower step, then rank, on
+// a tie), while positive, until the first that does not fit.
+constexpr int kMixClasses = 4;    // never quantised; ledger width 2, 4, 8
+constexpr int kMixTypes = 10;     // (class, step) lists: 4 + 2 + 2 + 2
+
+__device__ __forceinline__ int mix_steps(int ci, int maxP) {
+    return ci == 0 ? 2 + (maxP >= 2) + (maxP >= 4) : 2;
+}
+__device__ __forceinline__ int mix_width(int ci, int idx, int maxP) {
+    if (idx == 0) return 0;
+    if (ci != 0) return idx == 1 ? (2 << (ci - 1)) : 16;
+    return idx < mix_steps(0, maxP) ? (2 << (idx - 1)) : 16;
+}
+__device__ __forceinline__ int64_t mix_cost(const LayerDev &D, int bits) {
+    if (bits == 0) return 0;
+    if (bits == 16) return D.c_fp;
+    return (int64_t)D.w * D.Hkv * 2 * (kHeadDim * bits / 8 + 4 * kGroups);
+}
+__device__ __forceinline__ double exp2_neg(int a) {   // 2^-a, exact
+    return __longlong_as_double((long long)(1023 - a) << 52);
+}
+__device__ __forceinline__ unsigned long long orderable64(double x) {
+    const unsigned long long u = (unsigned long long)__double_as_longlong(x);
+    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+__device__ __forceinline__ int mix_class(int lbits) { return lbits == 0 ? 0 : lbits == 2 ? 1 : lbits == 4 ? 2 : 3; }
+
+// Target tiers of the ranked candidates (s_key[0] the open window, s_key[1 +
+// j] the rest in rank order). The taken upgrades are a prefix of the global
+// order, and along each (class, step) list of windows in rank order the gain
+// does not rise, so an upgrade is taken iff its gain is positive and the cost
+// of the prefix through it fits; that prefix is counted by a binary search in
+// every list. dyn: [upgrades] orderable gains, then [n] rank indices grouped
+// by class.
+__device__ void rd_mixed_targets(const LayerDev &D, const unsigned long long *s_key, uint8_t *s_tgt, int ncand,
+                                 int64_t budget, int64_t wb, int *s_warp, unsigned long long *dyn) {
+    __shared__ int s_coff[kMixClasses + 1], s_toff[kMixTypes + 1], s_tfirst[kMixClasses], s_take[kMixTypes];
+    __shared__ int s_tcls[kMixTypes], s_tstep[kMixTypes], s_ntypes;
+    __shared__ double s_tk[kMixTypes];
+    __shared__ long long s_tcost[kMixTypes];
+    const int tid = threadIdx.x, n = ncand - 1, maxP = D.maxP;
+    if (tid == 0) s_tgt[(int)(s_key[0] & 0xffffffffu)] = QEVICT_TIER_FP;
+    if (n <= 0) {
+        __syncthreads();
+        return;
+    }
+    // ---- group the rest by class, rank order kept within a class
+    const int per = (n + kPlanThreads - 1) / kPlanThreads;
+    const int j0 = tid * per, j1 = min(n, j0 + per);
+    int cnt[kMixClasses] = {0, 0, 0, 0};
+    for (int j = j0; j < j1; ++j) ++cnt[mix_class(D.lbits[wb + (int)(s_key[1 + j] & 0xffffffffu)])];
+    int excl[kMixClasses], tot[kMixClasses];
+#pragma unroll
+    for (int c = 0; c < kMixClasses; ++c) excl[c] = block_scan(cnt[c], &tot[c], s_warp);
+    uint16_t *s_rk = reinterpret_cast<uint16_t *>(dyn + (size_t)mix_steps(0, maxP) * D.Wmax);
+    if (tid == 0) {
+        int off = 0, t = 0;
+        for (int c = 0; c < kMixClasses; ++c) {
+            s_coff[c] = off;
+            off += tot[c];
+        }
+        s_coff[kMixClasses] = off;
+        int toff = 0;
+        for (int c = 0; c < kMixClasses; ++c) {
+            s_tfirst[c] = t;
+            for (int i = 0; i < mix_steps(c, maxP); ++i, ++t) {
+                const int a = mix_width(c, i, maxP), bw = mix_width(c, i + 1, maxP);
+                const int64_t cost = mix_cost(D, bw) - mix_cost(D, a);
+                s_tk[t] = (exp2_neg(a) - exp2_neg(bw)) / (double)cost;
+                s_tcost[t] = cost;
+                s_tcls[t] = c;
+                s_tstep[t] = i;
+                s_toff[t] = toff;
+                s_take[t] = 0;
+                toff += tot[c];
+            }
+        }
+        s_toff[t] = toff;
+        s_ntypes = t;
+    }
+    __syncthreads();
+    {
+        int run[kMixClasses] = {0, 0, 0, 0};
+        for (int j = j0; j < j1; ++j) {
+            const int c = mix_class(D.lbits[wb + (int)(s_key[1 + j] & 0xffffffffu)]);
+            s_rk[s_coff[c] + excl[c] + run[c]++] = (uint16_t)j;
+        }
+    }
+    __syncthreads();
+    const int nt = s_ntypes, U = s_toff[nt];
+    // ---- one gain per upgrade, list by list
+    for (int e = tid; e < U; e += kPlanThreads) {
+        int t = 0;
+        while (e >= s_toff[t + 1]) ++t;
+        const int j = s_rk[s_coff[s_tcls[t]] + e - s_toff[t]];
+        dyn[e] = orderable64(s_tk[t] * key_score(s_key[1 + j]));
+    }
+    __syncthreads();
+    // ---- which upgrades are taken: positive gain and the prefix through it fits
+    const int64_t room = budget - D.c_fp;
+    for (int e = tid; e < U; e += kPlanThreads) {
+        const unsigned long long g = dyn[e];
+        if (g <= 0x8000000000000000ull) continue;   // gain <= 0
+        int t = 0;
+        while (e >= s_toff[t + 1]) ++t;
+        const int step = s_tstep[t];
+        const int j = s_rk[s_coff[s_tcls[t]] + e - s_toff[t]];
+        int64_t prefix = s_tcost[t];
+        for (int t2 = 0; t2 < nt && prefix <= room; ++t2) {
+            const int base = s_toff[t2], len = s_toff[t2 + 1] - base, step2 = s_tstep[t2];
+            const int cbase = s_coff[s_tcls[t2]];
+            int lo = 0, hi = len;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                const unsigned long long g2 = dyn[base + mid];
+                const bool before = g2 > g || (g2 == g && (step2 < step || (step2 == step && s_rk[cbase + mid] < j)));
+                if (before)
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            prefix += (int64_t)lo * s_tcost[t2];
+        }
+        if (prefix <= room) atomicAdd(&s_take[t], 1);
+    }
+    __syncthreads();
+    // ---- each window's width: the steps of its chain taken, in order
+    {
+        int run[kMixClasses] = {0, 0, 0, 0};
+        for (int j = j0; j < j1; ++j) {
+            const int wi = (int)(s_key[1 + j] & 0xffffffffu);
+            const int c = mix_class(D.lbits[wb + wi]);
+            const int q = excl[c] + run[c]++;
+            int st = 0;
+            while (st < mix_steps(c, maxP) && q < s_take[s_tfirst[c] + st]) ++st;
+            const int bits = mix_width(c, st, maxP);
+            s_tgt[wi] = bits == 16 ? QEVICT_TIER_FP
+                        : bits == 8 ? QEVICT_TIER_Q8
+                        : bits == 4 ? QEVICT_TIER_Q4
+                        : bits == 2 ? QEVICT_TIER_Q
+                                    : QEVICT_TIER_E;
+        }
+    }
+    __syncthreads();
+}
+
 // One CTA per sequence. Computes the target tier of every window (by ranking
 // the cumulative scores under the budget, or from explicit tiers), then
 // applies the transitions: free the slots of evicted / demoted windows, take
@@ -195,6 +355,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     __shared__ uint8_t s_old[kPlanMaxW];   // tiers before this plan, for the move's counts
     __shared__ int s_warp[kPlanThreads / 32 + 1];
     __shared__ int s_cnt[8];
+    extern __shared__ unsigned long long s_dyn[];   // the mixed-width route's gains and lists
 
     const int b = blockIdx.x, tid = threadIdx.x;
     const int64_t wb = (int64_t)b * D.Wmax;
@@ -224,7 +385,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     // byte budget at this length: B_t = floor(beta * L * Hkv * d * 4)
     const int64_t budget = (int64_t)floor(D.beta * (double)(length * D.Hkv * kHeadDim * 4));
     const int nfp_budget = (int)floor((D.rho * (double)budget) / (double)D.c_fp);
-    if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD) &&
+    if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD ||
+         a.mode == PLAN_RD_MIXED) &&
         budget < D.c_fp) {
         if (tid == 0) {
             set_status(C, QEVICT_ERR_BUDGET, a.layer, b, (int)length);
@@ -308,7 +470,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         // ---- target tiers
         for (int i = tid; i < nw; i += kPlanThreads) s_tgt[i] = s_cur[i];
         int bad = 0;
-        if (a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD) {
+        if (a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD ||
+            a.mode == PLAN_RD_MIXED) {
             int P = 1;
             while (P < nw) P <<= 1;
             for (int i = tid; i < P; i += kPlanThreads) {
@@ -366,7 +529,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             int ncand;
             block_scan(ncand_local, &ncand, s_warp);
             int n_fp, n_q;
-            if (a.mode == PLAN_RD) {
+            if (a.mode == PLAN_RD_MIXED) {
+                rd_mixed_targets(D, s_key, s_tgt, ncand, budget, wb, s_warp, s_dyn);
+                n_fp = n_q = -1;   // the targets are set
+            } else if (a.mode == PLAN_RD) {
                 // Rate-distortion counts. After the open window (rank 0) come upgrades
                 // E -> INT2 of rank-i window (gain A[i] = alpha s_i, c_q bytes) and INT2 -> FP
                 // (Q[i] = gamma s_i, c_fp - c_q bytes), taken in the merged order of the two
@@ -377,11 +543,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                 // reference computes them.
                 const double alpha = 0.75 / (double)D.c_q;
                 const double gamma = (0.25 - 1.52587890625e-05) / (double)(D.c_fp - D.c_q);
-                auto score_at = [&](int i) {   // score of rank i + 1, back from its sort key
-                    const uint32_t o = ~(uint32_t)(s_key[1 + i] >> 32);
-                    const uint32_t u = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
-                    return (double)__uint_as_float(u);
-                };
+                auto score_at = [&](int i) { return key_score(s_key[1 + i]); };   // score of rank i + 1
                 const int n = ncand - 1;
                 const int64_t room = budget - D.c_fp;
                 int up_local = 0, fp_local = 0;
@@ -419,7 +581,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                 const int64_t rem = budget - (int64_t)n_fp * D.c_fp;
                 n_q = (int)min((int64_t)(ncand - n_fp), rem > 0 ? rem / D.c_q : 0);
             }
-            for (int r = tid; r < ncand; r += kPlanThreads) {
+            for (int r = tid; r < ncand && n_fp >= 0; r += kPlanThreads) {
                 const int wi = (int)(s_key[r] & 0xffffffffu);
                 s_tgt[wi] = r < n_fp ? QEVICT_TIER_FP : (r < n_fp + n_q ? QEVICT_TIER_Q : QEVICT_TIER_E);
             }
@@ -1051,8 +1213,23 @@ cudaError_t launch_append(const LayerDev &L, const CacheDev &C, int layer, const
     return cudaGetLastError();
 }
 
+// Dynamic shared memory of the mixed-width route: one 8-byte gain per chain step
+// of every window (a never-quantised window has the most steps), then one
+// 2-byte rank index per window.
+static size_t mixed_plan_smem(const LayerDev &L) {
+    const int steps = 2 + (L.maxP >= 2) + (L.maxP >= 4);
+    return (size_t)steps * L.Wmax * 8 + (size_t)L.Wmax * 2;
+}
+
 cudaError_t launch_plan(const LayerDev &L, const CacheDev &C, const PlanArgs &a, cudaStream_t s) {
-    plan_kernel<<<L.B, kPlanThreads, 0, s>>>(L, C, a);
+    size_t dyn = 0;
+    if (a.mode == PLAN_RD_MIXED) {
+        static const cudaError_t attr = cudaFuncSetAttribute(
+            plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(4 * kPlanMaxW * 8 + kPlanMaxW * 2));
+        if (attr != cudaSuccess) return attr;
+        dyn = mixed_plan_smem(L);
+    }
+    plan_kernel<<<L.B, kPlanThreads, dyn, s>>>(L, C, a);
     return cudaGetLastError();
 }
 
