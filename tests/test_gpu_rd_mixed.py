@@ -182,3 +182,56 @@ def test_rd_mixed_per_head_cache():
     ro, rm = ref.decode(O.queries_to_units(q.float().numpy(), Hkv), accumulate=False)
     close(out.cpu().numpy(), ro.reshape(B, Hq, 128), "attention output")
     close(mass.cpu().numpy(), rm.reshape(B, Hq, -1), "window mass")
+
+
+def test_rd_mixed_errors_leave_the_tables():
+    """A non-finite score among the candidates sets DEVICE and moves nothing; a
+    budget that cannot hold the open window is BUDGET on the host."""
+    B, Hq, Hkv, w, L = 1, 8, 2, 32, 256
+    W = L // w
+    cache, ref = make_wide(B, Hq, Hkv, w, L, 8, 0.5, seed=76)
+    before = [x.clone() for x in cache.tables(0)]
+    bad = torch.full((B, W), 0.1)
+    bad[0, 2] = float("inf")
+    cache.route_rd_mixed(0, scores_override=bad.cuda())
+    assert binding.STATUS[cache.status()] == "DEVICE"
+    cache.clear_status()
+    for x, y in zip(before, cache.tables(0)):
+        assert torch.equal(x, y)
+    small = binding.TieredCache(1, 1, 8, 2, 32, 64, budget_frac=0.05, max_ledger_bits=8)
+    small.append(0, *[x.cuda() for x in synth.kv_tokens(0, 0, 1, 0, 64, 2, 128)])
+    with pytest.raises(binding.QevictError) as ei:
+        small.route_rd_mixed(0)
+    assert ei.value.name == "BUDGET"
+
+
+@pytest.mark.parametrize("w,bits", [(128, 8), (128, 4), (16, 8)])
+def test_rd_mixed_window_sizes(w, bits):
+    B, Hq, Hkv, L, beta = 2, 16, 4, 4096 + 40, 0.12
+    W = -(-L // w)
+    cache, ref = make_wide(B, Hq, Hkv, w, L, bits, beta, seed=77 + w)
+    route_both(cache, ref, synth.zipf_scores(77, w, B, W), bits)
+    check_decode(cache, 0, ref, synth.queries(77, 0, 0, B, Hq, 128))
+
+
+def test_rd_mixed_second_event_moves_between_widths():
+    """Two events on different scores: windows quantised by the first keep their
+    width, are promoted back to bf16 or evicted by the second; the ledger is
+    reused, never rewritten."""
+    B, Hq, Hkv, w, L, beta = 2, 16, 4, 32, 3072, 0.15
+    W = L // w
+    cache, ref = make_wide(B, Hq, Hkv, w, L, 8, beta, seed=78)
+    route_both(cache, ref, synth.zipf_scores(78, 0, B, W), 8)
+    first = ref.tiers().copy()
+    route_both(cache, ref, synth.zipf_scores(79, 0, B, W), 8)
+    second = ref.tiers()
+    width = {O.TIER_Q: 2, O.TIER_Q4: 4, O.TIER_Q8: 8}
+    moved = 0
+    for b in range(B):
+        for wi in range(W):
+            if first[b, wi] in width and second[b, wi] in width:
+                assert width[first[b, wi]] == width[second[b, wi]]
+            moved += first[b, wi] != second[b, wi]
+    assert moved > 0
+    assert np.all(cache.tables(0)[3].numpy() <= 1), "a ledger entry was written twice"
+    check_decode(cache, 0, ref, synth.queries(78, 0, 0, B, Hq, 128))
