@@ -96,3 +96,104 @@ def test_promote_without_bf16_rounding_is_caught(monkeypatch):
     monkeypatch.setattr(QO, "dequant_promote", bad)
     monkeypatch.setattr(O, "dequant_promote", bad)
     assert _fails(P.test_promote_dequant_single_rounding)
+
+
+# ---- the 4- and 8-bit widths and the allocation over {0, 2, 4, 8, 16}
+
+def _mixed_widths_variant(k_of, stop):
+    """oracle.rd_mixed_widths with the per-byte gain factor and the stop rule
+    replaced (for planting mistakes)."""
+    def fn(S_ranked, chains, L, w, Hkv, d, beta):
+        c_fp = O.width_cost(w, Hkv, d, 16)
+        Bt = O.budget_bytes(L, Hkv, d, beta)
+        ups = []
+        for r, (s, ch) in enumerate(zip(S_ranked, chains)):
+            for i in range(len(ch) - 1):
+                a, b = ch[i], ch[i + 1]
+                cost = O.width_cost(w, Hkv, d, b) - O.width_cost(w, Hkv, d, a)
+                ups.append((k_of(a, b, cost) * float(s), i, r, cost))
+        ups.sort(key=lambda u: (-u[0], u[1], u[2]))
+        used, steps = c_fp, [0] * len(chains)
+        for gain, i, r, cost in ups:
+            if gain <= 0.0:
+                break
+            if used + cost > Bt:
+                if stop:
+                    break
+                continue
+            if steps[r] != i:
+                continue
+            used += cost
+            steps[r] += 1
+        return [ch[st] for ch, st in zip(chains, steps)]
+    return fn
+
+
+def _patch_both(monkeypatch, name, fn):
+    monkeypatch.setattr(QO, name, fn)
+    monkeypatch.setattr(O, name, fn)
+
+
+def _quantiser_variant(levels_of):
+    """oracle.quantize_groups (finite inputs) with the level count replaced."""
+    def fn(x, bits=2):
+        x = np.asarray(x, np.float32)
+        levels = levels_of(bits)
+        mn, mx = x.min(axis=-1), x.max(axis=-1)
+        mn16 = QO.half_round(mn)
+        s16 = QO.half_round(((mx - mn).astype(np.float32) / np.float32(levels)).astype(np.float32))
+        s, m = s16.astype(np.float32), mn16.astype(np.float32)
+        den = np.where(s == 0, np.float32(1), s)
+        q = np.rint(((x - m[..., None]).astype(np.float32) / den[..., None]).astype(np.float32))
+        codes = np.clip(np.where(s[..., None] == 0, 0, q), 0, levels).astype(np.uint8)
+        return codes, s16, mn16, np.zeros(mn.shape, bool)
+    return fn
+
+
+def test_mutant_harnesses_pass_without_a_plant(monkeypatch):
+    """Control: the re-implementations the plants below start from pass the pins."""
+    _patch_both(monkeypatch, "quantize_groups", _quantiser_variant(lambda b: (1 << b) - 1))
+    P.test_wide_quantiser_exact_grid_and_nearest_level(4)
+    P.test_wide_quantiser_exact_grid_and_nearest_level(8)
+    _patch_both(monkeypatch, "rd_mixed_widths",
+                _mixed_widths_variant(lambda a, b, c: (2.0 ** -a - 2.0 ** -b) / c, True))
+    P.test_rd_mixed_is_a_lagrangian_solution()
+    P.test_rd_mixed_hand_derived()
+    P.test_rd_mixed_route_keeps_ledger_widths_and_is_lagrangian()
+
+
+def test_wide_quantiser_with_2_to_the_b_levels_is_caught(monkeypatch):
+    # plant: 2^b levels instead of 2^b - 1
+    _patch_both(monkeypatch, "quantize_groups", _quantiser_variant(lambda b: 1 << b))
+    assert _fails(P.test_wide_quantiser_exact_grid_and_nearest_level, 4)
+    assert _fails(P.test_wide_quantiser_exact_grid_and_nearest_level, 8)
+
+
+def test_mixed_gain_without_the_upper_width_term_is_caught(monkeypatch):
+    # plant: the distortion removed by a -> b taken as 2^-a (the 2^-b left in is dropped)
+    _patch_both(monkeypatch, "rd_mixed_widths", _mixed_widths_variant(lambda a, b, c: 2.0 ** -a / c, True))
+    assert _fails(P.test_rd_mixed_is_a_lagrangian_solution)
+
+
+def test_mixed_greedy_that_skips_instead_of_stopping_is_caught(monkeypatch):
+    # plant: an upgrade that does not fit is skipped and later, cheaper ones still taken
+    _patch_both(monkeypatch, "rd_mixed_widths",
+                _mixed_widths_variant(lambda a, b, c: (2.0 ** -a - 2.0 ** -b) / c, False))
+    assert _fails(P.test_rd_mixed_is_a_lagrangian_solution)
+
+
+def test_mixed_route_ignoring_ledger_widths_is_caught(monkeypatch):
+    orig = QO.rd_mixed_widths
+
+    def free_chains(S_ranked, chains, L, w, Hkv, d, beta):
+        # plant: every window gets the chain of a window never quantised
+        return orig(S_ranked, [[0, 2, 4, 8, 16]] * len(chains), L, w, Hkv, d, beta)
+    _patch_both(monkeypatch, "rd_mixed_widths", free_chains)
+    assert _fails(P.test_rd_mixed_route_keeps_ledger_widths_and_is_lagrangian)
+
+
+def test_width_cost_without_meta_is_caught(monkeypatch):
+    # plant: the fp16 scale and minimum of each group left out of a quantised window's bytes
+    bad = lambda w, Hkv, d, bits: 0 if bits == 0 else (w * Hkv * d * 4 if bits == 16 else w * Hkv * 2 * (d * bits // 8))
+    _patch_both(monkeypatch, "width_cost", bad)
+    assert _fails(P.test_rd_mixed_hand_derived)

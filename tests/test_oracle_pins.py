@@ -973,3 +973,47 @@ def test_rd_mixed_route_on_int2_widths_is_route_rd():
             for x, y in zip(caches[0].win[b], caches[1].win[b]):
                 assert (x.ledger is None) == (y.ledger is None) and x.ledger_writes == y.ledger_writes
     assert caches[0].stats == caches[1].stats and caches[1].stats["ledger_reuses"] > 0
+
+
+def test_rd_mixed_route_keeps_ledger_widths_and_is_lagrangian():
+    """A routing event on a cache whose windows were quantised at 2, 4 and 8 bits
+    and promoted back: every window with a ledger entry ends at 0, its ledger
+    width or 16; the visible bytes fit the budget; and every candidate's width
+    minimises s 2^-b + lambda cost(b) over its own chain at the multiplier of
+    the first refused upgrade (the Lagrangian condition, written out here)."""
+    B, Hq, Hkv, w, d = 2, 4, 1, 16, 128
+    W = 24
+    L = W * w
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    t0 = rng.choice([O.TIER_FP, O.TIER_Q, O.TIER_Q4, O.TIER_Q8], size=(B, W)).astype(np.uint8)
+    t0[:, -1] = O.TIER_FP
+    for beta in (0.12, 0.3):
+        c = O.OracleCache(B, Hq, Hkv, d, w, beta=beta)
+        c.prefill(k, v, tiers=t0)
+        c.set_tiers(np.where(t0 == O.TIER_E, O.TIER_E, O.TIER_FP).astype(np.uint8))
+        lb = [[c.win[b][i].ledger_bits if c.win[b][i].ledger is not None else 0 for i in range(W)] for b in range(B)]
+        S = rng.pareto(1.2, (B, W))
+        O.route_rd_mixed(c, scores_override=S, max_bits=8)
+        t = c.tiers()
+        width = {O.TIER_FP: 16, O.TIER_Q: 2, O.TIER_Q4: 4, O.TIER_Q8: 8, O.TIER_E: 0}
+        cost = lambda x: O.width_cost(w, Hkv, d, x)
+        for b in range(B):
+            got = [width[int(x)] for x in t[b]]
+            assert got[-1] == 16
+            for i in range(W):
+                if lb[b][i]:
+                    assert got[i] in (0, lb[b][i], 16), (b, i, got[i], lb[b][i])
+            assert sum(cost(x) for x in got) <= O.budget_bytes(L, Hkv, d, beta)
+            chains = [[0, 2, 4, 8, 16] if lb[b][i] == 0 else [0, lb[b][i], 16] for i in range(W - 1)]
+            refused = []
+            for i, ch in enumerate(chains):
+                j = ch.index(got[i])
+                if j + 1 < len(ch):
+                    a, nb = ch[j], ch[j + 1]
+                    refused.append((2.0 ** -a - 2.0 ** -nb) / (cost(nb) - cost(a)) * S[b, i])
+            lam = max(refused) if refused else 0.0
+            for i, ch in enumerate(chains):
+                obj = {x: S[b, i] * 2.0 ** -x + lam * cost(x) for x in ch}
+                assert obj[got[i]] <= min(obj.values()) * (1 + 1e-12) + 1e-300, (beta, b, i, ch, got[i])
