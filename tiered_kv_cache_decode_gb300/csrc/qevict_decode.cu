@@ -1067,21 +1067,20 @@ cudaError_t prepare_one(int optin) {
 // record how many of its CTAs fit on one SM (called at cache creation,
 // outside any stream capture).
 cudaError_t prepare_decode() {
-    static bool done = false;
-    if (done) return cudaSuccess;
-    int dev = 0, optin = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess) e = prepare_one<1>(optin);
-    if (e == cudaSuccess) e = prepare_one<2>(optin);
-    if (e == cudaSuccess) e = prepare_one<3>(optin);
-    if (e == cudaSuccess) e = prepare_one<4>(optin);
-    if (e == cudaSuccess) e = prepare_one<5>(optin);
-    if (e == cudaSuccess) e = prepare_one<6>(optin);
-    if (e == cudaSuccess) e = prepare_one<7>(optin);
-    if (e == cudaSuccess) e = prepare_one<8>(optin);
-    if (e == cudaSuccess) done = true;
-    return e;
+    return once_per_device(0, []() {
+        int dev = 0, optin = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e == cudaSuccess) e = prepare_one<1>(optin);
+        if (e == cudaSuccess) e = prepare_one<2>(optin);
+        if (e == cudaSuccess) e = prepare_one<3>(optin);
+        if (e == cudaSuccess) e = prepare_one<4>(optin);
+        if (e == cudaSuccess) e = prepare_one<5>(optin);
+        if (e == cudaSuccess) e = prepare_one<6>(optin);
+        if (e == cudaSuccess) e = prepare_one<7>(optin);
+        if (e == cudaSuccess) e = prepare_one<8>(optin);
+        return e;
+    });
 }
 
 // Splits per (sequence, KV head): as many as keep the whole grid resident at

@@ -278,12 +278,10 @@ cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, cons
     uint32_t *cnt = S.bar;   // [B*Hkv][2]; the kernel counts on entry 2 * bk
     // two CTAs per SM, spread over the (sequence, KV head) pairs
     auto grid_for = [&](const void *fn) {
-        static bool attr[kMaxG + 1] = {};
-        if (!attr[L.G]) {
-            const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFmmSmem);
-            if (e != cudaSuccess) return -1;
-            attr[L.G] = true;
-        }
+        const cudaError_t e = once_per_device(L.G, [fn]() {
+            return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFmmSmem);
+        });
+        if (e != cudaSuccess) return -1;
         const int splits = (2 * num_sms + pairs - 1) / pairs;
         return max(1, min(splits, min(256, 2 * L.Wmax / 3)));
     };

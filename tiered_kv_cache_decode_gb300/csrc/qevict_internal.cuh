@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/qevict.h"
 
 namespace qevict {
@@ -168,6 +170,27 @@ cudaError_t launch_global_select(const GlobalArgs &g, const CacheDev &C, int seq
 cudaError_t launch_set_scores(const LayerDev &L, const float *scores, int n_win, cudaStream_t s);
 cudaError_t launch_append(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *k,
                           const __nv_bfloat16 *v, int n_new, cudaStream_t s);
+// Runs setup() once per (call site, key, current device) in the process, under
+// a lock; a set-up that failed runs again on the next call. Kernel
+// attributes such as the dynamic shared-memory limit belong to a device's
+// context, so each device the library meets gets its own set-up.
+constexpr int kOnceDevices = 64;
+constexpr int kOnceKeys = 16;
+template <class F>
+inline cudaError_t once_per_device(int key, F &&setup) {
+    static std::mutex mu;
+    static bool done[kOnceKeys][kOnceDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 0 || dev >= kOnceDevices || key < 0 || key >= kOnceKeys) return setup();
+    if (done[key][dev]) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess) done[key][dev] = true;
+    return e;
+}
+
 cudaError_t launch_plan(const LayerDev &L, const CacheDev &C, const PlanArgs &a, cudaStream_t s);
 cudaError_t launch_quantize(const LayerDev &L, const CacheDev &C, int layer, const __nv_bfloat16 *k_ext,
                             const __nv_bfloat16 *v_ext, int64_t ext_len, int max_entries,

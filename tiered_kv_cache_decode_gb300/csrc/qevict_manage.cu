@@ -1224,8 +1224,10 @@ static size_t mixed_plan_smem(const LayerDev &L) {
 cudaError_t launch_plan(const LayerDev &L, const CacheDev &C, const PlanArgs &a, cudaStream_t s) {
     size_t dyn = 0;
     if (a.mode == PLAN_RD_MIXED) {
-        static const cudaError_t attr = cudaFuncSetAttribute(
-            plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(4 * kPlanMaxW * 8 + kPlanMaxW * 2));
+        const cudaError_t attr = once_per_device(0, []() {
+            return cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)(4 * kPlanMaxW * 8 + kPlanMaxW * 2));
+        });
         if (attr != cudaSuccess) return attr;
         dyn = mixed_plan_smem(L);
     }
