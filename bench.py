@@ -772,7 +772,7 @@ def run_native(args, rank, world, local_rank):
         spent = max(r[1] for r in out)
         line["cpu_baseline"] = {"value": round(nb / spent / 1e9, 4), "unit": "GB/s", "cores": nw, "kind": "oracle",
                                 # each worker is one single-threaded process: its rate is the one-core figure
-                                "one_core_value": round(sum(r[0] / r[1] for r in out) / len(out) / 1e9, 4),
+                                "one_core_value": round(sum(r[0] / r[1] for r in out if r[1] > 0) / len(out) / 1e9, 4),
                                 "sample": f"{nw} layers of the workload, one per single-threaded process, "
                                           f"{sum(r[2] for r in out)} decode steps in total (append + fp64 attention "
                                           f"+ score accumulation) after a 32K-token prefill"}
