@@ -166,6 +166,21 @@ __device__ __forceinline__ uint32_t codes2(uint32_t x) {
 // the offsets' contribution is taken out through the accumulator's start value.
 __device__ __forceinline__ uint32_t kcodes_lo(uint32_t x) { return (x & 0x00030003u) | 0x43004300u; }
 __device__ __forceinline__ uint32_t kcodes_hi(uint32_t x) { return (x & 0x000C000Cu) | 0x43004300u; }
+// The same for 4-bit codes c = c0 + 4 c1 held in two 2-bit planes (x0: c0, x1:
+// c1, at the same bit positions): 128 + c and 128 + 4 c, exact in bf16.
+__device__ __forceinline__ uint32_t kcodes4_lo(uint32_t x0, uint32_t x1) {
+    return (x0 & 0x00030003u) | ((x1 & 0x00030003u) << 2) | 0x43004300u;
+}
+__device__ __forceinline__ uint32_t kcodes4_hi(uint32_t x0, uint32_t x1) {
+    return (x0 & 0x000C000Cu) | ((x1 & 0x000C000Cu) << 2) | 0x43004300u;
+}
+// Two 4-bit codes (bits 1:0 and 17:16 of each plane word) as an exact bf16 pair.
+__device__ __forceinline__ uint32_t codes4(uint32_t x0, uint32_t x1) {
+    uint32_t r = kcodes4_lo(x0, x1);
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r);
+    v = __hsub2(v, __floats2bfloat162_rn(128.f, 128.f));
+    return *reinterpret_cast<uint32_t *>(&v);
+}
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -526,8 +541,81 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma(o[mt], a0, a1, a2, a3, b0h, b1h);
                 mma(o[mt], a0, a1, a2, a3, b0l, b1l);
             }
+        } else if (kWide && P == 2) {
+            // ---------------- INT4 unit: the two code planes are joined in registers
+            // into 4-bit codes (exact in bf16 as 128 + c and 128 + 4 c), then the
+            // INT2 unit's arithmetic runs once: same query fragments, same offset
+            // correction, 4-bit codes in place of 2-bit ones.
+            const uint32_t kc = base, km = base + qtile_kmeta(2), vc = base + qtile_vcodes(2),
+                           vm = base + qtile_vmeta(2);
+            const int tA = (g & 1) ? g + 7 : g;
+            const int tB = (g & 1) ? g + 8 : g + 1;
+            uint4 kmeta[4];
+            kmeta[0] = lds128(km + (2 * t) * 16);
+            kmeta[1] = lds128(km + (2 * t + 8) * 16);
+            kmeta[2] = lds128(km + (2 * t + 1) * 16);
+            kmeta[3] = lds128(km + (2 * t + 9) * 16);
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int grp = 0; grp < kGroups; ++grp) {
+                const uint32_t kp = kc + (grp >= 2 ? 16 : 0);
+                const uint4 kA0 = lds128(kp + tA * 32), kB0 = lds128(kp + tB * 32);
+                const uint4 kA1 = lds128(kp + 512 + tA * 32), kB1 = lds128(kp + 512 + tB * 32);
+                float c0[4], c1[4];
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int ks = 2 * grp + kk;
+                    const uint32_t xa0 = pick(kA0, ks & 3) >> (4 * t), xa1 = pick(kA1, ks & 3) >> (4 * t);
+                    const uint32_t xb0 = pick(kB0, ks & 3) >> (4 * t), xb1 = pick(kB1, ks & 3) >> (4 * t);
+                    const uint2 aq = s_qf[(8 + ks) * 32 + lane];
+                    if (kk == 0) {   // start from minus the offsets' share (rows g; rows g + 8 are padding)
+                        mma_c(c0, aq.x, 0u, aq.y, 0u, kcodes4_lo(xa0, xa1), kcodes4_hi(xa0, xa1), qbias[grp], 0.f);
+                        mma_c(c1, aq.x, 0u, aq.y, 0u, kcodes4_lo(xb0, xb1), kcodes4_hi(xb0, xb1), qbias[grp], 0.f);
+                    } else {
+                        mma(c0, aq.x, 0u, aq.y, 0u, kcodes4_lo(xa0, xa1), kcodes4_hi(xa0, xa1));
+                        mma(c1, aq.x, 0u, aq.y, 0u, kcodes4_lo(xb0, xb1), kcodes4_hi(xb0, xb1));
+                    }
+                }
+                const float acc[4] = {c0[0], c0[1], c1[0], c1[1]};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 sm = h2f(pick(kmeta[i], grp));   // .x scale, .y min
+                    x[i] = fmaf(sm.x, acc[i], fmaf(sm.y, qsum[grp], x[i]));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[i] *= qk_scale;
+            softmax4(x);
+            const int vtok[4] = {2 * t, 2 * t + 8, 2 * t + 1, 2 * t + 9};
+#pragma unroll
+            for (int grp = 0; grp < kGroups; ++grp) {
+                const uint4 vv0 = lds128(vc + g * 64 + grp * 16), vv1 = lds128(vc + 512 + g * 64 + grp * 16);
+                uint32_t vmg[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vmg[i] = lds32(vm + vtok[i] * 16 + grp * 4);
+                float val[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 sm = h2f(vmg[i]);
+                    val[i] = x[i] * sm.x;
+                    minacc[grp] = fmaf(x[i], sm.y, minacc[grp]);
+                }
+                uint32_t b0h, b0l, b1h, b1l;
+                split2(val[0], val[1], b0h, b0l);
+                split2(val[2], val[3], b1h, b1l);
+#pragma unroll
+                for (int mm = 0; mm < 2; ++mm) {
+                    const int mt = 2 * grp + mm;
+                    const uint32_t x0 = pick(vv0, 2 * mm) >> (4 * t), x1 = pick(vv0, 2 * mm + 1) >> (4 * t);
+                    const uint32_t y0 = pick(vv1, 2 * mm) >> (4 * t), y1 = pick(vv1, 2 * mm + 1) >> (4 * t);
+                    const uint32_t a0 = codes4(x0, y0), a1 = codes4(x1, y1), a2 = codes4(x0 >> 2, y0 >> 2),
+                                   a3 = codes4(x1 >> 2, y1 >> 2);
+                    mma(o[mt], a0, a1, a2, a3, b0h, b1h);
+                    mma(o[mt], a0, a1, a2, a3, b0l, b1l);
+                }
+            }
         } else if (kWide && P > 1) {
-            // ---------------- INT4 / INT8 unit: P planes of 2-bit codes, code = sum_p 4^p c_p.
+            // ---------------- INT8 unit: P planes of 2-bit codes, code = sum_p 4^p c_p.
             // Each plane goes through the INT2 arithmetic with exact codes (no offset) and
             // plane p weighted by 4^p on the query (K) and on P.scale (V): exact scalings.
             const uint32_t kc = base, km = base + qtile_kmeta(P), vc = base + qtile_vcodes(P),
