@@ -615,11 +615,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (kWide && P > 1) {
-            // ---------------- INT8 unit: P planes of 2-bit codes, code = sum_p 4^p c_p.
-            // Each plane goes through the INT2 arithmetic with exact codes (no offset) and
-            // plane p weighted by 4^p on the query (K) and on P.scale (V): exact scalings.
-            const uint32_t kc = base, km = base + qtile_kmeta(P), vc = base + qtile_vcodes(P),
-                           vm = base + qtile_vmeta(P);
+            // ---------------- INT8 unit: four 2-bit planes, code = c0 + 4 c1 + 16 (c2 + 4 c3).
+            // The planes are joined in pairs into two 4-bit nibbles (exact in bf16), and each
+            // nibble goes through the INT2 arithmetic with exact codes (no offset), the high
+            // one weighted by 16 on the query (K) and on P.scale (V): exact scalings.
+            const uint32_t kc = base, km = base + qtile_kmeta(4), vc = base + qtile_vcodes(4),
+                           vm = base + qtile_vmeta(4);
             const int tA = (g & 1) ? g + 7 : g;
             const int tB = (g & 1) ? g + 8 : g + 1;
             uint4 kmeta[4];
@@ -631,23 +632,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int grp = 0; grp < kGroups; ++grp) {
                 float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int p = 0; p < P; ++p) {
-                    const uint32_t kp = kc + 512 * p + (grp >= 2 ? 16 : 0);
-                    const uint4 kA = lds128(kp + tA * 32), kB = lds128(kp + tB * 32);
-                    const __nv_bfloat162 w4 = __float2bfloat162_rn((float)(1 << (2 * p)));
+#pragma unroll 1
+                for (int pp = 0; pp < 2; ++pp) {
+                    const uint32_t kp = kc + 1024 * pp + (grp >= 2 ? 16 : 0);   // planes 2 pp, 2 pp + 1
+                    const uint4 kA0 = lds128(kp + tA * 32), kB0 = lds128(kp + tB * 32);
+                    const uint4 kA1 = lds128(kp + 512 + tA * 32), kB1 = lds128(kp + 512 + tB * 32);
+                    const __nv_bfloat162 w4 = __float2bfloat162_rn(pp ? 16.f : 1.f);
 #pragma unroll
                     for (int kk = 0; kk < 2; ++kk) {
                         const int ks = 2 * grp + kk;
-                        const uint32_t xa = pick(kA, ks & 3) >> (4 * t);
-                        const uint32_t xb = pick(kB, ks & 3) >> (4 * t);
+                        const uint32_t xa0 = pick(kA0, ks & 3) >> (4 * t), xa1 = pick(kA1, ks & 3) >> (4 * t);
+                        const uint32_t xb0 = pick(kB0, ks & 3) >> (4 * t), xb1 = pick(kB1, ks & 3) >> (4 * t);
                         const uint2 nq = s_qf[ks * 32 + lane];   // natural (q[2t], q[2t+1]), (q[2t+8], q[2t+9])
                         uint32_t a0 = __byte_perm(nq.x, nq.y, 0x5410), a2 = __byte_perm(nq.x, nq.y, 0x7632);
                         __nv_bfloat162 v0 = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a0), w4);
                         __nv_bfloat162 v2 = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&a2), w4);
                         a0 = *reinterpret_cast<uint32_t *>(&v0);
                         a2 = *reinterpret_cast<uint32_t *>(&v2);
-                        mma(c0, a0, 0u, a2, 0u, codes2(xa), codes2(xa >> 2));
-                        mma(c1, a0, 0u, a2, 0u, codes2(xb), codes2(xb >> 2));
+                        mma(c0, a0, 0u, a2, 0u, codes4(xa0, xa1), codes4(xa0 >> 2, xa1 >> 2));
+                        mma(c1, a0, 0u, a2, 0u, codes4(xb0, xb1), codes4(xb0 >> 2, xb1 >> 2));
                     }
                 }
                 const float acc[4] = {c0[0], c0[1], c1[0], c1[1]};
@@ -676,9 +679,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t b0h, b0l, b1h, b1l;
                 split2(val[0], val[1], b0h, b0l);
                 split2(val[2], val[3], b1h, b1l);
-                for (int p = 0; p < P; ++p) {
-                    const uint4 vv = lds128(vc + 512 * p + g * 64 + grp * 16);
-                    const __nv_bfloat162 w4 = __float2bfloat162_rn((float)(1 << (2 * p)));
+#pragma unroll 1
+                for (int pp = 0; pp < 2; ++pp) {
+                    const uint4 vv0 = lds128(vc + 1024 * pp + g * 64 + grp * 16);
+                    const uint4 vv1 = lds128(vc + 1024 * pp + 512 + g * 64 + grp * 16);
+                    const __nv_bfloat162 w4 = __float2bfloat162_rn(pp ? 16.f : 1.f);
                     uint32_t sc[4] = {b0h, b1h, b0l, b1l};
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
@@ -688,8 +693,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int mm = 0; mm < 2; ++mm) {
                         const int mt = 2 * grp + mm;
-                        const uint32_t x0 = pick(vv, 2 * mm) >> (4 * t), x1 = pick(vv, 2 * mm + 1) >> (4 * t);
-                        const uint32_t a0 = codes2(x0), a1 = codes2(x1), a2 = codes2(x0 >> 2), a3 = codes2(x1 >> 2);
+                        const uint32_t x0 = pick(vv0, 2 * mm) >> (4 * t), x1 = pick(vv0, 2 * mm + 1) >> (4 * t);
+                        const uint32_t y0 = pick(vv1, 2 * mm) >> (4 * t), y1 = pick(vv1, 2 * mm + 1) >> (4 * t);
+                        const uint32_t a0 = codes4(x0, y0), a1 = codes4(x1, y1), a2 = codes4(x0 >> 2, y0 >> 2),
+                                       a3 = codes4(x1 >> 2, y1 >> 2);
                         mma(o[mt], a0, a1, a2, a3, sc[0], sc[1]);
                         mma(o[mt], a0, a1, a2, a3, sc[2], sc[3]);
                     }
