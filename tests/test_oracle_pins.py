@@ -1017,3 +1017,31 @@ def test_rd_mixed_route_keeps_ledger_widths_and_is_lagrangian():
             for i, ch in enumerate(chains):
                 obj = {x: S[b, i] * 2.0 ** -x + lam * cost(x) for x in ch}
                 assert obj[got[i]] <= min(obj.values()) * (1 + 1e-12) + 1e-300, (beta, b, i, ch, got[i])
+
+
+def test_rd_mixed_route_with_the_last_window_evicted_keeps_the_top_candidate():
+    """A full last window that was evicted is no candidate: both rate-distortion
+    routes then keep their first-ranked candidate at full precision, and on
+    INT2 widths they agree."""
+    B, Hq, Hkv, w, d = 1, 4, 1, 16, 128
+    W = 12
+    L = W * w
+    rng = np.random.default_rng(22)
+    k = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, L, Hkv, d)).astype(np.float32)
+    t0 = np.zeros((B, W), np.uint8)
+    t0[0, -1] = O.TIER_E
+    S = rng.pareto(1.3, (B, W))
+    caches = []
+    for mixed in (False, True):
+        c = O.OracleCache(B, Hq, Hkv, d, w, beta=0.3)
+        c.prefill(k, v, tiers=t0)
+        if mixed:
+            O.route_rd_mixed(c, scores_override=S, max_bits=2)
+        else:
+            O.route_rd(c, scores_override=S)
+        caches.append(c)
+    t = caches[1].tiers()[0]
+    top = max(range(W - 1), key=lambda i: (S[0, i], -i))
+    assert t[top] == O.TIER_FP and t[-1] == O.TIER_E
+    assert np.array_equal(caches[0].tiers(), caches[1].tiers())
