@@ -1045,3 +1045,17 @@ def test_rd_mixed_route_with_the_last_window_evicted_keeps_the_top_candidate():
     top = max(range(W - 1), key=lambda i: (S[0, i], -i))
     assert t[top] == O.TIER_FP and t[-1] == O.TIER_E
     assert np.array_equal(caches[0].tiers(), caches[1].tiers())
+
+
+def test_rate_distortion_routes_on_an_all_evicted_layer_move_nothing():
+    """Every window evicted (the last one full): no candidates, nothing moves."""
+    B, Hq, Hkv, w, d, W = 1, 4, 1, 16, 128, 6
+    rng = np.random.default_rng(23)
+    k = rng.standard_normal((B, W * w, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, W * w, Hkv, d)).astype(np.float32)
+    for route in (O.route_rd, lambda c, scores_override: O.route_rd_mixed(c, scores_override, max_bits=8)):
+        c = O.OracleCache(B, Hq, Hkv, d, w, beta=0.5)
+        c.prefill(k, v, tiers=np.full((B, W), O.TIER_E, np.uint8))
+        route(c, scores_override=rng.random((B, W)))
+        assert np.all(c.tiers() == O.TIER_E)
+        assert np.all(c.last_counts == 0)

@@ -237,7 +237,7 @@ __device__ void rd_mixed_targets(const LayerDev &D, const unsigned long long *s_
     __shared__ double s_tk[kMixTypes];
     __shared__ long long s_tcost[kMixTypes];
     const int tid = threadIdx.x, n = ncand - 1, maxP = D.maxP;
-    if (tid == 0) s_tgt[(int)(s_key[0] & 0xffffffffu)] = QEVICT_TIER_FP;
+    if (tid == 0 && ncand > 0) s_tgt[(int)(s_key[0] & 0xffffffffu)] = QEVICT_TIER_FP;   // no candidate: key 0 is unset
     if (n <= 0) {
         __syncthreads();
         return;
