@@ -480,9 +480,12 @@ int64_t qevict_length(const qevict_cache *cache, int32_t layer);
  * be current (INVALID_ARG otherwise).
  *
  * Set-up: the first call on a device, with that device current, looks up the
- * array's address and clears it (the arrival counters in it must start at
- * zero; each launch leaves them at zero). That first call synchronises
- * the device, so make it before any stream capture begins.
+ * array's address and clears it. That first call synchronises the device, so
+ * make it before any stream capture begins. Where the counters, split
+ * records and partials lie in the array depends on the cache's shape, so
+ * every call clears that part of the array on `stream` before its launch
+ * (cudaMemsetAsync, which allocates nothing); calls on caches of different
+ * shapes can therefore follow one another on a stream.
  *
  * One array serves every cache and stream on a device: calls whose kernels
  * can overlap (other streams, other host threads, other caches) race on it

@@ -83,3 +83,26 @@ def test_static_scratch_rejects_a_cache_that_needs_more():
     torch.cuda.synchronize()
     assert cache.status() == 0
     assert torch.isfinite(out).all()
+
+
+def test_static_scratch_across_cache_shapes():
+    """Caches of different (sequences x KV heads) one after another on one
+    stream: the array's counters, records and partials sit at shape-dependent
+    offsets, so a call must not take what a call on another cache left there."""
+    caches = {shape: _routed_cache(*shape, seed=14) for shape in [(1, 32, 8, 64, 4096, 0.2),
+                                                                   (8, 32, 8, 64, 2048, 0.2)]}
+    order = [(1, 32, 8, 64, 4096, 0.2), (8, 32, 8, 64, 2048, 0.2), (1, 32, 8, 64, 4096, 0.2),
+             (8, 32, 8, 64, 2048, 0.2)]
+    for i, shape in enumerate(order):
+        cache = caches[shape]
+        B, Hq = shape[0], shape[1]
+        q = synth.queries(14, 0, i, B, Hq, 128).cuda()
+        ref_out, ref_mass = cache.decode(0, q, accumulate=False)
+        for call in range(2):
+            out = torch.full((B, Hq, 128), float("nan"), dtype=torch.float32, device="cuda")
+            mass = torch.full_like(ref_mass, float("nan"))
+            cache.decode_static_scratch(0, q, out, mass, accumulate=False)
+            torch.cuda.synchronize()
+            assert cache.status() == 0, cache.last_error()
+            close(out.cpu().numpy(), ref_out.cpu().numpy(), f"output, cache {shape}, call {call}")
+            close(mass.cpu().numpy(), ref_mass.cpu().numpy(), f"mass, cache {shape}, call {call}")

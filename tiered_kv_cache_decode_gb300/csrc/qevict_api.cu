@@ -910,10 +910,13 @@ void *g_static_ptr[kStaticMaxDevices];
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Scratch layout of one call: counters first (the arrival counts must start
-// at zero), the tagged split records (fixed stride, so that every cache maps a
-// (sequence, KV head, split) to the same words), split partials for `splits`
-// splits, and the window statistics.
+// Scratch layout of one call: counters first, the tagged split records, split
+// partials for `splits` splits, and the window statistics. The offsets depend
+// on the cache's shape, so one cache's counters can lie on another's records:
+// every call therefore clears everything before the window statistics on its
+// stream first (a memset, which allocates nothing). After the clear the
+// record generation is 0, so the launch's tag is 1 and no word left by an
+// earlier call carries it.
 struct StaticLayout {
     size_t o_ab, o_bar, o_rec, o_part, o_ws, total;
 };
@@ -930,8 +933,7 @@ StaticLayout static_layout(const qevict_cache *c, int splits) {
     return s;
 }
 
-// First use on a device: look up the array's address and clear it (the
-// arrival counters must start at zero; each launch leaves them at zero).
+// First use on a device: look up the array's address (and clear the array once).
 qevict_status static_scratch_setup(int dev, void **out) {
     std::lock_guard<std::mutex> lock(g_static_mu);
     if (!g_static_ptr[dev]) {
@@ -983,6 +985,8 @@ qevict_status qevict_decode_attention_static_scratch(qevict_cache *c, int32_t la
     S.rec = (unsigned long long *)(p + ly.o_rec);
     S.part = (unsigned long long *)(p + ly.o_part);
     S.wstat = (float2 *)(p + ly.o_ws);
+    e = cudaMemsetAsync(p, 0, ly.o_ws, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "static scratch clear");
     e = launch_decode(lh.dev, c->cdev, S, lh.tmap, layer, (const __nv_bfloat16 *)q, nullptr, nullptr, out, mass,
                       accumulate_scores, splits, false, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
