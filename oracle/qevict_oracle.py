@@ -828,10 +828,3 @@ def route_global(layers, hs=1, scores_override=None):
             counts.append(transition_counts(old, c.tiers_now(u)))
         c.last_counts = np.stack(counts)
 
-
-def tiered_bytes(cache: OracleCache) -> int:
-    """Attention-visible bytes resident for all sequences (FP c_fp, INT2 / INT4 /
-    INT8 their codes and meta, E 0)."""
-    t = cache.tiers()
-    return int(sum((t == tier).sum() * width_cost(cache.w, cache.Hkv, cache.d, bits)
-                   for bits, tier in TIER_OF_BITS.items()))
