@@ -79,6 +79,45 @@ def test_quantiser_edge_groups_bit_exact():
     check_decode(cache, 0, ref, synth.queries(5, 0, 0, B, 4, 128))
 
 
+def test_quantiser_flags_nonfinite_and_fp16_overflow_on_the_gpu():
+    """Groups holding +inf or -inf, a range whose step passes fp16 and a
+    minimum below -65504: the quantiser sets DEVICE in the status word and
+    stores each such group as zero codes with a zero scale and minimum. Every
+    other group is quantised exactly as the oracle quantises it."""
+    B, Hkv, w, L = 1, 2, 16, 64
+    k, v = synth.kv_tokens(15, 0, B, 0, L, Hkv, 128, "heavy")
+    k = k.clone()
+    v = v.clone()
+    k[0, 3, 0, 5] = float("inf")          # window 0, KV head 0, token 3, group 0
+    v[0, 7, 1, 40] = -float("inf")        # window 0, KV head 1, token 7, group 1
+    v[0, 9, 0, 70] = 3e5                  # window 0, group 2: (max - min) / 3 passes 65504
+    k[0, 2, 1, 96:128] = -7e4             # window 0, group 3: the minimum passes -65504
+    k[0, 20, 1, 64] = float("inf")        # window 1, KV head 1, token 4, group 2
+    tiers = torch.tensor([[1, 1, 0, 0]], dtype=torch.uint8)
+    cache = binding.TieredCache(B, 1, 4, Hkv, w, L, fp_capacity=4, ledger_capacity=4)
+    cache.prefill(0, k.cuda(), v.cuda(), tiers=tiers.cuda())
+    torch.cuda.synchronize()
+    assert binding.STATUS[cache.status()] == "DEVICE"
+    tier, _, lgs, _ = cache.tables(0)
+    assert tier[0].tolist() == [1, 1, 0, 0]
+    n_bad = 0
+    for wi in range(2):
+        codes, scale, mn = cache.ledger_window(0, int(lgs[0, wi]), 2)
+        for kv, x in enumerate((k, v)):
+            xs = x[0, wi * w:(wi + 1) * w].float().numpy().transpose(1, 0, 2)    # [Hkv][w][d]
+            ec, es, em, bad = O.quantize_groups(xs.reshape(Hkv, w, 4, 32))
+            ec = np.where(bad[..., None], 0, ec).reshape(Hkv, w, 128)
+            es = np.where(bad, np.float16(0), es)
+            em = np.where(bad, np.float16(0), em)
+            n_bad += int(bad.sum())
+            assert np.array_equal(codes[:, kv].numpy(), ec), ("codes", wi, kv)
+            assert np.array_equal(scale[:, kv].numpy().view(np.uint16), es.view(np.uint16)), ("scale", wi, kv)
+            assert np.array_equal(mn[:, kv].numpy().view(np.uint16), em.view(np.uint16)), ("min", wi, kv)
+    assert n_bad == 5
+    cache.clear_status()
+    assert cache.status() == 0
+
+
 def test_ledger_write_once_through_cycles():
     B, Hq, Hkv, w, L = 2, 8, 2, 32, 320
     W = L // w

@@ -235,3 +235,23 @@ def test_rd_mixed_second_event_moves_between_widths():
     assert moved > 0
     assert np.all(cache.tables(0)[3].numpy() <= 1), "a ledger entry was written twice"
     check_decode(cache, 0, ref, synth.queries(78, 0, 0, B, Hq, 128))
+
+
+@pytest.mark.parametrize("mixed", [False, True])
+def test_rate_distortion_routes_on_an_all_evicted_layer_move_nothing(mixed):
+    """Every window evicted, the last one full: there is no candidate, so both
+    rate-distortion routes leave every table as it is and count no move."""
+    B, Hq, Hkv, w, L = 2, 8, 2, 16, 96
+    W = L // w
+    cache, ref = make_wide(B, Hq, Hkv, w, L, 8, 0.5, seed=23, tiers=np.full((B, W), O.TIER_E, np.uint8))
+    scores = synth.zipf_scores(23, 0, B, W)
+    if mixed:
+        route_both(cache, ref, scores, 8)
+    else:
+        cache.route_rd(0, scores_override=scores.cuda())
+        O.route_rd(ref, scores_override=scores.numpy())
+        assert cache.status() == 0, cache.last_error()
+        check_state(cache, 0, ref)
+    assert np.all(cache.tables(0)[0].numpy() == O.TIER_E)
+    assert not cache.tier_move_counts(0).numpy().any()
+    assert not ref.last_counts.any()
