@@ -41,9 +41,18 @@ FALLBACK_HBM_GBS = 6800.0
 
 # --------------------------------------------------------------------------- helpers
 
-def workload():
+def all_workloads():
+    """Every benchmark workload by name: the fixed ones, then the Mistral-7B-shaped
+    sweep points (batch 4), named by context, window and budget."""
     from tiered_kv_cache_decode_gb300 import synth
-    return dict(synth.WORKLOADS[WORKLOAD])
+    out = {k: dict(v) for k, v in synth.WORKLOADS.items() if k != "tiny"}
+    for p in synth.mistral_sweep():
+        out[f"mistral7b_b4_{p['L'] // 1024}k_w{p['w']}_{round(p['beta'] * 100)}pct"] = dict(p)
+    return out
+
+
+def workload(name=None):
+    return dict(all_workloads()[name or WORKLOAD])
 
 
 def costs(wl):
@@ -149,13 +158,17 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def run_config(wl, NL, world):
+def run_config(wl, NL, world, route_events=None):
     """The workload description both arms print."""
-    return {"workload": WORKLOAD if NL == wl["layers"] else f"{WORKLOAD} ({NL} of {wl['layers']} layers)",
-            "batch": wl["B"], "layers": NL, "q_heads": wl["Hq"], "kv_heads": wl["Hkv"],
-            "head_dim": 128, "context": wl["L"], "window": wl["w"], "budget_frac": wl["beta"],
-            "fp_share": wl["rho"], "route_every": ROUTE_EVERY, "parallelism": f"replicas x{world}",
-            "l2": f"inputs larger than L2 ({NL} layers x ~26.8 MB of tiered cache)"}
+    per_layer = TierTracker(wl, wl["L"]).decode_bytes()
+    c = {"workload": WORKLOAD if NL == wl["layers"] else f"{WORKLOAD} ({NL} of {wl['layers']} layers)",
+         "batch": wl["B"], "layers": NL, "q_heads": wl["Hq"], "kv_heads": wl["Hkv"],
+         "head_dim": 128, "context": wl["L"], "window": wl["w"], "budget_frac": wl["beta"],
+         "fp_share": wl["rho"], "route_every": ROUTE_EVERY, "parallelism": f"replicas x{world}",
+         "l2": f"inputs larger than L2 ({NL} layers x {per_layer / 1e6:.1f} MB of tiered cache)"}
+    if route_events is not None:
+        c["route_events_in_timed_steps"] = route_events
+    return c
 
 
 def combine_ranks(ms, e2e_s, nbytes, e2e_bytes, world, device):
@@ -177,6 +190,8 @@ def profiled_traffic():
     taken on the current decode kernel source (else None)."""
     src = os.path.join(ROOT, "tiered_kv_cache_decode_gb300", "csrc", "qevict_decode.cu")
     summ = os.path.join(ROOT, "profiles", f"decode_{WORKLOAD}.md")
+    if not os.path.exists(summ):
+        return None
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         fields = {}
@@ -197,14 +212,14 @@ def profiled_traffic():
 def _oracle_worker(args):
     """One layer of the workload on the CPU oracle: prefill, then timed decode
     steps (append + attention + score accumulation) for about `budget_s` s."""
-    layer, budget_s, max_steps = args
+    layer, budget_s, max_steps, name = args
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[var] = "1"
     import torch
     torch.set_num_threads(1)
     import oracle as O
     from tiered_kv_cache_decode_gb300 import synth
-    wl = workload()
+    wl = workload(name)
     B, Hq, Hkv, w, L = wl["B"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"]
     k, v = synth.kv_tokens(0, layer, B, 0, L, Hkv, 128, wl["outliers"])
     c = O.OracleCache(B, Hq, Hkv, 128, w, beta=wl["beta"], rho=wl["rho"])
@@ -231,7 +246,7 @@ def oracle_throughput(n_workers, budget_s, max_steps):
     ctx = mp.get_context("spawn")
     t0 = time.perf_counter()
     with ctx.Pool(n_workers) as pool:
-        res = pool.map(_oracle_worker, [(l, budget_s, max_steps) for l in range(n_workers)])
+        res = pool.map(_oracle_worker, [(l, budget_s, max_steps, WORKLOAD) for l in range(n_workers)])
     wall = time.perf_counter() - t0
     nbytes = sum(r[0] for r in res)
     spent = max(r[1] for r in res)
@@ -551,6 +566,110 @@ def measure_mixed_widths(wl, NL, reps, dev, peak):
             "decode_frac_of_peak": round(nbytes / (us_dec * 1e-6) / 1e9 / peak, 4)}
 
 
+def measure_per_config(reps, dev, peak, which="all"):
+    """The decode kernel on every other workload: the Llama-3.1-8B-shaped batch
+    8 at 32K and 5 %, the Qwen2.5-7B-shaped batch 16 at 16K and 10 %, and the 27
+    Mistral-7B-shaped sweep points (batch 4; 8K / 32K / 128K tokens, windows of
+    32 / 64 / 128, budgets of 5 / 10 / 20 %). Each runs as many layers as make
+    its tiered cache at least three times the 129 MB L2 (at most its model's
+    layer count), routed on seeded Zipf scores; one CUDA graph decodes every
+    layer once, timed over `reps` replays. Then, at each sweep context (64-token
+    windows, 10 %), routing events on a fresh two-layer cache starting in full
+    precision time the quantise path (first quantisations) and the promote
+    path (promotions), with the bytes of the window rows they move."""
+    import torch
+    from tiered_kv_cache_decode_gb300 import binding, synth
+    names = [n for n in all_workloads() if n != WORKLOAD]
+    if which != "all":
+        names = [n for n in names if n in which.split(",")]
+    out = {}
+    d, seed = 128, 0
+    for name in names:
+        wl = workload(name)
+        B, Hq, Hkv, w, L0 = wl["B"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"]
+        W0 = -(-L0 // w)
+        per_layer = TierTracker(wl, L0).decode_bytes()
+        NL = int(min(wl["layers"], max(2, math.ceil(3 * 129e6 / per_layer))))
+        cache = binding.TieredCache(B, NL, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"])
+        cache.set_launch_overlap(True)
+        for l in range(NL):
+            k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
+            cache.prefill(l, k, v, scores=synth.zipf_scores(seed, l, B, W0, device=dev))
+            del k, v
+        q = [synth.queries(seed, l, 0, B, Hq, d, device=dev) for l in range(NL)]
+        xo = torch.empty(NL, B, Hq, d, dtype=torch.float32, device=dev)
+        stream = torch.cuda.Stream(device=dev)
+        g = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for l in range(NL):
+                    cache.decode(l, q[l], out=xo[l], want_mass=False, accumulate=True, stream=stream)
+            for _ in range(3):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        st = cache.status()
+        assert st == 0, f"{name}: device status {st}: {cache.last_error()}"
+        us = e0.elapsed_time(e1) * 1e3 / (reps * NL)
+        tr = TierTracker(wl, L0)
+        gbs = per_layer / (us * 1e-6) / 1e9
+        out[name] = {"layers_timed": NL, "windows_fp_int2_evicted": [tr.n_fp, tr.n_q, W0 - tr.n_fp - tr.n_q],
+                     "us_per_launch": round(us, 3), "bytes_per_launch": int(per_layer),
+                     "gbs": round(gbs, 2), "frac_of_peak": round(gbs / peak, 4)}
+        del cache, q, xo, g
+        torch.cuda.empty_cache()
+    # quantise / promote throughput against context (64-token windows, 10 %)
+    moves = {}
+    for L0 in (8192, 32768, 131072):
+        name = f"mistral7b_b4_{L0 // 1024}k_w64_10pct"
+        if which != "all" and name not in which.split(","):
+            continue
+        wl = workload(name)
+        B, Hq, Hkv, w = wl["B"], wl["Hq"], wl["Hkv"], wl["w"]
+        W0 = L0 // w
+        nl = 2
+        mc = binding.TieredCache(B, nl, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"],
+                                 fp_capacity=W0, ledger_capacity=W0)
+        for l in range(nl):
+            k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
+            mc.prefill(l, k, v, tiers=torch.zeros(B, W0, dtype=torch.uint8, device=dev))
+            del k, v
+        row = Hkv * w * (512 + 96)
+        stream = torch.cuda.Stream(device=dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        res = {}
+        for kind, sd in (("quantise", seed + 500), ("promote", seed + 501)):
+            ov = [synth.zipf_scores(sd, l, B, W0, device=dev) for l in range(nl)]
+            s0 = mc.stats()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for l in range(nl):
+                    mc.route(l, scores_override=ov[l], stream=stream)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3
+            s1 = mc.stats()
+            nq = s1["ledger_writes"] - s0["ledger_writes"]
+            npr = s1["promotions"] - s0["promotions"]
+            res[kind] = {"quantised_per_layer": nq / nl, "promoted_per_layer": npr / nl,
+                         "us_per_layer_event": round(us / nl, 2),
+                         "gbs": round((nq + npr) * row / (us * 1e-6) / 1e9, 2)}
+        st = mc.status()
+        assert st == 0, f"{name}: device status {st}: {mc.last_error()}"
+        mc.close()
+        del mc
+        torch.cuda.empty_cache()
+        moves[f"{L0 // 1024}k"] = res
+    out["mistral7b_b4_w64_10pct_route_moves"] = moves
+    return out
+
+
 def run_native(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -578,7 +697,8 @@ def run_native(args, rank, world, local_rank):
         nw = max(1, min(8, (os.cpu_count() or 2) // 2))
         ctx = mp.get_context("spawn")
         cpu_pool = ctx.Pool(nw)
-        pool_async = (cpu_pool, nw, cpu_pool.map_async(_oracle_worker, [(l, args.cpu_seconds, 200) for l in range(nw)]),
+        pool_async = (cpu_pool, nw, cpu_pool.map_async(_oracle_worker, [(l, args.cpu_seconds, 200, WORKLOAD)
+                                                                         for l in range(nw)]),
                       time.perf_counter())
 
     cache = binding.TieredCache(B, NL, Hq, Hkv, w, maxc, budget_frac=wl["beta"], fp_share=wl["rho"])
@@ -649,13 +769,14 @@ def run_native(args, rank, world, local_rank):
         nbytes = NL * (tracker.decode_bytes() + tracker.append_bytes())
         launches = NL
         gstep[0] += 1
-        if gstep[0] % ROUTE_EVERY == 0:
+        routed = gstep[0] % ROUTE_EVERY == 0
+        if routed:
             g_route.replay()
             tracker.route()
             launches += 3 * NL
         if host_out is not None:
             host_out.copy_(xout, non_blocking=True)
-        return nbytes, launches
+        return nbytes, launches, int(routed)
 
     def barrier():
         if world > 1:
@@ -679,11 +800,12 @@ def run_native(args, rank, world, local_rank):
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         ev0.record(stream)
-        nbytes, launches = 0, 0
+        nbytes, launches, route_events = 0, 0, 0
         for s in range(K):
-            b_, l_ = one_step(Wm + s)
+            b_, l_, r_ = one_step(Wm + s)
             nbytes += b_
             launches += l_
+            route_events += r_
         ev1.record(stream)
         barrier()
         clocks = finish_clocks(clk, local_rank)
@@ -709,7 +831,7 @@ def run_native(args, rank, world, local_rank):
         t0 = time.perf_counter()
         e2e_bytes = 0
         for s in range(0 if args.no_e2e else K):
-            b_, _ = one_step(Wm + K + s, host_in=host_pool[s], host_out=host_out)
+            b_, _, _ = one_step(Wm + K + s, host_in=host_pool[s], host_out=host_out)
             e2e_bytes += b_
             stream.synchronize()
         e2e_s = max(time.perf_counter() - t0, 1e-9)
@@ -742,7 +864,7 @@ def run_native(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": run_config(wl, NL, world),
+        "config": run_config(wl, NL, world, route_events),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "kernel": "decode_kernel (tiered split-K decode + combine + score + append)",
@@ -764,13 +886,16 @@ def run_native(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         line["variants"] = measure_variants(wl, NL, K, dev, peak)
         line["variants"]["mixed_widths"] = measure_mixed_widths(wl, NL, K, dev, peak)
+    if not args.no_per_config:
+        line["per_config"] = measure_per_config(K, dev, peak, args.per_config)
     if pool_async is not None:
         cpu_pool, nw, res, t_start = pool_async
         out = res.get()
         cpu_pool.close()
         nb = sum(r[0] for r in out)
         spent = max(r[1] for r in out)
-        line["cpu_baseline"] = {"value": round(nb / spent / 1e9, 4), "unit": "GB/s", "cores": nw, "kind": "oracle",
+        line["cpu_baseline"] = {"value": round(nb / spent / 1e9, 4), "unit": "GB/s", "cores": nw,
+                                "host_cores": os.cpu_count(), "kind": "oracle",
                                 # each worker is one single-threaded process: its rate is the one-core figure
                                 "one_core_value": round(sum(r[0] / r[1] for r in out if r[1] > 0) / len(out) / 1e9, 4),
                                 "sample": f"{nw} layers of the workload, one per single-threaded process, "
@@ -794,7 +919,8 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(spent / max(1, per_step) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": run_config(wl, wl["layers"], world),
-            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nw, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": nw, "host_cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -812,7 +938,19 @@ def main():
     ap.add_argument("--no-diag", action="store_true", help="skip the routing diagnostics leg")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the per-KV-head and global-routing leg")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the decode measurement on the other workloads")
+    ap.add_argument("--per-config", default="all",
+                    help="comma-separated workload names for the per-config leg (default: all)")
+    ap.add_argument("--workload", default=WORKLOAD, help="headline workload (see --list-workloads)")
+    ap.add_argument("--list-workloads", action="store_true")
     args = ap.parse_args()
+    if args.list_workloads:
+        print("\n".join(all_workloads()))
+        return
+    if args.workload not in all_workloads():
+        ap.error(f"unknown workload {args.workload}")
+    globals()["WORKLOAD"] = args.workload
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
