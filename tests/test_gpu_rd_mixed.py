@@ -243,10 +243,11 @@ def test_rate_distortion_routes_on_an_all_evicted_layer_move_nothing(mixed):
     rate-distortion routes leave every table as it is and count no move."""
     B, Hq, Hkv, w, L = 2, 8, 2, 16, 96
     W = L // w
-    cache, ref = make_wide(B, Hq, Hkv, w, L, 8, 0.5, seed=23, tiers=np.full((B, W), O.TIER_E, np.uint8))
+    bits = 8 if mixed else 0     # the INT2 rate-distortion route wants an INT2-only cache
+    cache, ref = make_wide(B, Hq, Hkv, w, L, bits, 0.5, seed=23, tiers=np.full((B, W), O.TIER_E, np.uint8))
     scores = synth.zipf_scores(23, 0, B, W)
     if mixed:
-        route_both(cache, ref, scores, 8)
+        route_both(cache, ref, scores, bits)
     else:
         cache.route_rd(0, scores_override=scores.cuda())
         O.route_rd(ref, scores_override=scores.numpy())
