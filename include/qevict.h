@@ -470,11 +470,11 @@ int64_t qevict_length(const qevict_cache *cache, int32_t layer);
  * a host thread that must not block on an allocator's lock.
  *
  * Arguments, outputs and errors are those of qevict_decode_attention.
- * The scratch a call needs is 8 B of window statistics per (sequence,
- * query head, window of max_context), 1 KiB per query head for each decode
- * split of each (sequence, KV head) (up to 32 splits, as many as fit the GPU
- * in one wave), 4 KiB of split records per (sequence, KV head) and a few
- * counters; a cache whose need passes
+ * The scratch a call needs is, per (sequence, KV head): 1 KiB per query head
+ * for each decode split (up to 32 splits, as many as fit the GPU in one
+ * wave), 4 KiB of split records, 8 B of counters, and 8 B per query head for
+ * each 16-token tile of every slot of the cache's full-precision and ledger
+ * pools (the per-claim records). A cache whose need passes
  * QEVICT_STATIC_SCRATCH_BYTES is rejected with INVALID_ARG before anything
  * is enqueued, and the error text gives both sizes. The cache's device must
  * be current (INVALID_ARG otherwise).

@@ -3,7 +3,7 @@
 qevict_decode_attention_static_scratch runs the same decode kernel with its
 per-call scratch in a library-owned device array. Two calls in a row must give
 what the regular entry point gives, within the attention tolerance, and must
-leave the array's arrival counters at zero for the next call. The file is
+leave nothing behind that a later call could read as its own. The file is
 named to be collected last, so it also runs after the other GPU tests have
 used the library in the same process; it passes alone as well (the first call
 in the process does the per-device set-up).
@@ -68,8 +68,10 @@ def test_static_scratch_without_mass():
 
 
 def test_static_scratch_rejects_a_cache_that_needs_more():
-    # 16 sequences x 32 query heads x 1024 windows x 8 B of window statistics is 4 MiB, plus the counters
-    cache = binding.TieredCache(16, 1, 32, 8, 16, 16384, budget_frac=0.05, fp_share=0.5)
+    # 128 (sequence, KV head) pairs x 2048 records (one per slot of 1024 full-precision and
+    # 1024 ledger slots of 16-token windows) x 4 query heads x 8 B is 8 MiB
+    cache = binding.TieredCache(16, 1, 32, 8, 16, 16384, budget_frac=0.05, fp_share=0.5, fp_capacity=1024,
+                                ledger_capacity=1024)
     k, v = synth.kv_tokens(13, 0, 16, 0, 100, 8, 128, "heavy", device="cuda")
     cache.append(0, k, v)
     q = synth.queries(13, 0, 0, 16, 32, 128).cuda()

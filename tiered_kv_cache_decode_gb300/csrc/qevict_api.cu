@@ -319,9 +319,11 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     // every allocation first, so that a failing allocator leaves nothing behind
     {
         Carver cv;
+        const int rec_stride = decode_records(c->CF, c->CQ, cfg.window, maxP);
         const size_t o_part = cv.take((size_t)B * Hkv * kMaxSplits * c->G * kHeadDim * 8);
-        const size_t o_rec = cv.take((size_t)B * Hkv * kMaxSplits * kMaxG * 16);
-        // window statistics; also the future-missed-mass partials (12 B per split and query head)
+        const size_t o_stat = cv.take((size_t)B * Hkv * kMaxSplits * kMaxG * 16);
+        const size_t o_rec = cv.take((size_t)B * Hkv * rec_stride * c->G * 8);
+        // the future-missed-mass partials (12 B per split and query head)
         const size_t o_ws = cv.take((size_t)B * Hq * (Wmax * 8 > 12 ? Wmax * 8 : 12));
         const size_t o_bar = cv.take((size_t)B * Hkv * 8);
         const size_t o_ab = cv.take((size_t)B * 4);
@@ -333,7 +335,9 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
             return fail(QEVICT_ERR_OUT_OF_MEMORY, "allocation of %zu B of decode scratch failed", need);
         }
         c->scratch.part = (unsigned long long *)(base + o_part);
-        c->scratch.rec = (unsigned long long *)(base + o_rec);
+        c->scratch.stat = (unsigned long long *)(base + o_stat);
+        c->scratch.rec = (float2 *)(base + o_rec);
+        c->scratch.rec_stride = rec_stride;
         c->scratch.wstat = (float2 *)(base + o_ws);
         c->scratch.bar = (uint32_t *)(base + o_bar);
         c->scratch.arrive_b = (uint32_t *)(base + o_ab);
@@ -439,7 +443,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         const LayerDev &D = c->layers[l].dev;
         const cuuint64_t dims[4] = {64, (cuuint64_t)w, 4, (cuuint64_t)B * c->CF * Hkv};
         const cuuint64_t strides[3] = {128, (cuuint64_t)w * 128, (cuuint64_t)w * 512};
-        const cuuint32_t box[4] = {64, 16, 4, 1};
+        const cuuint32_t box[4] = {64, 16, 4, 1};   // the K and V of a 16-token unit
         const cuuint32_t estr[4] = {1, 1, 1, 1};
         CUresult r = enc(&c->layers[l].tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, D.fp_pool, dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -892,8 +896,8 @@ int64_t qevict_length(const qevict_cache *c, int32_t layer) {
 }  // extern "C"
 
 // ---- decode with library-owned static scratch ------------------------------
-// The decode kernel needs per-call scratch (split partials, window
-// statistics, barrier and arrival counters). qevict_decode_attention_static_scratch takes it from the
+// The decode needs per-call scratch (split partials, records, chunk records
+// and the split arrival counters). qevict_decode_attention_static_scratch takes it from the
 // fixed device array below instead of the cache's own block, so the call
 // allocates nothing. Its address is looked up once per device, with that
 // device current, and then passed to the kernel as a plain pointer.
@@ -910,26 +914,28 @@ void *g_static_ptr[kStaticMaxDevices];
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Scratch layout of one call: counters first, the tagged split records, split
-// partials for `splits` splits, and the window statistics. The offsets depend
-// on the cache's shape, so one cache's counters can lie on another's records:
-// every call therefore clears everything before the window statistics on its
+// Scratch layout of one call: split arrival counters and record generations,
+// the tagged split records and partials, then the chunk records. The offsets
+// depend on the cache's shape, so one cache's counters could lie on another's
+// records: every call clears everything before the chunk records on its
 // stream first (a memset, which allocates nothing). After the clear the
 // record generation is 0, so the launch's tag is 1 and no word left by an
-// earlier call carries it.
+// earlier call carries it. The chunk records are written before they are read.
 struct StaticLayout {
-    size_t o_ab, o_bar, o_rec, o_part, o_ws, total;
+    size_t o_bar, o_stat, o_part, o_rec, total;
+    int rec_stride;
 };
 
 StaticLayout static_layout(const qevict_cache *c, int splits) {
-    const size_t B = (size_t)c->cfg.batch, Hkv = (size_t)c->cfg.num_kv_heads, Hq = (size_t)c->cfg.num_q_heads;
+    const size_t B = (size_t)c->cfg.batch, Hkv = (size_t)c->cfg.num_kv_heads;
+    const int maxP = c->cfg.max_ledger_bits > 2 ? c->cfg.max_ledger_bits / 2 : 1;
     StaticLayout s{};
-    s.o_ab = 0;
-    s.o_bar = s.o_ab + round256(B * 4);
-    s.o_rec = s.o_bar + round256(B * Hkv * 8);
-    s.o_part = s.o_rec + round256(B * Hkv * (size_t)kMaxSplits * kMaxG * 16);
-    s.o_ws = s.o_part + round256(B * Hkv * (size_t)splits * c->G * kHeadDim * 8);
-    s.total = s.o_ws + round256(B * Hq * (size_t)c->Wmax * 8);
+    s.rec_stride = decode_records(c->CF, c->CQ, c->cfg.window, maxP);
+    s.o_bar = 0;
+    s.o_stat = s.o_bar + round256(B * Hkv * 8);
+    s.o_part = s.o_stat + round256(B * Hkv * (size_t)kMaxSplits * kMaxG * 16);
+    s.o_rec = s.o_part + round256(B * Hkv * (size_t)splits * c->G * kHeadDim * 8);
+    s.total = s.o_rec + round256(B * Hkv * (size_t)s.rec_stride * c->G * 8);
     return s;
 }
 
@@ -980,12 +986,12 @@ qevict_status qevict_decode_attention_static_scratch(qevict_cache *c, int32_t la
     if (st) return st;
     uint8_t *p = (uint8_t *)base;
     DecodeScratch S{};
-    S.arrive_b = (uint32_t *)(p + ly.o_ab);
     S.bar = (uint32_t *)(p + ly.o_bar);
-    S.rec = (unsigned long long *)(p + ly.o_rec);
+    S.stat = (unsigned long long *)(p + ly.o_stat);
     S.part = (unsigned long long *)(p + ly.o_part);
-    S.wstat = (float2 *)(p + ly.o_ws);
-    e = cudaMemsetAsync(p, 0, ly.o_ws, (cudaStream_t)stream);
+    S.rec = (float2 *)(p + ly.o_rec);
+    S.rec_stride = ly.rec_stride;
+    e = cudaMemsetAsync(p, 0, ly.o_rec, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "static scratch clear");
     e = launch_decode(lh.dev, c->cdev, S, lh.tmap, layer, (const __nv_bfloat16 *)q, nullptr, nullptr, out, mass,
                       accumulate_scores, splits, false, (cudaStream_t)stream);

@@ -114,13 +114,15 @@ __device__ __forceinline__ int64_t src_row(const LayerDev &D, int u, int64_t n, 
 // Decode scratch, shared by all layers of a cache: a decode launch touches it
 // only after its dependency wait, so consecutive launches never overlap in it.
 struct DecodeScratch {
-    unsigned long long *part;  // [B*Hkv][splits][G][d] split partial outputs: float in the low half,
-                               // the launch's tag in the high half of each word
-    unsigned long long *rec;   // [B*Hkv][kMaxSplits][kMaxG][2] split (max, exp-sum), log2 domain, each
-                               // float in the low half of a word whose high half is the launch's tag
-    float2 *wstat;        // [B][Hq][Wmax] (window max, window exp-sum), log2 domain
+    unsigned long long *part;  // [B*Hkv][splits][G][d] split partial outputs (unnormalised, relative to the
+                               // split's max): float in the low half, the launch's tag in the high half
+    unsigned long long *stat;  // [B*Hkv][kMaxSplits][kMaxG][2] split (max, exp-sum), log2 domain, tagged likewise
+    float2 *rec;          // [B*Hkv][rec_stride][G] (reference max, exp-sum) of each full-precision unit and
+                          // quantised chunk, log2 domain (written and read by the same split)
+    int rec_stride;       // records per (sequence, KV head): decode_records(CF, CQ, w, maxP)
+    float2 *wstat;        // [B][Hq][max(Wmax, 2)] future-missed-mass partials
     uint32_t *bar;        // [B*Hkv][2] split arrival count (0 between launches), record generation
-    uint32_t *arrive_b;   // [B] KV-head arrival counters for the fused append (0 between launches)
+    uint32_t *arrive_b;   // [B] arrival counters of a sequence's CTAs for the fused append (0 between launches)
 };
 
 struct CacheDev {
@@ -210,6 +212,7 @@ cudaError_t launch_future_missed_mass(const LayerDev &L, const CacheDev &C, cons
                                       const CUtensorMap &kmap, const __nv_bfloat16 *q, int n_tokens, float *fmm,
                                       int num_sms, cudaStream_t s);
 int decode_splits(int pairs, int num_sms, int G);
+int decode_records(int CF, int CQ, int w, int maxP);
 cudaError_t prepare_decode();
 
 // ---- device helpers -------------------------------------------------------
