@@ -325,6 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int sl_p[kWarps][kSlots];      // code planes of a quantised chunk (kWide)
     __shared__ int s_next;                    // next claim
     __shared__ int s_span[4];                 // this split's quantised and full-precision windows
+    __shared__ long long s_len;               // the sequence's length at launch
+    __shared__ int s_slot_new;                // slot of the new token's window (split 0, fused append)
     __shared__ uint32_t s_gen;                // split-record generation of this launch
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -344,6 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_span[1] = p.nqw;
             s_span[2] = p.fw0;
             s_span[3] = p.nfw;
+            s_len = p.length;
+            if (knew != nullptr && split == 0 && p.length < D.max_context) {
+                const int64_t wn = p.length / w;
+                s_slot_new = (p.length % w == 0) ? D.ctr[b * kCtrN + CTR_NEXT] : D.fp_slot[(int64_t)b * D.Wmax + wn];
+            }
         }
         return p.N;
     }();
@@ -760,10 +767,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- merge the warps (the rings are free now); rows padded by 4 floats
     constexpr int kOwStride = kHeadDim + 4;
-    float *Ow = reinterpret_cast<float *>(smem);    // [warp][8 heads][kOwStride]
-    float *mw_s = Ow + kWarps * 8 * kOwStride;      // [warp][8]
-    float *lw_s = mw_s + kWarps * 8;                // [warp][8]
-    float *minw = lw_s + kWarps * 8;                // [warp][8][4]
+    float *Ow = reinterpret_cast<float *>(smem);    // [warp][8 columns][kOwStride]
+    float *mw_s = Ow + kWarps * 8 * kOwStride;      // [warp][8] running max
+    float *lw_s = mw_s + kWarps * 8;                // [warp][8] exp-sum
+    float *fw_s = lw_s + kWarps * 8;                // [warp][8] weight of the warp in the split
+    float *Mh_s = fw_s + kWarps * 8;                // [8] the split's max per head
 #pragma unroll
     for (int o2 = 4; o2 <= 16; o2 <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
@@ -775,27 +783,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     {
-        // every N column as it is (with kDup, columns 4..7 hold the lo parts of columns 0..3)
+        // every N column as it is (with kDup, columns 4..7 hold the lo parts of columns
+        // 0..3 and take no V minimum share); the minimum share joins its group's channels
         const int c0 = 2 * t, c1 = 2 * t + 1;
+        const float mk = (kDup && t >= 2) ? 0.f : 1.f;
         float *ob = Ow + warp * 8 * kOwStride;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            ob[c0 * kOwStride + 16 * mt + g] = o[mt][0];
-            ob[c0 * kOwStride + 16 * mt + g + 8] = o[mt][2];
-            ob[c1 * kOwStride + 16 * mt + g] = o[mt][1];
-            ob[c1 * kOwStride + 16 * mt + g + 8] = o[mt][3];
+            const float a0 = mk * mn0[mt >> 1], a1 = mk * mn1[mt >> 1];
+            ob[c0 * kOwStride + 16 * mt + g] = o[mt][0] + a0;
+            ob[c0 * kOwStride + 16 * mt + g + 8] = o[mt][2] + a0;
+            ob[c1 * kOwStride + 16 * mt + g] = o[mt][1] + a1;
+            ob[c1 * kOwStride + 16 * mt + g + 8] = o[mt][3] + a1;
         }
         if (g == 0) {
             mw_s[warp * 8 + c0] = m0;
             lw_s[warp * 8 + c0] = l0;
             mw_s[warp * 8 + c1] = m1;
             lw_s[warp * 8 + c1] = l1;
-#pragma unroll
-            for (int i = 0; i < kGroups; ++i) {
-                minw[(warp * 8 + c0) * 4 + i] = mn0[i];
-                minw[(warp * 8 + c1) * 4 + i] = mn1[i];
-            }
         }
+    }
+    __syncthreads();
+    if (tid < kWarps * 8) {
+        // the weight of warp ww in head hh's split result: 2^(m_ww - M)
+        const int ww = tid >> 3, hh = tid & 7;
+        float M = -INFINITY;
+#pragma unroll
+        for (int v = 0; v < kWarps; ++v) M = fmaxf(M, mw_s[v * 8 + hh]);
+        fw_s[tid] = M == -INFINITY ? 0.f : ex2(mw_s[tid] - M);
+        if (ww == 0) Mh_s[hh] = M;
     }
     __syncthreads();
     // ---- this split's partial output [G][128] (unnormalised, relative to its own
@@ -807,31 +823,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned long long *pw = S.part + ((int64_t)bk * splits + split) * G * kHeadDim;
         for (int i = tid; i < G * kHeadDim; i += kThreads) {
             const int hh = i / kHeadDim, c = i % kHeadDim;
-            float M = -INFINITY;
+            float acc = 0.f;
 #pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, mw_s[ww * 8 + hh]);
-            float acc = 0.f, l = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int ww = 0; ww < kWarps; ++ww) {
-                    const float f = ex2(mw_s[ww * 8 + hh] - M);
-                    float v = Ow[(ww * 8 + hh) * kOwStride + c] + minw[(ww * 8 + hh) * 4 + c / kGroup];
-                    if (kDup) v += Ow[(ww * 8 + hh + 4) * kOwStride + c];
-                    acc = fmaf(f, v, acc);
-                    l = fmaf(f, lw_s[ww * 8 + hh], l);
-                }
+            for (int ww = 0; ww < kWarps; ++ww) {
+                float v = Ow[(ww * 8 + hh) * kOwStride + c];
+                if (kDup) v += Ow[(ww * 8 + hh + 4) * kOwStride + c];
+                acc = fmaf(fw_s[ww * 8 + hh], v, acc);
             }
             const unsigned long long word = ((unsigned long long)tag << 32) | __float_as_uint(acc);
             asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(pw + i), "l"(word) : "memory");
             if (c == 0) {
+                float l = 0.f;
+#pragma unroll
+                for (int ww = 0; ww < kWarps; ++ww) l = fmaf(fw_s[ww * 8 + hh], lw_s[ww * 8 + hh], l);
                 unsigned long long *r = S.stat + (((int64_t)bk * kMaxSplits + split) * kMaxG + hh) * 2;
-                const unsigned long long m64 = ((unsigned long long)tag << 32) | __float_as_uint(M);
+                const unsigned long long m64 = ((unsigned long long)tag << 32) | __float_as_uint(Mh_s[hh]);
                 const unsigned long long l64 = ((unsigned long long)tag << 32) | __float_as_uint(l);
                 asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(r), "l"(m64), "l"(l64) : "memory");
             }
         }
     }
     __syncthreads();   // this CTA's chunk records are in global memory; the shared buffers are free again
+    if (knew != nullptr && tid == kThreads - 32) {
+        // every table read of this CTA is behind it (the release orders them before the count)
+        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(S.arrive_b + b), "r"(1u) : "memory");
+    }
 
     // ---- the tail: the splits meet, then each writes a slice of the output and the
     // masses of its own windows
@@ -841,8 +857,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *Fs = hM + 32;                            // [kMaxSplits][8] weight of each split
     float *sV = hM + 32 + kMaxSplits * 8;           // [128] the new token's V row
     float4 *red = reinterpret_cast<float4 *>(hM + 2048);   // [slice outputs][splits]
-    const int32_t *ctr = D.ctr + b * kCtrN;
-    const int64_t length = ctr[CTR_LEN];
+    // the tables as this launch found them: once every CTA of the sequence has
+    // published, one CTA moves them on, so nothing below reads them afresh
+    const int64_t length = s_len;
     const bool has_new = knew != nullptr && length < D.max_context;
     if (knew != nullptr && !has_new && tid == 0 && split == 0)   // replayed past the end of the tables
         set_status(C, QEVICT_ERR_INVALID_ARG, layer, b, (int)length);
@@ -1041,11 +1058,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (accumulate && fresh) atomicAdd(&sp[wi], sum * inv_hq);
     }
     // ---- the fused append (split 0): this KV head's K and V rows of the new token, into
-    // the slot that receives it (read before this CTA arrives below: the sequence's last
-    // CTA moves CTR_NEXT only after every CTA has arrived)
+    // the slot that receives it (read in the prologue, before this CTA's arrival: the
+    // tables move on only after every CTA of the sequence has arrived)
     if (has_new && split == 0 && tid < 32) {
-        const int slot_new = opens ? *(volatile const int32_t *)&ctr[CTR_NEXT]
-                                   : *(volatile const int32_t *)&D.fp_slot[wb + wnew];
+        const int slot_new = s_slot_new;
         if (slot_new >= 0) {
             const int row = (int)(length % w);
             const int kvs = tid >> 4, c = tid & 15;
@@ -1055,48 +1071,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(dst) = reinterpret_cast<const uint4 *>(src)[c];
         }
     }
-    __syncthreads();
-    if (tid == 0) {
-        // Two arrival counts. Per (sequence, KV head): the last split moves the record
-        // generation on for the next launch. Per sequence (fused append only): every
-        // CTA of the sequence has read its tables once all have arrived, so the last
-        // one moves them forward.
-        uint32_t *cnt = S.bar + 2 * bk, *gen = cnt + 1;
-        const uint32_t prev = atomicAdd(cnt, 1u);
-        if (prev == (uint32_t)(splits - 1)) {
-            *(volatile uint32_t *)cnt = 0u;
-            *(volatile uint32_t *)gen = tag;
+    // The record generation moves on once per launch (split 0, after its meet: every
+    // split of the pair has read it by then); the next launch reads it after its
+    // dependency wait.
+    if (split == 0 && tid == 0)
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(S.bar + 2 * bk + 1), "r"(1u) : "memory");
+    // With a new token, split 0 of KV head 0 moves the sequence's tables on once every
+    // CTA of the sequence has arrived (bounded wait): the length, and the window this
+    // step opens with the next free slot.
+    if (knew != nullptr && split == 0 && kvh == 0 && tid == 0) {
+        const uint32_t want = (uint32_t)(Hkv * splits);
+        uint32_t n = 0;
+        const long long t0 = clock64();
+        while (true) {
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(n) : "l"(S.arrive_b + b) : "memory");
+            if (n >= want) break;
+            if (clock64() - t0 > kWaitCycles) break;
+            __nanosleep(64);
         }
-        if (has_new) {
-            __threadfence();
-            const unsigned prev_b = atomicAdd(&S.arrive_b[b], 1u);
-            if (prev_b == (unsigned)(Hkv * splits - 1)) {
-                __threadfence();
-                int32_t *c = D.ctr + b * kCtrN;
+        if (n < want) {
+            set_status(C, QEVICT_ERR_TIMEOUT, layer, b, -5);
+        } else if (has_new) {
+            S.arrive_b[b] = 0u;
+            int32_t *c = D.ctr + b * kCtrN;
+            if (opens) {
                 const int n_fp = c[CTR_NFP];
-                if (opens) {
-                    const int slotn = c[CTR_NEXT];
-                    if (slotn < 0) {
-                        set_status(C, QEVICT_ERR_CAPACITY, layer, b, wnew);
+                const int slotn = c[CTR_NEXT];
+                if (slotn < 0) {
+                    set_status(C, QEVICT_ERR_CAPACITY, layer, b, wnew);
+                } else {
+                    D.tier[wb + wnew] = QEVICT_TIER_FP;
+                    D.fp_slot[wb + wnew] = slotn;
+                    D.lg_slot[wb + wnew] = -1;
+                    D.lwrites[wb + wnew] = 0;
+                    D.fp_list[b * D.CF + n_fp] = make_int2(wnew, slotn);
+                    c[CTR_NFP] = n_fp + 1;
+                    const int top = c[CTR_FP_TOP];
+                    if (top > 0) {
+                        c[CTR_NEXT] = D.fp_free[b * D.CF + top - 1];
+                        c[CTR_FP_TOP] = top - 1;
                     } else {
-                        D.tier[wb + wnew] = QEVICT_TIER_FP;
-                        D.fp_slot[wb + wnew] = slotn;
-                        D.lg_slot[wb + wnew] = -1;
-                        D.lwrites[wb + wnew] = 0;
-                        D.fp_list[b * D.CF + n_fp] = make_int2(wnew, slotn);
-                        c[CTR_NFP] = n_fp + 1;
-                        const int top = c[CTR_FP_TOP];
-                        if (top > 0) {
-                            c[CTR_NEXT] = D.fp_free[b * D.CF + top - 1];
-                            c[CTR_FP_TOP] = top - 1;
-                        } else {
-                            c[CTR_NEXT] = -1;
-                        }
+                        c[CTR_NEXT] = -1;
                     }
                 }
-                c[CTR_LEN] = (int)Lnew;
-                S.arrive_b[b] = 0u;
             }
+            c[CTR_LEN] = (int)Lnew;
+        } else {
+            S.arrive_b[b] = 0u;
         }
     }
 }
