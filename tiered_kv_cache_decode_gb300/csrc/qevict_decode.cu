@@ -183,15 +183,23 @@ __device__ __forceinline__ uint32_t bmul16(uint32_t r) {    // each bf16 half ti
 }
 // Code words: bits 1:0 and 17:16 of x (after the lane's shift) are two codes,
 // bits 3:2 and 19:18 two more. As bf16 pairs with the offset kept: 128 + c
-// and 128 + 4c (exact); without it (minus 128): c and 4c.
-__device__ __forceinline__ uint32_t off_lo(uint32_t x) { return (x & 0x00030003u) | 0x43004300u; }
-__device__ __forceinline__ uint32_t off_hi(uint32_t x) { return (x & 0x000C000Cu) | 0x43004300u; }
-// 4-bit codes c = c0 + 4 c1 from two planes (x0: c0, x1: c1 at the same positions)
-__device__ __forceinline__ uint32_t off4_lo(uint32_t x0, uint32_t x1) {
-    return (x0 & 0x00030003u) | ((x1 & 0x00030003u) << 2) | 0x43004300u;
+// and 128 + 4c (exact); without it (minus 128): c and 4c. The offset pattern
+// k = 0x43004300 comes in a register, so that each pair is one three-input
+// logic op (mask immediate, offset register).
+template <uint32_t M>
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t k) {   // (x & M) | k
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "n"(M), "r"(k));
+    return d;
 }
-__device__ __forceinline__ uint32_t off4_hi(uint32_t x0, uint32_t x1) {
-    return (x0 & 0x000C000Cu) | ((x1 & 0x000C000Cu) << 2) | 0x43004300u;
+__device__ __forceinline__ uint32_t off_lo(uint32_t x, uint32_t k) { return and_or<0x00030003u>(x, k); }
+__device__ __forceinline__ uint32_t off_hi(uint32_t x, uint32_t k) { return and_or<0x000C000Cu>(x, k); }
+// 4-bit codes c = c0 + 4 c1 from two planes (x0: c0, x1: c1 at the same positions)
+__device__ __forceinline__ uint32_t off4_lo(uint32_t x0, uint32_t x1, uint32_t k) {
+    return and_or<0x00030003u>(x0, and_or<0x000C000Cu>(x1 << 2, k));
+}
+__device__ __forceinline__ uint32_t off4_hi(uint32_t x0, uint32_t x1, uint32_t k) {
+    return and_or<0x000C000Cu>(x0, and_or<0x00300030u>(x1 << 2, k));
 }
 __device__ __forceinline__ uint32_t pack_rn(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -466,6 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lm_tok = ((lane >> 4) << 3) + (lane & 7);
     const int lm_hi = (lane >> 3) & 1;
     // the tokens of rows g and g + 8 in a quantised tile
+    // the bf16 offset pattern of the code operands, in a register (Hq >> 31 is 0)
+    const uint32_t k43 = 0x43004300u | ((uint32_t)Hq >> 31);
     const int tA = (g & 1) ? g + 7 : g;
     const int tB = (g & 1) ? g + 8 : g + 1;
 
@@ -572,10 +582,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint2 bq = s_qf[(8 + ks) * 32 + lane];
                     if (kk == 0) {
                         const float2 qb = s_qb[grp * 4 + t];
-                        mma_c(acc, off_lo(xa), off_lo(xb), off_hi(xa), off_hi(xb), bq.x, bq.y, qb.x, qb.y);
+                        mma_c(acc, off_lo(xa, k43), off_lo(xb, k43), off_hi(xa, k43), off_hi(xb, k43), bq.x, bq.y,
+                              qb.x, qb.y);
                     }
                     else
-                        mma(acc, off_lo(xa), off_lo(xb), off_hi(xa), off_hi(xb), bq.x, bq.y);
+                        mma(acc, off_lo(xa, k43), off_lo(xb, k43), off_hi(xa, k43), off_hi(xb, k43), bq.x, bq.y);
                 }
                 const float sA = h2f(pick(kmA, grp)).x, sB = h2f(pick(kmB, grp)).x;
                 x[0] = fmaf(sA, acc[0], x[0]);
@@ -602,11 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint2 bq = s_qf[(8 + ks) * 32 + lane];
                     if (kk == 0) {
                         const float2 qb = s_qb[grp * 4 + t];
-                        mma_c(acc, off4_lo(xa, ya), off4_lo(xb, yb), off4_hi(xa, ya), off4_hi(xb, yb), bq.x, bq.y,
-                              qb.x, qb.y);
+                        mma_c(acc, off4_lo(xa, ya, k43), off4_lo(xb, yb, k43), off4_hi(xa, ya, k43),
+                              off4_hi(xb, yb, k43), bq.x, bq.y, qb.x, qb.y);
                     }
                     else
-                        mma(acc, off4_lo(xa, ya), off4_lo(xb, yb), off4_hi(xa, ya), off4_hi(xb, yb), bq.x, bq.y);
+                        mma(acc, off4_lo(xa, ya, k43), off4_lo(xb, yb, k43), off4_hi(xa, ya, k43),
+                            off4_hi(xb, yb, k43), bq.x, bq.y);
                 }
                 const float sA = h2f(pick(kmA, grp)).x, sB = h2f(pick(kmB, grp)).x;
                 x[0] = fmaf(sA, acc[0], x[0]);
@@ -631,8 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t xa = (kk ? a0w.y : a0w.x) >> (4 * t), ya = (kk ? a1w.y : a1w.x) >> (4 * t);
                         const uint32_t xb = (kk ? b0w.y : b0w.x) >> (4 * t), yb = (kk ? b1w.y : b1w.x) >> (4 * t);
                         const uint2 bq = s_qf[(8 + ks) * 32 + lane];
-                        const uint32_t c0 = bsub128(off4_lo(xa, ya)), c1 = bsub128(off4_lo(xb, yb));
-                        const uint32_t c2 = bsub128(off4_hi(xa, ya)), c3 = bsub128(off4_hi(xb, yb));
+                        const uint32_t c0 = bsub128(off4_lo(xa, ya, k43)), c1 = bsub128(off4_lo(xb, yb, k43));
+                        const uint32_t c2 = bsub128(off4_hi(xa, ya, k43)), c3 = bsub128(off4_hi(xb, yb, k43));
                         if (pp == 0)
                             mma(acc, c0, c1, c2, c3, bq.x, bq.y);
                         else
@@ -666,8 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int mm = 0; mm < 2; ++mm) {
                     const uint32_t x0 = pick(vv, 2 * mm) >> (4 * t), x1 = pick(vv, 2 * mm + 1) >> (4 * t);
-                    pv_mma(o[2 * grp + mm], bsub128(off_lo(x0)), bsub128(off_lo(x1)), bsub128(off_hi(x0)),
-                           bsub128(off_hi(x1)), b0, b1, b2, b3);
+                    pv_mma(o[2 * grp + mm], bsub128(off_lo(x0, k43)), bsub128(off_lo(x1, k43)),
+                           bsub128(off_hi(x0, k43)), bsub128(off_hi(x1, k43)), b0, b1, b2, b3);
                 }
             } else if (P == 2) {
                 const uint4 vv = ld128(vc + g * 64 + grp * 16), vp = ld128(vc + 512 + g * 64 + grp * 16);
@@ -675,8 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int mm = 0; mm < 2; ++mm) {
                     const uint32_t x0 = pick(vv, 2 * mm) >> (4 * t), x1 = pick(vv, 2 * mm + 1) >> (4 * t);
                     const uint32_t y0 = pick(vp, 2 * mm) >> (4 * t), y1 = pick(vp, 2 * mm + 1) >> (4 * t);
-                    pv_mma(o[2 * grp + mm], bsub128(off4_lo(x0, y0)), bsub128(off4_lo(x1, y1)),
-                           bsub128(off4_hi(x0, y0)), bsub128(off4_hi(x1, y1)), b0, b1, b2, b3);
+                    pv_mma(o[2 * grp + mm], bsub128(off4_lo(x0, y0, k43)), bsub128(off4_lo(x1, y1, k43)),
+                           bsub128(off4_hi(x0, y0, k43)), bsub128(off4_hi(x1, y1, k43)), b0, b1, b2, b3);
                 }
             } else {
 #pragma unroll
@@ -689,8 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int mm = 0; mm < 2; ++mm) {
                         const uint32_t x0 = pick(vv, 2 * mm) >> (4 * t), x1 = pick(vv, 2 * mm + 1) >> (4 * t);
                         const uint32_t y0 = pick(vp, 2 * mm) >> (4 * t), y1 = pick(vp, 2 * mm + 1) >> (4 * t);
-                        pv_mma(o[2 * grp + mm], bsub128(off4_lo(x0, y0)), bsub128(off4_lo(x1, y1)),
-                               bsub128(off4_hi(x0, y0)), bsub128(off4_hi(x1, y1)), c0, c1, c2, c3);
+                        pv_mma(o[2 * grp + mm], bsub128(off4_lo(x0, y0, k43)), bsub128(off4_lo(x1, y1, k43)),
+                               bsub128(off4_hi(x0, y0, k43)), bsub128(off4_hi(x1, y1, k43)), c0, c1, c2, c3);
                     }
                 }
             }
