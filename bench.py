@@ -382,6 +382,7 @@ def measure_variants(wl, NL, reps, dev, peak):
     ph = binding.TieredCache(B, NL, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"], per_head=True,
                              fp_capacity=W0, ledger_capacity=W0)
     ph.set_launch_overlap(True)
+    ph.set_cooperative_launch(False)   # the decodes run alone on the GPU
     for l in range(NL):
         k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
         ph.prefill(l, k, v, scores=synth.zipf_scores(seed, l, units, W0, device=dev))
@@ -513,6 +514,7 @@ def measure_mixed_widths(wl, NL, reps, dev, peak):
     mc = binding.TieredCache(B, NL, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"], max_ledger_bits=8,
                              fp_capacity=W0, ledger_capacity=W0)
     mc.set_launch_overlap(True)
+    mc.set_cooperative_launch(False)   # the decodes run alone on the GPU
     zeros = torch.zeros(B, W0, dtype=torch.uint8, device=dev)
     for l in range(NL):
         k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
@@ -592,6 +594,7 @@ def measure_per_config(reps, dev, peak, which="all"):
         NL = int(min(wl["layers"], max(2, math.ceil(3 * 129e6 / per_layer))))
         cache = binding.TieredCache(B, NL, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"])
         cache.set_launch_overlap(True)
+        cache.set_cooperative_launch(False)   # the decodes run alone on the GPU
         for l in range(NL):
             k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
             cache.prefill(l, k, v, scores=synth.zipf_scores(seed, l, B, W0, device=dev))
@@ -704,6 +707,7 @@ def run_native(args, rank, world, local_rank):
     cache = binding.TieredCache(B, NL, Hq, Hkv, w, maxc, budget_frac=wl["beta"], fp_share=wl["rho"])
     # inside the step graph every decode follows the previous layer's decode kernel
     cache.set_launch_overlap(True)
+    cache.set_cooperative_launch(False)   # the decodes run alone on the GPU
     W0 = L0 // w
     for layer in range(NL):
         k, v = synth.kv_tokens(seed, layer, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
@@ -864,7 +868,9 @@ def run_native(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": run_config(wl, NL, world, route_events),
+        "config": dict(run_config(wl, NL, world, route_events),
+                       launch="CUDA graphs of decode launches with programmatic dependent launch; "
+                              "non-cooperative grids (nothing else runs on the GPU)"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(),
                      "kernel": "decode_kernel (tiered split-K decode + combine + score + append)",

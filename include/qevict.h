@@ -397,7 +397,10 @@ qevict_status qevict_get_view(const qevict_cache *cache, int32_t layer, qevict_v
  * device error happened since the last qevict_clear_status). */
 qevict_status qevict_get_status(qevict_cache *cache, void *stream);
 
-/* Reset the sticky device status to QEVICT_OK (enqueued on `stream`). */
+/* Reset the sticky device status to QEVICT_OK (enqueued on `stream`). It also
+ * clears the decode scratch's split records and counters (a decode that gave
+ * up waiting, QEVICT_ERR_TIMEOUT, can leave them inconsistent), so it must not
+ * overlap a decode of this cache on another stream. */
 qevict_status qevict_clear_status(qevict_cache *cache, void *stream);
 
 /* Synchronise `stream` and copy the transition counters to *stats (host). */
@@ -443,6 +446,29 @@ qevict_status qevict_future_missed_mass(qevict_cache *cache, int32_t layer, cons
  * or the projection that produces q): a copy or memset directly before the
  * launch is not waited for. Off by default. */
 qevict_status qevict_set_launch_overlap(qevict_cache *cache, int32_t enable);
+
+/* Launch the decode grid cooperatively (enable != 0, the default) or not. The
+ * splits of a (sequence, KV head) wait for one another, so all CTAs of a
+ * decode must be resident together: a cooperative grid starts only when they
+ * can be, so a kernel on another stream holding SMs delays the decode instead
+ * of leaving its resident splits waiting for the others (up to the wait
+ * limit below, then QEVICT_ERR_TIMEOUT). A cooperative grid cannot start its
+ * CTAs one by one as the kernel before it frees SMs, which costs about a
+ * microsecond per launch; disable it only where nothing else runs on the GPU
+ * while decodes run. */
+qevict_status qevict_set_cooperative_launch(qevict_cache *cache, int32_t enable);
+
+/* Limit, in SM clock cycles (clock64), of every wait of a decode on other CTAs
+ * of the same launch: the splits of a (sequence, KV head) waiting for one
+ * another's records, and the wait before the fused append moves the tables.
+ * A wait that runs out sets QEVICT_ERR_TIMEOUT in the status word and the
+ * kernel finishes without waiting further (its outputs are then not valid);
+ * waits on the CTA's own copies keep their own limit. cycles <= 0 restores the
+ * default, 4e9 cycles (about two seconds at GB300 clocks). With a cooperative
+ * launch all CTAs are resident together and a wait only outlasts the work of
+ * the slowest split when something is wrong; a short limit is a diagnostic,
+ * for tests of the timeout path. */
+qevict_status qevict_set_wait_limit(qevict_cache *cache, int64_t cycles);
 
 /* The kernels keep each layer's context length in device memory and read it
  * when they run, so a CUDA graph captured from these calls can be replayed:

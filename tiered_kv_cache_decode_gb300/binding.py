@@ -27,6 +27,7 @@ EXPORTS = ["qevict_pool_capacity", "qevict_cache_create", "qevict_cache_destroy"
            "qevict_decode_attention", "qevict_decode_step", "qevict_route", "qevict_demote_quantize",
            "qevict_promote_dequantize", "qevict_set_tiers", "qevict_get_scores", "qevict_get_view",
            "qevict_get_status", "qevict_clear_status", "qevict_get_stats", "qevict_set_launch_overlap",
+           "qevict_set_wait_limit", "qevict_set_cooperative_launch",
            "qevict_refresh_lengths", "qevict_decode_attention_static_scratch",
            "qevict_get_tier_move_counts", "qevict_future_missed_mass", "qevict_route_global", "qevict_route_logsparse", "qevict_route_rd",
            "qevict_route_rd_mixed",
@@ -110,6 +111,8 @@ def load() -> ctypes.CDLL:
         "qevict_clear_status": [P, P],
         "qevict_get_stats": [P, ctypes.POINTER(Stats), P],
         "qevict_set_launch_overlap": [P, I32],
+        "qevict_set_wait_limit": [P, I64],
+        "qevict_set_cooperative_launch": [P, I32],
         "qevict_refresh_lengths": [P, P],
         "qevict_decode_attention_static_scratch": [P, I32, P, P, P, I32, P],
         "qevict_get_tier_move_counts": [P, I32, P, P],
@@ -218,6 +221,12 @@ class TieredCache:
 
     def set_launch_overlap(self, enable=True):
         self._check(self.lib.qevict_set_launch_overlap(self.handle, 1 if enable else 0))
+
+    def set_cooperative_launch(self, enable=True):
+        self._check(self.lib.qevict_set_cooperative_launch(self.handle, 1 if enable else 0))
+
+    def set_wait_limit(self, cycles=0):
+        self._check(self.lib.qevict_set_wait_limit(self.handle, int(cycles)))
 
     def refresh_lengths(self, stream=None):
         self._check(self.lib.qevict_refresh_lengths(self.handle, _stream(stream)))

@@ -88,6 +88,7 @@ struct qevict_cache {
     unsigned long long *gkeys = nullptr, *gthr = nullptr;
     int32_t *gflag = nullptr, *gcnt = nullptr;
     bool allow_pdl = false;    // qevict_set_launch_overlap
+    bool coop = true;          // qevict_set_cooperative_launch
 };
 
 namespace {
@@ -315,6 +316,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
     }
     c->cdev.status = reinterpret_cast<int32_t *>(c->cbase);
     c->cdev.stats = reinterpret_cast<unsigned long long *>((uint8_t *)c->cbase + 64);
+    c->cdev.wait_cycles = kDefaultWaitCycles;
 
     // every allocation first, so that a failing allocator leaves nothing behind
     {
@@ -548,7 +550,7 @@ static qevict_status decode_common(qevict_cache *c, int32_t layer, const void *q
     const bool pdl = c->allow_pdl && c->prev_layer >= 0 && c->prev_layer != layer && c->prev_stream == stream;
     cudaError_t e = launch_decode(lh.dev, c->cdev, c->scratch, lh.tmap, layer, (const __nv_bfloat16 *)q,
                                   (const __nv_bfloat16 *)k_new, (const __nv_bfloat16 *)v_new, out, mass,
-                                  accumulate, splits, pdl, (cudaStream_t)stream);
+                                  accumulate, splits, pdl, c->coop, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
     if (k_new) lh.length += 1;
     return QEVICT_OK;
@@ -802,6 +804,29 @@ qevict_status qevict_clear_status(qevict_cache *c, void *stream) {
     if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
     cudaError_t e = cudaMemsetAsync(c->cdev.status, 0, 16, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "status reset");
+    // A decode that gave up waiting may leave tagged split records and counters
+    // behind that a later launch would take for its own: start them afresh.
+    uint8_t *sb = reinterpret_cast<uint8_t *>(c->scratch_base);
+    if (sb) {
+        const size_t n0 = (size_t)(reinterpret_cast<uint8_t *>(c->scratch.rec) - sb);
+        const size_t o1 = (size_t)(reinterpret_cast<uint8_t *>(c->scratch.bar) - sb);
+        e = cudaMemsetAsync(sb, 0, n0, (cudaStream_t)stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(sb + o1, 0, c->scratch_bytes - o1, (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode scratch reset");
+    }
+    note_op(c, -1, stream);
+    return QEVICT_OK;
+}
+
+qevict_status qevict_set_cooperative_launch(qevict_cache *c, int32_t enable) {
+    if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    c->coop = enable != 0;
+    return QEVICT_OK;
+}
+
+qevict_status qevict_set_wait_limit(qevict_cache *c, int64_t cycles) {
+    if (!c) return fail(QEVICT_ERR_INVALID_ARG, "cache is NULL");
+    c->cdev.wait_cycles = cycles > 0 ? (long long)cycles : kDefaultWaitCycles;
     return QEVICT_OK;
 }
 
@@ -994,7 +1019,7 @@ qevict_status qevict_decode_attention_static_scratch(qevict_cache *c, int32_t la
     e = cudaMemsetAsync(p, 0, ly.o_rec, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "static scratch clear");
     e = launch_decode(lh.dev, c->cdev, S, lh.tmap, layer, (const __nv_bfloat16 *)q, nullptr, nullptr, out, mass,
-                      accumulate_scores, splits, false, (cudaStream_t)stream);
+                      accumulate_scores, splits, false, c->coop, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel");
     note_op(c, layer, stream);
     return QEVICT_OK;

@@ -71,7 +71,7 @@ constexpr int kQChunk = 5;                // INT2 tiles per stage at most (7.5 K
 constexpr int kDescTab = 1024;            // claim descriptors of a split kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazy = 8.f;              // log2 headroom before the running max moves
-constexpr long long kWaitCycles = 4000000000ll;   // about two seconds at GB300 clocks
+constexpr long long kWaitCycles = kDefaultWaitCycles;   // waits on this CTA's own copies
 // ring stage: quantised chunk, full-precision unit, a claim of no tokens
 enum { EL_Q = 0, EL_F = 1, EL_SKIP = 3 };
 
@@ -940,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (true) {
                 asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(m64), "=l"(l64) : "l"(r) : "memory");
                 if ((uint32_t)(m64 >> 32) == tag && (uint32_t)(l64 >> 32) == tag) break;
-                if (clock64() - t0 > kWaitCycles) {
+                if (clock64() - t0 > C.wait_cycles) {
                     ok = false;
                     break;
                 }
@@ -987,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if ((uint32_t)(u0 >> 32) == tag && (uint32_t)(u1 >> 32) == tag && (uint32_t)(u2 >> 32) == tag &&
                     (uint32_t)(u3 >> 32) == tag)
                     break;
-                if (clock64() - t0 > kWaitCycles) {
+                if (clock64() - t0 > C.wait_cycles) {
                     ok = false;
                     break;
                 }
@@ -1098,7 +1098,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (true) {
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(n) : "l"(S.arrive_b + b) : "memory");
             if (n >= want) break;
-            if (clock64() - t0 > kWaitCycles) break;
+            if (clock64() - t0 > C.wait_cycles) break;
             __nanosleep(64);
         }
         if (n < want) {
@@ -1199,18 +1199,31 @@ int decode_records(int CF, int CQ, int w, int maxP) {
 
 cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, const CUtensorMap &tmap,
                           int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
-                          float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s) {
+                          float *out, float *mass, int accumulate, int splits, bool pdl, bool coop,
+                          cudaStream_t s) {
     const bool wide = L.maxP > 1;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // The splits of a (sequence, KV head) wait for one another. A cooperative grid
+    // starts only when every CTA can be resident at once, so another kernel holding
+    // SMs delays the start instead of stranding a waiting split.
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (coop) {
+        attr[na].id = cudaLaunchAttributeCooperative;
+        attr[na].val.cooperative = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(splits, L.B * L.Hkv);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kDynSmem;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = na;
 #define QV_CASE(GG)                                                                                          \
     case GG:                                                                                                 \
         return wide ? cudaLaunchKernelEx(&cfg, decode_kernel<GG, true>, L, C, S, tmap, layer, q, knew, vnew,  \

@@ -128,7 +128,9 @@ struct DecodeScratch {
 struct CacheDev {
     int32_t *status;              // [4]: code, layer, info0, info1
     unsigned long long *stats;    // [ST_N]
+    long long wait_cycles;        // limit of a decode's waits on other CTAs (clock64 cycles)
 };
+constexpr long long kDefaultWaitCycles = 4000000000ll;   // about two seconds at GB300 clocks
 
 enum PlanMode { PLAN_ROUTE = 0, PLAN_TIERS = 1, PLAN_PREFILL_SCORES = 2, PLAN_PREFILL_TIERS = 3,
                 PLAN_DEMOTE = 4, PLAN_PROMOTE = 5, PLAN_GLOBAL = 6, PLAN_LOGSPARSE = 7, PLAN_RD = 8,
@@ -204,7 +206,8 @@ cudaError_t launch_prefill_copy(const LayerDev &L, const __nv_bfloat16 *k_ext,
 cudaError_t launch_scores(const LayerDev &L, int n_win, float *out, cudaStream_t s);
 cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScratch &S, const CUtensorMap &tmap,
                           int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
-                          float *out, float *mass, int accumulate, int splits, bool pdl, cudaStream_t s);
+                          float *out, float *mass, int accumulate, int splits, bool pdl, bool coop,
+                          cudaStream_t s);
 cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s);
 // kmap: k_full [sequences * n_tokens][Hkv * hs][128] bf16 as a 3-D tiled map,
 // boxes of 64 channels x 1 KV head x 16 tokens, 128-byte swizzle
