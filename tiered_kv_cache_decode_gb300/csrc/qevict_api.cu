@@ -169,9 +169,12 @@ qevict_status run_plan(qevict_cache *c, LayerHost &lh, const PlanArgs &a, const 
                        const __nv_bfloat16 *v_ext, cudaStream_t s) {
     cudaError_t e = launch_plan(lh.dev, c->cdev, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "plan kernel");
-    const int maxq = c->Wmax < c->CQ ? c->Wmax : c->CQ;
     const int maxf = c->Wmax < c->CF ? c->Wmax : c->CF;
     const bool prefill = a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_PREFILL_TIERS;
+    // a plan quantises at most the windows it demotes from full precision (or, in a
+    // prefill, every window): the grids are sized for that many entries
+    int maxq = c->Wmax < c->CQ ? c->Wmax : c->CQ;
+    if (!prefill && maxf < maxq) maxq = maxf;
     if (a.mode != PLAN_PROMOTE) {
         e = launch_quantize(lh.dev, c->cdev, a.layer, k_ext, v_ext, a.prefill_len, maxq, s);
         if (e != cudaSuccess) return cuda_fail(e, "quantize kernel");

@@ -6,6 +6,7 @@
 // "Methodologie: QEvict" and "Kernmechanismen" (window routing under a byte
 // budget, cumulative scoring, demotion, promotion, write-once ledger).
 #include "qevict_internal.cuh"
+#include "qevict_div.cuh"
 
 #include <cooperative_groups.h>
 namespace cg = cooperative_groups;
@@ -155,6 +156,43 @@ __device__ __forceinline__ uint32_t logsparse_rank(int age, int recent) {
 }
 
 // Exclusive prefix sum over the block of one int per thread; *total gets the sum.
+// N exclusive prefix sums over the block at once (three barriers in all):
+// excl[n] is the sum of v[n] over the threads before this one, tot[n] over all.
+// s_warp holds N * (kPlanThreads / 32) ints.
+template <int N>
+__device__ void block_scan_n(const int (&v)[N], int (&excl)[N], int (&tot)[N], int *s_warp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int nwarp = kPlanThreads / 32;
+    int x[N];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        x[n] = v[n];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x[n], o);
+            if (lane >= o) x[n] += y;
+        }
+        if (lane == 31) s_warp[n * nwarp + warp] = x[n];
+    }
+    __syncthreads();
+    if (warp < N) {
+        int ws = s_warp[warp * nwarp + lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, ws, o);
+            if (lane >= o) ws += y;
+        }
+        s_warp[warp * nwarp + lane] = ws;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        excl[n] = x[n] - v[n] + (warp > 0 ? s_warp[n * nwarp + warp - 1] : 0);
+        tot[n] = s_warp[n * nwarp + nwarp - 1];
+    }
+    __syncthreads();
+}
+
 __device__ int block_scan(int v, int *total, int *s_warp) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int nwarp = kPlanThreads / 32;
@@ -353,8 +391,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     __shared__ uint8_t s_cur[kPlanMaxW];
     __shared__ uint8_t s_tgt[kPlanMaxW];
     __shared__ uint8_t s_old[kPlanMaxW];   // tiers before this plan, for the move's counts
-    __shared__ int s_warp[kPlanThreads / 32 + 1];
+    __shared__ int s_warp[4 * (kPlanThreads / 32)];
     __shared__ int s_cnt[8];
+    __shared__ long long s_budget;
+    __shared__ int s_nfp_budget;
     extern __shared__ unsigned long long s_dyn[];   // the mixed-width route's gains and lists
 
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -365,6 +405,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     const int nw = (int)((length + D.w - 1) / D.w);
     const bool partial_last = (length % D.w) != 0;
     if (tid < 8) s_cnt[tid] = 0;
+    // the tiers as they are (loaded before thread 0's counter updates, which do not touch them)
+    for (int i = tid; i < nw; i += kPlanThreads) s_old[i] = s_cur[i] = prefill ? QEVICT_TIER_FP : D.tier[wb + i];
     if (tid == 0) {   // nothing queued unless this plan queues it
         ctr[CTR_WQ] = 0;
         ctr[CTR_WP] = 0;
@@ -382,9 +424,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         if (tid == 0) reserve_next(D, ctr, b);
         return;
     }
-    // byte budget at this length: B_t = floor(beta * L * Hkv * d * 4)
-    const int64_t budget = (int64_t)floor(D.beta * (double)(length * D.Hkv * kHeadDim * 4));
-    const int nfp_budget = (int)floor((D.rho * (double)budget) / (double)D.c_fp);
+    // byte budget at this length: B_t = floor(beta * L * Hkv * d * 4), and the full-precision
+    // count of the share rule (float64, once, by thread 0: the double division is slow)
+    if (tid == 0) {
+        const int64_t bt = (int64_t)floor(D.beta * (double)(length * D.Hkv * kHeadDim * 4));
+        s_budget = bt;
+        s_nfp_budget = (int)floor((D.rho * (double)bt) / (double)D.c_fp);
+    }
+    __syncthreads();
+    const int64_t budget = s_budget;
+    const int nfp_budget = s_nfp_budget;
     if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD ||
          a.mode == PLAN_RD_MIXED) &&
         budget < D.c_fp) {
@@ -394,9 +443,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         }
         return;
     }
-
-    for (int i = tid; i < nw; i += kPlanThreads) s_old[i] = s_cur[i] = prefill ? QEVICT_TIER_FP : D.tier[wb + i];
-    __syncthreads();
 
     if (a.mode == PLAN_DEMOTE || a.mode == PLAN_PROMOTE) {
         // Listed transitions, applied one by one in list order.
@@ -485,8 +531,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                     if (a.scores) {
                         S = a.scores[(int64_t)b * nw + i];
                     } else {
+                        // the KV heads' partial scores, loaded together, added in head order
+                        const float *spb = D.score_part + (int64_t)b * D.Hkv * D.Wmax + i;
+                        float pv[8];
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) pv[h] = h < D.Hkv ? spb[(int64_t)h * D.Wmax] : 0.f;
                         S = 0.f;
-                        for (int h = 0; h < D.Hkv; ++h) S += D.score_part[((int64_t)b * D.Hkv + h) * D.Wmax + i];
+#pragma unroll
+                        for (int h = 0; h < 8; ++h)
+                            if (h < D.Hkv) S += pv[h];
+                        for (int h = 8; h < D.Hkv; ++h) S += spb[(int64_t)h * D.Wmax];
                     }
                     if (a.mult) S = S * a.mult[(int64_t)b * nw + i];
                     if (S == 0.f) S = 0.f;   // one zero: -0 and +0 rank as equal
@@ -507,9 +561,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                 }
                 return;
             }
-            // bitonic sort, ascending: forced window first, then score desc, index asc
+            // bitonic sort, ascending: forced window first, then score desc, index asc.
+            // Strides of 32 and more exchange through shared memory; the smaller ones
+            // pair lanes of one warp (index bits 0-4 are the lane) through shuffles.
             for (int kk = 2; kk <= P; kk <<= 1) {
-                for (int j = kk >> 1; j > 0; j >>= 1) {
+                int j = kk >> 1;
+                for (; j >= 32; j >>= 1) {
                     for (int i = tid; i < P; i += kPlanThreads) {
                         const int ixj = i ^ j;
                         if (ixj > i) {
@@ -523,6 +580,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                     }
                     __syncthreads();
                 }
+                for (int base = tid & ~31; base < P; base += kPlanThreads) {   // warp-uniform
+                    const int i = base + (tid & 31);
+                    unsigned long long x = i < P ? s_key[i] : ~0ull;
+                    for (int jj = j; jj > 0; jj >>= 1) {
+                        const unsigned ylo = __shfl_xor_sync(0xffffffffu, (unsigned)x, jj);
+                        const unsigned yhi = __shfl_xor_sync(0xffffffffu, (unsigned)(x >> 32), jj);
+                        const unsigned long long y = ((unsigned long long)yhi << 32) | ylo;
+                        // the lower index of an ascending pair keeps the smaller key
+                        const bool take_min = ((i & jj) == 0) == ((i & kk) == 0);
+                        x = take_min ? (x < y ? x : y) : (x < y ? y : x);
+                    }
+                    if (i < P) s_key[i] = x;
+                }
+                __syncthreads();
             }
             int ncand_local = 0;
             for (int i = tid; i < nw; i += kPlanThreads) ncand_local += s_cur[i] != QEVICT_TIER_E;
@@ -541,8 +612,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                 // upgrade finds its merged rank by binary search in the other list, adds up the cost
                 // of the prefix through itself and decides alone. float64 gains, as the counts'
                 // reference computes them.
-                const double alpha = 0.75 / (double)D.c_q;
-                const double gamma = (0.25 - 1.52587890625e-05) / (double)(D.c_fp - D.c_q);
+                __shared__ double s_ag[2];   // the two gain factors, divided once by thread 0
+                if (tid == 0) {
+                    s_ag[0] = 0.75 / (double)D.c_q;
+                    s_ag[1] = (0.25 - 1.52587890625e-05) / (double)(D.c_fp - D.c_q);
+                }
+                __syncthreads();
+                const double alpha = s_ag[0], gamma = s_ag[1];
                 auto score_at = [&](int i) { return key_score(s_key[1 + i]); };   // score of rank i + 1
                 const int n = ncand - 1;
                 const int64_t room = budget - D.c_fp;
@@ -571,9 +647,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
                             ++up_local;
                     }
                 }
-                int up, fp;
-                block_scan(up_local, &up, s_warp);
-                block_scan(fp_local, &fp, s_warp);
+                int rd_v[2] = {up_local, fp_local}, rd_o[2], rd_t[2];
+                block_scan_n<2>(rd_v, rd_o, rd_t, s_warp);
+                const int up = rd_t[0], fp = rd_t[1];
                 n_fp = ncand > 0 ? 1 + fp : 0;
                 n_q = up - fp;
             } else {
@@ -638,11 +714,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             if (c == QEVICT_TIER_FP && is_quant_tier(t) && lg < 0) ++need_lg;
             if ((is_quant_tier(c) && t == QEVICT_TIER_FP) || (prefill && t == QEVICT_TIER_FP)) ++need_fp;
         }
-        int tot_free_fp, tot_free_lg, tot_need_fp, tot_need_lg;
-        const int off_free_fp = block_scan(free_fp, &tot_free_fp, s_warp);
-        const int off_free_lg = block_scan(free_lg, &tot_free_lg, s_warp);
-        const int off_need_fp = block_scan(need_fp, &tot_need_fp, s_warp);
-        const int off_need_lg = block_scan(need_lg, &tot_need_lg, s_warp);
+        int cap_v[4] = {free_fp, free_lg, need_fp, need_lg}, cap_o[4], cap_t[4];
+        block_scan_n<4>(cap_v, cap_o, cap_t, s_warp);
+        const int off_free_fp = cap_o[0], off_free_lg = cap_o[1], off_need_fp = cap_o[2], off_need_lg = cap_o[3];
+        const int tot_free_fp = cap_t[0], tot_free_lg = cap_t[1], tot_need_fp = cap_t[2], tot_need_lg = cap_t[3];
         const int fp_top = ctr[CTR_FP_TOP], lg_top = ctr[CTR_LG_TOP];
         if (fp_top + tot_free_fp < tot_need_fp || lg_top + tot_free_lg < tot_need_lg) {
             if (tid == 0) {
@@ -673,10 +748,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             np_local += (!prefill && is_quant_tier(c) && t == QEVICT_TIER_FP);
             nc_local += (prefill && t == QEVICT_TIER_FP);
         }
-        int tq, tp, tc;
-        int oq = block_scan(nq_local, &tq, s_warp);
-        int op = block_scan(np_local, &tp, s_warp);
-        int oc = block_scan(nc_local, &tc, s_warp);
+        int mv_v[3] = {nq_local, np_local, nc_local}, mv_o[3], mv_t[3];
+        block_scan_n<3>(mv_v, mv_o, mv_t, s_warp);
+        int oq = mv_o[0], op = mv_o[1], oc = mv_o[2];
+        const int tq = mv_t[0], tp = mv_t[1], tc = mv_t[2];
         int nf = off_need_fp, nl = off_need_lg;
         unsigned long long st_dem = 0, st_pro = 0, st_evi = 0, st_lw = 0, st_lr = 0;
         for (int i = w0; i < w1; ++i) {
@@ -758,9 +833,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         nfp_local += s_tgt[i] == QEVICT_TIER_FP;
         nq_local += is_quant_tier(s_tgt[i]);
     }
-    int tf, tq;
-    int of = block_scan(nfp_local, &tf, s_warp);
-    int oq = block_scan(nq_local, &tq, s_warp);
+    int ls_v[2] = {nfp_local, nq_local}, ls_o[2], ls_t[2];
+    block_scan_n<2>(ls_v, ls_o, ls_t, s_warp);
+    int of = ls_o[0], oq = ls_o[1];
+    const int tf = ls_t[0], tq = ls_t[1];
     for (int i = w0; i < w1; ++i) {
         if (s_tgt[i] == QEVICT_TIER_FP) D.fp_list[b * D.CF + of++] = make_int2(i, D.fp_slot[wb + i]);
         if (is_quant_tier(s_tgt[i])) {   // the slot field carries log2 of the window's planes
@@ -800,7 +876,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
 // ---------------------------------------------------------------- quantise
 // INT2 quantisation of one window part (entry, KV head, K or V): per token and
 // group of 32 channels, min16 = fp16(min), scale16 = fp16(fl32(fl32(max-min)/3)),
-// code = clamp(rint(fl32(fl32(x - min16) / scale16)), 0, 3).
+// code = clamp(rint(fl32(fl32(x - min16) / scale16)), 0, 3). The rounded
+// quotient comes from the scale's rounded reciprocal and an FMA correction
+// (div_by_recip), not from a division per element.
 __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, int layer,
                                                         const __nv_bfloat16 *__restrict__ k_ext,
                                                         const __nv_bfloat16 *__restrict__ v_ext,
@@ -852,12 +930,23 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
             const bool bad = !finite || isinf(mq) || isinf(sq);
             if (bad) set_status(C, QEVICT_ERR_DEVICE, layer, b, wi);
             const bool zero = bad || sq == 0.f;
-            uint8_t *cs = s_codes + t * kHeadDim + g * kGroup;
+            // the quotients through the scale's reciprocal, corrected to the rounded quotient;
+            // clamped to [0, levels] (0 for a zero scale), then rounded half to even by adding
+            // 1.5 * 2^23, whose float has the integer in its low mantissa bits (clamping first
+            // gives the same code as rounding first)
+            const float sdiv = zero ? 1.f : sq;
+            const float rs = __frcp_rn(sdiv);
+            const float top = zero ? 0.f : levels;
+            uint32_t *cs = reinterpret_cast<uint32_t *>(s_codes + t * kHeadDim + g * kGroup);
 #pragma unroll
-            for (int j = 0; j < kGroup; ++j) {
-                float c = zero ? 0.f : rintf(__fdiv_rn(__fsub_rn(x[j], mq), zero ? 1.f : sq));
-                c = fminf(fmaxf(c, 0.f), levels);
-                cs[j] = (uint8_t)c;
+            for (int j = 0; j < kGroup; j += 4) {
+                uint32_t c4[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float qv = fminf(fmaxf(div_by_recip(__fsub_rn(x[j + k], mq), sdiv, rs), 0.f), top);
+                    c4[k] = __float_as_uint(__fadd_rn(qv, 12582912.f));
+                }
+                cs[j / 4] = __byte_perm(__byte_perm(c4[0], c4[1], 0x0040), __byte_perm(c4[2], c4[3], 0x0040), 0x5410);
             }
             __half2 *meta = reinterpret_cast<__half2 *>(slotp + lg_tile_off(h, w, t / 16, P) +
                                                         (kv ? qtile_vmeta(P) : qtile_kmeta(P))) +
@@ -1237,7 +1326,7 @@ cudaError_t launch_plan(const LayerDev &L, const CacheDev &C, const PlanArgs &a,
 
 static dim3 work_grid(const LayerDev &L, int max_entries) {
     int gx = max_entries < 1 ? 1 : max_entries;
-    if (gx > 64) gx = 64;
+    if (gx > 256) gx = 256;
     return dim3(gx, L.Hkv * 2, L.B);
 }
 
