@@ -278,6 +278,8 @@ class OracleCache:
         self.L = 0
         self.win = [[] for _ in range(B)]
         self.S = [np.zeros(0, np.float64) for _ in range(B)]
+        self.kch = None   # K-channel group widths [B][Hkv][4] once route_rd_kv has run
+        self.kch_locked = False   # after it: no further tier moves (route_rd_kv)
         self.stats = dict(demotions=0, promotions=0, evictions=0, ledger_writes=0,
                           ledger_reuses=0)
 
@@ -337,7 +339,10 @@ class OracleCache:
             raise StateError("demotion needs a full full-precision window")
         bits = BITS_OF_TIER[tier]
         if win.ledger is None:
-            ck, sk, mk, bk = quantize_groups(win.k.reshape(self.Hkv, self.w, -1, GROUP), bits)
+            if self.kch is None:
+                ck, sk, mk, bk = quantize_groups(win.k.reshape(self.Hkv, self.w, -1, GROUP), bits)
+            else:   # K groups at their channel widths (route_rd_kv)
+                ck, sk, mk, bk = quantize_k_groups(win.k.reshape(self.Hkv, self.w, -1, GROUP), self.kch[b])
             cv, sv, mv, bv = quantize_groups(win.v.reshape(self.Hkv, self.w, -1, GROUP), bits)
             if bk.any() or bv.any():
                 raise QuantError("non-finite value or fp16 overflow in a quantisation group")
@@ -369,6 +374,8 @@ class OracleCache:
 
     def apply_tiers(self, b, new):
         """Move sequence b's windows to tiers ``new``: evict, then demote, then promote."""
+        if self.kch_locked:
+            raise StateError("a layer with K-channel widths takes no further tier moves")
         cur = [win.tier for win in self.win[b]]
         for wi, (c, t) in enumerate(zip(cur, new)):
             if c == TIER_E and t != TIER_E:
@@ -425,12 +432,16 @@ class OracleCache:
             self.set_tiers(tiers)
 
     def demote(self, pairs, tier=TIER_Q):
+        if self.kch_locked:
+            raise StateError("a layer with K-channel widths takes no further tier moves")
         old = [self.tiers_now(b) for b in range(self.B)]
         for b, wi in pairs:
             self._demote(b, wi, tier)
         self.last_counts = np.stack([transition_counts(old[b], self.tiers_now(b)) for b in range(self.B)])
 
     def promote(self, pairs):
+        if self.kch_locked:
+            raise StateError("a layer with K-channel widths takes no further tier moves")
         old = [self.tiers_now(b) for b in range(self.B)]
         for b, wi in pairs:
             self._promote(b, wi)
@@ -828,3 +839,152 @@ def route_global(layers, hs=1, scores_override=None):
             counts.append(transition_counts(old, c.tiers_now(u)))
         c.last_counts = np.stack(counts)
 
+
+
+# ---- the K-channel half of the rate-distortion allocation (an option) -------
+#
+# "Technische Samenvatting: RDKV", 2.1: the distortion weight of a K-cache
+# channel c is the spectral norm of the logit change when the channel is set
+# to zero, w_c = (1/sqrt(d)) ||Q[:, c]||_2 ||K[:, c]||_2. 2.2: the weights are
+# computed once after the prefill (Fase 1); the channels then take widths by
+# the same Lagrangian knapsack, over the tokens Fase 2 kept (Fase 3), so one
+# token's K and V can have different widths. 2.3: the K rows of the packed old
+# stream (Zone A) carry widths {2, 4, 8}.
+#
+# Readings (the library follows the same ones):
+# * Q is the set of query vectors the caller observed over the prefill; the G
+#   query heads of a KV head pool their columns ([positions x G] rows).
+# * Units are the quantiser's groups of 32 channels per KV head: channels of a
+#   group share a scale, so they share a width; a group's weight is the sum of
+#   its 32 channel weights (float32 weights added in channel order in
+#   float64). The widths are {0, 2, 4, 8}: 0 drops the group's channels from
+#   the logits, 16-bit K belongs to full-precision windows (Zone B/C).
+# * Every group keeps its fp16 scale and minimum (zero for a dropped group), so
+#   a group costs 4 b + 4 bytes per token at width b.
+# * The K budget is what the K halves of the windows Fase 2 quantised occupy at
+#   their widths; the channel allocation redistributes it over the groups of
+#   all KV heads of the sequence: from all groups at 0, steps a -> b along
+#   0 -> 2 -> 4 -> 8 with gain (2^-a - 2^-b) W_g per byte are taken by gain,
+#   highest first (a lower step, then the lower unit (KV head, group) on a
+#   tie), while positive, until the first that does not fit, as in A31.
+# * The allocation runs with the layer's first quantisation: the K widths are
+#   then fixed for the sequence (the ledger is written once), and the layer
+#   takes no further routing events or listed moves.
+
+K_WIDTHS = (0, 2, 4, 8)
+
+
+def k_channel_weights(q_obs, k_full, Hkv: int):
+    """RDKV 2.1's K-channel weights, float64 [B][Hkv][d].
+
+    q_obs: [B][n_q][Hq][d] observed queries; k_full: [B][n][Hkv][d] the keys."""
+    q = np.asarray(q_obs, np.float64)
+    k = np.asarray(k_full, np.float64)
+    B, nq, Hq, d = q.shape
+    G = Hq // Hkv
+    qg = q.reshape(B, nq, Hkv, G, d)
+    qn = np.sqrt((qg * qg).sum(axis=(1, 3)))            # [B][Hkv][d]
+    kn = np.sqrt((k * k).sum(axis=1))                   # [B][Hkv][d]
+    return qn * kn / math.sqrt(d)
+
+
+def k_group_cost(bits: int) -> int:
+    """Bytes one token spends on one 32-channel K group at a width."""
+    return GROUP * bits // 8 + 4
+
+
+def k_channel_widths(weights32, n_tok: int, budget: int):
+    """Widths [Hkv][4] of one sequence's K groups (Fase 3), given the float32
+    channel weights [Hkv][d], the tokens of the quantised windows and the K
+    budget in bytes."""
+    wts = np.asarray(weights32, np.float32)
+    Hkv, d = wts.shape
+    ng = d // GROUP
+    units = [(h, g) for h in range(Hkv) for g in range(ng)]
+    Wg = [sum(float(x) for x in wts[h, g * GROUP:(g + 1) * GROUP]) for h, g in units]
+    widths = [0] * len(units)
+    if n_tok <= 0:
+        return np.zeros((Hkv, ng), np.int64)
+    used = n_tok * len(units) * k_group_cost(0)
+    ups = []
+    for u, W in enumerate(Wg):
+        for i in range(len(K_WIDTHS) - 1):
+            a, b = K_WIDTHS[i], K_WIDTHS[i + 1]
+            cost = n_tok * (k_group_cost(b) - k_group_cost(a))
+            kk = (2.0 ** -a - 2.0 ** -b) / cost
+            ups.append((kk * W, i, u, cost))
+    ups.sort(key=lambda e: (-e[0], e[1], e[2]))
+    steps = [0] * len(units)
+    for gain, i, u, cost in ups:
+        if gain <= 0.0 or used + cost > budget:
+            break
+        assert steps[u] == i, "a group's steps come in order"
+        used += cost
+        steps[u] += 1
+    for u in range(len(units)):
+        widths[u] = K_WIDTHS[steps[u]]
+    return np.array(widths, np.int64).reshape(Hkv, ng)
+
+
+def quantize_k_groups(x, kw):
+    """K of one window ([Hkv][w][ng][32] bf16 values) with group g of KV head h
+    at width kw[h][g]: codes, fp16 scale and minimum as quantize_groups gives
+    them at that width; a group at width 0 has zero codes and meta."""
+    x = np.asarray(x, np.float32)
+    Hkv, w, ng, _ = x.shape
+    codes = np.zeros(x.shape, np.uint8)
+    s16 = np.zeros((Hkv, w, ng), np.float16)
+    m16 = np.zeros((Hkv, w, ng), np.float16)
+    bad = np.zeros((Hkv, w, ng), bool)
+    for h in range(Hkv):
+        for g in range(ng):
+            bits = int(kw[h][g])
+            if bits == 0:
+                continue
+            c, sc, mn, bd = quantize_groups(x[h, :, g], bits)
+            codes[h, :, g], s16[h, :, g], m16[h, :, g], bad[h, :, g] = c, sc, mn, bd
+    return codes, s16, m16, bad
+
+
+def route_rd_kv(cache, weights32, scores_override=None, max_bits=8):
+    """The rate-distortion route with the K-channel half: the window widths of
+    route_rd_mixed (Fase 2), then the K group widths of each sequence
+    (Fase 3, k_channel_widths) from the float32 channel weights [B][Hkv][d];
+    the quantised windows' K groups take those widths, their V the window's.
+    Needs a layer none of whose windows has been quantised."""
+    if cache.kch is not None or any(win.ledger is not None for b in range(cache.B) for win in cache.win[b]):
+        raise StateError("the K-channel widths are set with the layer's first quantisation")
+    wts = np.asarray(weights32, np.float32)
+    if scores_override is not None:
+        ov = np.asarray(scores_override, np.float64)
+        cache.S = [ov[b, :cache.W].copy() for b in range(cache.B)]
+    W = cache.W
+    plans = []
+    for b in range(cache.B):
+        old = cache.tiers_now(b)
+        S = cache.S[b]
+        cand = [i for i in range(W) if old[i] != TIER_E]
+        if not all(math.isfinite(float(S[i])) for i in cand):
+            raise OracleError("non-finite score among routing candidates")
+        forced = W - 1
+        order = sorted(cand, key=lambda i: (i != forced, -float(S[i]), i))
+        rest = order[1:]
+        free = [0] + [x for x in (2, 4, 8) if x <= max_bits] + [16]
+        widths = rd_mixed_widths([S[i] for i in rest], [free] * len(rest), cache.L, cache.w, cache.Hkv,
+                                 cache.d, cache.beta)
+        new = np.array(old, np.uint8)
+        if order:
+            new[order[0]] = TIER_FP
+        for i, bits in zip(rest, widths):
+            new[i] = TIER_OF_BITS[bits]
+        q_bits = [bits for bits in widths if bits in (2, 4, 8)]
+        n_tok = len(q_bits) * cache.w
+        k_budget = sum(width_cost(cache.w, cache.Hkv, cache.d, bits) // 2 for bits in q_bits)
+        plans.append((old, new, k_channel_widths(wts[b], n_tok, k_budget)))
+    cache.kch = np.stack([p[2] for p in plans])
+    counts = []
+    for b, (old, new, _) in enumerate(plans):
+        cache.apply_tiers(b, new)
+        counts.append(transition_counts(old, cache.tiers_now(b)))
+    cache.last_counts = np.stack(counts)
+    cache.kch_locked = True
