@@ -169,6 +169,12 @@ typedef struct qevict_view {
     const uint8_t *ledger_pool;
     const uint8_t *ledger_bits;   /* [b * max_windows + w] width of the ledger entry: 0, 2, 4 or 8 */
     int32_t max_ledger_bits;
+    /* [b][Hkv][4] K group widths (0, 2, 4, 8) of a layer routed by
+     * qevict_route_rd_kv, else NULL. Its quantised windows' ledger tiles then
+     * hold, per 16 tokens: for each group in turn width / 2 planes of
+     * [16 tokens][8 B] codes, the K meta [16][4] half2 (scale, minimum), the V
+     * codes and V meta of the window's width; tiles at a stride of 4608 B. */
+    const uint8_t *k_group_bits;
 } qevict_view;
 
 typedef struct qevict_stats {
@@ -317,6 +323,48 @@ qevict_status qevict_route_rd(qevict_cache *cache, int32_t layer, const float *s
  * max_ledger_bits. */
 qevict_status qevict_route_rd_mixed(qevict_cache *cache, int32_t layer, const float *scores_override,
                                     const float *score_mult, void *stream);
+
+/* The distortion weights of the K-cache channels ("Technische Samenvatting:
+ * RDKV", 2.1: w_c = (1/sqrt(d)) ||Q[:, c]||_2 ||K[:, c]||_2; 2.2 Fase 1: once,
+ * after the prefill, from the uncompressed cache), per sequence, KV head and
+ * channel. Reads nothing of the cache but its shapes.
+ *  q_obs    bf16 [batch][n_q][Hq][head_dim], device: query vectors observed
+ *           over the prefill; the G query heads of a KV head pool their
+ *           columns (n_q * G rows per channel).
+ *  k_full   bf16 [batch][n_tokens][Hkv][head_dim], device: the layer's keys as
+ *           given to qevict_prefill.
+ *  weights  fp32 [batch][Hkv][head_dim], device, written. Sums of squares in
+ *           fp32 over eight interleaved stripes of rows, then their roots.
+ * INVALID_ARG for NULL pointers, non-positive counts or a cache with tiers
+ * per KV head. */
+qevict_status qevict_k_channel_weights(qevict_cache *cache, int32_t layer, const void *q_obs, int64_t n_q,
+                                      const void *k_full, int64_t n_tokens, float *weights, void *stream);
+
+/* The rate-distortion routing event with RDKV's K-channel half ("Technische
+ * Samenvatting: RDKV", 2.2 Fase 2 and 3, 2.3 Zone A). First the window widths
+ * of qevict_route_rd_mixed (every window is then full precision or evicted,
+ * so each has the chain 0, 2, 4, 8, 16). Then, per sequence, the 32-channel K
+ * groups of all KV heads take widths {0, 2, 4, 8} within the bytes the K
+ * halves of the quantised windows have at their widths: a group costs 4 b + 4
+ * bytes per token (codes, and the fp16 scale and minimum it always keeps),
+ * its weight W is the sum of its channels' weights (float32 from
+ * qevict_k_channel_weights, added in channel order in float64), and from all
+ * groups at 0 the steps a -> b of gain (2^-a - 2^-b) / (tokens * (cost(b) -
+ * cost(a))) * W per byte are taken by gain, highest first (a lower step, then
+ * the lower (KV head, group) on a tie), while positive, until the first that
+ * does not fit. The quantised windows' K groups are quantised at those
+ * widths (width 0: no codes, zero meta, the channels leave the logits), their
+ * V at the window's width; decoding reads both. The widths are fixed with the
+ * layer's first quantisation: the call needs a layer none of whose windows
+ * has a ledger entry (STATE in the device status otherwise), and afterwards
+ * the layer takes appends and decodes but no further tier moves (routes,
+ * listed moves and qevict_set_tiers return STATE).
+ *  weights  fp32 [batch][Hkv][head_dim], device (qevict_k_channel_weights).
+ * INVALID_ARG unless the cache has max_ledger_bits 8, shared tiers and at
+ * most 16 KV heads; otherwise the errors of qevict_route_rd_mixed. The
+ * widths can be read through qevict_get_view (k_group_bits). */
+qevict_status qevict_route_rd_kv(qevict_cache *cache, int32_t layer, const float *weights,
+                                 const float *scores_override, void *stream);
 
 /* A routing event by position instead of score ("Technische Samenvatting:
  * LogQuant", Methodologie 1-2: attention peaks thin out logarithmically with

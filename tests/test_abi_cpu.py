@@ -39,8 +39,9 @@ def test_struct_layouts_match_header_sizes():
     assert ctypes.sizeof(binding.Config) == 64
     assert binding.Config.tier_per_kv_head.offset == 56 and binding.Config.max_ledger_bits.offset == 60
     assert ctypes.sizeof(binding.Stats) == 48
-    # 9 int32, padding, 3 int64, 7 pointers, int32 and tail padding
-    assert ctypes.sizeof(binding.View) == 9 * 4 + 4 + 3 * 8 + 7 * 8 + 8
+    # 9 int32, padding, 3 int64, 7 pointers, int32 and padding, the K group widths pointer
+    assert ctypes.sizeof(binding.View) == 9 * 4 + 4 + 3 * 8 + 7 * 8 + 8 + 8
+    assert binding.View.k_group_bits.offset == 128
 
 
 def _cfg(**kw):

@@ -30,7 +30,7 @@ EXPORTS = ["qevict_pool_capacity", "qevict_cache_create", "qevict_cache_destroy"
            "qevict_set_wait_limit", "qevict_set_cooperative_launch",
            "qevict_refresh_lengths", "qevict_decode_attention_static_scratch",
            "qevict_get_tier_move_counts", "qevict_future_missed_mass", "qevict_route_global", "qevict_route_logsparse", "qevict_route_rd",
-           "qevict_route_rd_mixed",
+           "qevict_route_rd_mixed", "qevict_k_channel_weights", "qevict_route_rd_kv",
            "qevict_length",
            "qevict_last_error"]
 
@@ -70,7 +70,8 @@ class View(ctypes.Structure):
                 ("tier", ctypes.c_void_p), ("fp_slot", ctypes.c_void_p),
                 ("ledger_slot", ctypes.c_void_p), ("ledger_writes", ctypes.c_void_p),
                 ("fp_pool", ctypes.c_void_p), ("ledger_pool", ctypes.c_void_p),
-                ("ledger_bits", ctypes.c_void_p), ("max_ledger_bits", ctypes.c_int32)]
+                ("ledger_bits", ctypes.c_void_p), ("max_ledger_bits", ctypes.c_int32),
+                ("k_group_bits", ctypes.c_void_p)]
 
 
 class Stats(ctypes.Structure):
@@ -120,6 +121,8 @@ def load() -> ctypes.CDLL:
         "qevict_route_logsparse": [P, I32, I32, P],
         "qevict_route_rd": [P, I32, P, P, P],
         "qevict_route_rd_mixed": [P, I32, P, P, P],
+        "qevict_k_channel_weights": [P, I32, P, I64, P, I64, P, P],
+        "qevict_route_rd_kv": [P, I32, P, P, P],
         "qevict_future_missed_mass": [P, I32, P, P, I64, P, P],
         "qevict_length": [P, I32],
         "qevict_last_error": [],
@@ -374,17 +377,81 @@ class TieredCache:
         x = raw.view(torch.bfloat16).view(H, 2, 2, self.w, 64)     # [kvh][kv][half][token][64]
         return x.permute(0, 1, 3, 2, 4).reshape(H, 2, self.w, HEAD_DIM)
 
-    def ledger_window(self, layer, slot, bits=2):
+    def ledger_window(self, layer, slot, bits=2, seq=None):
         """Decoded ledger slot of a window quantised to `bits` (2, 4, 8): codes
-        uint8 [Hkv][2][w][d], scale/min fp16 [Hkv][2][w][d/32]."""
+        uint8 [Hkv][2][w][d], scale/min fp16 [Hkv][2][w][d/32]. On a layer
+        routed with K channels, `seq` names the sequence whose K group widths
+        the tiles follow."""
         v = self.view(layer)
         raw = device_tensor(v.ledger_pool + slot * v.ledger_slot_bytes, (v.ledger_slot_bytes,), "|u1").cpu()
+        if v.k_group_bits:
+            kgw = self.k_group_bits(layer)[seq if seq is not None else slot // v.ledger_capacity]
+            return decode_kch_slot(raw, v.num_kv_heads, self.w, bits, kgw)
         return decode_ledger_slot(raw, v.num_kv_heads, self.w, bits)
+
+    def k_group_bits(self, layer):
+        """uint8 [batch][Hkv][4] K group widths of a layer routed by route_rd_kv (else None)."""
+        v = self.view(layer)
+        if not v.k_group_bits:
+            return None
+        return device_tensor(v.k_group_bits, (v.batch, v.num_kv_heads, 4), "|u1").cpu()
+
+    # ---- RDKV's K-channel half -----------------------------------------------
+    def k_channel_weights(self, layer, q_obs, k_full, stream=None):
+        """fp32 [B][Hkv][d] channel weights from observed queries [B][n_q][Hq][d]
+        and keys [B][n][Hkv][d] (bf16, device)."""
+        out = torch.empty(self.B, self.Hkv, HEAD_DIM, dtype=torch.float32, device=k_full.device)
+        self._check(self.lib.qevict_k_channel_weights(self.handle, layer, _ptr(q_obs), q_obs.shape[1], _ptr(k_full),
+                                                      k_full.shape[1], _ptr(out), _stream(stream)))
+        return out
+
+    def route_rd_kv(self, layer, weights, scores_override=None, stream=None):
+        self._check(self.lib.qevict_route_rd_kv(self.handle, layer, _ptr(weights), _ptr(scores_override),
+                                                _stream(stream)))
 
     def ledger_bits(self, layer):
         """uint8 [units][W]: width of each window's ledger entry (0 none, 2, 4, 8), host copy."""
         v = self.view(layer)
         return device_tensor(v.ledger_bits, (v.batch, v.max_windows), "|u1")[:, :v.num_windows].cpu()
+
+
+def decode_kch_slot(raw: torch.Tensor, Hkv: int, w: int, bits: int, kgw):
+    """Unpack a K-channel ledger slot (see qevict_view.k_group_bits): tiles of
+    4608 B; per tile the K groups' planes in turn ([16 tokens][2 words] each),
+    the K meta, then the V codes and meta of a `bits` window. Returns what
+    decode_ledger_slot returns."""
+    d = HEAD_DIM
+    nt = w // 16
+    P = bits // 2
+    raw = raw[:Hkv * nt * 4608].view(Hkv, nt, 4608)
+    shifts = torch.arange(16, dtype=torch.int64) * 2
+    i = torch.arange(d)
+    ch = 16 * ((i >> 1) & 7) + (i >> 4) + 8 * (i & 1)
+    kcodes = torch.zeros(Hkv, nt * 16, d, dtype=torch.int64)
+    vcodes = torch.zeros(Hkv, nt * 16, d, dtype=torch.int64)
+    km = torch.zeros(Hkv, nt * 16, 4, 2, dtype=torch.float16)
+    vm = torch.zeros(Hkv, nt * 16, 4, 2, dtype=torch.float16)
+    for h in range(Hkv):
+        goff = 0
+        for g in range(4):
+            for p in range(int(kgw[h][g]) // 2):
+                kw = raw[h, :, goff + 128 * p:goff + 128 * (p + 1)].contiguous().view(torch.int32).to(torch.int64)
+                kc = ((kw & 0xFFFFFFFF).view(nt, 16, 2)[..., None] >> shifts) & 3                # [nt][tok][2][16]
+                kcodes[h, :, 32 * g:32 * (g + 1)] |= kc.reshape(nt * 16, 32) << (2 * p)
+            goff += 128 * (int(kgw[h][g]) // 2)
+        km[h] = raw[h, :, goff:goff + 256].contiguous().view(torch.float16).view(nt * 16, 4, 2)
+        for p in range(P):
+            v0 = goff + 256 + 512 * p
+            vw = raw[h, :, v0:v0 + 512].contiguous().view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+            vc = (vw[..., None] >> shifts) & 3
+            vp = torch.empty(nt, d, 16, dtype=torch.int64)
+            vp[:, ch] = vc
+            vcodes[h] |= vp.permute(0, 2, 1).reshape(nt * 16, d) << (2 * p)
+        v1 = goff + 256 + 512 * P
+        vm[h] = raw[h, :, v1:v1 + 256].contiguous().view(torch.float16).view(nt * 16, 4, 2)
+    codes = torch.stack([kcodes, vcodes], dim=1).to(torch.uint8)
+    meta = torch.stack([km, vm], dim=1)
+    return codes, meta[..., 0].clone(), meta[..., 1].clone()
 
 
 def decode_ledger_slot(raw: torch.Tensor, Hkv: int, w: int, bits: int = 2):

@@ -33,6 +33,7 @@ qevict_status cuda_fail(cudaError_t e, const char *what) {
 
 struct LayerHost {
     LayerDev dev{};
+    bool kch = false;       // routed by qevict_route_rd_kv: no further tier moves
     CUtensorMap tmap{};     // 4-D tiled view of the full-precision pool, 64 x 16 x 4 boxes
     int64_t length = 0;
     void *base = nullptr;
@@ -167,6 +168,8 @@ void note_op(qevict_cache *c, int layer, void *stream) {
 // slots released by demotions), then promote / prefill copy (write slots).
 qevict_status run_plan(qevict_cache *c, LayerHost &lh, const PlanArgs &a, const __nv_bfloat16 *k_ext,
                        const __nv_bfloat16 *v_ext, cudaStream_t s) {
+    if (lh.kch && a.mode != PLAN_RD_KV)
+        return fail(QEVICT_ERR_STATE, "layer %d has K-channel widths and takes no further tier moves", a.layer);
     cudaError_t e = launch_plan(lh.dev, c->cdev, a, s);
     if (e != cudaSuccess) return cuda_fail(e, "plan kernel");
     const int maxf = c->Wmax < c->CF ? c->Wmax : c->CF;
@@ -411,6 +414,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         const size_t o_wc = cv.take((size_t)B * Wmax * 16);
         const size_t o_dg = cv.take((size_t)B * 8 * 4);
         const size_t o_lb = cv.take((size_t)B * Wmax);
+        const size_t o_kg = cv.take((size_t)B * Hkv * kGroups);
         uint8_t *base = (uint8_t *)dev_alloc(c, cv.off);
         if (!base) {
             const size_t need = cv.off;
@@ -436,6 +440,7 @@ qevict_status qevict_cache_create(const qevict_config *config, const qevict_allo
         D.work_c = (int4 *)(base + o_wc);
         D.diag = (int32_t *)(base + o_dg);
         D.lbits = base + o_lb;
+        D.kgw = base + o_kg;
     }
     err = prepare_decode();
     EncodeTiledFn enc = encode_tiled();
@@ -591,6 +596,48 @@ qevict_status qevict_route_rd(qevict_cache *c, int32_t layer, const float *score
     a.layer = layer;
     a.scores = scores_override;
     a.mult = score_mult;
+    return run_plan(c, lh, a, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+qevict_status qevict_k_channel_weights(qevict_cache *c, int32_t layer, const void *q_obs, int64_t n_q,
+                                      const void *k_full, int64_t n_tokens, float *weights, void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!q_obs || !k_full || !weights) return fail(QEVICT_ERR_INVALID_ARG, "q_obs, k_full and weights must be set");
+    if (n_q < 1 || n_tokens < 1 || n_q > INT32_MAX)
+        return fail(QEVICT_ERR_INVALID_ARG, "n_q (%lld) and n_tokens (%lld) must be positive", (long long)n_q,
+                    (long long)n_tokens);
+    if (c->hs != 1) return fail(QEVICT_ERR_INVALID_ARG, "K-channel weights need shared tiers (not per KV head)");
+    cudaError_t e = launch_k_channel_weights(c->layers[layer].dev, (const __nv_bfloat16 *)q_obs, (int)n_q,
+                                             (const __nv_bfloat16 *)k_full, n_tokens, weights, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "K channel weights kernel");
+    note_op(c, -1, stream);
+    return QEVICT_OK;
+}
+
+qevict_status qevict_route_rd_kv(qevict_cache *c, int32_t layer, const float *weights, const float *scores_override,
+                                 void *stream) {
+    qevict_status st = check_layer(c, layer);
+    if (st) return st;
+    if (!weights) return fail(QEVICT_ERR_INVALID_ARG, "weights must be set");
+    if (c->cfg.max_ledger_bits != 8)
+        return fail(QEVICT_ERR_INVALID_ARG, "K-channel routing needs max_ledger_bits 8 (this cache: %d)",
+                    c->cfg.max_ledger_bits);
+    if (c->hs != 1) return fail(QEVICT_ERR_INVALID_ARG, "K-channel routing needs shared tiers (not per KV head)");
+    if (c->cfg.num_kv_heads > 16) return fail(QEVICT_ERR_INVALID_ARG, "K-channel routing takes at most 16 KV heads");
+    LayerHost &lh = c->layers[layer];
+    if (lh.kch) return fail(QEVICT_ERR_STATE, "layer %d already has its K-channel widths", layer);
+    if (lh.length == 0) return QEVICT_OK;
+    const int64_t Bt = budget_bytes(c->cfg, lh.length);
+    if (Bt < c->c_fp)
+        return fail(QEVICT_ERR_BUDGET, "budget %lld B cannot hold the open window (%lld B)", (long long)Bt,
+                    (long long)c->c_fp);
+    PlanArgs a{};
+    a.mode = PLAN_RD_KV;
+    a.layer = layer;
+    a.scores = scores_override;
+    a.kweights = weights;
+    lh.kch = true;
     return run_plan(c, lh, a, nullptr, nullptr, (cudaStream_t)stream);
 }
 
@@ -786,6 +833,7 @@ qevict_status qevict_get_view(const qevict_cache *c, int32_t layer, qevict_view 
     v->ledger_pool = D.lg_pool;
     v->ledger_bits = D.lbits;
     v->max_ledger_bits = 2 * D.maxP;
+    v->k_group_bits = lh.kch ? D.kgw : nullptr;
     return QEVICT_OK;
 }
 

@@ -236,13 +236,15 @@ constexpr int kRecMax = 8;     // records per window: 16-token tiles (w <= 128)
 struct ClaimPlan {
     int64_t length;
     int n_win, qw0, nqw, fw0, nfw, f0, nfl, tpc, cpw, tailw, nbig, N;
+    int kcodes;   // K code bytes of a K-channel tile of this KV head, or -1 (plane tiles)
 };
 
 template <bool kWide>
-__device__ __forceinline__ ClaimPlan claim_plan(const LayerDev &D, int b, int split, int splits, int mu) {
+__device__ __forceinline__ ClaimPlan claim_plan(const LayerDev &D, int b, int kvh, int split, int splits, int mu) {
     const int32_t *ctr = D.ctr + b * kCtrN;
     ClaimPlan p;
     p.length = ctr[CTR_LEN];
+    p.kcodes = (kWide && ctr[CTR_KCH] != 0) ? ktile_kcodes(D.kgw + ((int64_t)b * D.Hkv + kvh) * kGroups) : -1;
     const int n_fp = ctr[CTR_NFP], n_q = ctr[CTR_NQ];
     p.n_win = (int)((p.length + D.w - 1) / D.w);
     // (window counts are at most 4096 and splits at most 32: 32-bit products suffice)
@@ -297,6 +299,11 @@ __device__ __forceinline__ int4 claim_desc(const LayerDev &D, const ClaimPlan &p
     const int lgP = kWide ? (en.y >> kSlotBits) : 0;
     const int slot = kWide ? (en.y & ((1 << kSlotBits) - 1)) : en.y;
     const int P = 1 << lgP;
+    if (kWide && p.kcodes >= 0) {   // K-channel tiles sit at the widest tile's stride
+        const int64_t off = (int64_t)slot * D.lg_slot_bytes + ((int64_t)kvh * mu + u0) * qtile_bytes(4);
+        return make_int4(EL_Q | (n << 2) | (lgP << 7), D.CF * mu + e * mu + u0, (int)(off >> 9),
+                         n * ktile_bytes(p.kcodes, P));
+    }
     const int64_t off = (int64_t)slot * D.lg_slot_bytes + lg_tile_off(kvh, w, u0, P);
     return make_int4(EL_Q | (n << 2) | (lgP << 7), D.CF * mu + e * mu + u0, (int)(off >> 9), n * qtile_bytes(P));
 }
@@ -336,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ long long s_len;               // the sequence's length at launch
     __shared__ int s_slot_new;                // slot of the new token's window (split 0, fused append)
     __shared__ uint32_t s_gen;                // split-record generation of this launch
+    __shared__ int s_kg[9];                   // K-channel tiles: planes and code offset of each group, code bytes
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -347,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- claim descriptors, built by all threads at once
     const int N = [&]() {
-        const ClaimPlan p = claim_plan<kWide>(D, b, split, splits, mu);
+        const ClaimPlan p = claim_plan<kWide>(D, b, kvh, split, splits, mu);
         for (int c = tid; c < min(p.N, kDescTab); c += kThreads) s_desc[c] = claim_desc<kWide>(D, p, b, kvh, mu, c);
         if (tid == 0) {
             s_span[0] = p.qw0;
@@ -355,6 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_span[2] = p.fw0;
             s_span[3] = p.nfw;
             s_len = p.length;
+            s_kg[8] = p.kcodes;
+            if (kWide && p.kcodes >= 0) {
+                const uint8_t *kw = D.kgw + ((int64_t)b * Hkv + kvh) * kGroups;
+                int off = 0;
+                for (int gg = 0; gg < kGroups; ++gg) {
+                    s_kg[gg] = kgroup_planes(kw[gg]);
+                    s_kg[4 + gg] = off;
+                    off += 128 * s_kg[gg];
+                }
+            }
             if (knew != nullptr && split == 0 && p.length < D.max_context) {
                 const int64_t wn = p.length / w;
                 s_slot_new = (p.length % w == 0) ? D.ctr[b * kCtrN + CTR_NEXT] : D.fp_slot[(int64_t)b * D.Wmax + wn];
@@ -385,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const int4 d = c < kDescTab ? s_desc[c]
-                                        : claim_desc<kWide>(D, claim_plan<kWide>(D, b, split, splits, mu), b, kvh, mu, c);
+                                        : claim_desc<kWide>(D, claim_plan<kWide>(D, b, kvh, split, splits, mu), b,
+                                                            kvh, mu, c);
             const int kind = d.x & 3, n = (d.x >> 2) & 31;
             if (kind == EL_SKIP) continue;
             if (lane == 0) {
@@ -560,7 +579,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- one quantised 16-token tile at `base` with P code planes
     auto quant_tile = [&](const uint8_t *base, int P) {
-        const uint8_t *km = base + qtile_kmeta(P), *vc = base + qtile_vcodes(P), *vm = base + qtile_vmeta(P);
+        // a K-channel tile: K groups of their own widths ahead of the K meta (kcodes bytes)
+        const int kcodes = kWide ? s_kg[8] : -1;
+        const uint8_t *km = base + (kcodes >= 0 ? kcodes : qtile_kmeta(P));
+        const uint8_t *vc = base + (kcodes >= 0 ? kcodes + 256 : qtile_vcodes(P));
+        const uint8_t *vm = base + (kcodes >= 0 ? kcodes + 256 + 512 * P : qtile_vmeta(P));
         // minimum share: one fp16 MMA; A rows g / g + 8 hold the tokens' group-t minimums twice
         float x[4];
         {
@@ -568,7 +591,73 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16_k8(x, __byte_perm(mA, 0, 0x3232), __byte_perm(mB, 0, 0x3232), qs_frag);
         }
         const uint4 kmA = ld128(km + tA * 16), kmB = ld128(km + tB * 16);
-        if (!kWide || P == 1) {
+        if (kWide && kcodes >= 0) {
+            // K-channel tile: group grp has Pg planes of [16 tokens][8 B] at its offset;
+            // a group of width 0 takes no part (its minimum is 0 in the meta as well)
+#pragma unroll
+            for (int grp = 0; grp < kGroups; ++grp) {
+                const int Pg = s_kg[grp];
+                if (Pg == 0) continue;
+                const uint8_t *gb = base + s_kg[4 + grp];
+                const float sA = h2f(pick(kmA, grp)).x, sB = h2f(pick(kmB, grp)).x;
+                if (Pg == 1 || Pg == 2) {
+                    float acc[4];
+                    const uint2 a0 = ld64(gb + tA * 8), b0 = ld64(gb + tB * 8);
+                    uint2 a1 = a0, b1 = b0;
+                    if (Pg == 2) {
+                        a1 = ld64(gb + 128 + tA * 8);
+                        b1 = ld64(gb + 128 + tB * 8);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 2; ++kk) {
+                        const int ks = 2 * grp + kk;
+                        const uint32_t xa = (kk ? a0.y : a0.x) >> (4 * t), xb = (kk ? b0.y : b0.x) >> (4 * t);
+                        const uint32_t ya = (kk ? a1.y : a1.x) >> (4 * t), yb = (kk ? b1.y : b1.x) >> (4 * t);
+                        const uint32_t c0 = Pg == 1 ? off_lo(xa, k43) : off4_lo(xa, ya, k43);
+                        const uint32_t c1 = Pg == 1 ? off_lo(xb, k43) : off4_lo(xb, yb, k43);
+                        const uint32_t c2 = Pg == 1 ? off_hi(xa, k43) : off4_hi(xa, ya, k43);
+                        const uint32_t c3 = Pg == 1 ? off_hi(xb, k43) : off4_hi(xb, yb, k43);
+                        const uint2 bq = s_qf[(8 + ks) * 32 + lane];
+                        if (kk == 0) {
+                            const float2 qb = s_qb[grp * 4 + t];
+                            mma_c(acc, c0, c1, c2, c3, bq.x, bq.y, qb.x, qb.y);
+                        } else {
+                            mma(acc, c0, c1, c2, c3, bq.x, bq.y);
+                        }
+                    }
+                    x[0] = fmaf(sA, acc[0], x[0]);
+                    x[1] = fmaf(sA, acc[1], x[1]);
+                    x[2] = fmaf(sB, acc[2], x[2]);
+                    x[3] = fmaf(sB, acc[3], x[3]);
+                } else {
+                    // 8 bits: nibbles n0 = c0 + 4 c1 (planes 0, 1), n1 = c2 + 4 c3 (planes 2, 3)
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc16[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int pp = 0; pp < 2; ++pp) {
+                        const uint8_t *kp = gb + 256 * pp;
+                        const uint2 a0w = ld64(kp + tA * 8), a1w = ld64(kp + 128 + tA * 8);
+                        const uint2 b0w = ld64(kp + tB * 8), b1w = ld64(kp + 128 + tB * 8);
+#pragma unroll
+                        for (int kk = 0; kk < 2; ++kk) {
+                            const int ks = 2 * grp + kk;
+                            const uint32_t xa = (kk ? a0w.y : a0w.x) >> (4 * t), ya = (kk ? a1w.y : a1w.x) >> (4 * t);
+                            const uint32_t xb = (kk ? b0w.y : b0w.x) >> (4 * t), yb = (kk ? b1w.y : b1w.x) >> (4 * t);
+                            const uint2 bq = s_qf[(8 + ks) * 32 + lane];
+                            const uint32_t c0 = bsub128(off4_lo(xa, ya, k43)), c1 = bsub128(off4_lo(xb, yb, k43));
+                            const uint32_t c2 = bsub128(off4_hi(xa, ya, k43)), c3 = bsub128(off4_hi(xb, yb, k43));
+                            if (pp == 0)
+                                mma(acc, c0, c1, c2, c3, bq.x, bq.y);
+                            else
+                                mma(acc16, c0, c1, c2, c3, bq.x, bq.y);
+                        }
+                    }
+                    x[0] = fmaf(sA, fmaf(16.f, acc16[0], acc[0]), x[0]);
+                    x[1] = fmaf(sA, fmaf(16.f, acc16[1], acc[1]), x[1]);
+                    x[2] = fmaf(sB, fmaf(16.f, acc16[2], acc[2]), x[2]);
+                    x[3] = fmaf(sB, fmaf(16.f, acc16[3], acc[3]), x[3]);
+                }
+            }
+        } else if (!kWide || P == 1) {
             const uint4 kA0 = ld128(base + tA * 32), kA1 = ld128(base + tA * 32 + 16);
             const uint4 kB0 = ld128(base + tB * 32), kB1 = ld128(base + tB * 32 + 16);
 #pragma unroll

@@ -25,7 +25,9 @@ constexpr int kCtrN = 16;              // counters per sequence
 // counter slots (per sequence). CTR_NEXT is a full-precision slot taken off the
 // free list ahead of time for the next window to open (-1 if none was free).
 enum { CTR_NFP = 0, CTR_NQ = 1, CTR_FP_TOP = 2, CTR_LG_TOP = 3, CTR_WQ = 4, CTR_WP = 5,
-       CTR_WC = 6, CTR_LEN = 7, CTR_NEXT = 8 };
+       CTR_WC = 6, CTR_LEN = 7, CTR_NEXT = 8, CTR_KCH = 9 };
+// CTR_KCH: 1 once qevict_route_rd_kv has set the sequence's K group widths (its
+// quantised windows then hold K-channel tiles, see ktile_kcodes)
 
 // device stats slots
 enum { ST_DEMOTE = 0, ST_PROMOTE = 1, ST_EVICT = 2, ST_LWRITE = 3, ST_LREUSE = 4, ST_N = 8 };
@@ -103,7 +105,19 @@ struct LayerDev {
     int4 *work_c;         // [B][Wmax] prefill copy: {window, dst fp slot, 0, 0}
     int32_t *diag;        // [B][8] counts of the last completed tier move (see qevict_get_tier_move_counts)
     uint8_t *lbits;       // [B][Wmax] width of the window's ledger entry: 0 (none), 2, 4 or 8
+    uint8_t *kgw;         // [B][Hkv][4] K group widths (0, 2, 4, 8) where ctr[CTR_KCH] is set
 };
+
+// K-channel ledger tile (a layer routed by qevict_route_rd_kv): per 16-token tile,
+//   K codes of group g = 0..3 in turn: P_g planes (width / 2) of [16 tokens][8 B],
+//   K meta [16][4] half2 (scale, minimum; zero for a group of width 0),
+//   V codes (P_V planes of 512 B) and V meta (256 B) as in the plane tile.
+// Tiles sit at the stride of the widest plane tile (qtile_bytes(4)).
+__host__ __device__ inline int kgroup_planes(int bits) { return bits >> 1; }
+__host__ __device__ inline int ktile_kcodes(const uint8_t *kw) {   // bytes of the K codes
+    return 128 * (kgroup_planes(kw[0]) + kgroup_planes(kw[1]) + kgroup_planes(kw[2]) + kgroup_planes(kw[3]));
+}
+__host__ __device__ inline int ktile_bytes(int kcodes, int P) { return kcodes + 512 + 512 * P; }
 
 // Row of token t of unit u in a caller's [units / hs][n][Hkv * hs][d] token array
 // (a unit is a sequence, or with per-head tiers a (sequence, KV head) pair)
@@ -134,7 +148,7 @@ constexpr long long kDefaultWaitCycles = 4000000000ll;   // about two seconds at
 
 enum PlanMode { PLAN_ROUTE = 0, PLAN_TIERS = 1, PLAN_PREFILL_SCORES = 2, PLAN_PREFILL_TIERS = 3,
                 PLAN_DEMOTE = 4, PLAN_PROMOTE = 5, PLAN_GLOBAL = 6, PLAN_LOGSPARSE = 7, PLAN_RD = 8,
-                PLAN_RD_MIXED = 9 };
+                PLAN_RD_MIXED = 9, PLAN_RD_KV = 10 };
 
 struct PlanArgs {
     int mode;
@@ -151,6 +165,7 @@ struct PlanArgs {
     const unsigned long long *gthr;    // [sequences][2]: keys >= [0] full precision, >= [1] INT2
     const int32_t *gflag;              // [sequences]: 0 = leave this sequence's tiers unchanged
     int glayers;                       // layers in the key table
+    const float *kweights;             // PLAN_RD_KV: K channel weights [B][Hkv][d]
 };
 
 // One routing event over all layers of a cache under one budget per sequence.
@@ -208,6 +223,8 @@ cudaError_t launch_decode(const LayerDev &L, const CacheDev &C, const DecodeScra
                           int layer, const __nv_bfloat16 *q, const __nv_bfloat16 *knew, const __nv_bfloat16 *vnew,
                           float *out, float *mass, int accumulate, int splits, bool pdl, bool coop,
                           cudaStream_t s);
+cudaError_t launch_k_channel_weights(const LayerDev &L, const __nv_bfloat16 *q, int n_q, const __nv_bfloat16 *k,
+                                     int64_t n_tok, float *out, cudaStream_t s);
 cudaError_t launch_read_lengths(const LayerDev &L, int32_t *out, cudaStream_t s);
 // kmap: k_full [sequences * n_tokens][Hkv * hs][128] bf16 as a 3-D tiled map,
 // boxes of 64 channels x 1 KV head x 16 tokens, 128-byte swizzle

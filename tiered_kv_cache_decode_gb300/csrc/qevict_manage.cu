@@ -380,6 +380,84 @@ __device__ void rd_mixed_targets(const LayerDev &D, const unsigned long long *s_
     __syncthreads();
 }
 
+// ---------------------------------------------------------------- K-channel widths
+// "Technische Samenvatting: RDKV", 2.2 Fase 3: after the window widths, the
+// 32-channel K groups of the sequence's KV heads (units (KV head, group))
+// take widths along 0 -> 2 -> 4 -> 8 within the K bytes the quantised windows
+// have at their widths. A group costs 4 b + 4 bytes per token; the step a -> b
+// of a group of weight W (its channels' weights added in channel order,
+// float64) gains (2^-a - 2^-b) / (tokens (cost(b) - cost(a))) * W per byte.
+// Steps are taken by gain, highest first (lower step, then lower unit, on a
+// tie), while positive, until the first that does not fit. Units are at most
+// 64 (KV heads <= 16), steps at most 192.
+constexpr int kKchMaxUnits = 64;
+__device__ __forceinline__ int kgroup_cost(int bits) { return kGroup * bits / 8 + 4; }
+__device__ void k_channel_widths(const LayerDev &D, const float *kweights, const uint8_t *s_tgt, int nw, int b,
+                                 int *s_warp) {
+    __shared__ double s_wg[kKchMaxUnits], s_gain[3 * kKchMaxUnits], s_kstep[3];
+    __shared__ short s_ord[3 * kKchMaxUnits];
+    __shared__ long long s_cost[3];
+    const int tid = threadIdx.x, U = D.Hkv * kGroups, E = 3 * U;
+    // quantised windows by width
+    int c2 = 0, c4 = 0, c8 = 0;
+    for (int i = tid; i < nw; i += kPlanThreads) {
+        const uint8_t t = s_tgt[i];
+        c2 += t == QEVICT_TIER_Q;
+        c4 += t == QEVICT_TIER_Q4;
+        c8 += t == QEVICT_TIER_Q8;
+    }
+    int cv[3] = {c2, c4, c8}, co[3], ct[3];
+    block_scan_n<3>(cv, co, ct, s_warp);
+    const int64_t n_tok = (int64_t)(ct[0] + ct[1] + ct[2]) * D.w;
+    // K budget: the K halves of the quantised windows at their widths
+    const int64_t kbud = (int64_t)D.w * D.Hkv *
+                         ((int64_t)ct[0] * (16 * 2 + 16) + (int64_t)ct[1] * (16 * 4 + 16) + (int64_t)ct[2] * (16 * 8 + 16));
+    if (tid < U) {
+        const float *wp = kweights + ((int64_t)b * D.Hkv + tid / kGroups) * kHeadDim + (tid % kGroups) * kGroup;
+        double W = 0.0;
+        for (int c = 0; c < kGroup; ++c) W += (double)wp[c];
+        s_wg[tid] = W;
+    }
+    if (tid < 3) {
+        const int a0 = tid == 0 ? 0 : (2 << (tid - 1)), b0 = 2 << tid;
+        const long long cost = (long long)n_tok * (kgroup_cost(b0) - kgroup_cost(a0));
+        s_cost[tid] = cost;
+        s_kstep[tid] = cost > 0 ? (exp2_neg(a0) - exp2_neg(b0)) / (double)cost : 0.0;
+    }
+    __syncthreads();
+    // step e = (step i, unit u): its place in the order by (gain desc, step asc, unit asc)
+    if (tid < E) s_gain[tid] = s_kstep[tid / U] * s_wg[tid % U];
+    __syncthreads();
+    if (tid < E) {
+        const double g0 = s_gain[tid];
+        const int i0 = tid / U, u0 = tid % U;
+        int pos = 0;
+        for (int e = 0; e < E; ++e) {
+            const double g = s_gain[e];
+            const int i = e / U, u = e % U;
+            pos += g > g0 || (g == g0 && (i < i0 || (i == i0 && u < u0)));
+        }
+        s_ord[pos] = (short)tid;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int steps[kKchMaxUnits];
+        for (int u = 0; u < U; ++u) steps[u] = 0;
+        if (n_tok > 0) {
+            long long used = (long long)n_tok * U * kgroup_cost(0);
+            for (int r = 0; r < E; ++r) {
+                const int e = s_ord[r], i = e / U, u = e % U;
+                if (!(s_gain[e] > 0.0) || used + s_cost[i] > kbud) break;
+                used += s_cost[i];
+                steps[u] = i + 1;   // along a chain the gain falls, so a unit's steps come in order
+            }
+        }
+        for (int u = 0; u < U; ++u) D.kgw[(int64_t)b * U + u] = (uint8_t)(steps[u] == 0 ? 0 : (2 << (steps[u] - 1)));
+        D.ctr[b * kCtrN + CTR_KCH] = 1;
+    }
+    __syncthreads();
+}
+
 // One CTA per sequence. Computes the target tier of every window (by ranking
 // the cumulative scores under the budget, or from explicit tiers), then
 // applies the transitions: free the slots of evicted / demoted windows, take
@@ -435,7 +513,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
     const int64_t budget = s_budget;
     const int nfp_budget = s_nfp_budget;
     if ((a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD ||
-         a.mode == PLAN_RD_MIXED) &&
+         a.mode == PLAN_RD_MIXED || a.mode == PLAN_RD_KV) &&
         budget < D.c_fp) {
         if (tid == 0) {
             set_status(C, QEVICT_ERR_BUDGET, a.layer, b, (int)length);
@@ -517,7 +595,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
         for (int i = tid; i < nw; i += kPlanThreads) s_tgt[i] = s_cur[i];
         int bad = 0;
         if (a.mode == PLAN_ROUTE || a.mode == PLAN_PREFILL_SCORES || a.mode == PLAN_LOGSPARSE || a.mode == PLAN_RD ||
-            a.mode == PLAN_RD_MIXED) {
+            a.mode == PLAN_RD_MIXED || a.mode == PLAN_RD_KV) {
+            if (a.mode == PLAN_RD_KV) {
+                // the K widths are set with the layer's first quantisation
+                int has_ledger = 0;
+                for (int i = tid; i < nw; i += kPlanThreads) has_ledger |= D.lg_slot[wb + i] >= 0;
+                if (__syncthreads_or(has_ledger)) {
+                    if (tid == 0) {
+                        set_status(C, QEVICT_ERR_STATE, a.layer, b, -1);
+                        reserve_next(D, ctr, b);
+                    }
+                    return;
+                }
+            }
             int P = 1;
             while (P < nw) P <<= 1;
             for (int i = tid; i < P; i += kPlanThreads) {
@@ -600,8 +690,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev D, CacheDev
             int ncand;
             block_scan(ncand_local, &ncand, s_warp);
             int n_fp, n_q;
-            if (a.mode == PLAN_RD_MIXED) {
+            if (a.mode == PLAN_RD_MIXED || a.mode == PLAN_RD_KV) {
                 rd_mixed_targets(D, s_key, s_tgt, ncand, budget, wb, s_warp, s_dyn);
+                if (a.mode == PLAN_RD_KV) k_channel_widths(D, a.kweights, s_tgt, nw, b, s_warp);
                 n_fp = n_q = -1;   // the targets are set
             } else if (a.mode == PLAN_RD) {
                 // Rate-distortion counts. After the open window (rank 0) come upgrades
@@ -888,15 +979,24 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
     const int h = blockIdx.y >> 1, kv = blockIdx.y & 1;
     const int w = D.w;
     const int n = D.ctr[b * kCtrN + CTR_WQ];
+    // a K-channel layer: K group widths of this KV head, and the tiles' K code bytes
+    const bool kch = D.ctr[b * kCtrN + CTR_KCH] != 0;
+    const uint8_t *kw = kch ? D.kgw + ((int64_t)b * D.Hkv + h) * kGroups : nullptr;
+    const int kcodes = kch ? ktile_kcodes(kw) : 0;
     for (int e = blockIdx.x; e < n; e += gridDim.x) {
         const int4 job = D.work_q[(int64_t)b * D.Wmax + e];
         const int wi = job.x, src_slot = job.y, dst = job.z;
         // the width: 2, 4 or 8 bits, written as P 2-bit planes
         const int bits = job.w == 4 || job.w == 8 ? job.w : 2, P = bits / 2;
-        const float levels = (float)((1 << bits) - 1);
         uint8_t *slotp = D.lg_pool + (int64_t)dst * D.lg_slot_bytes;
+        // tile offsets in the slot, and the meta of this part within a tile
+        const int tstride = kch ? qtile_bytes(4) : qtile_bytes(P);
+        const int meta_off = kch ? (kv ? kcodes + 256 + 512 * P : kcodes) : (kv ? qtile_vmeta(P) : qtile_kmeta(P));
         for (int it = threadIdx.x; it < w * kGroups; it += blockDim.x) {
             const int t = it / kGroups, g = it % kGroups;
+            // K groups of a K-channel layer take their own widths; width 0 keeps no codes
+            const int gbits = (kw && kv == 0) ? kw[g] : bits;
+            const float levels = (float)((1 << (gbits > 0 ? gbits : 2)) - 1);
             const __nv_bfloat16 *src;
             if (src_slot >= 0) {
                 src = reinterpret_cast<const __nv_bfloat16 *>(D.fp_pool + (int64_t)src_slot * D.fp_slot_bytes) +
@@ -927,9 +1027,9 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
             const __half mn16 = __float2half_rn(mn);
             const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), levels));
             const float mq = __half2float(mn16), sq = __half2float(s16);
-            const bool bad = !finite || isinf(mq) || isinf(sq);
+            const bool bad = gbits > 0 && (!finite || isinf(mq) || isinf(sq));
             if (bad) set_status(C, QEVICT_ERR_DEVICE, layer, b, wi);
-            const bool zero = bad || sq == 0.f;
+            const bool zero = bad || sq == 0.f || gbits == 0;
             // the quotients through the scale's reciprocal, corrected to the rounded quotient;
             // clamped to [0, levels] (0 for a zero scale), then rounded half to even by adding
             // 1.5 * 2^23, whose float has the integer in its low mantissa bits (clamping first
@@ -948,13 +1048,30 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
                 }
                 cs[j / 4] = __byte_perm(__byte_perm(c4[0], c4[1], 0x0040), __byte_perm(c4[2], c4[3], 0x0040), 0x5410);
             }
-            __half2 *meta = reinterpret_cast<__half2 *>(slotp + lg_tile_off(h, w, t / 16, P) +
-                                                        (kv ? qtile_vmeta(P) : qtile_kmeta(P))) +
+            __half2 *meta = reinterpret_cast<__half2 *>(slotp + ((int64_t)h * (w / 16) + t / 16) * tstride + meta_off) +
                             (t % 16) * kGroups + g;
-            *meta = bad ? __halves2half2(__float2half_rn(0.f), __float2half_rn(0.f)) : __halves2half2(s16, mn16);
+            *meta = (bad || gbits == 0) ? __halves2half2(__float2half_rn(0.f), __float2half_rn(0.f))
+                                        : __halves2half2(s16, mn16);
         }
         __syncthreads();
-        if (kv == 0) {
+        if (kv == 0 && kw) {
+            // K of a K-channel layer: group g's planes in turn, each [16 tokens][2 words of 16
+            // channels], channel j of a word at bits 2*(j%16), plane p holding bits 2p, 2p + 1
+            int goff = 0;
+            for (int g = 0; g < kGroups; ++g) {
+                const int Pg = kgroup_planes(kw[g]);
+                for (int i = threadIdx.x; i < Pg * w * 2; i += blockDim.x) {
+                    const int p = i / (w * 2), r = i % (w * 2), t = r / 2, hq = r % 2;
+                    const uint8_t *cs = s_codes + t * kHeadDim + g * kGroup + hq * 16;
+                    uint32_t word = 0;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) word |= (uint32_t)((cs[j] >> (2 * p)) & 3u) << (2 * j);
+                    reinterpret_cast<uint32_t *>(slotp + ((int64_t)h * (w / 16) + t / 16) * tstride + goff + 128 * p)
+                        [(t % 16) * 2 + hq] = word;
+                }
+                goff += 128 * Pg;
+            }
+        } else if (kv == 0) {
             // K: per token 8 words of 16 channels, channel j of the word at bits 2*(j%16); plane p
             // of a wider code holds its bits 2p, 2p + 1
             for (int i = threadIdx.x; i < P * w * (kHeadDim / 16); i += blockDim.x) {
@@ -976,8 +1093,9 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
 #pragma unroll
                 for (int t = 0; t < kVTile; ++t)
                     word |= (uint32_t)((s_codes[(tile * kVTile + t) * kHeadDim + j] >> (2 * p)) & 3u) << (2 * t);
-                reinterpret_cast<uint32_t *>(slotp + lg_tile_off(h, w, tile, P) + qtile_vcodes(P) + 512 * p)[r % kHeadDim] =
-                    word;
+                const int vcodes = kw ? kcodes + 256 : qtile_vcodes(P);
+                reinterpret_cast<uint32_t *>(slotp + ((int64_t)h * (w / 16) + tile) * tstride + vcodes + 512 * p)
+                    [r % kHeadDim] = word;
             }
         }
         __syncthreads();
@@ -1312,7 +1430,7 @@ static size_t mixed_plan_smem(const LayerDev &L) {
 
 cudaError_t launch_plan(const LayerDev &L, const CacheDev &C, const PlanArgs &a, cudaStream_t s) {
     size_t dyn = 0;
-    if (a.mode == PLAN_RD_MIXED) {
+    if (a.mode == PLAN_RD_MIXED || a.mode == PLAN_RD_KV) {
         const cudaError_t attr = once_per_device(0, []() {
             return cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)(4 * kPlanMaxW * 8 + kPlanMaxW * 2));
@@ -1346,6 +1464,46 @@ cudaError_t launch_promote(const LayerDev &L, const CacheDev &C, int max_entries
 cudaError_t launch_prefill_copy(const LayerDev &L, const __nv_bfloat16 *k_ext, const __nv_bfloat16 *v_ext,
                                 int64_t ext_len, int max_entries, cudaStream_t s) {
     prefill_copy_kernel<<<work_grid(L, max_entries), 128, 0, s>>>(L, k_ext, v_ext, ext_len);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- K channel weights
+// "Technische Samenvatting: RDKV", 2.1: w_c = ||Q[:, c]|| ||K[:, c]|| / sqrt(d) per
+// (sequence, KV head, channel); the query heads of a KV head pool their columns.
+// One CTA per (sequence, KV head): eight stripes of tokens per channel, fp32 sums.
+__global__ void __launch_bounds__(1024) k_weights_kernel(LayerDev D, const __nv_bfloat16 *__restrict__ q, int n_q,
+                                                         const __nv_bfloat16 *__restrict__ k, int64_t n_tok,
+                                                         float *out) {
+    __shared__ float red[2][8][kHeadDim];
+    const int b = blockIdx.x / D.Hkv, h = blockIdx.x % D.Hkv;
+    const int c = threadIdx.x & (kHeadDim - 1), st = threadIdx.x >> 7;
+    const int G = D.G;
+    float sk = 0.f, sq = 0.f;
+    for (int64_t t = st; t < n_tok; t += 8) {
+        const float x = __bfloat162float(k[(((int64_t)b * n_tok + t) * D.Hkv + h) * kHeadDim + c]);
+        sk = fmaf(x, x, sk);
+    }
+    for (int64_t r = st; r < (int64_t)n_q * G; r += 8) {
+        const int64_t pos = r / G, j = r % G;
+        const float x = __bfloat162float(q[(((int64_t)b * n_q + pos) * D.Hq + h * G + j) * kHeadDim + c]);
+        sq = fmaf(x, x, sq);
+    }
+    red[0][st][c] = sk;
+    red[1][st][c] = sq;
+    __syncthreads();
+    if (st == 0) {
+        float K2 = 0.f, Q2 = 0.f;
+        for (int i = 0; i < 8; ++i) {
+            K2 += red[0][i][c];
+            Q2 += red[1][i][c];
+        }
+        out[((int64_t)b * D.Hkv + h) * kHeadDim + c] = sqrtf(Q2) * sqrtf(K2) / sqrtf((float)kHeadDim);
+    }
+}
+
+cudaError_t launch_k_channel_weights(const LayerDev &L, const __nv_bfloat16 *q, int n_q, const __nv_bfloat16 *k,
+                                     int64_t n_tok, float *out, cudaStream_t s) {
+    k_weights_kernel<<<L.B * L.Hkv, 1024, 0, s>>>(L, q, n_q, k, n_tok, out);
     return cudaGetLastError();
 }
 
