@@ -575,6 +575,88 @@ def measure_mixed_widths(wl, NL, reps, dev, peak):
             "decode_frac_of_peak": round(nbytes / (us_dec * 1e-6) / 1e9 / peak, 4)}
 
 
+def measure_k_channels(wl, NL, reps, dev, peak):
+    """RDKV's K-channel half on the workload: per layer the channel weights
+    from 64 seeded query vectors and the prefill keys, then one K-channel
+    routing event (window widths {0, 2, 4, 8, 16}, K group widths {0, 2, 4, 8}
+    within the quantised windows' K bytes) on seeded scores, then the decode
+    kernel over all layers on those tiers (CUDA graph; algorithmic bytes: the
+    full-precision windows, the quantised windows' K groups at their widths
+    with the K meta and their V at the window width, plus the query, output
+    and scores)."""
+    import torch
+    from tiered_kv_cache_decode_gb300 import binding, synth
+    B, Hq, Hkv, w, L0, d, seed = wl["B"], wl["Hq"], wl["Hkv"], wl["w"], wl["L"], 128, 0
+    W0 = L0 // w
+    kc = binding.TieredCache(B, NL, Hq, Hkv, w, L0, budget_frac=wl["beta"], fp_share=wl["rho"], max_ledger_bits=8,
+                             fp_capacity=W0, ledger_capacity=W0)
+    kc.set_launch_overlap(True)
+    kc.set_cooperative_launch(False)   # the decodes run alone on the GPU
+    zeros = torch.zeros(B, W0, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_w = t_r = 0.0
+    for l in range(NL):
+        k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, d, wl["outliers"], device=dev)
+        kc.prefill(l, k, v, tiers=zeros)
+        q_obs = torch.stack([synth.queries(seed, l, 1000 + i, B, Hq, d, device=dev) for i in range(64)], dim=1)
+        sc = synth.zipf_scores(seed + 500, l, B, W0, device=dev)
+        torch.cuda.synchronize()
+        e0.record()
+        wts = kc.k_channel_weights(l, q_obs, k)
+        e1.record()
+        torch.cuda.synchronize()
+        t_w += e0.elapsed_time(e1) * 1e3
+        e0.record()
+        kc.route_rd_kv(l, wts, scores_override=sc)
+        e1.record()
+        torch.cuda.synchronize()
+        t_r += e0.elapsed_time(e1) * 1e3
+        del k, v, q_obs
+    q = [synth.queries(seed, l, 0, B, Hq, d, device=dev) for l in range(NL)]
+    xo = torch.empty(NL, B, Hq, d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    g_dec = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_dec, stream=stream):
+            for l in range(NL):
+                kc.decode(l, q[l], out=xo[l], want_mass=False, accumulate=True, stream=stream)
+        for _ in range(3):
+            g_dec.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g_dec.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us_dec = e0.elapsed_time(e1) * 1e3 / (reps * NL)
+    nbytes, hist = 0, {b: 0 for b in (0, 2, 4, 8)}
+    n_fp = n_q = 0
+    for l in range(NL):
+        tiers = kc.tables(l)[0]
+        kgw = kc.k_group_bits(l)
+        for b in range(B):
+            kbytes = sum(4 * int(x) + 4 for x in kgw[b].reshape(-1))   # per token, all KV heads
+            for x in kgw[b].reshape(-1):
+                hist[int(x)] += 1
+            for t in tiers[b].tolist():
+                if t == 0:
+                    nbytes += w * Hkv * d * 4
+                    n_fp += 1
+                elif t in (1, 3, 4):
+                    vb = {1: 2, 3: 4, 4: 8}[t]
+                    nbytes += w * (kbytes + Hkv * (d * vb // 8 + 16))
+                    n_q += 1
+    nbytes = nbytes / NL + B * (Hq * d * 2 + Hq * d * 4 + Hkv * W0 * 8)
+    st = kc.status()
+    assert st == 0, f"device status {st}: {kc.last_error()}"
+    return {"layers": NL, "weights_us_per_layer": round(t_w / NL, 2), "route_us_per_layer": round(t_r / NL, 2),
+            "k_group_widths_0_2_4_8": [hist[b] for b in (0, 2, 4, 8)],
+            "windows_fp_quantised_per_sequence_mean": [round(n_fp / (NL * B), 2), round(n_q / (NL * B), 2)],
+            "decode_us_per_launch": round(us_dec, 3), "decode_bytes_per_launch": int(nbytes),
+            "decode_gbs": round(nbytes / (us_dec * 1e-6) / 1e9, 2),
+            "decode_frac_of_peak": round(nbytes / (us_dec * 1e-6) / 1e9 / peak, 4)}
+
+
 def measure_per_config(reps, dev, peak, which="all"):
     """The decode kernel on every other workload: the Llama-3.1-8B-shaped batch
     8 at 32K and 5 %, the Qwen2.5-7B-shaped batch 16 at 16K and 10 %, and the 27
@@ -899,6 +981,7 @@ def run_native(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         line["variants"] = measure_variants(wl, NL, K, dev, peak)
         line["variants"]["mixed_widths"] = measure_mixed_widths(wl, NL, K, dev, peak)
+        line["variants"]["k_channels"] = measure_k_channels(wl, NL, K, dev, peak)
     if not args.no_per_config:
         line["per_config"] = measure_per_config(K, dev, peak, args.per_config)
     if pool_async is not None:

@@ -1479,6 +1479,7 @@ __global__ void __launch_bounds__(1024) k_weights_kernel(LayerDev D, const __nv_
     const int c = threadIdx.x & (kHeadDim - 1), st = threadIdx.x >> 7;
     const int G = D.G;
     float sk = 0.f, sq = 0.f;
+#pragma unroll 8
     for (int64_t t = st; t < n_tok; t += 8) {
         const float x = __bfloat162float(k[(((int64_t)b * n_tok + t) * D.Hkv + h) * kHeadDim + c]);
         sk = fmaf(x, x, sk);
