@@ -270,18 +270,22 @@ __device__ __forceinline__ ClaimPlan claim_plan(const LayerDev &D, int b, int kv
 // quantised chunk of n tiles has z = (byte offset of its tiles in the ledger
 // pool) / 512 and w = its bytes; a full-precision unit of n tokens has z, w =
 // the TMA coordinates of its tile (slot * Hkv + kvh, 16 j).
+// Descriptor of the split's full-precision unit fb.
+__device__ __forceinline__ int4 fp_desc(const LayerDev &D, const ClaimPlan &p, int b, int kvh, int mu, int fb) {
+    const int w = D.w;
+    const int gf = p.f0 + fb, e = gf / mu, j = gf - e * mu;
+    const int2 en = D.fp_list[b * D.CF + e];
+    const int nt = ((en.x == p.n_win - 1) ? (int)(p.length - (int64_t)en.x * w) : w) - 16 * j;
+    if (nt <= 0) return make_int4(EL_SKIP, 0, 0, 0);   // past the open window's last token
+    return make_int4(EL_F | (min(16, nt) << 2), e * mu + j, en.y * D.Hkv + kvh, 16 * j);
+}
+
 template <bool kWide>
 __device__ __forceinline__ int4 claim_desc(const LayerDev &D, const ClaimPlan &p, int b, int kvh, int mu, int c) {
     const int w = D.w;
     // a split has at most 2^16 claims and 2^15 full-precision units: the products fit 32 bits
     const int fb = (int)((unsigned)c * p.nfl / p.N);
-    if ((int)((unsigned)(c + 1) * p.nfl / p.N) > fb) {
-        const int gf = p.f0 + fb, e = gf / mu, j = gf - e * mu;
-        const int2 en = D.fp_list[b * D.CF + e];
-        const int nt = ((en.x == p.n_win - 1) ? (int)(p.length - (int64_t)en.x * w) : w) - 16 * j;
-        if (nt <= 0) return make_int4(EL_SKIP, 0, 0, 0);   // past the open window's last token
-        return make_int4(EL_F | (min(16, nt) << 2), e * mu + j, en.y * D.Hkv + kvh, 16 * j);
-    }
+    if ((int)((unsigned)(c + 1) * p.nfl / p.N) > fb) return fp_desc(D, p, b, kvh, mu, fb);
     const int ci = c - fb;
     int k, u0, n;
     if (ci < p.nbig) {
@@ -305,6 +309,36 @@ __device__ __forceinline__ int4 claim_desc(const LayerDev &D, const ClaimPlan &p
                          n * ktile_bytes(p.kcodes, P));
     }
     const int64_t off = (int64_t)slot * D.lg_slot_bytes + lg_tile_off(kvh, w, u0, P);
+    return make_int4(EL_Q | (n << 2) | (lgP << 7), D.CF * mu + e * mu + u0, (int)(off >> 9), n * qtile_bytes(P));
+}
+
+// Wide plane tiles in chunks: a claim takes up to `tpc` tiles of one window,
+// at most what one stage holds at the window's width. Quantised claim ci
+// belongs to the window k with pref[k] <= ci < pref[k + 1] (pref: exclusive
+// prefix of the claims per window), interleaved with the full-precision units
+// as in claim_desc over N claims.
+__device__ __forceinline__ int wide_tpc(int P, int mu, int target) {
+    return min(target, min(mu, kSlot / qtile_bytes(P)));
+}
+__device__ __forceinline__ int4 chunk_desc(const LayerDev &D, const ClaimPlan &p, int b, int kvh, int mu, int c,
+                                           int N, const int *pref, int target) {
+    const int fb = (int)((unsigned)c * p.nfl / N);
+    if ((int)((unsigned)(c + 1) * p.nfl / N) > fb) return fp_desc(D, p, b, kvh, mu, fb);
+    const int ci = c - fb;
+    int lo = 0, hi = p.nqw - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pref[mid] <= ci)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int e = p.qw0 + lo;
+    const int2 en = D.q_list[b * D.CQ + e];
+    const int lgP = en.y >> kSlotBits, slot = en.y & ((1 << kSlotBits) - 1), P = 1 << lgP;
+    const int tpc = wide_tpc(P, mu, target);
+    const int u0 = (ci - pref[lo]) * tpc, n = min(tpc, mu - u0);
+    const int64_t off = (int64_t)slot * D.lg_slot_bytes + lg_tile_off(kvh, D.w, u0, P);
     return make_int4(EL_Q | (n << 2) | (lgP << 7), D.CF * mu + e * mu + u0, (int)(off >> 9), n * qtile_bytes(P));
 }
 
@@ -344,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_slot_new;                // slot of the new token's window (split 0, fused append)
     __shared__ uint32_t s_gen;                // split-record generation of this launch
     __shared__ int s_kg[9];                   // K-channel tiles: planes and code offset of each group, code bytes
+    __shared__ int s_ws[kWarps];              // per-warp sums of the chunk scan
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t = lane & 3;
@@ -356,7 +391,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- claim descriptors, built by all threads at once
     const int N = [&]() {
         const ClaimPlan p = claim_plan<kWide>(D, b, kvh, split, splits, mu);
-        for (int c = tid; c < min(p.N, kDescTab); c += kThreads) s_desc[c] = claim_desc<kWide>(D, p, b, kvh, mu, c);
+        int n_claims = p.N;
+        bool chunked = false;
+        if (kWide && p.kcodes < 0 && p.nqw > 0) {
+            // wide plane tiles: several tiles of a window per claim (wide_tpc); the claims per
+            // window are prefix-summed in the ring space, which no copy has reached yet
+            int *pref = reinterpret_cast<int *>(smem);
+            const int target = max(1, (p.nqw * mu) / (2 * kWarps));
+            const int per = (p.nqw + kThreads - 1) / kThreads;
+            const int k0 = min(p.nqw, tid * per), k1 = min(p.nqw, k0 + per);
+            int cnt = 0;
+            for (int k = k0; k < k1; ++k) {
+                const int P = 1 << (D.q_list[b * D.CQ + p.qw0 + k].y >> kSlotBits);
+                const int tpc = wide_tpc(P, mu, target);
+                pref[k] = (mu + tpc - 1) / tpc;
+                cnt += pref[k];
+            }
+            int x = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) s_ws[warp] = x;
+            __syncthreads();
+            int run = x - cnt, total = 0;
+            for (int i = 0; i < kWarps; ++i) {
+                run += i < warp ? s_ws[i] : 0;
+                total += s_ws[i];
+            }
+            for (int k = k0; k < k1; ++k) {
+                const int cw = pref[k];
+                pref[k] = run;
+                run += cw;
+            }
+            __syncthreads();
+            if (total + p.nfl <= kDescTab) {
+                chunked = true;
+                n_claims = total + p.nfl;
+                for (int c = tid; c < n_claims; c += kThreads)
+                    s_desc[c] = chunk_desc(D, p, b, kvh, mu, c, n_claims, pref, target);
+            }
+        }
+        if (!chunked)
+            for (int c = tid; c < min(p.N, kDescTab); c += kThreads) s_desc[c] = claim_desc<kWide>(D, p, b, kvh, mu, c);
         if (tid == 0) {
             s_span[0] = p.qw0;
             s_span[1] = p.nqw;
@@ -378,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_slot_new = (p.length % w == 0) ? D.ctr[b * kCtrN + CTR_NEXT] : D.fp_slot[(int64_t)b * D.Wmax + wn];
             }
         }
-        return p.N;
+        return n_claims;
     }();
     if (lane == 0)
         for (int i = 0; i < kSlots; ++i) mbar_init(smem_u32(&bars[warp][i]), 1);
