@@ -576,17 +576,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tA = (g & 1) ? g + 7 : g;
     const int tB = (g & 1) ? g + 8 : g + 1;
 
-    // softmax of x = {(row g, col 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)} in place
+    // softmax of the unscaled logits x = {(row g, col 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1)}
+    // in place; the scale (log2 e / sqrt(d)) joins each subtraction of the running max
     auto softmax = [&](float (&x)[4]) {
         const float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
-        if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy)) {
+        if (__any_sync(0xffffffffu, fmaf(mx0, qk_scale, -m0) > kLazy || fmaf(mx1, qk_scale, -m1) > kLazy)) {
             float h0 = mx0, h1 = mx1;
 #pragma unroll
             for (int o2 = 4; o2 <= 16; o2 <<= 1) {
                 h0 = fmaxf(h0, __shfl_xor_sync(0xffffffffu, h0, o2));
                 h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, o2));
             }
-            const float n0 = fmaxf(m0, h0), n1 = fmaxf(m1, h1);
+            const float n0 = fmaxf(m0, h0 * qk_scale), n1 = fmaxf(m1, h1 * qk_scale);
             const float a0 = ex2(m0 - n0), a1 = ex2(m1 - n1);
             m0 = n0;
             m1 = n1;
@@ -607,10 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o[i][3] *= a1;
             }
         }
-        x[0] = ex2(x[0] - m0);
-        x[1] = ex2(x[1] - m1);
-        x[2] = ex2(x[2] - m0);
-        x[3] = ex2(x[3] - m1);
+        x[0] = ex2(fmaf(x[0], qk_scale, -m0));
+        x[1] = ex2(fmaf(x[1], qk_scale, -m1));
+        x[2] = ex2(fmaf(x[2], qk_scale, -m0));
+        x[3] = ex2(fmaf(x[3], qk_scale, -m1));
         w0 += x[0] + x[2];
         w1 += x[1] + x[3];
     };
@@ -825,8 +826,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 x[3] = fmaf(sB, fmaf(16.f, acc16[3], acc[3]), x[3]);
             }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[i] *= qk_scale;
         softmax(x);
         // ---- PV. Rows g + 8 (k rows 8-15 of the operand) meet 4 x code, so their P
         // parts carry the V scale divided by 4 (exact).
@@ -909,8 +908,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint2 bq = s_qf[ks * 32 + lane];
                 mma(x, r0, r2, r1, r3, bq.x, bq.y);
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] *= qk_scale;
             if (n < 16) {
                 // rows past the open window's last token: P is 0 there, but the V rows
                 // hold stale slot memory and 0 * NaN would still poison the product
