@@ -1004,7 +1004,10 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
             } else {
                 src = (kv ? v_ext : k_ext) + src_row(D, b, ext_len, (int64_t)wi * w + t, h) * kHeadDim + g * kGroup;
             }
+            // the group's minimum and maximum on bf16 pairs, with NaN propagating, so that
+            // a NaN or an infinity anywhere in the group shows in them
             float x[kGroup];
+            __nv_bfloat162 mn2, mx2;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint4 u = reinterpret_cast<const uint4 *>(src)[c];
@@ -1014,16 +1017,13 @@ __global__ void __launch_bounds__(128) quantize_kernel(LayerDev D, CacheDev C, i
                     const float2 f = __bfloat1622float2(p2[j]);
                     x[c * 8 + 2 * j] = f.x;
                     x[c * 8 + 2 * j + 1] = f.y;
+                    mn2 = (c == 0 && j == 0) ? p2[j] : __hmin2_nan(mn2, p2[j]);
+                    mx2 = (c == 0 && j == 0) ? p2[j] : __hmax2_nan(mx2, p2[j]);
                 }
             }
-            bool finite = true;
-            float mn = x[0], mx = x[0];
-#pragma unroll
-            for (int j = 0; j < kGroup; ++j) {
-                finite &= isfinite(x[j]);
-                mn = fminf(mn, x[j]);
-                mx = fmaxf(mx, x[j]);
-            }
+            const float mn = __bfloat162float(__hmin_nan(__low2bfloat16(mn2), __high2bfloat16(mn2)));
+            const float mx = __bfloat162float(__hmax_nan(__low2bfloat16(mx2), __high2bfloat16(mx2)));
+            const bool finite = isfinite(mn) && isfinite(mx);
             const __half mn16 = __float2half_rn(mn);
             const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), levels));
             const float mq = __half2float(mn16), sq = __half2float(s16);
