@@ -1068,6 +1068,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kRecLd; ++k)
             mrec[k] = (k / G < mu) ? rec[(int64_t)mr0 * G + k] : make_float2(0.f, 0.f);
     }
+    // and the window's partial score (no other CTA writes it in this launch)
+    const float msp = (accumulate && mwi >= 0) ? sp[mwi] : 0.f;
     // the evicted windows of this split's slice of [0, n_out), and the window this step opens
     const int z0 = (int)((int64_t)split * n_out / splits), z1 = (int)((int64_t)(split + 1) * n_out / splits);
     const int zi = z0 + tid;
@@ -1217,7 +1219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mass) mass[((int64_t)b * Hq + kvh * G + hh) * n_out + wi] = m;
             sum += m;
         }
-        if (accumulate) sp[wi] += sum * inv_hq;
+        if (accumulate) sp[wi] = (wl == mi ? msp : sp[wi]) + sum * inv_hq;
     }
     // windows no list holds, in this split's slice: evicted ones (mass 0) and the window this step opens
     for (int wi = zi; wi < z1; wi += kThreads) {
