@@ -49,8 +49,8 @@
 // masses of its own windows (from its records; their mean over the Hq heads
 // grows the KV head's partial cumulative score) and the zero masses of its
 // slice of the evicted windows. With a new token, split 0 writes its K and V
-// rows into their slot and the last CTA of the sequence to arrive opens the
-// new window and moves the length.
+// rows into their slot, and once every CTA of the sequence has published, split
+// 0 of KV head 0 opens the new window and moves the length.
 //
 // With programmatic dependent launch the kernel reads its window lists and
 // issues its first copies before it waits for the previous kernel

@@ -135,7 +135,8 @@ struct DecodeScratch {
                           // quantised chunk, log2 domain (written and read by the same split)
     int rec_stride;       // records per (sequence, KV head): decode_records(CF, CQ, w, maxP)
     float2 *wstat;        // [B][Hq][max(Wmax, 2)] future-missed-mass partials
-    uint32_t *bar;        // [B*Hkv][2] split arrival count (0 between launches), record generation
+    uint32_t *bar;        // [B*Hkv][2] a counter of the missed-mass kernel (0 between launches), the
+                          // decode's record generation
     uint32_t *arrive_b;   // [B] arrival counters of a sequence's CTAs for the fused append (0 between launches)
 };
 
