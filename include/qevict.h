@@ -328,15 +328,17 @@ qevict_status qevict_route_rd_mixed(qevict_cache *cache, int32_t layer, const fl
  * RDKV", 2.1: w_c = (1/sqrt(d)) ||Q[:, c]||_2 ||K[:, c]||_2; 2.2 Fase 1: once,
  * after the prefill, from the uncompressed cache), per sequence, KV head and
  * channel. Reads nothing of the cache but its shapes.
- *  q_obs    bf16 [batch][n_q][Hq][head_dim], device: query vectors observed
- *           over the prefill; the G query heads of a KV head pool their
- *           columns (n_q * G rows per channel).
- *  k_full   bf16 [batch][n_tokens][Hkv][head_dim], device: the layer's keys as
- *           given to qevict_prefill.
+ *  q_obs    bf16 [batch][n_q][Hq][head_dim], device, 16-byte aligned: query
+ *           vectors observed over the prefill; the G query heads of a KV head
+ *           pool their columns (n_q * G rows per channel).
+ *  k_full   bf16 [batch][n_tokens][Hkv][head_dim], device, 16-byte aligned:
+ *           the layer's keys as given to qevict_prefill.
  *  weights  fp32 [batch][Hkv][head_dim], device, written. Sums of squares in
- *           fp32 over eight interleaved stripes of rows, then their roots.
- * INVALID_ARG for NULL pointers, non-positive counts or a cache with tiers
- * per KV head. */
+ *           fp32 in a fixed order (eight contiguous shares of the rows, each
+ *           over 32 interleaved row groups, then the shares in order), then
+ *           their roots: every call gives the same weights.
+ * INVALID_ARG for NULL or misaligned pointers, non-positive counts or a cache
+ * with tiers per KV head. */
 qevict_status qevict_k_channel_weights(qevict_cache *cache, int32_t layer, const void *q_obs, int64_t n_q,
                                       const void *k_full, int64_t n_tokens, float *weights, void *stream);
 

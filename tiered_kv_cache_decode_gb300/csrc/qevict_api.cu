@@ -608,6 +608,8 @@ qevict_status qevict_k_channel_weights(qevict_cache *c, int32_t layer, const voi
         return fail(QEVICT_ERR_INVALID_ARG, "n_q (%lld) and n_tokens (%lld) must be positive", (long long)n_q,
                     (long long)n_tokens);
     if (c->hs != 1) return fail(QEVICT_ERR_INVALID_ARG, "K-channel weights need shared tiers (not per KV head)");
+    if (((uintptr_t)q_obs | (uintptr_t)k_full) & 15)
+        return fail(QEVICT_ERR_INVALID_ARG, "q_obs and k_full must be 16-byte aligned");
     cudaError_t e = launch_k_channel_weights(c->layers[layer].dev, (const __nv_bfloat16 *)q_obs, (int)n_q,
                                              (const __nv_bfloat16 *)k_full, n_tokens, weights, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "K channel weights kernel");

@@ -1470,41 +1470,88 @@ cudaError_t launch_prefill_copy(const LayerDev &L, const __nv_bfloat16 *k_ext, c
 // ---------------------------------------------------------------- K channel weights
 // "Technische Samenvatting: RDKV", 2.1: w_c = ||Q[:, c]|| ||K[:, c]|| / sqrt(d) per
 // (sequence, KV head, channel); the query heads of a KV head pool their columns.
-// One CTA per (sequence, KV head): eight stripes of tokens per channel, fp32 sums.
-__global__ void __launch_bounds__(1024) k_weights_kernel(LayerDev D, const __nv_bfloat16 *__restrict__ q, int n_q,
-                                                         const __nv_bfloat16 *__restrict__ k, int64_t n_tok,
-                                                         float *out) {
-    __shared__ float red[2][8][kHeadDim];
-    const int b = blockIdx.x / D.Hkv, h = blockIdx.x % D.Hkv;
-    const int c = threadIdx.x & (kHeadDim - 1), st = threadIdx.x >> 7;
-    const int G = D.G;
-    float sk = 0.f, sq = 0.f;
-#pragma unroll 8
-    for (int64_t t = st; t < n_tok; t += 8) {
-        const float x = __bfloat162float(k[(((int64_t)b * n_tok + t) * D.Hkv + h) * kHeadDim + c]);
-        sk = fmaf(x, x, sk);
-    }
-    for (int64_t r = st; r < (int64_t)n_q * G; r += 8) {
-        const int64_t pos = r / G, j = r % G;
-        const float x = __bfloat162float(q[(((int64_t)b * n_q + pos) * D.Hq + h * G + j) * kHeadDim + c]);
-        sq = fmaf(x, x, sq);
-    }
-    red[0][st][c] = sk;
-    red[1][st][c] = sq;
-    __syncthreads();
-    if (st == 0) {
-        float K2 = 0.f, Q2 = 0.f;
-        for (int i = 0; i < 8; ++i) {
-            K2 += red[0][i][c];
-            Q2 += red[1][i][c];
+// One cluster of kKwCtas CTAs per (sequence, KV head); CTA r takes the r-th
+// contiguous share of the key rows and of the query rows. A thread holds eight
+// channels (one 16-byte load per row) and runs over every kKwRowGroups-th row of
+// the share; the CTA adds its row groups in order, and rank 0 adds the CTAs'
+// sums in rank order from distributed shared memory: fp32 throughout, in a
+// fixed order, so that every call gives the same weights.
+constexpr int kKwCtas = 8, kKwThreads = 512, kKwRowGroups = kKwThreads / 16;
+
+__device__ __forceinline__ void kw_rows(const __nv_bfloat16 *__restrict__ base, int64_t row_stride, int64_t r0,
+                                        int64_t r1, int rg, float (&acc)[8]) {
+    int64_t r = r0 + rg;
+#pragma unroll 4
+    for (; r < r1; r += kKwRowGroups) {
+        const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(base + r * row_stride));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(w[j] << 16), hi = __uint_as_float(w[j] & 0xffff0000u);
+            acc[2 * j] = fmaf(lo, lo, acc[2 * j]);
+            acc[2 * j + 1] = fmaf(hi, hi, acc[2 * j + 1]);
         }
-        out[((int64_t)b * D.Hkv + h) * kHeadDim + c] = sqrtf(Q2) * sqrtf(K2) / sqrtf((float)kHeadDim);
     }
+}
+
+__global__ void __cluster_dims__(kKwCtas, 1, 1) __launch_bounds__(kKwThreads)
+    k_weights_kernel(LayerDev D, const __nv_bfloat16 *__restrict__ q, int n_q, const __nv_bfloat16 *__restrict__ k,
+                     int64_t n_tok, float *out) {
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int bh = blockIdx.x / kKwCtas, b = bh / D.Hkv, h = bh % D.Hkv;
+    const int tid = threadIdx.x, rg = tid >> 4, c8 = (tid & 15) * 8;   // row group, first channel
+    __shared__ float red[2][kKwRowGroups][kHeadDim];
+    __shared__ float part[2][kHeadDim];   // this CTA's sums of squares: keys, queries
+    float ak[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, aq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // key rows t of (b, h): [b][t][h][d]
+    kw_rows(k + ((int64_t)b * n_tok * D.Hkv + h) * kHeadDim + c8, (int64_t)D.Hkv * kHeadDim,
+            n_tok * rank / kKwCtas, n_tok * (rank + 1) / kKwCtas, rg, ak);
+    // query rows (pos, j) of (b, h), pos-major: [b][pos][h G + j][d]
+    {
+        const int G = D.G;
+        const int64_t nr = (int64_t)n_q * G, r0 = nr * rank / kKwCtas, r1 = nr * (rank + 1) / kKwCtas;
+        for (int64_t r = r0 + rg; r < r1; r += kKwRowGroups) {
+            const int64_t pos = r / G, j = r % G;
+            const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(
+                q + (((int64_t)b * n_q + pos) * D.Hq + h * G + j) * kHeadDim + c8));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float lo = __uint_as_float(w[jj] << 16), hi = __uint_as_float(w[jj] & 0xffff0000u);
+                aq[2 * jj] = fmaf(lo, lo, aq[2 * jj]);
+                aq[2 * jj + 1] = fmaf(hi, hi, aq[2 * jj + 1]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        red[0][rg][c8 + j] = ak[j];
+        red[1][rg][c8 + j] = aq[j];
+    }
+    __syncthreads();
+    if (tid < 2 * kHeadDim) {
+        const int which = tid >> 7, c = tid & (kHeadDim - 1);
+        float sum = 0.f;
+        for (int i = 0; i < kKwRowGroups; ++i) sum += red[which][i][c];
+        part[which][c] = sum;
+    }
+    cl.sync();   // every CTA's sums are in its shared memory
+    if (rank == 0 && tid < kHeadDim) {
+        float K2 = 0.f, Q2 = 0.f;
+        for (int r = 0; r < kKwCtas; ++r) {
+            const float *pr = cl.map_shared_rank(&part[0][0], r);
+            K2 += pr[tid];
+            Q2 += pr[kHeadDim + tid];
+        }
+        out[((int64_t)b * D.Hkv + h) * kHeadDim + tid] = sqrtf(Q2) * sqrtf(K2) / sqrtf((float)kHeadDim);
+    }
+    cl.sync();   // rank 0 has read the others' shared memory
 }
 
 cudaError_t launch_k_channel_weights(const LayerDev &L, const __nv_bfloat16 *q, int n_q, const __nv_bfloat16 *k,
                                      int64_t n_tok, float *out, cudaStream_t s) {
-    k_weights_kernel<<<L.B * L.Hkv, 1024, 0, s>>>(L, q, n_q, k, n_tok, out);
+    k_weights_kernel<<<L.B * L.Hkv * kKwCtas, kKwThreads, 0, s>>>(L, q, n_q, k, n_tok, out);
     return cudaGetLastError();
 }
 
