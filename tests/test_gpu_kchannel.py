@@ -123,6 +123,12 @@ def test_k_channel_state_rules():
     assert other.status() == 0, other.last_error()
     other.route_rd_kv(0, other.k_channel_weights(0, q2.cuda(), k2.cuda()), scores_override=scores)
     assert binding.STATUS[other.status()] == "STATE"
+    # keys that do not start on a 16-byte boundary (the kernel reads rows in 16-byte pieces)
+    kk = torch.empty(k.numel() + 8, dtype=k.dtype, device="cuda")[1:1 + k.numel()].view(k.shape)
+    kk.copy_(k.cuda())
+    with pytest.raises(binding.QevictError) as e:
+        cache.k_channel_weights(0, q_obs.cuda(), kk)
+    assert e.value.code == 1   # INVALID_ARG
     # caches that cannot hold K-channel tiles
     int2 = binding.TieredCache(B, 1, Hq, Hkv, w, L, budget_frac=0.3)
     with pytest.raises(binding.QevictError) as e:

@@ -230,6 +230,12 @@ __device__ __forceinline__ float ex2(float x) {
 
 constexpr int kRecMax = 8;     // records per window: 16-token tiles (w <= 128)
 
+// A code-plane count known at compile time (converts to its int)
+template <int P>
+struct PlanesC {
+    __device__ constexpr operator int() const { return P; }
+};
+
 // One split's claims (see decode_kernel): whole quantised windows [qw0, qw0 +
 // nqw) and whole full-precision windows [fw0, fw0 + nfw), i.e. units [f0, f0 +
 // nfl), of one (sequence, KV head).
@@ -656,10 +662,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!kDup) mma(acc, a0, a1, a2, a3, b2, b3);
     };
 
-    // ---- one quantised 16-token tile at `base` with P code planes
-    auto quant_tile = [&](const uint8_t *base, int P) {
-        // a K-channel tile: K groups of their own widths ahead of the K meta (kcodes bytes)
-        const int kcodes = kWide ? s_kg[8] : -1;
+    // ---- one quantised 16-token tile at `base` with P code planes. Pc is the plane
+    // count, an int or a compile-time constant (PlanesC: the arithmetic of that width
+    // alone); kch_tile: a K-channel tile (K groups of their own widths ahead of the
+    // K meta, kcodes bytes)
+    auto quant_tile = [&](const uint8_t *base, auto Pc, bool kch_tile) {
+        const int P = static_cast<int>(Pc);
+        const int kcodes = (kWide && kch_tile) ? s_kg[8] : -1;
         const uint8_t *km = base + (kcodes >= 0 ? kcodes : qtile_kmeta(P));
         const uint8_t *vc = base + (kcodes >= 0 ? kcodes + 256 : qtile_vcodes(P));
         const uint8_t *vm = base + (kcodes >= 0 ? kcodes + 256 + 512 * P : qtile_vmeta(P));
@@ -894,7 +903,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int P = kWide ? sl_p[warp][sl] : 1;
             const int tb = kWide ? qtile_bytes(P) : kQTile;
             const uint8_t *tp = smem + warp * kRing + sl * kSlot;
-            for (int u = 0; u < n; ++u) quant_tile(tp + u * tb, P);
+            // the tile arithmetic compiled for each plane count (K-channel tiles: generic)
+            if (!kWide || (P == 1 && s_kg[8] < 0)) {
+                for (int u = 0; u < n; ++u) quant_tile(tp + u * tb, PlanesC<1>{}, false);
+            } else if (s_kg[8] >= 0) {
+                for (int u = 0; u < n; ++u) quant_tile(tp + u * tb, P, true);
+            } else if (P == 2) {
+                for (int u = 0; u < n; ++u) quant_tile(tp + u * tb, PlanesC<2>{}, false);
+            } else {
+                for (int u = 0; u < n; ++u) quant_tile(tp + u * tb, PlanesC<4>{}, false);
+            }
             write_record(id, n);
         } else if (kind == EL_F) {
             // ---------------- full-precision unit: QK, softmax, PV
