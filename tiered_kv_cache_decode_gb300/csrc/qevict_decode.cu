@@ -326,10 +326,16 @@ __device__ __forceinline__ int4 claim_desc(const LayerDev &D, const ClaimPlan &p
 __device__ __forceinline__ int wide_tpc(int P, int mu, int target) {
     return min(target, min(mu, kSlot / qtile_bytes(P)));
 }
-__device__ __forceinline__ int4 chunk_desc(const LayerDev &D, const ClaimPlan &p, int b, int kvh, int mu, int c,
-                                           int N, const int *pref, int target) {
+__device__ __forceinline__ int4 chunk_desc(const LayerDev &D, const ClaimPlan &p, int kvh, int mu, int c, int N,
+                                           const int *pref, const int *qy, const int2 *fpe, int target) {
     const int fb = (int)((unsigned)c * p.nfl / N);
-    if ((int)((unsigned)(c + 1) * p.nfl / N) > fb) return fp_desc(D, p, b, kvh, mu, fb);
+    if ((int)((unsigned)(c + 1) * p.nfl / N) > fb) {   // full-precision unit fb (its list entry in fpe)
+        const int gf = p.f0 + fb, e = gf / mu, j = gf - e * mu;
+        const int2 en = fpe[e - p.fw0];
+        const int nt = ((en.x == p.n_win - 1) ? (int)(p.length - (int64_t)en.x * D.w) : D.w) - 16 * j;
+        if (nt <= 0) return make_int4(EL_SKIP, 0, 0, 0);   // past the open window's last token
+        return make_int4(EL_F | (min(16, nt) << 2), e * mu + j, en.y * D.Hkv + kvh, 16 * j);
+    }
     const int ci = c - fb;
     int lo = 0, hi = p.nqw - 1;
     while (lo < hi) {
@@ -340,16 +346,18 @@ __device__ __forceinline__ int4 chunk_desc(const LayerDev &D, const ClaimPlan &p
             hi = mid - 1;
     }
     const int e = p.qw0 + lo;
-    const int2 en = D.q_list[b * D.CQ + e];
-    const int lgP = en.y >> kSlotBits, slot = en.y & ((1 << kSlotBits) - 1), P = 1 << lgP;
+    const int ey = qy[lo];   // the window's list entry .y: log2 planes, slot
+    const int lgP = ey >> kSlotBits, slot = ey & ((1 << kSlotBits) - 1), P = 1 << lgP;
     const int tpc = wide_tpc(P, mu, target);
     const int u0 = (ci - pref[lo]) * tpc, n = min(tpc, mu - u0);
     const int64_t off = (int64_t)slot * D.lg_slot_bytes + lg_tile_off(kvh, D.w, u0, P);
     return make_int4(EL_Q | (n << 2) | (lgP << 7), D.CF * mu + e * mu + u0, (int)(off >> 9), n * qtile_bytes(P));
 }
 
-// kWide: the cache may hold INT4 / INT8 windows (2 or 4 code planes); then a
-// quantised chunk is one tile. The instantiation without it is the INT2 /
+// kWide: the cache may hold INT4 / INT8 windows (2 or 4 code planes) or
+// K-channel tiles; then the tiles per claim follow each window's width
+// (wide_tpc; K-channel tiles one per claim), and each chunk runs the
+// arithmetic of its plane count. The instantiation without it is the INT2 /
 // full-precision kernel as such.
 //
 // A split's share of a (sequence, KV head)'s work is a proportional share of
@@ -401,15 +409,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool chunked = false;
         if (kWide && p.kcodes < 0 && p.nqw > 0) {
             // wide plane tiles: several tiles of a window per claim (wide_tpc); the claims per
-            // window are prefix-summed in the ring space, which no copy has reached yet
+            // window are prefix-summed in the ring space, which no copy has reached yet, beside
+            // the split's list entries (at most 4096 windows: 32 KB), read once here
             int *pref = reinterpret_cast<int *>(smem);
+            int *qy = pref + p.nqw;
+            int2 *fpe = reinterpret_cast<int2 *>(qy + p.nqw);   // 8-byte aligned: 8 nqw bytes in
+            for (int i = tid; i < p.nfw; i += kThreads) fpe[i] = D.fp_list[b * D.CF + p.fw0 + i];
             const int target = max(1, (p.nqw * mu) / (2 * kWarps));
             const int per = (p.nqw + kThreads - 1) / kThreads;
             const int k0 = min(p.nqw, tid * per), k1 = min(p.nqw, k0 + per);
             int cnt = 0;
             for (int k = k0; k < k1; ++k) {
-                const int P = 1 << (D.q_list[b * D.CQ + p.qw0 + k].y >> kSlotBits);
-                const int tpc = wide_tpc(P, mu, target);
+                const int ey = D.q_list[b * D.CQ + p.qw0 + k].y;
+                qy[k] = ey;
+                const int tpc = wide_tpc(1 << (ey >> kSlotBits), mu, target);
                 pref[k] = (mu + tpc - 1) / tpc;
                 cnt += pref[k];
             }
@@ -436,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 chunked = true;
                 n_claims = total + p.nfl;
                 for (int c = tid; c < n_claims; c += kThreads)
-                    s_desc[c] = chunk_desc(D, p, b, kvh, mu, c, n_claims, pref, target);
+                    s_desc[c] = chunk_desc(D, p, kvh, mu, c, n_claims, pref, qy, fpe, target);
             }
         }
         if (!chunked)
