@@ -994,9 +994,12 @@ def run_native(args, rank, world, local_rank):
     if not args.no_variants:
         del cache, pool
         torch.cuda.empty_cache()
-        line["variants"] = measure_variants(wl, NL, K, dev, peak)
-        line["variants"]["mixed_widths"] = measure_mixed_widths(wl, NL, K, dev, peak)
-        line["variants"]["k_channels"] = measure_k_channels(wl, NL, K, dev, peak)
+        legs = set(args.variants.split(","))
+        line["variants"] = measure_variants(wl, NL, K, dev, peak) if "all" in legs or "per_head" in legs else {}
+        if "all" in legs or "mixed_widths" in legs:
+            line["variants"]["mixed_widths"] = measure_mixed_widths(wl, NL, K, dev, peak)
+        if "all" in legs or "k_channels" in legs:
+            line["variants"]["k_channels"] = measure_k_channels(wl, NL, K, dev, peak)
     if not args.no_per_config:
         line["per_config"] = measure_per_config(K, dev, peak, args.per_config)
     if pool_async is not None:
@@ -1049,6 +1052,9 @@ def main():
     ap.add_argument("--no-diag", action="store_true", help="skip the routing diagnostics leg")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the per-KV-head and global-routing leg")
+    ap.add_argument("--variants", default="all",
+                    help="comma-separated variant legs: per_head (with the routers), mixed_widths, k_channels "
+                         "(default: all)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the decode measurement on the other workloads")
     ap.add_argument("--per-config", default="all",
