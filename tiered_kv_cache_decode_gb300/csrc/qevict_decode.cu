@@ -42,6 +42,15 @@
 //  of each product, which leaves every sum unchanged. After each claim the
 //  warp stores the claim's (reference max, exp-sum) per head as a record.
 //
+// The wide instantiation (decode_kernel<G, true>, caches that allow INT4 and
+// INT8 windows, "Technische Samenvatting: RDKV", 2.2 and 2.3) reads a window
+// of b bits as b / 2 two-bit code planes: INT4 joins its two planes into 4-bit
+// codes in registers and runs the INT2 arithmetic once, INT8 runs it on two
+// nibbles, the high one weighted 16. Its claims take as many tiles of a window
+// as a stage holds at the window's width, and each chunk runs the arithmetic
+// compiled for its plane count. On a layer with K-channel widths each
+// 32-channel K group is read at its own width (width 0: skipped).
+//
 // After the loop the warps merge in shared memory and the CTA publishes its
 // partial output and (max, exp-sum) per head as 64-bit words tagged with the
 // launch's generation. The splits of a (sequence, KV head) meet on those
