@@ -9,6 +9,8 @@ and meta, write counts, transition statistics; outputs, masses and scores
 within the attention tolerance. A second sweep does the same through the
 wide kernel: caches that allow INT4 and INT8, mixed-width routing events on
 seeded scores, fused steps, and a second event on the accumulated scores."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -19,8 +21,9 @@ from parity_util import check_decode, check_state, check_stats, close, make_pair
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 32
-N_WIDE = 16
+# more cases on request (the seeds continue the same sequences)
+N_CASES = int(os.environ.get("QEVICT_SWEEP_CASES", "32"))
+N_WIDE = int(os.environ.get("QEVICT_SWEEP_WIDE", "16"))
 
 
 @pytest.fixture(autouse=True, scope="module")
