@@ -64,3 +64,50 @@ def test_headline_shape_graph_of_fused_steps_non_cooperative_with_overlap():
         assert cache.length(l) == L0 + steps
         close(cache.scores(l).cpu().numpy(), np.stack(refs[l].S), f"scores of layer {l}")
         check_state(cache, l, refs[l])
+
+
+def test_mixed_width_shape_graph_of_decodes_non_cooperative_with_overlap():
+    """The bench's mixed-width leg in its launch configuration: two 32K layers
+    routed over widths {0, 2, 4, 8, 16}, decodes with score accumulation in one
+    CUDA graph, replayed; outputs after each replay against the oracle."""
+    import oracle as O
+    B, Hq, Hkv, w, L0, beta, NL, reps = 1, 32, 8, 64, 32768, 0.2, 2, 2
+    W = L0 // w
+    seed = 12
+    cache = binding.TieredCache(B, NL, Hq, Hkv, w, L0, budget_frac=beta, max_ledger_bits=8, fp_capacity=W,
+                                ledger_capacity=W)
+    cache.set_launch_overlap(True)
+    cache.set_cooperative_launch(False)
+    refs = []
+    t0 = np.zeros((B, W), np.uint8)
+    for l in range(NL):
+        k, v = synth.kv_tokens(seed, l, B, 0, L0, Hkv, 128)
+        cache.prefill(l, k.cuda(), v.cuda(), tiers=torch.from_numpy(t0).cuda())
+        ref = O.OracleCache(B, Hq, Hkv, 128, w, beta=beta)
+        ref.prefill(k.float().numpy(), v.float().numpy(), tiers=t0)
+        sc = synth.zipf_scores(seed, l, B, W)
+        cache.route_rd_mixed(l, scores_override=sc.cuda())
+        O.route_rd_mixed(ref, scores_override=sc.numpy(), max_bits=8)
+        refs.append(ref)
+    assert cache.status() == 0, cache.last_error()
+    assert any((r.tiers() == O.TIER_Q4).any() for r in refs)
+    q = [synth.queries(seed, l, 0, B, Hq, 128).cuda() for l in range(NL)]
+    out = [torch.empty(B, Hq, 128, dtype=torch.float32, device="cuda") for _ in range(NL)]
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for l in range(NL):
+                cache.decode(l, q[l], out=out[l], want_mass=False, accumulate=True, stream=s)
+    torch.cuda.synchronize()
+    for r in range(reps):
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(NL):
+            ro, _ = refs[l].decode(q[l].cpu().float().numpy())
+            close(out[l].cpu().numpy(), ro, f"replay {r} layer {l}")
+    assert cache.status() == 0, cache.last_error()
+    for l in range(NL):
+        close(cache.scores(l).cpu().numpy(), np.stack(refs[l].S), f"scores of layer {l}")
+        check_state(cache, l, refs[l])
